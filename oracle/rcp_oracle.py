@@ -1,0 +1,161 @@
+"""Oracle for rank-compressed paged attention: a plain, slow fp64 CPU restatement.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or links this
+module; only the tests, the package smoke check and the benchmark's CPU-baseline leg do.
+It shares no code with the CUDA library.
+
+What it computes follows the Proxima page (STAR-KV plugin for vLLM), intro paragraph:
+keys use a head-wise low-rank decomposition and values a joint one, kept in a compressed
+paged format; its "Per-decode-step attention" and "Per-prefill-chunk attention" sections
+name the two attention steps, and its "Kernel profiling breakdown" names the cache-write
+step (low-rank projection of each new token).  The page prints no equations; the exact
+definitions used here are:
+
+* append:   c_k[t,h] = fp16(U_k,h k_{t,h}),   c_v[t] = fp16(W_v v_t)
+            (v_t is the head-major concatenation of the H head vectors), written to
+            K page [s // bs][h][s % bs][:] and V page [s // bs][s % bs][:] for slot s;
+            slot -1 writes nothing.
+* decode:   q~_h = U_k,h q_h;  s_{h,t} = q~_h . c_k[t,h] / sqrt(d) for t < L;
+            p_h = softmax(s_h) (max subtracted first);  z_h = sum_t p_{h,t} c_v[t];
+            o_h = W_v[:, h*d:(h+1)*d]^T z_h.
+            Token t of request b lives in block block_table[b][t // bs] at offset t % bs.
+            L = 0 gives o = 0.
+* prefill:  the chunk is appended first; chunk query i of request b sits at absolute
+            position P_b + i with P_b = seq_len_b - chunk_len_b and attends keys
+            t <= P_b + i, read back from the pages (i.e. after fp16 rounding).
+
+All arithmetic is fp64 on the stored fp16 values; results are fp64 (fp16 only where the
+definition stores fp16: the coefficients an append writes).
+
+Pins (see tests/test_oracle.py): identity factors reduce decode to textbook multi-head
+attention computed by a library routine; explicit reconstruction K = C_k U_k, V = C_v W_v
+followed by library attention agrees to 1e-12; physical block permutation leaves outputs
+bitwise unchanged; softmax weights sum to 1; single-token, equal-key, power-of-two
+scaling, causal-prefill and hand-derived closed-form cases; coordinate-selection factors
+make appends exact copies.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a).astype(np.float64)
+
+
+def gather_request(k_pages, v_pages, block_table_row, seq_len: int, block_size: int):
+    """Logical-order coefficients of one request through its block-table row.
+
+    Returns c_k [L][H][r_k] and c_v [L][R] (fp64).  Token t is in physical block
+    block_table_row[t // block_size] at offset t % block_size (the paged layout the
+    Proxima page's intro calls "compressed paged format", addressed the vLLM way).
+    """
+    t = np.arange(int(seq_len))
+    row = np.asarray(block_table_row, dtype=np.int64)
+    blocks = row[t // block_size]
+    offs = t % block_size
+    ck = _f64(k_pages[blocks, :, offs, :])      # advanced indices first: [L, H, r_k]
+    cv = _f64(v_pages[blocks, offs, :])         # [L, R]
+    return ck, cv
+
+
+def attend(q, ck, cv, U_k, W_v, head_dim: int, n_keys=None):
+    """Rank-space attention of one query set against one request's coefficients.
+
+    q: [Q][H][d]; ck: [L][H][r_k]; cv: [L][R]; n_keys[i] = number of leading keys query i
+    may attend (default: all L).  Returns (o [Q][H][d], p [Q][H][L]) in fp64.
+    """
+    q = _f64(q)
+    U = _f64(U_k)
+    W = _f64(W_v)
+    nq, H, d = q.shape
+    L = ck.shape[0]
+    if n_keys is None:
+        n_keys = np.full(nq, L)
+    o = np.zeros((nq, H, d))
+    p_all = np.zeros((nq, H, L))
+    for i in range(nq):
+        n = int(n_keys[i])
+        if n == 0:
+            continue
+        qt = np.einsum("hkd,hd->hk", U, q[i])                     # q~_h = U_k,h q_h
+        s = np.einsum("thk,hk->ht", ck[:n], qt) / np.sqrt(head_dim)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        p = e / e.sum(axis=1, keepdims=True)                       # [H][n]
+        z = p @ cv[:n]                                             # [H][R]
+        for h in range(H):
+            o[i, h] = W[:, h * d:(h + 1) * d].T @ z[h]            # o_h = W_v,h^T z_h
+        p_all[i, :, :n] = p
+    return o, p_all
+
+
+def decode_attn(q, k_pages, v_pages, U_k, W_v, block_table, seq_lens, block_size: int = 16,
+                requests=None, return_weights: bool = False):
+    """Decode attention for a batch: one query per request.
+
+    q [B][H][d]; returns o [B][H][d] fp64 (only rows in ``requests`` if given, else all)
+    and, if asked, the list of softmax weight arrays [H][L_b].
+    """
+    q = np.asarray(q)
+    B, H, d = q.shape
+    reqs = range(B) if requests is None else list(requests)
+    out = np.zeros((len(reqs), H, d))
+    weights = []
+    for n, b in enumerate(reqs):
+        L = int(seq_lens[b])
+        ck, cv = gather_request(k_pages, v_pages, block_table[b], L, block_size)
+        o, p = attend(q[b:b + 1], ck, cv, U_k, W_v, d)
+        out[n] = o[0]
+        weights.append(p[0])
+    return (out, weights) if return_weights else out
+
+
+def append_kv(k_pages, v_pages, U_k, W_v, k, v, slot_mapping, block_size: int = 16):
+    """Project new tokens to coefficients and write them at their slots (returns copies).
+
+    k, v: [T][H][d]; slot_mapping: [T]; slot -1 is skipped.  Coefficients are rounded
+    from fp64 to fp16 (nearest, ties to even).
+    """
+    kp = np.array(k_pages, copy=True)
+    vp = np.array(v_pages, copy=True)
+    U = _f64(U_k)
+    W = _f64(W_v)
+    k = _f64(k)
+    v = _f64(v)
+    T, H, d = k.shape
+    for i in range(T):
+        s = int(slot_mapping[i])
+        if s < 0:
+            continue
+        blk, off = s // block_size, s % block_size
+        for h in range(H):
+            kp[blk, h, off, :] = (U[h] @ k[i, h]).astype(np.float16)
+        vp[blk, off, :] = (W @ v[i].reshape(H * d)).astype(np.float16)
+    return kp, vp
+
+
+def prefill_attn(q, cu_chunk_lens, k_pages, v_pages, U_k, W_v, block_table, seq_lens,
+                 block_size: int = 16, requests=None):
+    """Chunked-prefill attention over pages that already hold the chunk.
+
+    q: [sum chunk][H][d]; cu_chunk_lens [B+1]; seq_lens [B] include the chunk.  Returns
+    o [sum chunk][H][d] fp64 (rows of requests not in ``requests`` stay zero).
+    """
+    q = np.asarray(q)
+    T, H, d = q.shape
+    out = np.zeros((T, H, d))
+    B = len(seq_lens)
+    reqs = range(B) if requests is None else list(requests)
+    for b in reqs:
+        c0, c1 = int(cu_chunk_lens[b]), int(cu_chunk_lens[b + 1])
+        n = c1 - c0
+        if n == 0:
+            continue
+        L = int(seq_lens[b])
+        P = L - n
+        ck, cv = gather_request(k_pages, v_pages, block_table[b], L, block_size)
+        n_keys = P + 1 + np.arange(n)                  # causal: query i sees t <= P + i
+        o, _ = attend(q[c0:c1], ck, cv, U_k, W_v, d, n_keys=n_keys)
+        out[c0:c1] = o
+    return out

@@ -1,0 +1,322 @@
+"""Seeded synthetic inputs for rank-compressed paged attention.
+
+This module only draws random numbers and lays them out in the paged format; it holds
+none of the attention arithmetic (no projection into rank space, no score, softmax or
+contraction).  The oracle-side tests, the GPU tests, ``bench.py`` and the smoke run all
+take their inputs from here, so both sides of every parity check see identical bytes.
+
+Workloads mirror the decode / prefill shapes of the Proxima page ("Per-decode-step
+attention": 32-head MHA, head size 128, key rank 64, fp16, block size 16), with a joint
+value rank of 1024.  Coefficients are N(0,1) rounded to fp16; factors have orthonormal
+rows taken from a Householder QR of an N(0,1) matrix (fp64), rounded to fp16.
+
+Two generation routes exist:
+
+* ``make_paged_cache`` (numpy, host): draws *logical* per-request coefficient sequences
+  first, then scatters them into physical blocks through a seeded permutation.  Tests use
+  the logical sequences as an independent view of the cache.
+* ``make_paged_cache_device`` (torch on a CUDA device): fills every physical page
+  directly with seeded normal draws; used for the multi-GB workloads where host
+  generation would take minutes.  Parity at that size copies the sampled requests' pages
+  back to the host for the oracle.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK_SIZE = 16
+
+# Model shapes: (num_heads H, head_dim d, key rank r_k, joint value rank R).
+SHAPES = {
+    "tiny": dict(num_heads=4, head_dim=64, rank_k=16, rank_v=64),
+    "mha32": dict(num_heads=32, head_dim=128, rank_k=64, rank_v=1024),
+}
+
+# Named workloads.  ``seed`` = 1000 + position in the list of configurations.
+WORKLOADS = {
+    "decode_tiny_b2_l256": dict(shape="tiny", kind="decode", batch=2, seq_len=256, seed=1000),
+    "decode_b16_l1024": dict(shape="mha32", kind="decode", batch=16, seq_len=1024, seed=1001),
+    "decode_b64_l8192_append": dict(shape="mha32", kind="decode", batch=64, seq_len=8192,
+                                    append=True, seed=1002),
+    "decode_b20_l32768": dict(shape="mha32", kind="decode", batch=20, seq_len=32768, seed=1003),
+    "decode_ragged64_l128_16384": dict(shape="mha32", kind="decode", batch=64,
+                                       len_range=(128, 16384), seed=1003),
+    "prefill_b16_p4096_c256": dict(shape="mha32", kind="prefill", batch=16, prior=4096,
+                                   chunk=256, seed=1004),
+}
+
+
+def fp16(x) -> np.ndarray:
+    """Round to fp16 (numpy rounds float64 -> float16 to nearest, ties to even)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16)
+
+
+def orthonormal_rows(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
+    """fp64 matrix [rows][cols] with orthonormal rows (rows <= cols).
+
+    The first ``rows`` columns of Q from a Householder QR of a cols x rows N(0,1) matrix,
+    transposed.
+    """
+    assert rows <= cols
+    g = rng.standard_normal((cols, rows))
+    q, _ = np.linalg.qr(g, mode="reduced")
+    return q.T.copy()
+
+
+def make_factors(rng: np.random.Generator, num_heads: int, head_dim: int, rank_k: int,
+                 rank_v: int):
+    """U_k [H][r_k][d] and W_v [R][H*d], fp16, orthonormal rows before rounding."""
+    U = np.stack([orthonormal_rows(rng, rank_k, head_dim) for _ in range(num_heads)])
+    W = orthonormal_rows(rng, rank_v, num_heads * head_dim)
+    return fp16(U), fp16(W)
+
+
+def identity_factors(num_heads: int, head_dim: int):
+    """U_k,h = I_d (r_k = d) and W_v = I (R = H*d)."""
+    U = np.stack([np.eye(head_dim) for _ in range(num_heads)])
+    W = np.eye(num_heads * head_dim)
+    return fp16(U), fp16(W)
+
+
+def selection_factors(rng: np.random.Generator, num_heads: int, head_dim: int, rank_k: int,
+                      rank_v: int):
+    """Factors whose rows are distinct unit vectors (coordinate selections).
+
+    Projecting with them picks coordinates exactly, so coefficients written by an append
+    are exact copies of chosen input entries.
+    """
+    U = np.zeros((num_heads, rank_k, head_dim))
+    for h in range(num_heads):
+        cols = rng.permutation(head_dim)[:rank_k]
+        U[h, np.arange(rank_k), cols] = 1.0
+    W = np.zeros((rank_v, num_heads * head_dim))
+    cols = rng.permutation(num_heads * head_dim)[:rank_v]
+    W[np.arange(rank_v), cols] = 1.0
+    return fp16(U), fp16(W)
+
+
+def blocks_needed(seq_len: int, block_size: int = BLOCK_SIZE) -> int:
+    return (int(seq_len) + block_size - 1) // block_size
+
+
+@dataclass
+class PagedCache:
+    """A filled paged coefficient cache and the tables that address it."""
+    k_pages: np.ndarray          # [num_blocks][H][bs][r_k] fp16
+    v_pages: np.ndarray          # [num_blocks][bs][R] fp16
+    block_table: np.ndarray      # [B][max_blocks] int32, -1 past a request's blocks
+    seq_lens: np.ndarray         # [B] int32
+    spare_blocks: np.ndarray     # physical ids not referenced by any request
+    ck: list = field(default_factory=list)   # per request [L_b][H][r_k] fp16 (logical order)
+    cv: list = field(default_factory=list)   # per request [L_b][R] fp16
+
+
+def _assign_blocks(rng, seq_lens, spare_blocks, block_size, max_blocks=None):
+    nblk = [blocks_needed(L, block_size) for L in seq_lens]
+    used = int(sum(nblk))
+    num_blocks = used + int(spare_blocks)
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    mb = max(1, max(nblk) if nblk else 1)
+    if max_blocks is not None:
+        mb = max(mb, int(max_blocks))
+    table = np.full((len(seq_lens), mb), -1, dtype=np.int32)
+    cur = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[cur:cur + n]
+        cur += n
+    return num_blocks, table, perm[used:].copy()
+
+
+def make_paged_cache(rng: np.random.Generator, num_heads: int, rank_k: int, rank_v: int,
+                     seq_lens, block_size: int = BLOCK_SIZE, spare_blocks: int = 0,
+                     fill: float = 0.0, max_blocks: int | None = None) -> PagedCache:
+    """Random logical coefficient sequences scattered into shuffled physical blocks.
+
+    Slots that hold no token keep ``fill`` (tests use NaN to prove those slots are never
+    read into a result).
+    """
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    num_blocks, table, spare = _assign_blocks(rng, seq_lens, spare_blocks, block_size,
+                                              max_blocks)
+    kp = np.full((num_blocks, num_heads, block_size, rank_k), fill, dtype=np.float16)
+    vp = np.full((num_blocks, block_size, rank_v), fill, dtype=np.float16)
+    cks, cvs = [], []
+    for b, L in enumerate(seq_lens):
+        ck = fp16(rng.standard_normal((int(L), num_heads, rank_k)))
+        cv = fp16(rng.standard_normal((int(L), rank_v)))
+        for t in range(int(L)):
+            blk = table[b, t // block_size]
+            off = t % block_size
+            kp[blk, :, off, :] = ck[t]
+            vp[blk, off, :] = cv[t]
+        cks.append(ck)
+        cvs.append(cv)
+    return PagedCache(kp, vp, table, seq_lens, spare, cks, cvs)
+
+
+def permute_physical_blocks(cache: PagedCache, rng: np.random.Generator) -> PagedCache:
+    """Same logical cache, physical blocks relabelled by a random permutation."""
+    nb = cache.k_pages.shape[0]
+    perm = rng.permutation(nb)               # new id of old block i is perm[i]
+    kp = np.empty_like(cache.k_pages)
+    vp = np.empty_like(cache.v_pages)
+    kp[perm] = cache.k_pages
+    vp[perm] = cache.v_pages
+    table = cache.block_table.copy()
+    m = table >= 0
+    table[m] = perm[table[m]]
+    return PagedCache(kp, vp, table, cache.seq_lens.copy(), perm[cache.spare_blocks],
+                      cache.ck, cache.cv)
+
+
+def slot_for(block_table: np.ndarray, b: int, pos: int, block_size: int = BLOCK_SIZE) -> int:
+    """vLLM slot convention: physical block * block_size + offset in block."""
+    return int(block_table[b, pos // block_size]) * block_size + pos % block_size
+
+
+def ragged_lengths(rng: np.random.Generator, batch: int, lo: int, hi: int) -> np.ndarray:
+    return rng.integers(lo, hi + 1, size=batch).astype(np.int32)
+
+
+# ----------------------------------------------------------------------------- host workloads
+
+@dataclass
+class DecodeInputs:
+    shape: dict
+    U_k: np.ndarray
+    W_v: np.ndarray
+    cache: PagedCache
+    q: np.ndarray                      # [B][H][d] fp16
+    new_k: np.ndarray | None = None    # [B][H][d] fp16 (appended token, position L-1)
+    new_v: np.ndarray | None = None
+    slot_mapping: np.ndarray | None = None   # [B] int64
+
+
+def make_decode_inputs(shape: dict, seq_lens, seed: int, append: bool = False,
+                       spare_blocks: int = 4, fill: float = 0.0,
+                       max_blocks: int | None = None) -> DecodeInputs:
+    """Host-side decode workload.
+
+    Draw order: factors, K/V coefficient sequences (with the block permutation), q, then
+    the appended token's k and v.
+    """
+    rng = np.random.default_rng(seed)
+    H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
+    U, W = make_factors(rng, H, d, rk, R)
+    cache = make_paged_cache(rng, H, rk, R, seq_lens, spare_blocks=spare_blocks, fill=fill,
+                             max_blocks=max_blocks)
+    B = len(cache.seq_lens)
+    q = fp16(rng.standard_normal((B, H, d)))
+    out = DecodeInputs(shape, U, W, cache, q)
+    if append:
+        out.new_k = fp16(rng.standard_normal((B, H, d)))
+        out.new_v = fp16(rng.standard_normal((B, H, d)))
+        out.slot_mapping = np.array(
+            [slot_for(cache.block_table, b, int(L) - 1) if L > 0 else -1
+             for b, L in enumerate(cache.seq_lens)], dtype=np.int64)
+    return out
+
+
+@dataclass
+class PrefillInputs:
+    shape: dict
+    U_k: np.ndarray
+    W_v: np.ndarray
+    cache: PagedCache                  # holds prior tokens; chunk slots start as ``fill``
+    prior_lens: np.ndarray             # [B]
+    chunk_lens: np.ndarray             # [B]
+    cu_chunk_lens: np.ndarray          # [B+1] int32
+    q: np.ndarray                      # [sum chunk][H][d]
+    k: np.ndarray                      # [sum chunk][H][d]
+    v: np.ndarray                      # [sum chunk][H][d]
+    slot_mapping: np.ndarray           # [sum chunk] int64
+    seq_lens_after: np.ndarray         # [B] prior + chunk
+
+
+def make_prefill_inputs(shape: dict, prior_lens, chunk_lens, seed: int, spare_blocks: int = 4,
+                        fill: float = 0.0) -> PrefillInputs:
+    """Host-side chunked-prefill workload.
+
+    The cache holds ``prior_lens[b]`` random tokens; the blocks for the chunk are assigned
+    up front (their slots hold ``fill`` until the chunk is appended).  Draw order:
+    factors, prior coefficients, q, k, v of the chunk.
+    """
+    rng = np.random.default_rng(seed)
+    H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
+    U, W = make_factors(rng, H, d, rk, R)
+    prior = np.asarray(prior_lens, dtype=np.int32)
+    chunk = np.asarray(chunk_lens, dtype=np.int32)
+    after = prior + chunk
+    cache = make_paged_cache(rng, H, rk, R, prior, spare_blocks=spare_blocks, fill=fill,
+                             max_blocks=max(blocks_needed(x) for x in after) if len(after) else 1)
+    # extend each request's block list so that prior+chunk tokens fit
+    extra = [blocks_needed(a) - blocks_needed(p) for a, p in zip(after, prior)]
+    need = int(sum(extra))
+    nb0 = cache.k_pages.shape[0]
+    new_ids = (nb0 + rng.permutation(need)).astype(np.int32)
+    kp = np.concatenate([cache.k_pages,
+                         np.full((need,) + cache.k_pages.shape[1:], fill, np.float16)])
+    vp = np.concatenate([cache.v_pages,
+                         np.full((need,) + cache.v_pages.shape[1:], fill, np.float16)])
+    table = cache.block_table
+    cur = 0
+    for b in range(len(prior)):
+        n0 = blocks_needed(prior[b])
+        table[b, n0:n0 + extra[b]] = new_ids[cur:cur + extra[b]]
+        cur += extra[b]
+    cache = PagedCache(kp, vp, table, after.copy(), cache.spare_blocks, cache.ck, cache.cv)
+    T = int(chunk.sum())
+    cu = np.zeros(len(chunk) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(chunk)
+    q = fp16(rng.standard_normal((T, H, d)))
+    k = fp16(rng.standard_normal((T, H, d)))
+    v = fp16(rng.standard_normal((T, H, d)))
+    slots = np.empty(T, dtype=np.int64)
+    for b in range(len(chunk)):
+        for i in range(int(chunk[b])):
+            slots[cu[b] + i] = slot_for(table, b, int(prior[b]) + i)
+    return PrefillInputs(shape, U, W, cache, prior, chunk, cu, q, k, v, slots, after)
+
+
+# --------------------------------------------------------------------------- device workloads
+
+def make_paged_cache_device(seq_lens, shape: dict, seed: int, device="cuda",
+                            spare_blocks: int = 0, block_size: int = BLOCK_SIZE,
+                            chunk_blocks: int = 4096):
+    """Fill every physical page of a (multi-GB) cache with seeded N(0,1) fp16 on the device.
+
+    Returns (k_pages, v_pages, block_table numpy int32, seq_lens numpy int32).  The block
+    permutation is drawn on the host (numpy, ``seed``); page values by a torch generator
+    seeded with ``seed`` on ``device``, in chunks of ``chunk_blocks`` blocks.
+    """
+    import torch
+    rng = np.random.default_rng(seed)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    num_blocks, table, _ = _assign_blocks(rng, seq_lens, spare_blocks, block_size)
+    H, rk, R = shape["num_heads"], shape["rank_k"], shape["rank_v"]
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    kp = torch.empty((num_blocks, H, block_size, rk), dtype=torch.float16, device=device)
+    vp = torch.empty((num_blocks, block_size, R), dtype=torch.float16, device=device)
+    for s in range(0, num_blocks, chunk_blocks):
+        e = min(num_blocks, s + chunk_blocks)
+        kp[s:e] = torch.randn((e - s, H, block_size, rk), generator=g, device=device,
+                              dtype=torch.float32).half()
+        vp[s:e] = torch.randn((e - s, block_size, R), generator=g, device=device,
+                              dtype=torch.float32).half()
+    return kp, vp, table, seq_lens
+
+
+def algorithmic_bytes_decode(shape: dict, seq_lens) -> int:
+    """Coefficient bytes one decode step reads: (H*r_k + R) * 2 bytes per cached token."""
+    per_tok = (shape["num_heads"] * shape["rank_k"] + shape["rank_v"]) * 2
+    return int(np.sum(np.asarray(seq_lens, dtype=np.int64))) * per_tok
+
+
+def factor_bytes(shape: dict) -> int:
+    H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
+    return (H * rk * d + R * H * d) * 2
+
