@@ -1,0 +1,383 @@
+"""Benchmark: one decode step (append 1 token per sequence + decode attention) at
+batch 64, 8192 cached tokens per sequence, 32 heads, d=128, r_k=64, R=1024, fp16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  ``value`` is algorithmic GB/s: coefficient bytes one
+decode step must read ((H*r_k + R) * 2 bytes per cached token, 3,221,225,472 bytes per
+GPU) divided by the device time of the whole step, summed over ranks and divided by the
+slowest rank's time.  Under torchrun every rank runs its own batch of 64 independent
+sequences (weak scaling, no collective on the data path).
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+WORKLOAD = "decode_b64_l8192_append"
+METRIC = "decode-attn µs/step & GB/s at B=64,L=8192; fraction of GB300 HBM roofline"
+SHAPE = wl.SHAPES["mha32"]
+BATCH, SEQ = 64, 8192
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_b64_l8192.md")
+KERNEL_SRC = os.path.join(ROOT, "rank_compressed_paged_gb300", "csrc", "decode.cu")
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_src_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic_per_launch():
+    """DRAM bytes per decode-kernel launch from the committed ncu summary, or None when the
+    summary is missing or was taken on a different version of the kernel source."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    txt = open(PROFILE_SUMMARY).read()
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", txt)
+    t = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9]+)", txt)
+    if not h or not t or h.group(1) != kernel_src_hash():
+        return None
+    return int(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}",
+                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_workload(device, seed):
+    """Device-resident cache (pages drawn on the GPU) + the step's host inputs."""
+    import torch
+    seq_lens = np.full(BATCH, SEQ, np.int32)
+    kp, vp, table, seq_lens = wl.make_paged_cache_device(seq_lens, SHAPE, seed, device=device,
+                                                         spare_blocks=16)
+    rng = np.random.default_rng(seed)
+    U, W = wl.make_factors(rng, SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"],
+                           SHAPE["rank_v"])
+    H, d = SHAPE["num_heads"], SHAPE["head_dim"]
+    q = wl.fp16(rng.standard_normal((BATCH, H, d)))
+    nk = wl.fp16(rng.standard_normal((BATCH, H, d)))
+    nv = wl.fp16(rng.standard_normal((BATCH, H, d)))
+    slots = np.array([wl.slot_for(table, b, SEQ - 1) for b in range(BATCH)], np.int64)
+    return dict(kp=kp, vp=vp, table=table, seq_lens=seq_lens, U=U, W=W, q=q, nk=nk, nv=nv,
+                slots=slots)
+
+
+def oracle_sample(U, W, n_req, seed, budget_s):
+    """Time the fp64 oracle on up to n_req requests of the workload (host-generated pages
+    of the same shape / distribution); stops once budget_s seconds have been spent."""
+    from oracle import rcp_oracle as orc
+    H, d, rk, R = SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"], SHAPE["rank_v"]
+    rng = np.random.default_rng(seed + 7)
+    done, elapsed = 0, 0.0
+    while done < n_req and elapsed < budget_s:
+        nb = SEQ // 16
+        kp = wl.fp16(rng.standard_normal((nb, H, 16, rk), dtype=np.float32))
+        vp = wl.fp16(rng.standard_normal((nb, 16, R), dtype=np.float32))
+        table = rng.permutation(nb).astype(np.int32)[None]
+        q = wl.fp16(rng.standard_normal((1, H, d)))
+        nk = wl.fp16(rng.standard_normal((1, H, d)))
+        slot = np.array([wl.slot_for(table, 0, SEQ - 1)], np.int64)
+        t0 = time.perf_counter()
+        kp2, vp2 = orc.append_kv(kp, vp, U, W, nk, nk, slot, 16)
+        orc.decode_attn(q, kp2, vp2, U, W, table, np.array([SEQ], np.int32), 16)
+        elapsed += time.perf_counter() - t0
+        done += 1
+    per_req = wl.algorithmic_bytes_decode(SHAPE, [SEQ])
+    return done, elapsed, done * per_req / elapsed / 1e9
+
+
+def blas_threads() -> int:
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    rng = np.random.default_rng(2002)
+    U, W = wl.make_factors(rng, SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"],
+                           SHAPE["rank_v"])
+    for _ in range(args.warmup):
+        oracle_sample(U, W, 1, 1, 1e9)
+    times, nreq = [], 0
+    for s in range(args.steps):
+        n, el, _ = oracle_sample(U, W, 2, 100 + s, 1e9)
+        times.append(el)
+        nreq += n
+    per_req = wl.algorithmic_bytes_decode(SHAPE, [SEQ])
+    value = nreq * per_req / sum(times) / 1e9
+    sample = f"{nreq} of {BATCH} sequences (2 per step), append + decode, fp64 numpy oracle"
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(times) / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
+                   "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from rank_compressed_paged_gb300 import PagedCoeffCache
+    from rank_compressed_paged_gb300 import build as _build
+
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = make_workload(dev, seed=1002 + rank)
+    H, d = SHAPE["num_heads"], SHAPE["head_dim"]
+
+    def td(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    cache = PagedCoeffCache(H, d, SHAPE["rank_k"], SHAPE["rank_v"], w["kp"].shape[0], td(w["U"]),
+                            td(w["W"]), k_pages=w["kp"], v_pages=w["vp"])
+    q, nk, nv, slots = td(w["q"]), td(w["nk"]), td(w["nv"]), td(w["slots"])
+    table, lens = td(w["table"]), td(w["seq_lens"])
+    out = torch.empty_like(q)
+    ws = cache.workspace(BATCH)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        cache.append_kv(nk, nv, slots)
+        cache.decode_attn(q, table, lens, out=out, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region (inputs resident in HBM; pages 3.2 GB >> L2, no flush needed)
+    k_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k_stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    s_start = torch.cuda.Event(enable_timing=True)
+    s_stop = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        s_start.record(stream)
+        for i in range(args.steps):
+            cache.set_profile_events(k_starts[i], k_stops[i])
+            step()
+        s_stop.record(stream)
+        torch.cuda.synchronize()
+    cache.set_profile_events(None, None)
+    if world > 1:
+        dist.barrier()
+    step_ms = s_start.elapsed_time(s_stop) / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k_starts, k_stops))
+    assert cache.read_device_error() == 0, cache.read_device_error()
+
+    # ---- end to end through the public API with host buffers (pinned), copies included
+    hq = torch.from_numpy(w["q"]).pin_memory()
+    hk = torch.from_numpy(w["nk"]).pin_memory()
+    hv = torch.from_numpy(w["nv"]).pin_memory()
+    hs = torch.from_numpy(w["slots"]).pin_memory()
+    ht = torch.from_numpy(w["table"]).pin_memory()
+    hl = torch.from_numpy(w["seq_lens"]).pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(nk), torch.empty_like(nv)
+    ds, dt, dl = torch.empty_like(slots), torch.empty_like(table), torch.empty_like(lens)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hs, ht, hl))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ds.copy_(hs, non_blocking=True)
+        dt.copy_(ht, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        cache.append_kv(dk, dv, ds)
+        cache.decode_attn(dq, dt, dl, out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    # ---- aggregate over ranks (max time)
+    times = torch.tensor([step_ms, e2e_ms, kern_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    step_ms, e2e_ms, kern_ms = [float(x) for x in times.cpu()]
+    if rank != 0:
+        return
+    coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"])
+    value = world * coeff_bytes / (step_ms * 1e-3) / 1e9
+    e2e_value = world * coeff_bytes / (e2e_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = coeff_bytes / (kern_ms * 1e-3) / 1e9
+    traffic = ncu_traffic_per_launch()
+    # CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N=1)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n, el, gbs = oracle_sample(w["U"], w["W"], args.cpu_requests, 4242, args.cpu_budget_s)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} of {BATCH} sequences of 8192 tokens (append + decode), "
+                         f"{el:.1f} s of fp64 numpy oracle"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 4),
+        "us_per_step": round(step_ms * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
+                   "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16,
+                   "step": "append 1 token/seq + decode attention",
+                   "l2": "inputs larger than L2 (3.2 GB of pages per GPU), no flush",
+                   "parallelism": f"replicas x{world}, batch-sharded, no collective"},
+        "roofline": {"bound": "hbm", "kernel": "decode_main_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": coeff_bytes, "kernel_us": round(kern_ms * 1e3, 1),
+                     "frac_of_8TBps": round(achieved / 8000.0, 4)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * 5,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-requests", type=int, default=64)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,136 @@
+/*
+ * rcp.h -- C ABI of the rank-compressed paged attention library (GB300, sm_103a).
+ *
+ * The method (Proxima page, STAR-KV plugin for vLLM, intro paragraph): keys are kept as
+ * per-head low-rank coefficients c_k[t,h] = U_k,h k_{t,h} (r_k numbers per token and
+ * head, U_k,h an r_k x d factor with orthonormal rows), values as one joint coefficient
+ * vector per token c_v[t] = W_v v_t (R numbers, W_v an R x (H*d) factor), in a paged
+ * cache of fixed-size blocks.  Attention runs in rank space:
+ *     q~_h = U_k,h q_h,   s_{h,t} = q~_h . c_k[t,h] / sqrt(d),   p_h = softmax(s_h),
+ *     z_h = sum_t p_{h,t} c_v[t],   o_h = W_v[:, h*d:(h+1)*d]^T z_h.
+ *
+ * Memory layout (all device buffers are owned by the caller; the library never
+ * allocates device memory; every pointer must be 16-byte aligned):
+ *     K pages   [num_blocks][H][block_size][r_k]   fp16
+ *     V pages   [num_blocks][block_size][R]        fp16
+ *     U_k       [H][r_k][d]                        fp16
+ *     W_v       [R][H*d]   (column h*d + j = head h, element j)   fp16
+ *     q, out    [rows][H][d]                       fp16
+ *     block_table [rows_of_table][max_blocks_per_seq] int32, physical block ids
+ *     seq_lens  [batch] int32 (tokens in the cache, including any just appended)
+ * Token t of a request lives in block block_table[b][t / block_size] at offset
+ * t % block_size; a slot id is block * block_size + offset (vLLM convention).
+ *
+ * Errors: host-checkable problems (null or misaligned pointers, bad sizes, unsupported
+ * shapes, a workspace that is too small) return a status synchronously and launch
+ * nothing.  Values that live on the device (slots, block ids, lengths) are checked by the
+ * kernels: a bad value sets a bit in the caller-provided device error word
+ * (RCP_DEVERR_*) and the offending slot / block contributes nothing.  Launch failures
+ * return RCP_ERR_CUDA.  No call synchronises the host; all work is queued on the given
+ * stream.  No C++ exception crosses this interface.
+ */
+#ifndef RCP_H_
+#define RCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rcp_status {
+  RCP_OK = 0,
+  RCP_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, negative or inconsistent size */
+  RCP_ERR_UNSUPPORTED = 2,   /* shape this build has no kernel for */
+  RCP_ERR_CAPACITY = 3,      /* block pool exhausted / id out of range / double free */
+  RCP_ERR_WORKSPACE = 4,     /* workspace smaller than rcp_workspace_size() */
+  RCP_ERR_CUDA = 5           /* a CUDA runtime / driver call failed */
+} rcp_status;
+
+/* Bits a kernel ORs into the device error word. */
+#define RCP_DEVERR_BAD_SLOT 1u    /* append: slot >= num_blocks * block_size */
+#define RCP_DEVERR_BAD_BLOCK 2u   /* attention: block id outside [0, num_blocks) */
+#define RCP_DEVERR_BAD_LEN 4u     /* attention: seq_len < 0, > table capacity, or chunk > seq_len */
+#define RCP_DEVERR_TIMEOUT 8u     /* a pipeline wait exceeded its bound; results invalid */
+
+typedef struct rcp_cache_config {
+  int32_t num_heads;   /* H */
+  int32_t head_dim;    /* d */
+  int32_t rank_k;      /* r_k, key coefficients per token and head */
+  int32_t rank_v;      /* R, joint value coefficients per token */
+  int32_t block_size;  /* tokens per page; this build supports 16 */
+  int64_t num_blocks;  /* physical blocks in the K and V page buffers */
+} rcp_cache_config;
+
+typedef struct rcp_cache rcp_cache;   /* opaque handle: borrowed pointers + host free list */
+typedef void* rcp_stream;             /* a cudaStream_t; NULL means the legacy stream */
+
+/* Human-readable name of a status code (static string). */
+const char* rcp_status_string(rcp_status s);
+
+/* RCP_OK if this build has kernels for the shape.  Supported: block_size 16 and
+ * (H, d, r_k, R) = (32, 128, 64, 1024) or (4, 64, 16, 64). */
+rcp_status rcp_config_supported(const rcp_cache_config* cfg);
+
+/* Create a handle over caller-owned device buffers (layout above).  dev_error points to
+ * one device uint32 the kernels OR error bits into (the caller zeroes and reads it).
+ * Makes no CUDA call; the handle's host free list starts with all blocks free.
+ * Ownership: the caller keeps every buffer alive until rcp_destroy_cache. */
+rcp_status rcp_create_cache(const rcp_cache_config* cfg, void* k_pages, void* v_pages,
+                            const void* U_k, const void* W_v, uint32_t* dev_error,
+                            rcp_cache** out);
+rcp_status rcp_destroy_cache(rcp_cache* cache);
+
+/* Host-side block pool (capacity accounting for the paged cache).  alloc hands out n
+ * free physical ids (RCP_ERR_CAPACITY and no change if fewer are free); free returns
+ * ids (RCP_ERR_CAPACITY and no change on an out-of-range or already-free id). */
+rcp_status rcp_alloc_blocks(rcp_cache* cache, int32_t n, int32_t* ids_out);
+rcp_status rcp_free_blocks(rcp_cache* cache, int32_t n, const int32_t* ids);
+rcp_status rcp_num_free_blocks(const rcp_cache* cache, int64_t* n_free);
+
+/* Bytes of device workspace decode / prefill need for up to max_query_rows query rows
+ * (decode: batch; prefill: total chunk rows).  Pure host arithmetic. */
+rcp_status rcp_workspace_size(const rcp_cache* cache, int32_t max_query_rows, size_t* bytes);
+
+/* Append (Proxima page, "Kernel profiling breakdown": the cache-write kernel does the
+ * low-rank projection): for each of num_tokens new tokens i with slot s =
+ * slot_mapping[i] >= 0, write fp16(U_k,h k[i][h]) to K page [s/bs][h][s%bs] for every
+ * head and fp16(W_v v[i]) (v[i] flattened head-major) to V page [s/bs][s%bs].  slot -1
+ * is skipped.  k, v: [num_tokens][H][d] fp16 device; slot_mapping: [num_tokens] int64
+ * device.  Duplicate slots within one call are undefined. */
+rcp_status rcp_append_kv(rcp_cache* cache, const void* k, const void* v,
+                         const int64_t* slot_mapping, int32_t num_tokens, rcp_stream stream);
+
+/* Decode attention (Proxima page, "Per-decode-step attention"): one query per request,
+ * q [batch][H][d] fp16, attends the first seq_lens[b] tokens of request b through
+ * block_table row b.  out [batch][H][d] fp16; seq_len 0 gives zeros.  workspace must hold
+ * rcp_workspace_size(cache, batch) bytes (256-byte aligned); its contents are scratch. */
+rcp_status rcp_decode_attn(rcp_cache* cache, const void* q, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           rcp_stream stream);
+
+/* Chunked-prefill attention (Proxima page, "Per-prefill-chunk attention").  The chunk's
+ * K/V must already be appended.  Request b owns query rows cu_chunk_lens[b] ..
+ * cu_chunk_lens[b+1]-1 of q [num_query_rows][H][d]; seq_lens[b] counts prior + chunk
+ * tokens; chunk row i sits at position seq_lens[b] - chunk_b + i and attends keys
+ * 0 .. that position (causal).  out [num_query_rows][H][d] fp16.  workspace must hold
+ * rcp_workspace_size(cache, num_query_rows) bytes. */
+rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_chunk_lens,
+                            int32_t num_query_rows, const int32_t* block_table,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            rcp_stream stream);
+
+/* Measurement hook (the pages have no counterpart; it exists for roofline timing).  When
+ * both events are non-NULL, every later decode / prefill call records start_event on its
+ * stream just before the split-K attention kernel and stop_event just after it, so the
+ * caller can read that kernel's duration with cudaEventElapsedTime.  The events are
+ * cudaEvent_t handles owned by the caller; NULL, NULL turns the hook off. */
+rcp_status rcp_set_profile_events(rcp_cache* cache, void* start_event, void* stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+#endif  /* RCP_H_ */

@@ -1,0 +1,153 @@
+"""Rank-compressed paged attention on GB300 (sm_103a).
+
+A thin Python layer over the C ABI of ``librcp.so`` (``include/rcp.h``): it passes torch
+device pointers and the current CUDA stream through ctypes and does nothing else; every
+step of the path runs in the library's CUDA kernels.
+
+    cache = PagedCoeffCache(num_heads=32, head_dim=128, rank_k=64, rank_v=1024,
+                            num_blocks=..., U_k=U, W_v=W)       # U, W: fp16 CUDA tensors
+    cache.append_kv(k, v, slot_mapping)                          # project + scatter
+    out = cache.decode_attn(q, block_table, seq_lens)            # [B][H][d] fp16
+    out = cache.prefill_attn(q, cu_chunk_lens, block_table, seq_lens)
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import RcpError  # noqa: F401
+
+BLOCK_SIZE = 16
+
+
+def _ptr(t) -> int:
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+class PagedCoeffCache:
+    """Paged low-rank coefficient cache on one GPU.
+
+    Owns (as torch tensors) the K pages [num_blocks][H][16][r_k], V pages
+    [num_blocks][16][R], the factors, a device error word and a reusable workspace; the
+    library handle borrows their pointers.
+    """
+
+    def __init__(self, num_heads: int, head_dim: int, rank_k: int, rank_v: int,
+                 num_blocks: int, U_k, W_v, k_pages=None, v_pages=None, device=None):
+        import torch
+        lib = _lib.load()
+        dev = U_k.device if device is None else torch.device(device)
+        self.shape = dict(num_heads=num_heads, head_dim=head_dim, rank_k=rank_k, rank_v=rank_v)
+        self.num_blocks = int(num_blocks)
+        self.U_k = U_k.contiguous()
+        self.W_v = W_v.contiguous()
+        if k_pages is None:
+            k_pages = torch.zeros((num_blocks, num_heads, BLOCK_SIZE, rank_k),
+                                  dtype=torch.float16, device=dev)
+        if v_pages is None:
+            v_pages = torch.zeros((num_blocks, BLOCK_SIZE, rank_v), dtype=torch.float16,
+                                  device=dev)
+        self.k_pages = k_pages
+        self.v_pages = v_pages
+        self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._ws = None
+        self._cfg = _lib.CacheConfig(num_heads, head_dim, rank_k, rank_v, BLOCK_SIZE,
+                                     self.num_blocks)
+        h = ctypes.c_void_p()
+        _lib.check("rcp_create_cache", lib.rcp_create_cache(
+            ctypes.byref(self._cfg), _ptr(self.k_pages), _ptr(self.v_pages), _ptr(self.U_k),
+            _ptr(self.W_v), _ptr(self.dev_error), ctypes.byref(h)))
+        self._h = h
+        self._lib = lib
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.rcp_destroy_cache(h)
+            self._h = None
+
+    # ------------------------------------------------------------------ block pool
+    def alloc_blocks(self, n: int):
+        ids = (ctypes.c_int32 * max(n, 1))()
+        _lib.check("rcp_alloc_blocks", self._lib.rcp_alloc_blocks(self._h, n, ids))
+        return [ids[i] for i in range(n)]
+
+    def free_blocks(self, ids) -> None:
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _lib.check("rcp_free_blocks", self._lib.rcp_free_blocks(self._h, len(ids), arr))
+
+    def num_free_blocks(self) -> int:
+        n = ctypes.c_int64()
+        _lib.check("rcp_num_free_blocks", self._lib.rcp_num_free_blocks(self._h, ctypes.byref(n)))
+        return n.value
+
+    # ------------------------------------------------------------------ workspace
+    def workspace_bytes(self, rows: int) -> int:
+        n = ctypes.c_size_t()
+        _lib.check("rcp_workspace_size",
+                   self._lib.rcp_workspace_size(self._h, rows, ctypes.byref(n)))
+        return n.value
+
+    def workspace(self, rows: int):
+        import torch
+        need = self.workspace_bytes(rows)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.k_pages.device)
+        return self._ws
+
+    def read_device_error(self) -> int:
+        return int(self.dev_error.item())
+
+    def clear_device_error(self) -> None:
+        self.dev_error.zero_()
+
+    def set_profile_events(self, start=None, stop=None) -> None:
+        """Record torch.cuda.Event pair around the split-K attention kernel (None: off)."""
+        def handle(ev):
+            if ev is None:
+                return None
+            if not ev.cuda_event:
+                ev.record()            # torch creates the CUDA event lazily
+            return ev.cuda_event
+        _lib.check("rcp_set_profile_events",
+                   self._lib.rcp_set_profile_events(self._h, handle(start), handle(stop)))
+
+    # ------------------------------------------------------------------ hot path
+    def append_kv(self, k, v, slot_mapping, stream=None) -> None:
+        """k, v: [T][H][d] fp16; slot_mapping: [T] int64 (all on the cache's device)."""
+        T = int(slot_mapping.shape[0])
+        _lib.check("rcp_append_kv", self._lib.rcp_append_kv(
+            self._h, _ptr(k), _ptr(v), _ptr(slot_mapping), T, _stream(stream)))
+
+    def decode_attn(self, q, block_table, seq_lens, out=None, workspace=None, stream=None):
+        """q: [B][H][d] fp16; block_table: [B][max_blocks] int32; seq_lens: [B] int32."""
+        import torch
+        B = int(q.shape[0])
+        if out is None:
+            out = torch.empty_like(q)
+        ws = self.workspace(B) if workspace is None else workspace
+        _lib.check("rcp_decode_attn", self._lib.rcp_decode_attn(
+            self._h, _ptr(q), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), B,
+            _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        return out
+
+    def prefill_attn(self, q, cu_chunk_lens, block_table, seq_lens, out=None, workspace=None,
+                     stream=None):
+        """q: [sum chunk][H][d] fp16; cu_chunk_lens: [B+1] int32; seq_lens include the chunk."""
+        import torch
+        rows = int(q.shape[0])
+        B = int(seq_lens.shape[0])
+        if out is None:
+            out = torch.empty_like(q)
+        ws = self.workspace(rows) if workspace is None else workspace
+        _lib.check("rcp_prefill_attn", self._lib.rcp_prefill_attn(
+            self._h, _ptr(q), _ptr(cu_chunk_lens), rows, _ptr(block_table),
+            int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out), _ptr(ws),
+            ws.numel() * ws.element_size(), _stream(stream)))
+        return out

@@ -1,0 +1,334 @@
+// C ABI of the rank-compressed paged attention library: handle, host block pool,
+// argument checks, tensor-map set-up and kernel dispatch by shape.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "launch.h"
+#include "rcp.h"
+#include "shape.h"
+
+using rcp::ShapeMain;
+using rcp::ShapeTiny;
+
+enum ShapeId { kShapeNone = -1, kShapeMain = 0, kShapeTiny = 1 };
+
+struct rcp_cache {
+  rcp_cache_config cfg;
+  void* k_pages;
+  void* v_pages;
+  const void* U_k;
+  const void* W_v;
+  uint32_t* dev_err;
+  int shape;
+  std::vector<int32_t> free_ids;   // LIFO stack of free physical blocks
+  std::vector<uint8_t> is_free;
+  // device-side state, set up at the first kernel call on a device
+  int device;
+  int num_sms;
+  CUtensorMap tmap_v;
+  // optional events recorded around the split-K attention kernel
+  cudaEvent_t prof_start;
+  cudaEvent_t prof_stop;
+};
+
+namespace {
+
+int shape_of(const rcp_cache_config* c) {
+  if (c->block_size != rcp::kBlockSize) return kShapeNone;
+  if (c->num_heads == ShapeMain::H && c->head_dim == ShapeMain::D && c->rank_k == ShapeMain::RK &&
+      c->rank_v == ShapeMain::R)
+    return kShapeMain;
+  if (c->num_heads == ShapeTiny::H && c->head_dim == ShapeTiny::D && c->rank_k == ShapeTiny::RK &&
+      c->rank_v == ShapeTiny::R)
+    return kShapeTiny;
+  return kShapeNone;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn) return fn;
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  return fn;
+}
+
+// Device set-up on first use per device: SM count, kernel attributes and the tensor map
+// of the V pages ([num_blocks*16 rows][R] fp16, 64 x 16 boxes, 128-byte swizzle, which
+// is the MN-major operand layout the value MMA reads).
+rcp_status ensure_device(rcp_cache* c) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RCP_ERR_CUDA;
+  if (dev == c->device) return RCP_OK;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return RCP_ERR_CUDA;
+  cudaError_t e = c->shape == kShapeMain ? rcp::prepare_attn<ShapeMain>(dev)
+                                         : rcp::prepare_attn<ShapeTiny>(dev);
+  if (e != cudaSuccess) return RCP_ERR_CUDA;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return RCP_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c->cfg.rank_v),
+                              static_cast<cuuint64_t>(c->cfg.num_blocks) * rcp::kBlockSize};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c->cfg.rank_v) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(rcp::kBlockSize)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&c->tmap_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->v_pages, dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return RCP_ERR_CUDA;
+  c->num_sms = sms;
+  c->device = dev;
+  return RCP_OK;
+}
+
+template <class S>
+size_t ws_bytes_for(int64_t nq) {
+  return rcp::ws_layout<S>(nq).total;
+}
+
+size_t ws_bytes(const rcp_cache* c, int64_t nq) {
+  return c->shape == kShapeMain ? ws_bytes_for<ShapeMain>(nq) : ws_bytes_for<ShapeTiny>(nq);
+}
+
+template <class S>
+void fill_ws(rcp::AttnParams& p, void* ws, int64_t nq) {
+  const rcp::WsLayout w = rcp::ws_layout<S>(nq);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  p.cum = reinterpret_cast<int64_t*>(b + w.cum);
+  p.qlen = reinterpret_cast<int32_t*>(b + w.qlen);
+  p.qrow = reinterpret_cast<int32_t*>(b + w.qrow);
+  p.qt = reinterpret_cast<float*>(b + w.qt);
+  p.rec = reinterpret_cast<float*>(b + w.rec);
+  p.zfin = reinterpret_cast<float*>(b + w.zfin);
+}
+
+rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, int32_t nq,
+                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                         const int32_t* seq_lens, int32_t batch, void* out, void* ws,
+                         size_t ws_size, rcp_stream stream) {
+  if (!c || batch < 0 || nq < 0 || max_blocks_per_seq < 1) return RCP_ERR_INVALID_ARG;
+  if (nq == 0) return RCP_OK;
+  if (batch == 0 && cu_chunk) return RCP_ERR_INVALID_ARG;
+  if (!q || !block_table || !seq_lens || !out || !ws) return RCP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (cu_chunk && (reinterpret_cast<uintptr_t>(cu_chunk) & 3u)))
+    return RCP_ERR_INVALID_ARG;
+  if (ws_size < ws_bytes(c, nq)) return RCP_ERR_WORKSPACE;
+  rcp_status st = ensure_device(c);
+  if (st != RCP_OK) return st;
+  rcp::AttnParams p{};
+  p.q = q;
+  p.U_k = c->U_k;
+  p.W_v = c->W_v;
+  p.k_pages = c->k_pages;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.cu_chunk = cu_chunk;
+  p.out = out;
+  p.dev_err = c->dev_err;
+  p.num_blocks = c->cfg.num_blocks;
+  p.bt_stride = max_blocks_per_seq;
+  p.batch = batch;
+  p.nq = nq;
+  // work partitions: one CTA per SM, never more than the blocks that can exist
+  const int64_t max_blocks_total = static_cast<int64_t>(nq) * max_blocks_per_seq;
+  int64_t parts = c->num_sms < rcp::kMaxParts ? c->num_sms : rcp::kMaxParts;
+  if (parts > max_blocks_total) parts = max_blocks_total;
+  if (parts < 1) parts = 1;
+  p.parts = static_cast<int32_t>(parts);
+  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->cfg.head_dim)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (c->shape == kShapeMain) {
+    fill_ws<ShapeMain>(p, ws, nq);
+    e = rcp::launch_attn<ShapeMain>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
+  } else {
+    fill_ws<ShapeTiny>(p, ws, nq);
+    e = rcp::launch_attn<ShapeTiny>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
+  }
+  return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rcp_status_string(rcp_status s) {
+  switch (s) {
+    case RCP_OK: return "ok";
+    case RCP_ERR_INVALID_ARG: return "invalid argument";
+    case RCP_ERR_UNSUPPORTED: return "unsupported shape";
+    case RCP_ERR_CAPACITY: return "block pool capacity / block id error";
+    case RCP_ERR_WORKSPACE: return "workspace too small";
+    case RCP_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+rcp_status rcp_config_supported(const rcp_cache_config* cfg) {
+  if (!cfg) return RCP_ERR_INVALID_ARG;
+  return shape_of(cfg) == kShapeNone ? RCP_ERR_UNSUPPORTED : RCP_OK;
+}
+
+rcp_status rcp_create_cache(const rcp_cache_config* cfg, void* k_pages, void* v_pages,
+                            const void* U_k, const void* W_v, uint32_t* dev_error,
+                            rcp_cache** out) {
+  if (!cfg || !out) return RCP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg->num_blocks < 1 || cfg->num_blocks > (int64_t{1} << 26)) return RCP_ERR_INVALID_ARG;
+  const int sh = shape_of(cfg);
+  if (sh == kShapeNone) return RCP_ERR_UNSUPPORTED;
+  if (!k_pages || !v_pages || !U_k || !W_v || !dev_error) return RCP_ERR_INVALID_ARG;
+  if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(U_k) || !aligned16(W_v) ||
+      (reinterpret_cast<uintptr_t>(dev_error) & 3u))
+    return RCP_ERR_INVALID_ARG;
+  rcp_cache* c = new (std::nothrow) rcp_cache();
+  if (!c) return RCP_ERR_CAPACITY;
+  c->cfg = *cfg;
+  c->k_pages = k_pages;
+  c->v_pages = v_pages;
+  c->U_k = U_k;
+  c->W_v = W_v;
+  c->dev_err = dev_error;
+  c->shape = sh;
+  c->device = -1;
+  c->num_sms = 0;
+  c->prof_start = nullptr;
+  c->prof_stop = nullptr;
+  try {
+    c->free_ids.resize(static_cast<size_t>(cfg->num_blocks));
+    c->is_free.assign(static_cast<size_t>(cfg->num_blocks), 1);
+  } catch (...) {
+    delete c;
+    return RCP_ERR_CAPACITY;
+  }
+  // pop order hands out ids 0, 1, 2, ... first
+  for (int64_t i = 0; i < cfg->num_blocks; ++i)
+    c->free_ids[static_cast<size_t>(i)] = static_cast<int32_t>(cfg->num_blocks - 1 - i);
+  *out = c;
+  return RCP_OK;
+}
+
+rcp_status rcp_destroy_cache(rcp_cache* cache) {
+  if (!cache) return RCP_ERR_INVALID_ARG;
+  delete cache;
+  return RCP_OK;
+}
+
+rcp_status rcp_alloc_blocks(rcp_cache* c, int32_t n, int32_t* ids_out) {
+  if (!c || n < 0 || (n > 0 && !ids_out)) return RCP_ERR_INVALID_ARG;
+  if (static_cast<size_t>(n) > c->free_ids.size()) return RCP_ERR_CAPACITY;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t id = c->free_ids.back();
+    c->free_ids.pop_back();
+    c->is_free[static_cast<size_t>(id)] = 0;
+    ids_out[i] = id;
+  }
+  return RCP_OK;
+}
+
+rcp_status rcp_free_blocks(rcp_cache* c, int32_t n, const int32_t* ids) {
+  if (!c || n < 0 || (n > 0 && !ids)) return RCP_ERR_INVALID_ARG;
+  // validate all first so a bad list changes nothing (duplicates inside the list too)
+  std::vector<uint8_t> seen;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t id = ids[i];
+    if (id < 0 || id >= c->cfg.num_blocks || c->is_free[static_cast<size_t>(id)])
+      return RCP_ERR_CAPACITY;
+  }
+  if (n > 1) {
+    seen.assign(static_cast<size_t>(c->cfg.num_blocks), 0);
+    for (int32_t i = 0; i < n; ++i) {
+      if (seen[static_cast<size_t>(ids[i])]) return RCP_ERR_CAPACITY;
+      seen[static_cast<size_t>(ids[i])] = 1;
+    }
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    c->is_free[static_cast<size_t>(ids[i])] = 1;
+    c->free_ids.push_back(ids[i]);
+  }
+  return RCP_OK;
+}
+
+rcp_status rcp_num_free_blocks(const rcp_cache* c, int64_t* n_free) {
+  if (!c || !n_free) return RCP_ERR_INVALID_ARG;
+  *n_free = static_cast<int64_t>(c->free_ids.size());
+  return RCP_OK;
+}
+
+rcp_status rcp_workspace_size(const rcp_cache* c, int32_t max_query_rows, size_t* bytes) {
+  if (!c || !bytes || max_query_rows < 0) return RCP_ERR_INVALID_ARG;
+  *bytes = ws_bytes(c, max_query_rows);
+  return RCP_OK;
+}
+
+rcp_status rcp_append_kv(rcp_cache* c, const void* k, const void* v, const int64_t* slot_mapping,
+                         int32_t num_tokens, rcp_stream stream) {
+  if (!c || num_tokens < 0) return RCP_ERR_INVALID_ARG;
+  if (num_tokens == 0) return RCP_OK;
+  if (!k || !v || !slot_mapping) return RCP_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return RCP_ERR_INVALID_ARG;
+  rcp::AppendParams p{};
+  p.k = k;
+  p.v = v;
+  p.slots = slot_mapping;
+  p.U_k = c->U_k;
+  p.W_v = c->W_v;
+  p.k_pages = c->k_pages;
+  p.v_pages = c->v_pages;
+  p.dev_err = c->dev_err;
+  p.num_blocks = c->cfg.num_blocks;
+  p.T = num_tokens;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = c->shape == kShapeMain ? rcp::launch_append<ShapeMain>(p, s)
+                                               : rcp::launch_append<ShapeTiny>(p, s);
+  return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
+}
+
+rcp_status rcp_decode_attn(rcp_cache* c, const void* q, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           rcp_stream stream) {
+  return run_attention(c, q, nullptr, batch, block_table, max_blocks_per_seq, seq_lens, batch, out,
+                       workspace, workspace_bytes, stream);
+}
+
+rcp_status rcp_prefill_attn(rcp_cache* c, const void* q, const int32_t* cu_chunk_lens,
+                            int32_t num_query_rows, const int32_t* block_table,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            rcp_stream stream) {
+  if (!cu_chunk_lens) return RCP_ERR_INVALID_ARG;
+  return run_attention(c, q, cu_chunk_lens, num_query_rows, block_table, max_blocks_per_seq,
+                       seq_lens, batch, out, workspace, workspace_bytes, stream);
+}
+
+rcp_status rcp_set_profile_events(rcp_cache* c, void* start_event, void* stop_event) {
+  if (!c || ((start_event == nullptr) != (stop_event == nullptr))) return RCP_ERR_INVALID_ARG;
+  c->prof_start = static_cast<cudaEvent_t>(start_event);
+  c->prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return RCP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,690 @@
+// Decode / chunked-prefill attention over low-rank paged coefficients.
+//
+// One call runs four kernels on the caller's stream:
+//   1. plan_qproj:  CTA 0 validates lengths and builds the per-query-row work plan
+//                   (keys attended, block-table row, prefix sums of blocks); the other
+//                   CTAs project queries into rank space, q~_h = U_k,h q_h, scaled by
+//                   log2(e)/sqrt(d) so the softmax can use exp2.
+//   2. decode_main: persistent split-K kernel.  The concatenated list of all requests'
+//                   blocks is cut into `parts` equal contiguous ranges, one per CTA.  Per
+//                   block: a bulk copy brings the K page (all heads) and four tensor-map
+//                   copies bring the V page into shared memory; CUDA cores score the
+//                   block (warp per 2 heads x 16 tokens, one lane per token); an online
+//                   softmax with lazy rescaling turns scores into fp16 weights P; one
+//                   elected thread issues tcgen05 MMAs Z^T[R x heads] += C_v^T P^T into
+//                   tensor memory.  At the end of each (request, range) segment the
+//                   accumulator and the running (max, sum) go to a partial record.
+//   3. combine:     merges a request's partial records in a fixed order (deterministic).
+//   4. upproj:      o_h = W_v[:, h*d:(h+1)*d]^T z_h, written as fp16.
+//
+// The steps follow the Proxima page: "Per-decode-step attention" (rank-space scoring of
+// the compressed cache, split-K with a combine kernel named in "Kernel profiling
+// breakdown", plus one matmul per step) and "Per-prefill-chunk attention" (each chunk
+// row attends its causal prefix; here every chunk row is planned as its own query row).
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdint>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "shape.h"
+
+namespace rcp {
+
+// ----------------------------------------------------------------------------- plan + q~
+constexpr int kPlanThreads = 256;
+constexpr int kQprojTile = 16;   // query rows per q-projection CTA
+
+template <class S>
+__global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnParams p) {
+  if (blockIdx.x == 0) {
+    // ---- plan: qlen / qrow per query row, then cum = prefix sum of ceil(qlen / 16)
+    __shared__ int64_t part_sum[kPlanThreads];
+    const int tid = threadIdx.x;
+    const int32_t max_len = p.bt_stride * kBlockSize;
+    for (int r = tid; r < p.nq; r += kPlanThreads) {
+      p.qlen[r] = 0;
+      p.qrow[r] = 0;
+    }
+    __syncthreads();
+    for (int b = tid; b < p.batch; b += kPlanThreads) {
+      const int32_t L = p.seq_lens[b];
+      const bool len_ok = L >= 0 && L <= max_len;
+      if (p.cu_chunk == nullptr) {
+        if (!len_ok) atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
+        p.qlen[b] = len_ok ? L : 0;
+        p.qrow[b] = b;
+      } else {
+        const int32_t c0 = p.cu_chunk[b], c1 = p.cu_chunk[b + 1];
+        const int32_t n = c1 - c0;
+        if (!len_ok || c0 < 0 || n < 0 || c1 > p.nq || n > L) {
+          atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
+          continue;
+        }
+        for (int32_t i = 0; i < n; ++i) {
+          p.qlen[c0 + i] = L - n + i + 1;   // causal: row i sees keys 0 .. P + i
+          p.qrow[c0 + i] = b;
+        }
+      }
+    }
+    __syncthreads();
+    const int per = (p.nq + kPlanThreads - 1) / kPlanThreads;
+    const int r0 = min(p.nq, tid * per), r1 = min(p.nq, r0 + per);
+    int64_t s = 0;
+    for (int r = r0; r < r1; ++r) s += (p.qlen[r] + kBlockSize - 1) / kBlockSize;
+    part_sum[tid] = s;
+    __syncthreads();
+    if (tid == 0) {
+      int64_t acc = 0;
+      for (int i = 0; i < kPlanThreads; ++i) {
+        const int64_t v = part_sum[i];
+        part_sum[i] = acc;
+        acc += v;
+      }
+    }
+    __syncthreads();
+    int64_t acc = part_sum[tid];
+    if (tid == 0) p.cum[0] = 0;
+    for (int r = r0; r < r1; ++r) {
+      acc += (p.qlen[r] + kBlockSize - 1) / kBlockSize;
+      p.cum[r + 1] = acc;
+    }
+    return;
+  }
+  // ---- q~ = U_k,h q_h for a tile of query rows and one head
+  constexpr int H = S::H, D = S::D, RK = S::RK;
+  __shared__ float ut[D][RK];              // U_k,h transposed: ut[j][k] = U[h][k][j]
+  __shared__ float qs[kQprojTile][D + 1];
+  const int bid = blockIdx.x - 1;
+  const int h = bid % H;
+  const int q0 = (bid / H) * kQprojTile;
+  const __half* U = static_cast<const __half*>(p.U_k) + static_cast<size_t>(h) * RK * D;
+  const __half* Q = static_cast<const __half*>(p.q);
+  for (int i = threadIdx.x; i < RK * D; i += kPlanThreads) {
+    const int k = i / D, j = i % D;
+    ut[j][k] = __half2float(U[i]);
+  }
+  for (int i = threadIdx.x; i < kQprojTile * D; i += kPlanThreads) {
+    const int qq = i / D, j = i % D;
+    const int row = q0 + qq;
+    qs[qq][j] = row < p.nq ? __half2float(Q[(static_cast<size_t>(row) * H + h) * D + j]) : 0.f;
+  }
+  __syncthreads();
+  constexpr int NG = kPlanThreads / RK;         // query groups
+  constexpr int PER = kQprojTile / NG;          // rows per thread
+  const int k = threadIdx.x % RK, grp = threadIdx.x / RK;
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  for (int j = 0; j < D; ++j) {
+    const float u = ut[j][k];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = fmaf(u, qs[grp + i * NG][j], acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int row = q0 + grp + i * NG;
+    if (row < p.nq) p.qt[(static_cast<size_t>(row) * H + h) * RK + k] = acc[i] * p.qscale;
+  }
+}
+
+// ---------------------------------------------------------------------------- decode main
+template <class S>
+struct DecodeSmem {
+  static constexpr int KST = 2, VST = 2;
+  static constexpr int P_BYTES = S::HP * 16 * 2;
+  static constexpr int V_OFF = 0;                                   // 1024-aligned stages
+  static constexpr int K_OFF = V_OFF + VST * S::VSTAGE_BYTES;
+  static constexpr int P_OFF = K_OFF + KST * S::KPAGE_BYTES;
+  static constexpr int Q_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int A_OFF = Q_OFF + S::H * S::RK * 4;            // alpha[2][HP]
+  static constexpr int F_OFF = A_OFF + 2 * S::HP * 4;               // flags[2][4]
+  static constexpr int BAR_OFF = F_OFF + 32;                        // 12 mbarriers
+  static constexpr int MISC_OFF = BAR_OFF + 12 * 8;                 // tmem slot, abort flag
+  static constexpr int TOTAL = MISC_OFF + 16;
+  static constexpr int ALLOC = TOTAL + 1024;                        // base alignment slack
+  static_assert(S::KPAGE_BYTES % 128 == 0 && S::VSTAGE_BYTES % 1024 == 0, "alignment");
+  static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+constexpr int kDecodeThreads = 192;   // warp 0 copies, warp 1 MMA, warps 2-5 compute
+constexpr float kRescaleThreshold = 8.f;   // log2 units: weights stay <= 2^8 before a rescale
+
+// Walks the requests that a CTA's block range crosses.
+struct ReqWalker {
+  const int64_t* cum;
+  int b;
+  int64_t bstart, bend;
+  __device__ __forceinline__ void init(const int64_t* c, int nq, int64_t g0) {
+    cum = c;
+    int lo = 0, hi = nq - 1;   // largest b with cum[b] <= g0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum[mid] <= g0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    bstart = cum[b];
+    bend = cum[b + 1];
+  }
+  __device__ __forceinline__ void advance_to(int64_t g) {
+    while (g >= bend) {
+      ++b;
+      bstart = bend;
+      bend = cum[b + 1];
+    }
+  }
+};
+
+struct BlockInfo {
+  int64_t phys;
+  int nvalid;      // tokens of this block that are attended (0 for a rejected block id)
+  bool seg_first, seg_last;
+};
+
+__device__ __forceinline__ BlockInfo block_info(const AttnParams& p, const ReqWalker& w,
+                                                int64_t g, int64_t g0, int64_t g1) {
+  BlockInfo bi;
+  const int64_t j = g - w.bstart;
+  const int64_t row = p.qrow[w.b];
+  const int64_t phys = p.block_table[row * p.bt_stride + j];
+  const int32_t L = p.qlen[w.b];
+  const bool bad = phys < 0 || phys >= p.num_blocks;
+  bi.phys = bad ? 0 : phys;
+  const int64_t left = L - j * kBlockSize;
+  bi.nvalid = bad ? 0 : static_cast<int>(left < kBlockSize ? left : kBlockSize);
+  bi.seg_first = (g == g0) || (g == w.bstart);
+  bi.seg_last = (g == g1 - 1) || (g + 1 == w.bend);
+  return bi;
+}
+
+template <class S>
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    decode_main_kernel(const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+  using L = DecodeSmem<S>;
+  constexpr int KST = L::KST, VST = L::VST, HP = S::HP;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* vst = sm + L::V_OFF;
+  uint8_t* kst = sm + L::K_OFF;
+  uint8_t* pbuf = sm + L::P_OFF;
+  float* qs = reinterpret_cast<float*>(sm + L::Q_OFF);
+  float* alpha_s = reinterpret_cast<float*>(sm + L::A_OFF);
+  int* flags_s = reinterpret_cast<int*>(sm + L::F_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
+  uint64_t* kfull = bars + 0;
+  uint64_t* kempty = bars + 2;
+  uint64_t* vfull = bars + 4;
+  uint64_t* vempty = bars + 6;
+  uint64_t* pfull = bars + 8;
+  uint64_t* pfree = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+  const int64_t T = p.cum[p.nq];
+  // never more partitions than blocks, so every partition's range is non-empty
+  const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
+  if (cta >= G) return;   // uniform over the CTA
+  const int64_t g0 = static_cast<int64_t>(cta) * T / G;
+  const int64_t g1 = static_cast<int64_t>(cta + 1) * T / G;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 4);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], 1);
+      mbar_init(&pfull[i], 4);
+      mbar_init(&pfree[i], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  // Zero both P buffers (padded head rows stay zero) and any part of a V stage that no
+  // copy fills (value rank below a multiple of 128: those MMA rows are never stored).
+  for (int i = threadIdx.x; i < 2 * L::P_BYTES / 16; i += kDecodeThreads)
+    reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0, 0, 0, 0);
+  if constexpr (S::NBOX < 2 * S::NCHUNK) {
+    constexpr int ZB = (2 * S::NCHUNK - S::NBOX) * 2048 / 16;
+    for (int s = 0; s < VST; ++s)
+      for (int i = threadIdx.x; i < ZB; i += kDecodeThreads)
+        reinterpret_cast<uint4*>(vst + s * S::VSTAGE_BYTES + S::NBOX * 2048)[i] =
+            make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  ReqWalker walk;
+  walk.init(p.cum, p.nq, g0);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ copy producer
+    if (lane == 0) {
+      prefetch_tmap(&tmap_v);
+      const uint64_t pol = policy_evict_first();
+      const uint8_t* kpages = static_cast<const uint8_t*>(p.k_pages);
+      int64_t nk = 0, nv = 0;
+      for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
+        walk.advance_to(g);
+        const int64_t j = g - walk.bstart;
+        const int64_t raw = p.block_table[static_cast<int64_t>(p.qrow[walk.b]) * p.bt_stride + j];
+        const bool bad = raw < 0 || raw >= p.num_blocks;
+        if (bad) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
+        const int64_t phys = bad ? 0 : raw;
+        const int ks = static_cast<int>(it % KST);
+        if (it >= KST && !mbar_wait(&kempty[ks], ((it / KST) - 1) & 1, abort_flag, p.dev_err)) break;
+        mbar_arrive_expect_tx(&kfull[ks], S::KPAGE_BYTES);
+        bulk_g2s_hint(kst + ks * S::KPAGE_BYTES, kpages + phys * S::KPAGE_BYTES, S::KPAGE_BYTES,
+                      &kfull[ks], pol);
+        ++nk;
+        const int vs = static_cast<int>(it % VST);
+        if (it >= VST && !mbar_wait(&vempty[vs], ((it / VST) - 1) & 1, abort_flag, p.dev_err)) break;
+        mbar_arrive_expect_tx(&vfull[vs], S::VPAGE_BYTES);
+#pragma unroll 1
+        for (int bx = 0; bx < S::NBOX; ++bx)
+          tma_load_2d_hint(vst + vs * S::VSTAGE_BYTES + bx * 2048, &tmap_v, bx * 64,
+                           static_cast<int32_t>(phys * kBlockSize), &vfull[vs], pol);
+        ++nv;
+      }
+      if (*abort_flag) {   // let copies already in flight land before the CTA exits
+        for (int64_t i = (nk > KST ? nk - KST : 0); i < nk; ++i)
+          mbar_wait_drain(&kfull[i % KST], (i / KST) & 1);
+        for (int64_t i = (nv > VST ? nv - VST : 0); i < nv; ++i)
+          mbar_wait_drain(&vfull[i % VST], (i / VST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_f16(128, HP, /*a_mn_major=*/true, /*b_mn_major=*/false);
+      int64_t issued = 0;
+      for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
+        walk.advance_to(g);
+        const bool seg_first = (g == g0) || (g == walk.bstart);
+        const int vs = static_cast<int>(it % VST), ps = static_cast<int>(it & 1);
+        if (!mbar_wait(&vfull[vs], (it / VST) & 1, abort_flag, p.dev_err)) break;
+        if (!mbar_wait(&pfull[ps], (it >> 1) & 1, abort_flag, p.dev_err)) break;
+        tc_fence_after();
+        const uint32_t vaddr = smem_u32(vst + vs * S::VSTAGE_BYTES);
+        const uint64_t bdesc = make_sdesc(smem_u32(pbuf + ps * L::P_BYTES), 128, 256, kSwizzleNone);
+#pragma unroll
+        for (int i = 0; i < S::NCHUNK; ++i) {
+          const uint64_t adesc = make_sdesc(vaddr + i * 4096, 2048, 1024, kSwizzle128B);
+          umma_f16(tmem_base + i * HP, adesc, bdesc, idesc, seg_first ? 0u : 1u);
+        }
+        umma_commit(&vempty[vs]);
+        umma_commit(&pfree[ps]);
+        ++issued;
+      }
+      if (issued > 0) mbar_wait_drain(&pfree[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
+    }
+  } else {
+    // ------------------------------------------------- scores, softmax, P, epilogue
+    constexpr int HPW = S::H / 4;               // heads per compute warp
+    constexpr int ROUNDS = (HPW + 1) / 2;       // two heads (16 lanes each) per round
+    constexpr int NCH = S::RK / 8;              // 16-byte chunks per K row
+    const int cw = warp - 2;                    // head group
+    const int quarter = warp & 3;               // TMEM lane quarter this warp may access
+    const int hl = lane >> 4, t = lane & 15;
+    const int ctid = threadIdx.x - 64;          // 0..127 over the compute warps
+    float m_run[ROUNDS], l_run[ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) { m_run[r] = -INFINITY; l_run[r] = 0.f; }
+    const float4* qs4 = reinterpret_cast<const float4*>(qs);
+
+    for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
+      walk.advance_to(g);
+      const BlockInfo bi = block_info(p, walk, g, g0, g1);
+      bool ok = true;
+      if (bi.seg_first) {
+        // rank-space query of this request into the permuted layout
+        // qs[((h*2 + hi)*NCH + c)*4 + e] = q~[h][8c + 4hi + e]
+        const float* src = p.qt + static_cast<size_t>(walk.b) * S::H * S::RK;
+        for (int i = ctid; i < S::H * S::RK; i += 128) {
+          const int h = i / S::RK, k = i % S::RK;
+          const int c = k >> 3, hi = (k >> 2) & 1, e = k & 3;
+          qs[((h * 2 + hi) * NCH + c) * 4 + e] = src[i];
+        }
+        named_bar_sync(1, 128);
+      }
+      const int ks = static_cast<int>(it % KST);
+      ok = mbar_wait(&kfull[ks], (it / KST) & 1, abort_flag, p.dev_err);
+      float s[ROUNDS];
+#pragma unroll
+      for (int r = 0; r < ROUNDS; ++r) {
+        const int hw = 2 * r + hl;
+        s[r] = -INFINITY;
+        if (ok && hw < HPW) {
+          const int h = cw * HPW + hw;
+          const __half* krow = reinterpret_cast<const __half*>(kst + ks * S::KPAGE_BYTES) +
+                               (h * kBlockSize + t) * S::RK;
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int v = 0; v < NCH; ++v) {
+            const int c = (v + t) % NCH;   // rotation keeps the 16 lanes on distinct banks
+            const uint4 kv = *reinterpret_cast<const uint4*>(krow + c * 8);
+            const float4 qa = qs4[(h * 2 + 0) * NCH + c];
+            const float4 qb = qs4[(h * 2 + 1) * NCH + c];
+            const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kv.x));
+            const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kv.y));
+            const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kv.z));
+            const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kv.w));
+            a0 = fmaf(k01.x, qa.x, a0);
+            a1 = fmaf(k01.y, qa.y, a1);
+            a0 = fmaf(k23.x, qa.z, a0);
+            a1 = fmaf(k23.y, qa.w, a1);
+            a0 = fmaf(k45.x, qb.x, a0);
+            a1 = fmaf(k45.y, qb.y, a1);
+            a0 = fmaf(k67.x, qb.z, a0);
+            a1 = fmaf(k67.y, qb.w, a1);
+          }
+          s[r] = a0 + a1;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kempty[ks]);
+
+      // online softmax (base 2), lazy rescale: the reference max only moves when a block
+      // max exceeds it by more than kRescaleThreshold, so the accumulator is rarely touched
+      __half ph[ROUNDS];
+      float alpha[ROUNDS];
+      bool need_any = false;
+#pragma unroll
+      for (int r = 0; r < ROUNDS; ++r) {
+        const int hw = 2 * r + hl;
+        const bool valid = ok && hw < HPW && t < bi.nvalid;
+        const float sv = valid ? s[r] : -INFINITY;
+        float bmax = sv;
+        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 8));
+        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 4));
+        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
+        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+        const float m_old = bi.seg_first ? -INFINITY : m_run[r];
+        const float m_new = (bmax > m_old + kRescaleThreshold) ? bmax : m_old;
+        alpha[r] = (m_new == m_old) ? 1.f : exp2f(m_old - m_new);
+        need_any |= (m_new != m_old) && !bi.seg_first;
+        const float pv = valid ? exp2f(sv - m_new) : 0.f;
+        ph[r] = __float2half_rn(pv);
+        float psum = __half2float(ph[r]);
+        psum += __shfl_xor_sync(0xffffffffu, psum, 8);
+        psum += __shfl_xor_sync(0xffffffffu, psum, 4);
+        psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+        psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+        l_run[r] = (bi.seg_first ? 0.f : l_run[r] * alpha[r]) + psum;
+        m_run[r] = m_new;
+      }
+      const int fb = static_cast<int>(it & 1);
+#pragma unroll
+      for (int r = 0; r < ROUNDS; ++r) {
+        const int hw = 2 * r + hl;
+        if (t == 0 && hw < HPW) alpha_s[fb * HP + cw * HPW + hw] = alpha[r];
+      }
+      const bool warp_need = __any_sync(0xffffffffu, need_any);
+      if (lane == 0) flags_s[fb * 4 + cw] = (warp_need ? 1 : 0) | (*abort_flag ? 2 : 0);
+      named_bar_sync(1, 128);
+      const int f = flags_s[fb * 4 + 0] | flags_s[fb * 4 + 1] | flags_s[fb * 4 + 2] |
+                    flags_s[fb * 4 + 3];
+      if (f & 2) break;
+
+      const int ps = static_cast<int>(it & 1);
+      if (it >= 2) ok = mbar_wait(&pfree[ps], ((it >> 1) - 1) & 1, abort_flag, p.dev_err) && ok;
+      if (f & 1) {
+        // rescale the accumulator columns after the previous block's MMAs have landed
+        ok = mbar_wait(&pfree[(it - 1) & 1], ((it - 1) >> 1) & 1, abort_flag, p.dev_err) && ok;
+        tc_fence_after();
+        if (ok) {
+#pragma unroll 1
+          for (int i = 0; i < S::NCHUNK; ++i) {
+#pragma unroll
+            for (int hh = 0; hh < HP / 16; ++hh) {
+              const uint32_t ta = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                  i * HP + hh * 16;
+              float v[16];
+              tmem_ld16(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int h = hh * 16 + e;
+                v[e] *= (h < S::H) ? alpha_s[fb * HP + h] : 1.f;
+              }
+              tmem_st16(ta, v);
+            }
+          }
+          tmem_wait_st();
+        }
+      }
+      // weights P (K-major, no swizzle): byte(h, t) = (h/8)*256 + (t/8)*128 + (h%8)*16 + (t%8)*2
+      {
+        uint8_t* pb = pbuf + ps * L::P_BYTES;
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+          const int hw = 2 * r + hl;
+          if (hw < HPW) {
+            const int h = cw * HPW + hw;
+            *reinterpret_cast<__half*>(pb + (h >> 3) * 256 + (t >> 3) * 128 + (h & 7) * 16 +
+                                       (t & 7) * 2) = ph[r];
+          }
+        }
+      }
+      if (bi.nvalid < kBlockSize) {
+        // tokens past the sequence end (or a rejected block): zero their V rows so that
+        // whatever those slots hold cannot reach the accumulator through 0 * NaN
+        const int vs = static_cast<int>(it % VST);
+        ok = mbar_wait(&vfull[vs], (it / VST) & 1, abort_flag, p.dev_err) && ok;
+        const int nrow = kBlockSize - bi.nvalid;
+        uint8_t* vb = vst + vs * S::VSTAGE_BYTES;
+        for (int idx = ctid; idx < nrow * S::NBOX * 8; idx += 128) {
+          const int row = bi.nvalid + idx / (S::NBOX * 8);
+          const int rem = idx % (S::NBOX * 8);
+          *reinterpret_cast<uint4*>(vb + (rem >> 3) * 2048 + row * 128 + (rem & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull[ps]);
+
+      if (bi.seg_last) {
+        ok = mbar_wait(&pfree[ps], (it >> 1) & 1, abort_flag, p.dev_err) && ok;
+        tc_fence_after();
+        if (ok) {
+          float* rec = p.rec + static_cast<size_t>(walk.b + cta) * S::REC;
+#pragma unroll 1
+          for (int i = 0; i < S::NCHUNK; ++i) {
+            const int rrow = i * 128 + quarter * 32 + lane;
+#pragma unroll
+            for (int hh = 0; hh < HP / 16; ++hh) {
+              const uint32_t ta = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                  i * HP + hh * 16;
+              float v[16];
+              tmem_ld16(ta, v);
+              tmem_wait_ld();
+              if (rrow < S::R) {
+                float4* dst = reinterpret_cast<float4*>(rec + static_cast<size_t>(rrow) * HP + hh * 16);
+                dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+                dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                dst[2] = make_float4(v[8], v[9], v[10], v[11]);
+                dst[3] = make_float4(v[12], v[13], v[14], v[15]);
+              }
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < ROUNDS; ++r) {
+            const int hw = 2 * r + hl;
+            if (t == 0 && hw < HPW) {
+              const int h = cw * HPW + hw;
+              rec[static_cast<size_t>(S::R) * HP + h] = m_run[r];
+              rec[static_cast<size_t>(S::R) * HP + HP + h] = l_run[r];
+            }
+          }
+        }
+        tc_fence_before();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+// ----------------------------------------------------------------------------- combine
+constexpr int kCombineThreads = 256;
+constexpr int kCombineRows = 64;   // joint-rank rows per CTA
+
+__device__ __forceinline__ int part_of(int64_t g, int64_t T, int G) {
+  // the CTA whose range [c*T/G, (c+1)*T/G) holds block g
+  return static_cast<int>(((g + 1) * G + T - 1) / T - 1);
+}
+
+template <class S>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnParams p) {
+  constexpr int HP = S::HP, H = S::H;
+  __shared__ float wts[kMaxParts][H];
+  __shared__ float zt[H][kCombineRows + 1];
+  const int b = blockIdx.x;
+  const int r0 = blockIdx.y * kCombineRows;
+  const int tid = threadIdx.x;
+  const int64_t c0 = p.cum[b], c1 = p.cum[b + 1];
+  float* zf = p.zfin + static_cast<size_t>(b) * H * S::R;
+  if (c1 == c0) {
+    for (int i = tid; i < H * kCombineRows; i += kCombineThreads) {
+      const int h = i / kCombineRows, x = i % kCombineRows;
+      if (r0 + x < S::R) zf[static_cast<size_t>(h) * S::R + r0 + x] = 0.f;
+    }
+    return;
+  }
+  const int64_t T = p.cum[p.nq];
+  const int G = static_cast<int>(T < p.parts ? T : p.parts);   // as in decode_main_kernel
+  const int pf = part_of(c0, T, G), pl = part_of(c1 - 1, T, G);
+  const int nrec = pl - pf + 1;
+  if (tid < H) {
+    const int h = tid;
+    float M = -INFINITY;
+    for (int i = 0; i < nrec; ++i) {
+      const float* rec = p.rec + static_cast<size_t>(b + pf + i) * S::REC;
+      M = fmaxf(M, rec[static_cast<size_t>(S::R) * HP + h]);
+    }
+    float lsum = 0.f;
+    for (int i = 0; i < nrec; ++i) {
+      const float* rec = p.rec + static_cast<size_t>(b + pf + i) * S::REC;
+      const float m = rec[static_cast<size_t>(S::R) * HP + h];
+      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+      wts[i][h] = w;
+      lsum += w * rec[static_cast<size_t>(S::R) * HP + HP + h];
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    for (int i = 0; i < nrec; ++i) wts[i][h] *= inv;
+  }
+  __syncthreads();
+  // thread -> (row, head): consecutive threads read consecutive floats of a record row
+  constexpr int RPP = kCombineThreads / HP;   // rows per pass
+  const int h = tid % HP;
+  const int rr = tid / HP;
+  if (h < H) {
+#pragma unroll 1
+    for (int x = rr; x < kCombineRows; x += RPP) {
+      const int r = r0 + x;
+      float acc = 0.f;
+      if (r < S::R) {
+        for (int i = 0; i < nrec; ++i) {
+          const float* rec = p.rec + static_cast<size_t>(b + pf + i) * S::REC;
+          acc = fmaf(wts[i][h], rec[static_cast<size_t>(r) * HP + h], acc);
+        }
+      }
+      zt[h][x] = acc;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < H * kCombineRows; i += kCombineThreads) {
+    const int hh = i / kCombineRows, x = i % kCombineRows;
+    if (r0 + x < S::R) zf[static_cast<size_t>(hh) * S::R + r0 + x] = zt[hh][x];
+  }
+}
+
+// ----------------------------------------------------------------------------- upproj
+constexpr int kUpQ = 8;   // query rows per CTA
+
+template <class S>
+__global__ void __launch_bounds__(S::D) upproj_kernel(const AttnParams p) {
+  constexpr int H = S::H, D = S::D, R = S::R;
+  __shared__ float zs[kUpQ][R];
+  const int h = blockIdx.x;
+  const int q0 = blockIdx.y * kUpQ;
+  for (int i = threadIdx.x; i < kUpQ * R; i += D) {
+    const int qq = i / R, r = i % R;
+    const int row = q0 + qq;
+    zs[qq][r] = row < p.nq ? p.zfin[(static_cast<size_t>(row) * H + h) * R + r] : 0.f;
+  }
+  __syncthreads();
+  const int j = threadIdx.x;
+  const __half* W = static_cast<const __half*>(p.W_v) + h * D + j;
+  float acc[kUpQ];
+#pragma unroll
+  for (int i = 0; i < kUpQ; ++i) acc[i] = 0.f;
+#pragma unroll 16
+  for (int r = 0; r < R; ++r) {
+    const float w = __half2float(__ldg(W + static_cast<size_t>(r) * H * D));
+#pragma unroll
+    for (int i = 0; i < kUpQ; ++i) acc[i] = fmaf(w, zs[i][r], acc[i]);
+  }
+  __half* out = static_cast<__half*>(p.out);
+#pragma unroll
+  for (int i = 0; i < kUpQ; ++i) {
+    const int row = q0 + i;
+    if (row < p.nq) out[(static_cast<size_t>(row) * H + h) * D + j] = __float2half_rn(acc[i]);
+  }
+}
+
+// ----------------------------------------------------------------------------- launches
+template <class S>
+cudaError_t prepare_attn(int device) {
+  (void)device;
+  return cudaFuncSetAttribute(decode_main_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DecodeSmem<S>::ALLOC);
+}
+
+template <class S>
+cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStream_t stream,
+                        cudaEvent_t prof_start, cudaEvent_t prof_stop) {
+  const int qtiles = (p.nq + kQprojTile - 1) / kQprojTile;
+  plan_qproj_kernel<S><<<1 + S::H * qtiles, kPlanThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (prof_start && (e = cudaEventRecord(prof_start, stream)) != cudaSuccess) return e;
+  decode_main_kernel<S><<<p.parts, kDecodeThreads, DecodeSmem<S>::ALLOC, stream>>>(tmap_v, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
+  combine_kernel<S><<<dim3(p.nq, (S::R + kCombineRows - 1) / kCombineRows), kCombineThreads, 0,
+                      stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  upproj_kernel<S><<<dim3(S::H, (p.nq + kUpQ - 1) / kUpQ), S::D, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template cudaError_t prepare_attn<ShapeMain>(int);
+template cudaError_t prepare_attn<ShapeTiny>(int);
+template cudaError_t launch_attn<ShapeMain>(const CUtensorMap&, const AttnParams&, cudaStream_t,
+                                            cudaEvent_t, cudaEvent_t);
+template cudaError_t launch_attn<ShapeTiny>(const CUtensorMap&, const AttnParams&, cudaStream_t,
+                                            cudaEvent_t, cudaEvent_t);
+
+}  // namespace rcp

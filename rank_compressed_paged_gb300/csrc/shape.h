@@ -1,0 +1,96 @@
+// Compile-time shapes, kernel parameter blocks and the workspace layout shared by the
+// host launch code and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace rcp {
+
+constexpr int kBlockSize = 16;   // tokens per page
+constexpr int kMaxParts = 256;   // upper bound on decode work partitions (CTAs)
+
+constexpr int pow2_at_least(int x, int lo) {
+  int p = lo;
+  while (p < x) p *= 2;
+  return p;
+}
+
+// (H, d, r_k, R): heads, head dim, key rank per head, joint value rank.
+template <int H_, int D_, int RK_, int R_>
+struct Shape {
+  static constexpr int H = H_, D = D_, RK = RK_, R = R_, BS = kBlockSize;
+  static_assert(H % 4 == 0 && H <= 32, "heads are split over 4 compute warps, <= 32");
+  static_assert(RK % 8 == 0 && R % 64 == 0 && D % 32 == 0 && D <= 256, "shape");
+  static constexpr int HP = H <= 16 ? 16 : 32;          // heads padded to the MMA N
+  static constexpr int NCHUNK = (R + 127) / 128;        // M = 128 chunks of the value rank
+  static constexpr int NBOX = R / 64;                   // 64-wide tensor boxes per V page
+  static constexpr int TMEM_COLS = pow2_at_least(NCHUNK * HP, 32);
+  static constexpr int KPAGE_BYTES = H * BS * RK * 2;   // one block of K coefficients
+  static constexpr int VPAGE_BYTES = BS * R * 2;        // one block of V coefficients
+  static constexpr int VSTAGE_BYTES = NCHUNK * 2 * 2048;  // smem A operand of NCHUNK MMAs
+  static constexpr int REC = R * HP + 2 * HP;           // floats in one partial record
+  static_assert(NCHUNK * HP <= 512, "accumulator must fit in tensor memory");
+};
+
+using ShapeMain = Shape<32, 128, 64, 1024>;
+using ShapeTiny = Shape<4, 64, 16, 64>;
+
+// Workspace carve-up for nq query rows (all offsets 256-byte aligned).
+struct WsLayout {
+  size_t cum, qlen, qrow, qt, rec, zfin, total;
+};
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+template <class S>
+inline WsLayout ws_layout(int64_t nq) {
+  WsLayout w{};
+  size_t o = 0;
+  w.cum = o;  o = align256(o + sizeof(int64_t) * (nq + 1));
+  w.qlen = o; o = align256(o + sizeof(int32_t) * nq);
+  w.qrow = o; o = align256(o + sizeof(int32_t) * nq);
+  w.qt = o;   o = align256(o + sizeof(float) * nq * S::H * S::RK);
+  w.rec = o;  o = align256(o + sizeof(float) * (nq + kMaxParts) * static_cast<size_t>(S::REC));
+  w.zfin = o; o = align256(o + sizeof(float) * nq * S::H * static_cast<size_t>(S::R));
+  w.total = o;
+  return w;
+}
+
+// Everything the attention kernels of one call see.
+struct AttnParams {
+  const void* q;              // [nq][H][d] fp16
+  const void* U_k;            // [H][r_k][d] fp16
+  const void* W_v;            // [R][H*d] fp16
+  const void* k_pages;        // [num_blocks][H][16][r_k] fp16
+  const int32_t* block_table; // [rows][bt_stride]
+  const int32_t* seq_lens;    // [batch]
+  const int32_t* cu_chunk;    // prefill: [batch+1]; decode: nullptr
+  void* out;                  // [nq][H][d] fp16
+  uint32_t* dev_err;
+  // workspace regions
+  int64_t* cum;               // [nq+1] prefix sums of blocks per query row
+  int32_t* qlen;              // [nq] keys attended by each query row
+  int32_t* qrow;              // [nq] block-table row of each query row
+  float* qt;                  // [nq][H][r_k] rank-space queries, scaled by log2(e)/sqrt(d)
+  float* rec;                 // [(nq + parts)][REC] split partials
+  float* zfin;                // [nq][H][R] normalised weighted coefficient sums
+  int64_t num_blocks;
+  int32_t bt_stride;          // max_blocks_per_seq
+  int32_t batch;
+  int32_t nq;
+  int32_t parts;              // decode CTAs (work partitions)
+  float qscale;               // log2(e) / sqrt(d)
+};
+
+struct AppendParams {
+  const void* k;              // [T][H][d] fp16
+  const void* v;              // [T][H*d] fp16
+  const int64_t* slots;       // [T]
+  const void* U_k;
+  const void* W_v;
+  void* k_pages;
+  void* v_pages;
+  uint32_t* dev_err;
+  int64_t num_blocks;
+  int32_t T;
+};
+
+}  // namespace rcp

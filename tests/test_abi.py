@@ -1,0 +1,137 @@
+"""The C-ABI library: loads, exports every declared symbol, validates on the host (no GPU).
+
+None of these tests launches a kernel: every call here returns before any CUDA call
+(argument checks, block pool, workspace arithmetic).  Pointers are fake but aligned.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rank_compressed_paged_gb300 import build
+    build.build()
+    from rank_compressed_paged_gb300 import _lib
+    return _lib.load()
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "rcp.h")).read()
+    return sorted(set(re.findall(r"^(?:const char\*|rcp_status)\s+(rcp_\w+)\(", src, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _cfg(_lib, H=32, d=128, rk=64, R=1024, bs=16, nb=100):
+    return _lib.CacheConfig(H, d, rk, R, bs, nb)
+
+
+def _create(lib, _lib, cfg, ptrs=(0x10000, 0x20000, 0x30000, 0x40000, 0x50000)):
+    h = ctypes.c_void_p()
+    st = lib.rcp_create_cache(ctypes.byref(cfg), *ptrs, ctypes.byref(h))
+    return st, h
+
+
+def test_config_support_and_status_strings(lib):
+    from rank_compressed_paged_gb300 import _lib
+    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib))) == _lib.RCP_OK
+    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, 4, 64, 16, 64))) == _lib.RCP_OK
+    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, bs=32))) == _lib.RCP_ERR_UNSUPPORTED
+    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, rk=48))) == _lib.RCP_ERR_UNSUPPORTED
+    assert lib.rcp_config_supported(None) == _lib.RCP_ERR_INVALID_ARG
+    for code in range(6):
+        assert lib.rcp_status_string(code)
+    assert b"workspace" in lib.rcp_status_string(_lib.RCP_ERR_WORKSPACE)
+
+
+def test_create_cache_rejects_bad_arguments(lib):
+    from rank_compressed_paged_gb300 import _lib
+    st, _ = _create(lib, _lib, _cfg(_lib, rk=48))
+    assert st == _lib.RCP_ERR_UNSUPPORTED
+    st, _ = _create(lib, _lib, _cfg(_lib, nb=0))
+    assert st == _lib.RCP_ERR_INVALID_ARG
+    st, _ = _create(lib, _lib, _cfg(_lib), ptrs=(0x10008, 0x20000, 0x30000, 0x40000, 0x50000))
+    assert st == _lib.RCP_ERR_INVALID_ARG            # misaligned K pages
+    st, _ = _create(lib, _lib, _cfg(_lib), ptrs=(0x10000, None, 0x30000, 0x40000, 0x50000))
+    assert st == _lib.RCP_ERR_INVALID_ARG            # null V pages
+    st, h = _create(lib, _lib, _cfg(_lib))
+    assert st == _lib.RCP_OK and h.value
+    assert lib.rcp_destroy_cache(h) == _lib.RCP_OK
+
+
+def test_block_pool_alloc_free(lib):
+    from rank_compressed_paged_gb300 import _lib
+    st, h = _create(lib, _lib, _cfg(_lib, nb=10))
+    assert st == _lib.RCP_OK
+    n = ctypes.c_int64()
+    lib.rcp_num_free_blocks(h, ctypes.byref(n))
+    assert n.value == 10
+    ids = (ctypes.c_int32 * 10)()
+    assert lib.rcp_alloc_blocks(h, 7, ids) == _lib.RCP_OK
+    got = [ids[i] for i in range(7)]
+    assert len(set(got)) == 7 and all(0 <= i < 10 for i in got)
+    assert lib.rcp_alloc_blocks(h, 4, ids) == _lib.RCP_ERR_CAPACITY     # only 3 left
+    lib.rcp_num_free_blocks(h, ctypes.byref(n))
+    assert n.value == 3                                                # unchanged on failure
+    bad = (ctypes.c_int32 * 2)(got[0], got[0])
+    assert lib.rcp_free_blocks(h, 2, bad) == _lib.RCP_ERR_CAPACITY       # duplicate in list
+    oob = (ctypes.c_int32 * 1)(10)
+    assert lib.rcp_free_blocks(h, 1, oob) == _lib.RCP_ERR_CAPACITY       # out of range
+    fr = (ctypes.c_int32 * 2)(got[0], got[1])
+    assert lib.rcp_free_blocks(h, 2, fr) == _lib.RCP_OK
+    assert lib.rcp_free_blocks(h, 1, fr) == _lib.RCP_ERR_CAPACITY        # double free
+    lib.rcp_num_free_blocks(h, ctypes.byref(n))
+    assert n.value == 5
+    assert lib.rcp_alloc_blocks(h, 5, ids) == _lib.RCP_OK
+    assert sorted(ids[i] for i in range(5)) == sorted(set(range(10)) - set(got[2:]))
+    lib.rcp_destroy_cache(h)
+
+
+def test_workspace_size_and_host_checks(lib):
+    from rank_compressed_paged_gb300 import _lib
+    st, h = _create(lib, _lib, _cfg(_lib))
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.rcp_workspace_size(h, 16, ctypes.byref(a)) == _lib.RCP_OK
+    assert lib.rcp_workspace_size(h, 64, ctypes.byref(b)) == _lib.RCP_OK
+    assert b.value > a.value > 0 and a.value % 256 == 0
+    assert lib.rcp_workspace_size(h, -1, ctypes.byref(a)) == _lib.RCP_ERR_INVALID_ARG
+    ws = 0x100000
+    # too-small workspace is rejected before any launch
+    assert lib.rcp_decode_attn(h, 0x1000, 0x2000, 64, 0x3000, 16, 0x4000, ws, 1024, None) \
+        == _lib.RCP_ERR_WORKSPACE
+    # misaligned q, null table, bad max_blocks
+    assert lib.rcp_decode_attn(h, 0x1008, 0x2000, 64, 0x3000, 16, 0x4000, ws, b.value, None) \
+        == _lib.RCP_ERR_INVALID_ARG
+    assert lib.rcp_decode_attn(h, 0x1000, None, 64, 0x3000, 16, 0x4000, ws, b.value, None) \
+        == _lib.RCP_ERR_INVALID_ARG
+    assert lib.rcp_decode_attn(h, 0x1000, 0x2000, 0, 0x3000, 16, 0x4000, ws, b.value, None) \
+        == _lib.RCP_ERR_INVALID_ARG
+    assert lib.rcp_decode_attn(h, 0x1000, 0x2000, 64, 0x3000, 0, 0x4000, ws, b.value, None) \
+        == _lib.RCP_OK                                               # empty batch: no work
+    assert lib.rcp_prefill_attn(h, 0x1000, None, 8, 0x2000, 64, 0x3000, 2, 0x4000, ws, b.value,
+                                None) == _lib.RCP_ERR_INVALID_ARG
+    assert lib.rcp_append_kv(h, 0x1000, 0x2000, 0x3004, 4, None) == _lib.RCP_ERR_INVALID_ARG
+    assert lib.rcp_append_kv(h, 0x1000, 0x2000, 0x3000, 0, None) == _lib.RCP_OK
+    assert lib.rcp_append_kv(h, 0x1000, 0x2000, 0x3000, -1, None) == _lib.RCP_ERR_INVALID_ARG
+    lib.rcp_destroy_cache(h)
+
+
+def test_python_layer_fails_loudly_without_library(tmp_path):
+    from rank_compressed_paged_gb300 import _lib
+    saved = _lib._lib
+    _lib._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            _lib.load(str(tmp_path / "nope.so"))
+    finally:
+        _lib._lib = saved

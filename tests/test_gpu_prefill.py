@@ -1,0 +1,40 @@
+"""GPU chunked-prefill attention vs the oracle, through the C ABI (needs a GB300)."""
+import numpy as np
+import pytest
+
+import workloads as wl
+from oracle import rcp_oracle as orc
+from tests.gpu_util import assert_close, make_cache, t
+
+pytestmark = pytest.mark.gpu
+
+TINY = wl.SHAPES["tiny"]
+MAIN = wl.SHAPES["mha32"]
+
+
+def _run(inp):
+    import torch
+    c = inp.cache
+    cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    cache.append_kv(t(inp.k), t(inp.v), t(inp.slot_mapping))
+    out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
+                             t(inp.seq_lens_after))
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    kp, vp = orc.append_kv(c.k_pages, c.v_pages, inp.U_k, inp.W_v, inp.k, inp.v,
+                           inp.slot_mapping, 16)
+    ref = orc.prefill_attn(inp.q, inp.cu_chunk_lens, kp, vp, inp.U_k, inp.W_v, c.block_table,
+                           inp.seq_lens_after, 16)
+    return out.cpu().numpy(), ref
+
+
+def test_tiny_prefill_ragged_chunks():
+    inp = wl.make_prefill_inputs(TINY, [0, 37, 64, 5], [40, 21, 16, 0], seed=41, fill=np.nan)
+    out, ref = _run(inp)
+    assert_close(out, ref, what="tiny prefill")
+
+
+def test_main_prefill_small():
+    inp = wl.make_prefill_inputs(MAIN, [100, 256], [48, 64], seed=42, fill=np.nan)
+    out, ref = _run(inp)
+    assert_close(out, ref, what="main prefill")
