@@ -1,8 +1,9 @@
 """GPU append (project + scatter) vs the oracle, through the C ABI (needs a GB300).
 
 Indices are checked bit-exactly (every slot not written keeps its sentinel bits);
-coefficient values agree with the oracle's fp64 -> fp16 rounding to within one fp16 ulp,
-and exactly when the factors are coordinate selections (projection is then a copy).
+coefficient values agree with the oracle's fp64 -> fp16 rounding to within one fp16 ulp
+plus the fp32 accumulation error bound (nearly all within one ulp), and exactly when the
+factors are coordinate selections (projection is then a copy).
 """
 import numpy as np
 import pytest
@@ -26,7 +27,15 @@ def _append(shape, U, W, kp, vp, k, v, slots):
     return cache.k_pages.cpu().numpy(), cache.v_pages.cpu().numpy(), cache
 
 
+def _gamma(n):
+    u = 2.0 ** -24                      # fp32 unit roundoff
+    return n * u / (1 - n * u)
+
+
 def _check(shape, U, W, nb, T, slots, seed, exact=False):
+    """Written coefficients: |gpu - oracle| <= one fp16 ulp + the fp32 dot-product error
+    bound gamma_n * sum_i |a_i b_i| (n = d for keys, H*d for values); exact when the
+    factors are coordinate selections (a single nonzero product per output)."""
     H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
     rng = np.random.default_rng(seed)
     kp = np.full((nb, H, 16, rk), SENTINEL, np.float16)
@@ -42,11 +51,26 @@ def _check(shape, U, W, nb, T, slots, seed, exact=False):
     assert np.array_equal(np.isnan(gk), kn) and np.array_equal(np.isnan(gv), vn)
     assert np.array_equal(gk.view(np.uint16)[kn], ok_.view(np.uint16)[kn])
     assert np.array_equal(gv.view(np.uint16)[vn], ov.view(np.uint16)[vn])
-    dk = fp16_ulp_diff(gk[~kn], ok_[~kn])
-    dv = fp16_ulp_diff(gv[~vn], ov[~vn])
-    lim = 0 if exact else 1
-    assert dk.max(initial=0) <= lim and dv.max(initial=0) <= lim, (dk.max(initial=0),
-                                                                    dv.max(initial=0))
+    Ua = np.abs(U.astype(np.float64))
+    Wa = np.abs(W.astype(np.float64))
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        blk, off = s // 16, s % 16
+        g_k, r_k = gk[blk, :, off, :], ok_[blk, :, off, :]
+        g_v, r_v = gv[blk, off, :], ov[blk, off, :]
+        if exact:
+            assert np.array_equal(g_k.view(np.uint16), r_k.view(np.uint16))
+            assert np.array_equal(g_v.view(np.uint16), r_v.view(np.uint16))
+            continue
+        sk = np.einsum("hkd,hd->hk", Ua, np.abs(k[i].astype(np.float64)))
+        sv = Wa @ np.abs(v[i].astype(np.float64)).reshape(-1)
+        tol_k = np.spacing(np.abs(r_k)).astype(np.float64) + _gamma(d) * sk
+        tol_v = np.spacing(np.abs(r_v)).astype(np.float64) + _gamma(H * d) * sv
+        assert np.all(np.abs(g_k.astype(np.float64) - r_k) <= tol_k), i
+        assert np.all(np.abs(g_v.astype(np.float64) - r_v) <= tol_v), i
+        # and almost everywhere within one ulp
+        assert np.mean(fp16_ulp_diff(g_v, r_v) <= 1) > 0.99
 
 
 def test_append_tiny_random_factors():
