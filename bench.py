@@ -31,10 +31,9 @@ if ROOT not in sys.path:
 
 import workloads as wl  # noqa: E402
 
-WORKLOAD = "decode_b64_l8192_append"
 METRIC = "decode-attn µs/step & GB/s at B=64,L=8192; fraction of GB300 HBM roofline"
 SHAPE = wl.SHAPES["mha32"]
-BATCH, SEQ = 64, 8192
+BATCH, SEQ = 64, 8192   # the measured configuration; --batch / --seq-len shrink it for ncu
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_b64_l8192.md")
 KERNEL_SRC = os.path.join(ROOT, "rank_compressed_paged_gb300", "csrc", "decode.cu")
 
@@ -126,6 +125,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def workload_name():
+    return f"decode_b{BATCH}_l{SEQ}_append"
+
+
 def make_workload(device, seed):
     """Device-resident cache (pages drawn on the GPU) + the step's host inputs."""
     import torch
@@ -203,7 +206,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * sum(times) / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
+        "config": {"workload": workload_name(), "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
                    "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
                          "kind": "oracle", "sample": sample},
@@ -331,7 +334,7 @@ def run_ours(args, rank, world, local_rank):
         "us_per_step": round(step_ms * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
+        "config": {"workload": workload_name(), "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
                    "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16,
                    "step": "append 1 token/seq + decode attention",
                    "l2": "inputs larger than L2 (3.2 GB of pages per GPU), no flush",
@@ -351,6 +354,7 @@ def run_ours(args, rank, world, local_rank):
 
 
 def main():
+    global BATCH, SEQ
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -359,7 +363,10 @@ def main():
     ap.add_argument("--cpu-requests", type=int, default=64)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=BATCH)
+    ap.add_argument("--seq-len", type=int, default=SEQ)
     args = ap.parse_args()
+    BATCH, SEQ = args.batch, args.seq_len
     rank, world, local_rank = dist_env()
     if world > 1:
         import torch.distributed as dist
