@@ -130,6 +130,27 @@ rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_c
  * cudaEvent_t handles owned by the caller; NULL, NULL turns the hook off. */
 rcp_status rcp_set_profile_events(rcp_cache* cache, void* start_event, void* stop_event);
 
+/* Decode without any caller-provided or allocated device memory.  The paper has no
+ * counterpart; this entry point exists for callers that cannot allocate: a host runtime
+ * that owns all device memory and gives plugins no workspace, or a serving loop that must
+ * not call cudaMalloc after start-up (an allocation can wait on device-wide
+ * synchronisation).  Same arguments and result as rcp_decode_attn minus the workspace:
+ * the scratch is a fixed array of RCP_NOALLOC_SCRATCH_BYTES inside this library, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Limit: batch must satisfy rcp_workspace_size(cache, batch) <=
+ *     RCP_NOALLOC_SCRATCH_BYTES (for H=32, d=128, r_k=64, R=1024 that is batch <= 123);
+ *     a larger batch returns RCP_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Allocates nothing: no cudaMalloc / cudaFree and no allocating library routine.
+ *   - Every call shares the one array: calls that overlap on the GPU (other streams,
+ *     other threads, no ordering between them) race and give wrong results.  Each call
+ *     rewrites all the scratch it reads, so earlier contents never leak into a result. */
+#define RCP_NOALLOC_SCRATCH_BYTES (64ull << 20)
+rcp_status rcp_decode_attn_noalloc(rcp_cache* cache, const void* q, const int32_t* block_table,
+                                   int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                   int32_t batch, void* out, rcp_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

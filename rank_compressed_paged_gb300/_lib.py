@@ -46,7 +46,10 @@ _SIG = {
     "rcp_prefill_attn": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _I32, _P, _P,
                                         ctypes.c_size_t, _P]),
     "rcp_set_profile_events": (ctypes.c_int, [_P, _P, _P]),
+    "rcp_decode_attn_noalloc": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P]),
 }
+
+RCP_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 
