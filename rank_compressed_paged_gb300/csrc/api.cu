@@ -31,7 +31,10 @@ struct rcp_cache {
   // device-side state, set up at the first kernel call on a device
   int device;
   int num_sms;
-  CUtensorMap tmap_v;
+  CUtensorMap tmap_v;       // V pages as [num_blocks*16][R], 64 x 16 boxes (decode A operand)
+  CUtensorMap tmap_wv_k;    // W_v as [R][H*d], 64 x 128 boxes (append: K-major A)
+  CUtensorMap tmap_wv_mn;   // W_v as [R][H*d], 64 x 64 boxes (up-projection: MN-major A)
+  CUtensorMap tmap_uk;      // U_k as [H*r_k][d], 64 x 128 boxes (append: K-major A)
   // optional events recorded around the split-K attention kernel
   cudaEvent_t prof_start;
   cudaEvent_t prof_stop;
@@ -70,9 +73,30 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Device set-up on first use per device: SM count, kernel attributes and the tensor map
-// of the V pages ([num_blocks*16 rows][R] fp16, 64 x 16 boxes, 128-byte swizzle, which
-// is the MN-major operand layout the value MMA reads).
+// A 2-D fp16 tensor map with 128-byte swizzle: `inner` elements per row (contiguous),
+// `rows` rows `row_bytes` apart, boxes of box_inner x box_rows.
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rows == 0) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class S>
+cudaError_t prepare_kernels(int dev) {
+  cudaError_t e = rcp::prepare_attn<S>(dev);
+  if (e == cudaSuccess) e = rcp::prepare_gemm<S>();
+  return e;
+}
+
+// Device set-up on first use per device: SM count, kernel attributes and the tensor maps
+// of the buffers the handle owns pointers to (V pages, W_v twice, U_k).
 rcp_status ensure_device(rcp_cache* c) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return RCP_ERR_CUDA;
@@ -80,20 +104,19 @@ rcp_status ensure_device(rcp_cache* c) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return RCP_ERR_CUDA;
-  cudaError_t e = c->shape == kShapeMain ? rcp::prepare_attn<ShapeMain>(dev)
-                                         : rcp::prepare_attn<ShapeTiny>(dev);
+  cudaError_t e = c->shape == kShapeMain ? prepare_kernels<ShapeMain>(dev)
+                                         : prepare_kernels<ShapeTiny>(dev);
   if (e != cudaSuccess) return RCP_ERR_CUDA;
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return RCP_ERR_CUDA;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c->cfg.rank_v),
-                              static_cast<cuuint64_t>(c->cfg.num_blocks) * rcp::kBlockSize};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c->cfg.rank_v) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(rcp::kBlockSize)};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&c->tmap_v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->v_pages, dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return RCP_ERR_CUDA;
+  const rcp_cache_config& g = c->cfg;
+  const uint64_t hd = static_cast<uint64_t>(g.num_heads) * g.head_dim;
+  if (!encode_2d(&c->tmap_v, c->v_pages, g.rank_v, static_cast<uint64_t>(g.num_blocks) * 16,
+                 static_cast<uint64_t>(g.rank_v) * 2, 64, 16) ||
+      !encode_2d(&c->tmap_wv_k, c->W_v, hd, g.rank_v, hd * 2, 64, 128) ||
+      !encode_2d(&c->tmap_wv_mn, c->W_v, hd, g.rank_v, hd * 2, 64, 64) ||
+      !encode_2d(&c->tmap_uk, c->U_k, g.head_dim,
+                 static_cast<uint64_t>(g.num_heads) * g.rank_k, static_cast<uint64_t>(g.head_dim) * 2,
+                 64, 128))
+    return RCP_ERR_CUDA;
   c->num_sms = sms;
   c->device = dev;
   return RCP_OK;
@@ -117,7 +140,8 @@ void fill_ws(rcp::AttnParams& p, void* ws, int64_t nq) {
   p.qrow = reinterpret_cast<int32_t*>(b + w.qrow);
   p.qt = reinterpret_cast<float*>(b + w.qt);
   p.rec = reinterpret_cast<float*>(b + w.rec);
-  p.zfin = reinterpret_cast<float*>(b + w.zfin);
+  p.zhi = b + w.zhi;
+  p.zlo = b + w.zlo;
 }
 
 rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, int32_t nq,
@@ -159,12 +183,22 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->cfg.head_dim)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (c->shape == kShapeMain) fill_ws<ShapeMain>(p, ws, nq);
+  else fill_ws<ShapeTiny>(p, ws, nq);
+  // z_hi / z_lo ([nq][H*R] fp16) as the up-projection's B operands, 64 x 64 boxes
+  CUtensorMap zhi_map, zlo_map;
+  const uint64_t hr = static_cast<uint64_t>(c->cfg.num_heads) * c->cfg.rank_v;
+  if (!encode_2d(&zhi_map, p.zhi, hr, static_cast<uint64_t>(nq), hr * 2, 64, 64) ||
+      !encode_2d(&zlo_map, p.zlo, hr, static_cast<uint64_t>(nq), hr * 2, 64, 64))
+    return RCP_ERR_CUDA;
   if (c->shape == kShapeMain) {
-    fill_ws<ShapeMain>(p, ws, nq);
     e = rcp::launch_attn<ShapeMain>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
+    if (e == cudaSuccess)
+      e = rcp::launch_upproj_gemm<ShapeMain>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s);
   } else {
-    fill_ws<ShapeTiny>(p, ws, nq);
     e = rcp::launch_attn<ShapeTiny>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
+    if (e == cudaSuccess)
+      e = rcp::launch_upproj_gemm<ShapeTiny>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s);
   }
   return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
 }
@@ -289,6 +323,8 @@ rcp_status rcp_append_kv(rcp_cache* c, const void* k, const void* v, const int64
   if (!k || !v || !slot_mapping) return RCP_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
     return RCP_ERR_INVALID_ARG;
+  rcp_status st = ensure_device(c);
+  if (st != RCP_OK) return st;
   rcp::AppendParams p{};
   p.k = k;
   p.v = v;
@@ -300,9 +336,18 @@ rcp_status rcp_append_kv(rcp_cache* c, const void* k, const void* v, const int64
   p.dev_err = c->dev_err;
   p.num_blocks = c->cfg.num_blocks;
   p.T = num_tokens;
+  // the new tokens' k and v as [T][H*d] B operands (64-token tiles up to 256 tokens)
+  const uint64_t hd = static_cast<uint64_t>(c->cfg.num_heads) * c->cfg.head_dim;
+  const uint32_t nt = num_tokens <= 256 ? 64 : 256;
+  CUtensorMap vmap, kmap;
+  if (!encode_2d(&vmap, v, hd, static_cast<uint64_t>(num_tokens), hd * 2, 64, nt) ||
+      !encode_2d(&kmap, k, hd, static_cast<uint64_t>(num_tokens), hd * 2, 64, nt))
+    return RCP_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = c->shape == kShapeMain ? rcp::launch_append<ShapeMain>(p, s)
-                                               : rcp::launch_append<ShapeTiny>(p, s);
+  const cudaError_t e =
+      c->shape == kShapeMain
+          ? rcp::launch_append_gemm<ShapeMain>(c->tmap_wv_k, c->tmap_uk, vmap, kmap, p, s)
+          : rcp::launch_append_gemm<ShapeTiny>(c->tmap_wv_k, c->tmap_uk, vmap, kmap, p, s);
   return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
 }
 

@@ -1,6 +1,6 @@
 // Decode / chunked-prefill attention over low-rank paged coefficients.
 //
-// One call runs four kernels on the caller's stream:
+// One call runs four kernels on the caller's stream (three of them here):
 //   1. plan_qproj:  CTA 0 validates lengths and builds the per-query-row work plan
 //                   (keys attended, block-table row, prefix sums of blocks); the other
 //                   CTAs project queries into rank space, q~_h = U_k,h q_h, scaled by
@@ -14,8 +14,9 @@
 //                   elected thread issues tcgen05 MMAs Z^T[R x heads] += C_v^T P^T into
 //                   tensor memory.  At the end of each (request, range) segment the
 //                   accumulator and the running (max, sum) go to a partial record.
-//   3. combine:     merges a request's partial records in a fixed order (deterministic).
-//   4. upproj:      o_h = W_v[:, h*d:(h+1)*d]^T z_h, written as fp16.
+//   3. combine:     merges a request's partial records in a fixed order (deterministic)
+//                   and stores z as an fp16 (hi, lo) pair for the up-projection GEMM.
+//   4. (gemm.cu)    o_h = W_v[:, h*d:(h+1)*d]^T z_h on tensor cores, written as fp16.
 //
 // The steps follow the Proxima page: "Per-decode-step attention" (rank-space scoring of
 // the compressed cache, split-K with a combine kernel named in "Kernel profiling
@@ -562,11 +563,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnPara
   const int r0 = blockIdx.y * kCombineRows;
   const int tid = threadIdx.x;
   const int64_t c0 = p.cum[b], c1 = p.cum[b + 1];
-  float* zf = p.zfin + static_cast<size_t>(b) * H * S::R;
+  __half* zh = static_cast<__half*>(p.zhi) + static_cast<size_t>(b) * H * S::R;
+  __half* zl = static_cast<__half*>(p.zlo) + static_cast<size_t>(b) * H * S::R;
   if (c1 == c0) {
     for (int i = tid; i < H * kCombineRows; i += kCombineThreads) {
       const int h = i / kCombineRows, x = i % kCombineRows;
-      if (r0 + x < S::R) zf[static_cast<size_t>(h) * S::R + r0 + x] = 0.f;
+      if (r0 + x < S::R) {
+        zh[static_cast<size_t>(h) * S::R + r0 + x] = __float2half_rn(0.f);
+        zl[static_cast<size_t>(h) * S::R + r0 + x] = __float2half_rn(0.f);
+      }
     }
     return;
   }
@@ -612,43 +617,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnPara
     }
   }
   __syncthreads();
+  // z as an unevaluated fp16 pair (hi + lo) so the up-projection can run on fp16 tensor
+  // cores with fp32-level accuracy
   for (int i = tid; i < H * kCombineRows; i += kCombineThreads) {
     const int hh = i / kCombineRows, x = i % kCombineRows;
-    if (r0 + x < S::R) zf[static_cast<size_t>(hh) * S::R + r0 + x] = zt[hh][x];
-  }
-}
-
-// ----------------------------------------------------------------------------- upproj
-constexpr int kUpQ = 8;   // query rows per CTA
-
-template <class S>
-__global__ void __launch_bounds__(S::D) upproj_kernel(const AttnParams p) {
-  constexpr int H = S::H, D = S::D, R = S::R;
-  __shared__ float zs[kUpQ][R];
-  const int h = blockIdx.x;
-  const int q0 = blockIdx.y * kUpQ;
-  for (int i = threadIdx.x; i < kUpQ * R; i += D) {
-    const int qq = i / R, r = i % R;
-    const int row = q0 + qq;
-    zs[qq][r] = row < p.nq ? p.zfin[(static_cast<size_t>(row) * H + h) * R + r] : 0.f;
-  }
-  __syncthreads();
-  const int j = threadIdx.x;
-  const __half* W = static_cast<const __half*>(p.W_v) + h * D + j;
-  float acc[kUpQ];
-#pragma unroll
-  for (int i = 0; i < kUpQ; ++i) acc[i] = 0.f;
-#pragma unroll 16
-  for (int r = 0; r < R; ++r) {
-    const float w = __half2float(__ldg(W + static_cast<size_t>(r) * H * D));
-#pragma unroll
-    for (int i = 0; i < kUpQ; ++i) acc[i] = fmaf(w, zs[i][r], acc[i]);
-  }
-  __half* out = static_cast<__half*>(p.out);
-#pragma unroll
-  for (int i = 0; i < kUpQ; ++i) {
-    const int row = q0 + i;
-    if (row < p.nq) out[(static_cast<size_t>(row) * H + h) * D + j] = __float2half_rn(acc[i]);
+    if (r0 + x < S::R) {
+      const float z = zt[hh][x];
+      const __half hi = __float2half_rn(z);
+      zh[static_cast<size_t>(hh) * S::R + r0 + x] = hi;
+      zl[static_cast<size_t>(hh) * S::R + r0 + x] = __float2half_rn(z - __half2float(hi));
+    }
   }
 }
 
@@ -674,9 +652,6 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStre
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
   combine_kernel<S><<<dim3(p.nq, (S::R + kCombineRows - 1) / kCombineRows), kCombineThreads, 0,
                       stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  upproj_kernel<S><<<dim3(S::H, (p.nq + kUpQ - 1) / kUpQ), S::D, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,431 @@
+// Tensor-core projections: the append's key / value projections and the decode's W_v
+// up-projection, as tcgen05 GEMMs D[128 x NT] = A[128 x K] * B[NT x K]^T.
+//
+// Both operands come from global memory through 2-D tensor maps with 128-byte swizzle
+// (64 fp16 of K per row), four pipeline stages, one elected thread issuing
+// tcgen05.mma.cta_group::1.kind::f16 into a TMEM accumulator.  When the token / query
+// count is small, K is split over a thread-block cluster of KS CTAs; each CTA sends the
+// rows owned by every peer to that peer's shared memory (distributed shared memory
+// stores), a cluster barrier publishes them, and each CTA sums and writes its rows.
+//
+//   append, value job:  A = W_v rows [m0, m0+128) (K-major over H*d), B = v tokens,
+//                       D[r][t] -> V page [slot_t / 16][slot_t % 16][m0 + r]
+//   append, key job:    A = U_k rows [h*r_k, h*r_k + 128) (K-major over d; rows past
+//                       r_k are ignored), B = k tokens of head h,
+//                       D[k][t] -> K page [slot_t / 16][h][slot_t % 16][k], k < r_k
+//   up-projection:      A = W_v[:, h*d:(h+1)*d]^T (MN-major), B = z_hi and z_lo (the
+//                       fp16 high / low parts of the merged weighted coefficient sums),
+//                       D[j][q] = o_{q,h,j}, written as fp16.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "rcp.h"
+#include "shape.h"
+
+namespace rcp {
+
+constexpr int kGemmThreads = 128;
+constexpr int kGemmStages = 4;
+constexpr int kABytes = 128 * 64 * 2;   // one A stage: 128 rows x 64 K (or 64 K x 128 M)
+
+enum GemmMode : int { kModeAppend = 0, kModeUpproj = 1 };
+
+template <int NT, int KS, int NB>
+struct GemmSmem {
+  static constexpr int B_BYTES = NT * 128;                     // one B operand stage
+  static constexpr int STAGE = kABytes + NB * B_BYTES;
+  static constexpr int RECV_OFF = kGemmStages * STAGE;         // split-K receive buffer
+  static constexpr int RECV_BYTES = KS > 1 ? 128 * NT * 4 : 0;
+  static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;        // full[S], empty[S], acc
+  static constexpr int MISC_OFF = BAR_OFF + (2 * kGemmStages + 1) * 8;
+  static constexpr int TOTAL = MISC_OFF + 16;
+  static constexpr int ALLOC = TOTAL + 1024;
+  static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
+  static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+struct GemmParams {
+  // append
+  const int64_t* slots;
+  void* k_pages;
+  void* v_pages;
+  int32_t T;
+  int64_t num_blocks;
+  // up-projection
+  void* out;
+  int32_t nq;
+  uint32_t* dev_err;
+};
+
+// Where one CTA's job reads and writes.
+struct GemmJob {
+  int kind;        // 0 value (append), 1 key (append), 2 up-projection, -1 idle
+  int a_x, a_y;    // tensor-map coordinates of A's first k-block (x innermost)
+  int b_x, b_y;    // coordinates of B's first k-block
+  int a_step_x, a_step_y, b_step_x;   // per-k-block coordinate steps
+  int kb0, kb1;    // k-block range of this CTA
+  int m0;          // first output row (value rank row) / head index
+  int n0;          // first token / query of the tile
+  bool reduce;     // cluster split-K reduction
+};
+
+template <class S, int MODE, int NT, int KS>
+__device__ __forceinline__ GemmJob gemm_job(uint32_t rank) {
+  GemmJob j{};
+  const int cluster = blockIdx.x / KS;
+  if constexpr (MODE == kModeAppend) {
+    constexpr int NM = (S::R + 127) / 128;
+    constexpr int NKG = (S::H + KS - 1) / KS;
+    constexpr int KBV = S::H * S::D / 64;
+    constexpr int KBK = S::D / 64;
+    const int tile = cluster / (NM + NKG);
+    const int sub = cluster % (NM + NKG);
+    j.n0 = tile * NT;
+    if (sub < NM) {
+      j.kind = 0;
+      j.m0 = sub * 128;
+      j.kb0 = static_cast<int>(rank) * KBV / KS;
+      j.kb1 = (static_cast<int>(rank) + 1) * KBV / KS;
+      j.a_x = j.kb0 * 64; j.a_y = j.m0; j.a_step_x = 64; j.a_step_y = 0;
+      j.b_x = j.kb0 * 64; j.b_y = j.n0; j.b_step_x = 64;
+      j.reduce = KS > 1;
+    } else {
+      const int h = (sub - NM) * KS + static_cast<int>(rank);
+      j.kind = h < S::H ? 1 : -1;
+      j.m0 = h;
+      j.kb0 = 0;
+      j.kb1 = KBK;
+      j.a_x = 0; j.a_y = h * S::RK; j.a_step_x = 64; j.a_step_y = 0;
+      j.b_x = h * S::D; j.b_y = j.n0; j.b_step_x = 64;
+      j.reduce = false;
+    }
+  } else {
+    constexpr int KBR = S::R / 64;
+    const int h = cluster % S::H;
+    const int tile = cluster / S::H;
+    j.kind = 2;
+    j.m0 = h;
+    j.n0 = tile * NT;
+    j.kb0 = static_cast<int>(rank) * KBR / KS;
+    j.kb1 = (static_cast<int>(rank) + 1) * KBR / KS;
+    j.a_x = h * S::D; j.a_y = j.kb0 * 64; j.a_step_x = 0; j.a_step_y = 64;
+    j.b_x = h * S::R + j.kb0 * 64; j.b_y = j.n0; j.b_step_x = 64;
+    j.reduce = KS > 1;
+  }
+  return j;
+}
+
+// Write one finished output element (row, column) of a job.
+template <class S>
+__device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j, int row, int col,
+                                           float v) {
+  const int n = j.n0 + col;
+  if (j.kind == 2) {
+    if (row < S::D && n < p.nq)
+      static_cast<__half*>(p.out)[(static_cast<size_t>(n) * S::H + j.m0) * S::D + row] =
+          __float2half_rn(v);
+    return;
+  }
+  if (n >= p.T) return;
+  const int64_t s = p.slots[n];
+  if (s < 0) return;
+  if (s >= p.num_blocks * kBlockSize) {
+    atomicOr(p.dev_err, RCP_DEVERR_BAD_SLOT);
+    return;
+  }
+  const int64_t blk = s / kBlockSize, off = s % kBlockSize;
+  if (j.kind == 0) {
+    const int r = j.m0 + row;
+    if (r < S::R)
+      static_cast<__half*>(p.v_pages)[(blk * kBlockSize + off) * S::R + r] = __float2half_rn(v);
+  } else if (row < S::RK) {
+    static_cast<__half*>(p.k_pages)[((blk * S::H + j.m0) * kBlockSize + off) * S::RK + row] =
+        __float2half_rn(v);
+  }
+}
+
+template <class S, int MODE, int NT, int KS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a2,
+                const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2,
+                const GemmParams p) {
+  constexpr int NB = MODE == kModeUpproj ? 2 : 1;     // B operands per stage (z_hi, z_lo)
+  using L = GemmSmem<NT, KS, NB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
+  uint64_t* empty = full + kGemmStages;
+  uint64_t* accb = empty + kGemmStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
+  float* recv = reinterpret_cast<float*>(sm + L::RECV_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = KS > 1 ? cluster_ctarank() : 0;
+  const GemmJob j = gemm_job<S, MODE, NT, KS>(rank);
+  // A key job uses the U_k map; every other job reads W_v through map_a.
+  const CUtensorMap* amap = (j.kind == 1) ? &map_a2 : &map_a;
+  const CUtensorMap* bmap = (j.kind == 1) ? &map_b2 : &map_b;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemmStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accb, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (j.reduce) cluster_sync_all();   // every peer is running before any remote store
+
+  const int nkb = j.kind >= 0 ? j.kb1 - j.kb0 : 0;
+  if (warp == 0 && lane == 0 && nkb > 0) {
+    // -------------------------------------------------------------- TMA producer
+    prefetch_tmap(amap);
+    prefetch_tmap(bmap);
+    int issued = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kGemmStages;
+      if (kb >= kGemmStages &&
+          !mbar_wait(&empty[s], ((kb / kGemmStages) - 1) & 1, abort_flag, p.dev_err))
+        break;
+      uint8_t* st = sm + s * L::STAGE;
+      mbar_arrive_expect_tx(&full[s], kABytes + NB * L::B_BYTES);
+      if (MODE == kModeUpproj) {
+        // W_v^T slice: two 64(j) x 64(r) boxes (MN-major atoms), rows r = k
+        tma_load_2d(st, amap, j.a_x, j.a_y + kb * j.a_step_y, &full[s]);
+        tma_load_2d(st + kABytes / 2, amap, j.a_x + 64, j.a_y + kb * j.a_step_y, &full[s]);
+      } else {
+        tma_load_2d(st, amap, j.a_x + kb * j.a_step_x, j.a_y, &full[s]);
+      }
+      tma_load_2d(st + kABytes, bmap, j.b_x + kb * j.b_step_x, j.b_y, &full[s]);
+      if (NB == 2)
+        tma_load_2d(st + kABytes + L::B_BYTES, &map_b2, j.b_x + kb * j.b_step_x, j.b_y, &full[s]);
+      ++issued;
+    }
+    if (*abort_flag)
+      for (int i = (issued > kGemmStages ? issued - kGemmStages : 0); i < issued; ++i)
+        mbar_wait_drain(&full[i % kGemmStages], (i / kGemmStages) & 1);
+  } else if (warp == 1 && lane == 0 && nkb > 0) {
+    // -------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = make_idesc_f16(128, NT, MODE == kModeUpproj, false);
+    int kb = 0;
+    for (; kb < nkb; ++kb) {
+      const int s = kb % kGemmStages;
+      if (!mbar_wait(&full[s], (kb / kGemmStages) & 1, abort_flag, p.dev_err)) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sm + s * L::STAGE);
+      const uint32_t b0 = a0 + kABytes;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {   // four K=16 steps per 64-wide k-block
+        const uint64_t ad = MODE == kModeUpproj
+                                ? make_sdesc(a0 + k * 2048, kABytes / 2, 1024, kSwizzle128B)
+                                : make_sdesc(a0 + k * 32, 16, 1024, kSwizzle128B);
+        const uint64_t bd = make_sdesc(b0 + k * 32, 16, 1024, kSwizzle128B);
+        umma_f16(tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        if (NB == 2) {
+          const uint64_t bd2 = make_sdesc(b0 + L::B_BYTES + k * 32, 16, 1024, kSwizzle128B);
+          umma_f16(tmem, ad, bd2, idesc, 1u);
+        }
+      }
+      umma_commit(&empty[s]);
+    }
+    umma_commit(accb);
+    if (kb < nkb) mbar_wait_drain(accb, 0);
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------------ epilogue
+  const bool have_acc = nkb > 0 && mbar_wait(accb, 0, abort_flag, p.dev_err);
+  tc_fence_after();
+  const int row = warp * 32 + lane;                          // TMEM lane = output row
+  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  if (!j.reduce) {
+    if (have_acc) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < NT; c0 += 16) {
+        float v[16];
+        tmem_ld16(trow + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) gemm_store<S>(p, j, row, c0 + e, v[e]);
+      }
+    }
+  } else {
+    // split-K: row r belongs to peer r / RPC; send it to slot [my rank] of that peer
+    constexpr int RPC = 128 / KS;
+    const uint32_t recv_local = smem_u32(recv);
+    const uint32_t dst_rank = static_cast<uint32_t>(row / RPC);
+    const uint32_t dst = map_to_rank(recv_local, dst_rank) +
+                         ((rank * RPC + (row % RPC)) * NT) * 4;
+#pragma unroll 1
+    for (int c0 = 0; c0 < NT; c0 += 16) {
+      float v[16];
+      if (have_acc) {
+        tmem_ld16(trow + c0, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; e += 4)
+        st_cluster_v4(dst + (c0 + e) * 4, v[e], v[e + 1], v[e + 2], v[e + 3]);
+    }
+    cluster_sync_all();
+    // sum the KS partial slices of my RPC rows and write them
+    for (int i = threadIdx.x; i < RPC * NT; i += kGemmThreads) {
+      const int rr = i % RPC, col = i / RPC;
+      float acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < KS; ++s) acc += recv[(s * RPC + rr) * NT + col];
+      gemm_store<S>(p, j, static_cast<int>(rank) * RPC + rr, col, acc);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------------------- launchers
+template <class K>
+static cudaError_t launch_cluster(K kernel, int grid, int cluster, int smem, cudaStream_t stream,
+                                  const CUtensorMap& a, const CUtensorMap& a2,
+                                  const CUtensorMap& b, const CUtensorMap& b2,
+                                  const GemmParams& p) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, a2, b, b2, p);
+}
+
+// Append: small token counts split K over an 8-CTA cluster (64-token tiles); large ones
+// use 256-token tiles without a split.
+template <class S>
+struct AppendCfg {
+  static constexpr int KS_SMALL = (S::H * S::D / 64) < 8 ? (S::H * S::D / 64) : 8;
+};
+
+template <class S>
+cudaError_t prepare_gemm() {
+  cudaError_t e;
+  auto set = [&](auto kernel, int smem) {
+    cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    return r;
+  };
+  constexpr int KSS = AppendCfg<S>::KS_SMALL;
+  if ((e = set(gemm_kernel<S, kModeAppend, 64, KSS>, GemmSmem<64, KSS, 1>::ALLOC)) != cudaSuccess)
+    return e;
+  if ((e = set(gemm_kernel<S, kModeAppend, 256, 1>, GemmSmem<256, 1, 1>::ALLOC)) != cudaSuccess)
+    return e;
+  constexpr int KSU = UpprojCfg<S>::KS;
+  if ((e = set(gemm_kernel<S, kModeUpproj, UpprojCfg<S>::NT, KSU>,
+               GemmSmem<UpprojCfg<S>::NT, KSU, 2>::ALLOC)) != cudaSuccess)
+    return e;
+  return cudaSuccess;
+}
+
+template <class S>
+cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
+                               const CUtensorMap& v_rows, const CUtensorMap& k_rows,
+                               const AppendParams& ap, cudaStream_t stream) {
+  if (ap.T == 0) return cudaSuccess;
+  GemmParams p{};
+  p.slots = ap.slots;
+  p.k_pages = ap.k_pages;
+  p.v_pages = ap.v_pages;
+  p.T = ap.T;
+  p.num_blocks = ap.num_blocks;
+  p.dev_err = ap.dev_err;
+  constexpr int NM = (S::R + 127) / 128;
+  if (ap.T <= 256) {
+    constexpr int KS = AppendCfg<S>::KS_SMALL;
+    constexpr int NKG = (S::H + KS - 1) / KS;
+    const int tiles = (ap.T + 63) / 64;
+    return launch_cluster(gemm_kernel<S, kModeAppend, 64, KS>, tiles * (NM + NKG) * KS, KS,
+                          GemmSmem<64, KS, 1>::ALLOC, stream, w_v, u_k, v_rows, k_rows, p);
+  }
+  const int tiles = (ap.T + 255) / 256;
+  return launch_cluster(gemm_kernel<S, kModeAppend, 256, 1>, tiles * (NM + S::H), 1,
+                        GemmSmem<256, 1, 1>::ALLOC, stream, w_v, u_k, v_rows, k_rows, p);
+}
+
+template <class S>
+cudaError_t launch_upproj_gemm(const CUtensorMap& w_v_mn, const CUtensorMap& z_hi,
+                               const CUtensorMap& z_lo, void* out, int nq, uint32_t* dev_err,
+                               cudaStream_t stream) {
+  GemmParams p{};
+  p.out = out;
+  p.nq = nq;
+  p.dev_err = dev_err;
+  constexpr int NT = UpprojCfg<S>::NT, KS = UpprojCfg<S>::KS;
+  const int tiles = (nq + NT - 1) / NT;
+  return launch_cluster(gemm_kernel<S, kModeUpproj, NT, KS>, tiles * S::H * KS, KS,
+                        GemmSmem<NT, KS, 2>::ALLOC, stream, w_v_mn, w_v_mn, z_hi, z_lo, p);
+}
+
+template cudaError_t prepare_gemm<ShapeMain>();
+template cudaError_t prepare_gemm<ShapeTiny>();
+template cudaError_t launch_append_gemm<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
+                                                   const CUtensorMap&, const CUtensorMap&,
+                                                   const AppendParams&, cudaStream_t);
+template cudaError_t launch_append_gemm<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
+                                                   const CUtensorMap&, const CUtensorMap&,
+                                                   const AppendParams&, cudaStream_t);
+template cudaError_t launch_upproj_gemm<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
+                                                   const CUtensorMap&, void*, int, uint32_t*,
+                                                   cudaStream_t);
+template cudaError_t launch_upproj_gemm<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
+                                                   const CUtensorMap&, void*, int, uint32_t*,
+                                                   cudaStream_t);
+
+}  // namespace rcp

@@ -13,6 +13,16 @@ template <class S>
 cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStream_t stream,
                         cudaEvent_t prof_start, cudaEvent_t prof_stop);
 template <class S>
-cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t prepare_gemm();
+// k_rows / v_rows: tensor maps over the new tokens' k and v ([T][H*d], box 64 x NT with
+// NT = 64 when T <= 256, else 256).
+template <class S>
+cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
+                               const CUtensorMap& v_rows, const CUtensorMap& k_rows,
+                               const AppendParams& p, cudaStream_t stream);
+template <class S>
+cudaError_t launch_upproj_gemm(const CUtensorMap& w_v_mn, const CUtensorMap& z_hi,
+                               const CUtensorMap& z_lo, void* out, int nq, uint32_t* dev_err,
+                               cudaStream_t stream);
 
 }  // namespace rcp

@@ -35,9 +35,17 @@ struct Shape {
 using ShapeMain = Shape<32, 128, 64, 1024>;
 using ShapeTiny = Shape<4, 64, 16, 64>;
 
+// Up-projection GEMM: 64 query rows per tile; the value rank R is split over a cluster of
+// up to 8 CTAs (one 64-wide k-block at least per CTA).
+template <class S>
+struct UpprojCfg {
+  static constexpr int NT = 64;
+  static constexpr int KS = (S::R / 64) < 8 ? (S::R / 64) : 8;
+};
+
 // Workspace carve-up for nq query rows (all offsets 256-byte aligned).
 struct WsLayout {
-  size_t cum, qlen, qrow, qt, rec, zfin, total;
+  size_t cum, qlen, qrow, qt, rec, zhi, zlo, total;
 };
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 template <class S>
@@ -49,7 +57,8 @@ inline WsLayout ws_layout(int64_t nq) {
   w.qrow = o; o = align256(o + sizeof(int32_t) * nq);
   w.qt = o;   o = align256(o + sizeof(float) * nq * S::H * S::RK);
   w.rec = o;  o = align256(o + sizeof(float) * (nq + kMaxParts) * static_cast<size_t>(S::REC));
-  w.zfin = o; o = align256(o + sizeof(float) * nq * S::H * static_cast<size_t>(S::R));
+  w.zhi = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
+  w.zlo = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
   w.total = o;
   return w;
 }
@@ -71,7 +80,8 @@ struct AttnParams {
   int32_t* qrow;              // [nq] block-table row of each query row
   float* qt;                  // [nq][H][r_k] rank-space queries, scaled by log2(e)/sqrt(d)
   float* rec;                 // [(nq + parts)][REC] split partials
-  float* zfin;                // [nq][H][R] normalised weighted coefficient sums
+  void* zhi;                  // [nq][H][R] fp16 high part of the merged weighted sums z
+  void* zlo;                  // [nq][H][R] fp16 low part: z - fp16(z)
   int64_t num_blocks;
   int32_t bt_stride;          // max_blocks_per_seq
   int32_t batch;
