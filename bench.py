@@ -251,8 +251,6 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     # ---- device-timed region (inputs resident in HBM; pages 3.2 GB >> L2, no flush needed)
-    k_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    k_stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     s_start = torch.cuda.Event(enable_timing=True)
     s_stop = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -260,15 +258,22 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         s_start.record(stream)
-        for i in range(args.steps):
-            cache.set_profile_events(k_starts[i], k_stops[i])
+        for _ in range(args.steps):
             step()
         s_stop.record(stream)
         torch.cuda.synchronize()
-    cache.set_profile_events(None, None)
     if world > 1:
         dist.barrier()
     step_ms = s_start.elapsed_time(s_stop) / args.steps
+    # ---- the split-K attention kernel alone: events recorded around it on its stream
+    # (the library then launches it in plain stream order so the events bracket it)
+    k_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k_stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        cache.set_profile_events(k_starts[i], k_stops[i])
+        step()
+    torch.cuda.synchronize()
+    cache.set_profile_events(None, None)
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k_starts, k_stops))
     assert cache.read_device_error() == 0, cache.read_device_error()
 
@@ -353,6 +358,97 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def prefill_flops(prior, chunk, batch):
+    """Algorithmic FLOPs of one chunked-prefill step in rank space (per request: chunk rows,
+    row i attends prior + i + 1 keys): scores 2*H*r_k, weighted sum 2*H*R per attended
+    key, query projection 2*H*r_k*d and up-projection 2*H*R*d per row, and the append's
+    projections 2*(H*r_k*d + R*H*d) per chunk token."""
+    H, d, rk, R = SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"], SHAPE["rank_v"]
+    keys = batch * sum(prior + i + 1 for i in range(chunk))
+    rows = batch * chunk
+    attn = keys * 2 * H * (rk + R) + rows * 2 * H * (rk * d + R * d)
+    append = rows * 2 * (H * rk * d + R * H * d)
+    return attn, append
+
+
+def run_prefill(args):
+    """Chunked prefill at batch 16, 4096 cached tokens + a 256-token chunk per request:
+    append the chunk, then causal chunk attention.  One JSON line (not the default run)."""
+    import torch
+    from rank_compressed_paged_gb300 import PagedCoeffCache
+    from rank_compressed_paged_gb300 import build as _build
+    _build.build()
+    B, prior, chunk = 16, 4096, 256
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    after = np.full(B, prior + chunk, np.int32)
+    kp, vp, table, lens = wl.make_paged_cache_device(after, SHAPE, 1004, device=dev,
+                                                     spare_blocks=16)
+    rng = np.random.default_rng(1004)
+    U, W = wl.make_factors(rng, 32, 128, 64, 1024)
+    T = B * chunk
+
+    def td(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    q = td(wl.fp16(rng.standard_normal((T, 32, 128))))
+    k = td(wl.fp16(rng.standard_normal((T, 32, 128))))
+    v = td(wl.fp16(rng.standard_normal((T, 32, 128))))
+    slots = td(np.array([wl.slot_for(table, b, prior + i) for b in range(B) for i in range(chunk)],
+                        np.int64))
+    cu = td((np.arange(B + 1) * chunk).astype(np.int32))
+    cache = PagedCoeffCache(32, 128, 64, 1024, kp.shape[0], td(U), td(W), k_pages=kp, v_pages=vp)
+    tab, ln = td(table), td(lens)
+    out = torch.empty_like(q)
+    ws = cache.workspace(T)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        cache.append_kv(k, v, slots)
+        cache.prefill_attn(q, cu, tab, ln, out=out, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    step_ms = e0.elapsed_time(e1) / args.steps
+    ks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        cache.set_profile_events(ks[i], ke[i])
+        step()
+    torch.cuda.synchronize()
+    cache.set_profile_events(None, None)
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ks, ke))
+    assert cache.read_device_error() == 0
+    attn_f, app_f = prefill_flops(prior, chunk, B)
+    # the split-K kernel streams each query row's whole causal prefix of pages
+    kern_bytes = B * sum(prior + i + 1 for i in range(chunk)) * (32 * 64 + 1024) * 2
+    peak_bw, kind = measured_peaks()
+    line = {
+        "metric": "chunked-prefill ms/step & algorithmic TFLOP/s at B=16, prior 4096 + chunk 256",
+        "value": round((attn_f + app_f) / (step_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        "ms_per_step": round(step_ms, 3), "steps": args.steps, "warmup": max(args.warmup, 3),
+        "higher_is_better": True, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "prefill_b16_p4096_c256", "batch": B, "prior": prior,
+                   "chunk": chunk, "algorithmic_flops": attn_f + app_f,
+                   "path": "chunk rows planned as causal query rows of the split-K kernel"},
+        "roofline": {"bound": "hbm", "kernel": "decode_main_kernel",
+                     "achieved": round(kern_bytes / (kern_ms * 1e-3) / 1e9, 1),
+                     "peak": peak_bw, "peak_kind": kind, "unit": "GB/s",
+                     "frac": round(kern_bytes / (kern_ms * 1e-3) / 1e9 / peak_bw, 4),
+                     "kernel_ms": round(kern_ms, 3), "bytes_per_launch": kern_bytes},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     global BATCH, SEQ
     ap = argparse.ArgumentParser()
@@ -365,6 +461,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=BATCH)
     ap.add_argument("--seq-len", type=int, default=SEQ)
+    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
     args = ap.parse_args()
     BATCH, SEQ = args.batch, args.seq_len
     rank, world, local_rank = dist_env()
@@ -378,6 +475,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.workload == "prefill":
+            run_prefill(args)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

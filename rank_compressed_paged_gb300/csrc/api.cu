@@ -194,11 +194,13 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   if (c->shape == kShapeMain) {
     e = rcp::launch_attn<ShapeMain>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
     if (e == cudaSuccess)
-      e = rcp::launch_upproj_gemm<ShapeMain>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s);
+      e = rcp::launch_upproj_gemm<ShapeMain>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s,
+                                             c->prof_start == nullptr);
   } else {
     e = rcp::launch_attn<ShapeTiny>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
     if (e == cudaSuccess)
-      e = rcp::launch_upproj_gemm<ShapeTiny>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s);
+      e = rcp::launch_upproj_gemm<ShapeTiny>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s,
+                                             c->prof_start == nullptr);
   }
   return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
 }

@@ -41,9 +41,11 @@ constexpr int kQprojTile = 16;   // query rows per q-projection CTA
 
 template <class S>
 __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnParams p) {
+  griddep_wait();       // launched as a dependent of the caller's previous kernel
+  griddep_launch();
   if (blockIdx.x == 0) {
     // ---- plan: qlen / qrow per query row, then cum = prefix sum of ceil(qlen / 16)
-    __shared__ int64_t part_sum[kPlanThreads];
+    __shared__ int64_t warp_sum[kPlanThreads / 32];
     const int tid = threadIdx.x;
     const int32_t max_len = p.bt_stride * kBlockSize;
     for (int r = tid; r < p.nq; r += kPlanThreads) {
@@ -72,22 +74,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
       }
     }
     __syncthreads();
+    // block-wide exclusive scan of per-thread sums (contiguous row ranges per thread)
     const int per = (p.nq + kPlanThreads - 1) / kPlanThreads;
     const int r0 = min(p.nq, tid * per), r1 = min(p.nq, r0 + per);
     int64_t s = 0;
     for (int r = r0; r < r1; ++r) s += (p.qlen[r] + kBlockSize - 1) / kBlockSize;
-    part_sum[tid] = s;
-    __syncthreads();
-    if (tid == 0) {
-      int64_t acc = 0;
-      for (int i = 0; i < kPlanThreads; ++i) {
-        const int64_t v = part_sum[i];
-        part_sum[i] = acc;
-        acc += v;
-      }
+    const int lane = tid & 31, w = tid >> 5;
+    int64_t incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
+    if (lane == 31) warp_sum[w] = incl;
     __syncthreads();
-    int64_t acc = part_sum[tid];
+    int64_t acc = incl - s;
+    for (int i = 0; i < w; ++i) acc += warp_sum[i];
     if (tid == 0) p.cum[0] = 0;
     for (int r = r0; r < r1; ++r) {
       acc += (p.qlen[r] + kBlockSize - 1) / kBlockSize;
@@ -97,16 +99,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
   }
   // ---- q~ = U_k,h q_h for a tile of query rows and one head
   constexpr int H = S::H, D = S::D, RK = S::RK;
-  __shared__ float ut[D][RK];              // U_k,h transposed: ut[j][k] = U[h][k][j]
+  __shared__ float ut[D][RK + 1];          // U_k,h transposed: ut[j][k] = U[h][k][j]
   __shared__ float qs[kQprojTile][D + 1];
   const int bid = blockIdx.x - 1;
   const int h = bid % H;
   const int q0 = (bid / H) * kQprojTile;
   const __half* U = static_cast<const __half*>(p.U_k) + static_cast<size_t>(h) * RK * D;
   const __half* Q = static_cast<const __half*>(p.q);
-  for (int i = threadIdx.x; i < RK * D; i += kPlanThreads) {
-    const int k = i / D, j = i % D;
-    ut[j][k] = __half2float(U[i]);
+  for (int i = threadIdx.x; i < RK * D / 8; i += kPlanThreads) {
+    const uint4 u8 = reinterpret_cast<const uint4*>(U)[i];
+    const __half* uh = reinterpret_cast<const __half*>(&u8);
+    const int k = (i * 8) / D, j0 = (i * 8) % D;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ut[j0 + e][k] = __half2float(uh[e]);
   }
   for (int i = threadIdx.x; i < kQprojTile * D; i += kPlanThreads) {
     const int qq = i / D, j = i % D;
@@ -227,13 +232,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
-  const int64_t T = p.cum[p.nq];
-  // never more partitions than blocks, so every partition's range is non-empty
-  const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
-  if (cta >= G) return;   // uniform over the CTA
-  const int64_t g0 = static_cast<int64_t>(cta) * T / G;
-  const int64_t g1 = static_cast<int64_t>(cta + 1) * T / G;
 
+  // prologue: nothing here reads what the previous kernel writes
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&kfull[i], 1);
@@ -266,14 +266,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_v);
+
+  griddep_wait();      // plan and rank-space queries are ready
+  griddep_launch();
+  const int64_t T = p.cum[p.nq];
+  // never more partitions than blocks, so every partition's range is non-empty
+  const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
+  const bool active = cta < G;   // uniform over the CTA
+  const int64_t g0 = active ? static_cast<int64_t>(cta) * T / G : 0;
+  const int64_t g1 = active ? static_cast<int64_t>(cta + 1) * T / G : 0;
 
   ReqWalker walk;
-  walk.init(p.cum, p.nq, g0);
+  if (active) walk.init(p.cum, p.nq, g0);
 
-  if (warp == 0) {
+  if (!active) {
+    // no blocks for this CTA
+  } else if (warp == 0) {
     // ------------------------------------------------------------------ copy producer
     if (lane == 0) {
-      prefetch_tmap(&tmap_v);
       const uint64_t pol = policy_evict_first();
       const uint8_t* kpages = static_cast<const uint8_t*>(p.k_pages);
       int64_t nk = 0, nv = 0;
@@ -554,67 +565,60 @@ __device__ __forceinline__ int part_of(int64_t g, int64_t T, int G) {
   return static_cast<int>(((g + 1) * G + T - 1) / T - 1);
 }
 
+// One CTA per (request, 64 joint-rank rows); thread (head h, row group) keeps 8 rows of
+// z_h.  Every thread derives its head's merge weights from the records' (max, sum)
+// pairs itself (the 8 threads of a head read the same words), so there is no shared
+// state before the accumulation, which walks the records in a fixed order.
 template <class S>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnParams p) {
   constexpr int HP = S::HP, H = S::H;
-  __shared__ float wts[kMaxParts][H];
   __shared__ float zt[H][kCombineRows + 1];
+  griddep_wait();
+  griddep_launch();
   const int b = blockIdx.x;
   const int r0 = blockIdx.y * kCombineRows;
   const int tid = threadIdx.x;
   const int64_t c0 = p.cum[b], c1 = p.cum[b + 1];
   __half* zh = static_cast<__half*>(p.zhi) + static_cast<size_t>(b) * H * S::R;
   __half* zl = static_cast<__half*>(p.zlo) + static_cast<size_t>(b) * H * S::R;
-  if (c1 == c0) {
-    for (int i = tid; i < H * kCombineRows; i += kCombineThreads) {
-      const int h = i / kCombineRows, x = i % kCombineRows;
-      if (r0 + x < S::R) {
-        zh[static_cast<size_t>(h) * S::R + r0 + x] = __float2half_rn(0.f);
-        zl[static_cast<size_t>(h) * S::R + r0 + x] = __float2half_rn(0.f);
-      }
-    }
-    return;
-  }
-  const int64_t T = p.cum[p.nq];
-  const int G = static_cast<int>(T < p.parts ? T : p.parts);   // as in decode_main_kernel
-  const int pf = part_of(c0, T, G), pl = part_of(c1 - 1, T, G);
-  const int nrec = pl - pf + 1;
-  if (tid < H) {
-    const int h = tid;
-    float M = -INFINITY;
-    for (int i = 0; i < nrec; ++i) {
-      const float* rec = p.rec + static_cast<size_t>(b + pf + i) * S::REC;
-      M = fmaxf(M, rec[static_cast<size_t>(S::R) * HP + h]);
-    }
-    float lsum = 0.f;
-    for (int i = 0; i < nrec; ++i) {
-      const float* rec = p.rec + static_cast<size_t>(b + pf + i) * S::REC;
-      const float m = rec[static_cast<size_t>(S::R) * HP + h];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      wts[i][h] = w;
-      lsum += w * rec[static_cast<size_t>(S::R) * HP + HP + h];
-    }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    for (int i = 0; i < nrec; ++i) wts[i][h] *= inv;
-  }
-  __syncthreads();
-  // thread -> (row, head): consecutive threads read consecutive floats of a record row
-  constexpr int RPP = kCombineThreads / HP;   // rows per pass
+  constexpr int RPP = kCombineThreads / HP;       // rows per pass
+  constexpr int NR = kCombineRows / RPP;          // rows per thread
   const int h = tid % HP;
   const int rr = tid / HP;
-  if (h < H) {
-#pragma unroll 1
-    for (int x = rr; x < kCombineRows; x += RPP) {
-      const int r = r0 + x;
-      float acc = 0.f;
-      if (r < S::R) {
-        for (int i = 0; i < nrec; ++i) {
-          const float* rec = p.rec + static_cast<size_t>(b + pf + i) * S::REC;
-          acc = fmaf(wts[i][h], rec[static_cast<size_t>(r) * HP + h], acc);
-        }
-      }
-      zt[h][x] = acc;
+  if (c1 > c0 && h < H) {
+    const int64_t T = p.cum[p.nq];
+    const int G = static_cast<int>(T < p.parts ? T : p.parts);   // as in decode_main_kernel
+    const int pf = part_of(c0, T, G), pl = part_of(c1 - 1, T, G);
+    const int nrec = pl - pf + 1;
+    const float* rec0 = p.rec + static_cast<size_t>(b + pf) * S::REC;
+    const float* ml = rec0 + static_cast<size_t>(S::R) * HP + h;   // m at +0, l at +HP
+    float M = -INFINITY;
+    for (int i = 0; i < nrec; ++i) M = fmaxf(M, ml[static_cast<size_t>(i) * S::REC]);
+    float lsum = 0.f;
+    for (int i = 0; i < nrec; ++i) {
+      const float m = ml[static_cast<size_t>(i) * S::REC];
+      if (m != -INFINITY) lsum += exp2f(m - M) * ml[static_cast<size_t>(i) * S::REC + HP];
     }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    float acc[NR];
+#pragma unroll
+    for (int k = 0; k < NR; ++k) acc[k] = 0.f;
+    const float* base = rec0 + static_cast<size_t>(r0 + rr) * HP + h;
+    for (int i = 0; i < nrec; ++i) {
+      const float m = ml[static_cast<size_t>(i) * S::REC];
+      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M) * inv;
+      const float* rp = base + static_cast<size_t>(i) * S::REC;
+      float v[NR];
+#pragma unroll
+      for (int k = 0; k < NR; ++k) v[k] = (r0 + rr + k * RPP < S::R) ? rp[k * RPP * HP] : 0.f;
+#pragma unroll
+      for (int k = 0; k < NR; ++k) acc[k] = fmaf(w, v[k], acc[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < NR; ++k) zt[h][rr + k * RPP] = acc[k];
+  } else if (h < H) {
+#pragma unroll
+    for (int k = 0; k < NR; ++k) zt[h][rr + k * RPP] = 0.f;   // empty sequence: z = 0
   }
   __syncthreads();
   // z as an unevaluated fp16 pair (hi + lo) so the up-projection can run on fp16 tensor
@@ -634,25 +638,31 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnPara
 template <class S>
 cudaError_t prepare_attn(int device) {
   (void)device;
-  return cudaFuncSetAttribute(decode_main_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              DecodeSmem<S>::ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(decode_main_kernel<S>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DecodeSmem<S>::ALLOC);
+  return e;
 }
 
+// All kernels are launched as programmatic dependents of the kernel before them (each
+// waits for its predecessor before touching its outputs or the caller's inputs), so
+// launch latency and prologues overlap the predecessor's tail.  With profiling events
+// the plain stream order is kept so the events bracket decode_main exactly.
 template <class S>
 cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStream_t stream,
                         cudaEvent_t prof_start, cudaEvent_t prof_stop) {
+  const bool pdl = prof_start == nullptr;
   const int qtiles = (p.nq + kQprojTile - 1) / kQprojTile;
-  plan_qproj_kernel<S><<<1 + S::H * qtiles, kPlanThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(plan_qproj_kernel<S>, dim3(1 + S::H * qtiles), dim3(kPlanThreads), 0,
+                             stream, pdl, p);
   if (e != cudaSuccess) return e;
   if (prof_start && (e = cudaEventRecord(prof_start, stream)) != cudaSuccess) return e;
-  decode_main_kernel<S><<<p.parts, kDecodeThreads, DecodeSmem<S>::ALLOC, stream>>>(tmap_v, p);
-  e = cudaGetLastError();
+  e = launch_pdl(decode_main_kernel<S>, dim3(p.parts), dim3(kDecodeThreads), DecodeSmem<S>::ALLOC,
+                 stream, pdl, tmap_v, p);
   if (e != cudaSuccess) return e;
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
-  combine_kernel<S><<<dim3(p.nq, (S::R + kCombineRows - 1) / kCombineRows), kCombineThreads, 0,
-                      stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<S>, dim3(p.nq, (S::R + kCombineRows - 1) / kCombineRows),
+                    dim3(kCombineThreads), 0, stream, pdl, p);
 }
 
 template cudaError_t prepare_attn<ShapeMain>(int);

@@ -30,19 +30,18 @@
 namespace rcp {
 
 constexpr int kGemmThreads = 128;
-constexpr int kGemmStages = 4;
 constexpr int kABytes = 128 * 64 * 2;   // one A stage: 128 rows x 64 K (or 64 K x 128 M)
 
 enum GemmMode : int { kModeAppend = 0, kModeUpproj = 1 };
 
-template <int NT, int KS, int NB>
+template <int NT, int KS, int NB, int STG>
 struct GemmSmem {
   static constexpr int B_BYTES = NT * 128;                     // one B operand stage
   static constexpr int STAGE = kABytes + NB * B_BYTES;
-  static constexpr int RECV_OFF = kGemmStages * STAGE;         // split-K receive buffer
+  static constexpr int RECV_OFF = STG * STAGE;                 // split-K receive buffer
   static constexpr int RECV_BYTES = KS > 1 ? 128 * NT * 4 : 0;
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;        // full[S], empty[S], acc
-  static constexpr int MISC_OFF = BAR_OFF + (2 * kGemmStages + 1) * 8;
+  static constexpr int MISC_OFF = BAR_OFF + (2 * STG + 1) * 8;
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
@@ -170,13 +169,14 @@ __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j
   }
 }
 
-template <class S, int MODE, int NT, int KS>
+template <class S, int MODE, int NT, int KS, int STG>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a2,
                 const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2,
                 const GemmParams p) {
   constexpr int NB = MODE == kModeUpproj ? 2 : 1;     // B operands per stage (z_hi, z_lo)
-  using L = GemmSmem<NT, KS, NB>;
+  constexpr int kGemmStages = STG;
+  using L = GemmSmem<NT, KS, NB, STG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -212,6 +212,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (j.reduce) cluster_sync_all();   // every peer is running before any remote store
+  griddep_wait();                     // operands written by the previous kernel are visible
+  griddep_launch();
 
   const int nkb = j.kind >= 0 ? j.kb1 - j.kb0 : 0;
   if (warp == 0 && lane == 0 && nkb > 0) {
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // --------------------------------------------------------------------------- launchers
 template <class K>
 static cudaError_t launch_cluster(K kernel, int grid, int cluster, int smem, cudaStream_t stream,
-                                  const CUtensorMap& a, const CUtensorMap& a2,
+                                  bool pdl, const CUtensorMap& a, const CUtensorMap& a2,
                                   const CUtensorMap& b, const CUtensorMap& b2,
                                   const GemmParams& p) {
   cudaLaunchConfig_t cfg{};
@@ -336,13 +338,15 @@ static cudaError_t launch_cluster(K kernel, int grid, int cluster, int smem, cud
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, a, a2, b, b2, p);
 }
 
@@ -363,13 +367,15 @@ cudaError_t prepare_gemm() {
     return r;
   };
   constexpr int KSS = AppendCfg<S>::KS_SMALL;
-  if ((e = set(gemm_kernel<S, kModeAppend, 64, KSS>, GemmSmem<64, KSS, 1>::ALLOC)) != cudaSuccess)
+  if ((e = set(gemm_kernel<S, kModeAppend, 64, KSS, 4>, GemmSmem<64, KSS, 1, 4>::ALLOC)) !=
+      cudaSuccess)
     return e;
-  if ((e = set(gemm_kernel<S, kModeAppend, 256, 1>, GemmSmem<256, 1, 1>::ALLOC)) != cudaSuccess)
+  if ((e = set(gemm_kernel<S, kModeAppend, 256, 1, 4>, GemmSmem<256, 1, 1, 4>::ALLOC)) !=
+      cudaSuccess)
     return e;
-  constexpr int KSU = UpprojCfg<S>::KS;
-  if ((e = set(gemm_kernel<S, kModeUpproj, UpprojCfg<S>::NT, KSU>,
-               GemmSmem<UpprojCfg<S>::NT, KSU, 2>::ALLOC)) != cudaSuccess)
+  constexpr int KSU = UpprojCfg<S>::KS, STU = UpprojCfg<S>::STAGES;
+  if ((e = set(gemm_kernel<S, kModeUpproj, UpprojCfg<S>::NT, KSU, STU>,
+               GemmSmem<UpprojCfg<S>::NT, KSU, 2, STU>::ALLOC)) != cudaSuccess)
     return e;
   return cudaSuccess;
 }
@@ -391,26 +397,26 @@ cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
     constexpr int KS = AppendCfg<S>::KS_SMALL;
     constexpr int NKG = (S::H + KS - 1) / KS;
     const int tiles = (ap.T + 63) / 64;
-    return launch_cluster(gemm_kernel<S, kModeAppend, 64, KS>, tiles * (NM + NKG) * KS, KS,
-                          GemmSmem<64, KS, 1>::ALLOC, stream, w_v, u_k, v_rows, k_rows, p);
+    return launch_cluster(gemm_kernel<S, kModeAppend, 64, KS, 4>, tiles * (NM + NKG) * KS, KS,
+                          GemmSmem<64, KS, 1, 4>::ALLOC, stream, true, w_v, u_k, v_rows, k_rows, p);
   }
   const int tiles = (ap.T + 255) / 256;
-  return launch_cluster(gemm_kernel<S, kModeAppend, 256, 1>, tiles * (NM + S::H), 1,
-                        GemmSmem<256, 1, 1>::ALLOC, stream, w_v, u_k, v_rows, k_rows, p);
+  return launch_cluster(gemm_kernel<S, kModeAppend, 256, 1, 4>, tiles * (NM + S::H), 1,
+                        GemmSmem<256, 1, 1, 4>::ALLOC, stream, true, w_v, u_k, v_rows, k_rows, p);
 }
 
 template <class S>
 cudaError_t launch_upproj_gemm(const CUtensorMap& w_v_mn, const CUtensorMap& z_hi,
                                const CUtensorMap& z_lo, void* out, int nq, uint32_t* dev_err,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool pdl) {
   GemmParams p{};
   p.out = out;
   p.nq = nq;
   p.dev_err = dev_err;
-  constexpr int NT = UpprojCfg<S>::NT, KS = UpprojCfg<S>::KS;
+  constexpr int NT = UpprojCfg<S>::NT, KS = UpprojCfg<S>::KS, STG = UpprojCfg<S>::STAGES;
   const int tiles = (nq + NT - 1) / NT;
-  return launch_cluster(gemm_kernel<S, kModeUpproj, NT, KS>, tiles * S::H * KS, KS,
-                        GemmSmem<NT, KS, 2>::ALLOC, stream, w_v_mn, w_v_mn, z_hi, z_lo, p);
+  return launch_cluster(gemm_kernel<S, kModeUpproj, NT, KS, STG>, tiles * S::H * KS, KS,
+                        GemmSmem<NT, KS, 2, STG>::ALLOC, stream, pdl, w_v_mn, w_v_mn, z_hi, z_lo, p);
 }
 
 template cudaError_t prepare_gemm<ShapeMain>();
@@ -423,9 +429,9 @@ template cudaError_t launch_append_gemm<ShapeTiny>(const CUtensorMap&, const CUt
                                                    const AppendParams&, cudaStream_t);
 template cudaError_t launch_upproj_gemm<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
                                                    const CUtensorMap&, void*, int, uint32_t*,
-                                                   cudaStream_t);
+                                                   cudaStream_t, bool);
 template cudaError_t launch_upproj_gemm<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
                                                    const CUtensorMap&, void*, int, uint32_t*,
-                                                   cudaStream_t);
+                                                   cudaStream_t, bool);
 
 }  // namespace rcp

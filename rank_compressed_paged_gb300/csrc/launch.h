@@ -23,6 +23,6 @@ cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
 template <class S>
 cudaError_t launch_upproj_gemm(const CUtensorMap& w_v_mn, const CUtensorMap& z_hi,
                                const CUtensorMap& z_lo, void* out, int nq, uint32_t* dev_err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool pdl);
 
 }  // namespace rcp

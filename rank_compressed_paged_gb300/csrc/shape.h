@@ -41,6 +41,8 @@ template <class S>
 struct UpprojCfg {
   static constexpr int NT = 64;
   static constexpr int KS = (S::R / 64) < 8 ? (S::R / 64) : 8;
+  static constexpr int KB_PER_CTA = (S::R / 64) / KS;
+  static constexpr int STAGES = KB_PER_CTA < 4 ? KB_PER_CTA : 4;   // pipeline depth needed
 };
 
 // Workspace carve-up for nq query rows (all offsets 256-byte aligned).
