@@ -35,6 +35,7 @@ struct rcp_cache {
   CUtensorMap tmap_wv_k;    // W_v as [R][H*d], 64 x 128 boxes (append: K-major A)
   CUtensorMap tmap_wv_mn;   // W_v as [R][H*d], 64 x 64 boxes (up-projection: MN-major A)
   CUtensorMap tmap_uk;      // U_k as [H*r_k][d], 64 x 128 boxes (append: K-major A)
+  CUtensorMap tmap_kp;      // K pages as [num_blocks*H*16][r_k], 64 x 16 boxes (prefill B)
   // optional events recorded around the split-K attention kernel
   cudaEvent_t prof_start;
   cudaEvent_t prof_stop;
@@ -92,6 +93,7 @@ template <class S>
 cudaError_t prepare_kernels(int dev) {
   cudaError_t e = rcp::prepare_attn<S>(dev);
   if (e == cudaSuccess) e = rcp::prepare_gemm<S>();
+  if (e == cudaSuccess) e = rcp::prepare_prefill<S>();
   return e;
 }
 
@@ -115,7 +117,10 @@ rcp_status ensure_device(rcp_cache* c) {
       !encode_2d(&c->tmap_wv_mn, c->W_v, hd, g.rank_v, hd * 2, 64, 64) ||
       !encode_2d(&c->tmap_uk, c->U_k, g.head_dim,
                  static_cast<uint64_t>(g.num_heads) * g.rank_k, static_cast<uint64_t>(g.head_dim) * 2,
-                 64, 128))
+                 64, 128) ||
+      !encode_2d(&c->tmap_kp, c->k_pages, g.rank_k,
+                 static_cast<uint64_t>(g.num_blocks) * g.num_heads * 16,
+                 static_cast<uint64_t>(g.rank_k) * 2, 64, 16))
     return RCP_ERR_CUDA;
   c->num_sms = sms;
   c->device = dev;
@@ -133,6 +138,7 @@ size_t ws_bytes(const rcp_cache* c, int64_t nq) {
 
 template <class S>
 void fill_ws(rcp::AttnParams& p, void* ws, int64_t nq) {
+  using S_ = S;
   const rcp::WsLayout w = rcp::ws_layout<S>(nq);
   uint8_t* b = static_cast<uint8_t*>(ws);
   p.cum = reinterpret_cast<int64_t*>(b + w.cum);
@@ -142,6 +148,12 @@ void fill_ws(rcp::AttnParams& p, void* ws, int64_t nq) {
   p.rec = reinterpret_cast<float*>(b + w.rec);
   p.zhi = b + w.zhi;
   p.zlo = b + w.zlo;
+  p.tile_b = reinterpret_cast<int32_t*>(b + w.tile_b);
+  p.tile_qt = reinterpret_cast<int32_t*>(b + w.tile_qt);
+  p.tcount = reinterpret_cast<int32_t*>(b + w.tcount);
+  // prefill queries reuse the decode query region: hi then lo, [nq][H][64] fp16 each
+  p.qhi = b + w.qt;
+  p.qlo = b + w.qt + static_cast<size_t>(nq) * S::H * 64 * 2;
 }
 
 rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, int32_t nq,
@@ -185,6 +197,38 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   cudaError_t e;
   if (c->shape == kShapeMain) fill_ws<ShapeMain>(p, ws, nq);
   else fill_ws<ShapeTiny>(p, ws, nq);
+  const bool pdl = c->prof_start == nullptr;
+  if (cu_chunk) {
+    // chunked prefill: plan + fp16 rank-space queries, then the tiled tensor-core kernel
+    const uint64_t hq = static_cast<uint64_t>(c->cfg.num_heads) * 64;
+    CUtensorMap qhi_map, qlo_map;
+    if (static_cast<int64_t>(c->cfg.num_blocks) * c->cfg.num_heads * 16 >= (int64_t{1} << 31))
+      return RCP_ERR_UNSUPPORTED;
+    if (!encode_2d(&qhi_map, p.qhi, hq, static_cast<uint64_t>(nq), hq * 2, 64, 128) ||
+        !encode_2d(&qlo_map, p.qlo, hq, static_cast<uint64_t>(nq), hq * 2, 64, 128))
+      return RCP_ERR_CUDA;
+    const int max_tiles = static_cast<int>((nq + 127) / 128 + (batch < nq ? batch : nq));
+    if (c->shape == kShapeMain) {
+      e = rcp::launch_plan<ShapeMain>(p, s, pdl);
+      if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
+      if (e == cudaSuccess)
+        e = rcp::launch_prefill<ShapeMain>(qhi_map, qlo_map, c->tmap_kp, c->tmap_v, c->tmap_wv_mn,
+                                           p, max_tiles, s, pdl);
+    } else {
+      e = rcp::launch_plan<ShapeTiny>(p, s, pdl);
+      if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
+      if (e == cudaSuccess)
+        e = rcp::launch_prefill<ShapeTiny>(qhi_map, qlo_map, c->tmap_kp, c->tmap_v, c->tmap_wv_mn,
+                                           p, max_tiles, s, pdl);
+    }
+    if (e == cudaSuccess && c->prof_stop) e = cudaEventRecord(c->prof_stop, s);
+    return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
+  }
+  p.tile_b = nullptr;   // decode: no prefill tiles, fp32 queries
+  p.tile_qt = nullptr;
+  p.tcount = nullptr;
+  p.qhi = nullptr;
+  p.qlo = nullptr;
   // z_hi / z_lo ([nq][H*R] fp16) as the up-projection's B operands, 64 x 64 boxes
   CUtensorMap zhi_map, zlo_map;
   const uint64_t hr = static_cast<uint64_t>(c->cfg.num_heads) * c->cfg.rank_v;
@@ -195,12 +239,12 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
     e = rcp::launch_attn<ShapeMain>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
     if (e == cudaSuccess)
       e = rcp::launch_upproj_gemm<ShapeMain>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s,
-                                             c->prof_start == nullptr);
+                                             pdl);
   } else {
     e = rcp::launch_attn<ShapeTiny>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
     if (e == cudaSuccess)
       e = rcp::launch_upproj_gemm<ShapeTiny>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s,
-                                             c->prof_start == nullptr);
+                                             pdl);
   }
   return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
 }

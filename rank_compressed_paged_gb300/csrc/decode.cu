@@ -95,6 +95,39 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
       acc += (p.qlen[r] + kBlockSize - 1) / kBlockSize;
       p.cum[r + 1] = acc;
     }
+    if (p.tile_b != nullptr) {
+      // prefill: list the 128-row query tiles of every valid request, in request order
+      __syncthreads();
+      const int bper = (p.batch + kPlanThreads - 1) / kPlanThreads;
+      const int b0 = min(p.batch, tid * bper), b1 = min(p.batch, b0 + bper);
+      auto tiles_of = [&](int b) -> int {
+        const int32_t L = p.seq_lens[b], c0 = p.cu_chunk[b], c1 = p.cu_chunk[b + 1];
+        const int32_t n = c1 - c0;
+        const bool ok = L >= 0 && L <= max_len && c0 >= 0 && n >= 0 && c1 <= p.nq && n <= L;
+        return ok ? (n + 127) / 128 : 0;
+      };
+      int64_t ts = 0;
+      for (int b = b0; b < b1; ++b) ts += tiles_of(b);
+      int64_t tin = ts;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, tin, o);
+        if (lane >= o) tin += y;
+      }
+      if (lane == 31) warp_sum[w] = tin;
+      __syncthreads();
+      int64_t t0 = tin - ts;
+      for (int i = 0; i < w; ++i) t0 += warp_sum[i];
+      for (int b = b0; b < b1; ++b) {
+        const int nt = tiles_of(b);
+        for (int i = 0; i < nt; ++i) {
+          p.tile_b[t0 + i] = b;
+          p.tile_qt[t0 + i] = i;
+        }
+        t0 += nt;
+      }
+      if (tid == kPlanThreads - 1) *p.tcount = static_cast<int32_t>(t0);
+    }
     return;
   }
   // ---- q~ = U_k,h q_h for a tile of query rows and one head
@@ -133,7 +166,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int row = q0 + grp + i * NG;
-    if (row < p.nq) p.qt[(static_cast<size_t>(row) * H + h) * RK + k] = acc[i] * p.qscale;
+    if (row >= p.nq) continue;
+    const float qv = acc[i] * p.qscale;
+    if (p.qhi == nullptr) {
+      p.qt[(static_cast<size_t>(row) * H + h) * RK + k] = qv;
+    } else {
+      // prefill: fp16 (hi, lo) pair feeding the score MMA, zero-padded to 64 ranks
+      const __half hi = __float2half_rn(qv);
+      const size_t base = (static_cast<size_t>(row) * H + h) * 64;
+      static_cast<__half*>(p.qhi)[base + k] = hi;
+      static_cast<__half*>(p.qlo)[base + k] = __float2half_rn(qv - __half2float(hi));
+      for (int pad = RK + k; pad < 64; pad += RK) {
+        static_cast<__half*>(p.qhi)[base + pad] = __float2half_rn(0.f);
+        static_cast<__half*>(p.qlo)[base + pad] = __float2half_rn(0.f);
+      }
+    }
   }
 }
 
@@ -455,6 +502,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       if (f & 1) {
         // rescale the accumulator columns after the previous block's MMAs have landed
         ok = mbar_wait(&pfree[(it - 1) & 1], ((it - 1) >> 1) & 1, abort_flag, p.dev_err) && ok;
+        ok = __all_sync(0xffffffffu, ok);   // TMEM loads / stores are warp-collective
         tc_fence_after();
         if (ok) {
 #pragma unroll 1
@@ -511,6 +559,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
       if (bi.seg_last) {
         ok = mbar_wait(&pfree[ps], (it >> 1) & 1, abort_flag, p.dev_err) && ok;
+        ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         if (ok) {
           float* rec = p.rec + static_cast<size_t>(walk.b + cta) * S::REC;
@@ -665,6 +714,15 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStre
                     dim3(kCombineThreads), 0, stream, pdl, p);
 }
 
+template <class S>
+cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream, bool pdl) {
+  const int qtiles = (p.nq + kQprojTile - 1) / kQprojTile;
+  return launch_pdl(plan_qproj_kernel<S>, dim3(1 + S::H * qtiles), dim3(kPlanThreads), 0, stream,
+                    pdl, p);
+}
+
+template cudaError_t launch_plan<ShapeMain>(const AttnParams&, cudaStream_t, bool);
+template cudaError_t launch_plan<ShapeTiny>(const AttnParams&, cudaStream_t, bool);
 template cudaError_t prepare_attn<ShapeMain>(int);
 template cudaError_t prepare_attn<ShapeTiny>(int);
 template cudaError_t launch_attn<ShapeMain>(const CUtensorMap&, const AttnParams&, cudaStream_t,

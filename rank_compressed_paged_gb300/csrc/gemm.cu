@@ -49,26 +49,6 @@ struct GemmSmem {
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-
 struct GemmParams {
   // append
   const int64_t* slots;
@@ -273,7 +253,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncwarp();
 
   // ------------------------------------------------------------------ epilogue
-  const bool have_acc = nkb > 0 && mbar_wait(accb, 0, abort_flag, p.dev_err);
+  // warp-uniform, since TMEM loads are warp-collective
+  const bool have_acc = __all_sync(0xffffffffu, nkb > 0 && mbar_wait(accb, 0, abort_flag, p.dev_err));
   tc_fence_after();
   const int row = warp * 32 + lane;                          // TMEM lane = output row
   const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);

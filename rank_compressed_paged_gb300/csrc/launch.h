@@ -12,6 +12,15 @@ cudaError_t prepare_attn(int device);
 template <class S>
 cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStream_t stream,
                         cudaEvent_t prof_start, cudaEvent_t prof_stop);
+// Plan + rank-space queries only (the prefill path's first kernel).
+template <class S>
+cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream, bool pdl);
+template <class S>
+cudaError_t prepare_prefill();
+template <class S>
+cudaError_t launch_prefill(const CUtensorMap& qhi, const CUtensorMap& qlo, const CUtensorMap& kp,
+                           const CUtensorMap& vp, const CUtensorMap& w, const AttnParams& p,
+                           int max_tiles, cudaStream_t stream, bool pdl);
 template <class S>
 cudaError_t prepare_gemm();
 // k_rows / v_rows: tensor maps over the new tokens' k and v ([T][H*d], box 64 x NT with

@@ -1,0 +1,507 @@
+// Chunked-prefill attention over low-rank paged coefficients on tensor cores.
+//
+// The "Per-prefill-chunk attention" step of the Proxima page: every row i of a request's
+// chunk (absolute position P + i) attends keys 0 .. P + i of the paged cache, after the
+// chunk itself has been appended.  The scores are rank-space products and the values a
+// joint coefficient contraction, so one CTA owns (request, head h, 128 query rows, one
+// slice of up to 256 of the R joint ranks) and walks the causal key range in tiles of
+// 128 tokens (8 pages):
+//
+//   S   = Q~_h C_k,h^T          tcgen05, M=128 rows x N=128 keys x K=64 (q~ as fp16 hi+lo)
+//   P   = exp2(S - m)           one thread per query row (TMEM lane), lazy rescaling
+//   Z  += P C_v[:, slice]       tcgen05, M=128 x N=256 x K=128, accumulator in TMEM
+//
+// S is double-buffered in TMEM so the score MMA of tile j+1 overlaps the softmax of tile
+// j, and the softmax of tile j overlaps the value MMA of tile j-1.  At the end each row
+// is normalised, split into an fp16 (hi, lo) pair and multiplied by the slice's rows of
+// W_v[:, h*d:(h+1)*d] (tcgen05 again); the slices of one (request, head, tile) form a
+// thread-block cluster and sum their partial outputs through distributed shared memory.
+//
+// Warps: 0 issues the tensor copies, 1 issues the MMAs (and owns TMEM), 2-5 run the
+// softmax and the epilogue (warp w serves TMEM lanes 32*(w%4) .. +31).
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "rcp.h"
+#include "shape.h"
+
+namespace rcp {
+
+constexpr int kPfThreads = 192;
+constexpr float kPfRescale = 8.f;   // log2 units: weights stay below 2^8 between rescales
+
+template <class S>
+struct PfSmem {
+  using C = PrefillCfg<S>;
+  static constexpr int NG = C::RQ / 64;                 // 64-wide groups in the rank slice
+  static constexpr int Q_BYTES = 128 * 128;             // one [128][64] fp16 operand
+  static constexpr int K_BYTES = C::KT * 128;           // key coefficients of one tile
+  static constexpr int V_BYTES = C::KT * C::RQ * 2;     // value coefficients of one tile
+  static constexpr int STAGE = K_BYTES + V_BYTES;
+  static constexpr int P_BYTES = 128 * C::KT * 2;
+  static constexpr int ST_OFF = 2 * Q_BYTES;            // q~ hi at 0, q~ lo at Q_BYTES
+  static constexpr int P_OFF = ST_OFF + 2 * STAGE;
+  static constexpr int ZH_OFF = ST_OFF;                 // epilogue reuses the stage memory
+  static constexpr int ZL_OFF = ZH_OFF + 128 * C::RQ * 2;
+  static constexpr int W_OFF = ZL_OFF + 128 * C::RQ * 2;
+  static constexpr int W_BYTES = C::RQ * S::D * 2;
+  static constexpr int END = (P_OFF + P_BYTES > W_OFF + W_BYTES) ? P_OFF + P_BYTES
+                                                                   : W_OFF + W_BYTES;
+  static constexpr int BAR_OFF = END;                   // 13 mbarriers
+  static constexpr int MISC_OFF = BAR_OFF + 13 * 8;     // tmem slot, abort flag
+  static constexpr int TOTAL = MISC_OFF + 16;
+  static constexpr int ALLOC = TOTAL + 1024;
+  static constexpr int RPC = 128 / C::NQ;               // output rows each slice CTA sums
+  static constexpr int TMEM_COLS = pow2_at_least(256 + C::RQ, 32);
+  static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+  static_assert(C::NQ == 1 || C::NQ * RPC * S::D * 4 <= 2 * 128 * C::RQ * 2, "receive buffer");
+  static_assert(256 + C::RQ <= 512 && S::D <= 128, "tensor memory budget");
+};
+
+template <class S>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qhi_map,
+                   const __grid_constant__ CUtensorMap qlo_map,
+                   const __grid_constant__ CUtensorMap kp_map,
+                   const __grid_constant__ CUtensorMap vp_map,
+                   const __grid_constant__ CUtensorMap w_map, const AttnParams p) {
+  using C = PrefillCfg<S>;
+  using L = PfSmem<S>;
+  constexpr int KT = C::KT, RQ = C::RQ, NQ = C::NQ, NG = L::NG, D = S::D, H = S::H;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;     // [2]
+  uint64_t* kv_empty = bars + 3;    // [2]
+  uint64_t* s_full = bars + 5;      // [2]
+  uint64_t* p_full = bars + 7;
+  uint64_t* pv_done = bars + 8;
+  uint64_t* acc_done = bars + 9;
+  uint64_t* zq_full = bars + 10;
+  uint64_t* w_full = bars + 11;
+  uint64_t* o_done = bars + 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  griddep_wait();            // plan and rank-space queries are ready
+  griddep_launch();
+  const int slot = blockIdx.x / (H * NQ);
+  const int h = (blockIdx.x / NQ) % H;
+  const int slice = blockIdx.x % NQ;                    // cluster rank when NQ > 1
+  if (slot >= *p.tcount) return;                        // uniform over the cluster
+  const int b = p.tile_b[slot], qt = p.tile_qt[slot];
+  const int c0 = p.cu_chunk[b], n = p.cu_chunk[b + 1] - c0;
+  const int Lb = p.seq_lens[b], P0 = Lb - n;
+  const int i0 = qt * 128;                              // first chunk row of this tile
+  const int i_last = min(n, i0 + 128) - 1;
+  const int nkt = (P0 + i_last + 1 + KT - 1) / KT;      // key tiles (causal limit)
+  const int nblk = (Lb + kBlockSize - 1) / kBlockSize;
+  const int row0 = c0 + i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(acc_done, 1);
+    mbar_init(zq_full, 4);
+    mbar_init(w_full, 1);
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if constexpr (NQ > 1) cluster_sync_all();   // peers are running before any remote store
+
+  if (warp == 0) {
+    // -------------------------------------------------------------------- copies
+    if (lane == 0) {
+      prefetch_tmap(&kp_map);
+      prefetch_tmap(&vp_map);
+      mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
+      tma_load_2d(sm, &qhi_map, h * 64, row0, q_full);
+      tma_load_2d(sm + L::Q_BYTES, &qlo_map, h * 64, row0, q_full);
+      const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+      bool ok = true;
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
+        int32_t phys[KT / kBlockSize];
+        int nload = 0;
+#pragma unroll
+        for (int jb = 0; jb < KT / kBlockSize; ++jb) {
+          const int blk = j * (KT / kBlockSize) + jb;
+          int32_t id = blk < nblk ? table[blk] : -1;
+          if (blk < nblk && (id < 0 || id >= p.num_blocks)) {
+            atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
+            id = -1;
+          }
+          phys[jb] = id;
+          nload += id >= 0;
+        }
+        mbar_arrive_expect_tx(&kv_full[s], nload * (2048 + NG * 2048));
+        uint8_t* kst = sm + L::ST_OFF + s * L::STAGE;
+        uint8_t* vst = kst + L::K_BYTES;
+#pragma unroll 1
+        for (int jb = 0; jb < KT / kBlockSize; ++jb) {
+          if (phys[jb] < 0) continue;
+          tma_load_2d(kst + jb * 2048, &kp_map, 0, (phys[jb] * H + h) * kBlockSize, &kv_full[s]);
+#pragma unroll
+          for (int g = 0; g < NG; ++g)
+            tma_load_2d(vst + (g * (KT / kBlockSize) + jb) * 2048, &vp_map, slice * RQ + g * 64,
+                        phys[jb] * kBlockSize, &kv_full[s]);
+        }
+      }
+      // the W_v rows of this slice, into stage memory once every value MMA is done
+      if (mbar_wait(acc_done, 0, abort_flag, p.dev_err)) {
+        mbar_arrive_expect_tx(w_full, L::W_BYTES);
+        uint8_t* wst = sm + L::W_OFF;
+        for (int g = 0; g < D / 64; ++g)
+          for (int kb = 0; kb < RQ / 64; ++kb)
+            tma_load_2d(wst + (g * (RQ / 64) + kb) * 8192, &w_map, h * D + g * 64,
+                        slice * RQ + kb * 64, w_full);
+        mbar_wait_drain(w_full, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------------- MMAs
+    if (lane == 0) {
+      constexpr uint32_t id_s = make_idesc_f16(128, KT, false, false);
+      constexpr uint32_t id_pv = make_idesc_f16(128, RQ, false, true);
+      constexpr uint32_t id_o = make_idesc_f16(128, D, false, true);
+      const uint32_t qa = smem_u32(sm);
+      const uint32_t pa = smem_u32(sm + L::P_OFF);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.dev_err);
+      auto issue_pv = [&](int j) {
+        const uint32_t va = smem_u32(sm + L::ST_OFF + (j & 1) * L::STAGE + L::K_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < KT / 16; ++ks) {
+          const uint64_t ad = make_sdesc(pa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024,
+                                         kSwizzle128B);
+          const uint64_t bd = make_sdesc(va + ks * 2048, (KT / kBlockSize) * 2048, 1024,
+                                         kSwizzle128B);
+          umma_f16(tmem + 256, ad, bd, id_pv, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(pv_done);
+        umma_commit(&kv_empty[j & 1]);
+      };
+      int j = 0;
+      for (; ok && j < nkt; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.dev_err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t ka = smem_u32(sm + L::ST_OFF + s * L::STAGE);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = make_sdesc(ka + kk * 32, 16, 1024, kSwizzle128B);
+          umma_f16(tmem + s * 128, make_sdesc(qa + kk * 32, 16, 1024, kSwizzle128B), bd, id_s,
+                   kk > 0 ? 1u : 0u);
+          umma_f16(tmem + s * 128, make_sdesc(qa + L::Q_BYTES + kk * 32, 16, 1024, kSwizzle128B),
+                   bd, id_s, 1u);
+        }
+        umma_commit(&s_full[s]);
+        if (j > 0) {
+          if (!mbar_wait(p_full, (j - 1) & 1, abort_flag, p.dev_err)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(j - 1);
+        }
+      }
+      if (ok && mbar_wait(p_full, (nkt - 1) & 1, abort_flag, p.dev_err)) {
+        tc_fence_after();
+        issue_pv(nkt - 1);
+      }
+      umma_commit(acc_done);
+      // up-projection of this slice: O = (z_hi + z_lo) W_v[slice rows, h*d:(h+1)*d]
+      if (mbar_wait(zq_full, 0, abort_flag, p.dev_err) && mbar_wait(w_full, 0, abort_flag, p.dev_err)) {
+        tc_fence_after();
+        const uint32_t zh = smem_u32(sm + L::ZH_OFF), zl = smem_u32(sm + L::ZL_OFF);
+        const uint32_t wa = smem_u32(sm + L::W_OFF);
+#pragma unroll 1
+        for (int ks = 0; ks < RQ / 16; ++ks) {
+          const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+          const uint64_t bd = make_sdesc(wa + ks * 2048, (RQ / 64) * 8192, 1024, kSwizzle128B);
+          umma_f16(tmem, make_sdesc(zh + koff, 16, 1024, kSwizzle128B), bd, id_o, ks > 0 ? 1u : 0u);
+          umma_f16(tmem, make_sdesc(zl + koff, 16, 1024, kSwizzle128B), bd, id_o, 1u);
+        }
+      }
+      umma_commit(o_done);
+      mbar_wait_drain(o_done, 0);
+    }
+  } else {
+    // ----------------------------------------------- softmax (one thread per query row)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                  // query row within the tile
+    const int ci = i0 + r;                              // chunk row
+    const bool row_ok = ci < n;
+    const int pos = P0 + ci;                            // keys 0 .. pos are attended
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    uint8_t* pbuf = sm + L::P_OFF;
+    for (int j = 0; j < nkt; ++j) {
+      const int s = j & 1;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag, p.dev_err));
+      tc_fence_after();
+      const int lim = row_ok ? pos - j * KT : -1;       // columns 0 .. lim are valid
+      float mx = -INFINITY;
+      if (ok) {
+#pragma unroll 1
+        for (int c0c = 0; c0c < KT; c0c += 16) {
+          float v[16];
+          tmem_ld16(tl + s * 128 + c0c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (c0c + e <= lim) mx = fmaxf(mx, v[e]);
+        }
+      }
+      const float m_new = (mx > m_run + kPfRescale) ? mx : m_run;
+      const float alpha = (m_new == m_run) ? 1.f : exp2f(m_run - m_new);
+      uint32_t packed[KT / 2];
+      float rsum = 0.f;
+      if (ok) {
+#pragma unroll
+        for (int c0c = 0; c0c < KT; c0c += 16) {
+          float v[16];
+          tmem_ld16(tl + s * 128 + c0c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float p0 = (c0c + e <= lim) ? exp2f(v[e] - m_new) : 0.f;
+            const float p1 = (c0c + e + 1 <= lim) ? exp2f(v[e + 1] - m_new) : 0.f;
+            const __half2 hp = __floats2half2_rn(p0, p1);
+            const float2 back = __half22float2(hp);
+            rsum += back.x + back.y;
+            packed[(c0c + e) / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+          }
+        }
+      }
+      // the previous tile's value MMA must be done before P is overwritten / Z rescaled
+      if (j > 0) ok = mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.dev_err) && ok;
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      // tcgen05.ld / st are warp-collective: the whole warp rescales when any lane needs it
+      // (lanes whose max did not move multiply by 1)
+      if (__any_sync(0xffffffffu, ok && alpha != 1.f && j > 0)) {
+#pragma unroll 1
+        for (int c = 0; c < RQ; c += 16) {
+          float v[16];
+          tmem_ld16(tl + 256 + c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= alpha;
+          tmem_st16(tl + 256 + c, v);
+        }
+        tmem_wait_st();
+      }
+      // P row r, K-major with 128-byte swizzle: 16-byte chunk c of the row sits at c ^ (r % 8)
+#pragma unroll
+      for (int ch = 0; ch < KT / 8; ++ch) {
+        const int kb = ch >> 3, cc = ch & 7;
+        *reinterpret_cast<uint4*>(pbuf + kb * 16384 + r * 128 + ((cc ^ (r & 7)) << 4)) =
+            make_uint4(packed[ch * 4], packed[ch * 4 + 1], packed[ch * 4 + 2], packed[ch * 4 + 3]);
+      }
+      l_run = l_run * alpha + rsum;
+      m_run = m_new;
+      if (j * KT + KT > Lb) {
+        // tokens past the end of the request: zero their value rows so that whatever the
+        // slots hold (or stale bytes of skipped pages) never meet a zero weight as 0 * NaN
+        ok = mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.dev_err) && ok;
+        uint8_t* vst = sm + L::ST_OFF + s * L::STAGE + L::K_BYTES;
+        const int first = Lb - j * KT > 0 ? Lb - j * KT : 0;
+        const int nrow = KT - first;
+        for (int idx = threadIdx.x - 64; idx < nrow * NG * 8; idx += 128) {
+          const int tok = first + idx / (NG * 8);
+          const int rem = idx % (NG * 8);
+          const int g = rem >> 3, ch = rem & 7;
+          *reinterpret_cast<uint4*>(vst + (g * (KT / kBlockSize) + tok / kBlockSize) * 2048 +
+                                    (tok % kBlockSize) * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    // --------------------------------------------- normalise z, split into fp16 hi + lo
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag, p.dev_err));
+    tc_fence_after();
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    uint8_t* zh = sm + L::ZH_OFF;
+    uint8_t* zl = sm + L::ZL_OFF;
+#pragma unroll 1
+    for (int c = 0; c < RQ; c += 16) {
+      float v[16];
+      if (ok) {
+        tmem_ld16(tl + 256 + c, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+      }
+      uint32_t hw[8], lw[8];
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        const float z0 = v[e] * inv, z1 = v[e + 1] * inv;
+        const __half2 hi = __floats2half2_rn(z0, z1);
+        const float2 hb = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(z0 - hb.x, z1 - hb.y);
+        hw[e / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+        lw[e / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int ch = (c + half * 8) / 8;                 // 16-byte chunk index in the row
+        const int kb = ch >> 3, cc = ch & 7;
+        const int off = kb * 16384 + r * 128 + ((cc ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(zh + off) =
+            make_uint4(hw[half * 4], hw[half * 4 + 1], hw[half * 4 + 2], hw[half * 4 + 3]);
+        *reinterpret_cast<uint4*>(zl + off) =
+            make_uint4(lw[half * 4], lw[half * 4 + 1], lw[half * 4 + 2], lw[half * 4 + 3]);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(zq_full);
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------------- outputs
+  const bool have_o = __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag, p.dev_err));
+  tc_fence_after();
+  __half* out = static_cast<__half*>(p.out);
+  if constexpr (NQ == 1) {
+    if (warp >= 2) {
+      const int r = (warp & 3) * 32 + lane;
+      const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+      if (have_o) {   // warp-uniform: every lane loads, only rows of the chunk are stored
+        __half* dst = out + (static_cast<size_t>(row0 + r) * H + h) * D;
+        const bool store = i0 + r < n;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 16) {
+          float v[16];
+          tmem_ld16(tl + c, v);
+          tmem_wait_ld();
+          uint32_t w8[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const __half2 hv = __floats2half2_rn(v[e], v[e + 1]);
+            w8[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          if (store) {
+            *reinterpret_cast<uint4*>(dst + c) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+            *reinterpret_cast<uint4*>(dst + c + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          }
+        }
+      }
+    }
+  } else {
+    constexpr int RPC = L::RPC;
+    cluster_sync_all();                 // every slice is done reading its z hi / lo
+    float* recv = reinterpret_cast<float*>(sm + L::ZH_OFF);   // [NQ][RPC][D]
+    if (warp >= 2) {
+      const int r = (warp & 3) * 32 + lane;
+      const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+      const uint32_t dst = map_to_rank(smem_u32(recv), static_cast<uint32_t>(r / RPC)) +
+                           ((slice * RPC + r % RPC) * D) * 4;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 16) {
+        float v[16];
+        if (have_o) {
+          tmem_ld16(tl + c, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) st_cluster_v4(dst + (c + e) * 4, v[e], v[e + 1], v[e + 2], v[e + 3]);
+      }
+    }
+    cluster_sync_all();
+    for (int idx = threadIdx.x; idx < RPC * D / 2; idx += kPfThreads) {
+      const int rr = idx / (D / 2), d2 = (idx % (D / 2)) * 2;
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int s = 0; s < NQ; ++s) {
+        a0 += recv[(s * RPC + rr) * D + d2];
+        a1 += recv[(s * RPC + rr) * D + d2 + 1];
+      }
+      const int r = slice * RPC + rr;
+      if (i0 + r < n)
+        *reinterpret_cast<__half2*>(out + (static_cast<size_t>(row0 + r) * H + h) * D + d2) =
+            __floats2half2_rn(a0, a1);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------------------- launches
+template <class S>
+cudaError_t prepare_prefill() {
+  return cudaFuncSetAttribute(prefill_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PfSmem<S>::ALLOC);
+}
+
+template <class S>
+cudaError_t launch_prefill(const CUtensorMap& qhi, const CUtensorMap& qlo, const CUtensorMap& kp,
+                           const CUtensorMap& vp, const CUtensorMap& w, const AttnParams& p,
+                           int max_tiles, cudaStream_t stream, bool pdl) {
+  constexpr int NQ = PrefillCfg<S>::NQ;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(max_tiles * S::H * NQ);
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = PfSmem<S>::ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = NQ;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<S>, qhi, qlo, kp, vp, w, p);
+}
+
+template cudaError_t prepare_prefill<ShapeMain>();
+template cudaError_t prepare_prefill<ShapeTiny>();
+template cudaError_t launch_prefill<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
+                                               const CUtensorMap&, const CUtensorMap&,
+                                               const CUtensorMap&, const AttnParams&, int,
+                                               cudaStream_t, bool);
+template cudaError_t launch_prefill<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
+                                               const CUtensorMap&, const CUtensorMap&,
+                                               const CUtensorMap&, const AttnParams&, int,
+                                               cudaStream_t, bool);
+
+}  // namespace rcp

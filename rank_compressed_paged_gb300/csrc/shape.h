@@ -45,9 +45,24 @@ struct UpprojCfg {
   static constexpr int STAGES = KB_PER_CTA < 4 ? KB_PER_CTA : 4;   // pipeline depth needed
 };
 
+// Chunked prefill: 128 query rows x 128 keys per tile; the value rank is cut into slices
+// of at most 256 (one CTA each, clustered); key rank padded to 64 (one 128-byte row).
+template <class S>
+struct PrefillCfg {
+  static constexpr int QT = 128, KT = 128;
+  static constexpr int RQ = S::R >= 256 ? 256 : S::R;
+  static constexpr int NQ = S::R / RQ;
+  static constexpr int RKP = 64;
+  static_assert(S::R % RQ == 0 && RQ % 64 == 0 && S::RK <= 64 && S::D % 64 == 0, "prefill shape");
+};
+
+// Upper bound on 128-row prefill query tiles for nq query rows (each request with rows
+// adds at most one partial tile, and at most nq requests have rows).
+inline int64_t prefill_max_tiles(int64_t nq) { return (nq + 127) / 128 + nq; }
+
 // Workspace carve-up for nq query rows (all offsets 256-byte aligned).
 struct WsLayout {
-  size_t cum, qlen, qrow, qt, rec, zhi, zlo, total;
+  size_t cum, qlen, qrow, qt, rec, zhi, zlo, tile_b, tile_qt, tcount, total;
 };
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 template <class S>
@@ -57,10 +72,15 @@ inline WsLayout ws_layout(int64_t nq) {
   w.cum = o;  o = align256(o + sizeof(int64_t) * (nq + 1));
   w.qlen = o; o = align256(o + sizeof(int32_t) * nq);
   w.qrow = o; o = align256(o + sizeof(int32_t) * nq);
-  w.qt = o;   o = align256(o + sizeof(float) * nq * S::H * S::RK);
+  // rank-space queries: fp32 [nq][H][r_k] (decode) or fp16 hi + lo [nq][H][64] (prefill)
+  const size_t qt_row = static_cast<size_t>(S::H) * (S::RK > 64 ? S::RK : 64) * 4;
+  w.qt = o;   o = align256(o + qt_row * nq);
   w.rec = o;  o = align256(o + sizeof(float) * (nq + kMaxParts) * static_cast<size_t>(S::REC));
   w.zhi = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
   w.zlo = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
+  w.tile_b = o;  o = align256(o + sizeof(int32_t) * prefill_max_tiles(nq));
+  w.tile_qt = o; o = align256(o + sizeof(int32_t) * prefill_max_tiles(nq));
+  w.tcount = o;  o = align256(o + sizeof(int32_t));
   w.total = o;
   return w;
 }
@@ -84,6 +104,12 @@ struct AttnParams {
   float* rec;                 // [(nq + parts)][REC] split partials
   void* zhi;                  // [nq][H][R] fp16 high part of the merged weighted sums z
   void* zlo;                  // [nq][H][R] fp16 low part: z - fp16(z)
+  // prefill only (nullptr for decode)
+  int32_t* tile_b;            // [max tiles] request of each 128-row query tile
+  int32_t* tile_qt;           // [max tiles] tile index within its request
+  int32_t* tcount;            // [1] number of query tiles
+  void* qhi;                  // [nq][H][64] fp16 rank-space queries (scaled), zero past r_k
+  void* qlo;                  // [nq][H][64] fp16 remainder q~ - qhi
   int64_t num_blocks;
   int32_t bt_stride;          // max_blocks_per_seq
   int32_t batch;

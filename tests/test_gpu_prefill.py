@@ -38,3 +38,18 @@ def test_main_prefill_small():
     inp = wl.make_prefill_inputs(MAIN, [100, 256], [48, 64], seed=42, fill=np.nan)
     out, ref = _run(inp)
     assert_close(out, ref, what="main prefill")
+
+
+def test_main_prefill_multi_tile_chunks():
+    """Chunks longer than one 128-row tile, priors off block boundaries, a zero chunk."""
+    inp = wl.make_prefill_inputs(MAIN, [300, 0, 17, 40], [200, 130, 0, 129], seed=43,
+                                 fill=np.nan)
+    out, ref = _run(inp)
+    assert_close(out, ref, what="main prefill multi-tile")
+
+
+def test_prefill_is_deterministic():
+    inp = wl.make_prefill_inputs(MAIN, [64, 250], [100, 37], seed=44)
+    a, _ = _run(inp)
+    b, _ = _run(inp)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
