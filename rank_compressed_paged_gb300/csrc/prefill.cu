@@ -52,8 +52,8 @@ struct PfSmem {
   static constexpr int W_BYTES = C::RQ * S::D * 2;
   static constexpr int END = (P_OFF + P_BYTES > W_OFF + W_BYTES) ? P_OFF + P_BYTES
                                                                    : W_OFF + W_BYTES;
-  static constexpr int BAR_OFF = END;                   // 13 mbarriers
-  static constexpr int MISC_OFF = BAR_OFF + 13 * 8;     // tmem slot, abort flag
+  static constexpr int BAR_OFF = END;                   // 15 mbarriers
+  static constexpr int MISC_OFF = BAR_OFF + 15 * 8;     // tmem slot, abort flag
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr int RPC = 128 / C::NQ;               // output rows each slice CTA sums
@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* zq_full = bars + 10;
   uint64_t* w_full = bars + 11;
   uint64_t* o_done = bars + 12;
+  uint64_t* v_full = bars + 13;     // [2]; kv_full[s] then tracks only the key half
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&kv_full[s], 1);
+      mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
       mbar_init(&s_full[s], 1);
     }
@@ -141,34 +143,48 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tma_load_2d(sm, &qhi_map, h * 64, row0, q_full);
       tma_load_2d(sm + L::Q_BYTES, &qlo_map, h * 64, row0, q_full);
       const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-      bool ok = true;
-      for (int j = 0; j < nkt && ok; ++j) {
+      constexpr int BPT = KT / kBlockSize;                // pages per key tile
+      // block ids of the next tile are fetched one tile ahead, off the critical path
+      int32_t nxt[BPT];
+#pragma unroll
+      for (int jb = 0; jb < BPT; ++jb) nxt[jb] = jb < nblk ? table[jb] : -1;
+      for (int j = 0; j < nkt; ++j) {
         const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
-        int32_t phys[KT / kBlockSize];
+        int32_t phys[BPT];
         int nload = 0;
 #pragma unroll
-        for (int jb = 0; jb < KT / kBlockSize; ++jb) {
-          const int blk = j * (KT / kBlockSize) + jb;
-          int32_t id = blk < nblk ? table[blk] : -1;
+        for (int jb = 0; jb < BPT; ++jb) {
+          const int blk = j * BPT + jb;
+          int32_t id = nxt[jb];
           if (blk < nblk && (id < 0 || id >= p.num_blocks)) {
             atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
             id = -1;
           }
-          phys[jb] = id;
-          nload += id >= 0;
+          phys[jb] = blk < nblk ? id : -1;
+          nload += phys[jb] >= 0;
         }
-        mbar_arrive_expect_tx(&kv_full[s], nload * (2048 + NG * 2048));
+#pragma unroll
+        for (int jb = 0; jb < BPT; ++jb) {
+          const int blk = (j + 1) * BPT + jb;
+          nxt[jb] = blk < nblk ? table[blk] : -1;
+        }
+        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
         uint8_t* kst = sm + L::ST_OFF + s * L::STAGE;
         uint8_t* vst = kst + L::K_BYTES;
+        // keys first on their own barrier (the score MMA needs only them), then values
+        mbar_arrive_expect_tx(&kv_full[s], nload * 2048);
 #pragma unroll 1
-        for (int jb = 0; jb < KT / kBlockSize; ++jb) {
+        for (int jb = 0; jb < BPT; ++jb)
+          if (phys[jb] >= 0)
+            tma_load_2d(kst + jb * 2048, &kp_map, 0, (phys[jb] * H + h) * kBlockSize, &kv_full[s]);
+        mbar_arrive_expect_tx(&v_full[s], nload * NG * 2048);
+#pragma unroll 1
+        for (int jb = 0; jb < BPT; ++jb) {
           if (phys[jb] < 0) continue;
-          tma_load_2d(kst + jb * 2048, &kp_map, 0, (phys[jb] * H + h) * kBlockSize, &kv_full[s]);
 #pragma unroll
           for (int g = 0; g < NG; ++g)
-            tma_load_2d(vst + (g * (KT / kBlockSize) + jb) * 2048, &vp_map, slice * RQ + g * 64,
-                        phys[jb] * kBlockSize, &kv_full[s]);
+            tma_load_2d(vst + (g * BPT + jb) * 2048, &vp_map, slice * RQ + g * 64,
+                        phys[jb] * kBlockSize, &v_full[s]);
         }
       }
       // the W_v rows of this slice, into stage memory once every value MMA is done
@@ -192,6 +208,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint32_t pa = smem_u32(sm + L::P_OFF);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.dev_err);
       auto issue_pv = [&](int j) {
+        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag, p.dev_err)) return false;
+        tc_fence_after();
         const uint32_t va = smem_u32(sm + L::ST_OFF + (j & 1) * L::STAGE + L::K_BYTES);
 #pragma unroll
         for (int ks = 0; ks < KT / 16; ++ks) {
@@ -203,6 +221,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         umma_commit(pv_done);
         umma_commit(&kv_empty[j & 1]);
+        return true;
       };
       int j = 0;
       for (; ok && j < nkt; ++j) {
@@ -222,7 +241,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (j > 0) {
           if (!mbar_wait(p_full, (j - 1) & 1, abort_flag, p.dev_err)) { ok = false; break; }
           tc_fence_after();
-          issue_pv(j - 1);
+          if (!issue_pv(j - 1)) { ok = false; break; }
         }
       }
       if (ok && mbar_wait(p_full, (nkt - 1) & 1, abort_flag, p.dev_err)) {
@@ -261,37 +280,42 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       bool ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag, p.dev_err));
       tc_fence_after();
       const int lim = row_ok ? pos - j * KT : -1;       // columns 0 .. lim are valid
+      // the whole 128-column score row: eight loads in flight, one wait
+      float sv[KT];
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < KT; c += 16)
+          tmem_ld16(tl + s * 128 + c, *reinterpret_cast<float(*)[16]>(&sv[c]));
+        tmem_wait_ld();
+      }
+      const bool full_tile = __all_sync(0xffffffffu, lim >= KT - 1);   // below the diagonal
       float mx = -INFINITY;
       if (ok) {
-#pragma unroll 1
-        for (int c0c = 0; c0c < KT; c0c += 16) {
-          float v[16];
-          tmem_ld16(tl + s * 128 + c0c, v);
-          tmem_wait_ld();
+        if (full_tile) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            if (c0c + e <= lim) mx = fmaxf(mx, v[e]);
+          for (int c = 0; c < KT; ++c) mx = fmaxf(mx, sv[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < KT; ++c) mx = fmaxf(mx, c <= lim ? sv[c] : -INFINITY);
         }
       }
       const float m_new = (mx > m_run + kPfRescale) ? mx : m_run;
       const float alpha = (m_new == m_run) ? 1.f : exp2f(m_run - m_new);
       uint32_t packed[KT / 2];
       float rsum = 0.f;
-      if (ok) {
+      {
+        const float msub = (m_new == -INFINITY) ? 0.f : m_new;   // rows with no valid key
 #pragma unroll
-        for (int c0c = 0; c0c < KT; c0c += 16) {
-          float v[16];
-          tmem_ld16(tl + s * 128 + c0c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const float p0 = (c0c + e <= lim) ? exp2f(v[e] - m_new) : 0.f;
-            const float p1 = (c0c + e + 1 <= lim) ? exp2f(v[e + 1] - m_new) : 0.f;
-            const __half2 hp = __floats2half2_rn(p0, p1);
-            const float2 back = __half22float2(hp);
-            rsum += back.x + back.y;
-            packed[(c0c + e) / 2] = *reinterpret_cast<const uint32_t*>(&hp);
+        for (int c = 0; c < KT; c += 2) {
+          float p0 = exp2f(sv[c] - msub), p1 = exp2f(sv[c + 1] - msub);
+          if (!full_tile || !ok) {
+            p0 = (ok && c <= lim) ? p0 : 0.f;
+            p1 = (ok && c + 1 <= lim) ? p1 : 0.f;
           }
+          const __half2 hp = __floats2half2_rn(p0, p1);
+          const float2 back = __half22float2(hp);
+          rsum += back.x + back.y;
+          packed[c / 2] = *reinterpret_cast<const uint32_t*>(&hp);
         }
       }
       // the previous tile's value MMA must be done before P is overwritten / Z rescaled
@@ -302,13 +326,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // (lanes whose max did not move multiply by 1)
       if (__any_sync(0xffffffffu, ok && alpha != 1.f && j > 0)) {
 #pragma unroll 1
-        for (int c = 0; c < RQ; c += 16) {
-          float v[16];
+        for (int c = 0; c < RQ; c += 32) {
+          float v[16], w[16];
           tmem_ld16(tl + 256 + c, v);
+          tmem_ld16(tl + 256 + c + 16, w);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] *= alpha;
+          for (int e = 0; e < 16; ++e) {
+            v[e] *= alpha;
+            w[e] *= alpha;
+          }
           tmem_st16(tl + 256 + c, v);
+          tmem_st16(tl + 256 + c + 16, w);
         }
         tmem_wait_st();
       }
@@ -324,7 +353,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (j * KT + KT > Lb) {
         // tokens past the end of the request: zero their value rows so that whatever the
         // slots hold (or stale bytes of skipped pages) never meet a zero weight as 0 * NaN
-        ok = mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.dev_err) && ok;
+        ok = mbar_wait(&v_full[s], (j >> 1) & 1, abort_flag, p.dev_err) && ok;
         uint8_t* vst = sm + L::ST_OFF + s * L::STAGE + L::K_BYTES;
         const int first = Lb - j * KT > 0 ? Lb - j * KT : 0;
         const int nrow = KT - first;
@@ -348,18 +377,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint8_t* zh = sm + L::ZH_OFF;
     uint8_t* zl = sm + L::ZL_OFF;
 #pragma unroll 1
-    for (int c = 0; c < RQ; c += 16) {
-      float v[16];
+    for (int c = 0; c < RQ; c += 32) {
+      float v[32];
       if (ok) {
-        tmem_ld16(tl + 256 + c, v);
+        tmem_ld16(tl + 256 + c, *reinterpret_cast<float(*)[16]>(&v[0]));
+        tmem_ld16(tl + 256 + c + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+        for (int e = 0; e < 32; ++e) v[e] = 0.f;
       }
-      uint32_t hw[8], lw[8];
+      uint32_t hw[16], lw[16];
 #pragma unroll
-      for (int e = 0; e < 16; e += 2) {
+      for (int e = 0; e < 32; e += 2) {
         const float z0 = v[e] * inv, z1 = v[e + 1] * inv;
         const __half2 hi = __floats2half2_rn(z0, z1);
         const float2 hb = __half22float2(hi);
@@ -368,14 +398,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         lw[e / 2] = *reinterpret_cast<const uint32_t*>(&lo);
       }
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int ch = (c + half * 8) / 8;                 // 16-byte chunk index in the row
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int ch = (c + q4 * 8) / 8;                   // 16-byte chunk index in the row
         const int kb = ch >> 3, cc = ch & 7;
         const int off = kb * 16384 + r * 128 + ((cc ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(zh + off) =
-            make_uint4(hw[half * 4], hw[half * 4 + 1], hw[half * 4 + 2], hw[half * 4 + 3]);
+            make_uint4(hw[q4 * 4], hw[q4 * 4 + 1], hw[q4 * 4 + 2], hw[q4 * 4 + 3]);
         *reinterpret_cast<uint4*>(zl + off) =
-            make_uint4(lw[half * 4], lw[half * 4 + 1], lw[half * 4 + 2], lw[half * 4 + 3]);
+            make_uint4(lw[q4 * 4], lw[q4 * 4 + 1], lw[q4 * 4 + 2], lw[q4 * 4 + 3]);
       }
     }
     fence_proxy_async_smem();
