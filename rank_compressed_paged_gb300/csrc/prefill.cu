@@ -17,8 +17,10 @@
 // W_v[:, h*d:(h+1)*d] (tcgen05 again); the slices of one (request, head, tile) form a
 // thread-block cluster and sum their partial outputs through distributed shared memory.
 //
-// Warps: 0 issues the tensor copies, 1 issues the MMAs (and owns TMEM), 2-5 run the
-// softmax and the epilogue (warp w serves TMEM lanes 32*(w%4) .. +31).
+// Warps: 0 copies queries and key tiles, 6 copies value tiles and the W_v slice (two
+// independent streams: a key stage is freed by its score MMA, a value stage by its value
+// MMA), 1 issues the MMAs (and owns TMEM), 2-5 run the softmax and the epilogue (warp w
+// serves TMEM lanes 32*(w%4) .. +31).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -32,7 +34,7 @@
 
 namespace rcp {
 
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 224;   // 0 key copies, 1 MMAs, 2-5 softmax, 6 value copies
 constexpr float kPfRescale = 8.f;   // log2 units: weights stay below 2^8 between rescales
 
 template <class S>
@@ -52,8 +54,8 @@ struct PfSmem {
   static constexpr int W_BYTES = C::RQ * S::D * 2;
   static constexpr int END = (P_OFF + P_BYTES > W_OFF + W_BYTES) ? P_OFF + P_BYTES
                                                                    : W_OFF + W_BYTES;
-  static constexpr int BAR_OFF = END;                   // 15 mbarriers
-  static constexpr int MISC_OFF = BAR_OFF + 15 * 8;     // tmem slot, abort flag
+  static constexpr int BAR_OFF = END;                   // 17 mbarriers
+  static constexpr int MISC_OFF = BAR_OFF + 17 * 8;     // tmem slot, abort flag
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr int RPC = 128 / C::NQ;               // output rows each slice CTA sums
@@ -78,16 +80,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;     // [2]
-  uint64_t* kv_empty = bars + 3;    // [2]
-  uint64_t* s_full = bars + 5;      // [2]
-  uint64_t* p_full = bars + 7;
-  uint64_t* pv_done = bars + 8;
-  uint64_t* acc_done = bars + 9;
-  uint64_t* zq_full = bars + 10;
-  uint64_t* w_full = bars + 11;
-  uint64_t* o_done = bars + 12;
-  uint64_t* v_full = bars + 13;     // [2]; kv_full[s] then tracks only the key half
+  uint64_t* k_full = bars + 1;      // [2] key half of a stage landed
+  uint64_t* v_full = bars + 3;      // [2] value half of a stage landed
+  uint64_t* k_empty = bars + 5;     // [2] score MMA of the stage's tile done
+  uint64_t* v_empty = bars + 7;     // [2] value MMA of the stage's tile done
+  uint64_t* s_full = bars + 9;      // [2] scores of a tile in TMEM
+  uint64_t* p_full = bars + 11;     // softmax weights written (4 warps)
+  uint64_t* pv_done = bars + 12;
+  uint64_t* acc_done = bars + 13;
+  uint64_t* zq_full = bars + 14;
+  uint64_t* w_full = bars + 15;
+  uint64_t* o_done = bars + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -110,9 +113,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
     }
     mbar_init(p_full, 4);
@@ -134,14 +138,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tmem = *tmem_slot;
   if constexpr (NQ > 1) cluster_sync_all();   // peers are running before any remote store
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
     // -------------------------------------------------------------------- copies
     if (lane == 0) {
-      prefetch_tmap(&kp_map);
-      prefetch_tmap(&vp_map);
-      mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
-      tma_load_2d(sm, &qhi_map, h * 64, row0, q_full);
-      tma_load_2d(sm + L::Q_BYTES, &qlo_map, h * 64, row0, q_full);
+      const bool keys = warp == 0;
+      if (keys) {
+        prefetch_tmap(&kp_map);
+        mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
+        tma_load_2d(sm, &qhi_map, h * 64, row0, q_full);
+        tma_load_2d(sm + L::Q_BYTES, &qlo_map, h * 64, row0, q_full);
+      } else {
+        prefetch_tmap(&vp_map);
+      }
       const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
       constexpr int BPT = KT / kBlockSize;                // pages per key tile
       // block ids of the next tile are fetched one tile ahead, off the critical path
@@ -157,7 +165,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const int blk = j * BPT + jb;
           int32_t id = nxt[jb];
           if (blk < nblk && (id < 0 || id >= p.num_blocks)) {
-            atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
+            if (keys) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
             id = -1;
           }
           phys[jb] = blk < nblk ? id : -1;
@@ -168,27 +176,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const int blk = (j + 1) * BPT + jb;
           nxt[jb] = blk < nblk ? table[blk] : -1;
         }
-        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
         uint8_t* kst = sm + L::ST_OFF + s * L::STAGE;
         uint8_t* vst = kst + L::K_BYTES;
-        // keys first on their own barrier (the score MMA needs only them), then values
-        mbar_arrive_expect_tx(&kv_full[s], nload * 2048);
+        if (keys) {
+          if (j >= 2 && !mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
+          mbar_arrive_expect_tx(&k_full[s], nload * 2048);
 #pragma unroll 1
-        for (int jb = 0; jb < BPT; ++jb)
-          if (phys[jb] >= 0)
-            tma_load_2d(kst + jb * 2048, &kp_map, 0, (phys[jb] * H + h) * kBlockSize, &kv_full[s]);
-        mbar_arrive_expect_tx(&v_full[s], nload * NG * 2048);
+          for (int jb = 0; jb < BPT; ++jb)
+            if (phys[jb] >= 0)
+              tma_load_2d(kst + jb * 2048, &kp_map, 0, (phys[jb] * H + h) * kBlockSize, &k_full[s]);
+        } else {
+          if (j >= 2 && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
+          mbar_arrive_expect_tx(&v_full[s], nload * NG * 2048);
 #pragma unroll 1
-        for (int jb = 0; jb < BPT; ++jb) {
-          if (phys[jb] < 0) continue;
+          for (int jb = 0; jb < BPT; ++jb) {
+            if (phys[jb] < 0) continue;
 #pragma unroll
-          for (int g = 0; g < NG; ++g)
-            tma_load_2d(vst + (g * BPT + jb) * 2048, &vp_map, slice * RQ + g * 64,
-                        phys[jb] * kBlockSize, &v_full[s]);
+            for (int g = 0; g < NG; ++g)
+              tma_load_2d(vst + (g * BPT + jb) * 2048, &vp_map, slice * RQ + g * 64,
+                          phys[jb] * kBlockSize, &v_full[s]);
+          }
         }
       }
       // the W_v rows of this slice, into stage memory once every value MMA is done
-      if (mbar_wait(acc_done, 0, abort_flag, p.dev_err)) {
+      if (!keys && mbar_wait(acc_done, 0, abort_flag, p.dev_err)) {
         mbar_arrive_expect_tx(w_full, L::W_BYTES);
         uint8_t* wst = sm + L::W_OFF;
         for (int g = 0; g < D / 64; ++g)
@@ -200,6 +211,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------------- MMAs
+    // Issues whichever MMA is ready (non-blocking probes): the score MMA of tile js once
+    // its keys landed and the softmax of tile js-2 released that S buffer, the value MMA
+    // of tile jp once its weights are written and its values landed.  The tensor pipe
+    // runs them in order, so S(j+1) overlaps the softmax of tile j and PV(j) overlaps
+    // the softmax of tile j+1.
     if (lane == 0) {
       constexpr uint32_t id_s = make_idesc_f16(128, KT, false, false);
       constexpr uint32_t id_pv = make_idesc_f16(128, RQ, false, true);
@@ -207,46 +223,54 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint32_t qa = smem_u32(sm);
       const uint32_t pa = smem_u32(sm + L::P_OFF);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.dev_err);
-      auto issue_pv = [&](int j) {
-        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag, p.dev_err)) return false;
-        tc_fence_after();
-        const uint32_t va = smem_u32(sm + L::ST_OFF + (j & 1) * L::STAGE + L::K_BYTES);
-#pragma unroll
-        for (int ks = 0; ks < KT / 16; ++ks) {
-          const uint64_t ad = make_sdesc(pa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024,
-                                         kSwizzle128B);
-          const uint64_t bd = make_sdesc(va + ks * 2048, (KT / kBlockSize) * 2048, 1024,
-                                         kSwizzle128B);
-          umma_f16(tmem + 256, ad, bd, id_pv, (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(pv_done);
-        umma_commit(&kv_empty[j & 1]);
-        return true;
-      };
-      int j = 0;
-      for (; ok && j < nkt; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.dev_err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t ka = smem_u32(sm + L::ST_OFF + s * L::STAGE);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = make_sdesc(ka + kk * 32, 16, 1024, kSwizzle128B);
-          umma_f16(tmem + s * 128, make_sdesc(qa + kk * 32, 16, 1024, kSwizzle128B), bd, id_s,
-                   kk > 0 ? 1u : 0u);
-          umma_f16(tmem + s * 128, make_sdesc(qa + L::Q_BYTES + kk * 32, 16, 1024, kSwizzle128B),
-                   bd, id_s, 1u);
-        }
-        umma_commit(&s_full[s]);
-        if (j > 0) {
-          if (!mbar_wait(p_full, (j - 1) & 1, abort_flag, p.dev_err)) { ok = false; break; }
+      int js = 0, jp = 0;
+      uint64_t t_idle = 0;
+      while (ok && jp < nkt) {
+        bool progress = false;
+        if (js < nkt && js <= jp + 1 && mbar_test_wait(&k_full[js & 1], (js >> 1) & 1)) {
           tc_fence_after();
-          if (!issue_pv(j - 1)) { ok = false; break; }
+          const uint32_t ka = smem_u32(sm + L::ST_OFF + (js & 1) * L::STAGE);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = make_sdesc(ka + kk * 32, 16, 1024, kSwizzle128B);
+            umma_f16(tmem + (js & 1) * 128, make_sdesc(qa + kk * 32, 16, 1024, kSwizzle128B), bd,
+                     id_s, kk > 0 ? 1u : 0u);
+            umma_f16(tmem + (js & 1) * 128,
+                     make_sdesc(qa + L::Q_BYTES + kk * 32, 16, 1024, kSwizzle128B), bd, id_s, 1u);
+          }
+          umma_commit(&s_full[js & 1]);
+          umma_commit(&k_empty[js & 1]);
+          ++js;
+          progress = true;
         }
-      }
-      if (ok && mbar_wait(p_full, (nkt - 1) & 1, abort_flag, p.dev_err)) {
-        tc_fence_after();
-        issue_pv(nkt - 1);
+        if (jp < js && mbar_test_wait(p_full, jp & 1) &&
+            mbar_test_wait(&v_full[jp & 1], (jp >> 1) & 1)) {
+          tc_fence_after();
+          const uint32_t va = smem_u32(sm + L::ST_OFF + (jp & 1) * L::STAGE + L::K_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < KT / 16; ++ks) {
+            const uint64_t ad = make_sdesc(pa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024,
+                                           kSwizzle128B);
+            const uint64_t bd = make_sdesc(va + ks * 2048, (KT / kBlockSize) * 2048, 1024,
+                                           kSwizzle128B);
+            umma_f16(tmem + 256, ad, bd, id_pv, (jp > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(pv_done);
+          umma_commit(&v_empty[jp & 1]);
+          ++jp;
+          progress = true;
+        }
+        if (progress) {
+          t_idle = 0;
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (t_idle == 0) {
+          t_idle = globaltimer_ns();
+        } else if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicOr(p.dev_err, RCP_DEVERR_TIMEOUT);
+          ok = false;
+        }
       }
       umma_commit(acc_done);
       // up-projection of this slice: O = (z_hi + z_lo) W_v[slice rows, h*d:(h+1)*d]
@@ -289,34 +313,41 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_wait_ld();
       }
       const bool full_tile = __all_sync(0xffffffffu, lim >= KT - 1);   // below the diagonal
+      // row max and row sum as 8 independent partial reductions (no 128-long chains)
       float mx = -INFINITY;
       if (ok) {
-        if (full_tile) {
+        float m8[8];
 #pragma unroll
-          for (int c = 0; c < KT; ++c) mx = fmaxf(mx, sv[c]);
-        } else {
+        for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < KT; ++c) mx = fmaxf(mx, c <= lim ? sv[c] : -INFINITY);
-        }
+        for (int c = 0; c < KT; ++c)
+          m8[c & 7] = fmaxf(m8[c & 7], (full_tile || c <= lim) ? sv[c] : -INFINITY);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx = fmaxf(mx, m8[q]);
       }
       const float m_new = (mx > m_run + kPfRescale) ? mx : m_run;
-      const float alpha = (m_new == m_run) ? 1.f : exp2f(m_run - m_new);
+      const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
       uint32_t packed[KT / 2];
       float rsum = 0.f;
       {
         const float msub = (m_new == -INFINITY) ? 0.f : m_new;   // rows with no valid key
+        float s8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s8[q] = 0.f;
+        // the row sum is taken in fp32 before the weights are rounded to fp16
 #pragma unroll
         for (int c = 0; c < KT; c += 2) {
-          float p0 = exp2f(sv[c] - msub), p1 = exp2f(sv[c + 1] - msub);
+          float p0 = fast_exp2(sv[c] - msub), p1 = fast_exp2(sv[c + 1] - msub);
           if (!full_tile || !ok) {
             p0 = (ok && c <= lim) ? p0 : 0.f;
             p1 = (ok && c + 1 <= lim) ? p1 : 0.f;
           }
+          s8[(c >> 1) & 7] += p0 + p1;
           const __half2 hp = __floats2half2_rn(p0, p1);
-          const float2 back = __half22float2(hp);
-          rsum += back.x + back.y;
           packed[c / 2] = *reinterpret_cast<const uint32_t*>(&hp);
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) rsum += s8[q];
       }
       // the previous tile's value MMA must be done before P is overwritten / Z rescaled
       if (j > 0) ok = mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.dev_err) && ok;
@@ -357,7 +388,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint8_t* vst = sm + L::ST_OFF + s * L::STAGE + L::K_BYTES;
         const int first = Lb - j * KT > 0 ? Lb - j * KT : 0;
         const int nrow = KT - first;
-        for (int idx = threadIdx.x - 64; idx < nrow * NG * 8; idx += 128) {
+        for (int idx = threadIdx.x - 64; idx < nrow * NG * 8; idx += 128) {   // warps 2-5
           const int tok = first + idx / (NG * 8);
           const int rem = idx % (NG * 8);
           const int g = rem >> 3, ch = rem & 7;
@@ -419,7 +450,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   __half* out = static_cast<__half*>(p.out);
   if constexpr (NQ == 1) {
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
       const int r = (warp & 3) * 32 + lane;
       const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
       if (have_o) {   // warp-uniform: every lane loads, only rows of the chunk are stored
@@ -447,7 +478,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     constexpr int RPC = L::RPC;
     cluster_sync_all();                 // every slice is done reading its z hi / lo
     float* recv = reinterpret_cast<float*>(sm + L::ZH_OFF);   // [NQ][RPC][D]
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
       const int r = (warp & 3) * 32 + lane;
       const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
       const uint32_t dst = map_to_rank(smem_u32(recv), static_cast<uint32_t>(r / RPC)) +
