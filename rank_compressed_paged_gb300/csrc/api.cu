@@ -208,14 +208,24 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
         !encode_2d(&qlo_map, p.qlo, hq, static_cast<uint64_t>(nq), hq * 2, 64, 128))
       return RCP_ERR_CUDA;
     const int max_tiles = static_cast<int>((nq + 127) / 128 + (batch < nq ? batch : nq));
+    const uint64_t hdq = static_cast<uint64_t>(c->cfg.num_heads) * c->cfg.head_dim;
+    CUtensorMap q_map;
+    if (!encode_2d(&q_map, q, hdq, static_cast<uint64_t>(nq), hdq * 2, 64, nq <= 256 ? 64 : 256))
+      return RCP_ERR_CUDA;
     if (c->shape == kShapeMain) {
       e = rcp::launch_plan<ShapeMain>(p, s, pdl);
+      if (e == cudaSuccess)
+        e = rcp::launch_qproj_gemm<ShapeMain>(c->tmap_uk, q_map, p.qhi, p.qlo, nq, p.qscale,
+                                              c->dev_err, s, pdl);
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
       if (e == cudaSuccess)
         e = rcp::launch_prefill<ShapeMain>(qhi_map, qlo_map, c->tmap_kp, c->tmap_v, c->tmap_wv_mn,
                                            p, max_tiles, s, pdl);
     } else {
       e = rcp::launch_plan<ShapeTiny>(p, s, pdl);
+      if (e == cudaSuccess)
+        e = rcp::launch_qproj_gemm<ShapeTiny>(c->tmap_uk, q_map, p.qhi, p.qlo, nq, p.qscale,
+                                              c->dev_err, s, pdl);
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
       if (e == cudaSuccess)
         e = rcp::launch_prefill<ShapeTiny>(qhi_map, qlo_map, c->tmap_kp, c->tmap_v, c->tmap_wv_mn,

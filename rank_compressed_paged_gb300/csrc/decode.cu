@@ -714,11 +714,11 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStre
                     dim3(kCombineThreads), 0, stream, pdl, p);
 }
 
+// The plan alone (CTA 0 of the planning kernel); the prefill path projects its queries
+// on tensor cores instead.
 template <class S>
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream, bool pdl) {
-  const int qtiles = (p.nq + kQprojTile - 1) / kQprojTile;
-  return launch_pdl(plan_qproj_kernel<S>, dim3(1 + S::H * qtiles), dim3(kPlanThreads), 0, stream,
-                    pdl, p);
+  return launch_pdl(plan_qproj_kernel<S>, dim3(1), dim3(kPlanThreads), 0, stream, pdl, p);
 }
 
 template cudaError_t launch_plan<ShapeMain>(const AttnParams&, cudaStream_t, bool);

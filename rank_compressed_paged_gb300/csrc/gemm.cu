@@ -16,6 +16,9 @@
 //   up-projection:      A = W_v[:, h*d:(h+1)*d]^T (MN-major), B = z_hi and z_lo (the
 //                       fp16 high / low parts of the merged weighted coefficient sums),
 //                       D[j][q] = o_{q,h,j}, written as fp16.
+//   query projection:   as a key job with the chunk's queries as B: D[k][q] = q~_{q,h,k},
+//                       scaled by log2(e)/sqrt(d) and stored as an fp16 (hi, lo) pair
+//                       (zero past r_k, up to 64), the prefill score MMA's A operand.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -32,7 +35,7 @@ namespace rcp {
 constexpr int kGemmThreads = 128;
 constexpr int kABytes = 128 * 64 * 2;   // one A stage: 128 rows x 64 K (or 64 K x 128 M)
 
-enum GemmMode : int { kModeAppend = 0, kModeUpproj = 1 };
+enum GemmMode : int { kModeAppend = 0, kModeUpproj = 1, kModeQproj = 2 };
 
 template <int NT, int KS, int NB, int STG>
 struct GemmSmem {
@@ -60,6 +63,10 @@ struct GemmParams {
   void* out;
   int32_t nq;
   uint32_t* dev_err;
+  // rank-space queries for chunked prefill: fp16 hi / lo [nq][H][64], scaled
+  void* qhi;
+  void* qlo;
+  float qscale;
 };
 
 // Where one CTA's job reads and writes.
@@ -104,6 +111,16 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank) {
       j.b_x = h * S::D; j.b_y = j.n0; j.b_step_x = 64;
       j.reduce = false;
     }
+  } else if constexpr (MODE == kModeQproj) {
+    const int h = blockIdx.x % S::H;
+    j.kind = 3;
+    j.m0 = h;
+    j.n0 = (blockIdx.x / S::H) * NT;
+    j.kb0 = 0;
+    j.kb1 = S::D / 64;
+    j.a_x = 0; j.a_y = h * S::RK; j.a_step_x = 64; j.a_step_y = 0;
+    j.b_x = h * S::D; j.b_y = j.n0; j.b_step_x = 64;
+    j.reduce = false;
   } else {
     constexpr int KBR = S::R / 64;
     const int h = cluster % S::H;
@@ -125,6 +142,15 @@ template <class S>
 __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j, int row, int col,
                                            float v) {
   const int n = j.n0 + col;
+  if (j.kind == 3) {
+    if (n >= p.nq || row >= 64) return;
+    const size_t at = (static_cast<size_t>(n) * S::H + j.m0) * 64 + row;
+    float q = row < S::RK ? v * p.qscale : 0.f;   // rows past r_k belong to the next head
+    const __half hi = __float2half_rn(q);
+    static_cast<__half*>(p.qhi)[at] = hi;
+    static_cast<__half*>(p.qlo)[at] = __float2half_rn(q - __half2float(hi));
+    return;
+  }
   if (j.kind == 2) {
     if (row < S::D && n < p.nq)
       static_cast<__half*>(p.out)[(static_cast<size_t>(n) * S::H + j.m0) * S::D + row] =
@@ -171,8 +197,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t rank = KS > 1 ? cluster_ctarank() : 0;
   const GemmJob j = gemm_job<S, MODE, NT, KS>(rank);
   // A key job uses the U_k map; every other job reads W_v through map_a.
-  const CUtensorMap* amap = (j.kind == 1) ? &map_a2 : &map_a;
-  const CUtensorMap* bmap = (j.kind == 1) ? &map_b2 : &map_b;
+  // key and query jobs read U_k through map_a2 and their tokens through map_b2
+  const CUtensorMap* amap = (j.kind == 1 || j.kind == 3) ? &map_a2 : &map_a;
+  const CUtensorMap* bmap = (j.kind == 1 || j.kind == 3) ? &map_b2 : &map_b;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
@@ -354,6 +381,10 @@ cudaError_t prepare_gemm() {
   if ((e = set(gemm_kernel<S, kModeAppend, 256, 1, 4>, GemmSmem<256, 1, 1, 4>::ALLOC)) !=
       cudaSuccess)
     return e;
+  if ((e = set(gemm_kernel<S, kModeQproj, 64, 1, 2>, GemmSmem<64, 1, 1, 2>::ALLOC)) != cudaSuccess)
+    return e;
+  if ((e = set(gemm_kernel<S, kModeQproj, 256, 1, 2>, GemmSmem<256, 1, 1, 2>::ALLOC)) != cudaSuccess)
+    return e;
   constexpr int KSU = UpprojCfg<S>::KS, STU = UpprojCfg<S>::STAGES;
   if ((e = set(gemm_kernel<S, kModeUpproj, UpprojCfg<S>::NT, KSU, STU>,
                GemmSmem<UpprojCfg<S>::NT, KSU, 2, STU>::ALLOC)) != cudaSuccess)
@@ -381,9 +412,30 @@ cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
     return launch_cluster(gemm_kernel<S, kModeAppend, 64, KS, 4>, tiles * (NM + NKG) * KS, KS,
                           GemmSmem<64, KS, 1, 4>::ALLOC, stream, true, w_v, u_k, v_rows, k_rows, p);
   }
+  // many tokens: 256-token tiles, no split
   const int tiles = (ap.T + 255) / 256;
   return launch_cluster(gemm_kernel<S, kModeAppend, 256, 1, 4>, tiles * (NM + S::H), 1,
                         GemmSmem<256, 1, 1, 4>::ALLOC, stream, true, w_v, u_k, v_rows, k_rows, p);
+}
+
+template <class S>
+cudaError_t launch_qproj_gemm(const CUtensorMap& u_k, const CUtensorMap& q_rows, void* qhi,
+                              void* qlo, int nq, float qscale, uint32_t* dev_err,
+                              cudaStream_t stream, bool pdl) {
+  GemmParams p{};
+  p.nq = nq;
+  p.qhi = qhi;
+  p.qlo = qlo;
+  p.qscale = qscale;
+  p.dev_err = dev_err;
+  if (nq <= 256) {
+    const int tiles = (nq + 63) / 64;
+    return launch_cluster(gemm_kernel<S, kModeQproj, 64, 1, 2>, tiles * S::H, 1,
+                          GemmSmem<64, 1, 1, 2>::ALLOC, stream, pdl, u_k, u_k, q_rows, q_rows, p);
+  }
+  const int tiles = (nq + 255) / 256;
+  return launch_cluster(gemm_kernel<S, kModeQproj, 256, 1, 2>, tiles * S::H, 1,
+                        GemmSmem<256, 1, 1, 2>::ALLOC, stream, pdl, u_k, u_k, q_rows, q_rows, p);
 }
 
 template <class S>
@@ -408,6 +460,12 @@ template cudaError_t launch_append_gemm<ShapeMain>(const CUtensorMap&, const CUt
 template cudaError_t launch_append_gemm<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
                                                    const CUtensorMap&, const CUtensorMap&,
                                                    const AppendParams&, cudaStream_t);
+template cudaError_t launch_qproj_gemm<ShapeMain>(const CUtensorMap&, const CUtensorMap&, void*,
+                                                  void*, int, float, uint32_t*, cudaStream_t,
+                                                  bool);
+template cudaError_t launch_qproj_gemm<ShapeTiny>(const CUtensorMap&, const CUtensorMap&, void*,
+                                                  void*, int, float, uint32_t*, cudaStream_t,
+                                                  bool);
 template cudaError_t launch_upproj_gemm<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
                                                    const CUtensorMap&, void*, int, uint32_t*,
                                                    cudaStream_t, bool);

@@ -29,6 +29,12 @@ template <class S>
 cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
                                const CUtensorMap& v_rows, const CUtensorMap& k_rows,
                                const AppendParams& p, cudaStream_t stream);
+// Prefill rank-space queries on tensor cores (q_rows: [nq][H*d] fp16, boxes 64 x 64 when
+// nq <= 256, else 64 x 256).
+template <class S>
+cudaError_t launch_qproj_gemm(const CUtensorMap& u_k, const CUtensorMap& q_rows, void* qhi,
+                              void* qlo, int nq, float qscale, uint32_t* dev_err,
+                              cudaStream_t stream, bool pdl);
 template <class S>
 cudaError_t launch_upproj_gemm(const CUtensorMap& w_v_mn, const CUtensorMap& z_hi,
                                const CUtensorMap& z_lo, void* out, int nq, uint32_t* dev_err,
