@@ -43,6 +43,26 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own batch of sequences (weak scaling: work per GPU is fixed)."""
+    return 1002 + rank
+
+
+def reduce_max(values, world: int, device=None):
+    """Max over ranks of per-rank timings: the slowest rank bounds the whole job."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_gbs(bytes_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_rank / (max_ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -238,7 +258,7 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = make_workload(dev, seed=1002 + rank)
+    w = make_workload(dev, seed=rank_seed(rank))
     H, d = SHAPE["num_heads"], SHAPE["head_dim"]
 
     def td(x):
@@ -324,15 +344,12 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
     # ---- aggregate over ranks (max time)
-    times = torch.tensor([step_ms, e2e_ms, kern_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    step_ms, e2e_ms, kern_ms = [float(x) for x in times.cpu()]
+    step_ms, e2e_ms, kern_ms = reduce_max([step_ms, e2e_ms, kern_ms], world, dev)
     if rank != 0:
         return
     coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"])
-    value = world * coeff_bytes / (step_ms * 1e-3) / 1e9
-    e2e_value = world * coeff_bytes / (e2e_ms * 1e-3) / 1e9
+    value = job_gbs(coeff_bytes, world, step_ms)
+    e2e_value = job_gbs(coeff_bytes, world, e2e_ms)
     peak, peak_kind = measured_peaks()
     achieved = coeff_bytes / (kern_ms * 1e-3) / 1e9
     traffic = ncu_traffic_per_launch()
