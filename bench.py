@@ -273,8 +273,7 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step():
-        cache.append_kv(nk, nv, slots)
-        cache.decode_attn(q, table, lens, out=out, workspace=ws)
+        cache.decode_step(nk, nv, slots, q, table, lens, out=out, workspace=ws)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -327,8 +326,7 @@ def run_ours(args, rank, world, local_rank):
         ds.copy_(hs, non_blocking=True)
         dt.copy_(ht, non_blocking=True)
         dl.copy_(hl, non_blocking=True)
-        cache.append_kv(dk, dv, ds)
-        cache.decode_attn(dq, dt, dl, out=out, workspace=ws)
+        cache.decode_step(dk, dv, ds, dq, dt, dl, out=out, workspace=ws)
         hout.copy_(out, non_blocking=True)
 
     for _ in range(3):

@@ -111,6 +111,18 @@ rcp_status rcp_decode_attn(rcp_cache* cache, const void* q, const int32_t* block
                            void* out, void* workspace, size_t workspace_bytes,
                            rcp_stream stream);
 
+/* One decode step: rcp_append_kv(k, v, slot_mapping, num_tokens) followed by
+ * rcp_decode_attn(q, ...), with the same arguments and results (the pages' "per-decode-step"
+ * unit: the cache write and the attention of a step).  Queued together, the query
+ * projection of the attention runs alongside the append (it reads nothing the append
+ * writes), which shortens the step.  All checks of both calls apply before anything is
+ * launched except the append's own. */
+rcp_status rcp_decode_step(rcp_cache* cache, const void* k, const void* v,
+                           const int64_t* slot_mapping, int32_t num_tokens, const void* q,
+                           const int32_t* block_table, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t batch, void* out, void* workspace,
+                           size_t workspace_bytes, rcp_stream stream);
+
 /* Chunked-prefill attention (Proxima page, "Per-prefill-chunk attention").  The chunk's
  * K/V must already be appended.  Request b owns query rows cu_chunk_lens[b] ..
  * cu_chunk_lens[b+1]-1 of q [num_query_rows][H][d]; seq_lens[b] counts prior + chunk

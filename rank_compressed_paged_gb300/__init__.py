@@ -137,6 +137,20 @@ class PagedCoeffCache:
             _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
         return out
 
+    def decode_step(self, k, v, slot_mapping, q, block_table, seq_lens, out=None, workspace=None,
+                    stream=None):
+        """append_kv(k, v, slot_mapping) then decode_attn(q, ...), queued as one step."""
+        import torch
+        B = int(q.shape[0])
+        if out is None:
+            out = torch.empty_like(q)
+        ws = self.workspace(B) if workspace is None else workspace
+        _lib.check("rcp_decode_step", self._lib.rcp_decode_step(
+            self._h, _ptr(k), _ptr(v), _ptr(slot_mapping), int(slot_mapping.shape[0]), _ptr(q),
+            _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out), _ptr(ws),
+            ws.numel() * ws.element_size(), _stream(stream)))
+        return out
+
     def prefill_attn(self, q, cu_chunk_lens, block_table, seq_lens, out=None, workspace=None,
                      stream=None):
         """q: [sum chunk][H][d] fp16; cu_chunk_lens: [B+1] int32; seq_lens include the chunk."""

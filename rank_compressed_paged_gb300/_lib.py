@@ -43,6 +43,8 @@ _SIG = {
     "rcp_workspace_size": (ctypes.c_int, [_P, _I32, ctypes.POINTER(ctypes.c_size_t)]),
     "rcp_append_kv": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P]),
     "rcp_decode_attn": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, ctypes.c_size_t, _P]),
+    "rcp_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P,
+                                       ctypes.c_size_t, _P]),
     "rcp_prefill_attn": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _I32, _P, _P,
                                         ctypes.c_size_t, _P]),
     "rcp_set_profile_events": (ctypes.c_int, [_P, _P, _P]),

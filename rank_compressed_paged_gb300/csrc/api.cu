@@ -159,7 +159,7 @@ void fill_ws(rcp::AttnParams& p, void* ws, int64_t nq) {
 rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, int32_t nq,
                          const int32_t* block_table, int32_t max_blocks_per_seq,
                          const int32_t* seq_lens, int32_t batch, void* out, void* ws,
-                         size_t ws_size, rcp_stream stream) {
+                         size_t ws_size, rcp_stream stream, bool after_own_append = false) {
   if (!c || batch < 0 || nq < 0 || max_blocks_per_seq < 1) return RCP_ERR_INVALID_ARG;
   if (nq == 0) return RCP_OK;
   if (batch == 0 && cu_chunk) return RCP_ERR_INVALID_ARG;
@@ -192,6 +192,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   if (parts > max_blocks_total) parts = max_blocks_total;
   if (parts < 1) parts = 1;
   p.parts = static_cast<int32_t>(parts);
+  p.late_wait = after_own_append ? 1 : 0;
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->cfg.head_dim)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -405,6 +406,19 @@ rcp_status rcp_append_kv(rcp_cache* c, const void* k, const void* v, const int64
           ? rcp::launch_append_gemm<ShapeMain>(c->tmap_wv_k, c->tmap_uk, vmap, kmap, p, s)
           : rcp::launch_append_gemm<ShapeTiny>(c->tmap_wv_k, c->tmap_uk, vmap, kmap, p, s);
   return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
+}
+
+rcp_status rcp_decode_step(rcp_cache* c, const void* k, const void* v, const int64_t* slot_mapping,
+                           int32_t num_tokens, const void* q, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           rcp_stream stream) {
+  if (!c || batch < 0 || num_tokens < 0 || max_blocks_per_seq < 1) return RCP_ERR_INVALID_ARG;
+  if (batch > 0 && workspace_bytes < ws_bytes(c, batch)) return RCP_ERR_WORKSPACE;
+  rcp_status st = rcp_append_kv(c, k, v, slot_mapping, num_tokens, stream);
+  if (st != RCP_OK) return st;
+  return run_attention(c, q, nullptr, batch, block_table, max_blocks_per_seq, seq_lens, batch, out,
+                       workspace, workspace_bytes, stream, num_tokens > 0);
 }
 
 rcp_status rcp_decode_attn(rcp_cache* c, const void* q, const int32_t* block_table,

@@ -41,7 +41,11 @@ constexpr int kQprojTile = 16;   // query rows per q-projection CTA
 
 template <class S>
 __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnParams p) {
-  griddep_wait();       // launched as a dependent of the caller's previous kernel
+  // Launched as a programmatic dependent of the kernel before it.  Normally that kernel
+  // may have produced q / lengths, so wait first; within a fused decode step it is the
+  // step's own append, whose output this kernel never reads, so the wait moves to the end
+  // (completion of this kernel then still implies completion of the append).
+  if (!p.late_wait) griddep_wait();
   griddep_launch();
   if (blockIdx.x == 0) {
     // ---- plan: qlen / qrow per query row, then cum = prefix sum of ceil(qlen / 16)
@@ -128,6 +132,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
       }
       if (tid == kPlanThreads - 1) *p.tcount = static_cast<int32_t>(t0);
     }
+    if (p.late_wait) griddep_wait();
     return;
   }
   // ---- q~ = U_k,h q_h for a tile of query rows and one head
@@ -182,6 +187,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
       }
     }
   }
+  if (p.late_wait) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------- decode main

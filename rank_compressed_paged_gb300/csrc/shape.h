@@ -115,6 +115,8 @@ struct AttnParams {
   int32_t batch;
   int32_t nq;
   int32_t parts;              // decode CTAs (work partitions)
+  int32_t late_wait;          // planning kernel may run alongside its predecessor (an append
+                              // of the same step that it does not read) and waits at its end
   float qscale;               // log2(e) / sqrt(d)
 };
 

@@ -130,3 +130,23 @@ def test_append_then_decode_round_trip():
                            inp.slot_mapping, 16)
     ref = orc.decode_attn(inp.q, kp, vp, inp.U_k, inp.W_v, c.block_table, c.seq_lens, 16)
     assert_close(out.cpu().numpy(), ref, what="append+decode")
+
+
+def test_decode_step_equals_append_then_decode():
+    """The fused step queues the same work: outputs and pages are bitwise identical."""
+    import torch
+    inp = wl.make_decode_inputs(MAIN, [300, 17, 1024, 0], seed=41, append=True, fill=np.nan)
+    c = inp.cache
+    a = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    a.append_kv(t(inp.new_k), t(inp.new_v), t(inp.slot_mapping))
+    oa = a.decode_attn(t(inp.q), t(c.block_table), t(c.seq_lens))
+    b = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    ob = b.decode_step(t(inp.new_k), t(inp.new_v), t(inp.slot_mapping), t(inp.q),
+                       t(c.block_table), t(c.seq_lens))
+    torch.cuda.synchronize()
+    assert a.read_device_error() == 0 and b.read_device_error() == 0
+    assert np.array_equal(oa.cpu().numpy().view(np.uint16), ob.cpu().numpy().view(np.uint16))
+    assert np.array_equal(a.k_pages.cpu().numpy().view(np.uint16),
+                          b.k_pages.cpu().numpy().view(np.uint16))
+    assert np.array_equal(a.v_pages.cpu().numpy().view(np.uint16),
+                          b.v_pages.cpu().numpy().view(np.uint16))
