@@ -100,3 +100,30 @@ def test_decode_rejects_bad_block_ids_on_device():
     ref0 = orc.decode_attn(inp.q[:1], c.k_pages, c.v_pages, inp.U_k, inp.W_v, table[:1],
                            c.seq_lens[:1], 16)
     assert_close(o[:1], ref0, what="unaffected request")
+
+
+def test_main_decode_one_long_request_spans_every_partition():
+    """A single long sequence is split over all CTAs: many partial records to merge."""
+    inp = wl.make_decode_inputs(MAIN, [0, 12000, 0], seed=26, fill=np.nan)
+    out, _ = _run_decode(inp)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0)
+    assert_close(out, _oracle(inp), what="one long request")
+
+
+def test_decode_empty_request_after_a_full_one_gives_zeros():
+    """The same workspace first holds a merged z for request 0, then request 0 is empty."""
+    import torch
+    inp = wl.make_decode_inputs(MAIN, [500, 300], seed=27)
+    c = inp.cache
+    cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    ws = cache.workspace(2)
+    o1 = cache.decode_attn(t(inp.q), t(c.block_table), t(c.seq_lens), workspace=ws)
+    lens2 = c.seq_lens.copy()
+    lens2[0] = 0
+    o2 = cache.decode_attn(t(inp.q), t(c.block_table), t(lens2), workspace=ws)
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    o1, o2 = o1.cpu().numpy(), o2.cpu().numpy()
+    assert np.any(o1[0] != 0) and np.all(o2[0] == 0)
+    ref = orc.decode_attn(inp.q, c.k_pages, c.v_pages, inp.U_k, inp.W_v, c.block_table, lens2, 16)
+    assert_close(o2, ref, what="empty after full")
