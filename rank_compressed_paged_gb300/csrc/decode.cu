@@ -613,79 +613,130 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
 // ----------------------------------------------------------------------------- combine
 constexpr int kCombineThreads = 256;
-constexpr int kCombineRows = 64;   // joint-rank rows per CTA
 
 __device__ __forceinline__ int part_of(int64_t g, int64_t T, int G) {
   // the CTA whose range [c*T/G, (c+1)*T/G) holds block g
   return static_cast<int>(((g + 1) * G + T - 1) / T - 1);
 }
 
-// One CTA per (request, 64 joint-rank rows); thread (head h, row group) keeps 8 rows of
-// z_h.  Every thread derives its head's merge weights from the records' (max, sum)
-// pairs itself (the 8 threads of a head read the same words), so there is no shared
-// state before the accumulation, which walks the records in a fixed order.
-template <class S>
+// Merges a request's partial records (one per CTA range that touched it) into
+// z_h = sum_i 2^(m_i,h - M_h) z_i,h / sum_i 2^(m_i,h - M_h) l_i,h, M_h = max_i m_i,h.
+// One CTA per (request, slice of RB joint-rank rows); the slice of a record is RB * HP
+// contiguous floats.  Every pass is parallel over records: the (max, sum) pass spreads
+// the records over thread groups, the accumulation gives each float4 of the slice NG
+// threads that walk interleaved record subsets; partials are then added in a fixed order,
+// so the result does not depend on timing.  NG = 4 serves small batches, where a request
+// is split over many CTAs and there are few requests to spread the work.
+template <class S, int NG>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnParams p) {
-  constexpr int HP = S::HP, H = S::H;
-  __shared__ float zt[H][kCombineRows + 1];
+  constexpr int HP = S::HP, H = S::H, R = S::R;
+  constexpr int F4 = kCombineThreads / NG;     // float4 per slice
+  constexpr int RB = F4 * 4 / HP;              // joint-rank rows per CTA
+  constexpr int MG = kCombineThreads / HP;     // record groups of the (max, sum) pass
+  constexpr size_t REC4 = S::REC / 4;
+  static_assert(R % RB == 0 && S::REC % 4 == 0, "combine tiling");
+  __shared__ float4 e_s4[kMaxParts * HP / 4];  // unnormalised weights e_i,h
+  __shared__ float red[MG][HP];
+  __shared__ float inv_l[HP];
+  __shared__ float4 part[NG > 1 ? NG - 1 : 1][F4];
+  __shared__ float zt[HP][RB + 1];
   griddep_wait();
   griddep_launch();
   const int b = blockIdx.x;
-  const int r0 = blockIdx.y * kCombineRows;
+  const int r0 = blockIdx.y * RB;
   const int tid = threadIdx.x;
   const int64_t c0 = p.cum[b], c1 = p.cum[b + 1];
-  __half* zh = static_cast<__half*>(p.zhi) + static_cast<size_t>(b) * H * S::R;
-  __half* zl = static_cast<__half*>(p.zlo) + static_cast<size_t>(b) * H * S::R;
-  constexpr int RPP = kCombineThreads / HP;       // rows per pass
-  constexpr int NR = kCombineRows / RPP;          // rows per thread
-  const int h = tid % HP;
-  const int rr = tid / HP;
-  if (c1 > c0 && h < H) {
-    const int64_t T = p.cum[p.nq];
-    const int G = static_cast<int>(T < p.parts ? T : p.parts);   // as in decode_main_kernel
-    const int pf = part_of(c0, T, G), pl = part_of(c1 - 1, T, G);
-    const int nrec = pl - pf + 1;
-    const float* rec0 = p.rec + static_cast<size_t>(b + pf) * S::REC;
-    const float* ml = rec0 + static_cast<size_t>(S::R) * HP + h;   // m at +0, l at +HP
+  __half* zh = static_cast<__half*>(p.zhi) + static_cast<size_t>(b) * H * R;
+  __half* zl = static_cast<__half*>(p.zlo) + static_cast<size_t>(b) * H * R;
+  if (c1 == c0) {   // empty sequence: z = 0
+    for (int i = tid; i < H * RB; i += kCombineThreads) {
+      const size_t at = static_cast<size_t>(i / RB) * R + r0 + i % RB;
+      zh[at] = __float2half_rn(0.f);
+      zl[at] = __float2half_rn(0.f);
+    }
+    return;
+  }
+  const int64_t T = p.cum[p.nq];
+  const int G = static_cast<int>(T < p.parts ? T : p.parts);   // as in decode_main_kernel
+  const int pf = part_of(c0, T, G), pl = part_of(c1 - 1, T, G);
+  const int nrec = pl - pf + 1;
+  const float* rec0 = p.rec + static_cast<size_t>(b + pf) * S::REC;
+  float* e_s = reinterpret_cast<float*>(e_s4);
+  {
+    // ---- per-head maximum, then e_i,h = 2^(m_i,h - M_h) and the sum of e_i,h l_i,h
+    const int h = tid % HP, g = tid / HP;
+    const float* ml = rec0 + static_cast<size_t>(R) * HP + h;   // m at +0, l at +HP
+    float mx = -INFINITY;
+    for (int i = g; i < nrec; i += MG) {
+      const float m = __ldcg(ml + static_cast<size_t>(i) * S::REC);
+      e_s[i * HP + h] = m;
+      mx = fmaxf(mx, m);
+    }
+    red[g][h] = mx;
+    __syncthreads();
     float M = -INFINITY;
-    for (int i = 0; i < nrec; ++i) M = fmaxf(M, ml[static_cast<size_t>(i) * S::REC]);
-    float lsum = 0.f;
-    for (int i = 0; i < nrec; ++i) {
-      const float m = ml[static_cast<size_t>(i) * S::REC];
-      if (m != -INFINITY) lsum += exp2f(m - M) * ml[static_cast<size_t>(i) * S::REC + HP];
+#pragma unroll
+    for (int gg = 0; gg < MG; ++gg) M = fmaxf(M, red[gg][h]);
+    float sum = 0.f;
+    for (int i = g; i < nrec; i += MG) {
+      const float m = e_s[i * HP + h];
+      const float e = (m == -INFINITY) ? 0.f : exp2f(m - M);
+      e_s[i * HP + h] = e;
+      sum = fmaf(e, __ldcg(ml + static_cast<size_t>(i) * S::REC + HP), sum);
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    float acc[NR];
+    __syncthreads();   // every thread has read red[] for its maximum
+    red[g][h] = sum;
+    __syncthreads();
+    if (tid < HP) {
+      float L = 0.f;
 #pragma unroll
-    for (int k = 0; k < NR; ++k) acc[k] = 0.f;
-    const float* base = rec0 + static_cast<size_t>(r0 + rr) * HP + h;
-    for (int i = 0; i < nrec; ++i) {
-      const float m = ml[static_cast<size_t>(i) * S::REC];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M) * inv;
-      const float* rp = base + static_cast<size_t>(i) * S::REC;
-      float v[NR];
-#pragma unroll
-      for (int k = 0; k < NR; ++k) v[k] = (r0 + rr + k * RPP < S::R) ? rp[k * RPP * HP] : 0.f;
-#pragma unroll
-      for (int k = 0; k < NR; ++k) acc[k] = fmaf(w, v[k], acc[k]);
+      for (int gg = 0; gg < MG; ++gg) L += red[gg][tid];
+      inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
     }
+  }
+  // ---- accumulate this thread's float4 of the slice over its subset of the records
+  const int f = tid % F4, grp = tid / F4;
+  const int rr = (4 * f) / HP, h0 = (4 * f) % HP;
+  const float4* src = reinterpret_cast<const float4*>(rec0 + static_cast<size_t>(r0 + rr) * HP + h0);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int i = grp; i < nrec; i += NG) {
+    const float4 v = __ldcg(src + static_cast<size_t>(i) * REC4);
+    const float4 e = e_s4[(i * HP + h0) / 4];
+    acc.x = fmaf(e.x, v.x, acc.x);
+    acc.y = fmaf(e.y, v.y, acc.y);
+    acc.z = fmaf(e.z, v.z, acc.z);
+    acc.w = fmaf(e.w, v.w, acc.w);
+  }
+  if (NG > 1) {
+    if (grp > 0) part[grp - 1][f] = acc;
+    __syncthreads();
+    if (grp == 0) {
 #pragma unroll
-    for (int k = 0; k < NR; ++k) zt[h][rr + k * RPP] = acc[k];
-  } else if (h < H) {
-#pragma unroll
-    for (int k = 0; k < NR; ++k) zt[h][rr + k * RPP] = 0.f;   // empty sequence: z = 0
+      for (int gg = 0; gg < NG - 1; ++gg) {
+        const float4 q = part[gg][f];
+        acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+      }
+    }
+  } else {
+    __syncthreads();   // inv_l is ready
+  }
+  if (grp == 0) {
+    zt[h0 + 0][rr] = acc.x * inv_l[h0 + 0];
+    zt[h0 + 1][rr] = acc.y * inv_l[h0 + 1];
+    zt[h0 + 2][rr] = acc.z * inv_l[h0 + 2];
+    zt[h0 + 3][rr] = acc.w * inv_l[h0 + 3];
   }
   __syncthreads();
   // z as an unevaluated fp16 pair (hi + lo) so the up-projection can run on fp16 tensor
   // cores with fp32-level accuracy
-  for (int i = tid; i < H * kCombineRows; i += kCombineThreads) {
-    const int hh = i / kCombineRows, x = i % kCombineRows;
-    if (r0 + x < S::R) {
-      const float z = zt[hh][x];
-      const __half hi = __float2half_rn(z);
-      zh[static_cast<size_t>(hh) * S::R + r0 + x] = hi;
-      zl[static_cast<size_t>(hh) * S::R + r0 + x] = __float2half_rn(z - __half2float(hi));
-    }
+  for (int i = tid; i < H * RB; i += kCombineThreads) {
+    const int hh = i / RB, x = i % RB;
+    const float z = zt[hh][x];
+    const __half hi = __float2half_rn(z);
+    const size_t at = static_cast<size_t>(hh) * R + r0 + x;
+    zh[at] = hi;
+    zl[at] = __float2half_rn(z - __half2float(hi));
   }
 }
 
@@ -716,8 +767,14 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStre
                  stream, pdl, tmap_v, p);
   if (e != cudaSuccess) return e;
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
-  return launch_pdl(combine_kernel<S>, dim3(p.nq, (S::R + kCombineRows - 1) / kCombineRows),
-                    dim3(kCombineThreads), 0, stream, pdl, p);
+  // small batches: four threads per slice element so that a request's many records are
+  // read with more parallelism
+  constexpr int RB1 = kCombineThreads * 4 / S::HP, RB4 = RB1 / 4;
+  if (static_cast<int64_t>(p.nq) * (S::R / RB1) >= 2 * static_cast<int64_t>(p.parts))
+    return launch_pdl(combine_kernel<S, 1>, dim3(p.nq, S::R / RB1), dim3(kCombineThreads), 0,
+                      stream, pdl, p);
+  return launch_pdl(combine_kernel<S, 4>, dim3(p.nq, S::R / RB4), dim3(kCombineThreads), 0,
+                    stream, pdl, p);
 }
 
 // The plan alone (CTA 0 of the planning kernel); the prefill path projects its queries
