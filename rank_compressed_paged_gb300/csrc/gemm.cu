@@ -45,7 +45,8 @@ struct GemmSmem {
   static constexpr int RECV_BYTES = KS > 1 ? 128 * NT * 4 : 0;
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;        // full[S], empty[S], acc
   static constexpr int MISC_OFF = BAR_OFF + (2 * STG + 1) * 8;
-  static constexpr int TOTAL = MISC_OFF + 16;
+  static constexpr int DST_OFF = MISC_OFF + 16;                // append: page offset per column
+  static constexpr int TOTAL = DST_OFF + NT * 8;
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
   static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment");
@@ -137,10 +138,29 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank) {
   return j;
 }
 
+// Page offset (in fp16 elements) that column col of an append job writes from, or -1 when
+// the token is padding (slot < 0), past the token count, or has an out-of-range slot
+// (which also raises the device error bit).  Computed once per column before the
+// epilogue so that the store loop issues no dependent loads.
+template <class S>
+__device__ __forceinline__ int64_t append_dst(const GemmParams& p, const GemmJob& j, int col) {
+  const int n = j.n0 + col;
+  if ((j.kind != 0 && j.kind != 1) || n >= p.T) return -1;
+  const int64_t s = p.slots[n];
+  if (s < 0) return -1;
+  if (s >= p.num_blocks * kBlockSize) {
+    atomicOr(p.dev_err, RCP_DEVERR_BAD_SLOT);
+    return -1;
+  }
+  const int64_t blk = s / kBlockSize, off = s % kBlockSize;
+  return j.kind == 0 ? (blk * kBlockSize + off) * S::R
+                     : ((blk * S::H + j.m0) * kBlockSize + off) * S::RK;
+}
+
 // Write one finished output element (row, column) of a job.
 template <class S>
-__device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j, int row, int col,
-                                           float v) {
+__device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j,
+                                           const int64_t* dst, int row, int col, float v) {
   const int n = j.n0 + col;
   if (j.kind == 3) {
     if (n >= p.nq || row >= 64) return;
@@ -157,21 +177,13 @@ __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j
           __float2half_rn(v);
     return;
   }
-  if (n >= p.T) return;
-  const int64_t s = p.slots[n];
-  if (s < 0) return;
-  if (s >= p.num_blocks * kBlockSize) {
-    atomicOr(p.dev_err, RCP_DEVERR_BAD_SLOT);
-    return;
-  }
-  const int64_t blk = s / kBlockSize, off = s % kBlockSize;
+  const int64_t d = dst[col];
+  if (d < 0) return;
   if (j.kind == 0) {
     const int r = j.m0 + row;
-    if (r < S::R)
-      static_cast<__half*>(p.v_pages)[(blk * kBlockSize + off) * S::R + r] = __float2half_rn(v);
+    if (r < S::R) static_cast<__half*>(p.v_pages)[d + r] = __float2half_rn(v);
   } else if (row < S::RK) {
-    static_cast<__half*>(p.k_pages)[((blk * S::H + j.m0) * kBlockSize + off) * S::RK + row] =
-        __float2half_rn(v);
+    static_cast<__half*>(p.k_pages)[d + row] = __float2half_rn(v);
   }
 }
 
@@ -219,32 +231,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (j.reduce) cluster_sync_all();   // every peer is running before any remote store
+
+  const int nkb = j.kind >= 0 ? j.kb1 - j.kb0 : 0;
+  auto load_a = [&](int kb, int s) {
+    uint8_t* st = sm + s * L::STAGE;
+    if (MODE == kModeUpproj) {
+      // W_v^T slice: two 64(j) x 64(r) boxes (MN-major atoms), rows r = k
+      tma_load_2d(st, amap, j.a_x, j.a_y + kb * j.a_step_y, &full[s]);
+      tma_load_2d(st + kABytes / 2, amap, j.a_x + 64, j.a_y + kb * j.a_step_y, &full[s]);
+    } else {
+      tma_load_2d(st, amap, j.a_x + kb * j.a_step_x, j.a_y, &full[s]);
+    }
+  };
+  auto load_b = [&](int kb, int s) {
+    uint8_t* st = sm + s * L::STAGE;
+    tma_load_2d(st + kABytes, bmap, j.b_x + kb * j.b_step_x, j.b_y, &full[s]);
+    if (NB == 2)
+      tma_load_2d(st + kABytes + L::B_BYTES, &map_b2, j.b_x + kb * j.b_step_x, j.b_y, &full[s]);
+  };
+  // A is always a factor (W_v or U_k), which no kernel writes: its first stages are
+  // fetched before waiting on the previous kernel, whose outputs only B may read.
+  const int pre = nkb < kGemmStages ? nkb : kGemmStages;
+  if (warp == 0 && lane == 0 && nkb > 0) {
+    prefetch_tmap(amap);
+    prefetch_tmap(bmap);
+    for (int kb = 0; kb < pre; ++kb) {
+      mbar_arrive_expect_tx(&full[kb], kABytes + NB * L::B_BYTES);
+      load_a(kb, kb);
+    }
+  }
   griddep_wait();                     // operands written by the previous kernel are visible
   griddep_launch();
 
-  const int nkb = j.kind >= 0 ? j.kb1 - j.kb0 : 0;
   if (warp == 0 && lane == 0 && nkb > 0) {
     // -------------------------------------------------------------- TMA producer
-    prefetch_tmap(amap);
-    prefetch_tmap(bmap);
     int issued = 0;
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % kGemmStages;
-      if (kb >= kGemmStages &&
-          !mbar_wait(&empty[s], ((kb / kGemmStages) - 1) & 1, abort_flag, p.dev_err))
-        break;
-      uint8_t* st = sm + s * L::STAGE;
-      mbar_arrive_expect_tx(&full[s], kABytes + NB * L::B_BYTES);
-      if (MODE == kModeUpproj) {
-        // W_v^T slice: two 64(j) x 64(r) boxes (MN-major atoms), rows r = k
-        tma_load_2d(st, amap, j.a_x, j.a_y + kb * j.a_step_y, &full[s]);
-        tma_load_2d(st + kABytes / 2, amap, j.a_x + 64, j.a_y + kb * j.a_step_y, &full[s]);
-      } else {
-        tma_load_2d(st, amap, j.a_x + kb * j.a_step_x, j.a_y, &full[s]);
+      if (kb >= pre) {
+        if (!mbar_wait(&empty[s], ((kb / kGemmStages) - 1) & 1, abort_flag, p.dev_err)) break;
+        mbar_arrive_expect_tx(&full[s], kABytes + NB * L::B_BYTES);
+        load_a(kb, s);
       }
-      tma_load_2d(st + kABytes, bmap, j.b_x + kb * j.b_step_x, j.b_y, &full[s]);
-      if (NB == 2)
-        tma_load_2d(st + kABytes + L::B_BYTES, &map_b2, j.b_x + kb * j.b_step_x, j.b_y, &full[s]);
+      load_b(kb, s);
       ++issued;
     }
     if (*abort_flag)
@@ -278,6 +307,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (kb < nkb) mbar_wait_drain(accb, 0);
   }
   __syncwarp();
+  int64_t* dst_s = reinterpret_cast<int64_t*>(sm + L::DST_OFF);
+  if (MODE == kModeAppend) {
+    // idle warps get here while the main loop runs; the two issuing lanes join after it
+    for (int c = threadIdx.x; c < NT; c += kGemmThreads) dst_s[c] = append_dst<S>(p, j, c);
+    __syncthreads();
+  }
 
   // ------------------------------------------------------------------ epilogue
   // warp-uniform, since TMEM loads are warp-collective
@@ -293,7 +328,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_ld16(trow + c0, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) gemm_store<S>(p, j, row, c0 + e, v[e]);
+        for (int e = 0; e < 16; ++e) gemm_store<S>(p, j, dst_s, row, c0 + e, v[e]);
       }
     }
   } else {
@@ -324,7 +359,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       float acc = 0.f;
 #pragma unroll
       for (int s = 0; s < KS; ++s) acc += recv[(s * RPC + rr) * NT + col];
-      gemm_store<S>(p, j, static_cast<int>(rank) * RPC + rr, col, acc);
+      gemm_store<S>(p, j, dst_s, static_cast<int>(rank) * RPC + rr, col, acc);
     }
   }
   tc_fence_before();
