@@ -396,6 +396,15 @@ def prefill_flops(prior, chunk, batch):
     return attn, append
 
 
+def prefill_recon_flops(prior, chunk, batch):
+    """FLOPs the reconstructing variant executes in its attention proper: V^ = C_v W_v for
+    every cached key (2*R*H*d per key), then scores 2*H*r_k and O += P V^ 2*H*d per
+    attended key."""
+    H, d, rk, R = SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"], SHAPE["rank_v"]
+    keys = batch * sum(prior + i + 1 for i in range(chunk))
+    return batch * (prior + chunk) * 2 * R * H * d + keys * 2 * H * (rk + d)
+
+
 def run_prefill(args):
     """Chunked prefill at batch 16, 4096 cached tokens + a 256-token chunk per request:
     append the chunk, then causal chunk attention.  One JSON line (not the default run)."""
@@ -428,9 +437,15 @@ def run_prefill(args):
     ws = cache.workspace(T)
     stream = torch.cuda.current_stream()
 
+    variant = args.prefill_variant
+    if variant == "auto":
+        variant = "reconstruct" if chunk >= cache.prefill_crossover_rows() else "rank"
+    if variant == "reconstruct":
+        ws = cache.workspace(T, cache.reconstruct_workspace_bytes(T, B, table.shape[1]))
+
     def step():
         cache.append_kv(k, v, slots)
-        cache.prefill_attn(q, cu, tab, ln, out=out, workspace=ws)
+        cache.prefill_attn(q, cu, tab, ln, out=out, workspace=ws, variant=variant)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -453,20 +468,25 @@ def run_prefill(args):
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ks, ke))
     assert cache.read_device_error() == 0
     attn_f, app_f = prefill_flops(prior, chunk, B)
+    kern_f = attn_f if variant == "rank" else prefill_recon_flops(prior, chunk, B)
     peak_tf, kind = measured_tensor_peak()
     line = {
         "metric": "chunked-prefill ms/step & algorithmic TFLOP/s at B=16, prior 4096 + chunk 256",
+        "variant": variant,
         "value": round((attn_f + app_f) / (step_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
         "ms_per_step": round(step_ms, 3), "steps": args.steps, "warmup": max(args.warmup, 3),
         "higher_is_better": True, "dtype": "f16", "data": "synthetic",
         "config": {"workload": f"prefill_b{B}_p{prior}_c{chunk}", "batch": B, "prior": prior,
                    "chunk": chunk, "algorithmic_flops": attn_f + app_f,
-                   "step": "append the chunk (T = B*chunk tokens) + chunk attention"},
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel",
-                     "achieved": round(attn_f / (kern_ms * 1e-3) / 1e12, 2),
+                   "step": "append the chunk (T = B*chunk tokens) + chunk attention",
+                   "value_flops": "rank-space work of the method, the same for both variants"},
+        "roofline": {"bound": "tensor",
+                     "kernel": "prefill_kernel" if variant == "rank"
+                     else "recon_kernel + prefill_kernel (reconstructing)",
+                     "achieved": round(kern_f / (kern_ms * 1e-3) / 1e12, 2),
                      "peak": peak_tf, "peak_kind": kind, "unit": "TFLOP/s",
-                     "frac": round(attn_f / (kern_ms * 1e-3) / 1e12 / peak_tf, 4),
-                     "kernel_ms": round(kern_ms, 3), "flops_per_launch": attn_f,
+                     "frac": round(kern_f / (kern_ms * 1e-3) / 1e12 / peak_tf, 4),
+                     "kernel_ms": round(kern_ms, 3), "flops_per_launch": kern_f,
                      "note": "fp16 dense tensor rate = the measured bf16 sustained rate"},
         "clocks": clk.summary(),
     }
@@ -487,6 +507,7 @@ def main():
     ap.add_argument("--seq-len", type=int, default=SEQ)
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
     ap.add_argument("--prefill-batch", type=int, default=16)
+    ap.add_argument("--prefill-variant", choices=["auto", "rank", "reconstruct"], default="auto")
     args = ap.parse_args()
     BATCH, SEQ = args.batch, args.seq_len
     rank, world, local_rank = dist_env()

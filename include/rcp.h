@@ -135,6 +135,31 @@ rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_c
                             void* out, void* workspace, size_t workspace_bytes,
                             rcp_stream stream);
 
+/* Chunked prefill, reconstructing variant (Proxima page, "Per-prefill-chunk attention":
+ * the prefill path rebuilds dense values from the coefficients).  Same arguments, layout and
+ * results as rcp_prefill_attn, up to rounding: the values of every cached key of the
+ * requests with chunk rows are first reconstructed as V^ = C_v W_v (fp32 accumulation,
+ * stored fp16) and the attention then runs on V^ with O = P V^ per head.  Cheaper than
+ * the rank-space variant once a request's chunk has more than rcp_prefill_crossover_rows
+ * rows.  workspace must hold rcp_prefill_reconstruct_workspace_size(cache, num_query_rows,
+ * batch, max_blocks_per_seq) bytes (256-byte aligned; it grows with the pages the batch
+ * can reach, 2 * H * d * 16 bytes per page). */
+rcp_status rcp_prefill_attn_reconstruct(rcp_cache* cache, const void* q,
+                                        const int32_t* cu_chunk_lens, int32_t num_query_rows,
+                                        const int32_t* block_table, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, int32_t batch, void* out,
+                                        void* workspace, size_t workspace_bytes,
+                                        rcp_stream stream);
+
+/* Workspace bytes of rcp_prefill_attn_reconstruct. */
+rcp_status rcp_prefill_reconstruct_workspace_size(const rcp_cache* cache, int32_t max_query_rows,
+                                                  int32_t batch, int32_t max_blocks_per_seq,
+                                                  size_t* bytes);
+
+/* Chunk rows per request above which the reconstructing prefill does fewer multiply-adds:
+ * ceil(R d / (R - d)) (147 for R = 1024, d = 128); INT32_MAX when R <= d. */
+rcp_status rcp_prefill_crossover_rows(const rcp_cache* cache, int32_t* rows);
+
 /* Measurement hook (the pages have no counterpart; it exists for roofline timing).  When
  * both events are non-NULL, every later decode / prefill call records start_event on its
  * stream just before the split-K attention kernel and stop_event just after it, so the

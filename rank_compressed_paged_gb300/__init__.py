@@ -94,12 +94,25 @@ class PagedCoeffCache:
                    self._lib.rcp_workspace_size(self._h, rows, ctypes.byref(n)))
         return n.value
 
-    def workspace(self, rows: int):
+    def workspace(self, rows: int, need: int | None = None):
         import torch
-        need = self.workspace_bytes(rows)
+        need = self.workspace_bytes(rows) if need is None else need
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(need, dtype=torch.uint8, device=self.k_pages.device)
         return self._ws
+
+    def reconstruct_workspace_bytes(self, rows: int, batch: int, max_blocks_per_seq: int) -> int:
+        n = ctypes.c_size_t()
+        _lib.check("rcp_prefill_reconstruct_workspace_size",
+                   self._lib.rcp_prefill_reconstruct_workspace_size(
+                       self._h, rows, batch, max_blocks_per_seq, ctypes.byref(n)))
+        return n.value
+
+    def prefill_crossover_rows(self) -> int:
+        n = ctypes.c_int32()
+        _lib.check("rcp_prefill_crossover_rows",
+                   self._lib.rcp_prefill_crossover_rows(self._h, ctypes.byref(n)))
+        return n.value
 
     def read_device_error(self) -> int:
         return int(self.dev_error.item())
@@ -152,16 +165,31 @@ class PagedCoeffCache:
         return out
 
     def prefill_attn(self, q, cu_chunk_lens, block_table, seq_lens, out=None, workspace=None,
-                     stream=None):
-        """q: [sum chunk][H][d] fp16; cu_chunk_lens: [B+1] int32; seq_lens include the chunk."""
+                     stream=None, variant: str = "auto"):
+        """q: [sum chunk][H][d] fp16; cu_chunk_lens: [B+1] int32; seq_lens include the chunk.
+
+        variant: "rank" (joint-coefficient contraction per head), "reconstruct" (dense values
+        C_v W_v rebuilt once per key), or "auto": reconstruct when the mean chunk length
+        reaches the library's crossover."""
         import torch
         rows = int(q.shape[0])
         B = int(seq_lens.shape[0])
+        mb = int(block_table.shape[1])
+        if variant == "auto":
+            variant = "reconstruct" if B > 0 and rows >= B * self.prefill_crossover_rows() \
+                else "rank"
+        if variant not in ("rank", "reconstruct"):
+            raise ValueError(f"unknown prefill variant {variant!r}")
         if out is None:
             out = torch.empty_like(q)
-        ws = self.workspace(rows) if workspace is None else workspace
-        _lib.check("rcp_prefill_attn", self._lib.rcp_prefill_attn(
-            self._h, _ptr(q), _ptr(cu_chunk_lens), rows, _ptr(block_table),
-            int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out), _ptr(ws),
-            ws.numel() * ws.element_size(), _stream(stream)))
+        if variant == "rank":
+            ws = self.workspace(rows) if workspace is None else workspace
+            fn, name = self._lib.rcp_prefill_attn, "rcp_prefill_attn"
+        else:
+            ws = self.workspace(rows, self.reconstruct_workspace_bytes(rows, B, mb)) \
+                if workspace is None else workspace
+            fn, name = self._lib.rcp_prefill_attn_reconstruct, "rcp_prefill_attn_reconstruct"
+        _lib.check(name, fn(
+            self._h, _ptr(q), _ptr(cu_chunk_lens), rows, _ptr(block_table), mb, _ptr(seq_lens), B,
+            _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
         return out

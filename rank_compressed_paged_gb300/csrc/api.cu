@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -94,6 +95,7 @@ cudaError_t prepare_kernels(int dev) {
   cudaError_t e = rcp::prepare_attn<S>(dev);
   if (e == cudaSuccess) e = rcp::prepare_gemm<S>();
   if (e == cudaSuccess) e = rcp::prepare_prefill<S>();
+  if (e == cudaSuccess) e = rcp::prepare_recon<S>();
   return e;
 }
 
@@ -154,12 +156,28 @@ void fill_ws(rcp::AttnParams& p, void* ws, int64_t nq) {
   // prefill queries reuse the decode query region: hi then lo, [nq][H][64] fp16 each
   p.qhi = b + w.qt;
   p.qlo = b + w.qt + static_cast<size_t>(nq) * S::H * 64 * 2;
+  p.vcum = nullptr;
+  p.vhat = nullptr;
+}
+
+template <class S>
+void fill_recon(rcp::AttnParams& p, void* ws, int64_t nq, int64_t batch, int64_t max_blocks) {
+  const rcp::ReconLayout r = rcp::recon_layout<S>(nq, batch, max_blocks);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  p.vcum = reinterpret_cast<int64_t*>(b + r.vcum);
+  p.vhat = b + r.vhat;
+}
+
+size_t recon_ws_bytes(const rcp_cache* c, int64_t nq, int64_t batch, int64_t max_blocks) {
+  return c->shape == kShapeMain ? rcp::recon_layout<ShapeMain>(nq, batch, max_blocks).total
+                                : rcp::recon_layout<ShapeTiny>(nq, batch, max_blocks).total;
 }
 
 rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, int32_t nq,
                          const int32_t* block_table, int32_t max_blocks_per_seq,
                          const int32_t* seq_lens, int32_t batch, void* out, void* ws,
-                         size_t ws_size, rcp_stream stream, bool after_own_append = false) {
+                         size_t ws_size, rcp_stream stream, bool after_own_append = false,
+                         bool recon = false) {
   if (!c || batch < 0 || nq < 0 || max_blocks_per_seq < 1) return RCP_ERR_INVALID_ARG;
   if (nq == 0) return RCP_OK;
   if (batch == 0 && cu_chunk) return RCP_ERR_INVALID_ARG;
@@ -169,7 +187,8 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
       (cu_chunk && (reinterpret_cast<uintptr_t>(cu_chunk) & 3u)))
     return RCP_ERR_INVALID_ARG;
-  if (ws_size < ws_bytes(c, nq)) return RCP_ERR_WORKSPACE;
+  if (ws_size < (recon ? recon_ws_bytes(c, nq, batch, max_blocks_per_seq) : ws_bytes(c, nq)))
+    return RCP_ERR_WORKSPACE;
   rcp_status st = ensure_device(c);
   if (st != RCP_OK) return st;
   rcp::AttnParams p{};
@@ -213,24 +232,41 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
     CUtensorMap q_map;
     if (!encode_2d(&q_map, q, hdq, static_cast<uint64_t>(nq), hdq * 2, 64, nq <= 256 ? 64 : 256))
       return RCP_ERR_CUDA;
+    // reconstructing variant: V^ rows for at most batch x max_blocks_per_seq pages
+    const int64_t max_pages = static_cast<int64_t>(batch) * max_blocks_per_seq;
+    CUtensorMap vhat_map = c->tmap_v;
+    if (recon) {
+      if (max_pages * 16 >= (int64_t{1} << 31)) return RCP_ERR_UNSUPPORTED;
+      if (c->shape == kShapeMain) fill_recon<ShapeMain>(p, ws, nq, batch, max_blocks_per_seq);
+      else fill_recon<ShapeTiny>(p, ws, nq, batch, max_blocks_per_seq);
+      if (!encode_2d(&vhat_map, p.vhat, hdq, static_cast<uint64_t>(max_pages) * 16, hdq * 2, 64, 128))
+        return RCP_ERR_CUDA;
+    }
+    const CUtensorMap& vals = recon ? vhat_map : c->tmap_v;
     if (c->shape == kShapeMain) {
       e = rcp::launch_plan<ShapeMain>(p, s, pdl);
       if (e == cudaSuccess)
         e = rcp::launch_qproj_gemm<ShapeMain>(c->tmap_uk, q_map, p.qhi, p.qlo, nq, p.qscale,
                                               c->dev_err, s, pdl);
+      // profiling events bracket the attention proper: reconstruction + prefill kernel
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
+      if (e == cudaSuccess && recon)
+        e = rcp::launch_recon<ShapeMain>(c->tmap_v, c->tmap_wv_mn, p, max_pages, s, pdl);
       if (e == cudaSuccess)
-        e = rcp::launch_prefill<ShapeMain>(qhi_map, qlo_map, c->tmap_kp, c->tmap_v, c->tmap_wv_mn,
-                                           p, max_tiles, s, pdl);
+        e = rcp::launch_prefill<ShapeMain>(qhi_map, qlo_map, c->tmap_kp, vals, c->tmap_wv_mn, p,
+                                           max_tiles, s, pdl, recon);
     } else {
       e = rcp::launch_plan<ShapeTiny>(p, s, pdl);
       if (e == cudaSuccess)
         e = rcp::launch_qproj_gemm<ShapeTiny>(c->tmap_uk, q_map, p.qhi, p.qlo, nq, p.qscale,
                                               c->dev_err, s, pdl);
+      // profiling events bracket the attention proper: reconstruction + prefill kernel
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
+      if (e == cudaSuccess && recon)
+        e = rcp::launch_recon<ShapeTiny>(c->tmap_v, c->tmap_wv_mn, p, max_pages, s, pdl);
       if (e == cudaSuccess)
-        e = rcp::launch_prefill<ShapeTiny>(qhi_map, qlo_map, c->tmap_kp, c->tmap_v, c->tmap_wv_mn,
-                                           p, max_tiles, s, pdl);
+        e = rcp::launch_prefill<ShapeTiny>(qhi_map, qlo_map, c->tmap_kp, vals, c->tmap_wv_mn, p,
+                                           max_tiles, s, pdl, recon);
     }
     if (e == cudaSuccess && c->prof_stop) e = cudaEventRecord(c->prof_stop, s);
     return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
@@ -437,6 +473,33 @@ rcp_status rcp_prefill_attn(rcp_cache* c, const void* q, const int32_t* cu_chunk
   if (!cu_chunk_lens) return RCP_ERR_INVALID_ARG;
   return run_attention(c, q, cu_chunk_lens, num_query_rows, block_table, max_blocks_per_seq,
                        seq_lens, batch, out, workspace, workspace_bytes, stream);
+}
+
+rcp_status rcp_prefill_attn_reconstruct(rcp_cache* c, const void* q, const int32_t* cu_chunk_lens,
+                                        int32_t num_query_rows, const int32_t* block_table,
+                                        int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                        int32_t batch, void* out, void* workspace,
+                                        size_t workspace_bytes, rcp_stream stream) {
+  if (!cu_chunk_lens) return RCP_ERR_INVALID_ARG;
+  return run_attention(c, q, cu_chunk_lens, num_query_rows, block_table, max_blocks_per_seq,
+                       seq_lens, batch, out, workspace, workspace_bytes, stream, false, true);
+}
+
+rcp_status rcp_prefill_reconstruct_workspace_size(const rcp_cache* c, int32_t max_query_rows,
+                                                  int32_t batch, int32_t max_blocks_per_seq,
+                                                  size_t* bytes) {
+  if (!c || !bytes || max_query_rows < 0 || batch < 0 || max_blocks_per_seq < 0)
+    return RCP_ERR_INVALID_ARG;
+  *bytes = recon_ws_bytes(c, max_query_rows, batch, max_blocks_per_seq);
+  return RCP_OK;
+}
+
+rcp_status rcp_prefill_crossover_rows(const rcp_cache* c, int32_t* rows) {
+  if (!c || !rows) return RCP_ERR_INVALID_ARG;
+  const int64_t R = c->cfg.rank_v, d = c->cfg.head_dim;
+  // equal multiply-adds per (key, head): rows * R (rank space) = R * d + rows * d
+  *rows = R > d ? static_cast<int32_t>((R * d + (R - d) - 1) / (R - d)) : INT32_MAX;
+  return RCP_OK;
 }
 
 rcp_status rcp_set_profile_events(rcp_cache* c, void* start_event, void* stop_event) {

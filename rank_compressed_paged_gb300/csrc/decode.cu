@@ -131,6 +131,29 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
         t0 += nt;
       }
       if (tid == kPlanThreads - 1) *p.tcount = static_cast<int32_t>(t0);
+      if (p.vcum != nullptr) {
+        // reconstructing prefill: pages of every request with chunk rows, in request
+        // order (the rows of V^)
+        __syncthreads();
+        int64_t vs = 0;
+        for (int b = b0; b < b1; ++b)
+          if (tiles_of(b) > 0) vs += (p.seq_lens[b] + kBlockSize - 1) / kBlockSize;
+        int64_t vin = vs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t y = __shfl_up_sync(0xffffffffu, vin, o);
+          if (lane >= o) vin += y;
+        }
+        if (lane == 31) warp_sum[w] = vin;
+        __syncthreads();
+        int64_t v0 = vin - vs;
+        for (int i = 0; i < w; ++i) v0 += warp_sum[i];
+        if (tid == 0) p.vcum[0] = 0;
+        for (int b = b0; b < b1; ++b) {
+          if (tiles_of(b) > 0) v0 += (p.seq_lens[b] + kBlockSize - 1) / kBlockSize;
+          p.vcum[b + 1] = v0;
+        }
+      }
     }
     if (p.late_wait) griddep_wait();
     return;

@@ -17,10 +17,18 @@ template <class S>
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream, bool pdl);
 template <class S>
 cudaError_t prepare_prefill();
+// recon: attend reconstructed values (vp = tensor map of V^, w unused) instead of joint
+// coefficients.
 template <class S>
 cudaError_t launch_prefill(const CUtensorMap& qhi, const CUtensorMap& qlo, const CUtensorMap& kp,
                            const CUtensorMap& vp, const CUtensorMap& w, const AttnParams& p,
-                           int max_tiles, cudaStream_t stream, bool pdl);
+                           int max_tiles, cudaStream_t stream, bool pdl, bool recon);
+// V^ = C_v W_v for the pages of every request with chunk rows (max_pages bounds them).
+template <class S>
+cudaError_t prepare_recon();
+template <class S>
+cudaError_t launch_recon(const CUtensorMap& vp, const CUtensorMap& w_v_mn, const AttnParams& p,
+                         int64_t max_pages, cudaStream_t stream, bool pdl);
 template <class S>
 cudaError_t prepare_gemm();
 // k_rows / v_rows: tensor maps over the new tokens' k and v ([T][H*d], box 64 x NT with

@@ -37,13 +37,17 @@ namespace rcp {
 constexpr int kPfThreads = 224;   // 0 key copies, 1 MMAs, 2-5 softmax, 6 value copies
 constexpr float kPfRescale = 8.f;   // log2 units: weights stay below 2^8 between rescales
 
-template <class S>
+// RECON: the values are the reconstructed V^ rows of head h (N = d) instead of a slice
+// of the joint coefficients (N = RQ), and the epilogue writes O directly.
+template <class S, bool RECON>
 struct PfSmem {
   using C = PrefillCfg<S>;
-  static constexpr int NG = C::RQ / 64;                 // 64-wide groups in the rank slice
+  static constexpr int VN = RECON ? S::D : C::RQ;       // value MMA N
+  static constexpr int NQ = RECON ? 1 : C::NQ;          // CTAs per (tile, head)
+  static constexpr int NG = VN / 64;                    // 64-wide groups of the value tile
   static constexpr int Q_BYTES = 128 * 128;             // one [128][64] fp16 operand
   static constexpr int K_BYTES = C::KT * 128;           // key coefficients of one tile
-  static constexpr int V_BYTES = C::KT * C::RQ * 2;     // value coefficients of one tile
+  static constexpr int V_BYTES = C::KT * VN * 2;        // value tile
   static constexpr int STAGE = K_BYTES + V_BYTES;
   static constexpr int P_BYTES = 128 * C::KT * 2;
   static constexpr int ST_OFF = 2 * Q_BYTES;            // q~ hi at 0, q~ lo at Q_BYTES
@@ -52,20 +56,20 @@ struct PfSmem {
   static constexpr int ZL_OFF = ZH_OFF + 128 * C::RQ * 2;
   static constexpr int W_OFF = ZL_OFF + 128 * C::RQ * 2;
   static constexpr int W_BYTES = C::RQ * S::D * 2;
-  static constexpr int END = (P_OFF + P_BYTES > W_OFF + W_BYTES) ? P_OFF + P_BYTES
-                                                                   : W_OFF + W_BYTES;
+  static constexpr int END = (RECON || P_OFF + P_BYTES > W_OFF + W_BYTES) ? P_OFF + P_BYTES
+                                                                             : W_OFF + W_BYTES;
   static constexpr int BAR_OFF = END;                   // 17 mbarriers
   static constexpr int MISC_OFF = BAR_OFF + 17 * 8;     // tmem slot, abort flag
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
-  static constexpr int RPC = 128 / C::NQ;               // output rows each slice CTA sums
-  static constexpr int TMEM_COLS = pow2_at_least(256 + C::RQ, 32);
+  static constexpr int RPC = 128 / NQ;                  // output rows each slice CTA sums
+  static constexpr int TMEM_COLS = pow2_at_least(256 + VN, 32);
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
-  static_assert(C::NQ == 1 || C::NQ * RPC * S::D * 4 <= 2 * 128 * C::RQ * 2, "receive buffer");
-  static_assert(256 + C::RQ <= 512 && S::D <= 128, "tensor memory budget");
+  static_assert(NQ == 1 || NQ * RPC * S::D * 4 <= 2 * 128 * C::RQ * 2, "receive buffer");
+  static_assert(256 + VN <= 512 && S::D <= 128, "tensor memory budget");
 };
 
-template <class S>
+template <class S, bool RECON>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qhi_map,
                    const __grid_constant__ CUtensorMap qlo_map,
@@ -73,8 +77,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                    const __grid_constant__ CUtensorMap vp_map,
                    const __grid_constant__ CUtensorMap w_map, const AttnParams p) {
   using C = PrefillCfg<S>;
-  using L = PfSmem<S>;
-  constexpr int KT = C::KT, RQ = C::RQ, NQ = C::NQ, NG = L::NG, D = S::D, H = S::H;
+  using L = PfSmem<S, RECON>;
+  constexpr int KT = C::KT, RQ = C::RQ, NQ = L::NQ, NG = L::NG, VN = L::VN, D = S::D, H = S::H;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -185,6 +189,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int jb = 0; jb < BPT; ++jb)
             if (phys[jb] >= 0)
               tma_load_2d(kst + jb * 2048, &kp_map, 0, (phys[jb] * H + h) * kBlockSize, &k_full[s]);
+        } else if constexpr (RECON) {
+          // V^ rows of the request are contiguous: one 64-column box of 128 keys per group
+          if (j >= 2 && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
+          mbar_arrive_expect_tx(&v_full[s], NG * KT * 128);
+          const int64_t vrow = p.vcum[b] * kBlockSize + static_cast<int64_t>(j) * KT;
+#pragma unroll
+          for (int g = 0; g < NG; ++g)
+            tma_load_2d(vst + g * KT * 128, &vp_map, h * D + g * 64, static_cast<int32_t>(vrow),
+                        &v_full[s]);
         } else {
           if (j >= 2 && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
           mbar_arrive_expect_tx(&v_full[s], nload * NG * 2048);
@@ -199,7 +212,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       // the W_v rows of this slice, into stage memory once every value MMA is done
-      if (!keys && mbar_wait(acc_done, 0, abort_flag, p.dev_err)) {
+      if (!RECON && !keys && mbar_wait(acc_done, 0, abort_flag, p.dev_err)) {
         mbar_arrive_expect_tx(w_full, L::W_BYTES);
         uint8_t* wst = sm + L::W_OFF;
         for (int g = 0; g < D / 64; ++g)
@@ -218,7 +231,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // the softmax of tile j+1.
     if (lane == 0) {
       constexpr uint32_t id_s = make_idesc_f16(128, KT, false, false);
-      constexpr uint32_t id_pv = make_idesc_f16(128, RQ, false, true);
+      constexpr uint32_t id_pv = make_idesc_f16(128, VN, false, true);
       constexpr uint32_t id_o = make_idesc_f16(128, D, false, true);
       const uint32_t qa = smem_u32(sm);
       const uint32_t pa = smem_u32(sm + L::P_OFF);
@@ -274,7 +287,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       umma_commit(acc_done);
       // up-projection of this slice: O = (z_hi + z_lo) W_v[slice rows, h*d:(h+1)*d]
-      if (mbar_wait(zq_full, 0, abort_flag, p.dev_err) && mbar_wait(w_full, 0, abort_flag, p.dev_err)) {
+      if (!RECON && mbar_wait(zq_full, 0, abort_flag, p.dev_err) &&
+          mbar_wait(w_full, 0, abort_flag, p.dev_err)) {
         tc_fence_after();
         const uint32_t zh = smem_u32(sm + L::ZH_OFF), zl = smem_u32(sm + L::ZL_OFF);
         const uint32_t wa = smem_u32(sm + L::W_OFF);
@@ -286,8 +300,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           umma_f16(tmem, make_sdesc(zl + koff, 16, 1024, kSwizzle128B), bd, id_o, 1u);
         }
       }
-      umma_commit(o_done);
-      mbar_wait_drain(o_done, 0);
+      if (!RECON) {
+        umma_commit(o_done);
+        mbar_wait_drain(o_done, 0);
+      }
     }
   } else {
     // ----------------------------------------------- softmax (one thread per query row)
@@ -357,7 +373,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // (lanes whose max did not move multiply by 1)
       if (__any_sync(0xffffffffu, ok && alpha != 1.f && j > 0)) {
 #pragma unroll 1
-        for (int c = 0; c < RQ; c += 32) {
+        for (int c = 0; c < VN; c += 32) {
           float v[16], w[16];
           tmem_ld16(tl + 256 + c, v);
           tmem_ld16(tl + 256 + c + 16, w);
@@ -401,55 +417,82 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    // --------------------------------------------- normalise z, split into fp16 hi + lo
     const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag, p.dev_err));
     tc_fence_after();
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    uint8_t* zh = sm + L::ZH_OFF;
-    uint8_t* zl = sm + L::ZL_OFF;
+    if constexpr (RECON) {
+      // ------------------------------------------- O / l straight to the output rows
+      if (ok) {   // warp-uniform: every lane loads, only rows of the chunk are stored
+        __half* dst = static_cast<__half*>(p.out) + (static_cast<size_t>(row0 + r) * H + h) * D;
 #pragma unroll 1
-    for (int c = 0; c < RQ; c += 32) {
-      float v[32];
-      if (ok) {
-        tmem_ld16(tl + 256 + c, *reinterpret_cast<float(*)[16]>(&v[0]));
-        tmem_ld16(tl + 256 + c + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
-        tmem_wait_ld();
-      } else {
+        for (int c = 0; c < D; c += 16) {
+          float v[16];
+          tmem_ld16(tl + 256 + c, v);
+          tmem_wait_ld();
+          uint32_t w8[8];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          for (int e = 0; e < 16; e += 2) {
+            const __half2 hv = __floats2half2_rn(v[e] * inv, v[e + 1] * inv);
+            w8[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          if (row_ok) {
+            *reinterpret_cast<uint4*>(dst + c) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+            *reinterpret_cast<uint4*>(dst + c + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          }
+        }
       }
-      uint32_t hw[16], lw[16];
+    } else {
+      // ------------------------------------------- normalise z, split into fp16 hi + lo
+      uint8_t* zh = sm + L::ZH_OFF;
+      uint8_t* zl = sm + L::ZL_OFF;
+#pragma unroll 1
+      for (int c = 0; c < RQ; c += 32) {
+        float v[32];
+        if (ok) {
+          tmem_ld16(tl + 256 + c, *reinterpret_cast<float(*)[16]>(&v[0]));
+          tmem_ld16(tl + 256 + c + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float z0 = v[e] * inv, z1 = v[e + 1] * inv;
-        const __half2 hi = __floats2half2_rn(z0, z1);
-        const float2 hb = __half22float2(hi);
-        const __half2 lo = __floats2half2_rn(z0 - hb.x, z1 - hb.y);
-        hw[e / 2] = *reinterpret_cast<const uint32_t*>(&hi);
-        lw[e / 2] = *reinterpret_cast<const uint32_t*>(&lo);
-      }
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        }
+        uint32_t hw[16], lw[16];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int ch = (c + q4 * 8) / 8;                   // 16-byte chunk index in the row
-        const int kb = ch >> 3, cc = ch & 7;
-        const int off = kb * 16384 + r * 128 + ((cc ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(zh + off) =
-            make_uint4(hw[q4 * 4], hw[q4 * 4 + 1], hw[q4 * 4 + 2], hw[q4 * 4 + 3]);
-        *reinterpret_cast<uint4*>(zl + off) =
-            make_uint4(lw[q4 * 4], lw[q4 * 4 + 1], lw[q4 * 4 + 2], lw[q4 * 4 + 3]);
+        for (int e = 0; e < 32; e += 2) {
+          const float z0 = v[e] * inv, z1 = v[e + 1] * inv;
+          const __half2 hi = __floats2half2_rn(z0, z1);
+          const float2 hb = __half22float2(hi);
+          const __half2 lo = __floats2half2_rn(z0 - hb.x, z1 - hb.y);
+          hw[e / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+          lw[e / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int ch = (c + q4 * 8) / 8;                   // 16-byte chunk index in the row
+          const int kb = ch >> 3, cc = ch & 7;
+          const int off = kb * 16384 + r * 128 + ((cc ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(zh + off) =
+              make_uint4(hw[q4 * 4], hw[q4 * 4 + 1], hw[q4 * 4 + 2], hw[q4 * 4 + 3]);
+          *reinterpret_cast<uint4*>(zl + off) =
+              make_uint4(lw[q4 * 4], lw[q4 * 4 + 1], lw[q4 * 4 + 2], lw[q4 * 4 + 3]);
+        }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(zq_full);
     }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(zq_full);
   }
   __syncwarp();
 
   // ------------------------------------------------------------------- outputs
-  const bool have_o = __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag, p.dev_err));
+  const bool have_o =
+      RECON || __all_sync(0xffffffffu, mbar_wait(o_done, 0, abort_flag, p.dev_err));
   tc_fence_after();
   __half* out = static_cast<__half*>(p.out);
-  if constexpr (NQ == 1) {
+  if constexpr (RECON) {
+    (void)have_o;
+    (void)out;   // written by the softmax warps
+  } else if constexpr (NQ == 1) {
     if (warp >= 2 && warp < 6) {
       const int r = (warp & 3) * 32 + lane;
       const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -523,19 +566,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // --------------------------------------------------------------------------- launches
 template <class S>
 cudaError_t prepare_prefill() {
-  return cudaFuncSetAttribute(prefill_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              PfSmem<S>::ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<S, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PfSmem<S, false>::ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_kernel<S, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PfSmem<S, true>::ALLOC);
+  return e;
 }
 
+// recon: vp is the tensor map of V^ ([rows][H*d], 64 x 128 boxes) and w is not read.
 template <class S>
 cudaError_t launch_prefill(const CUtensorMap& qhi, const CUtensorMap& qlo, const CUtensorMap& kp,
                            const CUtensorMap& vp, const CUtensorMap& w, const AttnParams& p,
-                           int max_tiles, cudaStream_t stream, bool pdl) {
-  constexpr int NQ = PrefillCfg<S>::NQ;
+                           int max_tiles, cudaStream_t stream, bool pdl, bool recon) {
+  const int NQ = recon ? 1 : PrefillCfg<S>::NQ;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(max_tiles * S::H * NQ);
   cfg.blockDim = dim3(kPfThreads);
-  cfg.dynamicSmemBytes = PfSmem<S>::ALLOC;
+  cfg.dynamicSmemBytes = recon ? PfSmem<S, true>::ALLOC : PfSmem<S, false>::ALLOC;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -551,7 +600,8 @@ cudaError_t launch_prefill(const CUtensorMap& qhi, const CUtensorMap& qlo, const
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel<S>, qhi, qlo, kp, vp, w, p);
+  if (recon) return cudaLaunchKernelEx(&cfg, prefill_kernel<S, true>, qhi, qlo, kp, vp, w, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<S, false>, qhi, qlo, kp, vp, w, p);
 }
 
 template cudaError_t prepare_prefill<ShapeMain>();
@@ -559,10 +609,10 @@ template cudaError_t prepare_prefill<ShapeTiny>();
 template cudaError_t launch_prefill<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
                                                const CUtensorMap&, const CUtensorMap&,
                                                const CUtensorMap&, const AttnParams&, int,
-                                               cudaStream_t, bool);
+                                               cudaStream_t, bool, bool);
 template cudaError_t launch_prefill<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
                                                const CUtensorMap&, const CUtensorMap&,
                                                const CUtensorMap&, const AttnParams&, int,
-                                               cudaStream_t, bool);
+                                               cudaStream_t, bool, bool);
 
 }  // namespace rcp

@@ -56,6 +56,15 @@ struct PrefillCfg {
   static_assert(S::R % RQ == 0 && RQ % 64 == 0 && S::RK <= 64 && S::D % 64 == 0, "prefill shape");
 };
 
+// Reconstructing prefill: V^ = C_v W_v for every cached key of the batch, 128 keys (8
+// pages) x 256 columns of H*d per CTA, K = R in 64-wide k-blocks, two pipeline stages
+// (two CTAs share an SM, so one's epilogue overlaps the other's main loop).
+template <class S>
+struct ReconCfg {
+  static constexpr int MT = 128, NT = 256, KB = S::R / 64, STG = 2;
+  static_assert((S::H * S::D) % NT == 0 && S::R % 64 == 0, "reconstruct tiling");
+};
+
 // Upper bound on 128-row prefill query tiles for nq query rows (each request with rows
 // adds at most one partial tile, and at most nq requests have rows).
 inline int64_t prefill_max_tiles(int64_t nq) { return (nq + 127) / 128 + nq; }
@@ -75,14 +84,32 @@ inline WsLayout ws_layout(int64_t nq) {
   // rank-space queries: fp32 [nq][H][r_k] (decode) or fp16 hi + lo [nq][H][64] (prefill)
   const size_t qt_row = static_cast<size_t>(S::H) * (S::RK > 64 ? S::RK : 64) * 4;
   w.qt = o;   o = align256(o + qt_row * nq);
-  w.rec = o;  o = align256(o + sizeof(float) * (nq + kMaxParts) * static_cast<size_t>(S::REC));
-  w.zhi = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
-  w.zlo = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
   w.tile_b = o;  o = align256(o + sizeof(int32_t) * prefill_max_tiles(nq));
   w.tile_qt = o; o = align256(o + sizeof(int32_t) * prefill_max_tiles(nq));
   w.tcount = o;  o = align256(o + sizeof(int32_t));
+  // decode only from here on
+  w.rec = o;  o = align256(o + sizeof(float) * (nq + kMaxParts) * static_cast<size_t>(S::REC));
+  w.zhi = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
+  w.zlo = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
   w.total = o;
   return w;
+}
+
+// The reconstructing prefill never uses the decode-only regions at the end (rec, zhi, zlo):
+// its per-request block prefix sums and the reconstructed values V^ start where they
+// start, for at most batch x max_blocks_per_seq pages.
+struct ReconLayout {
+  size_t vcum, vhat, total;
+};
+template <class S>
+inline ReconLayout recon_layout(int64_t nq, int64_t batch, int64_t max_blocks) {
+  const WsLayout w = ws_layout<S>(nq);
+  ReconLayout r;
+  size_t o = w.rec;
+  r.vcum = o;  o = align256(o + sizeof(int64_t) * (batch + 1));
+  r.vhat = o;  o = align256(o + 2 * static_cast<size_t>(batch) * max_blocks * kBlockSize * S::H * S::D);
+  r.total = o > w.total ? o : w.total;
+  return r;
 }
 
 // Everything the attention kernels of one call see.
@@ -110,6 +137,9 @@ struct AttnParams {
   int32_t* tcount;            // [1] number of query tiles
   void* qhi;                  // [nq][H][64] fp16 rank-space queries (scaled), zero past r_k
   void* qlo;                  // [nq][H][64] fp16 remainder q~ - qhi
+  // reconstructing prefill only (nullptr otherwise)
+  int64_t* vcum;              // [batch+1] prefix sums of blocks per request
+  void* vhat;                 // [sum of blocks * 16][H*d] fp16 reconstructed values C_v W_v
   int64_t num_blocks;
   int32_t bt_stride;          // max_blocks_per_seq
   int32_t batch;

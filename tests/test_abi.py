@@ -135,3 +135,28 @@ def test_python_layer_fails_loudly_without_library(tmp_path):
             _lib.load(str(tmp_path / "nope.so"))
     finally:
         _lib._lib = saved
+
+
+def test_prefill_crossover_and_reconstruct_workspace(lib):
+    from rank_compressed_paged_gb300 import _lib
+    st, h = _create(lib, _lib, _cfg(_lib))
+    assert st == _lib.RCP_OK
+    rows = ctypes.c_int32()
+    assert lib.rcp_prefill_crossover_rows(h, ctypes.byref(rows)) == _lib.RCP_OK
+    assert rows.value == 147                 # ceil(1024 * 128 / (1024 - 128))
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    # V^ (2 * H * d bytes per key) dominates once pages outnumber the query rows
+    assert lib.rcp_prefill_reconstruct_workspace_size(h, 64, 16, 272, ctypes.byref(a)) == 0
+    assert lib.rcp_prefill_reconstruct_workspace_size(h, 64, 16, 273, ctypes.byref(b)) == 0
+    assert b.value - a.value >= 16 * 16 * 32 * 128 * 2   # one more page per request
+    assert a.value >= 16 * 272 * 16 * 32 * 128 * 2
+    small = ctypes.c_size_t()
+    assert lib.rcp_workspace_size(h, 64, ctypes.byref(small)) == 0
+    assert a.value > small.value
+    assert lib.rcp_prefill_reconstruct_workspace_size(h, -1, 16, 272, ctypes.byref(a)) == \
+        _lib.RCP_ERR_INVALID_ARG
+    lib.rcp_destroy_cache(h)
+    st, h = _create(lib, _lib, _cfg(_lib, 4, 64, 16, 64))
+    assert lib.rcp_prefill_crossover_rows(h, ctypes.byref(rows)) == _lib.RCP_OK
+    assert rows.value == 2**31 - 1           # R <= d: rank space is never dearer
+    lib.rcp_destroy_cache(h)

@@ -76,7 +76,8 @@ def test_decode_ragged64_sampled():
     _decode_sampled(lens, 1013, sample, append=False)
 
 
-def test_prefill_b16_p4096_c256_sampled():
+@pytest.mark.parametrize("variant", ["rank", "reconstruct"])
+def test_prefill_b16_p4096_c256_sampled(variant):
     import torch
     B, prior, chunk = 16, 4096, 256
     after = np.full(B, prior + chunk, np.int32)
@@ -91,7 +92,7 @@ def test_prefill_b16_p4096_c256_sampled():
     sample = [0, 11]
     hosts = {b: _host_request(cache, table, b, wl.blocks_needed(after[b])) for b in sample}
     cache.append_kv(t(k), t(v), t(slots))
-    out = cache.prefill_attn(t(q), t(cu), t(table), t(lens)).cpu().numpy()
+    out = cache.prefill_attn(t(q), t(cu), t(table), t(lens), variant=variant).cpu().numpy()
     torch.cuda.synchronize()
     assert cache.read_device_error() == 0
     for b in sample:
@@ -101,4 +102,4 @@ def test_prefill_b16_p4096_c256_sampled():
         kp, vp = orc.append_kv(kp, vp, U, W, k[rows], v[rows], loc, 16)
         ref = orc.prefill_attn(q[rows], np.array([0, chunk], np.int32), kp, vp, U, W, tab,
                                after[b:b + 1], 16)
-        assert_close(out[rows], ref, what=f"prefill request {b}")
+        assert_close(out[rows], ref, what=f"prefill request {b} ({variant})")

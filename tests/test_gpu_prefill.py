@@ -12,13 +12,16 @@ TINY = wl.SHAPES["tiny"]
 MAIN = wl.SHAPES["mha32"]
 
 
-def _run(inp):
+VARIANTS = ["rank", "reconstruct"]
+
+
+def _run(inp, variant="rank"):
     import torch
     c = inp.cache
     cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
     cache.append_kv(t(inp.k), t(inp.v), t(inp.slot_mapping))
     out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
-                             t(inp.seq_lens_after))
+                             t(inp.seq_lens_after), variant=variant)
     torch.cuda.synchronize()
     assert cache.read_device_error() == 0
     kp, vp = orc.append_kv(c.k_pages, c.v_pages, inp.U_k, inp.W_v, inp.k, inp.v,
@@ -28,28 +31,41 @@ def _run(inp):
     return out.cpu().numpy(), ref
 
 
-def test_tiny_prefill_ragged_chunks():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_tiny_prefill_ragged_chunks(variant):
     inp = wl.make_prefill_inputs(TINY, [0, 37, 64, 5], [40, 21, 16, 0], seed=41, fill=np.nan)
-    out, ref = _run(inp)
-    assert_close(out, ref, what="tiny prefill")
+    out, ref = _run(inp, variant)
+    assert_close(out, ref, what=f"tiny prefill ({variant})")
 
 
-def test_main_prefill_small():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_main_prefill_small(variant):
     inp = wl.make_prefill_inputs(MAIN, [100, 256], [48, 64], seed=42, fill=np.nan)
-    out, ref = _run(inp)
-    assert_close(out, ref, what="main prefill")
+    out, ref = _run(inp, variant)
+    assert_close(out, ref, what=f"main prefill ({variant})")
 
 
-def test_main_prefill_multi_tile_chunks():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_main_prefill_multi_tile_chunks(variant):
     """Chunks longer than one 128-row tile, priors off block boundaries, a zero chunk."""
     inp = wl.make_prefill_inputs(MAIN, [300, 0, 17, 40], [200, 130, 0, 129], seed=43,
                                  fill=np.nan)
-    out, ref = _run(inp)
-    assert_close(out, ref, what="main prefill multi-tile")
+    out, ref = _run(inp, variant)
+    assert_close(out, ref, what=f"main prefill multi-tile ({variant})")
 
 
-def test_prefill_is_deterministic():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_is_deterministic(variant):
     inp = wl.make_prefill_inputs(MAIN, [64, 250], [100, 37], seed=44)
-    a, _ = _run(inp)
-    b, _ = _run(inp)
+    a, _ = _run(inp, variant)
+    b, _ = _run(inp, variant)
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_prefill_variants_agree_on_a_long_chunk():
+    """Above the crossover both formulations give the oracle's result."""
+    inp = wl.make_prefill_inputs(MAIN, [512, 77], [300, 260], seed=45, fill=np.nan)
+    a, ref = _run(inp, "rank")
+    b, _ = _run(inp, "reconstruct")
+    assert_close(a, ref, what="rank")
+    assert_close(b, ref, what="reconstruct")
