@@ -412,7 +412,7 @@ def run_prefill(args):
     from rank_compressed_paged_gb300 import PagedCoeffCache
     from rank_compressed_paged_gb300 import build as _build
     _build.build()
-    B, prior, chunk = args.prefill_batch, 4096, 256
+    B, prior, chunk = args.prefill_batch, args.prefill_prior, args.prefill_chunk
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     after = np.full(B, prior + chunk, np.int32)
@@ -471,7 +471,7 @@ def run_prefill(args):
     kern_f = attn_f if variant == "rank" else prefill_recon_flops(prior, chunk, B)
     peak_tf, kind = measured_tensor_peak()
     line = {
-        "metric": "chunked-prefill ms/step & algorithmic TFLOP/s at B=16, prior 4096 + chunk 256",
+        "metric": f"chunked-prefill ms/step & algorithmic TFLOP/s at B={B}, prior {prior} + chunk {chunk}",
         "variant": variant,
         "value": round((attn_f + app_f) / (step_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
         "ms_per_step": round(step_ms, 3), "steps": args.steps, "warmup": max(args.warmup, 3),
@@ -508,6 +508,8 @@ def main():
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
     ap.add_argument("--prefill-batch", type=int, default=16)
     ap.add_argument("--prefill-variant", choices=["auto", "rank", "reconstruct"], default="auto")
+    ap.add_argument("--prefill-prior", type=int, default=4096)
+    ap.add_argument("--prefill-chunk", type=int, default=256)
     args = ap.parse_args()
     BATCH, SEQ = args.batch, args.seq_len
     rank, world, local_rank = dist_env()

@@ -49,17 +49,19 @@ struct PfSmem {
   static constexpr int K_BYTES = C::KT * 128;           // key coefficients of one tile
   static constexpr int V_BYTES = C::KT * VN * 2;        // value tile
   static constexpr int STAGE = K_BYTES + V_BYTES;
+  static constexpr int NS = RECON ? 3 : 2;              // key/value pipeline stages
   static constexpr int P_BYTES = 128 * C::KT * 2;
   static constexpr int ST_OFF = 2 * Q_BYTES;            // q~ hi at 0, q~ lo at Q_BYTES
-  static constexpr int P_OFF = ST_OFF + 2 * STAGE;
+  static constexpr int P_OFF = ST_OFF + NS * STAGE;
   static constexpr int ZH_OFF = ST_OFF;                 // epilogue reuses the stage memory
   static constexpr int ZL_OFF = ZH_OFF + 128 * C::RQ * 2;
   static constexpr int W_OFF = ZL_OFF + 128 * C::RQ * 2;
   static constexpr int W_BYTES = C::RQ * S::D * 2;
   static constexpr int END = (RECON || P_OFF + P_BYTES > W_OFF + W_BYTES) ? P_OFF + P_BYTES
                                                                              : W_OFF + W_BYTES;
-  static constexpr int BAR_OFF = END;                   // 17 mbarriers
-  static constexpr int MISC_OFF = BAR_OFF + 17 * 8;     // tmem slot, abort flag
+  static constexpr int NBAR = 9 + 4 * NS;
+  static constexpr int BAR_OFF = END;                   // NBAR mbarriers
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // tmem slot, abort flag
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr int RPC = 128 / NQ;                  // output rows each slice CTA sums
@@ -83,18 +85,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
+  constexpr int NS = L::NS;
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;      // [2] key half of a stage landed
-  uint64_t* v_full = bars + 3;      // [2] value half of a stage landed
-  uint64_t* k_empty = bars + 5;     // [2] score MMA of the stage's tile done
-  uint64_t* v_empty = bars + 7;     // [2] value MMA of the stage's tile done
-  uint64_t* s_full = bars + 9;      // [2] scores of a tile in TMEM
-  uint64_t* p_full = bars + 11;     // softmax weights written (4 warps)
-  uint64_t* pv_done = bars + 12;
-  uint64_t* acc_done = bars + 13;
-  uint64_t* zq_full = bars + 14;
-  uint64_t* w_full = bars + 15;
-  uint64_t* o_done = bars + 16;
+  uint64_t* k_full = bars + 1;              // [NS] key half of a stage landed
+  uint64_t* v_full = k_full + NS;           // [NS] value half of a stage landed
+  uint64_t* k_empty = v_full + NS;          // [NS] score MMA of the stage's tile done
+  uint64_t* v_empty = k_empty + NS;         // [NS] value MMA of the stage's tile done
+  uint64_t* s_full = v_empty + NS;          // [2] scores of a tile in TMEM
+  uint64_t* p_full = s_full + 2;            // softmax weights written (4 warps)
+  uint64_t* pv_done = p_full + 1;
+  uint64_t* acc_done = pv_done + 1;
+  uint64_t* zq_full = acc_done + 1;
+  uint64_t* w_full = zq_full + 1;
+  uint64_t* o_done = w_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -116,13 +119,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
-      mbar_init(&s_full[s], 1);
     }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(p_full, 4);
     mbar_init(pv_done, 1);
     mbar_init(acc_done, 1);
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int jb = 0; jb < BPT; ++jb) nxt[jb] = jb < nblk ? table[jb] : -1;
       for (int j = 0; j < nkt; ++j) {
-        const int s = j & 1;
+        const int s = j % NS;
         int32_t phys[BPT];
         int nload = 0;
 #pragma unroll
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint8_t* kst = sm + L::ST_OFF + s * L::STAGE;
         uint8_t* vst = kst + L::K_BYTES;
         if (keys) {
-          if (j >= 2 && !mbar_wait(&k_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
+          if (j >= NS && !mbar_wait(&k_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err)) break;
           mbar_arrive_expect_tx(&k_full[s], nload * 2048);
 #pragma unroll 1
           for (int jb = 0; jb < BPT; ++jb)
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               tma_load_2d(kst + jb * 2048, &kp_map, 0, (phys[jb] * H + h) * kBlockSize, &k_full[s]);
         } else if constexpr (RECON) {
           // V^ rows of the request are contiguous: one 64-column box of 128 keys per group
-          if (j >= 2 && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
+          if (j >= NS && !mbar_wait(&v_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err)) break;
           mbar_arrive_expect_tx(&v_full[s], NG * KT * 128);
           const int64_t vrow = p.vcum[b] * kBlockSize + static_cast<int64_t>(j) * KT;
 #pragma unroll
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tma_load_2d(vst + g * KT * 128, &vp_map, h * D + g * 64, static_cast<int32_t>(vrow),
                         &v_full[s]);
         } else {
-          if (j >= 2 && !mbar_wait(&v_empty[s], ((j >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
+          if (j >= NS && !mbar_wait(&v_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err)) break;
           mbar_arrive_expect_tx(&v_full[s], nload * NG * 2048);
 #pragma unroll 1
           for (int jb = 0; jb < BPT; ++jb) {
@@ -240,9 +244,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       uint64_t t_idle = 0;
       while (ok && jp < nkt) {
         bool progress = false;
-        if (js < nkt && js <= jp + 1 && mbar_test_wait(&k_full[js & 1], (js >> 1) & 1)) {
+        if (js < nkt && js <= jp + 1 && mbar_test_wait(&k_full[js % NS], (js / NS) & 1)) {
           tc_fence_after();
-          const uint32_t ka = smem_u32(sm + L::ST_OFF + (js & 1) * L::STAGE);
+          const uint32_t ka = smem_u32(sm + L::ST_OFF + (js % NS) * L::STAGE);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = make_sdesc(ka + kk * 32, 16, 1024, kSwizzle128B);
@@ -252,14 +256,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                      make_sdesc(qa + L::Q_BYTES + kk * 32, 16, 1024, kSwizzle128B), bd, id_s, 1u);
           }
           umma_commit(&s_full[js & 1]);
-          umma_commit(&k_empty[js & 1]);
+          umma_commit(&k_empty[js % NS]);
           ++js;
           progress = true;
         }
         if (jp < js && mbar_test_wait(p_full, jp & 1) &&
-            mbar_test_wait(&v_full[jp & 1], (jp >> 1) & 1)) {
+            mbar_test_wait(&v_full[jp % NS], (jp / NS) & 1)) {
           tc_fence_after();
-          const uint32_t va = smem_u32(sm + L::ST_OFF + (jp & 1) * L::STAGE + L::K_BYTES);
+          const uint32_t va = smem_u32(sm + L::ST_OFF + (jp % NS) * L::STAGE + L::K_BYTES);
 #pragma unroll
           for (int ks = 0; ks < KT / 16; ++ks) {
             const uint64_t ad = make_sdesc(pa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024,
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             umma_f16(tmem + 256, ad, bd, id_pv, (jp > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(pv_done);
-          umma_commit(&v_empty[jp & 1]);
+          umma_commit(&v_empty[jp % NS]);
           ++jp;
           progress = true;
         }
@@ -329,41 +333,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_wait_ld();
       }
       const bool full_tile = __all_sync(0xffffffffu, lim >= KT - 1);   // below the diagonal
-      // row max and row sum as 8 independent partial reductions (no 128-long chains)
-      float mx = -INFINITY;
-      if (ok) {
-        float m8[8];
+      // masked columns (diagonal tiles, rows past the chunk, a failed wait) become -inf, so
+      // the max and the exponentials below need no per-element test (exp2(-inf) = 0)
+      if (!ok || !full_tile) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
+        for (int c = 0; c < KT; ++c) sv[c] = (ok && c <= lim) ? sv[c] : -INFINITY;
+      }
+      // row max: four independent chains of three-input maxima
+      float mx;
+      {
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < KT; ++c)
-          m8[c & 7] = fmaxf(m8[c & 7], (full_tile || c <= lim) ? sv[c] : -INFINITY);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mx = fmaxf(mx, m8[q]);
+        for (int c = 0; c < KT; c += 8) {
+          m4[0] = max3f(m4[0], sv[c], sv[c + 1]);
+          m4[1] = max3f(m4[1], sv[c + 2], sv[c + 3]);
+          m4[2] = max3f(m4[2], sv[c + 4], sv[c + 5]);
+          m4[3] = max3f(m4[3], sv[c + 6], sv[c + 7]);
+        }
+        mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
       }
       const float m_new = (mx > m_run + kPfRescale) ? mx : m_run;
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
       uint32_t packed[KT / 2];
-      float rsum = 0.f;
+      float rsum;
       {
         const float msub = (m_new == -INFINITY) ? 0.f : m_new;   // rows with no valid key
-        float s8[8];
+        const float2 msub2 = make_float2(msub, msub);
+        float2 s4[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) s8[q] = 0.f;
-        // the row sum is taken in fp32 before the weights are rounded to fp16
+        for (int q = 0; q < 4; ++q) s4[q] = make_float2(0.f, 0.f);
+        // the row sum is taken in fp32 before the weights are rounded to fp16; pairs of
+        // columns go through the packed fp32x2 add / subtract
 #pragma unroll
         for (int c = 0; c < KT; c += 2) {
-          float p0 = fast_exp2(sv[c] - msub), p1 = fast_exp2(sv[c + 1] - msub);
-          if (!full_tile || !ok) {
-            p0 = (ok && c <= lim) ? p0 : 0.f;
-            p1 = (ok && c + 1 <= lim) ? p1 : 0.f;
-          }
-          s8[(c >> 1) & 7] += p0 + p1;
-          const __half2 hp = __floats2half2_rn(p0, p1);
+          const float2 d = sub_f32x2(make_float2(sv[c], sv[c + 1]), msub2);
+          const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+          s4[(c >> 1) & 3] = add_f32x2(s4[(c >> 1) & 3], pp);
+          const __half2 hp = __floats2half2_rn(pp.x, pp.y);
           packed[c / 2] = *reinterpret_cast<const uint32_t*>(&hp);
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) rsum += s8[q];
+        const float2 t2 = add_f32x2(add_f32x2(s4[0], s4[1]), add_f32x2(s4[2], s4[3]));
+        rsum = t2.x + t2.y;
       }
       // the previous tile's value MMA must be done before P is overwritten / Z rescaled
       if (j > 0) ok = mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.dev_err) && ok;
@@ -400,8 +410,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (j * KT + KT > Lb) {
         // tokens past the end of the request: zero their value rows so that whatever the
         // slots hold (or stale bytes of skipped pages) never meet a zero weight as 0 * NaN
-        ok = mbar_wait(&v_full[s], (j >> 1) & 1, abort_flag, p.dev_err) && ok;
-        uint8_t* vst = sm + L::ST_OFF + s * L::STAGE + L::K_BYTES;
+        ok = mbar_wait(&v_full[j % NS], (j / NS) & 1, abort_flag, p.dev_err) && ok;
+        uint8_t* vst = sm + L::ST_OFF + (j % NS) * L::STAGE + L::K_BYTES;
         const int first = Lb - j * KT > 0 ? Lb - j * KT : 0;
         const int nrow = KT - first;
         for (int idx = threadIdx.x - 64; idx < nrow * NG * 8; idx += 128) {   // warps 2-5
