@@ -35,7 +35,8 @@ struct rcp_cache {
   CUtensorMap tmap_v;       // V pages as [num_blocks*16][R], 64 x 16 boxes (decode A operand)
   CUtensorMap tmap_wv_k;    // W_v as [R][H*d], 64 x 128 boxes (append: K-major A)
   CUtensorMap tmap_wv_mn;   // W_v as [R][H*d], 64 x 64 boxes (up-projection: MN-major A)
-  CUtensorMap tmap_uk;      // U_k as [H*r_k][d], 64 x 128 boxes (append: K-major A)
+  CUtensorMap tmap_uk;      // U_k as [H*r_k][d], 64 x 128 boxes (query projection: A)
+  CUtensorMap tmap_uk64;    // U_k as [H*r_k][d], 64 x 64 boxes (append key pairs: A)
   CUtensorMap tmap_kp;      // K pages as [num_blocks*H*16][r_k], 64 x 16 boxes (prefill B)
   // optional events recorded around the split-K attention kernel
   cudaEvent_t prof_start;
@@ -120,6 +121,9 @@ rcp_status ensure_device(rcp_cache* c) {
       !encode_2d(&c->tmap_uk, c->U_k, g.head_dim,
                  static_cast<uint64_t>(g.num_heads) * g.rank_k, static_cast<uint64_t>(g.head_dim) * 2,
                  64, 128) ||
+      !encode_2d(&c->tmap_uk64, c->U_k, g.head_dim,
+                 static_cast<uint64_t>(g.num_heads) * g.rank_k, static_cast<uint64_t>(g.head_dim) * 2,
+                 64, 64) ||
       !encode_2d(&c->tmap_kp, c->k_pages, g.rank_k,
                  static_cast<uint64_t>(g.num_blocks) * g.num_heads * 16,
                  static_cast<uint64_t>(g.rank_k) * 2, 64, 16))
@@ -439,8 +443,8 @@ rcp_status rcp_append_kv(rcp_cache* c, const void* k, const void* v, const int64
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e =
       c->shape == kShapeMain
-          ? rcp::launch_append_gemm<ShapeMain>(c->tmap_wv_k, c->tmap_uk, vmap, kmap, p, s)
-          : rcp::launch_append_gemm<ShapeTiny>(c->tmap_wv_k, c->tmap_uk, vmap, kmap, p, s);
+          ? rcp::launch_append_gemm<ShapeMain>(c->tmap_wv_k, c->tmap_uk64, vmap, kmap, p, s)
+          : rcp::launch_append_gemm<ShapeTiny>(c->tmap_wv_k, c->tmap_uk64, vmap, kmap, p, s);
   return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
 }
 

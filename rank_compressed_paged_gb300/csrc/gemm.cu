@@ -10,9 +10,11 @@
 //
 //   append, value job:  A = W_v rows [m0, m0+128) (K-major over H*d), B = v tokens,
 //                       D[r][t] -> V page [slot_t / 16][slot_t % 16][m0 + r]
-//   append, key job:    A = U_k rows [h*r_k, h*r_k + 128) (K-major over d; rows past
-//                       r_k are ignored), B = k tokens of head h,
-//                       D[k][t] -> K page [slot_t / 16][h][slot_t % 16][k], k < r_k
+//   append, key job:    two heads h, h+1 at once as a block-diagonal product (K = 2d):
+//                       A = [U_k,h 0; 0 U_k,h+1] (64-row boxes; the zero quadrants are
+//                       boxes past the end of U_k, which the copy fills with zeros),
+//                       B = k tokens of heads h and h+1 (adjacent columns),
+//                       D[64 i + k][t] -> K page [slot_t / 16][h + i][slot_t % 16][k]
 //   up-projection:      A = W_v[:, h*d:(h+1)*d]^T (MN-major), B = z_hi and z_lo (the
 //                       fp16 high / low parts of the merged weighted coefficient sums),
 //                       D[j][q] = o_{q,h,j}, written as fp16.
@@ -88,7 +90,8 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank) {
   const int cluster = blockIdx.x / KS;
   if constexpr (MODE == kModeAppend) {
     constexpr int NM = (S::R + 127) / 128;
-    constexpr int NKG = (S::H + KS - 1) / KS;
+    constexpr int NP = S::H / 2;                 // head pairs
+    constexpr int NKG = (NP + KS - 1) / KS;
     constexpr int KBV = S::H * S::D / 64;
     constexpr int KBK = S::D / 64;
     const int tile = cluster / (NM + NKG);
@@ -103,13 +106,13 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank) {
       j.b_x = j.kb0 * 64; j.b_y = j.n0; j.b_step_x = 64;
       j.reduce = KS > 1;
     } else {
-      const int h = (sub - NM) * KS + static_cast<int>(rank);
-      j.kind = h < S::H ? 1 : -1;
-      j.m0 = h;
+      const int pr = (sub - NM) * KS + static_cast<int>(rank);
+      j.kind = pr < NP ? 1 : -1;
+      j.m0 = 2 * pr;                             // first head of the pair
       j.kb0 = 0;
-      j.kb1 = KBK;
-      j.a_x = 0; j.a_y = h * S::RK; j.a_step_x = 64; j.a_step_y = 0;
-      j.b_x = h * S::D; j.b_y = j.n0; j.b_step_x = 64;
+      j.kb1 = 2 * KBK;
+      j.a_x = 0; j.a_y = j.m0 * S::RK; j.a_step_x = 64; j.a_step_y = 0;
+      j.b_x = j.m0 * S::D; j.b_y = j.n0; j.b_step_x = 64;
       j.reduce = false;
     }
   } else if constexpr (MODE == kModeQproj) {
@@ -182,8 +185,11 @@ __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j
   if (j.kind == 0) {
     const int r = j.m0 + row;
     if (r < S::R) static_cast<__half*>(p.v_pages)[d + r] = __float2half_rn(v);
-  } else if (row < S::RK) {
-    static_cast<__half*>(p.k_pages)[d + row] = __float2half_rn(v);
+  } else {
+    // rows 0..63 belong to head m0, rows 64..127 to head m0 + 1 (next head in the page)
+    const int hh = row >> 6, rr = row & 63;
+    if (rr < S::RK)
+      static_cast<__half*>(p.k_pages)[d + hh * kBlockSize * S::RK + rr] = __float2half_rn(v);
   }
 }
 
@@ -239,6 +245,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // W_v^T slice: two 64(j) x 64(r) boxes (MN-major atoms), rows r = k
       tma_load_2d(st, amap, j.a_x, j.a_y + kb * j.a_step_y, &full[s]);
       tma_load_2d(st + kABytes / 2, amap, j.a_x + 64, j.a_y + kb * j.a_step_y, &full[s]);
+    } else if (MODE == kModeAppend && j.kind == 1) {
+      // block-diagonal pair: k-blocks [0, d/64) meet head m0's rows (top), the rest head
+      // m0 + 1's (bottom); the other half is a box past the last row of U_k (zeros)
+      constexpr int KBK = S::D / 64, OOB = S::H * S::RK;
+      const int half = kb / KBK, kk = kb % KBK;
+      tma_load_2d(st, amap, kk * 64, half == 0 ? j.m0 * S::RK : OOB, &full[s]);
+      tma_load_2d(st + kABytes / 2, amap, kk * 64, half == 1 ? (j.m0 + 1) * S::RK : OOB, &full[s]);
     } else {
       tma_load_2d(st, amap, j.a_x + kb * j.a_step_x, j.a_y, &full[s]);
     }
@@ -442,14 +455,14 @@ cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
   constexpr int NM = (S::R + 127) / 128;
   if (ap.T <= 256) {
     constexpr int KS = AppendCfg<S>::KS_SMALL;
-    constexpr int NKG = (S::H + KS - 1) / KS;
+    constexpr int NKG = (S::H / 2 + KS - 1) / KS;
     const int tiles = (ap.T + 63) / 64;
     return launch_cluster(gemm_kernel<S, kModeAppend, 64, KS, 4>, tiles * (NM + NKG) * KS, KS,
                           GemmSmem<64, KS, 1, 4>::ALLOC, stream, true, w_v, u_k, v_rows, k_rows, p);
   }
   // many tokens: 256-token tiles, no split
   const int tiles = (ap.T + 255) / 256;
-  return launch_cluster(gemm_kernel<S, kModeAppend, 256, 1, 4>, tiles * (NM + S::H), 1,
+  return launch_cluster(gemm_kernel<S, kModeAppend, 256, 1, 4>, tiles * (NM + S::H / 2), 1,
                         GemmSmem<256, 1, 1, 4>::ALLOC, stream, true, w_v, u_k, v_rows, k_rows, p);
 }
 
