@@ -135,8 +135,9 @@ rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_c
                             void* out, void* workspace, size_t workspace_bytes,
                             rcp_stream stream);
 
-/* Chunked prefill, reconstructing variant (Proxima page, "Per-prefill-chunk attention":
- * the prefill path rebuilds dense values from the coefficients).  Same arguments, layout and
+/* Chunked prefill, reconstructing variant (Proxima page, "Per-prefill-chunk attention",
+ * whose prefill kernel expands compressed keys per query tile; here the joint value
+ * coefficients are the ones expanded, once per key).  Same arguments, layout and
  * results as rcp_prefill_attn, up to rounding: the values of every cached key of the
  * requests with chunk rows are first reconstructed as V^ = C_v W_v (fp32 accumulation,
  * stored fp16) and the attention then runs on V^ with O = P V^ per head.  Cheaper than

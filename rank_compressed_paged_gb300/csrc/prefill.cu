@@ -17,6 +17,11 @@
 // W_v[:, h*d:(h+1)*d] (tcgen05 again); the slices of one (request, head, tile) form a
 // thread-block cluster and sum their partial outputs through distributed shared memory.
 //
+// The reconstructing variant (RECON) attends V^ = C_v W_v rows of head h, rebuilt once per
+// key by the reconstruction GEMM: O += P V^_h (M=128 x N=d x K=128) in TMEM, no rank slices,
+// and the softmax warps write O / l straight to the output; its key/value ring has three
+// stages.
+//
 // Warps: 0 copies queries and key tiles, 6 copies value tiles and the W_v slice (two
 // independent streams: a key stage is freed by its score MMA, a value stage by its value
 // MMA), 1 issues the MMAs (and owns TMEM), 2-5 run the softmax and the epilogue (warp w

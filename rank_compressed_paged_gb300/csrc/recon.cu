@@ -1,10 +1,12 @@
 // Value reconstruction for the reconstructing chunked prefill: V^ = C_v W_v for every
 // cached key of the requests that have chunk rows, on tensor cores.
 //
-// The Proxima page's prefill ("Per-prefill-chunk attention") reconstructs dense values
-// from the joint coefficients before the attention; with R = 1024 and d = 128 that costs
-// R*H*d multiply-adds per key once, against R per (query row, key, head) in rank space,
-// so it wins once a chunk has more than R*d/(R-d) ~ 146 rows per request.
+// The Proxima page's prefill kernel ("Per-prefill-chunk attention") expands compressed K
+// from its low-rank basis per query tile.  Here the keys stay in rank space (r_k = 64 per
+// head is cheaper than d = 128) and the joint value coefficients are expanded instead:
+// with R = 1024 and d = 128 that costs R*H*d multiply-adds per key once, against R per
+// (query row, key, head) in rank space, so it does less work once a chunk has more than
+// R*d/(R-d) ~ 146 rows per request.
 //
 // The keys of all such requests, page after page in request order (prefix sums in
 // vcum), are the rows of one GEMM D[keys x H*d] = C_v[keys x R] * W_v[R x H*d]:
