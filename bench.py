@@ -439,7 +439,8 @@ def run_prefill(args):
 
     variant = args.prefill_variant
     if variant == "auto":
-        variant = "reconstruct" if chunk >= cache.prefill_crossover_rows() else "rank"
+        from rank_compressed_paged_gb300 import RECONSTRUCT_MIN_CHUNK
+        variant = "reconstruct" if chunk >= RECONSTRUCT_MIN_CHUNK else "rank"
     if variant == "reconstruct":
         ws = cache.workspace(T, cache.reconstruct_workspace_bytes(T, B, table.shape[1]))
 

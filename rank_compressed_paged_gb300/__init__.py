@@ -18,6 +18,7 @@ from . import _lib
 from ._lib import RcpError  # noqa: F401
 
 BLOCK_SIZE = 16
+RECONSTRUCT_MIN_CHUNK = 16   # mean chunk rows from which prefill_attn(variant="auto") rebuilds V
 
 
 def _ptr(t) -> int:
@@ -169,15 +170,17 @@ class PagedCoeffCache:
         """q: [sum chunk][H][d] fp16; cu_chunk_lens: [B+1] int32; seq_lens include the chunk.
 
         variant: "rank" (joint-coefficient contraction per head), "reconstruct" (dense values
-        C_v W_v rebuilt once per key), or "auto": reconstruct when the mean chunk length
-        reaches the library's crossover."""
+        C_v W_v rebuilt once per key), or "auto": reconstruct when chunks average at least
+        RECONSTRUCT_MIN_CHUNK rows.  The multiply-add count favours reconstruction above
+        prefill_crossover_rows() (147 for R = 1024, d = 128); measured on GB300 it is the
+        faster variant from 16-row chunks on (priors 4096 to 32768), because a chunk shorter
+        than one 128-row tile costs the rank-space kernel a whole tile per R slice."""
         import torch
         rows = int(q.shape[0])
         B = int(seq_lens.shape[0])
         mb = int(block_table.shape[1])
         if variant == "auto":
-            variant = "reconstruct" if B > 0 and rows >= B * self.prefill_crossover_rows() \
-                else "rank"
+            variant = "reconstruct" if B > 0 and rows >= B * RECONSTRUCT_MIN_CHUNK else "rank"
         if variant not in ("rank", "reconstruct"):
             raise ValueError(f"unknown prefill variant {variant!r}")
         if out is None:
