@@ -27,6 +27,9 @@ definitions used here are:
 All arithmetic is fp64 on the stored fp16 values; results are fp64 (fp16 only where the
 definition stores fp16: the coefficients an append writes).
 
+fp8 pages (E4M3 codes, see e4m3_encode) hold the same coefficients rounded to E4M3 instead
+of fp16; decode over them is the decode above on the decoded values.
+
 Pins (see tests/test_oracle.py): identity factors reduce decode to textbook multi-head
 attention computed by a library routine; explicit reconstruction K = C_k U_k, V = C_v W_v
 followed by library attention agrees to 1e-12; physical block permutation leaves outputs
@@ -132,6 +135,64 @@ def append_kv(k_pages, v_pages, U_k, W_v, k, v, slot_mapping, block_size: int = 
         for h in range(H):
             kp[blk, h, off, :] = (U[h] @ k[i, h]).astype(np.float16)
         vp[blk, off, :] = (W @ v[i].reshape(H * d)).astype(np.float16)
+    return kp, vp
+
+
+# ---------------------------------------------------------------------------------------
+# fp8 coefficient pages.  E4M3 as defined by the OCP 8-bit floating point format (the
+# "E4M3" encoding, also NVIDIA's e4m3): sign bit, 4 exponent bits with bias 7, 3 mantissa
+# bits; exponent field 0 holds subnormals m * 2^-9; no infinities; S.1111.111 is NaN, so
+# the largest finite magnitude is S.1111.110 = 1.75 * 2^8 = 448.
+
+def e4m3_decode(codes) -> np.ndarray:
+    """fp64 values of E4M3 codes (uint8 array)."""
+    c = np.asarray(codes).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    mag = np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+    return sign * mag
+
+
+_E4M3_POS = e4m3_decode(np.arange(0x7F))        # codes 0x00 .. 0x7E, ascending, 0 .. 448
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 code to each value (ties to the even code), magnitudes above 448
+    saturating to 448 (the "satfinite" conversion), NaN to 0x7F; the sign of zero kept."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 1, 0x7E)
+    lo = hi - 1
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a >= 448.0, 0x7E, code)
+    code = np.where(a == 0.0, 0, code)
+    code = code | np.where(np.signbit(x), 0x80, 0)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def append_kv_fp8(k_pages, v_pages, U_k, W_v, k, v, slot_mapping, block_size: int = 16):
+    """append_kv for E4M3 pages: the same projections, rounded from fp64 to E4M3 codes
+    (uint8 pages, same layout).  Read the pages back with e4m3_decode."""
+    kp = np.array(k_pages, copy=True)
+    vp = np.array(v_pages, copy=True)
+    U = _f64(U_k)
+    W = _f64(W_v)
+    k = _f64(k)
+    v = _f64(v)
+    T, H, d = k.shape
+    for i in range(T):
+        s = int(slot_mapping[i])
+        if s < 0:
+            continue
+        blk, off = s // block_size, s % block_size
+        for h in range(H):
+            kp[blk, h, off, :] = e4m3_encode(U[h] @ k[i, h])
+        vp[blk, off, :] = e4m3_encode(W @ v[i].reshape(H * d))
     return kp, vp
 
 

@@ -277,3 +277,95 @@ def test_workload_generator_is_seeded():
     U = a.U_k.astype(np.float64)
     for h in range(U.shape[0]):
         np.testing.assert_allclose(U[h] @ U[h].T, np.eye(U.shape[1]), atol=3e-3)
+
+
+# ------------------------------------------------------------------------- E4M3 pages
+# Values fixed by the E4M3 format definition (OCP 8-bit floating point, "E4M3"): bias 7,
+# three mantissa bits, subnormals m * 2^-9, S.1111.111 = NaN, max finite 448.
+E4M3_TABLE = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+              0x30: 0.5, 0x38: 1.0, 0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x77: 240.0,
+              0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+
+
+def test_e4m3_decode_matches_the_format_definition():
+    for code, val in E4M3_TABLE.items():
+        got = orc.e4m3_decode(np.array([code], np.uint8))[0]
+        assert got == val and np.signbit(got) == np.signbit(val), (hex(code), got, val)
+    assert np.isnan(orc.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    np.testing.assert_array_equal(orc.e4m3_encode(orc.e4m3_decode(codes)), codes)
+
+
+def test_e4m3_encode_rounds_to_nearest_even_and_saturates():
+    cases = {1.0625: 0x38,          # halfway 1.0 / 1.125 -> even mantissa (1.0)
+             1.1875: 0x3A,          # halfway 1.125 / 1.25 -> even mantissa (1.25)
+             1.07: 0x39, 2.0 ** -10: 0x00, 3 * 2.0 ** -10: 0x02,
+             448.0: 0x7E, 470.0: 0x7E, 1e9: 0x7E, -1e9: 0xFE, -1.0625: 0xB8}
+    for x, code in cases.items():
+        assert orc.e4m3_encode(np.array([x]))[0] == code, (x, hex(code))
+    assert orc.e4m3_encode(np.array([np.nan]))[0] == 0x7F
+
+
+def test_e4m3_encode_is_the_nearest_finite_code_brute_force():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal(3000) * np.exp(rng.uniform(-10, 6, 3000))
+    finite = orc.e4m3_decode(np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8))
+    got = orc.e4m3_decode(orc.e4m3_encode(x))
+    best = np.min(np.abs(np.clip(x, -448, 448)[:, None] - finite[None, :]), axis=1)
+    np.testing.assert_array_equal(np.abs(np.clip(x, -448, 448) - got), best)
+
+
+def test_e4m3_encode_agrees_with_torch_float8_in_range():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-12, 5, 20000))
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(orc.e4m3_encode(x), ref)
+
+
+def test_fp8_append_with_selection_factors_stores_the_inputs_rounded():
+    """Coordinate-selection factors make the fp8 append a rounding of the inputs."""
+    H, d, rk, R = 4, 64, 16, 64
+    rng = np.random.default_rng(16)
+    U, W = wl.selection_factors(rng, H, d, rk, R)
+    k = wl.fp16(rng.standard_normal((5, H, d)) * 200)   # some values past 448 saturate
+    v = wl.fp16(rng.standard_normal((5, H, d)))
+    slots = np.array([17, -1, 95, 0, 40], np.int64)
+    kp, vp = orc.append_kv_fp8(np.full((6, H, 16, rk), 0x55, np.uint8),
+                               np.full((6, 16, R), 0x55, np.uint8), U, W, k, v, slots, 16)
+    assert kp.dtype == np.uint8 and vp.dtype == np.uint8
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        for h in range(H):
+            cols = np.argmax(U[h] != 0, axis=1)
+            np.testing.assert_array_equal(kp[s // 16, h, s % 16],
+                                          orc.e4m3_encode(k[i, h, cols].astype(np.float64)))
+        colsv = np.argmax(W != 0, axis=1)
+        np.testing.assert_array_equal(vp[s // 16, s % 16],
+                                      orc.e4m3_encode(v[i].reshape(-1)[colsv].astype(np.float64)))
+    assert (kp == 0x7E).any() or (kp == 0xFE).any()      # saturation was exercised
+    written = {(int(s) // 16, int(s) % 16) for s in slots if s >= 0}
+    for blk in range(6):
+        for off in range(16):
+            if (blk, off) not in written:
+                assert (kp[blk, :, off] == 0x55).all() and (vp[blk, off] == 0x55).all()
+
+
+def test_fp8_decode_is_decode_on_the_decoded_pages():
+    """An fp8 cache holding E4M3 roundings of fp16 pages: the oracle's answer moves by at
+    most what E4M3 rounding allows (each coefficient within 2^-4 relative)."""
+    inp = wl.make_decode_inputs(wl.SHAPES["mha32"], [300, 77], seed=17)
+    c = inp.cache
+    k8 = orc.e4m3_decode(orc.e4m3_encode(c.k_pages.astype(np.float64)))
+    v8 = orc.e4m3_decode(orc.e4m3_encode(c.v_pages.astype(np.float64)))
+    rel_k = np.abs(k8 - c.k_pages) / np.maximum(np.abs(c.k_pages.astype(np.float64)), 2.0 ** -6)
+    assert rel_k.max() <= 2.0 ** -4 + 1e-12
+    o16 = orc.decode_attn(inp.q, c.k_pages, c.v_pages, inp.U_k, inp.W_v, c.block_table,
+                          c.seq_lens, 16)
+    o8 = orc.decode_attn(inp.q, k8, v8, inp.U_k, inp.W_v, c.block_table, c.seq_lens, 16)
+    rel = np.linalg.norm(o8 - o16) / np.linalg.norm(o16)
+    assert 1e-3 < rel < 0.1
