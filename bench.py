@@ -264,8 +264,15 @@ def run_ours(args, rank, world, local_rank):
     def td(x):
         return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
 
-    cache = PagedCoeffCache(H, d, SHAPE["rank_k"], SHAPE["rank_v"], w["kp"].shape[0], td(w["U"]),
-                            td(w["W"]), k_pages=w["kp"], v_pages=w["vp"])
+    kp_dev, vp_dev = w["kp"], w["vp"]
+    if args.pages == "fp8_e4m3":
+        # the same seeded coefficients stored as E4M3 codes (torch's float8 cast)
+        kp_dev = kp_dev.to(torch.float8_e4m3fn).view(torch.uint8)
+        vp_dev = vp_dev.to(torch.float8_e4m3fn).view(torch.uint8)
+        del w["kp"], w["vp"]
+        torch.cuda.empty_cache()
+    cache = PagedCoeffCache(H, d, SHAPE["rank_k"], SHAPE["rank_v"], kp_dev.shape[0], td(w["U"]),
+                            td(w["W"]), k_pages=kp_dev, v_pages=vp_dev, page_format=args.pages)
     q, nk, nv, slots = td(w["q"]), td(w["nk"]), td(w["nv"]), td(w["slots"])
     table, lens = td(w["table"]), td(w["seq_lens"])
     out = torch.empty_like(q)
@@ -348,12 +355,13 @@ def run_ours(args, rank, world, local_rank):
     step_ms, e2e_ms, kern_ms = reduce_max([step_ms, e2e_ms, kern_ms], world, dev)
     if rank != 0:
         return
-    coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"])
+    coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"],
+                                              1 if args.pages == "fp8_e4m3" else 2)
     value = job_gbs(coeff_bytes, world, step_ms)
     e2e_value = job_gbs(coeff_bytes, world, e2e_ms)
     peak, peak_kind = measured_peaks()
     achieved = coeff_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = ncu_traffic_per_launch()
+    traffic = ncu_traffic_per_launch() if args.pages == "fp16" else None
     # CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N=1)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -365,11 +373,12 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 4),
         "us_per_step": round(step_ms * 1e3, 1),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if args.pages == "fp16" else "e4m3 pages, f16/f32 arithmetic",
         "data": "synthetic",
         "config": {"workload": workload_name(), "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
                    "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16,
-                   "step": "append 1 token/seq + decode attention",
+                   "step": "append 1 token/seq + decode attention", "pages": args.pages,
                    "l2": "inputs larger than L2 (3.2 GB of pages per GPU), no flush",
                    "parallelism": f"replicas x{world}, batch-sharded, no collective"},
         "roofline": {"bound": "hbm", "kernel": "decode_main_kernel",
@@ -514,6 +523,8 @@ def main():
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
     ap.add_argument("--prefill-batch", type=int, default=16)
     ap.add_argument("--prefill-variant", choices=["auto", "rank", "reconstruct"], default="auto")
+    ap.add_argument("--pages", choices=["fp16", "fp8_e4m3"], default="fp16",
+                    help="decode page format (fp16 is the measured configuration)")
     ap.add_argument("--prefill-prior", type=int, default=4096)
     ap.add_argument("--prefill-chunk", type=int, default=256)
     args = ap.parse_args()

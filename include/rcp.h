@@ -11,8 +11,8 @@
  *
  * Memory layout (all device buffers are owned by the caller; the library never
  * allocates device memory; every pointer must be 16-byte aligned):
- *     K pages   [num_blocks][H][block_size][r_k]   fp16
- *     V pages   [num_blocks][block_size][R]        fp16
+ *     K pages   [num_blocks][H][block_size][r_k]   fp16 (or E4M3 bytes, see page_format)
+ *     V pages   [num_blocks][block_size][R]        fp16 (or E4M3 bytes)
  *     U_k       [H][r_k][d]                        fp16
  *     W_v       [R][H*d]   (column h*d + j = head h, element j)   fp16
  *     q, out    [rows][H][d]                       fp16
@@ -54,6 +54,13 @@ typedef enum rcp_status {
 #define RCP_DEVERR_BAD_LEN 4u     /* attention: seq_len < 0, > table capacity, or chunk > seq_len */
 #define RCP_DEVERR_TIMEOUT 8u     /* a pipeline wait exceeded its bound; results invalid */
 
+/* Element type of the K and V pages. */
+#define RCP_PAGES_FP16 0      /* IEEE fp16 coefficients */
+#define RCP_PAGES_FP8_E4M3 1  /* E4M3 codes (OCP 8-bit float: bias 7, 3 mantissa bits, max
+                                 448): the append rounds to nearest even and saturates to
+                                 +-448; half the bytes per token.  Decode only: the prefill
+                                 entry points return RCP_ERR_UNSUPPORTED for such a cache. */
+
 typedef struct rcp_cache_config {
   int32_t num_heads;   /* H */
   int32_t head_dim;    /* d */
@@ -61,6 +68,7 @@ typedef struct rcp_cache_config {
   int32_t rank_v;      /* R, joint value coefficients per token */
   int32_t block_size;  /* tokens per page; this build supports 16 */
   int64_t num_blocks;  /* physical blocks in the K and V page buffers */
+  int32_t page_format; /* RCP_PAGES_FP16 or RCP_PAGES_FP8_E4M3 */
 } rcp_cache_config;
 
 typedef struct rcp_cache rcp_cache;   /* opaque handle: borrowed pointers + host free list */

@@ -36,30 +36,38 @@ class PagedCoeffCache:
 
     Owns (as torch tensors) the K pages [num_blocks][H][16][r_k], V pages
     [num_blocks][16][R], the factors, a device error word and a reusable workspace; the
-    library handle borrows their pointers.
+    library handle borrows their pointers.  page_format "fp16" stores fp16 coefficients,
+    "fp8_e4m3" stores E4M3 codes (uint8 tensors; decode and append only).
     """
 
     def __init__(self, num_heads: int, head_dim: int, rank_k: int, rank_v: int,
-                 num_blocks: int, U_k, W_v, k_pages=None, v_pages=None, device=None):
+                 num_blocks: int, U_k, W_v, k_pages=None, v_pages=None, device=None,
+                 page_format: str = "fp16"):
         import torch
         lib = _lib.load()
         dev = U_k.device if device is None else torch.device(device)
+        fmt = {"fp16": _lib.RCP_PAGES_FP16, "fp8_e4m3": _lib.RCP_PAGES_FP8_E4M3}[page_format]
+        page_dtype = torch.float16 if fmt == _lib.RCP_PAGES_FP16 else torch.uint8
+        self.page_format = page_format
         self.shape = dict(num_heads=num_heads, head_dim=head_dim, rank_k=rank_k, rank_v=rank_v)
         self.num_blocks = int(num_blocks)
         self.U_k = U_k.contiguous()
         self.W_v = W_v.contiguous()
         if k_pages is None:
             k_pages = torch.zeros((num_blocks, num_heads, BLOCK_SIZE, rank_k),
-                                  dtype=torch.float16, device=dev)
+                                  dtype=page_dtype, device=dev)
         if v_pages is None:
-            v_pages = torch.zeros((num_blocks, BLOCK_SIZE, rank_v), dtype=torch.float16,
+            v_pages = torch.zeros((num_blocks, BLOCK_SIZE, rank_v), dtype=page_dtype,
                                   device=dev)
+        for pg in (k_pages, v_pages):
+            if pg.element_size() != (2 if fmt == _lib.RCP_PAGES_FP16 else 1):
+                raise ValueError(f"{page_format} pages need {page_dtype} elements, got {pg.dtype}")
         self.k_pages = k_pages
         self.v_pages = v_pages
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)
         self._ws = None
         self._cfg = _lib.CacheConfig(num_heads, head_dim, rank_k, rank_v, BLOCK_SIZE,
-                                     self.num_blocks)
+                                     self.num_blocks, fmt)
         h = ctypes.c_void_p()
         _lib.check("rcp_create_cache", lib.rcp_create_cache(
             ctypes.byref(self._cfg), _ptr(self.k_pages), _ptr(self.v_pages), _ptr(self.U_k),

@@ -25,7 +25,8 @@ RCP_DEVERR_TIMEOUT = 8
 class CacheConfig(ctypes.Structure):
     _fields_ = [("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("rank_k", ctypes.c_int32), ("rank_v", ctypes.c_int32),
-                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64)]
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64),
+                ("page_format", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -57,6 +58,8 @@ _SIG = {
 }
 
 RCP_NOALLOC_SCRATCH_BYTES = 64 << 20
+RCP_PAGES_FP16 = 0
+RCP_PAGES_FP8_E4M3 = 1
 
 _lib = None
 

@@ -200,6 +200,8 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   p.U_k = c->U_k;
   p.W_v = c->W_v;
   p.k_pages = c->k_pages;
+  p.v_pages = c->v_pages;
+  p.fp8_pages = c->cfg.page_format == RCP_PAGES_FP8_E4M3 ? 1 : 0;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.cu_chunk = cu_chunk;
@@ -222,6 +224,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   if (c->shape == kShapeMain) fill_ws<ShapeMain>(p, ws, nq);
   else fill_ws<ShapeTiny>(p, ws, nq);
   const bool pdl = c->prof_start == nullptr;
+  if (cu_chunk && p.fp8_pages) return RCP_ERR_UNSUPPORTED;   // prefill reads fp16 pages
   if (cu_chunk) {
     // chunked prefill: plan + fp16 rank-space queries, then the tiled tensor-core kernel
     const uint64_t hq = static_cast<uint64_t>(c->cfg.num_heads) * 64;
@@ -318,6 +321,8 @@ const char* rcp_status_string(rcp_status s) {
 
 rcp_status rcp_config_supported(const rcp_cache_config* cfg) {
   if (!cfg) return RCP_ERR_INVALID_ARG;
+  if (cfg->page_format != RCP_PAGES_FP16 && cfg->page_format != RCP_PAGES_FP8_E4M3)
+    return RCP_ERR_UNSUPPORTED;
   return shape_of(cfg) == kShapeNone ? RCP_ERR_UNSUPPORTED : RCP_OK;
 }
 
@@ -328,7 +333,7 @@ rcp_status rcp_create_cache(const rcp_cache_config* cfg, void* k_pages, void* v_
   *out = nullptr;
   if (cfg->num_blocks < 1 || cfg->num_blocks > (int64_t{1} << 26)) return RCP_ERR_INVALID_ARG;
   const int sh = shape_of(cfg);
-  if (sh == kShapeNone) return RCP_ERR_UNSUPPORTED;
+  if (sh == kShapeNone || rcp_config_supported(cfg) != RCP_OK) return RCP_ERR_UNSUPPORTED;
   if (!k_pages || !v_pages || !U_k || !W_v || !dev_error) return RCP_ERR_INVALID_ARG;
   if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(U_k) || !aligned16(W_v) ||
       (reinterpret_cast<uintptr_t>(dev_error) & 3u))
@@ -433,6 +438,7 @@ rcp_status rcp_append_kv(rcp_cache* c, const void* k, const void* v, const int64
   p.dev_err = c->dev_err;
   p.num_blocks = c->cfg.num_blocks;
   p.T = num_tokens;
+  p.fp8_pages = c->cfg.page_format == RCP_PAGES_FP8_E4M3 ? 1 : 0;
   // the new tokens' k and v as [T][H*d] B operands (64-token tiles up to 256 tokens)
   const uint64_t hd = static_cast<uint64_t>(c->cfg.num_heads) * c->cfg.head_dim;
   const uint32_t nt = num_tokens <= 256 ? 64 : 256;

@@ -24,6 +24,7 @@
 // row attends its causal prefix; here every chunk row is planned as its own query row).
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -214,25 +215,55 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
 }
 
 // ---------------------------------------------------------------------------- decode main
-template <class S>
+// F8: pages hold E4M3 codes.  K pages are scored straight from their bytes; V pages land
+// in raw stages and the compute warps widen them to fp16 in the swizzled layout the
+// tensor-core MMA reads (the layout the fp16 path's tensor-map copies produce).
+template <class S, bool F8>
 struct DecodeSmem {
-  static constexpr int KST = 2, VST = 2;
+  static constexpr int KST = F8 ? 3 : 2;                            // key page stages
+  static constexpr int VST = 2;                                     // fp16 V stages (MMA A)
+  static constexpr int VRS = F8 ? 3 : VST;                          // stages V copies land in
+  static constexpr int KP = F8 ? S::KPAGE_BYTES / 2 : S::KPAGE_BYTES;   // bytes per K page
+  static constexpr int VP = F8 ? S::VPAGE_BYTES / 2 : S::VPAGE_BYTES;   // bytes per V page
+  static constexpr int NBAR = 2 * KST + 2 * VRS + 4 + (F8 ? 2 * VST : 0);
   static constexpr int P_BYTES = S::HP * 16 * 2;
   static constexpr int V_OFF = 0;                                   // 1024-aligned stages
   static constexpr int K_OFF = V_OFF + VST * S::VSTAGE_BYTES;
-  static constexpr int P_OFF = K_OFF + KST * S::KPAGE_BYTES;
+  static constexpr int VR_OFF = K_OFF + KST * KP;                   // raw E4M3 V stages
+  static constexpr int P_OFF = VR_OFF + (F8 ? VRS * VP : 0);
   static constexpr int Q_OFF = P_OFF + 2 * P_BYTES;
   static constexpr int A_OFF = Q_OFF + S::H * S::RK * 4;            // alpha[2][HP]
   static constexpr int F_OFF = A_OFF + 2 * S::HP * 4;               // flags[2][4]
-  static constexpr int BAR_OFF = F_OFF + 32;                        // 12 mbarriers
-  static constexpr int MISC_OFF = BAR_OFF + 12 * 8;                 // tmem slot, abort flag
-  static constexpr int TOTAL = MISC_OFF + 16;
+  static constexpr int BAR_OFF = F_OFF + 64;                        // NBAR mbarriers
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;               // tmem slot, abort flag
+  static constexpr int INFO_OFF = MISC_OFF + 16;                    // valid tokens per stage:
+  static constexpr int TOTAL = INFO_OFF + (KST + VRS) * 4;          //   K stages, then V
   static constexpr int ALLOC = TOTAL + 1024;                        // base alignment slack
-  static_assert(S::KPAGE_BYTES % 128 == 0 && S::VSTAGE_BYTES % 1024 == 0, "alignment");
+  static_assert(KP % 128 == 0 && VP % 16 == 0 && S::VSTAGE_BYTES % 1024 == 0, "alignment");
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-constexpr int kDecodeThreads = 192;   // warp 0 copies, warp 1 MMA, warps 2-5 compute
+// Warp 0 copies, warp 1 issues the MMAs, warps 2 .. compute.
+// F8: eight compute warps (2-9; scoring E4M3 keys costs more per byte) and warps 10-11,
+// which widen the E4M3 V pages while the compute warps score.
+template <class S, bool F8>
+constexpr int decode_compute_warps() { return (F8 && S::H % 8 == 0) ? 8 : 4; }
+template <class S, bool F8>
+constexpr int decode_threads() { return 32 * (2 + decode_compute_warps<S, F8>() + (F8 ? 2 : 0)); }
+
+// Two E4M3 codes (low byte first) to an fp16 pair / fp32 pair; E4M3 values are exact in
+// fp16.  (Widening by integer bit moves instead measured slower: more instructions.)
+__device__ __forceinline__ uint32_t e4m3x2_to_half2_bits(uint16_t codes) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes),
+                                                   __NV_E4M3);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
+  const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes),
+                                                   __NV_E4M3);
+  return __half22float2(__half2(r));
+}
+
 constexpr float kRescaleThreshold = 8.f;   // log2 units: weights stay <= 2^8 before a rescale
 
 // Walks the requests that a CTA's block range crosses.
@@ -261,62 +292,66 @@ struct ReqWalker {
 };
 
 struct BlockInfo {
-  int64_t phys;
   int nvalid;      // tokens of this block that are attended (0 for a rejected block id)
   bool seg_first, seg_last;
 };
 
-__device__ __forceinline__ BlockInfo block_info(const AttnParams& p, const ReqWalker& w,
-                                                int64_t g, int64_t g0, int64_t g1) {
-  BlockInfo bi;
-  const int64_t j = g - w.bstart;
-  const int64_t row = p.qrow[w.b];
-  const int64_t phys = p.block_table[row * p.bt_stride + j];
-  const int32_t L = p.qlen[w.b];
-  const bool bad = phys < 0 || phys >= p.num_blocks;
-  bi.phys = bad ? 0 : phys;
-  const int64_t left = L - j * kBlockSize;
-  bi.nvalid = bad ? 0 : static_cast<int>(left < kBlockSize ? left : kBlockSize);
-  bi.seg_first = (g == g0) || (g == w.bstart);
-  bi.seg_last = (g == g1 - 1) || (g + 1 == w.bend);
-  return bi;
-}
 
-template <class S>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+template <class S, bool F8>
+__global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
     decode_main_kernel(const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
-  using L = DecodeSmem<S>;
-  constexpr int KST = L::KST, VST = L::VST, HP = S::HP;
+  using L = DecodeSmem<S, F8>;
+  constexpr int KST = L::KST, VST = L::VST, VRS = L::VRS, HP = S::HP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* vst = sm + L::V_OFF;
   uint8_t* kst = sm + L::K_OFF;
+  uint8_t* vraw = sm + L::VR_OFF;
   uint8_t* pbuf = sm + L::P_OFF;
   float* qs = reinterpret_cast<float*>(sm + L::Q_OFF);
   float* alpha_s = reinterpret_cast<float*>(sm + L::A_OFF);
   int* flags_s = reinterpret_cast<int*>(sm + L::F_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
-  uint64_t* kfull = bars + 0;
-  uint64_t* kempty = bars + 2;
-  uint64_t* vfull = bars + 4;
-  uint64_t* vempty = bars + 6;
-  uint64_t* pfull = bars + 8;
-  uint64_t* pfree = bars + 10;
+  uint64_t* kfull = bars;                 // [KST]
+  uint64_t* kempty = kfull + KST;         // [KST] the four compute warps scored the page
+  uint64_t* vfull = kempty + KST;         // [VRS] a V page landed
+  uint64_t* vempty = vfull + VRS;         // [VRS] its stage is free (MMA, or F8: widened)
+  uint64_t* pfull = vempty + VRS;         // [2]
+  uint64_t* pfree = pfull + 2;            // [2]
+  uint64_t* vcvt = pfree + 2;             // F8 [VST] fp16 V stage written by warps 6-7
+  uint64_t* vfree = vcvt + VST;           // F8 [VST] fp16 V stage read by its MMAs
+  constexpr int NTHR = decode_threads<S, F8>();
+  constexpr int NCW = decode_compute_warps<S, F8>();   // compute warps 2 .. NCW+1
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
+  // tokens of the block in each stage that are attended, published by the copy thread
+  // before it arms the stage's barrier (so a waiter sees it), so that no other warp
+  // reads the block table or lengths from global memory on its critical path
+  int* kinfo = reinterpret_cast<int*>(sm + L::INFO_OFF);
+  int* vinfo = kinfo + KST;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
 
   // prologue: nothing here reads what the previous kernel writes
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < KST; ++i) {
       mbar_init(&kfull[i], 1);
-      mbar_init(&kempty[i], 4);
+      mbar_init(&kempty[i], NCW);
+    }
+    for (int i = 0; i < VRS; ++i) {
       mbar_init(&vfull[i], 1);
-      mbar_init(&vempty[i], 1);
-      mbar_init(&pfull[i], 4);
+      mbar_init(&vempty[i], F8 ? 2 : 1);
+    }
+    if constexpr (F8) {
+      for (int i = 0; i < VST; ++i) {
+        mbar_init(&vcvt[i], 2);
+        mbar_init(&vfree[i], 1);
+      }
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pfull[i], NCW);
       mbar_init(&pfree[i], 1);
     }
     *abort_flag = 0;
@@ -328,12 +363,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
   // Zero both P buffers (padded head rows stay zero) and any part of a V stage that no
   // copy fills (value rank below a multiple of 128: those MMA rows are never stored).
-  for (int i = threadIdx.x; i < 2 * L::P_BYTES / 16; i += kDecodeThreads)
+  for (int i = threadIdx.x; i < 2 * L::P_BYTES / 16; i += NTHR)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0, 0, 0, 0);
   if constexpr (S::NBOX < 2 * S::NCHUNK) {
     constexpr int ZB = (2 * S::NCHUNK - S::NBOX) * 2048 / 16;
     for (int s = 0; s < VST; ++s)
-      for (int i = threadIdx.x; i < ZB; i += kDecodeThreads)
+      for (int i = threadIdx.x; i < ZB; i += NTHR)
         reinterpret_cast<uint4*>(vst + s * S::VSTAGE_BYTES + S::NBOX * 2048)[i] =
             make_uint4(0, 0, 0, 0);
   }
@@ -371,26 +406,35 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const bool bad = raw < 0 || raw >= p.num_blocks;
         if (bad) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
         const int64_t phys = bad ? 0 : raw;
+        const int64_t left = p.qlen[walk.b] - j * kBlockSize;
+        const int nvalid = bad ? 0 : static_cast<int>(left < kBlockSize ? left : kBlockSize);
         const int ks = static_cast<int>(it % KST);
         if (it >= KST && !mbar_wait(&kempty[ks], ((it / KST) - 1) & 1, abort_flag, p.dev_err)) break;
-        mbar_arrive_expect_tx(&kfull[ks], S::KPAGE_BYTES);
-        bulk_g2s_hint(kst + ks * S::KPAGE_BYTES, kpages + phys * S::KPAGE_BYTES, S::KPAGE_BYTES,
-                      &kfull[ks], pol);
+        kinfo[ks] = nvalid;
+        mbar_arrive_expect_tx(&kfull[ks], L::KP);
+        bulk_g2s_hint(kst + ks * L::KP, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
         ++nk;
-        const int vs = static_cast<int>(it % VST);
-        if (it >= VST && !mbar_wait(&vempty[vs], ((it / VST) - 1) & 1, abort_flag, p.dev_err)) break;
-        mbar_arrive_expect_tx(&vfull[vs], S::VPAGE_BYTES);
+        const int vs = static_cast<int>(it % VRS);
+        if (it >= VRS && !mbar_wait(&vempty[vs], ((it / VRS) - 1) & 1, abort_flag, p.dev_err)) break;
+        vinfo[vs] = nvalid;
+        mbar_arrive_expect_tx(&vfull[vs], L::VP);
+        if constexpr (F8) {
+          // the page's [16][R] codes, contiguous
+          bulk_g2s_hint(vraw + vs * L::VP, static_cast<const uint8_t*>(p.v_pages) + phys * L::VP,
+                        L::VP, &vfull[vs], pol);
+        } else {
 #pragma unroll 1
-        for (int bx = 0; bx < S::NBOX; ++bx)
-          tma_load_2d_hint(vst + vs * S::VSTAGE_BYTES + bx * 2048, &tmap_v, bx * 64,
-                           static_cast<int32_t>(phys * kBlockSize), &vfull[vs], pol);
+          for (int bx = 0; bx < S::NBOX; ++bx)
+            tma_load_2d_hint(vst + vs * S::VSTAGE_BYTES + bx * 2048, &tmap_v, bx * 64,
+                             static_cast<int32_t>(phys * kBlockSize), &vfull[vs], pol);
+        }
         ++nv;
       }
       if (*abort_flag) {   // let copies already in flight land before the CTA exits
         for (int64_t i = (nk > KST ? nk - KST : 0); i < nk; ++i)
           mbar_wait_drain(&kfull[i % KST], (i / KST) & 1);
-        for (int64_t i = (nv > VST ? nv - VST : 0); i < nv; ++i)
-          mbar_wait_drain(&vfull[i % VST], (i / VST) & 1);
+        for (int64_t i = (nv > VRS ? nv - VRS : 0); i < nv; ++i)
+          mbar_wait_drain(&vfull[i % VRS], (i / VRS) & 1);
       }
     }
   } else if (warp == 1) {
@@ -402,7 +446,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         walk.advance_to(g);
         const bool seg_first = (g == g0) || (g == walk.bstart);
         const int vs = static_cast<int>(it % VST), ps = static_cast<int>(it & 1);
-        if (!mbar_wait(&vfull[vs], (it / VST) & 1, abort_flag, p.dev_err)) break;
+        if (!mbar_wait(F8 ? &vcvt[vs] : &vfull[vs], (it / VST) & 1, abort_flag, p.dev_err)) break;
         if (!mbar_wait(&pfull[ps], (it >> 1) & 1, abort_flag, p.dev_err)) break;
         tc_fence_after();
         const uint32_t vaddr = smem_u32(vst + vs * S::VSTAGE_BYTES);
@@ -412,21 +456,62 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const uint64_t adesc = make_sdesc(vaddr + i * 4096, 2048, 1024, kSwizzle128B);
           umma_f16(tmem_base + i * HP, adesc, bdesc, idesc, seg_first ? 0u : 1u);
         }
-        umma_commit(&vempty[vs]);
+        umma_commit(F8 ? &vfree[vs] : &vempty[vs]);
         umma_commit(&pfree[ps]);
         ++issued;
       }
       if (issued > 0) mbar_wait_drain(&pfree[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
     }
+  } else if (F8 && warp >= 2 + NCW) {
+    // ------------------------------------------ F8: widen E4M3 V pages to fp16 stages
+    // The MMA's layout: 64-column box g at g * 2048, token row t at t * 128, 16-byte chunk
+    // c at chunk c ^ (t % 8).  Tokens past the sequence end (or a rejected block) get zero
+    // rows, so whatever those slots hold cannot reach the accumulator through 0 * NaN.
+    const int vt = threadIdx.x - 32 * (2 + NCW);   // 0..63
+    constexpr int NCV = S::NBOX * kBlockSize * 8;   // 16-byte fp16 chunks per page
+    static_assert(NCV % 64 == 0, "whole passes of the 64 widening threads");
+    for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
+      const int vr = static_cast<int>(it % VRS), vs = static_cast<int>(it % VST);
+      bool ok = mbar_wait(&vfull[vr], (it / VRS) & 1, abort_flag, p.dev_err);
+      if (it >= VST) ok = mbar_wait(&vfree[vs], ((it / VST) - 1) & 1, abort_flag, p.dev_err) && ok;
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int nvalid = vinfo[vr];
+      const uint8_t* src = vraw + vr * L::VP;
+      uint8_t* vb = vst + vs * S::VSTAGE_BYTES;
+#pragma unroll 4
+      for (int i = 0; i < NCV / 64; ++i) {
+        const int idx = vt + 64 * i;
+        const int c = idx & 7, tt = (idx >> 3) % kBlockSize, gb = (idx >> 3) / kBlockSize;
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (tt < nvalid) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(src + tt * S::R + gb * 64 + c * 8);
+          o.x = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x & 0xFFFFu));
+          o.y = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x >> 16));
+          o.z = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y & 0xFFFFu));
+          o.w = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y >> 16));
+        }
+        *reinterpret_cast<uint4*>(vb + gb * 2048 + tt * 128 + ((c ^ (tt & 7)) << 4)) = o;
+      }
+      fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&vempty[vr]);   // raw page consumed
+        mbar_arrive(&vcvt[vs]);     // fp16 stage ready
+      }
+    }
   } else {
     // ------------------------------------------------- scores, softmax, P, epilogue
-    constexpr int HPW = S::H / 4;               // heads per compute warp
+    constexpr int HPW = S::H / NCW;             // heads per compute warp
     constexpr int ROUNDS = (HPW + 1) / 2;       // two heads (16 lanes each) per round
     constexpr int NCH = S::RK / 8;              // 16-byte chunks per K row
     const int cw = warp - 2;                    // head group
     const int quarter = warp & 3;               // TMEM lane quarter this warp may access
     const int hl = lane >> 4, t = lane & 15;
-    const int ctid = threadIdx.x - 64;          // 0..127 over the compute warps
+    const int ctid = threadIdx.x - 64;          // 0 .. 32*NCW-1 over the compute warps
+    constexpr int CT = 32 * NCW;                // compute threads
+    // warps sharing a TMEM lane quarter split the accumulator's 128-row chunks
+    const int chunk0 = cw / 4;
+    constexpr int CSTEP = NCW / 4;
     float m_run[ROUNDS], l_run[ROUNDS];
 #pragma unroll
     for (int r = 0; r < ROUNDS; ++r) { m_run[r] = -INFINITY; l_run[r] = 0.f; }
@@ -434,21 +519,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
       walk.advance_to(g);
-      const BlockInfo bi = block_info(p, walk, g, g0, g1);
+      BlockInfo bi;
+      bi.seg_first = (g == g0) || (g == walk.bstart);
+      bi.seg_last = (g == g1 - 1) || (g + 1 == walk.bend);
       bool ok = true;
       if (bi.seg_first) {
         // rank-space query of this request into the permuted layout
         // qs[((h*2 + hi)*NCH + c)*4 + e] = q~[h][8c + 4hi + e]
         const float* src = p.qt + static_cast<size_t>(walk.b) * S::H * S::RK;
-        for (int i = ctid; i < S::H * S::RK; i += 128) {
+        for (int i = ctid; i < S::H * S::RK; i += CT) {
           const int h = i / S::RK, k = i % S::RK;
           const int c = k >> 3, hi = (k >> 2) & 1, e = k & 3;
           qs[((h * 2 + hi) * NCH + c) * 4 + e] = src[i];
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, CT);
       }
       const int ks = static_cast<int>(it % KST);
       ok = mbar_wait(&kfull[ks], (it / KST) & 1, abort_flag, p.dev_err);
+      bi.nvalid = kinfo[ks];
       float s[ROUNDS];
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
@@ -456,29 +544,51 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         s[r] = -INFINITY;
         if (ok && hw < HPW) {
           const int h = cw * HPW + hw;
-          const __half* krow = reinterpret_cast<const __half*>(kst + ks * S::KPAGE_BYTES) +
-                               (h * kBlockSize + t) * S::RK;
-          float a0 = 0.f, a1 = 0.f;
+          // two packed fp32x2 accumulators = four independent chains
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          if constexpr (F8) {
+            // 16 E4M3 codes per 16-byte chunk; lanes 2u and 2u+1 start at chunk u so the
+            // 16 tokens' 64-byte rows spread over all banks
+            constexpr int NCH8 = S::RK / 16;
+            const uint8_t* krow = kst + ks * L::KP + (h * kBlockSize + t) * S::RK;
 #pragma unroll
-          for (int v = 0; v < NCH; ++v) {
-            const int c = (v + t) % NCH;   // rotation keeps the 16 lanes on distinct banks
-            const uint4 kv = *reinterpret_cast<const uint4*>(krow + c * 8);
-            const float4 qa = qs4[(h * 2 + 0) * NCH + c];
-            const float4 qb = qs4[(h * 2 + 1) * NCH + c];
-            const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kv.x));
-            const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kv.y));
-            const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kv.z));
-            const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kv.w));
-            a0 = fmaf(k01.x, qa.x, a0);
-            a1 = fmaf(k01.y, qa.y, a1);
-            a0 = fmaf(k23.x, qa.z, a0);
-            a1 = fmaf(k23.y, qa.w, a1);
-            a0 = fmaf(k45.x, qb.x, a0);
-            a1 = fmaf(k45.y, qb.y, a1);
-            a0 = fmaf(k67.x, qb.z, a0);
-            a1 = fmaf(k67.y, qb.w, a1);
+            for (int v = 0; v < NCH8; ++v) {
+              const int c8 = (v + (t >> 1)) % NCH8;
+              const uint4 kv = *reinterpret_cast<const uint4*>(krow + c8 * 16);
+              const float4 qa0 = qs4[(h * 2 + 0) * NCH + 2 * c8];
+              const float4 qb0 = qs4[(h * 2 + 1) * NCH + 2 * c8];
+              const float4 qa1 = qs4[(h * 2 + 0) * NCH + 2 * c8 + 1];
+              const float4 qb1 = qs4[(h * 2 + 1) * NCH + 2 * c8 + 1];
+              const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+              const float4 qv[4] = {qa0, qb0, qa1, qb1};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w4[u] & 0xFFFFu));
+                const float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w4[u] >> 16));
+                acc0 = fma_f32x2(lo, make_float2(qv[u].x, qv[u].y), acc0);
+                acc1 = fma_f32x2(hi, make_float2(qv[u].z, qv[u].w), acc1);
+              }
+            }
+          } else {
+            const __half* krow = reinterpret_cast<const __half*>(kst + ks * L::KP) +
+                                 (h * kBlockSize + t) * S::RK;
+#pragma unroll
+            for (int v = 0; v < NCH; ++v) {
+              const int c = (v + t) % NCH;   // rotation keeps the 16 lanes on distinct banks
+              const uint4 kv = *reinterpret_cast<const uint4*>(krow + c * 8);
+              const float4 qa = qs4[(h * 2 + 0) * NCH + c];
+              const float4 qb = qs4[(h * 2 + 1) * NCH + c];
+              const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kv.x));
+              const float2 k23 = __half22float2(*reinterpret_cast<const __half2*>(&kv.y));
+              const float2 k45 = __half22float2(*reinterpret_cast<const __half2*>(&kv.z));
+              const float2 k67 = __half22float2(*reinterpret_cast<const __half2*>(&kv.w));
+              acc0 = fma_f32x2(k01, make_float2(qa.x, qa.y), acc0);
+              acc1 = fma_f32x2(k23, make_float2(qa.z, qa.w), acc1);
+              acc0 = fma_f32x2(k45, make_float2(qb.x, qb.y), acc0);
+              acc1 = fma_f32x2(k67, make_float2(qb.z, qb.w), acc1);
+            }
           }
-          s[r] = a0 + a1;
+          s[r] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
       }
       __syncwarp();
@@ -486,32 +596,44 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
       // online softmax (base 2), lazy rescale: the reference max only moves when a block
       // max exceeds it by more than kRescaleThreshold, so the accumulator is rarely touched
+      // The ROUNDS independent butterflies advance level by level, so their shuffle
+      // latencies overlap instead of adding up.
       __half ph[ROUNDS];
-      float alpha[ROUNDS];
+      float alpha[ROUNDS], sv[ROUNDS], bmax[ROUNDS], psum[ROUNDS], m_new[ROUNDS];
+      bool valid[ROUNDS];
       bool need_any = false;
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
         const int hw = 2 * r + hl;
-        const bool valid = ok && hw < HPW && t < bi.nvalid;
-        const float sv = valid ? s[r] : -INFINITY;
-        float bmax = sv;
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 8));
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 4));
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+        valid[r] = ok && hw < HPW && t < bi.nvalid;
+        sv[r] = valid[r] ? s[r] : -INFINITY;
+        bmax[r] = sv[r];
+      }
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) {
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r)
+          bmax[r] = fmaxf(bmax[r], __shfl_xor_sync(0xffffffffu, bmax[r], o));
+      }
+#pragma unroll
+      for (int r = 0; r < ROUNDS; ++r) {
         const float m_old = bi.seg_first ? -INFINITY : m_run[r];
-        const float m_new = (bmax > m_old + kRescaleThreshold) ? bmax : m_old;
-        alpha[r] = (m_new == m_old) ? 1.f : exp2f(m_old - m_new);
-        need_any |= (m_new != m_old) && !bi.seg_first;
-        const float pv = valid ? exp2f(sv - m_new) : 0.f;
+        m_new[r] = (bmax[r] > m_old + kRescaleThreshold) ? bmax[r] : m_old;
+        alpha[r] = (m_new[r] == m_old) ? 1.f : exp2f(m_old - m_new[r]);
+        need_any |= (m_new[r] != m_old) && !bi.seg_first;
+        const float pv = valid[r] ? exp2f(sv[r] - m_new[r]) : 0.f;
         ph[r] = __float2half_rn(pv);
-        float psum = __half2float(ph[r]);
-        psum += __shfl_xor_sync(0xffffffffu, psum, 8);
-        psum += __shfl_xor_sync(0xffffffffu, psum, 4);
-        psum += __shfl_xor_sync(0xffffffffu, psum, 2);
-        psum += __shfl_xor_sync(0xffffffffu, psum, 1);
-        l_run[r] = (bi.seg_first ? 0.f : l_run[r] * alpha[r]) + psum;
-        m_run[r] = m_new;
+        psum[r] = __half2float(ph[r]);
+      }
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) {
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) psum[r] += __shfl_xor_sync(0xffffffffu, psum[r], o);
+      }
+#pragma unroll
+      for (int r = 0; r < ROUNDS; ++r) {
+        l_run[r] = (bi.seg_first ? 0.f : l_run[r] * alpha[r]) + psum[r];
+        m_run[r] = m_new[r];
       }
       const int fb = static_cast<int>(it & 1);
 #pragma unroll
@@ -520,10 +642,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (t == 0 && hw < HPW) alpha_s[fb * HP + cw * HPW + hw] = alpha[r];
       }
       const bool warp_need = __any_sync(0xffffffffu, need_any);
-      if (lane == 0) flags_s[fb * 4 + cw] = (warp_need ? 1 : 0) | (*abort_flag ? 2 : 0);
-      named_bar_sync(1, 128);
-      const int f = flags_s[fb * 4 + 0] | flags_s[fb * 4 + 1] | flags_s[fb * 4 + 2] |
-                    flags_s[fb * 4 + 3];
+      if (lane == 0) flags_s[fb * NCW + cw] = (warp_need ? 1 : 0) | (*abort_flag ? 2 : 0);
+      named_bar_sync(1, CT);
+      int f = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < NCW; ++w2) f |= flags_s[fb * NCW + w2];
       if (f & 2) break;
 
       const int ps = static_cast<int>(it & 1);
@@ -535,7 +658,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         tc_fence_after();
         if (ok) {
 #pragma unroll 1
-          for (int i = 0; i < S::NCHUNK; ++i) {
+          for (int i = chunk0; i < S::NCHUNK; i += CSTEP) {
 #pragma unroll
             for (int hh = 0; hh < HP / 16; ++hh) {
               const uint32_t ta = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
@@ -567,14 +690,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
         }
       }
-      if (bi.nvalid < kBlockSize) {
+      if (!F8 && bi.nvalid < kBlockSize) {
         // tokens past the sequence end (or a rejected block): zero their V rows so that
         // whatever those slots hold cannot reach the accumulator through 0 * NaN
         const int vs = static_cast<int>(it % VST);
         ok = mbar_wait(&vfull[vs], (it / VST) & 1, abort_flag, p.dev_err) && ok;
         const int nrow = kBlockSize - bi.nvalid;
         uint8_t* vb = vst + vs * S::VSTAGE_BYTES;
-        for (int idx = ctid; idx < nrow * S::NBOX * 8; idx += 128) {
+        for (int idx = ctid; idx < nrow * S::NBOX * 8; idx += CT) {
           const int row = bi.nvalid + idx / (S::NBOX * 8);
           const int rem = idx % (S::NBOX * 8);
           *reinterpret_cast<uint4*>(vb + (rem >> 3) * 2048 + row * 128 + (rem & 7) * 16) =
@@ -593,7 +716,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (ok) {
           float* rec = p.rec + static_cast<size_t>(walk.b + cta) * S::REC;
 #pragma unroll 1
-          for (int i = 0; i < S::NCHUNK; ++i) {
+          for (int i = chunk0; i < S::NCHUNK; i += CSTEP) {
             const int rrow = i * 128 + quarter * 32 + lane;
 #pragma unroll
             for (int hh = 0; hh < HP / 16; ++hh) {
@@ -767,9 +890,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnPara
 template <class S>
 cudaError_t prepare_attn(int device) {
   (void)device;
-  cudaError_t e = cudaFuncSetAttribute(decode_main_kernel<S>,
+  cudaError_t e = cudaFuncSetAttribute(decode_main_kernel<S, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DecodeSmem<S>::ALLOC);
+                                       DecodeSmem<S, false>::ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_main_kernel<S, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecodeSmem<S, true>::ALLOC);
   return e;
 }
 
@@ -786,8 +913,12 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStre
                              stream, pdl, p);
   if (e != cudaSuccess) return e;
   if (prof_start && (e = cudaEventRecord(prof_start, stream)) != cudaSuccess) return e;
-  e = launch_pdl(decode_main_kernel<S>, dim3(p.parts), dim3(kDecodeThreads), DecodeSmem<S>::ALLOC,
-                 stream, pdl, tmap_v, p);
+  if (p.fp8_pages)
+    e = launch_pdl(decode_main_kernel<S, true>, dim3(p.parts), dim3(decode_threads<S, true>()),
+                   DecodeSmem<S, true>::ALLOC, stream, pdl, tmap_v, p);
+  else
+    e = launch_pdl(decode_main_kernel<S, false>, dim3(p.parts), dim3(decode_threads<S, false>()),
+                   DecodeSmem<S, false>::ALLOC, stream, pdl, tmap_v, p);
   if (e != cudaSuccess) return e;
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
   // small batches: four threads per slice element so that a request's many records are

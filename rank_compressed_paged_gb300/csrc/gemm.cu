@@ -23,6 +23,7 @@
 //                       (zero past r_k, up to 64), the prefill score MMA's A operand.
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -61,6 +62,7 @@ struct GemmParams {
   void* k_pages;
   void* v_pages;
   int32_t T;
+  int32_t fp8;            // pages hold E4M3 codes (round to nearest even, saturate)
   int64_t num_blocks;
   // up-projection
   void* out;
@@ -182,15 +184,24 @@ __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j
   }
   const int64_t d = dst[col];
   if (d < 0) return;
+  int64_t at;
+  void* pages;
   if (j.kind == 0) {
     const int r = j.m0 + row;
-    if (r < S::R) static_cast<__half*>(p.v_pages)[d + r] = __float2half_rn(v);
+    if (r >= S::R) return;
+    at = d + r;
+    pages = p.v_pages;
   } else {
     // rows 0..63 belong to head m0, rows 64..127 to head m0 + 1 (next head in the page)
     const int hh = row >> 6, rr = row & 63;
-    if (rr < S::RK)
-      static_cast<__half*>(p.k_pages)[d + hh * kBlockSize * S::RK + rr] = __float2half_rn(v);
+    if (rr >= S::RK) return;
+    at = d + hh * kBlockSize * S::RK + rr;
+    pages = p.k_pages;
   }
+  if (p.fp8)
+    static_cast<__nv_fp8_storage_t*>(pages)[at] = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+  else
+    static_cast<__half*>(pages)[at] = __float2half_rn(v);
 }
 
 template <class S, int MODE, int NT, int KS, int STG>
@@ -450,6 +461,7 @@ cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
   p.k_pages = ap.k_pages;
   p.v_pages = ap.v_pages;
   p.T = ap.T;
+  p.fp8 = ap.fp8_pages;
   p.num_blocks = ap.num_blocks;
   p.dev_err = ap.dev_err;
   constexpr int NM = (S::R + 127) / 128;

@@ -290,6 +290,14 @@ __device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
       : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
   return *reinterpret_cast<const float2*>(&d);
 }
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&d);
+}
 __device__ __forceinline__ float2 sub_f32x2(float2 a, float2 b) {
   uint64_t d;
   asm("sub.rn.f32x2 %0, %1, %2;"

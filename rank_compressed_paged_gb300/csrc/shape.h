@@ -117,7 +117,8 @@ struct AttnParams {
   const void* q;              // [nq][H][d] fp16
   const void* U_k;            // [H][r_k][d] fp16
   const void* W_v;            // [R][H*d] fp16
-  const void* k_pages;        // [num_blocks][H][16][r_k] fp16
+  const void* k_pages;        // [num_blocks][H][16][r_k] fp16 (or E4M3 codes)
+  const void* v_pages;        // [num_blocks][16][R] fp16 (or E4M3 codes)
   const int32_t* block_table; // [rows][bt_stride]
   const int32_t* seq_lens;    // [batch]
   const int32_t* cu_chunk;    // prefill: [batch+1]; decode: nullptr
@@ -145,6 +146,7 @@ struct AttnParams {
   int32_t batch;
   int32_t nq;
   int32_t parts;              // decode CTAs (work partitions)
+  int32_t fp8_pages;          // pages hold E4M3 codes (decode only)
   int32_t late_wait;          // planning kernel may run alongside its predecessor (an append
                               // of the same step that it does not read) and waits at its end
   float qscale;               // log2(e) / sqrt(d)
@@ -161,6 +163,7 @@ struct AppendParams {
   uint32_t* dev_err;
   int64_t num_blocks;
   int32_t T;
+  int32_t fp8_pages;          // store E4M3 codes instead of fp16
 };
 
 }  // namespace rcp

@@ -32,8 +32,8 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
-def _cfg(_lib, H=32, d=128, rk=64, R=1024, bs=16, nb=100):
-    return _lib.CacheConfig(H, d, rk, R, bs, nb)
+def _cfg(_lib, H=32, d=128, rk=64, R=1024, bs=16, nb=100, fmt=0):
+    return _lib.CacheConfig(H, d, rk, R, bs, nb, fmt)
 
 
 def _create(lib, _lib, cfg, ptrs=(0x10000, 0x20000, 0x30000, 0x40000, 0x50000)):
@@ -48,6 +48,9 @@ def test_config_support_and_status_strings(lib):
     assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, 4, 64, 16, 64))) == _lib.RCP_OK
     assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, bs=32))) == _lib.RCP_ERR_UNSUPPORTED
     assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, rk=48))) == _lib.RCP_ERR_UNSUPPORTED
+    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, fmt=_lib.RCP_PAGES_FP8_E4M3))) == \
+        _lib.RCP_OK
+    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, fmt=2))) == _lib.RCP_ERR_UNSUPPORTED
     assert lib.rcp_config_supported(None) == _lib.RCP_ERR_INVALID_ARG
     for code in range(6):
         assert lib.rcp_status_string(code)

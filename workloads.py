@@ -310,9 +310,10 @@ def make_paged_cache_device(seq_lens, shape: dict, seed: int, device="cuda",
     return kp, vp, table, seq_lens
 
 
-def algorithmic_bytes_decode(shape: dict, seq_lens) -> int:
-    """Coefficient bytes one decode step reads: (H*r_k + R) * 2 bytes per cached token."""
-    per_tok = (shape["num_heads"] * shape["rank_k"] + shape["rank_v"]) * 2
+def algorithmic_bytes_decode(shape: dict, seq_lens, elem_bytes: int = 2) -> int:
+    """Coefficient bytes one decode step reads: (H*r_k + R) * elem_bytes per cached token
+    (2 for fp16 pages, 1 for E4M3 pages)."""
+    per_tok = (shape["num_heads"] * shape["rank_k"] + shape["rank_v"]) * elem_bytes
     return int(np.sum(np.asarray(seq_lens, dtype=np.int64))) * per_tok
 
 
