@@ -264,6 +264,30 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
   return __half22float2(__half2(r));
 }
 
+// Widens boxes [b0, b1) (64 columns each) of an E4M3 V page ([16][R] codes at src) into the
+// fp16 stage vb in the layout of the value MMA: box g at g * 2048, token row t at t * 128,
+// 16-byte chunk c at chunk c ^ (t % 8).  Tokens at or past nvalid (the sequence end, or a
+// rejected block) get zero rows, so whatever those slots hold cannot reach the accumulator
+// through 0 * NaN.  NT threads, this one is tid.
+template <class S, int NT>
+__device__ __forceinline__ void widen_v_boxes(const uint8_t* src, uint8_t* vb, int nvalid, int b0,
+                                              int b1, int tid) {
+  const int n = (b1 - b0) * kBlockSize * 8;
+#pragma unroll 4
+  for (int idx = tid; idx < n; idx += NT) {
+    const int c = idx & 7, tt = (idx >> 3) % kBlockSize, gb = b0 + (idx >> 3) / kBlockSize;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (tt < nvalid) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(src + tt * S::R + gb * 64 + c * 8);
+      o.x = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x & 0xFFFFu));
+      o.y = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x >> 16));
+      o.z = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y & 0xFFFFu));
+      o.w = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y >> 16));
+    }
+    *reinterpret_cast<uint4*>(vb + gb * 2048 + tt * 128 + ((c ^ (tt & 7)) << 4)) = o;
+  }
+}
+
 constexpr float kRescaleThreshold = 8.f;   // log2 units: weights stay <= 2^8 before a rescale
 
 // Walks the requests that a CTA's block range crosses.
@@ -323,6 +347,9 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
   uint64_t* vfree = vcvt + VST;           // F8 [VST] fp16 V stage read by its MMAs
   constexpr int NTHR = decode_threads<S, F8>();
   constexpr int NCW = decode_compute_warps<S, F8>();   // compute warps 2 .. NCW+1
+  // F8: V boxes widened by warps 10-11; the compute warps widen the remaining ones (a
+  // split measured to balance the two groups' time per block)
+  constexpr int WB = S::NBOX >= 16 ? 10 : S::NBOX;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
   // tokens of the block in each stage that are attended, published by the copy thread
@@ -342,7 +369,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
     }
     for (int i = 0; i < VRS; ++i) {
       mbar_init(&vfull[i], 1);
-      mbar_init(&vempty[i], F8 ? 2 : 1);
+      mbar_init(&vempty[i], F8 ? 2 + (WB < S::NBOX ? NCW : 0) : 1);
     }
     if constexpr (F8) {
       for (int i = 0; i < VST; ++i) {
@@ -464,39 +491,19 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
     }
   } else if (F8 && warp >= 2 + NCW) {
     // ------------------------------------------ F8: widen E4M3 V pages to fp16 stages
-    // The MMA's layout: 64-column box g at g * 2048, token row t at t * 128, 16-byte chunk
-    // c at chunk c ^ (t % 8).  Tokens past the sequence end (or a rejected block) get zero
-    // rows, so whatever those slots hold cannot reach the accumulator through 0 * NaN.
+    // boxes [0, WB) here; the compute warps widen the rest after writing P
     const int vt = threadIdx.x - 32 * (2 + NCW);   // 0..63
-    constexpr int NCV = S::NBOX * kBlockSize * 8;   // 16-byte fp16 chunks per page
-    static_assert(NCV % 64 == 0, "whole passes of the 64 widening threads");
     for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
       const int vr = static_cast<int>(it % VRS), vs = static_cast<int>(it % VST);
       bool ok = mbar_wait(&vfull[vr], (it / VRS) & 1, abort_flag, p.dev_err);
       if (it >= VST) ok = mbar_wait(&vfree[vs], ((it / VST) - 1) & 1, abort_flag, p.dev_err) && ok;
       if (!__all_sync(0xffffffffu, ok)) break;
-      const int nvalid = vinfo[vr];
-      const uint8_t* src = vraw + vr * L::VP;
-      uint8_t* vb = vst + vs * S::VSTAGE_BYTES;
-#pragma unroll 4
-      for (int i = 0; i < NCV / 64; ++i) {
-        const int idx = vt + 64 * i;
-        const int c = idx & 7, tt = (idx >> 3) % kBlockSize, gb = (idx >> 3) / kBlockSize;
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (tt < nvalid) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(src + tt * S::R + gb * 64 + c * 8);
-          o.x = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x & 0xFFFFu));
-          o.y = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x >> 16));
-          o.z = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y & 0xFFFFu));
-          o.w = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y >> 16));
-        }
-        *reinterpret_cast<uint4*>(vb + gb * 2048 + tt * 128 + ((c ^ (tt & 7)) << 4)) = o;
-      }
+      widen_v_boxes<S, 64>(vraw + vr * L::VP, vst + vs * S::VSTAGE_BYTES, vinfo[vr], 0, WB, vt);
       fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&vempty[vr]);   // raw page consumed
-        mbar_arrive(&vcvt[vs]);     // fp16 stage ready
+        mbar_arrive(&vempty[vr]);   // this warp is done with the raw page
+        mbar_arrive(&vcvt[vs]);     // its part of the fp16 stage is ready
       }
     }
   } else {
@@ -689,6 +696,16 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
                                        (t & 7) * 2) = ph[r];
           }
         }
+      }
+      if (F8 && WB < S::NBOX) {
+        // this block's remaining V boxes; the fp16 stage is free (pfree above covers the
+        // MMA that read it two blocks ago)
+        const int vr = static_cast<int>(it % VRS);
+        ok = mbar_wait(&vfull[vr], (it / VRS) & 1, abort_flag, p.dev_err) && ok;
+        widen_v_boxes<S, CT>(vraw + vr * L::VP, vst + static_cast<int>(it % VST) * S::VSTAGE_BYTES,
+                             bi.nvalid, WB, S::NBOX, ctid);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&vempty[vr]);
       }
       if (!F8 && bi.nvalid < kBlockSize) {
         // tokens past the sequence end (or a rejected block): zero their V rows so that
