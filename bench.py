@@ -34,6 +34,7 @@ import workloads as wl  # noqa: E402
 METRIC = "decode-attn µs/step & GB/s at B=64,L=8192; fraction of GB300 HBM roofline"
 SHAPE = wl.SHAPES["mha32"]
 BATCH, SEQ = 64, 8192   # the measured configuration; --batch / --seq-len shrink it for ncu
+RAGGED = None           # (lo, hi): per-sequence lengths uniform in [lo, hi] instead of SEQ
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_b64_l8192.md")
 KERNEL_SRC = os.path.join(ROOT, "rank_compressed_paged_gb300", "csrc", "decode.cu")
 
@@ -156,13 +157,16 @@ class ClockSampler:
 
 
 def workload_name():
+    if RAGGED:
+        return f"decode_b{BATCH}_ragged{RAGGED[0]}-{RAGGED[1]}_append"
     return f"decode_b{BATCH}_l{SEQ}_append"
 
 
 def make_workload(device, seed):
     """Device-resident cache (pages drawn on the GPU) + the step's host inputs."""
     import torch
-    seq_lens = np.full(BATCH, SEQ, np.int32)
+    seq_lens = (wl.ragged_lengths(np.random.default_rng(seed + 1), BATCH, *RAGGED) if RAGGED
+                else np.full(BATCH, SEQ, np.int32))
     kp, vp, table, seq_lens = wl.make_paged_cache_device(seq_lens, SHAPE, seed, device=device,
                                                          spare_blocks=16)
     rng = np.random.default_rng(seed)
@@ -172,7 +176,8 @@ def make_workload(device, seed):
     q = wl.fp16(rng.standard_normal((BATCH, H, d)))
     nk = wl.fp16(rng.standard_normal((BATCH, H, d)))
     nv = wl.fp16(rng.standard_normal((BATCH, H, d)))
-    slots = np.array([wl.slot_for(table, b, SEQ - 1) for b in range(BATCH)], np.int64)
+    slots = np.array([wl.slot_for(table, b, int(seq_lens[b]) - 1) for b in range(BATCH)],
+                     np.int64)
     return dict(kp=kp, vp=vp, table=table, seq_lens=seq_lens, U=U, W=W, q=q, nk=nk, nv=nv,
                 slots=slots)
 
@@ -236,7 +241,9 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * sum(times) / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_name(), "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
+        "config": {"workload": workload_name(), "batch": BATCH,
+                   "seq_len": SEQ if not RAGGED else f"uniform {RAGGED[0]}..{RAGGED[1]}",
+                   "num_heads": 32,
                    "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
                          "kind": "oracle", "sample": sample},
@@ -376,10 +383,14 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if args.pages == "fp16" else "e4m3 pages, f16/f32 arithmetic",
         "data": "synthetic",
-        "config": {"workload": workload_name(), "batch": BATCH, "seq_len": SEQ, "num_heads": 32,
+        "config": {"workload": workload_name(), "batch": BATCH,
+                   "seq_len": SEQ if not RAGGED else f"uniform {RAGGED[0]}..{RAGGED[1]}",
+                   "num_heads": 32,
                    "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16,
                    "step": "append 1 token/seq + decode attention", "pages": args.pages,
-                   "l2": "inputs larger than L2 (3.2 GB of pages per GPU), no flush",
+                   "l2": f"inputs larger than L2 ({coeff_bytes / 1e9:.2f} GB of pages per GPU), "
+                         "no flush" if coeff_bytes > 2 * 129e6 else
+                         "pages smaller than 2x L2: later steps may hit L2",
                    "parallelism": f"replicas x{world}, batch-sharded, no collective"},
         "roofline": {"bound": "hbm", "kernel": "decode_main_kernel",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
@@ -509,7 +520,7 @@ def run_prefill(args):
 
 
 def main():
-    global BATCH, SEQ
+    global BATCH, SEQ, RAGGED
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -520,6 +531,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=BATCH)
     ap.add_argument("--seq-len", type=int, default=SEQ)
+    ap.add_argument("--ragged", type=str, default=None,
+                    help="LO,HI: per-sequence lengths uniform in [LO, HI] (seeded)")
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
     ap.add_argument("--prefill-batch", type=int, default=16)
     ap.add_argument("--prefill-variant", choices=["auto", "rank", "reconstruct"], default="auto")
@@ -529,6 +542,8 @@ def main():
     ap.add_argument("--prefill-chunk", type=int, default=256)
     args = ap.parse_args()
     BATCH, SEQ = args.batch, args.seq_len
+    if args.ragged:
+        RAGGED = tuple(int(x) for x in args.ragged.split(","))
     rank, world, local_rank = dist_env()
     if world > 1:
         import torch.distributed as dist
