@@ -127,3 +127,34 @@ def test_decode_empty_request_after_a_full_one_gives_zeros():
     assert np.any(o1[0] != 0) and np.all(o2[0] == 0)
     ref = orc.decode_attn(inp.q, c.k_pages, c.v_pages, inp.U_k, inp.W_v, c.block_table, lens2, 16)
     assert_close(o2, ref, what="empty after full")
+
+
+def test_decode_with_shared_prefix_blocks():
+    """Prefix caching: several requests' tables point at the same physical blocks."""
+    inp = wl.make_decode_inputs(MAIN, [320, 300, 170, 16], seed=28, fill=np.nan)
+    c = inp.cache
+    table = c.block_table.copy()
+    table[1, :10] = table[0, :10]     # request 1 shares request 0's first 160 tokens
+    table[2, :5] = table[0, :5]       # request 2 shares the first 80
+    table[3, 0] = table[0, 0]         # request 3 is one shared block
+    inp2 = wl.DecodeInputs(inp.shape, inp.U_k, inp.W_v, c, inp.q)
+    inp2.cache.block_table = table
+    out, _ = _run_decode(inp2)
+    assert_close(out, _oracle(inp2), what="shared prefix blocks")
+
+
+def test_decode_ignores_table_entries_past_each_sequence():
+    """Entries beyond ceil(L/16) are never read, so garbage there raises no error."""
+    import torch
+    inp = wl.make_decode_inputs(MAIN, [40, 200, 0], seed=29, fill=np.nan)
+    c = inp.cache
+    need = (c.seq_lens + 15) // 16
+    table = np.full((3, 40), 1 << 30, np.int32)
+    for b in range(3):
+        table[b, :need[b]] = c.block_table[b, :need[b]]
+    cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    out = cache.decode_attn(t(inp.q), t(table), t(c.seq_lens))
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    ref = orc.decode_attn(inp.q, c.k_pages, c.v_pages, inp.U_k, inp.W_v, table, c.seq_lens, 16)
+    assert_close(out.cpu().numpy(), ref, what="padded table")
