@@ -35,7 +35,10 @@ attention computed by a library routine; explicit reconstruction K = C_k U_k, V 
 followed by library attention agrees to 1e-12; physical block permutation leaves outputs
 bitwise unchanged; softmax weights sum to 1; single-token, equal-key, power-of-two
 scaling, causal-prefill and hand-derived closed-form cases; coordinate-selection factors
-make appends exact copies.
+make appends exact copies.  Block-sparse skipping (tests/test_oracle_sparse.py): attention
+over a page subset equals attention over a compacted block table and a scalar textbook
+loop; the skippable set matches a hand-built score pattern; a sequential running-maximum
+pass drops a subset of it; the output change stays within the derived bound.
 """
 from __future__ import annotations
 
@@ -112,6 +115,109 @@ def decode_attn(q, k_pages, v_pages, U_k, W_v, block_table, seq_lens, block_size
         out[n] = o[0]
         weights.append(p[0])
     return (out, weights) if return_weights else out
+
+
+# ------------------------------------------------------------------ block-sparse skipping
+# The "KV-cache LLM serving" page's sparse decode (its BLASST kernels, "What it measured",
+# item 3) skips blocks whose weights are small, judged with the online softmax.
+# Here a block is a page, and the value coefficients of a page are shared by every head
+# (joint decomposition), so a page's values can only be left out when no head needs them.
+# Readings taken (the page gives no formula): a page is dropped when, for every head, its
+# largest weight is below ``threshold`` times that head's largest weight so far; a
+# dropped page takes part in neither the numerator nor the denominator of the softmax.
+# Which pages a single pass drops depends on the order it meets them in, so the oracle
+# provides (a) attention restricted to any given set of pages, (b) the set of pages that
+# any order may drop (judged against the maximum over the whole sequence, the largest
+# value a running maximum can reach), and (c) the bound on the output change that
+# dropping a set of pages can cause.
+
+def page_max_scores(q, k_pages, U_k, block_table_row, seq_len: int, block_size: int = 16):
+    """Largest score (natural-log units) of each head in each page of one request.
+
+    q [H][d]; returns [n_pages][H] fp64 with n_pages = ceil(seq_len / block_size).
+    """
+    q = _f64(q)
+    H, d = q.shape
+    L = int(seq_len)
+    t = np.arange(L)
+    blocks = np.asarray(block_table_row, dtype=np.int64)[t // block_size]
+    ck = _f64(k_pages[blocks, :, t % block_size, :])                   # [L][H][r_k]
+    qt = np.einsum("hkd,hd->hk", _f64(U_k), q)
+    s = np.einsum("thk,hk->th", ck, qt) / np.sqrt(d)                # [L][H]
+    n_pages = (L + block_size - 1) // block_size
+    out = np.full((n_pages, H), -np.inf)
+    for j in range(n_pages):
+        out[j] = s[j * block_size:min(L, (j + 1) * block_size)].max(axis=0)
+    return out
+
+
+def skippable_pages(q, k_pages, U_k, block_table, seq_lens, threshold: float,
+                    block_size: int = 16):
+    """Pages that skipping with weight threshold ``threshold`` may drop, per request.
+
+    Page j of request b qualifies when, for every head h, exp(max_t in page s_{h,t} - M_h)
+    < threshold, with M_h the largest score of head h over the whole sequence.  Returns a
+    list of bool arrays [n_pages_b].  A running maximum never exceeds M_h, so a single pass
+    in any page order drops a subset of these.
+    """
+    q = np.asarray(q)
+    res = []
+    for b in range(q.shape[0]):
+        L = int(seq_lens[b])
+        if L == 0:
+            res.append(np.zeros(0, bool))
+            continue
+        pm = page_max_scores(q[b], k_pages, U_k, block_table[b], L, block_size)
+        M = pm.max(axis=0)
+        res.append(np.all(pm - M < np.log(threshold), axis=1) if threshold > 0
+                   else np.zeros(pm.shape[0], bool))
+    return res
+
+
+def decode_attn_kept(q, k_pages, v_pages, U_k, W_v, block_table, seq_lens, kept,
+                     block_size: int = 16):
+    """Decode attention over the kept pages only: token t of request b takes part iff
+    kept[b][t // block_size].  A request with no kept token gives zeros."""
+    q = np.asarray(q)
+    B, H, d = q.shape
+    out = np.zeros((B, H, d))
+    for b in range(B):
+        L = int(seq_lens[b])
+        ck, cv = gather_request(k_pages, v_pages, block_table[b], L, block_size)
+        sel = np.array([bool(kept[b][t // block_size]) for t in range(L)], dtype=bool)
+        if sel.any():
+            out[b] = attend(q[b:b + 1], ck[sel], cv[sel], U_k, W_v, d)[0][0]
+    return out
+
+
+def skip_error_bound(q, k_pages, v_pages, U_k, W_v, block_table, seq_lens, dropped,
+                     block_size: int = 16):
+    """Largest change, per (request, head), that leaving out the dropped pages can make to
+    the decode output.
+
+    With A the kept set and S the dropped one, weights w_t = exp(s_t - max),
+    o_all = (sum_A w v + sum_S w v) / (sum_A w + sum_S w) and o_A = sum_A w v / sum_A w, so
+    o_A - o_all = (w_S / w_all) (o_A - sum_S w v / w_S) and every component is at most
+    (w_S / w_all) * 2 max_t |v_t| in size, v_t = W_v,h^T c_v[t] the value of token t.
+    Returns [B][H] fp64.
+    """
+    q = np.asarray(q)
+    B, H, d = q.shape
+    W = _f64(W_v)
+    bound = np.zeros((B, H))
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L == 0:
+            continue
+        ck, cv = gather_request(k_pages, v_pages, block_table[b], L, block_size)
+        qt = np.einsum("hkd,hd->hk", _f64(U_k), _f64(q[b]))
+        s = np.einsum("thk,hk->ht", ck, qt) / np.sqrt(d)              # [H][L]
+        w = np.exp(s - s.max(axis=1, keepdims=True))
+        drop = np.array([bool(dropped[b][t // block_size]) for t in range(L)], dtype=bool)
+        for h in range(H):
+            vmax = np.abs(cv @ W[:, h * d:(h + 1) * d]).max()
+            bound[b, h] = w[h, drop].sum() / w[h].sum() * 2.0 * vmax
+    return bound
 
 
 def append_kv(k_pages, v_pages, U_k, W_v, k, v, slot_mapping, block_size: int = 16):

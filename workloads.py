@@ -49,6 +49,32 @@ WORKLOADS = {
 }
 
 
+# Peaked attention for the block-sparse decode.  The sparse-decode measurements on the
+# "KV-cache LLM serving" page come from a real model whose attention leaves about 42 % of
+# KV blocks with negligible weight ("What it measured", item 3, and "What did not work").
+# Synthetic stand-in: a random 42 % of each request's pages (never its first page, the
+# attention sink, nor its last, the recent tokens) hold background keys whose coefficients
+# are scaled down 16x, and queries are scaled up 6x, so that the remaining pages dominate
+# every head's softmax.
+PEAKED = dict(background_frac=0.42, background_scale=1.0 / 16, q_scale=6.0)
+
+
+def background_pages(rng: np.random.Generator, seq_lens, frac: float,
+                     block_size: int = BLOCK_SIZE) -> list:
+    """Per request, a bool array over its pages: True marks a background page.  Each
+    page is drawn independently with probability ``frac``; the first and the last page of
+    a request are never background."""
+    out = []
+    for L in seq_lens:
+        n = blocks_needed(int(L), block_size)
+        m = rng.random(n) < frac
+        if n:
+            m[0] = False
+            m[-1] = False
+        out.append(m)
+    return out
+
+
 def fp16(x) -> np.ndarray:
     """Round to fp16 (numpy rounds float64 -> float16 to nearest, ties to even)."""
     return np.asarray(x, dtype=np.float64).astype(np.float16)
@@ -193,15 +219,18 @@ class DecodeInputs:
     new_k: np.ndarray | None = None    # [B][H][d] fp16 (appended token, position L-1)
     new_v: np.ndarray | None = None
     slot_mapping: np.ndarray | None = None   # [B] int64
+    background: list | None = None     # peaked workloads: per request, background pages
 
 
 def make_decode_inputs(shape: dict, seq_lens, seed: int, append: bool = False,
                        spare_blocks: int = 4, fill: float = 0.0,
-                       max_blocks: int | None = None) -> DecodeInputs:
+                       max_blocks: int | None = None, peaked: dict | None = None) -> DecodeInputs:
     """Host-side decode workload.
 
     Draw order: factors, K/V coefficient sequences (with the block permutation), q, then
-    the appended token's k and v.
+    the appended token's k and v, then (``peaked``, e.g. ``PEAKED``) the background pages,
+    whose key coefficients are then scaled by ``background_scale``; q is scaled by
+    ``q_scale``.
     """
     rng = np.random.default_rng(seed)
     H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
@@ -217,6 +246,17 @@ def make_decode_inputs(shape: dict, seq_lens, seed: int, append: bool = False,
         out.slot_mapping = np.array(
             [slot_for(cache.block_table, b, int(L) - 1) if L > 0 else -1
              for b, L in enumerate(cache.seq_lens)], dtype=np.int64)
+    if peaked:
+        bg = background_pages(rng, cache.seq_lens, peaked["background_frac"])
+        scale = peaked["background_scale"]
+        for b, m in enumerate(bg):
+            for j in np.nonzero(m)[0]:
+                blk = cache.block_table[b, j]
+                cache.k_pages[blk] = fp16(cache.k_pages[blk].astype(np.float64) * scale)
+                lo, hi = j * BLOCK_SIZE, min(int(cache.seq_lens[b]), (j + 1) * BLOCK_SIZE)
+                cache.ck[b][lo:hi] = cache.k_pages[blk][:, :hi - lo, :].transpose(1, 0, 2)
+        out.q = fp16(q.astype(np.float64) * peaked["q_scale"])
+        out.background = bg
     return out
 
 
@@ -285,12 +325,14 @@ def make_prefill_inputs(shape: dict, prior_lens, chunk_lens, seed: int, spare_bl
 
 def make_paged_cache_device(seq_lens, shape: dict, seed: int, device="cuda",
                             spare_blocks: int = 0, block_size: int = BLOCK_SIZE,
-                            chunk_blocks: int = 4096):
+                            chunk_blocks: int = 4096, peaked: dict | None = None):
     """Fill every physical page of a (multi-GB) cache with seeded N(0,1) fp16 on the device.
 
     Returns (k_pages, v_pages, block_table numpy int32, seq_lens numpy int32).  The block
     permutation is drawn on the host (numpy, ``seed``); page values by a torch generator
-    seeded with ``seed`` on ``device``, in chunks of ``chunk_blocks`` blocks.
+    seeded with ``seed`` on ``device``, in chunks of ``chunk_blocks`` blocks.  With
+    ``peaked`` the background pages are then drawn on the host (same numpy stream) and
+    their key coefficients scaled by ``background_scale`` (q scaling is the caller's).
     """
     import torch
     rng = np.random.default_rng(seed)
@@ -307,6 +349,13 @@ def make_paged_cache_device(seq_lens, shape: dict, seed: int, device="cuda",
                               dtype=torch.float32).half()
         vp[s:e] = torch.randn((e - s, block_size, R), generator=g, device=device,
                               dtype=torch.float32).half()
+    if peaked:
+        bg = background_pages(rng, seq_lens, peaked["background_frac"], block_size)
+        ids = np.concatenate([table[b, :len(m)][m] for b, m in enumerate(bg)] + [
+            np.zeros(0, np.int32)]).astype(np.int64)
+        for s in range(0, len(ids), chunk_blocks):
+            idx = torch.from_numpy(ids[s:s + chunk_blocks]).to(device)
+            kp[idx] = (kp[idx].float() * peaked["background_scale"]).half()
     return kp, vp, table, seq_lens
 
 
