@@ -35,7 +35,9 @@ METRIC = "decode-attn µs/step & GB/s at B=64,L=8192; fraction of GB300 HBM roof
 SHAPE = wl.SHAPES["mha32"]
 BATCH, SEQ = 64, 8192   # the measured configuration; --batch / --seq-len shrink it for ncu
 RAGGED = None           # (lo, hi): per-sequence lengths uniform in [lo, hi] instead of SEQ
+PEAKED = False          # peaked-attention pages and queries (workloads.PEAKED)
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_b64_l8192.md")
+SPARSE_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_sparse_b64_l8192_peaked.md")
 KERNEL_SRC = os.path.join(ROOT, "rank_compressed_paged_gb300", "csrc", "decode.cu")
 
 
@@ -88,12 +90,13 @@ def kernel_src_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def ncu_traffic_per_launch():
-    """DRAM bytes per decode-kernel launch from the committed ncu summary, or None when the
+def ncu_traffic_per_launch(summary=None):
+    """DRAM bytes per decode-kernel launch from a committed ncu summary, or None when the
     summary is missing or was taken on a different version of the kernel source."""
-    if not os.path.exists(PROFILE_SUMMARY):
+    summary = summary or PROFILE_SUMMARY
+    if not os.path.exists(summary):
         return None
-    txt = open(PROFILE_SUMMARY).read()
+    txt = open(summary).read()
     h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", txt)
     t = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9]+)", txt)
     if not h or not t or h.group(1) != kernel_src_hash():
@@ -157,9 +160,10 @@ class ClockSampler:
 
 
 def workload_name():
+    tail = "_append" + ("_peaked" if PEAKED else "")
     if RAGGED:
-        return f"decode_b{BATCH}_ragged{RAGGED[0]}-{RAGGED[1]}_append"
-    return f"decode_b{BATCH}_l{SEQ}_append"
+        return f"decode_b{BATCH}_ragged{RAGGED[0]}-{RAGGED[1]}{tail}"
+    return f"decode_b{BATCH}_l{SEQ}{tail}"
 
 
 def make_workload(device, seed):
@@ -168,12 +172,13 @@ def make_workload(device, seed):
     seq_lens = (wl.ragged_lengths(np.random.default_rng(seed + 1), BATCH, *RAGGED) if RAGGED
                 else np.full(BATCH, SEQ, np.int32))
     kp, vp, table, seq_lens = wl.make_paged_cache_device(seq_lens, SHAPE, seed, device=device,
-                                                         spare_blocks=16)
+                                                         spare_blocks=16,
+                                                         peaked=wl.PEAKED if PEAKED else None)
     rng = np.random.default_rng(seed)
     U, W = wl.make_factors(rng, SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"],
                            SHAPE["rank_v"])
     H, d = SHAPE["num_heads"], SHAPE["head_dim"]
-    q = wl.fp16(rng.standard_normal((BATCH, H, d)))
+    q = wl.fp16(rng.standard_normal((BATCH, H, d)) * (wl.PEAKED["q_scale"] if PEAKED else 1.0))
     nk = wl.fp16(rng.standard_normal((BATCH, H, d)))
     nv = wl.fp16(rng.standard_normal((BATCH, H, d)))
     slots = np.array([wl.slot_for(table, b, int(seq_lens[b]) - 1) for b in range(BATCH)],
@@ -287,7 +292,11 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step():
-        cache.decode_step(nk, nv, slots, q, table, lens, out=out, workspace=ws)
+        if args.sparse is None:
+            cache.decode_step(nk, nv, slots, q, table, lens, out=out, workspace=ws)
+        else:   # the same step with the block-sparse decode
+            cache.append_kv(nk, nv, slots)
+            cache.decode_attn_sparse(q, table, lens, args.sparse, out=out, workspace=ws)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -342,8 +351,13 @@ def run_ours(args, rank, world, local_rank):
 
     def e2e_step():
         dbuf.copy_(hbuf, non_blocking=True)
-        cache.decode_step(dview["k"], dview["v"], dview["s"], dview["q"], dview["t"], dview["l"],
-                          out=out, workspace=ws)
+        if args.sparse is None:
+            cache.decode_step(dview["k"], dview["v"], dview["s"], dview["q"], dview["t"],
+                              dview["l"], out=out, workspace=ws)
+        else:
+            cache.append_kv(dview["k"], dview["v"], dview["s"])
+            cache.decode_attn_sparse(dview["q"], dview["t"], dview["l"], args.sparse, out=out,
+                                     workspace=ws)
         hout.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -358,17 +372,45 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
+    # ---- block-sparse decode: which pages the timed configuration reads (deterministic)
+    sparse = None
+    coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"],
+                                              1 if args.pages == "fp8_e4m3" else 2)
+    read_bytes = coeff_bytes
+    if args.sparse is not None:
+        kept = torch.zeros(w["table"].shape, dtype=torch.uint8, device=dev)
+        cache.decode_attn_sparse(q, table, lens, args.sparse, page_kept=kept, out=out,
+                                 workspace=ws)
+        kept = kept.cpu().numpy()
+        L = w["seq_lens"].astype(np.int64)
+        kept_tok = sum(int(min(16, L[b] - 16 * j)) for b in range(BATCH)
+                       for j in range(wl.blocks_needed(int(L[b]))) if kept[b, j])
+        n_pages = sum(wl.blocks_needed(int(x)) for x in L)
+        n_kept = sum(int(kept[b, :wl.blocks_needed(int(L[b]))].sum()) for b in range(BATCH))
+        # keys of every token + values of the kept pages' tokens
+        read_bytes = int(L.sum()) * SHAPE["num_heads"] * SHAPE["rank_k"] * 2 + \
+            kept_tok * SHAPE["rank_v"] * 2
+        sparse = {"threshold": args.sparse, "pages": n_pages,
+                  "pages_skipped_frac": round(1 - n_kept / n_pages, 4),
+                  "bytes_read": read_bytes,
+                  "note": "value counts the dense decode's coefficient bytes (comparable with "
+                          "the dense line on the same workload); roofline.achieved counts the "
+                          "bytes the sparse pass reads (all keys, kept pages' values)"}
+
     # ---- aggregate over ranks (max time)
     step_ms, e2e_ms, kern_ms = reduce_max([step_ms, e2e_ms, kern_ms], world, dev)
     if rank != 0:
         return
-    coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"],
-                                              1 if args.pages == "fp8_e4m3" else 2)
     value = job_gbs(coeff_bytes, world, step_ms)
     e2e_value = job_gbs(coeff_bytes, world, e2e_ms)
     peak, peak_kind = measured_peaks()
-    achieved = coeff_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = ncu_traffic_per_launch() if args.pages == "fp16" else None
+    achieved = read_bytes / (kern_ms * 1e-3) / 1e9
+    traffic = None
+    if args.pages == "fp16" and not RAGGED and BATCH == 64 and SEQ == 8192:
+        if args.sparse is None and not PEAKED:
+            traffic = ncu_traffic_per_launch()
+        elif args.sparse == 2.0 ** -8 and PEAKED:
+            traffic = ncu_traffic_per_launch(SPARSE_PROFILE_SUMMARY)
     # CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N=1)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -387,21 +429,26 @@ def run_ours(args, rank, world, local_rank):
                    "seq_len": SEQ if not RAGGED else f"uniform {RAGGED[0]}..{RAGGED[1]}",
                    "num_heads": 32,
                    "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16,
-                   "step": "append 1 token/seq + decode attention", "pages": args.pages,
+                   "step": "append 1 token/seq + decode attention" +
+                           (f" (block-sparse, threshold {args.sparse})" if args.sparse is not None
+                            else ""), "pages": args.pages,
+                   "attention": "peaked (42% background pages)" if PEAKED else "N(0,1) scores",
                    "l2": f"inputs larger than L2 ({coeff_bytes / 1e9:.2f} GB of pages per GPU), "
                          "no flush" if coeff_bytes > 2 * 129e6 else
                          "pages smaller than 2x L2: later steps may hit L2",
                    "parallelism": f"replicas x{world}, batch-sharded, no collective"},
-        "roofline": {"bound": "hbm", "kernel": "decode_main_kernel",
+        "roofline": {"bound": "hbm", "kernel": "decode_main_kernel" +
+                               ("<sparse>" if args.sparse is not None else ""),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": coeff_bytes, "kernel_us": round(kern_ms * 1e3, 1),
+                     "algorithmic_bytes": read_bytes, "kernel_us": round(kern_ms * 1e3, 1),
                      "frac_of_8TBps": round(achieved / 8000.0, 4)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "inputs packed in one pinned buffer: one H2D copy and one D2H copy "
                           "per step, on the step's stream"},
+        "sparse": sparse,
         "gpu_launches": args.steps * 5,
         "clocks": clk.summary(),
     }
@@ -520,7 +567,7 @@ def run_prefill(args):
 
 
 def main():
-    global BATCH, SEQ, RAGGED
+    global BATCH, SEQ, RAGGED, PEAKED
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -540,8 +587,15 @@ def main():
                     help="decode page format (fp16 is the measured configuration)")
     ap.add_argument("--prefill-prior", type=int, default=4096)
     ap.add_argument("--prefill-chunk", type=int, default=256)
+    ap.add_argument("--peaked", action="store_true",
+                    help="decode on peaked attention: 42%% of pages hold background keys")
+    ap.add_argument("--sparse", type=float, default=None, metavar="THRESHOLD",
+                    help="decode step with the block-sparse decode at this weight threshold")
     args = ap.parse_args()
     BATCH, SEQ = args.batch, args.seq_len
+    PEAKED = args.peaked
+    if args.sparse is not None and args.pages != "fp16":
+        ap.error("--sparse needs fp16 pages")
     if args.ragged:
         RAGGED = tuple(int(x) for x in args.ragged.split(","))
     rank, world, local_rank = dist_env()

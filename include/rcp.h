@@ -119,6 +119,29 @@ rcp_status rcp_decode_attn(rcp_cache* cache, const void* q, const int32_t* block
                            void* out, void* workspace, size_t workspace_bytes,
                            rcp_stream stream);
 
+/* Block-sparse decode ("KV-cache LLM serving" page, "What it measured", item 3: decode
+ * kernels that skip low-weight blocks using the online softmax).  Same arguments and
+ * result as rcp_decode_attn, except that a page is left out when, for every head, its
+ * largest softmax weight is below skip_threshold times the largest weight that head has
+ * met so far in the pass: its value coefficients are not read and its tokens take part
+ * in neither the softmax numerator nor its denominator.  Keys are always read (scores
+ * decide).  Value coefficients are shared by all heads, so a page is read when any head
+ * needs it.  The pass keeps one running maximum per work partition (a partition starts
+ * with its first page kept), so which pages are left out depends on how the batch is
+ * partitioned; every page left out satisfies the rule against the running maximum, which
+ * never exceeds the maximum over the whole sequence.
+ *   skip_threshold: in [0, 1); 0 leaves no page out (same result as rcp_decode_attn, bit
+ *     for bit); otherwise RCP_ERR_INVALID_ARG.
+ *   page_kept: NULL, or device uint8 [batch][max_blocks_per_seq]: entry (b, j) is set to 1
+ *     if page j of request b was read and 0 if it was left out; entries at or past
+ *     ceil(seq_lens[b] / 16) are not written.
+ * fp16 pages only (RCP_ERR_UNSUPPORTED for E4M3 pages).  Workspace as rcp_decode_attn. */
+rcp_status rcp_decode_attn_sparse(rcp_cache* cache, const void* q, const int32_t* block_table,
+                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t batch, float skip_threshold, uint8_t* page_kept,
+                                  void* out, void* workspace, size_t workspace_bytes,
+                                  rcp_stream stream);
+
 /* One decode step: rcp_append_kv(k, v, slot_mapping, num_tokens) followed by
  * rcp_decode_attn(q, ...), with the same arguments and results (the pages' "per-decode-step"
  * unit: the cache write and the attention of a step).  Queued together, the query

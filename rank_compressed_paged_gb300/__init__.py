@@ -159,6 +159,26 @@ class PagedCoeffCache:
             _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
         return out
 
+    def decode_attn_sparse(self, q, block_table, seq_lens, skip_threshold: float,
+                           page_kept=None, out=None, workspace=None, stream=None):
+        """Block-sparse decode: as decode_attn, but a page is left out (its values unread,
+        its tokens out of the softmax) when every head's largest weight in it is below
+        ``skip_threshold`` times that head's running maximum weight.  ``page_kept``: None
+        or a [B][max_blocks] uint8 tensor that receives 1 / 0 per page read / left out."""
+        import torch
+        B = int(q.shape[0])
+        if out is None:
+            out = torch.empty_like(q)
+        if page_kept is not None and (page_kept.dtype != torch.uint8 or
+                                      tuple(page_kept.shape) != tuple(block_table.shape)):
+            raise ValueError("page_kept must be uint8 shaped like block_table")
+        ws = self.workspace(B) if workspace is None else workspace
+        _lib.check("rcp_decode_attn_sparse", self._lib.rcp_decode_attn_sparse(
+            self._h, _ptr(q), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), B,
+            float(skip_threshold), _ptr(page_kept) if page_kept is not None else None,
+            _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        return out
+
     def decode_step(self, k, v, slot_mapping, q, block_table, seq_lens, out=None, workspace=None,
                     stream=None):
         """append_kv(k, v, slot_mapping) then decode_attn(q, ...), queued as one step."""

@@ -44,6 +44,8 @@ _SIG = {
     "rcp_workspace_size": (ctypes.c_int, [_P, _I32, ctypes.POINTER(ctypes.c_size_t)]),
     "rcp_append_kv": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P]),
     "rcp_decode_attn": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _P, ctypes.c_size_t, _P]),
+    "rcp_decode_attn_sparse": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, ctypes.c_float, _P,
+                                              _P, _P, ctypes.c_size_t, _P]),
     "rcp_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _P,
                                        ctypes.c_size_t, _P]),
     "rcp_prefill_attn": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _I32, _P, _P,

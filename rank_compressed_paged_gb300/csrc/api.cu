@@ -177,11 +177,17 @@ size_t recon_ws_bytes(const rcp_cache* c, int64_t nq, int64_t batch, int64_t max
                                 : rcp::recon_layout<ShapeTiny>(nq, batch, max_blocks).total;
 }
 
+// Block-sparse decode options (rcp_decode_attn_sparse).
+struct SparseArgs {
+  float tau;            // log2 units, +inf leaves no page out
+  uint8_t* page_kept;
+};
+
 rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, int32_t nq,
                          const int32_t* block_table, int32_t max_blocks_per_seq,
                          const int32_t* seq_lens, int32_t batch, void* out, void* ws,
                          size_t ws_size, rcp_stream stream, bool after_own_append = false,
-                         bool recon = false) {
+                         bool recon = false, const SparseArgs* sparse = nullptr) {
   if (!c || batch < 0 || nq < 0 || max_blocks_per_seq < 1) return RCP_ERR_INVALID_ARG;
   if (nq == 0) return RCP_OK;
   if (batch == 0 && cu_chunk) return RCP_ERR_INVALID_ARG;
@@ -193,6 +199,8 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
     return RCP_ERR_INVALID_ARG;
   if (ws_size < (recon ? recon_ws_bytes(c, nq, batch, max_blocks_per_seq) : ws_bytes(c, nq)))
     return RCP_ERR_WORKSPACE;
+  // block-sparse decode reads fp16 pages
+  if (sparse && (cu_chunk || c->cfg.page_format != RCP_PAGES_FP16)) return RCP_ERR_UNSUPPORTED;
   rcp_status st = ensure_device(c);
   if (st != RCP_OK) return st;
   rcp::AttnParams p{};
@@ -218,6 +226,9 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   if (parts < 1) parts = 1;
   p.parts = static_cast<int32_t>(parts);
   p.late_wait = after_own_append ? 1 : 0;
+  p.sparse = sparse ? 1 : 0;
+  p.skip_tau = sparse ? sparse->tau : 0.f;
+  p.page_kept = sparse ? sparse->page_kept : nullptr;
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c->cfg.head_dim)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -473,6 +484,20 @@ rcp_status rcp_decode_attn(rcp_cache* c, const void* q, const int32_t* block_tab
                            rcp_stream stream) {
   return run_attention(c, q, nullptr, batch, block_table, max_blocks_per_seq, seq_lens, batch, out,
                        workspace, workspace_bytes, stream);
+}
+
+rcp_status rcp_decode_attn_sparse(rcp_cache* c, const void* q, const int32_t* block_table,
+                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t batch, float skip_threshold, uint8_t* page_kept,
+                                  void* out, void* workspace, size_t workspace_bytes,
+                                  rcp_stream stream) {
+  if (!(skip_threshold >= 0.f && skip_threshold < 1.f)) return RCP_ERR_INVALID_ARG;   // NaN too
+  // weight ratio 2^(s - m) < threshold  <=>  s < m - (-log2 threshold)
+  SparseArgs sp{skip_threshold > 0.f ? static_cast<float>(-std::log2(static_cast<double>(skip_threshold)))
+                                     : INFINITY,
+                page_kept};
+  return run_attention(c, q, nullptr, batch, block_table, max_blocks_per_seq, seq_lens, batch, out,
+                       workspace, workspace_bytes, stream, false, false, &sp);
 }
 
 rcp_status rcp_prefill_attn(rcp_cache* c, const void* q, const int32_t* cu_chunk_lens,

@@ -218,14 +218,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
 // F8: pages hold E4M3 codes.  K pages are scored straight from their bytes; V pages land
 // in raw stages and the compute warps widen them to fp16 in the swizzled layout the
 // tensor-core MMA reads (the layout the fp16 path's tensor-map copies produce).
-template <class S, bool F8>
+template <class S, bool F8, bool SKIP = false>
 struct DecodeSmem {
+  static constexpr int DS = 4;                                      // SKIP: decision ring
   static constexpr int KST = F8 ? 3 : 2;                            // key page stages
   static constexpr int VST = 2;                                     // fp16 V stages (MMA A)
   static constexpr int VRS = F8 ? 3 : VST;                          // stages V copies land in
   static constexpr int KP = F8 ? S::KPAGE_BYTES / 2 : S::KPAGE_BYTES;   // bytes per K page
   static constexpr int VP = F8 ? S::VPAGE_BYTES / 2 : S::VPAGE_BYTES;   // bytes per V page
-  static constexpr int NBAR = 2 * KST + 2 * VRS + 4 + (F8 ? 2 * VST : 0);
+  static constexpr int NBAR = 2 * KST + 2 * VRS + 4 + (F8 ? 2 * VST : 0) + (SKIP ? 2 * DS : 0);
   static constexpr int P_BYTES = S::HP * 16 * 2;
   static constexpr int V_OFF = 0;                                   // 1024-aligned stages
   static constexpr int K_OFF = V_OFF + VST * S::VSTAGE_BYTES;
@@ -237,7 +238,9 @@ struct DecodeSmem {
   static constexpr int BAR_OFF = F_OFF + 64;                        // NBAR mbarriers
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;               // tmem slot, abort flag
   static constexpr int INFO_OFF = MISC_OFF + 16;                    // valid tokens per stage:
-  static constexpr int TOTAL = INFO_OFF + (KST + VRS) * 4;          //   K stages, then V
+  // K stages, then V; SKIP adds the physical block of each K stage, the decision ring and
+  // the info word of each P buffer
+  static constexpr int TOTAL = INFO_OFF + (KST + VRS) * 4 + (SKIP ? (KST + DS + 2) * 4 : 0);
   static constexpr int ALLOC = TOTAL + 1024;                        // base alignment slack
   static_assert(KP % 128 == 0 && VP % 16 == 0 && S::VSTAGE_BYTES % 1024 == 0, "alignment");
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
@@ -246,10 +249,14 @@ struct DecodeSmem {
 // Warp 0 copies, warp 1 issues the MMAs, warps 2 .. compute.
 // F8: eight compute warps (2-9; scoring E4M3 keys costs more per byte) and warps 10-11,
 // which widen the E4M3 V pages while the compute warps score.
-template <class S, bool F8>
+// SKIP: warp 0 copies keys only and warp 6 copies the value pages the compute warps keep.
+// (Eight compute warps measured slower there: more registers spilled and barrier traffic.)
+template <class S, bool F8, bool SKIP = false>
 constexpr int decode_compute_warps() { return (F8 && S::H % 8 == 0) ? 8 : 4; }
-template <class S, bool F8>
-constexpr int decode_threads() { return 32 * (2 + decode_compute_warps<S, F8>() + (F8 ? 2 : 0)); }
+template <class S, bool F8, bool SKIP = false>
+constexpr int decode_threads() {
+  return 32 * (2 + decode_compute_warps<S, F8, SKIP>() + (F8 ? 2 : 0) + (SKIP ? 1 : 0));
+}
 
 // Two E4M3 codes (low byte first) to an fp16 pair / fp32 pair; E4M3 values are exact in
 // fp16.  (Widening by integer bit moves instead measured slower: more instructions.)
@@ -321,10 +328,11 @@ struct BlockInfo {
 };
 
 
-template <class S, bool F8>
-__global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
+template <class S, bool F8, bool SKIP>
+__global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
     decode_main_kernel(const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
-  using L = DecodeSmem<S, F8>;
+  static_assert(!(F8 && SKIP), "block-sparse decode reads fp16 pages");
+  using L = DecodeSmem<S, F8, SKIP>;
   constexpr int KST = L::KST, VST = L::VST, VRS = L::VRS, HP = S::HP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -338,15 +346,17 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
   int* flags_s = reinterpret_cast<int*>(sm + L::F_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
   uint64_t* kfull = bars;                 // [KST]
-  uint64_t* kempty = kfull + KST;         // [KST] the four compute warps scored the page
+  uint64_t* kempty = kfull + KST;         // [KST] the compute warps scored the page
   uint64_t* vfull = kempty + KST;         // [VRS] a V page landed
   uint64_t* vempty = vfull + VRS;         // [VRS] its stage is free (MMA, or F8: widened)
   uint64_t* pfull = vempty + VRS;         // [2]
   uint64_t* pfree = pfull + 2;            // [2]
   uint64_t* vcvt = pfree + 2;             // F8 [VST] fp16 V stage written by warps 6-7
   uint64_t* vfree = vcvt + VST;           // F8 [VST] fp16 V stage read by its MMAs
-  constexpr int NTHR = decode_threads<S, F8>();
-  constexpr int NCW = decode_compute_warps<S, F8>();   // compute warps 2 .. NCW+1
+  uint64_t* decfull = pfree + 2 + (F8 ? 2 * VST : 0);   // SKIP [DS] a decision was posted
+  uint64_t* decempty = decfull + L::DS;                  // SKIP [DS] ... and taken
+  constexpr int NTHR = decode_threads<S, F8, SKIP>();
+  constexpr int NCW = decode_compute_warps<S, F8, SKIP>();   // compute warps 2 .. NCW+1
   // F8: V boxes widened by warps 10-11; the compute warps widen the remaining ones (a
   // split measured to balance the two groups' time per block)
   constexpr int WB = S::NBOX >= 16 ? 10 : S::NBOX;
@@ -357,6 +367,12 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
   // reads the block table or lengths from global memory on its critical path
   int* kinfo = reinterpret_cast<int*>(sm + L::INFO_OFF);
   int* vinfo = kinfo + KST;
+  // SKIP: the physical block of each K stage; the decision ring (physical block of each
+  // kept page, in order, -1 = no more pages); per P buffer 1 = first page of a segment,
+  // 0 = a later one, -1 = no more pages
+  int* kphys = vinfo + VRS;
+  int* dec_s = kphys + KST;
+  int* pinfo = dec_s + L::DS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -380,6 +396,12 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&pfull[i], NCW);
       mbar_init(&pfree[i], 1);
+    }
+    if constexpr (SKIP) {
+      for (int i = 0; i < L::DS; ++i) {
+        mbar_init(&decfull[i], 1);
+        mbar_init(&decempty[i], 1);
+      }
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -438,9 +460,11 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
         const int ks = static_cast<int>(it % KST);
         if (it >= KST && !mbar_wait(&kempty[ks], ((it / KST) - 1) & 1, abort_flag, p.dev_err)) break;
         kinfo[ks] = nvalid;
+        if constexpr (SKIP) kphys[ks] = static_cast<int>(phys);
         mbar_arrive_expect_tx(&kfull[ks], L::KP);
         bulk_g2s_hint(kst + ks * L::KP, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
         ++nk;
+        if constexpr (SKIP) continue;   // values wait until the page is known to be needed
         const int vs = static_cast<int>(it % VRS);
         if (it >= VRS && !mbar_wait(&vempty[vs], ((it / VRS) - 1) & 1, abort_flag, p.dev_err)) break;
         vinfo[vs] = nvalid;
@@ -469,7 +493,29 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc_f16(128, HP, /*a_mn_major=*/true, /*b_mn_major=*/false);
       int64_t issued = 0;
-      for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
+      if constexpr (SKIP) {
+        // kept pages only, in order; the info word of each P buffer says whether the page
+        // opens a segment (accumulator overwritten) or that no page follows
+        for (int64_t kk = 0;; ++kk) {
+          const int vs = static_cast<int>(kk % VST), ps = static_cast<int>(kk & 1);
+          if (!mbar_wait(&pfull[ps], (kk >> 1) & 1, abort_flag, p.dev_err)) break;
+          const int info = pinfo[ps];
+          if (info < 0) break;
+          if (!mbar_wait(&vfull[vs], (kk / VST) & 1, abort_flag, p.dev_err)) break;
+          tc_fence_after();
+          const uint32_t vaddr = smem_u32(vst + vs * S::VSTAGE_BYTES);
+          const uint64_t bdesc = make_sdesc(smem_u32(pbuf + ps * L::P_BYTES), 128, 256, kSwizzleNone);
+#pragma unroll
+          for (int i = 0; i < S::NCHUNK; ++i) {
+            const uint64_t adesc = make_sdesc(vaddr + i * 4096, 2048, 1024, kSwizzle128B);
+            umma_f16(tmem_base + i * HP, adesc, bdesc, idesc, info ? 0u : 1u);
+          }
+          umma_commit(&vempty[vs]);
+          umma_commit(&pfree[ps]);
+          ++issued;
+        }
+      }
+      for (int64_t g = g0, it = 0; !SKIP && g < g1; ++g, ++it) {
         walk.advance_to(g);
         const bool seg_first = (g == g0) || (g == walk.bstart);
         const int vs = static_cast<int>(it % VST), ps = static_cast<int>(it & 1);
@@ -488,6 +534,30 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
         ++issued;
       }
       if (issued > 0) mbar_wait_drain(&pfree[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
+    }
+  } else if (SKIP && warp == 2 + NCW) {
+    // ------------------------------------------ SKIP: value pages of the kept pages
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int64_t nv = 0;
+      for (int64_t n = 0;; ++n) {
+        const int ds = static_cast<int>(n % L::DS);
+        if (!mbar_wait(&decfull[ds], (n / L::DS) & 1, abort_flag, p.dev_err)) break;
+        const int phys = dec_s[ds];
+        mbar_arrive(&decempty[ds]);
+        if (phys < 0) break;
+        const int vs = static_cast<int>(nv % VST);
+        if (nv >= VST && !mbar_wait(&vempty[vs], ((nv / VST) - 1) & 1, abort_flag, p.dev_err)) break;
+        mbar_arrive_expect_tx(&vfull[vs], L::VP);
+#pragma unroll 1
+        for (int bx = 0; bx < S::NBOX; ++bx)
+          tma_load_2d_hint(vst + vs * S::VSTAGE_BYTES + bx * 2048, &tmap_v, bx * 64,
+                           phys * kBlockSize, &vfull[vs], pol);
+        ++nv;
+      }
+      if (*abort_flag)   // let copies already in flight land before the CTA exits
+        for (int64_t i = (nv > VST ? nv - VST : 0); i < nv; ++i)
+          mbar_wait_drain(&vfull[i % VST], (i / VST) & 1);
     }
   } else if (F8 && warp >= 2 + NCW) {
     // ------------------------------------------ F8: widen E4M3 V pages to fp16 stages
@@ -520,9 +590,16 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
     const int chunk0 = cw / 4;
     constexpr int CSTEP = NCW / 4;
     float m_run[ROUNDS], l_run[ROUNDS];
+    float mt[ROUNDS];   // SKIP: largest score of the segment's kept pages (log2 units)
 #pragma unroll
-    for (int r = 0; r < ROUNDS; ++r) { m_run[r] = -INFINITY; l_run[r] = 0.f; }
+    for (int r = 0; r < ROUNDS; ++r) { m_run[r] = -INFINITY; l_run[r] = 0.f; mt[r] = -INFINITY; }
     const float4* qs4 = reinterpret_cast<const float4*>(qs);
+    // warp cw takes heads cw*HPW .., two per round (one per half-warp)
+    auto head_ok = [&](int r) { return 2 * r + hl < HPW; };
+    auto head_of = [&](int r) { return cw * HPW + 2 * r + hl; };
+    int64_t kk = 0;     // pages accumulated so far (SKIP: the kept ones), orders P / V use
+    int64_t nd = 0;     // SKIP: decisions posted to the value-copy warp
+    bool aborted = false;
 
     for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
       walk.advance_to(g);
@@ -544,20 +621,22 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
       const int ks = static_cast<int>(it % KST);
       ok = mbar_wait(&kfull[ks], (it / KST) & 1, abort_flag, p.dev_err);
       bi.nvalid = kinfo[ks];
+      const int kph = SKIP ? kphys[ks] : 0;
       float s[ROUNDS];
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
-        const int hw = 2 * r + hl;
         s[r] = -INFINITY;
-        if (ok && hw < HPW) {
-          const int h = cw * HPW + hw;
+        if (ok && head_ok(r)) {
+          const int h = head_of(r);
+          const uint8_t* kstage = kst + ks * L::KP;
+          const int hk = h;
           // two packed fp32x2 accumulators = four independent chains
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
           if constexpr (F8) {
             // 16 E4M3 codes per 16-byte chunk; lanes 2u and 2u+1 start at chunk u so the
             // 16 tokens' 64-byte rows spread over all banks
             constexpr int NCH8 = S::RK / 16;
-            const uint8_t* krow = kst + ks * L::KP + (h * kBlockSize + t) * S::RK;
+            const uint8_t* krow = kstage + (hk * kBlockSize + t) * S::RK;
 #pragma unroll
             for (int v = 0; v < NCH8; ++v) {
               const int c8 = (v + (t >> 1)) % NCH8;
@@ -577,8 +656,8 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
               }
             }
           } else {
-            const __half* krow = reinterpret_cast<const __half*>(kst + ks * L::KP) +
-                                 (h * kBlockSize + t) * S::RK;
+            const __half* krow = reinterpret_cast<const __half*>(kstage) +
+                                 (hk * kBlockSize + t) * S::RK;
 #pragma unroll
             for (int v = 0; v < NCH; ++v) {
               const int c = (v + t) % NCH;   // rotation keeps the 16 lanes on distinct banks
@@ -611,8 +690,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
       bool need_any = false;
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
-        const int hw = 2 * r + hl;
-        valid[r] = ok && hw < HPW && t < bi.nvalid;
+        valid[r] = ok && head_ok(r) && t < bi.nvalid;
         sv[r] = valid[r] ? s[r] : -INFINITY;
         bmax[r] = sv[r];
       }
@@ -621,6 +699,16 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
 #pragma unroll
         for (int r = 0; r < ROUNDS; ++r)
           bmax[r] = fmaxf(bmax[r], __shfl_xor_sync(0xffffffffu, bmax[r], o));
+      }
+      // SKIP: the page is needed if one of this warp's heads has a score within skip_tau
+      // of its running maximum (the first page of a segment always is)
+      bool keep_mine = !SKIP;
+      if constexpr (SKIP) {
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+          const float ref = bi.seg_first ? -INFINITY : mt[r];
+          keep_mine |= head_ok(r) && !(bmax[r] < ref - p.skip_tau);
+        }
       }
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
@@ -637,30 +725,67 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
 #pragma unroll
         for (int r = 0; r < ROUNDS; ++r) psum[r] += __shfl_xor_sync(0xffffffffu, psum[r], o);
       }
+      // SKIP: the running state moves only once the page is known to be kept (computing
+      // the weights before the vote measured faster than after it: it keeps the vote off
+      // the path to the P write)
+      float l_new[ROUNDS];
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
-        l_run[r] = (bi.seg_first ? 0.f : l_run[r] * alpha[r]) + psum[r];
-        m_run[r] = m_new[r];
+        l_new[r] = (bi.seg_first ? 0.f : l_run[r] * alpha[r]) + psum[r];
+        if constexpr (!SKIP) {
+          l_run[r] = l_new[r];
+          m_run[r] = m_new[r];
+        }
       }
       const int fb = static_cast<int>(it & 1);
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
-        const int hw = 2 * r + hl;
-        if (t == 0 && hw < HPW) alpha_s[fb * HP + cw * HPW + hw] = alpha[r];
+        if (t == 0 && head_ok(r)) alpha_s[fb * HP + head_of(r)] = alpha[r];
       }
       const bool warp_need = __any_sync(0xffffffffu, need_any);
-      if (lane == 0) flags_s[fb * NCW + cw] = (warp_need ? 1 : 0) | (*abort_flag ? 2 : 0);
+      const bool warp_keep = SKIP ? __any_sync(0xffffffffu, keep_mine) : true;
+      if (lane == 0)
+        flags_s[fb * NCW + cw] = (warp_need ? 1 : 0) | (*abort_flag ? 2 : 0) | (warp_keep ? 4 : 0);
       named_bar_sync(1, CT);
       int f = 0;
 #pragma unroll
       for (int w2 = 0; w2 < NCW; ++w2) f |= flags_s[fb * NCW + w2];
-      if (f & 2) break;
+      if (f & 2) {
+        aborted = true;
+        break;
+      }
+      const bool kept = !SKIP || (f & 4);
+      if constexpr (SKIP) {
+        if (ctid == 0 && p.page_kept != nullptr)
+          p.page_kept[static_cast<int64_t>(p.qrow[walk.b]) * p.bt_stride + (g - walk.bstart)] =
+              kept ? 1 : 0;
+        if (kept) {
+          if (ctid == 0) {   // its value page: to the value-copy warp, as early as possible
+            const int ds = static_cast<int>(nd % L::DS);
+            if (nd < L::DS ||
+                mbar_wait(&decempty[ds], ((nd / L::DS) - 1) & 1, abort_flag, p.dev_err)) {
+              dec_s[ds] = kph;
+              mbar_arrive(&decfull[ds]);
+            }
+          }
+          ++nd;
+#pragma unroll
+          for (int r = 0; r < ROUNDS; ++r) {
+            l_run[r] = l_new[r];
+            m_run[r] = m_new[r];
+            mt[r] = bi.seg_first ? bmax[r] : fmaxf(mt[r], bmax[r]);
+          }
+        }
+      }
 
-      const int ps = static_cast<int>(it & 1);
-      if (it >= 2) ok = mbar_wait(&pfree[ps], ((it >> 1) - 1) & 1, abort_flag, p.dev_err) && ok;
+      // P buffer / V stage order of this page among the accumulated ones
+      const int64_t pi = SKIP ? kk : it;
+      const int ps = static_cast<int>(pi & 1);
+      if (kept) {
+      if (pi >= 2) ok = mbar_wait(&pfree[ps], ((pi >> 1) - 1) & 1, abort_flag, p.dev_err) && ok;
       if (f & 1) {
         // rescale the accumulator columns after the previous block's MMAs have landed
-        ok = mbar_wait(&pfree[(it - 1) & 1], ((it - 1) >> 1) & 1, abort_flag, p.dev_err) && ok;
+        ok = mbar_wait(&pfree[(pi - 1) & 1], ((pi - 1) >> 1) & 1, abort_flag, p.dev_err) && ok;
         ok = __all_sync(0xffffffffu, ok);   // TMEM loads / stores are warp-collective
         tc_fence_after();
         if (ok) {
@@ -689,9 +814,8 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
         uint8_t* pb = pbuf + ps * L::P_BYTES;
 #pragma unroll
         for (int r = 0; r < ROUNDS; ++r) {
-          const int hw = 2 * r + hl;
-          if (hw < HPW) {
-            const int h = cw * HPW + hw;
+          if (head_ok(r)) {
+            const int h = head_of(r);
             *reinterpret_cast<__half*>(pb + (h >> 3) * 256 + (t >> 3) * 128 + (h & 7) * 16 +
                                        (t & 7) * 2) = ph[r];
           }
@@ -710,8 +834,8 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
       if (!F8 && bi.nvalid < kBlockSize) {
         // tokens past the sequence end (or a rejected block): zero their V rows so that
         // whatever those slots hold cannot reach the accumulator through 0 * NaN
-        const int vs = static_cast<int>(it % VST);
-        ok = mbar_wait(&vfull[vs], (it / VST) & 1, abort_flag, p.dev_err) && ok;
+        const int vs = static_cast<int>(pi % VST);
+        ok = mbar_wait(&vfull[vs], (pi / VST) & 1, abort_flag, p.dev_err) && ok;
         const int nrow = kBlockSize - bi.nvalid;
         uint8_t* vb = vst + vs * S::VSTAGE_BYTES;
         for (int idx = ctid; idx < nrow * S::NBOX * 8; idx += CT) {
@@ -721,13 +845,19 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
               make_uint4(0, 0, 0, 0);
         }
       }
+      if constexpr (SKIP)
+        if (ctid == 0) pinfo[ps] = bi.seg_first ? 1 : 0;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pfull[ps]);
+      ++kk;
+      }   // kept
 
       if (bi.seg_last) {
-        ok = mbar_wait(&pfree[ps], (it >> 1) & 1, abort_flag, p.dev_err) && ok;
+        // the segment's last accumulated page (a segment's first page is always kept)
+        const int64_t last = SKIP ? kk - 1 : it;
+        ok = mbar_wait(&pfree[last & 1], (last >> 1) & 1, abort_flag, p.dev_err) && ok;
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         if (ok) {
@@ -753,15 +883,33 @@ __global__ void __launch_bounds__(decode_threads<S, F8>(), 1)
           }
 #pragma unroll
           for (int r = 0; r < ROUNDS; ++r) {
-            const int hw = 2 * r + hl;
-            if (t == 0 && hw < HPW) {
-              const int h = cw * HPW + hw;
+            if (t == 0 && head_ok(r)) {
+              const int h = head_of(r);
               rec[static_cast<size_t>(S::R) * HP + h] = m_run[r];
               rec[static_cast<size_t>(S::R) * HP + HP + h] = l_run[r];
             }
           }
         }
         tc_fence_before();
+      }
+    }
+    if constexpr (SKIP) {
+      if (!aborted) {
+        // no page follows: tell the MMA thread (the next P buffer's info word; its
+        // previous use was read before the MMAs the last record waited for) and the
+        // value-copy warp
+        const int ps = static_cast<int>(kk & 1);
+        if (ctid == 0) {
+          pinfo[ps] = -1;
+          const int ds = static_cast<int>(nd % L::DS);
+          if (nd < L::DS ||
+              mbar_wait(&decempty[ds], ((nd / L::DS) - 1) & 1, abort_flag, p.dev_err)) {
+            dec_s[ds] = -1;
+            mbar_arrive(&decfull[ds]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[ps]);
       }
     }
   }
@@ -907,13 +1055,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnPara
 template <class S>
 cudaError_t prepare_attn(int device) {
   (void)device;
-  cudaError_t e = cudaFuncSetAttribute(decode_main_kernel<S, false>,
+  cudaError_t e = cudaFuncSetAttribute(decode_main_kernel<S, false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DecodeSmem<S, false>::ALLOC);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_main_kernel<S, true>,
+    e = cudaFuncSetAttribute(decode_main_kernel<S, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DecodeSmem<S, true>::ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_main_kernel<S, false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecodeSmem<S, false, true>::ALLOC);
   return e;
 }
 
@@ -931,11 +1083,17 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStre
   if (e != cudaSuccess) return e;
   if (prof_start && (e = cudaEventRecord(prof_start, stream)) != cudaSuccess) return e;
   if (p.fp8_pages)
-    e = launch_pdl(decode_main_kernel<S, true>, dim3(p.parts), dim3(decode_threads<S, true>()),
-                   DecodeSmem<S, true>::ALLOC, stream, pdl, tmap_v, p);
+    e = launch_pdl(decode_main_kernel<S, true, false>, dim3(p.parts),
+                   dim3(decode_threads<S, true>()), DecodeSmem<S, true>::ALLOC, stream, pdl,
+                   tmap_v, p);
+  else if (p.sparse)
+    e = launch_pdl(decode_main_kernel<S, false, true>, dim3(p.parts),
+                   dim3(decode_threads<S, false, true>()), DecodeSmem<S, false, true>::ALLOC,
+                   stream, pdl, tmap_v, p);
   else
-    e = launch_pdl(decode_main_kernel<S, false>, dim3(p.parts), dim3(decode_threads<S, false>()),
-                   DecodeSmem<S, false>::ALLOC, stream, pdl, tmap_v, p);
+    e = launch_pdl(decode_main_kernel<S, false, false>, dim3(p.parts),
+                   dim3(decode_threads<S, false>()), DecodeSmem<S, false>::ALLOC, stream, pdl,
+                   tmap_v, p);
   if (e != cudaSuccess) return e;
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
   // small batches: four threads per slice element so that a request's many records are

@@ -147,6 +147,11 @@ struct AttnParams {
   int32_t nq;
   int32_t parts;              // decode CTAs (work partitions)
   int32_t fp8_pages;          // pages hold E4M3 codes (decode only)
+  // block-sparse decode: a page whose every head's largest score is more than skip_tau
+  // (log2 units) below that head's running maximum is left out, values unread
+  int32_t sparse;
+  float skip_tau;
+  uint8_t* page_kept;         // sparse, optional: [rows][bt_stride], 1 = page read, 0 = skipped
   int32_t late_wait;          // planning kernel may run alongside its predecessor (an append
                               // of the same step that it does not read) and waits at its end
   float qscale;               // log2(e) / sqrt(d)

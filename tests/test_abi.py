@@ -163,3 +163,26 @@ def test_prefill_crossover_and_reconstruct_workspace(lib):
     assert lib.rcp_prefill_crossover_rows(h, ctypes.byref(rows)) == _lib.RCP_OK
     assert rows.value == 2**31 - 1           # R <= d: rank space is never dearer
     lib.rcp_destroy_cache(h)
+
+
+def test_sparse_decode_host_checks(lib):
+    """Threshold range, page format and workspace are checked before any CUDA call."""
+    from rank_compressed_paged_gb300 import _lib
+    st, h = _create(lib, _lib, _cfg(_lib))
+    b = ctypes.c_size_t()
+    assert lib.rcp_workspace_size(h, 16, ctypes.byref(b)) == _lib.RCP_OK
+    ws = 0x100000
+    args = (h, 0x1000, 0x2000, 64, 0x3000, 16)
+    for bad in (1.0, -0.25, float("nan"), float("inf")):
+        assert lib.rcp_decode_attn_sparse(*args, bad, None, 0x4000, ws, b.value, None) \
+            == _lib.RCP_ERR_INVALID_ARG, bad
+    assert lib.rcp_decode_attn_sparse(*args, 0.01, None, 0x4000, ws, 1024, None) \
+        == _lib.RCP_ERR_WORKSPACE
+    assert lib.rcp_decode_attn_sparse(h, 0x1000, 0x2000, 64, 0x3000, 0, 0.01, None, 0x4000, ws,
+                                      b.value, None) == _lib.RCP_OK   # empty batch
+    lib.rcp_destroy_cache(h)
+    st, h8 = _create(lib, _lib, _cfg(_lib, fmt=_lib.RCP_PAGES_FP8_E4M3))
+    assert st == _lib.RCP_OK
+    assert lib.rcp_decode_attn_sparse(h8, 0x1000, 0x2000, 64, 0x3000, 16, 0.01, None, 0x4000, ws,
+                                      b.value, None) == _lib.RCP_ERR_UNSUPPORTED
+    lib.rcp_destroy_cache(h8)
