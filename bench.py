@@ -86,8 +86,15 @@ def measured_tensor_peak():
 
 
 def kernel_src_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the sha256 of the decode kernel source with its // comments
+    and blank lines removed (a comment edit does not change the kernel's traffic)."""
+    lines = []
+    with open(KERNEL_SRC) as f:
+        for ln in f.read().splitlines():
+            code = ln.split("//", 1)[0].rstrip()
+            if code:
+                lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
 def ncu_traffic_per_launch(summary=None):

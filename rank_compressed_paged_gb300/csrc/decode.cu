@@ -7,13 +7,17 @@
 //                   log2(e)/sqrt(d) so the softmax can use exp2.
 //   2. decode_main: persistent split-K kernel.  The concatenated list of all requests'
 //                   blocks is cut into `parts` equal contiguous ranges, one per CTA.  Per
-//                   block: a bulk copy brings the K page (all heads) and four tensor-map
-//                   copies bring the V page into shared memory; CUDA cores score the
-//                   block (warp per 2 heads x 16 tokens, one lane per token); an online
-//                   softmax with lazy rescaling turns scores into fp16 weights P; one
-//                   elected thread issues tcgen05 MMAs Z^T[R x heads] += C_v^T P^T into
-//                   tensor memory.  At the end of each (request, range) segment the
-//                   accumulator and the running (max, sum) go to a partial record.
+//                   block: a bulk copy brings the K page (all heads) and sixteen
+//                   tensor-map boxes bring the V page into shared memory; CUDA cores
+//                   score the block (a warp per 8 heads, 2 heads x 16 tokens per round,
+//                   one lane per token); an online softmax with lazy rescaling turns
+//                   scores into fp16 weights P; one elected thread issues tcgen05 MMAs
+//                   Z^T[R x heads] += C_v^T P^T into tensor memory.  At the end of each
+//                   (request, range) segment the accumulator and the running (max, sum)
+//                   go to a partial record.  Variants: E4M3 pages (codes widened to fp16
+//                   in shared memory) and block-sparse (a page's V is loaded only when
+//                   some head's weight in it reaches the threshold; "KV-cache LLM
+//                   serving" page, "What it measured", item 3).
 //   3. combine:     merges a request's partial records in a fixed order (deterministic)
 //                   and stores z as an fp16 (hi, lo) pair for the up-projection GEMM.
 //   4. (gemm.cu)    o_h = W_v[:, h*d:(h+1)*d]^T z_h on tensor cores, written as fp16.
