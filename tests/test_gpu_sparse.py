@@ -181,3 +181,73 @@ def test_sparse_b64_l8192_peaked_sampled():
         _check_valid(q[b:b + 1], hk, U, tab, lens[b:b + 1], masks[b:b + 1], 2.0 ** -8)
         ref = orc.decode_attn_kept(q[b:b + 1], hk, hv, U, W, tab, lens[b:b + 1], masks[b:b + 1])
         assert_close(out[b:b + 1], ref, what=f"sparse request {b}")
+
+
+def test_sparse_is_block_relabelling_invariant():
+    """Decisions depend on scores and page order only, not on physical block ids."""
+    inp = wl.make_decode_inputs(MAIN, [9000, 5000, 33], seed=68, spare_blocks=9,
+                                peaked=wl.PEAKED)
+    a, ka, _ = _run(inp, 2.0 ** -8)
+    c2 = wl.permute_physical_blocks(inp.cache, np.random.default_rng(4))
+    inp2 = wl.DecodeInputs(inp.shape, inp.U_k, inp.W_v, c2, inp.q)
+    b, kb, _ = _run(inp2, 2.0 ** -8)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    np.testing.assert_array_equal(ka, kb)
+    assert (ka[:, :1] == 1).all() and (ka == 0).any()
+
+
+def test_sparse_rejects_bad_block_ids_on_device():
+    """A bad id sets the error bit and its page contributes nothing; others unaffected."""
+    import torch
+    from rank_compressed_paged_gb300 import _lib
+    inp = wl.make_decode_inputs(MAIN, [3000, 3000], seed=69, peaked=wl.PEAKED)
+    c = inp.cache
+    table = c.block_table.copy()
+    table[1, 5] = c.k_pages.shape[0] + 7            # out-of-range physical id
+    cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    kept = torch.full(table.shape, UNTOUCHED, dtype=torch.uint8, device="cuda")
+    out = cache.decode_attn_sparse(t(inp.q), t(table), t(c.seq_lens), 2.0 ** -8,
+                                   page_kept=kept)
+    torch.cuda.synchronize()
+    assert cache.read_device_error() & _lib.RCP_DEVERR_BAD_BLOCK
+    o = out.cpu().numpy()
+    assert np.all(np.isfinite(o))
+    masks = _masks(kept.cpu().numpy(), c.seq_lens)
+    ref0 = orc.decode_attn_kept(inp.q[:1], c.k_pages, c.v_pages, inp.U_k, inp.W_v, table[:1],
+                                c.seq_lens[:1], masks[:1])
+    assert_close(o[:1], ref0, what="unaffected request")
+
+
+def test_sparse_decode_replays_from_a_cuda_graph():
+    import torch
+    inp = wl.make_decode_inputs(MAIN, [9000, 33, 4000, 0], seed=70, peaked=wl.PEAKED)
+    c = inp.cache
+    cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    q, table, lens = t(inp.q), t(c.block_table), t(c.seq_lens)
+    ws = cache.workspace(q.shape[0])
+    kept = torch.zeros(c.block_table.shape, dtype=torch.uint8, device="cuda")
+    eager = cache.decode_attn_sparse(q, table, lens, 2.0 ** -8, page_kept=kept,
+                                     workspace=ws).clone()
+    eager_kept = kept.clone()
+    out = torch.empty_like(q)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # warm the capture stream
+        cache.decode_attn_sparse(q, table, lens, 2.0 ** -8, page_kept=kept, out=out,
+                                 workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    out.fill_(float("nan"))
+    kept.fill_(9)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cache.decode_attn_sparse(q, table, lens, 2.0 ** -8, page_kept=kept, out=out,
+                                 workspace=ws)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    assert np.array_equal(eager.cpu().numpy().view(np.uint16), out.cpu().numpy().view(np.uint16))
+    n = [wl.blocks_needed(int(x)) for x in c.seq_lens]
+    for b in range(len(n)):
+        assert np.array_equal(eager_kept[b, :n[b]].cpu().numpy(), kept[b, :n[b]].cpu().numpy())
