@@ -519,7 +519,12 @@ def run_prefill(args):
     slots = td(np.array([wl.slot_for(table, b, prior + i) for b in range(B) for i in range(chunk)],
                         np.int64))
     cu = td((np.arange(B + 1) * chunk).astype(np.int32))
-    cache = PagedCoeffCache(32, 128, 64, 1024, kp.shape[0], td(U), td(W), k_pages=kp, v_pages=vp)
+    if args.pages == "fp8_e4m3":   # the same seeded coefficients as E4M3 codes
+        kp = kp.to(torch.float8_e4m3fn).view(torch.uint8)
+        vp = vp.to(torch.float8_e4m3fn).view(torch.uint8)
+        torch.cuda.empty_cache()
+    cache = PagedCoeffCache(32, 128, 64, 1024, kp.shape[0], td(U), td(W), k_pages=kp, v_pages=vp,
+                            page_format=args.pages)
     tab, ln = td(table), td(lens)
     out = torch.empty_like(q)
     ws = cache.workspace(T)
@@ -528,7 +533,8 @@ def run_prefill(args):
     variant = args.prefill_variant
     if variant == "auto":
         from rank_compressed_paged_gb300 import RECONSTRUCT_MIN_CHUNK
-        variant = "reconstruct" if chunk >= RECONSTRUCT_MIN_CHUNK else "rank"
+        variant = "reconstruct" if (chunk >= RECONSTRUCT_MIN_CHUNK or
+                                    args.pages == "fp8_e4m3") else "rank"
     if variant == "reconstruct":
         ws = cache.workspace(T, cache.reconstruct_workspace_bytes(T, B, table.shape[1]))
 
@@ -564,10 +570,11 @@ def run_prefill(args):
         "variant": variant,
         "value": round((attn_f + app_f) / (step_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
         "ms_per_step": round(step_ms, 3), "steps": args.steps, "warmup": max(args.warmup, 3),
-        "higher_is_better": True, "dtype": "f16", "data": "synthetic",
+        "higher_is_better": True, "data": "synthetic",
+        "dtype": "f16" if args.pages == "fp16" else "e4m3 pages widened to f16, f16/f32 arithmetic",
         "config": {"workload": f"prefill_b{B}_p{prior}_c{chunk}", "batch": B, "prior": prior,
                    "chunk": chunk, "algorithmic_flops": attn_f + app_f,
-                   "step": "append the chunk (T = B*chunk tokens) + chunk attention",
+                   "step": "append the chunk (T = B*chunk tokens) + chunk attention", "pages": args.pages,
                    "value_flops": "rank-space work of the method, the same for both variants"},
         "roofline": {"bound": "tensor",
                      "kernel": "prefill_kernel" if variant == "rank"

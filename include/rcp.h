@@ -58,8 +58,9 @@ typedef enum rcp_status {
 #define RCP_PAGES_FP16 0      /* IEEE fp16 coefficients */
 #define RCP_PAGES_FP8_E4M3 1  /* E4M3 codes (OCP 8-bit float: bias 7, 3 mantissa bits, max
                                  448): the append rounds to nearest even and saturates to
-                                 +-448; half the bytes per token.  Decode only: the prefill
-                                 entry points return RCP_ERR_UNSUPPORTED for such a cache. */
+                                 +-448; half the bytes per token.  Append, decode and the
+                                 reconstructing prefill; rcp_prefill_attn and the
+                                 block-sparse decode return RCP_ERR_UNSUPPORTED. */
 
 typedef struct rcp_cache_config {
   int32_t num_heads;   /* H */
@@ -159,7 +160,8 @@ rcp_status rcp_decode_step(rcp_cache* cache, const void* k, const void* v,
  * cu_chunk_lens[b+1]-1 of q [num_query_rows][H][d]; seq_lens[b] counts prior + chunk
  * tokens; chunk row i sits at position seq_lens[b] - chunk_b + i and attends keys
  * 0 .. that position (causal).  out [num_query_rows][H][d] fp16.  workspace must hold
- * rcp_workspace_size(cache, num_query_rows) bytes. */
+ * rcp_workspace_size(cache, num_query_rows) bytes.  fp16 pages only (RCP_ERR_UNSUPPORTED
+ * for E4M3 pages: use rcp_prefill_attn_reconstruct). */
 rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_chunk_lens,
                             int32_t num_query_rows, const int32_t* block_table,
                             int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
@@ -175,7 +177,10 @@ rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_c
  * the rank-space variant once a request's chunk has more than rcp_prefill_crossover_rows
  * rows.  workspace must hold rcp_prefill_reconstruct_workspace_size(cache, num_query_rows,
  * batch, max_blocks_per_seq) bytes (256-byte aligned; it grows with the pages the batch
- * can reach, 2 * H * d * 16 bytes per page). */
+ * can reach, 2 * H * d * 16 bytes per page).  E4M3 pages: every page the batch reads is
+ * first widened to fp16 (exact) in the workspace, which then also holds
+ * 2 * 16 * (H * r_k + R) + 4 bytes per page the batch can reach; the result is that of the
+ * same call on fp16 pages holding the decoded codes. */
 rcp_status rcp_prefill_attn_reconstruct(rcp_cache* cache, const void* q,
                                         const int32_t* cu_chunk_lens, int32_t num_query_rows,
                                         const int32_t* block_table, int32_t max_blocks_per_seq,

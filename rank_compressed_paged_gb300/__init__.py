@@ -37,7 +37,8 @@ class PagedCoeffCache:
     Owns (as torch tensors) the K pages [num_blocks][H][16][r_k], V pages
     [num_blocks][16][R], the factors, a device error word and a reusable workspace; the
     library handle borrows their pointers.  page_format "fp16" stores fp16 coefficients,
-    "fp8_e4m3" stores E4M3 codes (uint8 tensors; decode and append only).
+    "fp8_e4m3" stores E4M3 codes (uint8 tensors; prefill on them takes the reconstructing
+    variant, which first widens the pages it reads to fp16 in the workspace).
     """
 
     def __init__(self, num_heads: int, head_dim: int, rank_k: int, rank_v: int,
@@ -208,7 +209,8 @@ class PagedCoeffCache:
         B = int(seq_lens.shape[0])
         mb = int(block_table.shape[1])
         if variant == "auto":
-            variant = "reconstruct" if B > 0 and rows >= B * RECONSTRUCT_MIN_CHUNK else "rank"
+            variant = "reconstruct" if (self.page_format == "fp8_e4m3" or
+                                        (B > 0 and rows >= B * RECONSTRUCT_MIN_CHUNK)) else "rank"
         if variant not in ("rank", "reconstruct"):
             raise ValueError(f"unknown prefill variant {variant!r}")
         if out is None:

@@ -164,17 +164,28 @@ void fill_ws(rcp::AttnParams& p, void* ws, int64_t nq) {
   p.vhat = nullptr;
 }
 
+// E4M3 pages: fp16 copies of the batch's pages for the reconstructing prefill
+struct Widened {
+  void* k16;
+  void* v16;
+  int32_t* table16;
+};
+
 template <class S>
-void fill_recon(rcp::AttnParams& p, void* ws, int64_t nq, int64_t batch, int64_t max_blocks) {
-  const rcp::ReconLayout r = rcp::recon_layout<S>(nq, batch, max_blocks);
+Widened fill_recon(rcp::AttnParams& p, void* ws, int64_t nq, int64_t batch, int64_t max_blocks,
+                   bool widen) {
+  const rcp::ReconLayout r = rcp::recon_layout<S>(nq, batch, max_blocks, widen);
   uint8_t* b = static_cast<uint8_t*>(ws);
   p.vcum = reinterpret_cast<int64_t*>(b + r.vcum);
   p.vhat = b + r.vhat;
+  if (!widen) return Widened{nullptr, nullptr, nullptr};
+  return Widened{b + r.kw, b + r.vw, reinterpret_cast<int32_t*>(b + r.tw)};
 }
 
 size_t recon_ws_bytes(const rcp_cache* c, int64_t nq, int64_t batch, int64_t max_blocks) {
-  return c->shape == kShapeMain ? rcp::recon_layout<ShapeMain>(nq, batch, max_blocks).total
-                                : rcp::recon_layout<ShapeTiny>(nq, batch, max_blocks).total;
+  const bool widen = c->cfg.page_format == RCP_PAGES_FP8_E4M3;
+  return c->shape == kShapeMain ? rcp::recon_layout<ShapeMain>(nq, batch, max_blocks, widen).total
+                                : rcp::recon_layout<ShapeTiny>(nq, batch, max_blocks, widen).total;
 }
 
 // Block-sparse decode options (rcp_decode_attn_sparse).
@@ -235,7 +246,9 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   if (c->shape == kShapeMain) fill_ws<ShapeMain>(p, ws, nq);
   else fill_ws<ShapeTiny>(p, ws, nq);
   const bool pdl = c->prof_start == nullptr;
-  if (cu_chunk && p.fp8_pages) return RCP_ERR_UNSUPPORTED;   // prefill reads fp16 pages
+  // the prefill kernels read fp16 pages; E4M3 pages are widened first (reconstructing
+  // variant only: its workspace is sized by the pages the batch can reach)
+  if (cu_chunk && p.fp8_pages && !recon) return RCP_ERR_UNSUPPORTED;
   if (cu_chunk) {
     // chunked prefill: plan + fp16 rank-space queries, then the tiled tensor-core kernel
     const uint64_t hq = static_cast<uint64_t>(c->cfg.num_heads) * 64;
@@ -252,15 +265,36 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
       return RCP_ERR_CUDA;
     // reconstructing variant: V^ rows for at most batch x max_blocks_per_seq pages
     const int64_t max_pages = static_cast<int64_t>(batch) * max_blocks_per_seq;
-    CUtensorMap vhat_map = c->tmap_v;
+    const bool widen = recon && p.fp8_pages;
+    CUtensorMap vhat_map = c->tmap_v, kp16_map = c->tmap_kp, vp16_map = c->tmap_v;
+    Widened wd{nullptr, nullptr, nullptr};
+    rcp::AttnParams pw = p;   // the widening pass reads the cache's own pages and table
     if (recon) {
       if (max_pages * 16 >= (int64_t{1} << 31)) return RCP_ERR_UNSUPPORTED;
-      if (c->shape == kShapeMain) fill_recon<ShapeMain>(p, ws, nq, batch, max_blocks_per_seq);
-      else fill_recon<ShapeTiny>(p, ws, nq, batch, max_blocks_per_seq);
+      if (widen && max_pages * c->cfg.num_heads * 16 >= (int64_t{1} << 31)) return RCP_ERR_UNSUPPORTED;
+      wd = c->shape == kShapeMain
+               ? fill_recon<ShapeMain>(p, ws, nq, batch, max_blocks_per_seq, widen)
+               : fill_recon<ShapeTiny>(p, ws, nq, batch, max_blocks_per_seq, widen);
       if (!encode_2d(&vhat_map, p.vhat, hdq, static_cast<uint64_t>(max_pages) * 16, hdq * 2, 64, 128))
         return RCP_ERR_CUDA;
+      if (widen) {
+        pw = p;   // with the plan's page prefix sums
+        const uint64_t rk = c->cfg.rank_k, rv = c->cfg.rank_v;
+        if (!encode_2d(&kp16_map, wd.k16, rk,
+                       static_cast<uint64_t>(max_pages) * c->cfg.num_heads * 16, rk * 2, 64, 16) ||
+            !encode_2d(&vp16_map, wd.v16, rv, static_cast<uint64_t>(max_pages) * 16, rv * 2, 64, 16))
+          return RCP_ERR_CUDA;
+        // the kernels after the widening pass read the fp16 copies
+        p.k_pages = wd.k16;
+        p.v_pages = wd.v16;
+        p.block_table = wd.table16;
+        p.num_blocks = max_pages;
+        p.fp8_pages = 0;
+      }
     }
     const CUtensorMap& vals = recon ? vhat_map : c->tmap_v;
+    const CUtensorMap& kmap = widen ? kp16_map : c->tmap_kp;
+    const CUtensorMap& vsrc = widen ? vp16_map : c->tmap_v;
     if (c->shape == kShapeMain) {
       e = rcp::launch_plan<ShapeMain>(p, s, pdl);
       if (e == cudaSuccess)
@@ -268,10 +302,13 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
                                               c->dev_err, s, pdl);
       // profiling events bracket the attention proper: reconstruction + prefill kernel
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
+      if (e == cudaSuccess && widen)
+        e = rcp::launch_widen<ShapeMain>(pw, wd.k16, wd.v16, wd.table16, max_pages, c->num_sms, s,
+                                         pdl);
       if (e == cudaSuccess && recon)
-        e = rcp::launch_recon<ShapeMain>(c->tmap_v, c->tmap_wv_mn, p, max_pages, s, pdl);
+        e = rcp::launch_recon<ShapeMain>(vsrc, c->tmap_wv_mn, p, max_pages, s, pdl);
       if (e == cudaSuccess)
-        e = rcp::launch_prefill<ShapeMain>(qhi_map, qlo_map, c->tmap_kp, vals, c->tmap_wv_mn, p,
+        e = rcp::launch_prefill<ShapeMain>(qhi_map, qlo_map, kmap, vals, c->tmap_wv_mn, p,
                                            max_tiles, s, pdl, recon);
     } else {
       e = rcp::launch_plan<ShapeTiny>(p, s, pdl);
@@ -280,10 +317,13 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
                                               c->dev_err, s, pdl);
       // profiling events bracket the attention proper: reconstruction + prefill kernel
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
+      if (e == cudaSuccess && widen)
+        e = rcp::launch_widen<ShapeTiny>(pw, wd.k16, wd.v16, wd.table16, max_pages, c->num_sms, s,
+                                         pdl);
       if (e == cudaSuccess && recon)
-        e = rcp::launch_recon<ShapeTiny>(c->tmap_v, c->tmap_wv_mn, p, max_pages, s, pdl);
+        e = rcp::launch_recon<ShapeTiny>(vsrc, c->tmap_wv_mn, p, max_pages, s, pdl);
       if (e == cudaSuccess)
-        e = rcp::launch_prefill<ShapeTiny>(qhi_map, qlo_map, c->tmap_kp, vals, c->tmap_wv_mn, p,
+        e = rcp::launch_prefill<ShapeTiny>(qhi_map, qlo_map, kmap, vals, c->tmap_wv_mn, p,
                                            max_tiles, s, pdl, recon);
     }
     if (e == cudaSuccess && c->prof_stop) e = cudaEventRecord(c->prof_stop, s);

@@ -29,6 +29,10 @@ cudaError_t prepare_recon();
 template <class S>
 cudaError_t launch_recon(const CUtensorMap& vp, const CUtensorMap& w_v_mn, const AttnParams& p,
                          int64_t max_pages, cudaStream_t stream, bool pdl);
+// E4M3 pages: fp16 copies of the batch's pages (plan order) and the re-addressed table.
+template <class S>
+cudaError_t launch_widen(const AttnParams& p, void* k16, void* v16, int32_t* table16,
+                         int64_t max_pages, int num_sms, cudaStream_t stream, bool pdl);
 template <class S>
 cudaError_t prepare_gemm();
 // k_rows / v_rows: tensor maps over the new tokens' k and v ([T][H*d], box 64 x NT with

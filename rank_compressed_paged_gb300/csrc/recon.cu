@@ -19,6 +19,7 @@
 //     its sequence (so that the attention can never meet 0 * NaN there).
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -202,7 +203,82 @@ __global__ void __launch_bounds__(kRcThreads, 2)
   }
 }
 
+// ------------------------------------------------------------- E4M3 pages for prefill
+// The prefill kernels read fp16 pages through tensor maps.  For a cache of E4M3 pages the
+// reconstructing prefill first widens every page the batch reads (the plan's page order,
+// as for V^) into fp16 copies in the workspace and re-addresses the block table to them;
+// E4M3 values are exact in fp16, so the kernels that follow compute the same result as
+// on the codes themselves.  A streaming pass: 48 KiB read and 96 KiB written per page.
+constexpr int kWidenThreads = 256;
+
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t codes) {   // low byte -> low half
+  const __half2_raw r =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+template <class S>
+__global__ void __launch_bounds__(kWidenThreads)
+    widen_pages_kernel(const AttnParams p, __half* k16, __half* v16, int32_t* table16) {
+  constexpr int KB8 = S::H * kBlockSize * S::RK;   // bytes of an E4M3 key page
+  constexpr int VB8 = kBlockSize * S::R;           // bytes of an E4M3 value page
+  constexpr int KC = KB8 / 16, VC = VB8 / 16;      // 16-byte chunks of codes
+  static_assert(KB8 % 16 == 0 && VB8 % 16 == 0, "page size");
+  __shared__ int64_t s_phys;
+  griddep_wait();   // page prefix sums (plan) and the appended chunk are visible
+  griddep_launch();
+  const int64_t total = p.vcum[p.batch];
+  const uint8_t* k8 = static_cast<const uint8_t*>(p.k_pages);
+  const uint8_t* v8 = static_cast<const uint8_t*>(p.v_pages);
+  for (int64_t g = blockIdx.x; g < total; g += gridDim.x) {   // uniform over the CTA
+    if (threadIdx.x == 0) {
+      int lo = 0, hi = p.batch;                 // request b with vcum[b] <= g < vcum[b+1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.vcum[mid] <= g) lo = mid; else hi = mid;
+      }
+      const int64_t j = g - p.vcum[lo];
+      const int64_t at = static_cast<int64_t>(lo) * p.bt_stride + j;
+      int64_t id = p.block_table[at];
+      if (id < 0 || id >= p.num_blocks) {
+        atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
+        id = -1;
+      }
+      table16[at] = id < 0 ? -1 : static_cast<int32_t>(g);
+      s_phys = id;
+    }
+    __syncthreads();
+    const int64_t phys = s_phys;
+    if (phys >= 0) {
+      const uint4* ks = reinterpret_cast<const uint4*>(k8 + phys * KB8);
+      const uint4* vs = reinterpret_cast<const uint4*>(v8 + phys * VB8);
+      uint4* kd = reinterpret_cast<uint4*>(k16 + g * KB8);
+      uint4* vd = reinterpret_cast<uint4*>(v16 + g * VB8);
+      for (int c = threadIdx.x; c < KC + VC; c += kWidenThreads) {
+        const bool key = c < KC;
+        const uint4 raw = key ? ks[c] : vs[c - KC];
+        uint4* dst = key ? kd + 2 * c : vd + 2 * (c - KC);
+        dst[0] = make_uint4(widen_e4m3x2(raw.x), widen_e4m3x2(raw.x >> 16), widen_e4m3x2(raw.y),
+                            widen_e4m3x2(raw.y >> 16));
+        dst[1] = make_uint4(widen_e4m3x2(raw.z), widen_e4m3x2(raw.z >> 16), widen_e4m3x2(raw.w),
+                            widen_e4m3x2(raw.w >> 16));
+      }
+    }
+    __syncthreads();   // s_phys is rewritten for the next page
+  }
+}
+
 // --------------------------------------------------------------------------- launches
+template <class S>
+cudaError_t launch_widen(const AttnParams& p, void* k16, void* v16, int32_t* table16,
+                         int64_t max_pages, int num_sms, cudaStream_t stream, bool pdl) {
+  if (max_pages <= 0) return cudaSuccess;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;   // grid-stride over the pages
+  const unsigned grid = static_cast<unsigned>(max_pages < cap ? max_pages : cap);
+  return launch_pdl(widen_pages_kernel<S>, dim3(grid), dim3(kWidenThreads), 0, stream, pdl, p,
+                    static_cast<__half*>(k16), static_cast<__half*>(v16), table16);
+}
+
 template <class S>
 cudaError_t prepare_recon() {
   return cudaFuncSetAttribute(recon_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -229,5 +305,9 @@ template cudaError_t launch_recon<ShapeMain>(const CUtensorMap&, const CUtensorM
                                              const AttnParams&, int64_t, cudaStream_t, bool);
 template cudaError_t launch_recon<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
                                              const AttnParams&, int64_t, cudaStream_t, bool);
+template cudaError_t launch_widen<ShapeMain>(const AttnParams&, void*, void*, int32_t*, int64_t, int,
+                                             cudaStream_t, bool);
+template cudaError_t launch_widen<ShapeTiny>(const AttnParams&, void*, void*, int32_t*, int64_t, int,
+                                             cudaStream_t, bool);
 
 }  // namespace rcp

@@ -99,15 +99,24 @@ inline WsLayout ws_layout(int64_t nq) {
 // its per-request block prefix sums and the reconstructed values V^ start where they
 // start, for at most batch x max_blocks_per_seq pages.
 struct ReconLayout {
-  size_t vcum, vhat, total;
+  size_t vcum, vhat, kw, vw, tw, total;
 };
+// widen (E4M3 pages): also fp16 copies of the pages the batch reads, [pages][H][16][r_k]
+// and [pages][16][R], and the block table re-addressed to them, [batch][max_blocks].
 template <class S>
-inline ReconLayout recon_layout(int64_t nq, int64_t batch, int64_t max_blocks) {
+inline ReconLayout recon_layout(int64_t nq, int64_t batch, int64_t max_blocks, bool widen = false) {
   const WsLayout w = ws_layout<S>(nq);
+  const size_t pages = static_cast<size_t>(batch) * max_blocks;
   ReconLayout r;
   size_t o = w.rec;
   r.vcum = o;  o = align256(o + sizeof(int64_t) * (batch + 1));
-  r.vhat = o;  o = align256(o + 2 * static_cast<size_t>(batch) * max_blocks * kBlockSize * S::H * S::D);
+  r.vhat = o;  o = align256(o + 2 * pages * kBlockSize * S::H * S::D);
+  r.kw = r.vw = r.tw = 0;
+  if (widen) {
+    r.kw = o;  o = align256(o + 2 * pages * S::H * kBlockSize * S::RK);
+    r.vw = o;  o = align256(o + 2 * pages * kBlockSize * S::R);
+    r.tw = o;  o = align256(o + sizeof(int32_t) * pages);
+  }
   r.total = o > w.total ? o : w.total;
   return r;
 }

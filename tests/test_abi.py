@@ -186,3 +186,20 @@ def test_sparse_decode_host_checks(lib):
     assert lib.rcp_decode_attn_sparse(h8, 0x1000, 0x2000, 64, 0x3000, 16, 0.01, None, 0x4000, ws,
                                       b.value, None) == _lib.RCP_ERR_UNSUPPORTED
     lib.rcp_destroy_cache(h8)
+
+
+def test_reconstruct_workspace_grows_by_the_widened_pages_for_e4m3(lib):
+    """E4M3 pages: the reconstructing prefill's workspace also holds fp16 copies of the
+    pages the batch can reach (2 * 16 * (H r_k + R) bytes each) and their table (4 bytes)."""
+    from rank_compressed_paged_gb300 import _lib
+    st, h16 = _create(lib, _lib, _cfg(_lib))
+    st8, h8 = _create(lib, _lib, _cfg(_lib, fmt=_lib.RCP_PAGES_FP8_E4M3))
+    assert st == st8 == _lib.RCP_OK
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.rcp_prefill_reconstruct_workspace_size(h16, 64, 16, 272, ctypes.byref(a)) == 0
+    assert lib.rcp_prefill_reconstruct_workspace_size(h8, 64, 16, 272, ctypes.byref(b)) == 0
+    pages = 16 * 272
+    extra = pages * 2 * 16 * (32 * 64 + 1024) + pages * 4
+    assert extra <= b.value - a.value <= extra + 3 * 256
+    lib.rcp_destroy_cache(h16)
+    lib.rcp_destroy_cache(h8)

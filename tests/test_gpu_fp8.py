@@ -111,22 +111,24 @@ def test_fp8_decode_step_equals_append_then_decode():
     inp = wl.make_decode_inputs(MAIN, [300, 17, 1024, 0], seed=86, append=True)
     c = inp.cache
     kp8, vp8 = _codes(c.k_pages), _codes(c.v_pages)
-    a = _fp8_cache(MAIN, inp.U_k, inp.W_v, kp8, vp8)
+    # coordinate-selection factors: the appended codes are exact on both sides, so the
+    # oracle's own append gives the GPU's pages
+    U, W = wl.selection_factors(np.random.default_rng(186), 32, 128, 64, 1024)
+    a = _fp8_cache(MAIN, U, W, kp8, vp8)
     a.append_kv(t(inp.new_k), t(inp.new_v), t(inp.slot_mapping))
     oa = a.decode_attn(t(inp.q), t(c.block_table), t(c.seq_lens))
-    b = _fp8_cache(MAIN, inp.U_k, inp.W_v, kp8, vp8)
+    b = _fp8_cache(MAIN, U, W, kp8, vp8)
     ob = b.decode_step(t(inp.new_k), t(inp.new_v), t(inp.slot_mapping), t(inp.q),
                        t(c.block_table), t(c.seq_lens))
     torch.cuda.synchronize()
     assert np.array_equal(oa.cpu().numpy().view(np.uint16), ob.cpu().numpy().view(np.uint16))
-    # and the step's result is the oracle's on the pages the GPU appended
-    ref = orc.decode_attn(inp.q, orc.e4m3_decode(b.k_pages.cpu().numpy()),
-                          orc.e4m3_decode(b.v_pages.cpu().numpy()), inp.U_k, inp.W_v,
+    ko, vo = orc.append_kv_fp8(kp8, vp8, U, W, inp.new_k, inp.new_v, inp.slot_mapping, 16)
+    ref = orc.decode_attn(inp.q, orc.e4m3_decode(ko), orc.e4m3_decode(vo), U, W,
                           c.block_table, c.seq_lens, 16)
     assert_close(ob.cpu().numpy(), ref, what="fp8 step")
 
 
-def test_fp8_cache_rejects_prefill():
+def test_fp8_cache_rejects_rank_space_prefill():
     from rank_compressed_paged_gb300 import RcpError
     inp = wl.make_prefill_inputs(MAIN, [40], [20], seed=87)
     c = inp.cache
@@ -134,3 +136,47 @@ def test_fp8_cache_rejects_prefill():
     with pytest.raises(RcpError):
         cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
                            t(inp.seq_lens_after), variant="rank")
+
+
+@pytest.mark.parametrize("shape,prior,chunk,seed", [
+    (TINY, [37, 0, 100, 5], [21, 16, 40, 0], 88),
+    (MAIN, [300, 0, 1024, 17], [64, 130, 3, 1], 89),
+])
+def test_fp8_prefill_on_oracle_pages(shape, prior, chunk, seed):
+    """Every page, the chunk's included, holds the oracle's own E4M3 codes; the GPU runs
+    the prefill alone (widening pass, reconstruction, attention)."""
+    import torch
+    inp = wl.make_prefill_inputs(shape, prior, chunk, seed=seed, fill=np.nan)
+    c = inp.cache
+    ko, vo = orc.append_kv_fp8(_codes(c.k_pages), _codes(c.v_pages), inp.U_k, inp.W_v, inp.k,
+                               inp.v, inp.slot_mapping, 16)
+    cache = _fp8_cache(shape, inp.U_k, inp.W_v, ko, vo)
+    out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
+                             t(inp.seq_lens_after))
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    ref = orc.prefill_attn(inp.q, inp.cu_chunk_lens, orc.e4m3_decode(ko), orc.e4m3_decode(vo),
+                           inp.U_k, inp.W_v, c.block_table, inp.seq_lens_after, 16)
+    assert_close(out.cpu().numpy(), ref, what="fp8 prefill")
+    # the pages themselves are untouched by the widening pass
+    assert np.array_equal(cache.k_pages.cpu().numpy(), ko)
+    assert np.array_equal(cache.v_pages.cpu().numpy(), vo)
+
+
+def test_fp8_prefill_after_its_own_append():
+    """Chunk appended by the GPU (selection factors: exact codes), then the prefill."""
+    import torch
+    inp = wl.make_prefill_inputs(MAIN, [500, 64, 0], [100, 33, 16], seed=90, fill=np.nan)
+    c = inp.cache
+    U, W = wl.selection_factors(np.random.default_rng(190), 32, 128, 64, 1024)
+    kp8, vp8 = _codes(c.k_pages), _codes(c.v_pages)
+    cache = _fp8_cache(MAIN, U, W, kp8, vp8)
+    cache.append_kv(t(inp.k), t(inp.v), t(inp.slot_mapping))
+    out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
+                             t(inp.seq_lens_after))
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    ko, vo = orc.append_kv_fp8(kp8, vp8, U, W, inp.k, inp.v, inp.slot_mapping, 16)
+    ref = orc.prefill_attn(inp.q, inp.cu_chunk_lens, orc.e4m3_decode(ko), orc.e4m3_decode(vo),
+                           U, W, c.block_table, inp.seq_lens_after, 16)
+    assert_close(out.cpu().numpy(), ref, what="fp8 prefill after append")
