@@ -55,7 +55,10 @@ struct PfSmem {
   static constexpr int V_BYTES = C::KT * VN * 2;        // value tile
   static constexpr int STAGE = K_BYTES + V_BYTES;
   static constexpr int NS = RECON ? 3 : 2;              // key/value pipeline stages
-  static constexpr int P_BYTES = 128 * C::KT * 2;
+  // RECON keeps P in tensor memory (two buffers at columns P_TM and P_TM + KT/2, the A
+  // operand of the value MMA); the rank-space variant stages it in shared memory
+  static constexpr int P_BYTES = RECON ? 0 : 128 * C::KT * 2;
+  static constexpr int P_TM = 256 + VN;
   static constexpr int ST_OFF = 2 * Q_BYTES;            // q~ hi at 0, q~ lo at Q_BYTES
   static constexpr int P_OFF = ST_OFF + NS * STAGE;
   static constexpr int ZH_OFF = ST_OFF;                 // epilogue reuses the stage memory
@@ -64,7 +67,7 @@ struct PfSmem {
   static constexpr int W_BYTES = C::RQ * S::D * 2;
   static constexpr int END = (RECON || P_OFF + P_BYTES > W_OFF + W_BYTES) ? P_OFF + P_BYTES
                                                                              : W_OFF + W_BYTES;
-  static constexpr int NBAR = 9 + 4 * NS;
+  static constexpr int NBAR = 11 + 4 * NS;
   static constexpr int BAR_OFF = END;                   // NBAR mbarriers
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;   // tmem slot, abort flag
   static constexpr int TOTAL = MISC_OFF + 16;
@@ -74,6 +77,7 @@ struct PfSmem {
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
   static_assert(NQ == 1 || NQ * RPC * S::D * 4 <= 2 * 128 * C::RQ * 2, "receive buffer");
   static_assert(256 + VN <= 512 && S::D <= 128, "tensor memory budget");
+  static_assert(!RECON || P_TM + C::KT <= TMEM_COLS, "P buffers in tensor memory");
 };
 
 template <class S, bool RECON>
@@ -97,9 +101,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t* k_empty = v_full + NS;          // [NS] score MMA of the stage's tile done
   uint64_t* v_empty = k_empty + NS;         // [NS] value MMA of the stage's tile done
   uint64_t* s_full = v_empty + NS;          // [2] scores of a tile in TMEM
-  uint64_t* p_full = s_full + 2;            // softmax weights written (4 warps)
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* acc_done = pv_done + 1;
+  uint64_t* p_full = s_full + 2;            // [2] softmax weights written (4 warps)
+  uint64_t* pv_done = p_full + 2;           // [2] value MMA of a P buffer done
+  uint64_t* acc_done = pv_done + 2;
   uint64_t* zq_full = acc_done + 1;
   uint64_t* w_full = zq_full + 1;
   uint64_t* o_done = w_full + 1;
@@ -132,8 +136,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
+    }
     mbar_init(acc_done, 1);
     mbar_init(zq_full, 4);
     mbar_init(w_full, 1);
@@ -265,19 +271,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ++js;
           progress = true;
         }
-        if (jp < js && mbar_test_wait(p_full, jp & 1) &&
+        // RECON: P buffer jp & 1, each with its own barriers; rank space: one P buffer
+        const int pb = RECON ? (jp & 1) : 0;
+        const uint32_t pph = RECON ? (jp >> 1) & 1 : jp & 1;
+        if (jp < js && mbar_test_wait(&p_full[pb], pph) &&
             mbar_test_wait(&v_full[jp % NS], (jp / NS) & 1)) {
           tc_fence_after();
           const uint32_t va = smem_u32(sm + L::ST_OFF + (jp % NS) * L::STAGE + L::K_BYTES);
 #pragma unroll
           for (int ks = 0; ks < KT / 16; ++ks) {
-            const uint64_t ad = make_sdesc(pa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024,
-                                           kSwizzle128B);
             const uint64_t bd = make_sdesc(va + ks * 2048, (KT / kBlockSize) * 2048, 1024,
                                            kSwizzle128B);
-            umma_f16(tmem + 256, ad, bd, id_pv, (jp > 0 || ks > 0) ? 1u : 0u);
+            if constexpr (RECON) {
+              umma_f16_ta(tmem + 256, tmem + L::P_TM + pb * (KT / 2) + ks * 8, bd, id_pv,
+                          (jp > 0 || ks > 0) ? 1u : 0u);
+            } else {
+              const uint64_t ad = make_sdesc(pa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024,
+                                             kSwizzle128B);
+              umma_f16(tmem + 256, ad, bd, id_pv, (jp > 0 || ks > 0) ? 1u : 0u);
+            }
           }
-          umma_commit(pv_done);
+          umma_commit(&pv_done[pb]);
           umma_commit(&v_empty[jp % NS]);
           ++jp;
           progress = true;
@@ -380,13 +394,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const float2 t2 = add_f32x2(add_f32x2(s4[0], s4[1]), add_f32x2(s4[2], s4[3]));
         rsum = t2.x + t2.y;
       }
-      // the previous tile's value MMA must be done before P is overwritten / Z rescaled
-      if (j > 0) ok = mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.dev_err) && ok;
+      // rank space: the previous tile's value MMA must be done before P is overwritten or
+      // Z rescaled.  RECON: P buffer j & 1 must be free (value MMA of tile j-2), and only a
+      // rescale needs the previous tile's value MMA
+      const bool rescale = __any_sync(0xffffffffu, ok && alpha != 1.f && j > 0);
+      if constexpr (RECON) {
+        if (j >= 2) ok = mbar_wait(&pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag, p.dev_err) && ok;
+        if (rescale)
+          ok = mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.dev_err) && ok;
+      } else {
+        if (j > 0) ok = mbar_wait(&pv_done[0], (j - 1) & 1, abort_flag, p.dev_err) && ok;
+      }
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
       // tcgen05.ld / st are warp-collective: the whole warp rescales when any lane needs it
       // (lanes whose max did not move multiply by 1)
-      if (__any_sync(0xffffffffu, ok && alpha != 1.f && j > 0)) {
+      if (ok && rescale) {
 #pragma unroll 1
         for (int c = 0; c < VN; c += 32) {
           float v[16], w[16];
@@ -403,12 +426,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         tmem_wait_st();
       }
-      // P row r, K-major with 128-byte swizzle: 16-byte chunk c of the row sits at c ^ (r % 8)
+      if constexpr (RECON) {
+        // P row r into tensor memory lane r: column c holds keys 2c and 2c+1
+        if (ok) {
 #pragma unroll
-      for (int ch = 0; ch < KT / 8; ++ch) {
-        const int kb = ch >> 3, cc = ch & 7;
-        *reinterpret_cast<uint4*>(pbuf + kb * 16384 + r * 128 + ((cc ^ (r & 7)) << 4)) =
-            make_uint4(packed[ch * 4], packed[ch * 4 + 1], packed[ch * 4 + 2], packed[ch * 4 + 3]);
+          for (int c = 0; c < KT / 2; c += 16) tmem_st16u(tl + L::P_TM + (j & 1) * (KT / 2) + c, &packed[c]);
+          tmem_wait_st();
+        }
+      } else {
+        // P row r, K-major, 128-byte swizzle: 16-byte chunk c of the row sits at c ^ (r % 8)
+#pragma unroll
+        for (int ch = 0; ch < KT / 8; ++ch) {
+          const int kb = ch >> 3, cc = ch & 7;
+          *reinterpret_cast<uint4*>(pbuf + kb * 16384 + r * 128 + ((cc ^ (r & 7)) << 4)) =
+              make_uint4(packed[ch * 4], packed[ch * 4 + 1], packed[ch * 4 + 2], packed[ch * 4 + 3]);
+        }
       }
       l_run = l_run * alpha + rsum;
       m_run = m_new;
@@ -430,7 +462,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[RECON ? (j & 1) : 0]);
     }
     const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag, p.dev_err));
     tc_fence_after();
