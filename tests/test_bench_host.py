@@ -1,0 +1,101 @@
+"""Host-side logic of bench.py (no GPU): clock-sample windowing, the source hash that gates
+recorded DRAM traffic, byte accounting, and the reference arm's JSON line."""
+import datetime
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+import bench
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _sample_line(ts, sm, reasons=("Not Active",) * 4):
+    stamp = datetime.datetime.fromtimestamp(ts).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return f"{stamp}, {sm}, 2070, 900.00, 0x0, " + ", ".join(reasons) + "\n"
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_region():
+    c = bench.ClockSampler(0)
+    now = time.time()
+    c.t0, c.t1 = now, now + 0.1
+    c.proc = object()                       # as if nvidia-smi had been started
+    with open(c.path, "w") as f:
+        f.write(_sample_line(now - 0.2, 1000, ("Active",) * 4))   # before: ignored
+        f.write(_sample_line(now + 0.02, 2070))
+        f.write(_sample_line(now + 0.05, 2060, ("Not Active", "Not Active", "Not Active",
+                                                "Active")))
+        f.write(_sample_line(now + 0.08, 2070))
+        f.write(_sample_line(now + 0.3, 900, ("Active",) * 4))    # after: ignored
+        f.write("garbage line\n")
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["window"] == "timed region"
+    assert not os.path.exists(c.path)
+
+
+def test_clock_summary_widens_the_window_for_a_short_region():
+    c = bench.ClockSampler(0)
+    now = time.time()
+    c.t0, c.t1 = now, now + 0.001
+    c.proc = object()
+    with open(c.path, "w") as f:
+        f.write(_sample_line(now + 0.02, 2070))
+    s = c.summary()
+    assert s["samples"] == 1 and s["window"] == "timed region +- 50 ms"
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("int a = 1;  // one\n\n// a comment line\nint b = 2;\n")
+    monkeypatch.setattr(bench, "KERNEL_SRC", str(src))
+    h0 = bench.kernel_src_hash()
+    src.write_text("int a = 1;  // changed comment\nint b = 2;   \n")
+    assert bench.kernel_src_hash() == h0
+    src.write_text("int a = 1;\nint b = 3;\n")
+    assert bench.kernel_src_hash() != h0
+
+
+def test_recorded_traffic_is_used_only_for_the_matching_source(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("int a = 1;\n")
+    monkeypatch.setattr(bench, "KERNEL_SRC", str(src))
+    prof = tmp_path / "p.md"
+    prof.write_text(f"kernel_source_sha256_16: {bench.kernel_src_hash()}\n"
+                    "dram_bytes_per_launch_full_size: 12345\n")
+    assert bench.ncu_traffic_per_launch(str(prof)) == 12345
+    src.write_text("int a = 2;\n")
+    assert bench.ncu_traffic_per_launch(str(prof)) is None
+    assert bench.ncu_traffic_per_launch(str(tmp_path / "missing.md")) is None
+
+
+def test_byte_accounting():
+    shape = wl.SHAPES["mha32"]
+    coeff = wl.algorithmic_bytes_decode(shape, np.full(64, 8192))
+    assert coeff == 64 * 8192 * (32 * 64 + 1024) * 2 == 3221225472
+    assert wl.factor_bytes(shape) == (32 * 64 * 128 + 1024 * 32 * 128) * 2 == 8912896
+    assert wl.algorithmic_bytes_decode(shape, [100], 1) * 2 == wl.algorithmic_bytes_decode(
+        shape, [100])
+    per_req = bench.bytes_per_request()
+    assert abs(per_req * bench.BATCH - (coeff + wl.factor_bytes(shape))) < 1e-3
+
+
+def test_reference_arm_prints_one_json_line_with_the_contract_keys():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--seq-len", "256"], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "impl", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
