@@ -406,6 +406,7 @@ def run_ours(args, rank, world, local_rank):
     coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"],
                                               1 if args.pages == "fp8_e4m3" else 2)
     read_bytes = coeff_bytes
+    kept_tok = None   # block-sparse decode: tokens of the pages it reads
     if args.sparse is not None:
         kept = torch.zeros(w["table"].shape, dtype=torch.uint8, device=dev)
         cache.decode_attn_sparse(q, table, lens, args.sparse, page_kept=kept, out=out,
@@ -434,6 +435,7 @@ def run_ours(args, rank, world, local_rank):
     step_bytes = coeff_bytes + wl.factor_bytes(SHAPE)
     value = job_gbs(step_bytes, world, step_ms)
     e2e_value = job_gbs(step_bytes, world, e2e_ms)
+    flops = decode_step_flops(w["seq_lens"], kept_tok)
     peak, peak_kind = measured_peaks()
     achieved = read_bytes / (kern_ms * 1e-3) / 1e9
     traffic = None
@@ -482,11 +484,33 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "inputs packed in one pinned buffer: one H2D copy and one D2H copy "
                           "per step, on the step's stream"},
+        "contraction": {"flops_per_step": flops,
+                        "tflops_step": round(world * flops["total"] / (step_ms * 1e-3) / 1e12, 2),
+                        "pv_tflops_kernel": round(flops["pv"] / (kern_ms * 1e-3) / 1e12, 2),
+                        "note": "P*C_v on tcgen05 (fp16 in, fp32 accumulation); scores on CUDA "
+                                "cores; query / output projections and the append on tcgen05"},
         "sparse": sparse,
         "gpu_launches": args.steps * 5,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
+
+
+def decode_step_flops(seq_lens, kept_tokens=None) -> dict:
+    """Multiply-add work of one decode step (2 FLOPs each): P*C_v (H*R per cached token, or
+    per kept token for the block-sparse decode), scores (H*r_k per token), the query and the
+    output projections (H*r_k*d and H*R*d per request) and the append of one token per
+    request (H*r_k*d + R*H*d)."""
+    H, d, rk, R = SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"], SHAPE["rank_v"]
+    L = int(np.sum(np.asarray(seq_lens, np.int64)))
+    B = len(seq_lens)
+    f = {"pv": 2 * (L if kept_tokens is None else kept_tokens) * H * R,
+         "scores": 2 * L * H * rk,
+         "qproj": 2 * B * H * rk * d,
+         "upproj": 2 * B * H * R * d,
+         "append": 2 * B * (H * rk * d + R * H * d)}
+    f["total"] = sum(f.values())
+    return f
 
 
 def prefill_flops(prior, chunk, batch):

@@ -99,3 +99,12 @@ def test_reference_arm_prints_one_json_line_with_the_contract_keys():
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+
+
+def test_decode_step_flop_count():
+    f = bench.decode_step_flops(np.full(64, 8192))
+    assert f["pv"] == 2 * 64 * 8192 * 32 * 1024 == 34359738368
+    assert f["scores"] == 2 * 64 * 8192 * 32 * 64
+    assert f["upproj"] == 2 * 64 * 32 * 1024 * 128
+    assert f["total"] == sum(v for k, v in f.items() if k != "total")
+    assert bench.decode_step_flops([16, 16], kept_tokens=16)["pv"] == 2 * 16 * 32 * 1024
