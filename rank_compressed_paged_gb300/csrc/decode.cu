@@ -632,15 +632,14 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
         s[r] = -INFINITY;
         if (ok && head_ok(r)) {
           const int h = head_of(r);
-          const uint8_t* kstage = kst + ks * L::KP;
-          const int hk = h;
+          const uint8_t* kstage = kst + ks * L::KP;   // this page's key stage
           // two packed fp32x2 accumulators = four independent chains
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
           if constexpr (F8) {
             // 16 E4M3 codes per 16-byte chunk; lanes 2u and 2u+1 start at chunk u so the
             // 16 tokens' 64-byte rows spread over all banks
             constexpr int NCH8 = S::RK / 16;
-            const uint8_t* krow = kstage + (hk * kBlockSize + t) * S::RK;
+            const uint8_t* krow = kstage + (h * kBlockSize + t) * S::RK;
 #pragma unroll
             for (int v = 0; v < NCH8; ++v) {
               const int c8 = (v + (t >> 1)) % NCH8;
@@ -661,7 +660,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
             }
           } else {
             const __half* krow = reinterpret_cast<const __half*>(kstage) +
-                                 (hk * kBlockSize + t) * S::RK;
+                                 (h * kBlockSize + t) * S::RK;
 #pragma unroll
             for (int v = 0; v < NCH; ++v) {
               const int c = (v + t) % NCH;   // rotation keeps the 16 lanes on distinct banks
