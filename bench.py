@@ -269,7 +269,8 @@ def run_reference(args, rank, world):
         times.append(el)
         nreq += n
     value = nreq * bytes_per_request() / sum(times) / 1e9
-    sample = f"{nreq} of {BATCH} sequences (2 per step), append + decode, fp64 numpy oracle"
+    sample = (f"{nreq} sequences of {SEQ} tokens in all, 2 per step (each like one of the "
+              f"batch's {BATCH}), append + decode, fp64 numpy oracle")
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
