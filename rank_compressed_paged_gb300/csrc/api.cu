@@ -38,6 +38,7 @@ struct rcp_cache {
   CUtensorMap tmap_uk;      // U_k as [H*r_k][d], 64 x 128 boxes (query projection: A)
   CUtensorMap tmap_uk64;    // U_k as [H*r_k][d], 64 x 64 boxes (append key pairs: A)
   CUtensorMap tmap_kp;      // K pages as [num_blocks*H*16][r_k], 64 x 16 boxes (prefill B)
+  CUtensorMap tmap_kpage;   // the same rows, 64 x 256 boxes (decode: half a page per box)
   // optional events recorded around the split-K attention kernel
   cudaEvent_t prof_start;
   cudaEvent_t prof_stop;
@@ -126,7 +127,11 @@ rcp_status ensure_device(rcp_cache* c) {
                  64, 64) ||
       !encode_2d(&c->tmap_kp, c->k_pages, g.rank_k,
                  static_cast<uint64_t>(g.num_blocks) * g.num_heads * 16,
-                 static_cast<uint64_t>(g.rank_k) * 2, 64, 16))
+                 static_cast<uint64_t>(g.rank_k) * 2, 64, 16) ||
+      !encode_2d(&c->tmap_kpage, c->k_pages, g.rank_k,
+                 static_cast<uint64_t>(g.num_blocks) * g.num_heads * 16,
+                 static_cast<uint64_t>(g.rank_k) * 2, 64,
+                 g.num_heads * 16 < 256 ? static_cast<uint32_t>(g.num_heads * 16) : 256))
     return RCP_ERR_CUDA;
   c->num_sms = sms;
   c->device = dev;
@@ -341,12 +346,12 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
       !encode_2d(&zlo_map, p.zlo, hr, static_cast<uint64_t>(nq), hr * 2, 64, 64))
     return RCP_ERR_CUDA;
   if (c->shape == kShapeMain) {
-    e = rcp::launch_attn<ShapeMain>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
+    e = rcp::launch_attn<ShapeMain>(c->tmap_v, c->tmap_kpage, p, s, c->prof_start, c->prof_stop);
     if (e == cudaSuccess)
       e = rcp::launch_upproj_gemm<ShapeMain>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s,
                                              pdl);
   } else {
-    e = rcp::launch_attn<ShapeTiny>(c->tmap_v, p, s, c->prof_start, c->prof_stop);
+    e = rcp::launch_attn<ShapeTiny>(c->tmap_v, c->tmap_kpage, p, s, c->prof_start, c->prof_stop);
     if (e == cudaSuccess)
       e = rcp::launch_upproj_gemm<ShapeTiny>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s,
                                              pdl);

@@ -334,8 +334,13 @@ struct BlockInfo {
 
 template <class S, bool F8, bool SKIP>
 __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
-    decode_main_kernel(const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+    decode_main_kernel(const __grid_constant__ CUtensorMap tmap_v,
+                       const __grid_constant__ CUtensorMap tmap_k, const AttnParams p) {
   static_assert(!(F8 && SKIP), "block-sparse decode reads fp16 pages");
+  // fp16 key pages with 128-byte rows (r_k = 64) arrive 128-byte swizzled (two TMA boxes of
+  // 256 rows): chunk c of row r sits at chunk c ^ (r % 8), so the 16 lanes scoring one
+  // head read the same logical chunk, conflict-free on the keys and as a broadcast on q~
+  constexpr bool KSWZ = !F8 && S::RK == 64;
   using L = DecodeSmem<S, F8, SKIP>;
   constexpr int KST = L::KST, VST = L::VST, VRS = L::VRS, HP = S::HP;
   extern __shared__ uint8_t smem_raw[];
@@ -466,7 +471,15 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
         kinfo[ks] = nvalid;
         if constexpr (SKIP) kphys[ks] = static_cast<int>(phys);
         mbar_arrive_expect_tx(&kfull[ks], L::KP);
-        bulk_g2s_hint(kst + ks * L::KP, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
+        if constexpr (KSWZ) {
+          constexpr int ROWS = S::H * kBlockSize;   // key rows of a page
+#pragma unroll
+          for (int half = 0; half < ROWS / 256; ++half)
+            tma_load_2d_hint(kst + ks * L::KP + half * 256 * 128, &tmap_k, 0,
+                             static_cast<int32_t>(phys * ROWS + half * 256), &kfull[ks], pol);
+        } else {
+          bulk_g2s_hint(kst + ks * L::KP, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
+        }
         ++nk;
         if constexpr (SKIP) continue;   // values wait until the page is known to be needed
         const int vs = static_cast<int>(it % VRS);
@@ -663,8 +676,11 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
                                  (h * kBlockSize + t) * S::RK;
 #pragma unroll
             for (int v = 0; v < NCH; ++v) {
-              const int c = (v + t) % NCH;   // rotation keeps the 16 lanes on distinct banks
-              const uint4 kv = *reinterpret_cast<const uint4*>(krow + c * 8);
+              // swizzled stage: the same chunk for all lanes (q~ read as a broadcast);
+              // otherwise a rotation keeps the 16 lanes on distinct banks
+              const int c = KSWZ ? v : (v + t) % NCH;
+              const uint4 kv = *reinterpret_cast<const uint4*>(
+                  krow + (KSWZ ? ((c ^ (t & 7)) * 8) : c * 8));
               const float4 qa = qs4[(h * 2 + 0) * NCH + c];
               const float4 qb = qs4[(h * 2 + 1) * NCH + c];
               const float2 k01 = __half22float2(*reinterpret_cast<const __half2*>(&kv.x));
@@ -1077,8 +1093,8 @@ cudaError_t prepare_attn(int device) {
 // launch latency and prologues overlap the predecessor's tail.  With profiling events
 // the plain stream order is kept so the events bracket decode_main exactly.
 template <class S>
-cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStream_t stream,
-                        cudaEvent_t prof_start, cudaEvent_t prof_stop) {
+cudaError_t launch_attn(const CUtensorMap& tmap_v, const CUtensorMap& tmap_k, const AttnParams& p,
+                        cudaStream_t stream, cudaEvent_t prof_start, cudaEvent_t prof_stop) {
   const bool pdl = prof_start == nullptr;
   const int qtiles = (p.nq + kQprojTile - 1) / kQprojTile;
   cudaError_t e = launch_pdl(plan_qproj_kernel<S>, dim3(1 + S::H * qtiles), dim3(kPlanThreads), 0,
@@ -1088,15 +1104,15 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStre
   if (p.fp8_pages)
     e = launch_pdl(decode_main_kernel<S, true, false>, dim3(p.parts),
                    dim3(decode_threads<S, true>()), DecodeSmem<S, true>::ALLOC, stream, pdl,
-                   tmap_v, p);
+                   tmap_v, tmap_k, p);
   else if (p.sparse)
     e = launch_pdl(decode_main_kernel<S, false, true>, dim3(p.parts),
                    dim3(decode_threads<S, false, true>()), DecodeSmem<S, false, true>::ALLOC,
-                   stream, pdl, tmap_v, p);
+                   stream, pdl, tmap_v, tmap_k, p);
   else
     e = launch_pdl(decode_main_kernel<S, false, false>, dim3(p.parts),
                    dim3(decode_threads<S, false>()), DecodeSmem<S, false>::ALLOC, stream, pdl,
-                   tmap_v, p);
+                   tmap_v, tmap_k, p);
   if (e != cudaSuccess) return e;
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
   // small batches: four threads per slice element so that a request's many records are
@@ -1120,9 +1136,11 @@ template cudaError_t launch_plan<ShapeMain>(const AttnParams&, cudaStream_t, boo
 template cudaError_t launch_plan<ShapeTiny>(const AttnParams&, cudaStream_t, bool);
 template cudaError_t prepare_attn<ShapeMain>(int);
 template cudaError_t prepare_attn<ShapeTiny>(int);
-template cudaError_t launch_attn<ShapeMain>(const CUtensorMap&, const AttnParams&, cudaStream_t,
-                                            cudaEvent_t, cudaEvent_t);
-template cudaError_t launch_attn<ShapeTiny>(const CUtensorMap&, const AttnParams&, cudaStream_t,
-                                            cudaEvent_t, cudaEvent_t);
+template cudaError_t launch_attn<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
+                                            const AttnParams&, cudaStream_t, cudaEvent_t,
+                                            cudaEvent_t);
+template cudaError_t launch_attn<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
+                                            const AttnParams&, cudaStream_t, cudaEvent_t,
+                                            cudaEvent_t);
 
 }  // namespace rcp

@@ -10,8 +10,8 @@ namespace rcp {
 template <class S>
 cudaError_t prepare_attn(int device);
 template <class S>
-cudaError_t launch_attn(const CUtensorMap& tmap_v, const AttnParams& p, cudaStream_t stream,
-                        cudaEvent_t prof_start, cudaEvent_t prof_stop);
+cudaError_t launch_attn(const CUtensorMap& tmap_v, const CUtensorMap& tmap_k, const AttnParams& p,
+                        cudaStream_t stream, cudaEvent_t prof_start, cudaEvent_t prof_stop);
 // Plan + rank-space queries only (the prefill path's first kernel).
 template <class S>
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream, bool pdl);
