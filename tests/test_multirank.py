@@ -50,3 +50,20 @@ def test_two_gloo_ranks_agree_on_max_time_and_draw_distinct_batches(tmp_path):
         assert gbs == pytest.approx(2 * 1e9 / 2e-3 / 1e9)
     q0, q1 = np.load(tmp_path / "q0.npy"), np.load(tmp_path / "q1.npy")
     assert not np.array_equal(q0, q1)
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    """The launch the benchmark contract uses for N > 1: only rank 0 runs and prints."""
+    import json
+    import subprocess
+    import sys
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+           "--seq-len", "256"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
