@@ -20,7 +20,8 @@
 // The reconstructing variant (RECON) attends V^ = C_v W_v rows of head h, rebuilt once per
 // key by the reconstruction GEMM: O += P V^_h (M=128 x N=d x K=128) in TMEM, no rank slices,
 // and the softmax warps write O / l straight to the output; its key/value ring has three
-// stages.
+// stages, and P stays in tensor memory (two buffers, stored by the softmax threads with
+// tcgen05.st and read as the value MMA's A operand).
 //
 // Warps: 0 copies queries and key tiles, 6 copies value tiles and the W_v slice (two
 // independent streams: a key stage is freed by its score MMA, a value stage by its value
