@@ -203,3 +203,25 @@ def test_reconstruct_workspace_grows_by_the_widened_pages_for_e4m3(lib):
     assert extra <= b.value - a.value <= extra + 3 * 256
     lib.rcp_destroy_cache(h16)
     lib.rcp_destroy_cache(h8)
+
+
+def _declared_param_counts():
+    """Parameter count of every function the header declares (comments stripped)."""
+    src = open(os.path.join(ROOT, "include", "rcp.h")).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"^(?:const char\*|rcp_status)\s+(rcp_\w+)\(([^)]*)\)\s*;", src,
+                         re.M | re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes prototype the binding declares has the header's parameter count."""
+    from rank_compressed_paged_gb300 import _lib
+    decl = _declared_param_counts()
+    assert set(decl) == set(_declared_symbols())
+    assert set(_lib._SIG) == set(decl)            # and the binding covers all of them
+    for name, (_, args) in _lib._SIG.items():
+        assert len(args) == decl[name], (name, len(args), decl[name])
