@@ -38,7 +38,11 @@ scaling, causal-prefill and hand-derived closed-form cases; coordinate-selection
 make appends exact copies.  Block-sparse skipping (tests/test_oracle_sparse.py): attention
 over a page subset equals attention over a compacted block table and a scalar textbook
 loop; the skippable set matches a hand-built score pattern; a sequential running-maximum
-pass drops a subset of it; the output change stays within the derived bound.
+pass drops a subset of it; the output change stays within the derived bound.  4-bit
+pages and rotation (tests/test_oracle_int4.py): grid values round-trip exactly, codes are
+the nearest grid points by enumeration, errors stay within half a step without saturation,
+a hand-packed byte fixes the nibble order, and a rotation folded into the factors leaves
+decode unchanged.
 """
 from __future__ import annotations
 
@@ -300,6 +304,83 @@ def append_kv_fp8(k_pages, v_pages, U_k, W_v, k, v, slot_mapping, block_size: in
             kp[blk, h, off, :] = e4m3_encode(U[h] @ k[i, h])
         vp[blk, off, :] = e4m3_encode(W @ v[i].reshape(H * d))
     return kp, vp
+
+
+# ------------------------------------------------------ 4-bit coefficient pages, rotation
+# The "KV-cache LLM serving" page's TurboQuant pages rotate before they quantize to 4 bits,
+# which keeps accuracy ("What it measured", item 1).  The page gives no format; readings
+# taken here:
+#   * codes are symmetric 4-bit integers in [-7, 7], one fp16 scale per group: a group is
+#     one (token, head) key row (r_k values) or 64 consecutive joint value coefficients;
+#   * the scale is max|x| / 7 of the group, rounded up to the next fp16 so that no code
+#     saturates; code = round-half-even(x / scale); a group of zeros has scale 0, codes 0;
+#   * two codes per byte, even index in the low nibble, two's complement;
+#   * the rotation is an orthogonal matrix applied to the coefficients before they are
+#     quantized.  It folds into the factors (U_k,h -> Q_h U_k,h, W_v -> Q W_v): every score
+#     and output is unchanged, so it needs no step of its own at decode time.
+
+def int4_encode(x, group: int):
+    """Codes (int8 in [-7, 7], same shape as x) and fp16 scales ([..., n / group]) of x,
+    grouped along its last axis."""
+    x = _f64(x)
+    n = x.shape[-1]
+    assert n % group == 0
+    g = x.reshape(x.shape[:-1] + (n // group, group))
+    amax = np.abs(g).max(axis=-1)
+    s = (amax / 7.0).astype(np.float16)
+    low = s.astype(np.float64) * 7.0 < amax                 # fp16 rounding went down
+    s[low] = np.nextafter(s[low], np.float16(np.inf))
+    s64 = s.astype(np.float64)[..., None]
+    q = np.where(s64 > 0, g / np.where(s64 > 0, s64, 1.0), 0.0)
+    codes = np.clip(np.round(q), -7, 7).astype(np.int8)     # np.round: half to even
+    return codes.reshape(x.shape), s
+
+
+def int4_decode(codes, scales, group: int) -> np.ndarray:
+    """fp64 values code * scale of its group."""
+    c = np.asarray(codes, np.float64)
+    n = c.shape[-1]
+    g = c.reshape(c.shape[:-1] + (n // group, group))
+    return (g * np.asarray(scales, np.float64)[..., None]).reshape(c.shape)
+
+
+def pack_int4(codes) -> np.ndarray:
+    """Two codes per byte along the last axis: even index in the low nibble."""
+    c = np.asarray(codes, np.int16) & 0xF
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_int4(packed) -> np.ndarray:
+    """Inverse of pack_int4 (int8 codes, sign-extended nibbles)."""
+    p = np.asarray(packed, np.int16)
+    lo, hi = p & 0xF, (p >> 4) & 0xF
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), np.int16)
+    out[..., 0::2], out[..., 1::2] = lo, hi
+    return np.where(out >= 8, out - 16, out).astype(np.int8)
+
+
+def rotate_factors(U_k, W_v, Q_k, Q_v):
+    """Factors with the coefficient rotation folded in: U_k,h -> Q_k[h] U_k,h (Q_k [H][r_k]
+    [r_k] orthogonal) and W_v -> Q_v W_v (Q_v [R][R] orthogonal), in fp64."""
+    U = np.einsum("hij,hjd->hid", _f64(Q_k), _f64(U_k))
+    W = _f64(Q_v) @ _f64(W_v)
+    return U, W
+
+
+def int4_pages(k_pages, v_pages, v_group: int = 64):
+    """Quantize coefficient pages (fp64 values) to 4 bits: K groups are the r_k values of one
+    (block, head, slot) row, V groups v_group consecutive joint coefficients.  Returns
+    (k_codes, k_scales, v_codes, v_scales) with codes unpacked (int8)."""
+    kc, ks = int4_encode(k_pages, _f64(k_pages).shape[-1])
+    vc, vs = int4_encode(v_pages, v_group)
+    return kc, ks[..., 0], vc, vs
+
+
+def int4_page_values(kc, ks, vc, vs, v_group: int = 64):
+    """The coefficient values 4-bit pages hold (fp64), for the decode definition above."""
+    kv = int4_decode(kc, ks[..., None], kc.shape[-1])
+    vv = int4_decode(vc, vs, v_group)
+    return kv, vv
 
 
 def prefill_attn(q, cu_chunk_lens, k_pages, v_pages, U_k, W_v, block_table, seq_lens,
