@@ -82,32 +82,49 @@ const char* rcp_status_string(rcp_status s);
  * (H, d, r_k, R) = (32, 128, 64, 1024) or (4, 64, 16, 64). */
 rcp_status rcp_config_supported(const rcp_cache_config* cfg);
 
-/* Create a handle over caller-owned device buffers (layout above).  dev_error points to
- * one device uint32 the kernels OR error bits into (the caller zeroes and reads it).
- * Makes no CUDA call; the handle's host free list starts with all blocks free.
- * Ownership: the caller keeps every buffer alive until rcp_destroy_cache. */
+/* Create a handle over caller-owned device buffers (layout above): the compressed paged
+ * cache of the Proxima page (STAR-KV plugin for vLLM), intro paragraph, which keeps the
+ * per-head key coefficients and the joint value coefficients in fixed-size pages and
+ * holds the factors U_k and W_v beside them.  dev_error points to one device uint32 the
+ * kernels OR error bits into (the caller zeroes and reads it).  Makes no CUDA call; the
+ * handle's host free list starts with all blocks free.
+ * Errors: RCP_ERR_UNSUPPORTED for a shape or page format without kernels;
+ * RCP_ERR_INVALID_ARG for a null or misaligned pointer or num_blocks outside [1, 2^26].
+ * Ownership: the caller keeps every buffer alive until rcp_destroy_cache, which frees only
+ * the handle's host memory (never the caller's buffers). */
 rcp_status rcp_create_cache(const rcp_cache_config* cfg, void* k_pages, void* v_pages,
                             const void* U_k, const void* W_v, uint32_t* dev_error,
                             rcp_cache** out);
 rcp_status rcp_destroy_cache(rcp_cache* cache);
 
-/* Host-side block pool (capacity accounting for the paged cache).  alloc hands out n
- * free physical ids (RCP_ERR_CAPACITY and no change if fewer are free); free returns
- * ids (RCP_ERR_CAPACITY and no change on an out-of-range or already-free id). */
+/* Host-side block pool: capacity accounting for the paged cache, in the unit the Proxima
+ * page counts capacity in ("KV-cache capacity": GPU KV blocks that fit the same memory
+ * budget).  alloc hands out n free physical ids into ids_out[0..n) (host array, caller
+ * owned; RCP_ERR_CAPACITY and no change if fewer are free); free returns n ids from a
+ * host array (RCP_ERR_CAPACITY and no change on an out-of-range, already-free or repeated
+ * id); num_free reports the free count.  Pure host bookkeeping, no CUDA call; a handle is
+ * not thread-safe. */
 rcp_status rcp_alloc_blocks(rcp_cache* cache, int32_t n, int32_t* ids_out);
 rcp_status rcp_free_blocks(rcp_cache* cache, int32_t n, const int32_t* ids);
 rcp_status rcp_num_free_blocks(const rcp_cache* cache, int64_t* n_free);
 
 /* Bytes of device workspace decode / prefill need for up to max_query_rows query rows
- * (decode: batch; prefill: total chunk rows).  Pure host arithmetic. */
+ * (decode: batch; prefill: total chunk rows): the split-K partial records of the
+ * "Per-decode-step attention" section's split attention and its combine step (Proxima
+ * page, "Kernel profiling breakdown", the combine-splits kernel), the plan and the
+ * rank-space queries.  The caller allocates it (256-byte aligned) and may reuse it for
+ * every call on one stream.  Pure host arithmetic; RCP_ERR_INVALID_ARG for a null
+ * handle or output, or a negative row count. */
 rcp_status rcp_workspace_size(const rcp_cache* cache, int32_t max_query_rows, size_t* bytes);
 
 /* Append (Proxima page, "Kernel profiling breakdown": the cache-write kernel does the
  * low-rank projection): for each of num_tokens new tokens i with slot s =
  * slot_mapping[i] >= 0, write fp16(U_k,h k[i][h]) to K page [s/bs][h][s%bs] for every
  * head and fp16(W_v v[i]) (v[i] flattened head-major) to V page [s/bs][s%bs].  slot -1
- * is skipped.  k, v: [num_tokens][H][d] fp16 device; slot_mapping: [num_tokens] int64
- * device.  Duplicate slots within one call are undefined. */
+ * is skipped.  Each coefficient is accumulated in fp32 and rounded once to the page format,
+ * to nearest with ties to even (fp16 pages; E4M3 pages also saturate at +-448).
+ * k, v: [num_tokens][H][d] fp16 device; slot_mapping: [num_tokens] int64 device.
+ * Duplicate slots within one call are undefined. */
 rcp_status rcp_append_kv(rcp_cache* cache, const void* k, const void* v,
                          const int64_t* slot_mapping, int32_t num_tokens, rcp_stream stream);
 
@@ -159,7 +176,9 @@ rcp_status rcp_decode_step(rcp_cache* cache, const void* k, const void* v,
  * K/V must already be appended.  Request b owns query rows cu_chunk_lens[b] ..
  * cu_chunk_lens[b+1]-1 of q [num_query_rows][H][d]; seq_lens[b] counts prior + chunk
  * tokens; chunk row i sits at position seq_lens[b] - chunk_b + i and attends keys
- * 0 .. that position (causal).  out [num_query_rows][H][d] fp16.  workspace must hold
+ * 0 .. that position (causal).  cu_chunk_lens must not decrease: if any entry is below
+ * the one before it, RCP_DEVERR_BAD_LEN is set and no row of out is written (so that no
+ * two requests can claim the same rows).  out [num_query_rows][H][d] fp16.  workspace must hold
  * rcp_workspace_size(cache, num_query_rows) bytes.  fp16 pages only (RCP_ERR_UNSUPPORTED
  * for E4M3 pages: use rcp_prefill_attn_reconstruct). */
 rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_chunk_lens,
@@ -215,7 +234,9 @@ rcp_status rcp_set_profile_events(rcp_cache* cache, void* start_event, void* sto
  *     RCP_NOALLOC_SCRATCH_BYTES (for H=32, d=128, r_k=64, R=1024 that is batch <= 123);
  *     a larger batch returns RCP_ERR_WORKSPACE and launches nothing.
  *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current) and keeps it for the life of the process; make that
+ *     first call before any stream capture.  A cudaDeviceReset between calls is not
+ *     supported: it unloads the module, and the kept address goes stale.
  *   - Allocates nothing: no cudaMalloc / cudaFree and no allocating library routine.
  *   - Every call shares the one array: calls that overlap on the GPU (other streams,
  *     other threads, no ordering between them) race and give wrong results.  Each call

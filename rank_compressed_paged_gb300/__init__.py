@@ -25,6 +25,74 @@ def _ptr(t) -> int:
     return t.data_ptr()
 
 
+def _need(name: str, x, dtype, shape=None, device=None) -> None:
+    """Check one tensor argument before its pointer crosses the C ABI, which cannot see
+    dtypes, strides or devices: raise ValueError unless ``x`` is a contiguous tensor of
+    ``dtype`` on ``device`` whose shape matches ``shape`` (None entries match any size)."""
+    import torch
+    if not isinstance(x, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor, got {type(x).__name__}")
+    if x.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {x.dtype}")
+    if shape is not None:
+        if x.dim() != len(shape) or any(e is not None and x.shape[i] != e
+                                        for i, e in enumerate(shape)):
+            want = "[" + ", ".join("*" if e is None else str(e) for e in shape) + "]"
+            raise ValueError(f"{name} must have shape {want}, got {list(x.shape)}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and x.device != device:
+        raise ValueError(f"{name} must be on {device}, got {x.device}")
+
+
+def _validate_append(device, H: int, d: int, k, v, slot_mapping) -> int:
+    """k, v: [T][H][d] fp16; slot_mapping: [T] int64.  Returns T."""
+    import torch
+    _need("slot_mapping", slot_mapping, torch.int64, (None,), device)
+    T = int(slot_mapping.shape[0])
+    _need("k", k, torch.float16, (T, H, d), device)
+    _need("v", v, torch.float16, (T, H, d), device)
+    return T
+
+
+def _validate_decode(device, H: int, d: int, q, block_table, seq_lens, out) -> int:
+    """q, out: [B][H][d] fp16; block_table: [>= B][max_blocks] int32; seq_lens: [B] int32.
+    Returns B."""
+    import torch
+    _need("q", q, torch.float16, (None, H, d), device)
+    B = int(q.shape[0])
+    _need("seq_lens", seq_lens, torch.int32, (B,), device)
+    _need("block_table", block_table, torch.int32, (None, None), device)
+    if block_table.shape[0] < B or block_table.shape[1] < 1:
+        raise ValueError(f"block_table needs at least {B} rows and one column, "
+                         f"got {list(block_table.shape)}")
+    _need("out", out, torch.float16, (B, H, d), device)
+    return B
+
+
+def _validate_prefill(device, H: int, d: int, q, cu_chunk_lens, block_table, seq_lens,
+                      out) -> tuple[int, int]:
+    """q, out: [rows][H][d] fp16; seq_lens: [B] int32; cu_chunk_lens: [B+1] int32;
+    block_table: [>= B][max_blocks] int32.  Returns (rows, B)."""
+    import torch
+    _need("q", q, torch.float16, (None, H, d), device)
+    rows = int(q.shape[0])
+    _need("seq_lens", seq_lens, torch.int32, (None,), device)
+    B = int(seq_lens.shape[0])
+    _need("cu_chunk_lens", cu_chunk_lens, torch.int32, (B + 1,), device)
+    _need("block_table", block_table, torch.int32, (None, None), device)
+    if block_table.shape[0] < B or block_table.shape[1] < 1:
+        raise ValueError(f"block_table needs at least {B} rows and one column, "
+                         f"got {list(block_table.shape)}")
+    _need("out", out, torch.float16, (rows, H, d), device)
+    return rows, B
+
+
+def _validate_workspace(device, ws) -> None:
+    import torch
+    _need("workspace", ws, torch.uint8, (None,), device)
+
+
 def _stream(stream=None) -> int:
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -47,22 +115,31 @@ class PagedCoeffCache:
         import torch
         lib = _lib.load()
         dev = U_k.device if device is None else torch.device(device)
-        fmt = {"fp16": _lib.RCP_PAGES_FP16, "fp8_e4m3": _lib.RCP_PAGES_FP8_E4M3}[page_format]
+        if dev.type != "cuda":
+            raise ValueError(f"the cache lives on a CUDA device, got {dev}")
+        if dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        formats = {"fp16": _lib.RCP_PAGES_FP16, "fp8_e4m3": _lib.RCP_PAGES_FP8_E4M3}
+        if page_format not in formats:
+            raise ValueError(f"unknown page_format {page_format!r}")
+        fmt = formats[page_format]
         page_dtype = torch.float16 if fmt == _lib.RCP_PAGES_FP16 else torch.uint8
         self.page_format = page_format
         self.shape = dict(num_heads=num_heads, head_dim=head_dim, rank_k=rank_k, rank_v=rank_v)
         self.num_blocks = int(num_blocks)
-        self.U_k = U_k.contiguous()
-        self.W_v = W_v.contiguous()
+        self.device = dev
+        _need("U_k", U_k, torch.float16, (num_heads, rank_k, head_dim), dev)
+        _need("W_v", W_v, torch.float16, (rank_v, num_heads * head_dim), dev)
+        self.U_k = U_k
+        self.W_v = W_v
         if k_pages is None:
             k_pages = torch.zeros((num_blocks, num_heads, BLOCK_SIZE, rank_k),
                                   dtype=page_dtype, device=dev)
         if v_pages is None:
             v_pages = torch.zeros((num_blocks, BLOCK_SIZE, rank_v), dtype=page_dtype,
                                   device=dev)
-        for pg in (k_pages, v_pages):
-            if pg.element_size() != (2 if fmt == _lib.RCP_PAGES_FP16 else 1):
-                raise ValueError(f"{page_format} pages need {page_dtype} elements, got {pg.dtype}")
+        _need("k_pages", k_pages, page_dtype, (num_blocks, num_heads, BLOCK_SIZE, rank_k), dev)
+        _need("v_pages", v_pages, page_dtype, (num_blocks, BLOCK_SIZE, rank_v), dev)
         self.k_pages = k_pages
         self.v_pages = v_pages
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -144,17 +221,20 @@ class PagedCoeffCache:
     # ------------------------------------------------------------------ hot path
     def append_kv(self, k, v, slot_mapping, stream=None) -> None:
         """k, v: [T][H][d] fp16; slot_mapping: [T] int64 (all on the cache's device)."""
-        T = int(slot_mapping.shape[0])
+        H, d = self.shape["num_heads"], self.shape["head_dim"]
+        T = _validate_append(self.device, H, d, k, v, slot_mapping)
         _lib.check("rcp_append_kv", self._lib.rcp_append_kv(
             self._h, _ptr(k), _ptr(v), _ptr(slot_mapping), T, _stream(stream)))
 
     def decode_attn(self, q, block_table, seq_lens, out=None, workspace=None, stream=None):
         """q: [B][H][d] fp16; block_table: [B][max_blocks] int32; seq_lens: [B] int32."""
         import torch
-        B = int(q.shape[0])
         if out is None:
             out = torch.empty_like(q)
+        H, d = self.shape["num_heads"], self.shape["head_dim"]
+        B = _validate_decode(self.device, H, d, q, block_table, seq_lens, out)
         ws = self.workspace(B) if workspace is None else workspace
+        _validate_workspace(self.device, ws)
         _lib.check("rcp_decode_attn", self._lib.rcp_decode_attn(
             self._h, _ptr(q), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), B,
             _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
@@ -167,13 +247,14 @@ class PagedCoeffCache:
         ``skip_threshold`` times that head's running maximum weight.  ``page_kept``: None
         or a [B][max_blocks] uint8 tensor that receives 1 / 0 per page read / left out."""
         import torch
-        B = int(q.shape[0])
         if out is None:
             out = torch.empty_like(q)
-        if page_kept is not None and (page_kept.dtype != torch.uint8 or
-                                      tuple(page_kept.shape) != tuple(block_table.shape)):
-            raise ValueError("page_kept must be uint8 shaped like block_table")
+        H, d = self.shape["num_heads"], self.shape["head_dim"]
+        B = _validate_decode(self.device, H, d, q, block_table, seq_lens, out)
+        if page_kept is not None:
+            _need("page_kept", page_kept, torch.uint8, tuple(block_table.shape), self.device)
         ws = self.workspace(B) if workspace is None else workspace
+        _validate_workspace(self.device, ws)
         _lib.check("rcp_decode_attn_sparse", self._lib.rcp_decode_attn_sparse(
             self._h, _ptr(q), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), B,
             float(skip_threshold), _ptr(page_kept) if page_kept is not None else None,
@@ -184,10 +265,13 @@ class PagedCoeffCache:
                     stream=None):
         """append_kv(k, v, slot_mapping) then decode_attn(q, ...), queued as one step."""
         import torch
-        B = int(q.shape[0])
         if out is None:
             out = torch.empty_like(q)
+        H, d = self.shape["num_heads"], self.shape["head_dim"]
+        _validate_append(self.device, H, d, k, v, slot_mapping)
+        B = _validate_decode(self.device, H, d, q, block_table, seq_lens, out)
         ws = self.workspace(B) if workspace is None else workspace
+        _validate_workspace(self.device, ws)
         _lib.check("rcp_decode_step", self._lib.rcp_decode_step(
             self._h, _ptr(k), _ptr(v), _ptr(slot_mapping), int(slot_mapping.shape[0]), _ptr(q),
             _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), B, _ptr(out), _ptr(ws),
@@ -205,16 +289,17 @@ class PagedCoeffCache:
         faster variant from 16-row chunks on (priors 4096 to 32768), because a chunk shorter
         than one 128-row tile costs the rank-space kernel a whole tile per R slice."""
         import torch
-        rows = int(q.shape[0])
-        B = int(seq_lens.shape[0])
+        if out is None:
+            out = torch.empty_like(q)
+        H, d = self.shape["num_heads"], self.shape["head_dim"]
+        rows, B = _validate_prefill(self.device, H, d, q, cu_chunk_lens, block_table, seq_lens,
+                                    out)
         mb = int(block_table.shape[1])
         if variant == "auto":
             variant = "reconstruct" if (self.page_format == "fp8_e4m3" or
                                         (B > 0 and rows >= B * RECONSTRUCT_MIN_CHUNK)) else "rank"
         if variant not in ("rank", "reconstruct"):
             raise ValueError(f"unknown prefill variant {variant!r}")
-        if out is None:
-            out = torch.empty_like(q)
         if variant == "rank":
             ws = self.workspace(rows) if workspace is None else workspace
             fn, name = self._lib.rcp_prefill_attn, "rcp_prefill_attn"
@@ -222,6 +307,7 @@ class PagedCoeffCache:
             ws = self.workspace(rows, self.reconstruct_workspace_bytes(rows, B, mb)) \
                 if workspace is None else workspace
             fn, name = self._lib.rcp_prefill_attn_reconstruct, "rcp_prefill_attn_reconstruct"
+        _validate_workspace(self.device, ws)
         _lib.check(name, fn(
             self._h, _ptr(q), _ptr(cu_chunk_lens), rows, _ptr(block_table), mb, _ptr(seq_lens), B,
             _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))

@@ -55,13 +55,23 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
   if (blockIdx.x == 0) {
     // ---- plan: qlen / qrow per query row, then cum = prefix sum of ceil(qlen / 16)
     __shared__ int64_t warp_sum[kPlanThreads / 32];
+    __shared__ int cu_bad;
     const int tid = threadIdx.x;
     const int32_t max_len = p.bt_stride * kBlockSize;
+    if (tid == 0) cu_bad = 0;
     for (int r = tid; r < p.nq; r += kPlanThreads) {
       p.qlen[r] = 0;
       p.qrow[r] = 0;
     }
     __syncthreads();
+    // prefill: chunk offsets must not decrease, or two requests could claim the same query
+    // rows; if they do, no request is planned (every row stays empty)
+    if (p.cu_chunk != nullptr)
+      for (int b = tid; b < p.batch; b += kPlanThreads)
+        if (p.cu_chunk[b + 1] < p.cu_chunk[b]) cu_bad = 1;
+    __syncthreads();
+    const bool cu_ok = cu_bad == 0;
+    if (!cu_ok && tid == 0) atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
     for (int b = tid; b < p.batch; b += kPlanThreads) {
       const int32_t L = p.seq_lens[b];
       const bool len_ok = L >= 0 && L <= max_len;
@@ -72,7 +82,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
       } else {
         const int32_t c0 = p.cu_chunk[b], c1 = p.cu_chunk[b + 1];
         const int32_t n = c1 - c0;
-        if (!len_ok || c0 < 0 || n < 0 || c1 > p.nq || n > L) {
+        if (!cu_ok || !len_ok || c0 < 0 || n < 0 || c1 > p.nq || n > L) {
           atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
           continue;
         }
@@ -112,7 +122,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
       auto tiles_of = [&](int b) -> int {
         const int32_t L = p.seq_lens[b], c0 = p.cu_chunk[b], c1 = p.cu_chunk[b + 1];
         const int32_t n = c1 - c0;
-        const bool ok = L >= 0 && L <= max_len && c0 >= 0 && n >= 0 && c1 <= p.nq && n <= L;
+        const bool ok =
+            cu_ok && L >= 0 && L <= max_len && c0 >= 0 && n >= 0 && c1 <= p.nq && n <= L;
         return ok ? (n + 127) / 128 : 0;
       };
       int64_t ts = 0;

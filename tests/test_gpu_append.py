@@ -32,16 +32,21 @@ def _gamma(n):
     return n * u / (1 - n * u)
 
 
-def _check(shape, U, W, nb, T, slots, seed, exact=False):
+def _check(shape, U, W, nb, T, slots, seed, exact=False, narrow=False):
     """Written coefficients: |gpu - oracle| <= one fp16 ulp + the fp32 dot-product error
-    bound gamma_n * sum_i |a_i b_i| (n = d for keys, H*d for values); exact when the
-    factors are coordinate selections (a single nonzero product per output)."""
+    bound gamma_n * sum_i |a_i b_i| (n = d for keys, H*d for values); exact when every
+    fp32 sum the kernel forms is exact, so that its fp32 -> fp16 conversion is the only
+    rounding (coordinate-selection factors; or pair-sum factors with ``narrow`` inputs)."""
     H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
     rng = np.random.default_rng(seed)
     kp = np.full((nb, H, 16, rk), SENTINEL, np.float16)
     vp = np.full((nb, 16, R), SENTINEL, np.float16)
-    k = wl.fp16(rng.standard_normal((T, H, d)))
-    v = wl.fp16(rng.standard_normal((T, H, d)))
+    if narrow:
+        k = wl.fp16_narrow(rng, (T, H, d))
+        v = wl.fp16_narrow(rng, (T, H, d))
+    else:
+        k = wl.fp16(rng.standard_normal((T, H, d)))
+        v = wl.fp16(rng.standard_normal((T, H, d)))
     gk, gv, cache = _append(shape, U, W, kp, vp, k, v, slots)
     assert cache.read_device_error() == 0
     ok_, ov = orc.append_kv(kp, vp, U, W, k, v, slots, 16)
@@ -100,6 +105,41 @@ def test_append_main_chunk_with_skips():
     U, W = wl.selection_factors(rng, 32, 128, 64, 1024)
     slots = [int(s) if i % 7 else -1 for i, s in enumerate(rng.permutation(40 * 16)[:300])]
     _check(MAIN, U, W, 40, 300, slots, seed=38, exact=True)
+
+
+def _rounding_counts(U, W, k, v):
+    """How many exact projections fp16 cannot hold, and how many of those are ties."""
+    ex = np.concatenate([np.einsum("hkd,thd->thk", U.astype(np.float64),
+                                   k.astype(np.float64)).ravel(),
+                         (v.astype(np.float64).reshape(len(v), -1) @
+                          W.astype(np.float64).T).ravel()])
+    lo = ex.astype(np.float16)
+    inexact = lo.astype(np.float64) != ex
+    up = np.nextafter(lo, np.where(lo.astype(np.float64) < ex, np.float16(np.inf),
+                                   np.float16(-np.inf)))
+    tie = inexact & (np.abs(up.astype(np.float64) - ex) == np.abs(lo.astype(np.float64) - ex))
+    return int(inexact.sum()), int(tie.sum())
+
+
+@pytest.mark.parametrize("shape_name,T,nb", [("tiny", 40, 6), ("mha32", 64, 80),
+                                             ("mha32", 300, 40)])
+def test_append_pair_sum_factors_round_to_nearest_even_bit_exact(shape_name, T, nb):
+    """Every coefficient is the sum of two fp16 inputs whose exact sum fits in fp32, so the
+    kernel's fp32 accumulation (tensor-core partial sums, the cluster's split-K reduction)
+    is exact and its fp32 -> fp16 conversion is the only rounding: the pages must equal
+    the oracle's fp64 -> fp16 round-to-nearest-even bit for bit, ties included.  T = 64
+    takes the split-K cluster path, T = 300 the 256-token tiles."""
+    shape = wl.SHAPES[shape_name]
+    H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
+    rng = np.random.default_rng(41 + T)
+    U, W = wl.pair_sum_factors(rng, H, d, rk, R)
+    slots = [int(s) if i % 9 else -1 for i, s in enumerate(rng.permutation(nb * 16)[:T])]
+    seed = 42 + T
+    r2 = np.random.default_rng(seed)
+    inexact, ties = _rounding_counts(U, W, wl.fp16_narrow(r2, (T, H, d)),
+                                     wl.fp16_narrow(r2, (T, H, d)))
+    assert inexact > T * (H * rk + R) // 3 and ties > 20, (inexact, ties)   # rounding happens
+    _check(shape, U, W, nb, T, slots, seed=seed, exact=True, narrow=True)
 
 
 def test_append_bad_slot_sets_error_and_writes_nothing():

@@ -106,6 +106,36 @@ def test_fp8_append_with_selection_factors_is_bit_exact():
     assert np.array_equal(cache.v_pages.cpu().numpy(), vo)
 
 
+@pytest.mark.parametrize("shape_name,T,nb", [("tiny", 40, 6), ("mha32", 64, 80),
+                                             ("mha32", 300, 40)])
+def test_fp8_append_pair_sum_factors_round_to_nearest_even_bit_exact(shape_name, T, nb):
+    """Pair-sum factors on narrow-range inputs: every fp32 sum the kernel forms is exact,
+    so its conversion to E4M3 is the only rounding and the codes must equal the oracle's
+    fp64 -> E4M3 round-to-nearest-even codes bit for bit (split-K cluster path at T = 64,
+    256-token tiles at T = 300)."""
+    import torch
+    shape = wl.SHAPES[shape_name]
+    H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
+    rng = np.random.default_rng(91 + T)
+    U, W = wl.pair_sum_factors(rng, H, d, rk, R)
+    k = wl.fp16_narrow(rng, (T, H, d))
+    v = wl.fp16_narrow(rng, (T, H, d))
+    slots = np.array([int(s) if i % 9 else -1 for i, s in
+                      enumerate(rng.permutation(nb * 16)[:T])], np.int64)
+    kp8 = np.full((nb, H, 16, rk), 0x55, np.uint8)
+    vp8 = np.full((nb, 16, R), 0x55, np.uint8)
+    cache = _fp8_cache(shape, U, W, kp8, vp8)
+    cache.append_kv(t(k), t(v), t(slots))
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    ko, vo = orc.append_kv_fp8(kp8, vp8, U, W, k, v, slots, 16)
+    # the case exercises rounding: most exact sums fall between two E4M3 codes
+    ex = np.einsum("hkd,thd->thk", U.astype(np.float64), k.astype(np.float64))
+    assert np.mean(orc.e4m3_decode(orc.e4m3_encode(ex)) != ex) > 0.5
+    assert np.array_equal(cache.k_pages.cpu().numpy(), ko)
+    assert np.array_equal(cache.v_pages.cpu().numpy(), vo)
+
+
 def test_fp8_decode_step_equals_append_then_decode():
     import torch
     inp = wl.make_decode_inputs(MAIN, [300, 17, 1024, 0], seed=86, append=True)

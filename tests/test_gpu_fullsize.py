@@ -1,15 +1,17 @@
-"""Full-size workloads on the GPU, checked on sampled requests against the oracle.
+"""Full-size workloads on the GPU, every request checked against the oracle.
 
-The GPU runs every request at the sizes and launch configuration the benchmark uses
-(one CTA per SM split-K); the oracle recomputes a few sampled requests from host copies
-of their *input* pages (taken before any append, which the oracle redoes itself).
+The GPU runs each batch at the sizes and in the launch configuration the benchmark uses
+(one CTA per SM, split-K over equal slices of the global block list); partitions cut
+requests at arbitrary blocks, so every request is compared, not a sample.  The oracle
+recomputes each request from host copies of its *input* pages (taken before any append,
+which the oracle redoes itself), in a spawn process pool.
 """
 import numpy as np
 import pytest
 
 import workloads as wl
-from oracle import rcp_oracle as orc
 from tests.gpu_util import assert_close, t
+from tests.oracle_jobs import decode_request, prefill_request, run_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -34,15 +36,15 @@ def _host_request(cache, table, b, n_blocks):
     ids = torch.from_numpy(table[b, :n_blocks].astype(np.int64)).cuda()
     kp = cache.k_pages.index_select(0, ids).cpu().numpy()
     vp = cache.v_pages.index_select(0, ids).cpu().numpy()
-    return kp, vp, np.arange(n_blocks, dtype=np.int32)[None]
+    return kp, vp
 
 
-def _decode_sampled(seq_lens, seed, sample, append):
+def _decode_every_request(seq_lens, seed, append):
     import torch
     cache, table, lens, U, W, rng = _device_cache(seq_lens, seed)
     B = len(lens)
     q = wl.fp16(rng.standard_normal((B, 32, 128)))
-    hosts = {b: _host_request(cache, table, b, wl.blocks_needed(lens[b])) for b in sample}
+    hosts = [_host_request(cache, table, b, wl.blocks_needed(lens[b])) for b in range(B)]
     if append:
         nk = wl.fp16(rng.standard_normal((B, 32, 128)))
         nv = wl.fp16(rng.standard_normal((B, 32, 128)))
@@ -51,33 +53,32 @@ def _decode_sampled(seq_lens, seed, sample, append):
     out = cache.decode_attn(t(q), t(table), t(lens)).cpu().numpy()
     torch.cuda.synchronize()
     assert cache.read_device_error() == 0
-    for b in sample:
-        kp, vp, tab = hosts[b]
-        if append:
-            L = int(lens[b])
-            kp, vp = orc.append_kv(kp, vp, U, W, nk[b:b + 1], nv[b:b + 1],
-                                   np.array([(L - 1)], np.int64), 16)
-        ref = orc.decode_attn(q[b:b + 1], kp, vp, U, W, tab, lens[b:b + 1], 16)
+    del cache
+    torch.cuda.empty_cache()
+    jobs = [(q[b:b + 1], hosts[b][0], hosts[b][1], U, W, int(lens[b]),
+             (nk[b:b + 1], nv[b:b + 1]) if append else None) for b in range(B)]
+    hosts.clear()
+    refs = run_pool(decode_request, jobs)
+    for b, ref in enumerate(refs):
         assert_close(out[b:b + 1], ref, what=f"request {b} (L={lens[b]})")
+    # and the batch as a whole
+    assert_close(out, np.concatenate(refs), what="whole batch")
 
 
-def test_decode_b64_l8192_with_append_sampled():
-    _decode_sampled(np.full(64, 8192, np.int32), 1002, [0, 37, 63], append=True)
+def test_decode_b64_l8192_with_append_every_request():
+    _decode_every_request(np.full(64, 8192, np.int32), 1002, append=True)
 
 
-def test_decode_b20_l32768_sampled():
-    _decode_sampled(np.full(20, 32768, np.int32), 1003, [0, 19], append=False)
+def test_decode_b20_l32768_every_request():
+    _decode_every_request(np.full(20, 32768, np.int32), 1003, append=False)
 
 
-def test_decode_ragged64_sampled():
+def test_decode_ragged64_every_request():
     lens = wl.ragged_lengths(np.random.default_rng(1003), 64, 128, 16384)
-    order = np.argsort(lens)
-    sample = sorted({int(order[0]), int(order[-1]), 5, 40})
-    _decode_sampled(lens, 1013, sample, append=False)
+    _decode_every_request(lens, 1013, append=False)
 
 
-@pytest.mark.parametrize("variant", ["rank", "reconstruct"])
-def test_prefill_b16_p4096_c256_sampled(variant):
+def test_prefill_b16_p4096_c256_every_request_both_variants():
     import torch
     B, prior, chunk = 16, 4096, 256
     after = np.full(B, prior + chunk, np.int32)
@@ -89,17 +90,23 @@ def test_prefill_b16_p4096_c256_sampled(variant):
     slots = np.array([wl.slot_for(table, b, prior + i) for b in range(B) for i in range(chunk)],
                      np.int64)
     cu = (np.arange(B + 1) * chunk).astype(np.int32)
-    sample = [0, 11]
-    hosts = {b: _host_request(cache, table, b, wl.blocks_needed(after[b])) for b in sample}
+    hosts = [_host_request(cache, table, b, wl.blocks_needed(after[b])) for b in range(B)]
     cache.append_kv(t(k), t(v), t(slots))
-    out = cache.prefill_attn(t(q), t(cu), t(table), t(lens), variant=variant).cpu().numpy()
+    outs = {}
+    for variant in ("rank", "reconstruct"):
+        outs[variant] = cache.prefill_attn(t(q), t(cu), t(table), t(lens),
+                                           variant=variant).cpu().numpy()
     torch.cuda.synchronize()
     assert cache.read_device_error() == 0
-    for b in sample:
-        kp, vp, tab = hosts[b]
+    del cache
+    torch.cuda.empty_cache()
+    jobs = []
+    for b in range(B):
         rows = slice(b * chunk, (b + 1) * chunk)
-        loc = np.arange(prior, prior + chunk, dtype=np.int64)     # re-addressed slots
-        kp, vp = orc.append_kv(kp, vp, U, W, k[rows], v[rows], loc, 16)
-        ref = orc.prefill_attn(q[rows], np.array([0, chunk], np.int32), kp, vp, U, W, tab,
-                               after[b:b + 1], 16)
-        assert_close(out[rows], ref, what=f"prefill request {b} ({variant})")
+        jobs.append((q[rows], k[rows], v[rows], hosts[b][0], hosts[b][1], U, W, prior, chunk))
+    hosts.clear()
+    refs = run_pool(prefill_request, jobs)
+    for variant, out in outs.items():
+        for b, ref in enumerate(refs):
+            rows = slice(b * chunk, (b + 1) * chunk)
+            assert_close(out[rows], ref, what=f"prefill request {b} ({variant})")

@@ -69,3 +69,24 @@ def test_prefill_variants_agree_on_a_long_chunk():
     b, _ = _run(inp, "reconstruct")
     assert_close(a, ref, what="rank")
     assert_close(b, ref, what="reconstruct")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_rejects_decreasing_chunk_offsets(variant):
+    """cu_chunk_lens = [0, 10, 5, 20]: request 2 would start inside request 0's rows.  The
+    plan refuses the whole batch: the length error bit is set and no output row is
+    written (the rows keep their NaN fill)."""
+    import torch
+    from rank_compressed_paged_gb300 import _lib
+    inp = wl.make_prefill_inputs(MAIN, [40, 40, 40], [10, 0, 10], seed=46)
+    c = inp.cache
+    cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    q = t(wl.fp16(np.random.default_rng(47).standard_normal((20, 32, 128))))
+    cu = t(np.array([0, 10, 5, 20], np.int32))
+    lens = t(np.array([50, 40, 50], np.int32))      # within each request's valid blocks
+    table = t(c.block_table)
+    out = torch.full_like(q, float("nan"))
+    cache.prefill_attn(q, cu, table, lens, out=out, variant=variant)
+    torch.cuda.synchronize()
+    assert cache.read_device_error() & _lib.RCP_DEVERR_BAD_LEN
+    assert torch.isnan(out).all()

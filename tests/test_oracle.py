@@ -247,6 +247,92 @@ def test_append_with_selection_factors_copies_exactly():
                 assert np.all(np.isnan(kp2[blk, :, off])) and np.all(np.isnan(vp2[blk, off]))
 
 
+def test_golden_append_rounds_to_nearest_even():
+    """Hand-derived fp16 bit patterns of projections that fp16 cannot hold exactly: ties
+    in both directions, a tie that an intermediate binary32 rounding would create, a
+    subnormal tie, the top of the range and the overflow to infinity
+    (tests/golden/append_rounding.json)."""
+    with open(os.path.join(GOLDEN, "append_rounding.json")) as f:
+        g = json.load(f)
+    s = g["shape"]
+
+    def hexf(a):
+        return np.vectorize(float.fromhex, otypes=[np.float64])(np.array(a, dtype=object))
+
+    U, W = hexf(g["U_k"]), hexf(g["W_v"])
+    # every factor and input entry is a binary16 value, so nothing rounds on the way in
+    toks = g["tokens"]
+    k = np.stack([hexf(tk["k"]) for tk in toks])
+    v = np.stack([hexf(tk["v"]) for tk in toks])
+    for a in (U, W, k, v):
+        assert np.array_equal(a.astype(np.float16).astype(np.float64), a)
+    slots = np.array([tk["slot"] for tk in toks], np.int64)
+    kp = np.full((s["num_blocks"], s["num_heads"], 16, s["rank_k"]), -7.0, np.float16)
+    vp = np.full((s["num_blocks"], 16, s["rank_v"]), -7.0, np.float16)
+    kp2, vp2 = orc.append_kv(kp, vp, U.astype(np.float16), W.astype(np.float16),
+                             k.astype(np.float16), v.astype(np.float16), slots, 16)
+    for e in g["expected"]:
+        kb = np.array([[int(x, 16) for x in row] for row in e["k_bits"]], np.uint16)
+        vb = np.array([int(x, 16) for x in e["v_bits"]], np.uint16)
+        assert np.array_equal(kp2[e["block"], :, e["offset"], :].view(np.uint16), kb), e
+        assert np.array_equal(vp2[e["block"], e["offset"], :].view(np.uint16), vb), e
+    untouched = np.ones(kp.shape[:3], bool)
+    for e in g["expected"]:
+        untouched[e["block"], :, e["offset"]] = False
+    assert np.all(kp2[untouched] == -7.0)
+
+
+def _fp16_nearest_even(x: float) -> int:
+    """Bit pattern of the binary16 value nearest to x (ties: even fraction), by search
+    over all finite binary16 values and the two infinities (IEEE 754 rounds to infinity
+    at or beyond 65520)."""
+    if x >= 65520.0:
+        return 0x7C00
+    if x <= -65520.0:
+        return 0xFC00
+    bits = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    vals = bits.view(np.float16).astype(np.float64)
+    ok = np.isfinite(vals)
+    d = np.abs(vals - x)
+    d[~ok] = np.inf
+    best = np.nonzero(d == d.min())[0]
+    if len(best) > 1:
+        even = [b for b in best if (b & 1) == 0]
+        best = even if even else best
+        if x == 0.0:
+            best = [0x8000 if math.copysign(1.0, x) < 0 else 0x0000]
+    return int(best[0])
+
+
+def test_append_with_pair_sum_factors_matches_brute_force_rounding():
+    """Two-unit-entry factors sum two fp16 inputs per coefficient; the oracle's fp16 result
+    must be the nearest-even binary16 of that exact sum, found by enumeration."""
+    H, d, rk, R = 4, 64, 16, 64
+    rng = np.random.default_rng(16)
+    U, W = wl.pair_sum_factors(rng, H, d, rk, R)
+    k = wl.fp16_narrow(rng, (3, H, d))
+    v = wl.fp16_narrow(rng, (3, H, d))
+    slots = np.array([3, 40, 77], np.int64)
+    kp = np.zeros((6, H, 16, rk), np.float16)
+    vp = np.zeros((6, 16, R), np.float16)
+    kp2, vp2 = orc.append_kv(kp, vp, U, W, k, v, slots, 16)
+    ties = inexact = 0
+    for i, s in enumerate(slots):
+        exact_k = np.einsum("hkd,hd->hk", U.astype(np.float64), k[i].astype(np.float64))
+        exact_v = W.astype(np.float64) @ v[i].astype(np.float64).reshape(-1)
+        got_k = kp2[s // 16, :, s % 16, :].view(np.uint16)
+        got_v = vp2[s // 16, s % 16, :].view(np.uint16)
+        for x, gbits in zip(list(exact_k.ravel()) + list(exact_v), list(got_k.ravel()) +
+                            list(got_v)):
+            assert int(gbits) == _fp16_nearest_even(float(x)), x
+            lo = np.float16(x)
+            inexact += float(lo) != x
+            # halfway cases: the exact sum sits midway between two binary16 neighbours
+            nb = np.nextafter(lo, np.float16(np.inf if float(lo) < x else -np.inf))
+            ties += float(lo) != x and abs(float(nb) - x) == abs(float(lo) - x)
+    assert inexact > 100 and ties > 5, (inexact, ties)
+
+
 def test_append_then_gather_round_trip():
     """Scatter through slots, gather back through the block table: the projections."""
     inp = wl.make_prefill_inputs(TINY, [5, 30], [12, 9], seed=15, fill=np.nan)

@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 
 import workloads as wl
+from oracle import rcp_oracle as orc
 from tests.gpu_util import assert_close, make_cache, t
 
 pytestmark = pytest.mark.gpu
@@ -39,29 +40,40 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
     cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
     table = t(c.block_table)
     rng = np.random.default_rng(77)
-    cases = [(t(inp.q), t(c.seq_lens)),
-             (t(wl.fp16(rng.standard_normal(inp.q.shape))),
-              t(rng.integers(0, 1025, size=16).astype(np.int32)))]
-    for q, lens in cases:
+    q2 = wl.fp16(rng.standard_normal(inp.q.shape))
+    lens2 = rng.integers(0, 1025, size=16).astype(np.int32)
+    cases = [(inp.q, c.seq_lens), (q2, lens2)]
+    for qh, lh in cases:
+        q, lens = t(qh), t(lh)
         ref = cache.decode_attn(q, table, lens)
         out = torch.full_like(q, float("nan"))
         assert _noalloc(cache, q, table, lens, out) == _lib.RCP_OK
         torch.cuda.synchronize()
         assert cache.read_device_error() == 0
-        assert_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64), what="noalloc")
+        got = out.cpu().numpy()
+        assert_close(got, ref.cpu().numpy().astype(np.float64), what="noalloc vs workspace")
+        # and against the fp64 oracle on the same inputs
+        oref = orc.decode_attn(qh, c.k_pages, c.v_pages, inp.U_k, inp.W_v, c.block_table, lh, 16)
+        assert_close(got, oref, what="noalloc vs oracle")
 
 
-def test_noalloc_refuses_batch_beyond_scratch_limit():
+def test_noalloc_limit_is_batch_123_at_the_main_shape():
+    """The header's limit for (H, d, r_k, R) = (32, 128, 64, 1024): batch 123 runs, batch
+    124 is refused without a launch."""
     import torch
     from rank_compressed_paged_gb300 import _lib
     inp = wl.make_decode_inputs(MAIN, [16], seed=5)
     c = inp.cache
     cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
-    big = 1
-    while cache.workspace_bytes(big) <= _lib.RCP_NOALLOC_SCRATCH_BYTES:
-        big += 1
-    q = torch.zeros((big, 32, 128), dtype=torch.float16, device="cuda")
-    lens = torch.zeros(big, dtype=torch.int32, device="cuda")
-    table = torch.zeros((big, 1), dtype=torch.int32, device="cuda")
-    out = torch.zeros_like(q)
-    assert _noalloc(cache, q, table, lens, out) == _lib.RCP_ERR_WORKSPACE
+    assert cache.workspace_bytes(123) <= _lib.RCP_NOALLOC_SCRATCH_BYTES
+    assert cache.workspace_bytes(124) > _lib.RCP_NOALLOC_SCRATCH_BYTES
+    for big, want in ((123, _lib.RCP_OK), (124, _lib.RCP_ERR_WORKSPACE)):
+        q = torch.zeros((big, 32, 128), dtype=torch.float16, device="cuda")
+        lens = torch.zeros(big, dtype=torch.int32, device="cuda")        # empty sequences
+        table = torch.zeros((big, 1), dtype=torch.int32, device="cuda")
+        out = torch.full_like(q, float("nan"))
+        assert _noalloc(cache, q, table, lens, out) == want
+        torch.cuda.synchronize()
+        if want == _lib.RCP_OK:
+            assert cache.read_device_error() == 0
+            assert torch.all(out == 0)                 # L = 0 gives zeros

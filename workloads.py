@@ -124,6 +124,38 @@ def selection_factors(rng: np.random.Generator, num_heads: int, head_dim: int, r
     return fp16(U), fp16(W)
 
 
+def pair_sum_factors(rng: np.random.Generator, num_heads: int, head_dim: int, rank_k: int,
+                     rank_v: int):
+    """Factors whose rows each hold two unit entries in distinct, seeded columns.
+
+    Projecting with them sums two chosen input entries per output.  With inputs from
+    ``fp16_narrow`` every such sum is exact in fp32 (and in fp64), so rounding the sum to
+    the page format is the only rounding an append performs.
+    """
+    U = np.zeros((num_heads, rank_k, head_dim))
+    for h in range(num_heads):
+        for k in range(rank_k):
+            a, b = rng.choice(head_dim, size=2, replace=False)
+            U[h, k, a] = U[h, k, b] = 1.0
+    W = np.zeros((rank_v, num_heads * head_dim))
+    for r in range(rank_v):
+        a, b = rng.choice(num_heads * head_dim, size=2, replace=False)
+        W[r, a] = W[r, b] = 1.0
+    return fp16(U), fp16(W)
+
+
+def fp16_narrow(rng: np.random.Generator, shape, emin: int = -4, emax: int = 3) -> np.ndarray:
+    """fp16 values with a random sign, a binary exponent uniform in [emin, emax] and a
+    uniformly random 10-bit fraction.  Two of them differ by at most emax - emin binades,
+    so their sum needs at most 11 + (emax - emin) + 1 significant bits: exact in fp32 for
+    the default range (19 bits), while most sums carry bits below fp16 precision and some
+    sit exactly halfway between two fp16 neighbours."""
+    e = rng.integers(emin, emax + 1, size=shape)
+    frac = rng.integers(0, 1024, size=shape)
+    sign = np.where(rng.random(shape) < 0.5, -1.0, 1.0)
+    return fp16(sign * (1.0 + frac / 1024.0) * np.exp2(e))
+
+
 def blocks_needed(seq_len: int, block_size: int = BLOCK_SIZE) -> int:
     return (int(seq_len) + block_size - 1) // block_size
 
