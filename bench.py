@@ -191,48 +191,107 @@ def workload_name():
     return f"decode_b{BATCH}_l{SEQ}{tail}"
 
 
-def make_workload(device, seed):
-    """Device-resident cache (pages drawn on the GPU) + the step's host inputs."""
-    import torch
-    seq_lens = (wl.ragged_lengths(np.random.default_rng(seed + 1), BATCH, *RAGGED) if RAGGED
-                else np.full(BATCH, SEQ, np.int32))
-    kp, vp, table, seq_lens = wl.make_paged_cache_device(seq_lens, SHAPE, seed, device=device,
+def make_workload(device, seed, shape=None, batch=None, seq=None, ragged="default",
+                  peaked=None):
+    """Device-resident cache (pages drawn on the GPU) + the step's host inputs.  Defaults
+    are the measured configuration (module globals)."""
+    shape = SHAPE if shape is None else shape
+    batch = BATCH if batch is None else batch
+    seq = SEQ if seq is None else seq
+    ragged = RAGGED if ragged == "default" else ragged
+    peaked = PEAKED if peaked is None else peaked
+    seq_lens = (wl.ragged_lengths(np.random.default_rng(seed + 1), batch, *ragged) if ragged
+                else np.full(batch, seq, np.int32))
+    kp, vp, table, seq_lens = wl.make_paged_cache_device(seq_lens, shape, seed, device=device,
                                                          spare_blocks=16,
-                                                         peaked=wl.PEAKED if PEAKED else None)
+                                                         peaked=wl.PEAKED if peaked else None)
     rng = np.random.default_rng(seed)
-    U, W = wl.make_factors(rng, SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"],
-                           SHAPE["rank_v"])
-    H, d = SHAPE["num_heads"], SHAPE["head_dim"]
-    q = wl.fp16(rng.standard_normal((BATCH, H, d)) * (wl.PEAKED["q_scale"] if PEAKED else 1.0))
-    nk = wl.fp16(rng.standard_normal((BATCH, H, d)))
-    nv = wl.fp16(rng.standard_normal((BATCH, H, d)))
-    slots = np.array([wl.slot_for(table, b, int(seq_lens[b]) - 1) for b in range(BATCH)],
+    H, d = shape["num_heads"], shape["head_dim"]
+    U, W = wl.make_factors(rng, H, d, shape["rank_k"], shape["rank_v"])
+    q = wl.fp16(rng.standard_normal((batch, H, d)) * (wl.PEAKED["q_scale"] if peaked else 1.0))
+    nk = wl.fp16(rng.standard_normal((batch, H, d)))
+    nv = wl.fp16(rng.standard_normal((batch, H, d)))
+    slots = np.array([wl.slot_for(table, b, int(seq_lens[b]) - 1) for b in range(batch)],
                      np.int64)
     return dict(kp=kp, vp=vp, table=table, seq_lens=seq_lens, U=U, W=W, q=q, nk=nk, nv=nv,
-                slots=slots)
+                slots=slots, shape=shape, batch=batch)
 
 
-def oracle_sample(U, W, n_req, seed, budget_s):
-    """Time the fp64 oracle on up to n_req requests of the workload (host-generated pages
-    of the same shape / distribution); stops once budget_s seconds have been spent."""
+# ------------------------------------------------------------------ CPU baseline (oracle)
+def oracle_worker(job):
+    """One host process of the CPU baseline: for each of its requests, draw the pages of
+    one sequence of the workload (untimed), then time the oracle's append of the step's new
+    token and its decode.  Runs single-threaded (the pool caps BLAS at one thread)."""
     from oracle import rcp_oracle as orc
+    seed, n_req, budget_s, seq, U, W = job
     H, d, rk, R = SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"], SHAPE["rank_v"]
-    rng = np.random.default_rng(seed + 7)
-    done, elapsed = 0, 0.0
-    while done < n_req and elapsed < budget_s:
-        nb = SEQ // 16
+    rng = np.random.default_rng(seed)
+    done, busy = 0, 0.0
+    while done < n_req and busy < budget_s:
+        nb = seq // 16
         kp = wl.fp16(rng.standard_normal((nb, H, 16, rk), dtype=np.float32))
         vp = wl.fp16(rng.standard_normal((nb, 16, R), dtype=np.float32))
         table = rng.permutation(nb).astype(np.int32)[None]
         q = wl.fp16(rng.standard_normal((1, H, d)))
         nk = wl.fp16(rng.standard_normal((1, H, d)))
-        slot = np.array([wl.slot_for(table, 0, SEQ - 1)], np.int64)
+        slot = np.array([wl.slot_for(table, 0, seq - 1)], np.int64)
         t0 = time.perf_counter()
         kp2, vp2 = orc.append_kv(kp, vp, U, W, nk, nk, slot, 16)
-        orc.decode_attn(q, kp2, vp2, U, W, table, np.array([SEQ], np.int32), 16)
-        elapsed += time.perf_counter() - t0
+        orc.decode_attn(q, kp2, vp2, U, W, table, np.array([seq], np.int32), 16)
+        busy += time.perf_counter() - t0
         done += 1
-    return done, elapsed, done * bytes_per_request() / elapsed / 1e9
+    return done, busy
+
+
+def _worker_ready(i):
+    return i
+
+
+class OraclePool:
+    """Spawn pool of single-threaded oracle workers, one per host core (a process forked
+    from one that has used the GPU can hang, so the pool spawns).  The workers are started
+    and idle before the constructor returns, so their start-up never overlaps a GPU timed
+    region."""
+
+    def __init__(self, workers=None):
+        import multiprocessing as mp
+        self.n = workers or os.cpu_count() or 1
+        keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+        saved = {k: os.environ.get(k) for k in keys}
+        for k in keys:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.n)
+            self.pool.map(_worker_ready, range(4 * self.n), chunksize=1)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def run(self, U, W, per_worker, seed, budget_s):
+        """Every worker times up to per_worker requests; returns (requests, seconds), the
+        seconds being the busiest worker's oracle time (the workers run concurrently)."""
+        jobs = [(seed + 7919 * i, per_worker, budget_s, SEQ, U, W) for i in range(self.n)]
+        res = self.pool.map(oracle_worker, jobs, chunksize=1)
+        return sum(r[0] for r in res), max(r[1] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def oracle_sample(U, W, n_req, seed, budget_s):
+    """Time the fp64 oracle on about n_req requests of the workload, spread over every host
+    core; returns (requests, seconds, GB/s, processes)."""
+    pool = OraclePool()
+    try:
+        per = max(1, (n_req + pool.n - 1) // pool.n)
+        done, busy = pool.run(U, W, per, seed, budget_s)
+    finally:
+        pool.close()
+    return done, busy, done * bytes_per_request() / busy / 1e9, pool.n
 
 
 def bytes_per_request() -> float:
@@ -261,16 +320,22 @@ def run_reference(args, rank, world):
     rng = np.random.default_rng(2002)
     U, W = wl.make_factors(rng, SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"],
                            SHAPE["rank_v"])
-    for _ in range(args.warmup):
-        oracle_sample(U, W, 1, 1, 1e9)
-    times, nreq = [], 0
-    for s in range(args.steps):
-        n, el, _ = oracle_sample(U, W, 2, 100 + s, 1e9)
-        times.append(el)
-        nreq += n
+    pool = OraclePool()
+    try:
+        for i in range(args.warmup):
+            pool.run(U, W, 1, 1 + i, 1e9)
+        times, nreq = [], 0
+        for s in range(args.steps):
+            n, busy = pool.run(U, W, 1, 100 + s, 1e9)
+            times.append(busy)
+            nreq += n
+    finally:
+        pool.close()
     value = nreq * bytes_per_request() / sum(times) / 1e9
-    sample = (f"{nreq} sequences of {SEQ} tokens in all, 2 per step (each like one of the "
-              f"batch's {BATCH}), append + decode, fp64 numpy oracle")
+    sample = (f"{nreq} sequences of {SEQ} tokens in all: each step one sequence (like one of "
+              f"the batch's {BATCH}) per host process, {pool.n} single-threaded processes "
+              "running concurrently, append + decode, fp64 numpy oracle; a step's time is "
+              "the busiest process's oracle time")
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -280,18 +345,141 @@ def run_reference(args, rank, world):
                    "seq_len": SEQ if not RAGGED else f"uniform {RAGGED[0]}..{RAGGED[1]}",
                    "num_heads": 32,
                    "head_dim": 128, "rank_k": 64, "rank_v": 1024, "block_size": 16},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
-                         "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": pool.n,
+                         "host_cores": os.cpu_count(), "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------- GPU timing
+L2_BYTES = 129e6
+
+
+def time_steps(step, steps, stream, flush=None, cache=None):
+    """Mean device time (ms) of one step, by CUDA events on ``stream``.  Without ``flush``
+    the steps run back to back inside one event pair; with it, ``flush()`` (a write larger
+    than L2) runs before each step and each step has its own event pair.  With ``cache``
+    the steps are run again with its profile events around the split-K attention kernel,
+    whose mean time is returned as well (else None)."""
+    import torch
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    torch.cuda.synchronize()
+    if flush is None:
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        step_ms = a.elapsed_time(b) / steps
+    else:
+        pairs = [(ev(), ev()) for _ in range(steps)]
+        for a, b in pairs:
+            flush()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        step_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    kern_ms = None
+    if cache is not None:
+        pairs = [(ev(), ev()) for _ in range(steps)]
+        for a, b in pairs:
+            if flush is not None:
+                flush()
+            cache.set_profile_events(a, b)
+            step()
+        torch.cuda.synchronize()
+        cache.set_profile_events(None, None)
+        kern_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    return step_ms, kern_ms
+
+
+def make_flush(dev):
+    """A callable that overwrites a buffer of 4x the L2 size (evicts every cached line)."""
+    import torch
+    buf = torch.empty(int(4 * L2_BYTES), dtype=torch.uint8, device=dev)
+    return lambda: buf.fill_(1)
+
+
+def build_decode(dev, w, pages="fp16"):
+    """The library cache and device tensors of a decode workload from make_workload."""
+    import torch
+    from rank_compressed_paged_gb300 import PagedCoeffCache
+    shape = w["shape"]
+
+    def td(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    kp_dev, vp_dev = w["kp"], w["vp"]
+    if pages == "fp8_e4m3":
+        # the same seeded coefficients stored as E4M3 codes (torch's float8 cast)
+        kp_dev = kp_dev.to(torch.float8_e4m3fn).view(torch.uint8)
+        vp_dev = vp_dev.to(torch.float8_e4m3fn).view(torch.uint8)
+        del w["kp"], w["vp"]
+        torch.cuda.empty_cache()
+    cache = PagedCoeffCache(shape["num_heads"], shape["head_dim"], shape["rank_k"],
+                            shape["rank_v"], kp_dev.shape[0], td(w["U"]), td(w["W"]),
+                            k_pages=kp_dev, v_pages=vp_dev, page_format=pages)
+    t = dict(q=td(w["q"]), nk=td(w["nk"]), nv=td(w["nv"]), slots=td(w["slots"]),
+             table=td(w["table"]), lens=td(w["seq_lens"]))
+    t["out"] = torch.empty_like(t["q"])
+    t["ws"] = cache.workspace(w["batch"])
+    return cache, t
+
+
+def measure_decode_config(dev, stream, steps, warmup, shape_name, batch, seq=None,
+                          ragged=None, seed=1001, pages="fp16"):
+    """One decode configuration (append 1 token per sequence + decode), timed like the
+    headline; inputs smaller than twice the L2 size are timed one step at a time with L2
+    overwritten before each.  Returns a dict of the figures the bench line reports."""
+    import torch
+    shape = wl.SHAPES[shape_name]
+    w = make_workload(dev, seed, shape=shape, batch=batch, seq=seq, ragged=ragged,
+                      peaked=False)
+    cache, t = build_decode(dev, w, pages)
+
+    def step():
+        cache.decode_step(t["nk"], t["nv"], t["slots"], t["q"], t["table"], t["lens"],
+                          out=t["out"], workspace=t["ws"])
+
+    for _ in range(max(warmup, 3)):
+        step()
+    coeff = wl.algorithmic_bytes_decode(shape, w["seq_lens"], 1 if pages == "fp8_e4m3" else 2)
+    step_bytes = coeff + wl.factor_bytes(shape)
+    flush = make_flush(dev) if coeff < 2 * L2_BYTES else None
+    step_ms, kern_ms = time_steps(step, steps, stream, flush=flush, cache=cache)
+    assert cache.read_device_error() == 0, cache.read_device_error()
+    peak, kind = measured_peaks()
+    res = {"shape": shape_name, "batch": batch,
+           "seq_len": seq if ragged is None else f"uniform {ragged[0]}..{ragged[1]}",
+           "tokens": int(np.sum(w["seq_lens"])), "pages": pages,
+           "step": "append 1 token/seq + decode",
+           "l2": "flushed before each timed step" if flush else "inputs larger than L2",
+           "us_per_step": round(step_ms * 1e3, 2),
+           "step_bytes": step_bytes, "coefficient_bytes": coeff,
+           "step_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
+           "step_frac_of_8TBps": round(step_bytes / (step_ms * 1e-3) / 8e12, 4),
+           "kernel": "decode_main_kernel", "kernel_us": round(kern_ms * 1e3, 2),
+           "kernel_gbs": round(coeff / (kern_ms * 1e-3) / 1e9, 1),
+           "kernel_frac_of_peak": round(coeff / (kern_ms * 1e-3) / 1e9 / peak, 4),
+           "peak_gbs": peak, "peak_kind": kind,
+           "kernel_frac_of_8TBps": round(coeff / (kern_ms * 1e-3) / 8e12, 4),
+           "pv_tflops_kernel": round(decode_step_flops(w["seq_lens"], shape=shape)["pv"] /
+                                     (kern_ms * 1e-3) / 1e12, 2)}
+    del cache, t, w
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
-    from rank_compressed_paged_gb300 import PagedCoeffCache
     from rank_compressed_paged_gb300 import build as _build
 
     if rank == 0 or world == 1:
@@ -300,25 +488,12 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    # the CPU baseline's pool is spawned before the device work starts
+    pool = OraclePool() if (world == 1 and not args.no_cpu_baseline) else None
     w = make_workload(dev, seed=rank_seed(rank))
-    H, d = SHAPE["num_heads"], SHAPE["head_dim"]
-
-    def td(x):
-        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
-
-    kp_dev, vp_dev = w["kp"], w["vp"]
-    if args.pages == "fp8_e4m3":
-        # the same seeded coefficients stored as E4M3 codes (torch's float8 cast)
-        kp_dev = kp_dev.to(torch.float8_e4m3fn).view(torch.uint8)
-        vp_dev = vp_dev.to(torch.float8_e4m3fn).view(torch.uint8)
-        del w["kp"], w["vp"]
-        torch.cuda.empty_cache()
-    cache = PagedCoeffCache(H, d, SHAPE["rank_k"], SHAPE["rank_v"], kp_dev.shape[0], td(w["U"]),
-                            td(w["W"]), k_pages=kp_dev, v_pages=vp_dev, page_format=args.pages)
-    q, nk, nv, slots = td(w["q"]), td(w["nk"]), td(w["nv"]), td(w["slots"])
-    table, lens = td(w["table"]), td(w["seq_lens"])
-    out = torch.empty_like(q)
-    ws = cache.workspace(BATCH)
+    cache, tt = build_decode(dev, w, args.pages)
+    q, nk, nv, slots = tt["q"], tt["nk"], tt["nv"], tt["slots"]
+    table, lens, out, ws = tt["table"], tt["lens"], tt["out"], tt["ws"]
     stream = torch.cuda.current_stream()
 
     def step():
@@ -430,13 +605,26 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- aggregate over ranks (max time)
     step_ms, e2e_ms, kern_ms = reduce_max([step_ms, e2e_ms, kern_ms], world, dev)
+    w_seq_lens, w_U, w_W = w["seq_lens"], w["U"], w["W"]
+    del cache, tt, w, dbuf
+    torch.cuda.empty_cache()
+
+    # ---- every other configuration (1 GPU runs only; rank 0 of a replica job skips them)
+    configs = None
+    if world == 1 and not args.no_configs and args.sparse is None and args.pages == "fp16" \
+            and not RAGGED and not PEAKED and BATCH == 64 and SEQ == 8192:
+        with ClockSampler(local_rank) as cclk:
+            configs = measure_configs(dev, stream, args)
+        configs["clocks"] = cclk.summary()
     if rank != 0:
+        if pool is not None:
+            pool.close()
         return
     # the step's bytes: the coefficients plus the factors U_k and W_v, each counted once
     step_bytes = coeff_bytes + wl.factor_bytes(SHAPE)
     value = job_gbs(step_bytes, world, step_ms)
     e2e_value = job_gbs(step_bytes, world, e2e_ms)
-    flops = decode_step_flops(w["seq_lens"], kept_tok)
+    flops = decode_step_flops(w_seq_lens, kept_tok)
     peak, peak_kind = measured_peaks()
     achieved = read_bytes / (kern_ms * 1e-3) / 1e9
     traffic = None
@@ -445,13 +633,23 @@ def run_ours(args, rank, world, local_rank):
             traffic = ncu_traffic_per_launch()
         elif args.sparse == 2.0 ** -8 and PEAKED:
             traffic = ncu_traffic_per_launch(SPARSE_PROFILE_SUMMARY)
+    if configs is not None:
+        configs["C2_b64_l8192_append"] = {
+            "see": "headline keys (value, us_per_step, roofline)", "us_per_step":
+            round(step_ms * 1e3, 2), "kernel_us": round(kern_ms * 1e3, 2),
+            "kernel_frac_of_peak": round(achieved / peak, 4)}
     # CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N=1)
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        n, el, gbs = oracle_sample(w["U"], w["W"], args.cpu_requests, 4242, args.cpu_budget_s)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{n} of {BATCH} sequences of 8192 tokens (append + decode), "
-                         f"{el:.1f} s of fp64 numpy oracle"}
+    if pool is not None:
+        per = max(1, (args.cpu_requests + pool.n - 1) // pool.n)
+        n, busy = pool.run(w_U, w_W, per, 4242, args.cpu_budget_s)
+        pool.close()
+        cpu = {"value": round(n * bytes_per_request() / busy / 1e9, 4), "unit": "GB/s",
+               "cores": pool.n, "host_cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{n} sequences of {SEQ} tokens (append + decode), each like one "
+                         f"of the batch's {BATCH}, over {pool.n} single-threaded processes "
+                         f"running concurrently; {busy:.1f} s of fp64 numpy oracle in the "
+                         "busiest process"}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 4),
@@ -468,7 +666,7 @@ def run_ours(args, rank, world, local_rank):
                             else ""), "pages": args.pages,
                    "attention": "peaked (42% background pages)" if PEAKED else "N(0,1) scores",
                    "l2": f"inputs larger than L2 ({coeff_bytes / 1e9:.2f} GB of pages per GPU), "
-                         "no flush" if coeff_bytes > 2 * 129e6 else
+                         "no flush" if coeff_bytes > 2 * L2_BYTES else
                          "pages smaller than 2x L2: later steps may hit L2",
                    "parallelism": f"replicas x{world}, batch-sharded, no collective",
                    "step_bytes": {"coefficients": coeff_bytes, "factors": wl.factor_bytes(SHAPE),
@@ -491,18 +689,47 @@ def run_ours(args, rank, world, local_rank):
                         "note": "P*C_v on tcgen05 (fp16 in, fp32 accumulation); scores on CUDA "
                                 "cores; query / output projections and the append on tcgen05"},
         "sparse": sparse,
-        "gpu_launches": args.steps * 5,
+        "gpu_launches": args.steps * LAUNCHES_PER_DECODE_STEP,
         "clocks": clk.summary(),
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
 
 
-def decode_step_flops(seq_lens, kept_tokens=None) -> dict:
+# kernels one decode step launches: append GEMM, plan + query projection, split-K
+# attention, combine, up-projection GEMM
+LAUNCHES_PER_DECODE_STEP = 5
+
+
+def measure_configs(dev, stream, args):
+    """Every other configuration of the workload list, each timed on its own (one GPU):
+    decode steps at the tiny shape, batch 16 x 1024, E4M3 pages at batch 64 x 8192,
+    batch 20 x 32768, 64 ragged sequences, and the chunked prefill in both variants."""
+    steps = max(args.steps, 20)
+    out = {}
+    out["C0_tiny_b2_l256"] = measure_decode_config(dev, stream, steps, args.warmup, "tiny", 2,
+                                                   seq=256, seed=1000)
+    out["C1_b16_l1024"] = measure_decode_config(dev, stream, steps, args.warmup, "mha32", 16,
+                                                seq=1024, seed=1001)
+    out["C2_b64_l8192_append_e4m3"] = measure_decode_config(
+        dev, stream, steps, args.warmup, "mha32", 64, seq=8192, seed=1002, pages="fp8_e4m3")
+    out["C3_b20_l32768"] = measure_decode_config(dev, stream, steps, args.warmup, "mha32", 20,
+                                                 seq=32768, seed=1003)
+    out["C3_ragged64_l128_16384"] = measure_decode_config(
+        dev, stream, steps, args.warmup, "mha32", 64, ragged=(128, 16384), seed=1013)
+    for variant in ("rank", "reconstruct"):
+        out[f"C4_prefill_b16_p4096_c256_{variant}"] = measure_prefill(
+            dev, stream, 16, 4096, 256, variant, "fp16", steps, args.warmup)
+    return out
+
+
+def decode_step_flops(seq_lens, kept_tokens=None, shape=None) -> dict:
     """Multiply-add work of one decode step (2 FLOPs each): P*C_v (H*R per cached token, or
     per kept token for the block-sparse decode), scores (H*r_k per token), the query and the
     output projections (H*r_k*d and H*R*d per request) and the append of one token per
     request (H*r_k*d + R*H*d)."""
-    H, d, rk, R = SHAPE["num_heads"], SHAPE["head_dim"], SHAPE["rank_k"], SHAPE["rank_v"]
+    shape = SHAPE if shape is None else shape
+    H, d, rk, R = shape["num_heads"], shape["head_dim"], shape["rank_k"], shape["rank_v"]
     L = int(np.sum(np.asarray(seq_lens, np.int64)))
     B = len(seq_lens)
     f = {"pv": 2 * (L if kept_tokens is None else kept_tokens) * H * R,
@@ -536,16 +763,11 @@ def prefill_recon_flops(prior, chunk, batch):
     return batch * (prior + chunk) * 2 * R * H * d + keys * 2 * H * (rk + d)
 
 
-def run_prefill(args):
-    """Chunked prefill at batch 16, 4096 cached tokens + a 256-token chunk per request:
-    append the chunk, then causal chunk attention.  One JSON line (not the default run)."""
+def measure_prefill(dev, stream, B, prior, chunk, variant, pages, steps, warmup):
+    """Chunked prefill: append the chunk, then causal chunk attention; returns the figures
+    of the prefill line (step time, the attention kernels' time and tensor rate)."""
     import torch
     from rank_compressed_paged_gb300 import PagedCoeffCache
-    from rank_compressed_paged_gb300 import build as _build
-    _build.build()
-    B, prior, chunk = args.prefill_batch, args.prefill_prior, args.prefill_chunk
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
     after = np.full(B, prior + chunk, np.int32)
     kp, vp, table, lens = wl.make_paged_cache_device(after, SHAPE, 1004, device=dev,
                                                      spare_blocks=16)
@@ -562,70 +784,78 @@ def run_prefill(args):
     slots = td(np.array([wl.slot_for(table, b, prior + i) for b in range(B) for i in range(chunk)],
                         np.int64))
     cu = td((np.arange(B + 1) * chunk).astype(np.int32))
-    if args.pages == "fp8_e4m3":   # the same seeded coefficients as E4M3 codes
+    if pages == "fp8_e4m3":   # the same seeded coefficients as E4M3 codes
         kp = kp.to(torch.float8_e4m3fn).view(torch.uint8)
         vp = vp.to(torch.float8_e4m3fn).view(torch.uint8)
         torch.cuda.empty_cache()
     cache = PagedCoeffCache(32, 128, 64, 1024, kp.shape[0], td(U), td(W), k_pages=kp, v_pages=vp,
-                            page_format=args.pages)
+                            page_format=pages)
     tab, ln = td(table), td(lens)
     out = torch.empty_like(q)
-    ws = cache.workspace(T)
-    stream = torch.cuda.current_stream()
-
-    variant = args.prefill_variant
     if variant == "auto":
         from rank_compressed_paged_gb300 import RECONSTRUCT_MIN_CHUNK
         variant = "reconstruct" if (chunk >= RECONSTRUCT_MIN_CHUNK or
-                                    args.pages == "fp8_e4m3") else "rank"
-    if variant == "reconstruct":
-        ws = cache.workspace(T, cache.reconstruct_workspace_bytes(T, B, table.shape[1]))
+                                    pages == "fp8_e4m3") else "rank"
+    ws = (cache.workspace(T, cache.reconstruct_workspace_bytes(T, B, table.shape[1]))
+          if variant == "reconstruct" else cache.workspace(T))
 
     def step():
         cache.append_kv(k, v, slots)
         cache.prefill_attn(q, cu, tab, ln, out=out, workspace=ws, variant=variant)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(0) as clk:
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    step_ms = e0.elapsed_time(e1) / args.steps
-    ks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ke = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        cache.set_profile_events(ks[i], ke[i])
-        step()
-    torch.cuda.synchronize()
-    cache.set_profile_events(None, None)
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ks, ke))
+    step_ms, kern_ms = time_steps(step, steps, stream, cache=cache)
     assert cache.read_device_error() == 0
     attn_f, app_f = prefill_flops(prior, chunk, B)
     kern_f = attn_f if variant == "rank" else prefill_recon_flops(prior, chunk, B)
     peak_tf, kind = measured_tensor_peak()
+    res = {"variant": variant, "batch": B, "prior": prior, "chunk": chunk, "pages": pages,
+           "step": "append the chunk (T = B*chunk tokens) + chunk attention",
+           "ms_per_step": round(step_ms, 4),
+           "algorithmic_flops": attn_f + app_f,
+           "algorithmic_tflops_step": round((attn_f + app_f) / (step_ms * 1e-3) / 1e12, 2),
+           "kernel": "prefill_kernel" if variant == "rank"
+           else "recon_kernel + prefill_kernel (reconstructing)",
+           "kernel_ms": round(kern_ms, 4), "kernel_flops_executed": kern_f,
+           "kernel_tflops": round(kern_f / (kern_ms * 1e-3) / 1e12, 2),
+           "kernel_frac_of_peak": round(kern_f / (kern_ms * 1e-3) / 1e12 / peak_tf, 4),
+           "peak_tflops": peak_tf, "peak_kind": kind,
+           "l2": "inputs larger than L2 (0.43 GB of pages, 0.57 GB of reconstructed values)"}
+    del cache, kp, vp, q, k, v, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_prefill(args):
+    """Chunked prefill at batch 16, 4096 cached tokens + a 256-token chunk per request:
+    append the chunk, then causal chunk attention.  One JSON line (not the default run)."""
+    import torch
+    from rank_compressed_paged_gb300 import build as _build
+    _build.build()
+    B, prior, chunk = args.prefill_batch, args.prefill_prior, args.prefill_chunk
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    with ClockSampler(0) as clk:
+        r = measure_prefill(dev, stream, B, prior, chunk, args.prefill_variant, args.pages,
+                            args.steps, args.warmup)
     line = {
         "metric": f"chunked-prefill ms/step & algorithmic TFLOP/s at B={B}, prior {prior} + chunk {chunk}",
-        "variant": variant,
-        "value": round((attn_f + app_f) / (step_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-        "ms_per_step": round(step_ms, 3), "steps": args.steps, "warmup": max(args.warmup, 3),
+        "variant": r["variant"],
+        "value": r["algorithmic_tflops_step"], "unit": "TFLOP/s",
+        "ms_per_step": r["ms_per_step"], "steps": args.steps, "warmup": max(args.warmup, 3),
         "higher_is_better": True, "data": "synthetic",
         "dtype": "f16" if args.pages == "fp16" else "e4m3 pages widened to f16, f16/f32 arithmetic",
         "config": {"workload": f"prefill_b{B}_p{prior}_c{chunk}", "batch": B, "prior": prior,
-                   "chunk": chunk, "algorithmic_flops": attn_f + app_f,
-                   "step": "append the chunk (T = B*chunk tokens) + chunk attention", "pages": args.pages,
+                   "chunk": chunk, "algorithmic_flops": r["algorithmic_flops"],
+                   "step": r["step"], "pages": args.pages,
                    "value_flops": "rank-space work of the method, the same for both variants"},
-        "roofline": {"bound": "tensor",
-                     "kernel": "prefill_kernel" if variant == "rank"
-                     else "recon_kernel + prefill_kernel (reconstructing)",
-                     "achieved": round(kern_f / (kern_ms * 1e-3) / 1e12, 2),
-                     "peak": peak_tf, "peak_kind": kind, "unit": "TFLOP/s",
-                     "frac": round(kern_f / (kern_ms * 1e-3) / 1e12 / peak_tf, 4),
-                     "kernel_ms": round(kern_ms, 3), "flops_per_launch": kern_f,
+        "roofline": {"bound": "tensor", "kernel": r["kernel"],
+                     "achieved": r["kernel_tflops"], "peak": r["peak_tflops"],
+                     "peak_kind": r["peak_kind"], "unit": "TFLOP/s",
+                     "frac": r["kernel_frac_of_peak"], "kernel_ms": r["kernel_ms"],
+                     "flops_per_launch": r["kernel_flops_executed"],
                      "note": "fp16 dense tensor rate = the measured bf16 sustained rate"},
         "clocks": clk.summary(),
     }
@@ -642,6 +872,8 @@ def main():
     ap.add_argument("--cpu-requests", type=int, default=64)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations (C0, C1, C3, ragged, E4M3, prefill)")
     ap.add_argument("--batch", type=int, default=BATCH)
     ap.add_argument("--seq-len", type=int, default=SEQ)
     ap.add_argument("--ragged", type=str, default=None,
