@@ -696,9 +696,9 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-# kernels one decode step launches: append GEMM, plan + query projection, split-K
-# attention, combine, up-projection GEMM
-LAUNCHES_PER_DECODE_STEP = 5
+# kernels one decode step launches: the append with the query projection, the split-K
+# attention, the combine fused with the up-projection
+LAUNCHES_PER_DECODE_STEP = 3
 
 
 def measure_configs(dev, stream, args):

@@ -231,7 +231,7 @@ rcp_status rcp_set_profile_events(rcp_cache* cache, void* start_event, void* sto
  * the scratch is a fixed array of RCP_NOALLOC_SCRATCH_BYTES inside this library, which
  * every GPU that loads the library holds until the process exits.
  *   - Limit: batch must satisfy rcp_workspace_size(cache, batch) <=
- *     RCP_NOALLOC_SCRATCH_BYTES (for H=32, d=128, r_k=64, R=1024 that is batch <= 123);
+ *     RCP_NOALLOC_SCRATCH_BYTES (for H=32, d=128, r_k=64, R=1024 that is batch <= 157);
  *     a larger batch returns RCP_ERR_WORKSPACE and launches nothing.
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current) and keeps it for the life of the process; make that

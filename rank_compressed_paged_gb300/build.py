@@ -20,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "librcp.so")
-SOURCES = ["api.cu", "decode.cu", "gemm.cu", "prefill.cu", "recon.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "decode.cu", "gemm.cu", "combine.cu", "prefill.cu", "recon.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -92,10 +92,36 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 2-D fp32 tensor map without swizzle (the split-K records for the combine).
+bool encode_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rows == 0) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The combine's tensor maps over the records of nq query rows: slices of one head's ranks
+// of a CTA, and 4-float groups of (m, l).
+template <class S>
+bool encode_records(CUtensorMap* slices, CUtensorMap* ml, const float* rec, int64_t nq) {
+  using U = rcp::CombineCfg<S>;
+  const uint64_t rows = static_cast<uint64_t>(nq) + rcp::kMaxParts;
+  const uint64_t inner = S::REC, bytes = static_cast<uint64_t>(S::REC) * 4;
+  return encode_2d_f32(slices, rec, inner, rows, bytes, U::RANKS, U::CHUNK) &&
+         encode_2d_f32(ml, rec, inner, rows, bytes, 4, U::REC_ROWS);
+}
+
 template <class S>
 cudaError_t prepare_kernels(int dev) {
   cudaError_t e = rcp::prepare_attn<S>(dev);
   if (e == cudaSuccess) e = rcp::prepare_gemm<S>();
+  if (e == cudaSuccess) e = rcp::prepare_combine<S>();
   if (e == cudaSuccess) e = rcp::prepare_prefill<S>();
   if (e == cudaSuccess) e = rcp::prepare_recon<S>();
   return e;
@@ -157,8 +183,7 @@ void fill_ws(rcp::AttnParams& p, void* ws, int64_t nq) {
   p.qrow = reinterpret_cast<int32_t*>(b + w.qrow);
   p.qt = reinterpret_cast<float*>(b + w.qt);
   p.rec = reinterpret_cast<float*>(b + w.rec);
-  p.zhi = b + w.zhi;
-  p.zlo = b + w.zlo;
+  p.ucnt = reinterpret_cast<int32_t*>(b + w.ucnt);
   p.tile_b = reinterpret_cast<int32_t*>(b + w.tile_b);
   p.tile_qt = reinterpret_cast<int32_t*>(b + w.tile_qt);
   p.tcount = reinterpret_cast<int32_t*>(b + w.tcount);
@@ -199,13 +224,79 @@ struct SparseArgs {
   uint8_t* page_kept;
 };
 
+// New tokens a decode step appends before its attention (rcp_decode_step).
+struct AppendArgs {
+  const void* k;
+  const void* v;
+  const int64_t* slots;
+  int32_t T;
+};
+
+rcp_status check_append(const AppendArgs& a) {
+  if (a.T < 0) return RCP_ERR_INVALID_ARG;
+  if (a.T == 0) return RCP_OK;
+  if (!a.k || !a.v || !a.slots) return RCP_ERR_INVALID_ARG;
+  if (!aligned16(a.k) || !aligned16(a.v) || (reinterpret_cast<uintptr_t>(a.slots) & 7u))
+    return RCP_ERR_INVALID_ARG;
+  return RCP_OK;
+}
+
+// The projection launch: a step's append (app->T tokens; none when app is null) and, when
+// nq > 0, the decode's rank-space queries q~ (fp32 into qt), as tcgen05 jobs of one grid.
+rcp_status launch_front(rcp_cache* c, const AppendArgs* app, const void* q, int32_t nq,
+                        float* qt, float qscale, cudaStream_t s) {
+  const int32_t T = app ? app->T : 0;
+  if (T == 0 && nq == 0) return RCP_OK;
+  rcp::AppendParams p{};
+  p.k = T ? app->k : nullptr;
+  p.v = T ? app->v : nullptr;
+  p.slots = T ? app->slots : nullptr;
+  p.U_k = c->U_k;
+  p.W_v = c->W_v;
+  p.k_pages = c->k_pages;
+  p.v_pages = c->v_pages;
+  p.dev_err = c->dev_err;
+  p.num_blocks = c->cfg.num_blocks;
+  p.T = T;
+  p.fp8_pages = c->cfg.page_format == RCP_PAGES_FP8_E4M3 ? 1 : 0;
+  p.qt = qt;
+  p.nq = nq;
+  p.qscale = qscale;
+  // the new tokens' k and v and the queries as [rows][H*d] B operands (16-row tiles up to
+  // 16 rows, 64-row tiles up to 256, else 256-row tiles); an absent operand takes another's
+  // map (never read)
+  const uint64_t hd = static_cast<uint64_t>(c->cfg.num_heads) * c->cfg.head_dim;
+  const int32_t rows = T > nq ? T : nq;
+  const uint32_t nt = rows <= 16 ? 16 : (rows <= 256 ? 64 : 256);
+  CUtensorMap vmap, kmap, qmap;
+  if (T > 0 && (!encode_2d(&vmap, app->v, hd, static_cast<uint64_t>(T), hd * 2, 64, nt) ||
+                !encode_2d(&kmap, app->k, hd, static_cast<uint64_t>(T), hd * 2, 64, nt)))
+    return RCP_ERR_CUDA;
+  if (nq > 0 && !encode_2d(&qmap, q, hd, static_cast<uint64_t>(nq), hd * 2, 64, nt))
+    return RCP_ERR_CUDA;
+  if (T == 0) vmap = kmap = qmap;
+  if (nq == 0) qmap = kmap;
+  const cudaError_t e =
+      c->shape == kShapeMain
+          ? rcp::launch_append_gemm<ShapeMain>(c->tmap_wv_k, c->tmap_uk64, vmap, kmap, qmap, p, s)
+          : rcp::launch_append_gemm<ShapeTiny>(c->tmap_wv_k, c->tmap_uk64, vmap, kmap, qmap, p, s);
+  return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
+}
+
 rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, int32_t nq,
                          const int32_t* block_table, int32_t max_blocks_per_seq,
                          const int32_t* seq_lens, int32_t batch, void* out, void* ws,
-                         size_t ws_size, rcp_stream stream, bool after_own_append = false,
+                         size_t ws_size, rcp_stream stream, const AppendArgs* app = nullptr,
                          bool recon = false, const SparseArgs* sparse = nullptr) {
   if (!c || batch < 0 || nq < 0 || max_blocks_per_seq < 1) return RCP_ERR_INVALID_ARG;
-  if (nq == 0) return RCP_OK;
+  if (app && check_append(*app) != RCP_OK) return RCP_ERR_INVALID_ARG;
+  if (nq == 0) {
+    // nothing to attend; a step still appends its tokens
+    if (!app || app->T == 0) return RCP_OK;
+    rcp_status st = ensure_device(c);
+    if (st != RCP_OK) return st;
+    return launch_front(c, app, nullptr, 0, nullptr, 0.f, static_cast<cudaStream_t>(stream));
+  }
   if (batch == 0 && cu_chunk) return RCP_ERR_INVALID_ARG;
   if (!q || !block_table || !seq_lens || !out || !ws) return RCP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
@@ -241,7 +332,8 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   if (parts > max_blocks_total) parts = max_blocks_total;
   if (parts < 1) parts = 1;
   p.parts = static_cast<int32_t>(parts);
-  p.late_wait = after_own_append ? 1 : 0;
+  p.slots = app && app->T > 0 ? app->slots : nullptr;
+  p.n_slots = app ? app->T : 0;
   p.sparse = sparse ? 1 : 0;
   p.skip_tau = sparse ? sparse->tau : 0.f;
   p.page_kept = sparse ? sparse->page_kept : nullptr;
@@ -339,22 +431,33 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   p.tcount = nullptr;
   p.qhi = nullptr;
   p.qlo = nullptr;
-  // z_hi / z_lo ([nq][H*R] fp16) as the up-projection's B operands, 64 x 64 boxes
-  CUtensorMap zhi_map, zlo_map;
-  const uint64_t hr = static_cast<uint64_t>(c->cfg.num_heads) * c->cfg.rank_v;
-  if (!encode_2d(&zhi_map, p.zhi, hr, static_cast<uint64_t>(nq), hr * 2, 64, 64) ||
-      !encode_2d(&zlo_map, p.zlo, hr, static_cast<uint64_t>(nq), hr * 2, 64, 64))
+  // three launches: (A) the step's append with the rank-space queries, (B) the split-K
+  // attention, (C) the split-K combine fused with the W_v up-projection (combine.cu)
+  CUtensorMap rec_slices, rec_ml;
+  if (!(c->shape == kShapeMain ? encode_records<ShapeMain>(&rec_slices, &rec_ml, p.rec, nq)
+                               : encode_records<ShapeTiny>(&rec_slices, &rec_ml, p.rec, nq)))
     return RCP_ERR_CUDA;
+  rcp_status st2 = launch_front(c, app, q, nq, p.qt, p.qscale, s);
+  if (st2 != RCP_OK) return st2;
+  rcp::CombineParams cp{};
+  cp.cum = p.cum;
+  cp.rec = p.rec;
+  cp.upart = reinterpret_cast<float*>(
+      static_cast<uint8_t*>(ws) +
+      (c->shape == kShapeMain ? rcp::ws_layout<ShapeMain>(nq) : rcp::ws_layout<ShapeTiny>(nq)).upart);
+  cp.ucnt = p.ucnt;
+  cp.out = out;
+  cp.dev_err = c->dev_err;
+  cp.nq = nq;
+  cp.parts = p.parts;
   if (c->shape == kShapeMain) {
     e = rcp::launch_attn<ShapeMain>(c->tmap_v, c->tmap_kpage, p, s, c->prof_start, c->prof_stop);
     if (e == cudaSuccess)
-      e = rcp::launch_upproj_gemm<ShapeMain>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s,
-                                             pdl);
+      e = rcp::launch_combine_upproj<ShapeMain>(c->tmap_wv_mn, rec_slices, rec_ml, cp, s, pdl);
   } else {
     e = rcp::launch_attn<ShapeTiny>(c->tmap_v, c->tmap_kpage, p, s, c->prof_start, c->prof_stop);
     if (e == cudaSuccess)
-      e = rcp::launch_upproj_gemm<ShapeTiny>(c->tmap_wv_mn, zhi_map, zlo_map, out, nq, c->dev_err, s,
-                                             pdl);
+      e = rcp::launch_combine_upproj<ShapeTiny>(c->tmap_wv_mn, rec_slices, rec_ml, cp, s, pdl);
   }
   return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
 }
@@ -478,36 +581,11 @@ rcp_status rcp_append_kv(rcp_cache* c, const void* k, const void* v, const int64
                          int32_t num_tokens, rcp_stream stream) {
   if (!c || num_tokens < 0) return RCP_ERR_INVALID_ARG;
   if (num_tokens == 0) return RCP_OK;
-  if (!k || !v || !slot_mapping) return RCP_ERR_INVALID_ARG;
-  if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
-    return RCP_ERR_INVALID_ARG;
+  const AppendArgs app{k, v, slot_mapping, num_tokens};
+  if (check_append(app) != RCP_OK) return RCP_ERR_INVALID_ARG;
   rcp_status st = ensure_device(c);
   if (st != RCP_OK) return st;
-  rcp::AppendParams p{};
-  p.k = k;
-  p.v = v;
-  p.slots = slot_mapping;
-  p.U_k = c->U_k;
-  p.W_v = c->W_v;
-  p.k_pages = c->k_pages;
-  p.v_pages = c->v_pages;
-  p.dev_err = c->dev_err;
-  p.num_blocks = c->cfg.num_blocks;
-  p.T = num_tokens;
-  p.fp8_pages = c->cfg.page_format == RCP_PAGES_FP8_E4M3 ? 1 : 0;
-  // the new tokens' k and v as [T][H*d] B operands (64-token tiles up to 256 tokens)
-  const uint64_t hd = static_cast<uint64_t>(c->cfg.num_heads) * c->cfg.head_dim;
-  const uint32_t nt = num_tokens <= 256 ? 64 : 256;
-  CUtensorMap vmap, kmap;
-  if (!encode_2d(&vmap, v, hd, static_cast<uint64_t>(num_tokens), hd * 2, 64, nt) ||
-      !encode_2d(&kmap, k, hd, static_cast<uint64_t>(num_tokens), hd * 2, 64, nt))
-    return RCP_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e =
-      c->shape == kShapeMain
-          ? rcp::launch_append_gemm<ShapeMain>(c->tmap_wv_k, c->tmap_uk64, vmap, kmap, p, s)
-          : rcp::launch_append_gemm<ShapeTiny>(c->tmap_wv_k, c->tmap_uk64, vmap, kmap, p, s);
-  return e == cudaSuccess ? RCP_OK : RCP_ERR_CUDA;
+  return launch_front(c, &app, nullptr, 0, nullptr, 0.f, static_cast<cudaStream_t>(stream));
 }
 
 rcp_status rcp_decode_step(rcp_cache* c, const void* k, const void* v, const int64_t* slot_mapping,
@@ -516,11 +594,9 @@ rcp_status rcp_decode_step(rcp_cache* c, const void* k, const void* v, const int
                            void* out, void* workspace, size_t workspace_bytes,
                            rcp_stream stream) {
   if (!c || batch < 0 || num_tokens < 0 || max_blocks_per_seq < 1) return RCP_ERR_INVALID_ARG;
-  if (batch > 0 && workspace_bytes < ws_bytes(c, batch)) return RCP_ERR_WORKSPACE;
-  rcp_status st = rcp_append_kv(c, k, v, slot_mapping, num_tokens, stream);
-  if (st != RCP_OK) return st;
+  const AppendArgs app{k, v, slot_mapping, num_tokens};
   return run_attention(c, q, nullptr, batch, block_table, max_blocks_per_seq, seq_lens, batch, out,
-                       workspace, workspace_bytes, stream, num_tokens > 0);
+                       workspace, workspace_bytes, stream, &app);
 }
 
 rcp_status rcp_decode_attn(rcp_cache* c, const void* q, const int32_t* block_table,
@@ -542,7 +618,7 @@ rcp_status rcp_decode_attn_sparse(rcp_cache* c, const void* q, const int32_t* bl
                                      : INFINITY,
                 page_kept};
   return run_attention(c, q, nullptr, batch, block_table, max_blocks_per_seq, seq_lens, batch, out,
-                       workspace, workspace_bytes, stream, false, false, &sp);
+                       workspace, workspace_bytes, stream, nullptr, false, &sp);
 }
 
 rcp_status rcp_prefill_attn(rcp_cache* c, const void* q, const int32_t* cu_chunk_lens,
@@ -562,7 +638,7 @@ rcp_status rcp_prefill_attn_reconstruct(rcp_cache* c, const void* q, const int32
                                         size_t workspace_bytes, rcp_stream stream) {
   if (!cu_chunk_lens) return RCP_ERR_INVALID_ARG;
   return run_attention(c, q, cu_chunk_lens, num_query_rows, block_table, max_blocks_per_seq,
-                       seq_lens, batch, out, workspace, workspace_bytes, stream, false, true);
+                       seq_lens, batch, out, workspace, workspace_bytes, stream, nullptr, true);
 }
 
 rcp_status rcp_prefill_reconstruct_workspace_size(const rcp_cache* c, int32_t max_query_rows,

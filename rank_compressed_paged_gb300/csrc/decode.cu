@@ -1,31 +1,34 @@
-// Decode / chunked-prefill attention over low-rank paged coefficients.
+// Decode attention over low-rank paged coefficients, and the chunked prefill's plan.
 //
-// One call runs four kernels on the caller's stream (three of them here):
-//   1. plan_qproj:  CTA 0 validates lengths and builds the per-query-row work plan
-//                   (keys attended, block-table row, prefix sums of blocks); the other
-//                   CTAs project queries into rank space, q~_h = U_k,h q_h, scaled by
-//                   log2(e)/sqrt(d) so the softmax can use exp2.
-//   2. decode_main: persistent split-K kernel.  The concatenated list of all requests'
-//                   blocks is cut into `parts` equal contiguous ranges, one per CTA.  Per
-//                   block: a bulk copy brings the K page (all heads) and sixteen
-//                   tensor-map boxes bring the V page into shared memory; CUDA cores
-//                   score the block (a warp per 8 heads, 2 heads x 16 tokens per round,
-//                   one lane per token); an online softmax with lazy rescaling turns
-//                   scores into fp16 weights P; one elected thread issues tcgen05 MMAs
-//                   Z^T[R x heads] += C_v^T P^T into tensor memory.  At the end of each
-//                   (request, range) segment the accumulator and the running (max, sum)
-//                   go to a partial record.  Variants: E4M3 pages (codes widened to fp16
-//                   in shared memory) and block-sparse (a page's V is loaded only when
-//                   some head's weight in it reaches the threshold; "KV-cache LLM
-//                   serving" page, "What it measured", item 3).
-//   3. combine:     merges a request's partial records in a fixed order (deterministic)
-//                   and stores z as an fp16 (hi, lo) pair for the up-projection GEMM.
-//   4. (gemm.cu)    o_h = W_v[:, h*d:(h+1)*d]^T z_h on tensor cores, written as fp16.
+// A decode call is three launches on the caller's stream (programmatic dependent launch
+// between them):
+//   A. (gemm.cu)    the rank-space queries q~_h = U_k,h q_h, scaled by log2(e)/sqrt(d) so
+//                   the softmax can use exp2, in the same tensor-core launch as a decode
+//                   step's append.
+//   B. decode_main: persistent split-K kernel.  Every partition plans its own work from
+//                   the lengths (no planning launch): the concatenated list of all
+//                   requests' blocks is cut into `parts` equal contiguous ranges, one per
+//                   CTA.  Per block: tensor-map copies bring the K page (all heads) and the
+//                   V page into shared memory; CUDA cores score the block (a warp per 8
+//                   heads, 2 heads x 16 tokens per round, one lane per token); an online
+//                   softmax with lazy rescaling turns scores into fp16 weights P; one
+//                   elected thread issues tcgen05 MMAs Z^T[R x heads] += C_v^T P^T into
+//                   tensor memory.  At the end of each (request, range) segment the
+//                   accumulator and the running (max, sum) go to a partial record.  The
+//                   copies start while launch A still runs: only the compute warps wait
+//                   for it (for q~), and the copy thread only before a page that a decode
+//                   step's own append writes.  Variants: E4M3 pages (codes widened to fp16
+//                   in shared memory) and block-sparse (a page's V is loaded only when some
+//                   head's weight in it reaches the threshold; "KV-cache LLM serving" page,
+//                   "What it measured", item 3).
+//   C. (gemm.cu)    the split-K combine, merging each request's records in a fixed order
+//                   (deterministic), fused with o_h = W_v[:, h*d:(h+1)*d]^T z_h on tensor
+//                   cores.
 //
 // The steps follow the Proxima page: "Per-decode-step attention" (rank-space scoring of
 // the compressed cache, split-K with a combine kernel named in "Kernel profiling
 // breakdown", plus one matmul per step) and "Per-prefill-chunk attention" (each chunk
-// row attends its causal prefix; here every chunk row is planned as its own query row).
+// row attends its causal prefix; the plan below lists every chunk row and its tiles).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -40,19 +43,18 @@
 
 namespace rcp {
 
-// ----------------------------------------------------------------------------- plan + q~
+// ----------------------------------------------------------------------------- prefill plan
 constexpr int kPlanThreads = 256;
-constexpr int kQprojTile = 16;   // query rows per q-projection CTA
 
+// One CTA: keys attended (qlen) and block-table row (qrow) of every chunk row, the prefix
+// sums of their blocks, the list of 128-row query tiles and (reconstructing variant) the
+// page prefix sums of the requests with chunk rows.  Launched as a programmatic dependent
+// of the kernel before it, which may have produced the lengths, so it waits first.
 template <class S>
-__global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnParams p) {
-  // Launched as a programmatic dependent of the kernel before it.  Normally that kernel
-  // may have produced q / lengths, so wait first; within a fused decode step it is the
-  // step's own append, whose output this kernel never reads, so the wait moves to the end
-  // (completion of this kernel then still implies completion of the append).
-  if (!p.late_wait) griddep_wait();
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const AttnParams p) {
+  griddep_wait();
   griddep_launch();
-  if (blockIdx.x == 0) {
+  {
     // ---- plan: qlen / qrow per query row, then cum = prefix sum of ceil(qlen / 16)
     __shared__ int64_t warp_sum[kPlanThreads / 32];
     __shared__ int cu_bad;
@@ -171,65 +173,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_qproj_kernel(const AttnPara
         }
       }
     }
-    if (p.late_wait) griddep_wait();
-    return;
   }
-  // ---- q~ = U_k,h q_h for a tile of query rows and one head
-  constexpr int H = S::H, D = S::D, RK = S::RK;
-  __shared__ float ut[D][RK + 1];          // U_k,h transposed: ut[j][k] = U[h][k][j]
-  __shared__ float qs[kQprojTile][D + 1];
-  const int bid = blockIdx.x - 1;
-  const int h = bid % H;
-  const int q0 = (bid / H) * kQprojTile;
-  const __half* U = static_cast<const __half*>(p.U_k) + static_cast<size_t>(h) * RK * D;
-  const __half* Q = static_cast<const __half*>(p.q);
-  for (int i = threadIdx.x; i < RK * D / 8; i += kPlanThreads) {
-    const uint4 u8 = reinterpret_cast<const uint4*>(U)[i];
-    const __half* uh = reinterpret_cast<const __half*>(&u8);
-    const int k = (i * 8) / D, j0 = (i * 8) % D;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ut[j0 + e][k] = __half2float(uh[e]);
-  }
-  for (int i = threadIdx.x; i < kQprojTile * D; i += kPlanThreads) {
-    const int qq = i / D, j = i % D;
-    const int row = q0 + qq;
-    qs[qq][j] = row < p.nq ? __half2float(Q[(static_cast<size_t>(row) * H + h) * D + j]) : 0.f;
-  }
-  __syncthreads();
-  constexpr int NG = kPlanThreads / RK;         // query groups
-  constexpr int PER = kQprojTile / NG;          // rows per thread
-  const int k = threadIdx.x % RK, grp = threadIdx.x / RK;
-  float acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  for (int j = 0; j < D; ++j) {
-    const float u = ut[j][k];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = fmaf(u, qs[grp + i * NG][j], acc[i]);
-  }
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int row = q0 + grp + i * NG;
-    if (row >= p.nq) continue;
-    const float qv = acc[i] * p.qscale;
-    if (p.qhi == nullptr) {
-      p.qt[(static_cast<size_t>(row) * H + h) * RK + k] = qv;
-    } else {
-      // prefill: fp16 (hi, lo) pair feeding the score MMA, zero-padded to 64 ranks
-      const __half hi = __float2half_rn(qv);
-      const size_t base = (static_cast<size_t>(row) * H + h) * 64;
-      static_cast<__half*>(p.qhi)[base + k] = hi;
-      static_cast<__half*>(p.qlo)[base + k] = __float2half_rn(qv - __half2float(hi));
-      for (int pad = RK + k; pad < 64; pad += RK) {
-        static_cast<__half*>(p.qhi)[base + pad] = __float2half_rn(0.f);
-        static_cast<__half*>(p.qlo)[base + pad] = __float2half_rn(0.f);
-      }
-    }
-  }
-  if (p.late_wait) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------- decode main
+constexpr int kAppendSetBits = 9;
+constexpr int kAppendSetSize = 1 << kAppendSetBits;   // a step appending more tokens than
+                                                      // half this waits before any copy
 // F8: pages hold E4M3 codes.  K pages are scored straight from their bytes; V pages land
 // in raw stages and the compute warps widen them to fp16 in the swizzled layout the
 // tensor-core MMA reads (the layout the fp16 path's tensor-map copies produce).
@@ -255,7 +205,15 @@ struct DecodeSmem {
   static constexpr int INFO_OFF = MISC_OFF + 16;                    // valid tokens per stage:
   // K stages, then V; SKIP adds the physical block of each K stage, the decision ring and
   // the info word of each P buffer
-  static constexpr int TOTAL = INFO_OFF + (KST + VRS) * 4 + (SKIP ? (KST + DS + 2) * 4 : 0);
+  static constexpr int INFO_BYTES = (KST + VRS) * 4 + (SKIP ? (KST + DS + 2) * 4 : 0);
+  // the partition's plan: 32 warp partials of the scans, then the block total, the first
+  // request and its first block; then the set of blocks a decode step's append writes
+  static constexpr int PLAN_OFF = (INFO_OFF + INFO_BYTES + 7) & ~7;
+  static constexpr int HASH_OFF = PLAN_OFF + (32 + 4) * 8;
+  static constexpr int TOTAL = HASH_OFF + kAppendSetSize * 4;
+  static_assert(PLAN_OFF % 8 == 0 && HASH_OFF % 4 == 0 && A_OFF % 16 == 0 && Q_OFF % 16 == 0 &&
+                    BAR_OFF % 8 == 0,
+                "region alignment");
   static constexpr int ALLOC = TOTAL + 1024;                        // base alignment slack
   static_assert(KP % 128 == 0 && VP % 16 == 0 && S::VSTAGE_BYTES % 1024 == 0, "alignment");
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
@@ -312,30 +270,43 @@ __device__ __forceinline__ void widen_v_boxes(const uint8_t* src, uint8_t* vb, i
 
 constexpr float kRescaleThreshold = 8.f;   // log2 units: weights stay <= 2^8 before a rescale
 
-// Walks the requests that a CTA's block range crosses.
+// Keys of request b: its length when 0 <= L_b <= the table's capacity (max_len), else 0
+// (the partition that reports errors sets the length bit for it).
+__device__ __forceinline__ int32_t valid_len(int32_t L, int32_t max_len) {
+  return (L >= 0 && L <= max_len) ? L : 0;
+}
+
+// Walks the requests that a partition's block range crosses; request b covers blocks
+// [bstart, bend) of the concatenated list of all requests' blocks.
 struct ReqWalker {
-  const int64_t* cum;
+  const int32_t* lens;
+  int32_t max_len;
   int b;
   int64_t bstart, bend;
-  __device__ __forceinline__ void init(const int64_t* c, int nq, int64_t g0) {
-    cum = c;
-    int lo = 0, hi = nq - 1;   // largest b with cum[b] <= g0
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (cum[mid] <= g0) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-    bstart = cum[b];
-    bend = cum[b + 1];
+  __device__ __forceinline__ int64_t nblk(int r) const {
+    return (valid_len(lens[r], max_len) + kBlockSize - 1) / kBlockSize;
+  }
+  __device__ __forceinline__ void init(const int32_t* l, int32_t ml, int b0, int64_t s0) {
+    lens = l;
+    max_len = ml;
+    b = b0;
+    bstart = s0;
+    bend = s0 + nblk(b0);
   }
   __device__ __forceinline__ void advance_to(int64_t g) {
     while (g >= bend) {
       ++b;
       bstart = bend;
-      bend = cum[b + 1];
+      bend += nblk(b);
     }
   }
+  __device__ __forceinline__ int32_t len() const { return valid_len(lens[b], max_len); }
 };
+
+// Blocks a decode step's append writes, as an open-addressing set in shared memory.
+__device__ __forceinline__ uint32_t block_hash(int64_t blk) {
+  return (static_cast<uint32_t>(blk) * 2654435761u) >> (32 - kAppendSetBits);
+}
 
 struct BlockInfo {
   int nvalid;      // tokens of this block that are attended (0 for a rejected block id)
@@ -441,24 +412,128 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
         reinterpret_cast<uint4*>(vst + s * S::VSTAGE_BYTES + S::NBOX * 2048)[i] =
             make_uint4(0, 0, 0, 0);
   }
+
+  // ---- plan, from the lengths alone (inputs of the call, complete before the launch
+  // ahead of this one started, so they are read before waiting on it): request b covers
+  // ceil(L_b / 16) blocks of the concatenated list (none for an invalid length); the list
+  // is cut into G equal ranges, one per partition.  Partition 0 also reports invalid
+  // lengths and writes the block prefix sums for the combine.
+  constexpr int NWARP = NTHR / 32;
+  const int32_t max_len = p.bt_stride * kBlockSize;
+  int64_t* red = reinterpret_cast<int64_t*>(sm + L::PLAN_OFF);   // [32] warp partials
+  int64_t* plan = red + 32;                                       // first request, its block
+  {
+    int64_t part = 0;
+    for (int b = threadIdx.x; b < p.nq; b += NTHR)
+      part += (valid_len(p.seq_lens[b], max_len) + kBlockSize - 1) / kBlockSize;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) red[warp] = part;
+    if (threadIdx.x == 0) {
+      plan[0] = -1;
+      plan[1] = 0;
+    }
+  }
+  __syncthreads();
+  int64_t T = 0;
+#pragma unroll
+  for (int i = 0; i < NWARP; ++i) T += red[i];
+  // never more partitions than blocks, so every partition's range is non-empty
+  const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
+  const bool active = cta < G;   // uniform over the CTA
+  const int64_t g0 = active ? static_cast<int64_t>(cta) * T / G : 0;
+  const int64_t g1 = active ? static_cast<int64_t>(cta + 1) * T / G : 0;
+  const bool writer = cta == 0;
+  __syncthreads();   // every thread has its total before red[] is reused
+  if (writer) {
+    if (threadIdx.x == 0) p.cum[0] = 0;
+    // the combine's arrival counters, one per (tile of requests, head)
+    const int groups = (p.nq + CombineCfg<S>::NT - 1) / CombineCfg<S>::NT * S::H;
+    for (int i = threadIdx.x; i < groups; i += NTHR) p.ucnt[i] = 0;
+  }
+  if (writer || active) {
+    // chunked block-wide scan of the block counts until the request holding g0 is found
+    // (partition 0 scans them all)
+    int64_t base = 0;
+    for (int c0 = 0; c0 < p.nq; c0 += NTHR) {
+      const int b = c0 + threadIdx.x;
+      int64_t v = 0;
+      if (b < p.nq) {
+        const int32_t Lb = p.seq_lens[b];
+        if (writer && (Lb < 0 || Lb > max_len)) atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
+        v = (valid_len(Lb, max_len) + kBlockSize - 1) / kBlockSize;
+      }
+      int64_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) red[warp] = incl;
+      __syncthreads();
+      int64_t tot = 0;
+#pragma unroll
+      for (int i = 0; i < NWARP; ++i) {
+        if (i < warp) incl += red[i];
+        tot += red[i];
+      }
+      incl += base;
+      if (b < p.nq) {
+        if (writer) p.cum[b + 1] = incl;
+        if (active && v > 0 && incl - v <= g0 && g0 < incl) {
+          plan[0] = b;
+          plan[1] = incl - v;
+        }
+      }
+      base += tot;
+      __syncthreads();   // red[] is reused; plan[] is visible
+      if (!writer && plan[0] >= 0) break;   // uniform: read after the barrier
+    }
+  }
+  const int b_first = static_cast<int>(plan[0]);
+  const int64_t s_first = plan[1];
+  // ---- a decode step's own append (the launch ahead) writes these blocks: the copy thread
+  // waits for it before copying one of them, and before any copy when the step appends
+  // more tokens than the set holds
+  int* aset = reinterpret_cast<int*>(sm + L::HASH_OFF);
+  const bool step = p.n_slots > 0;
+  const bool wait_first = p.n_slots > kAppendSetSize / 2;
+  if (step && !wait_first) {
+    for (int i = threadIdx.x; i < kAppendSetSize; i += NTHR) aset[i] = -1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < p.n_slots; i += NTHR) {
+      const int64_t sl = p.slots[i];
+      if (sl < 0 || sl >= p.num_blocks * kBlockSize) continue;
+      const int blk = static_cast<int>(sl / kBlockSize);
+      uint32_t h = block_hash(blk);
+      for (int probe = 0; probe < kAppendSetSize; ++probe) {
+        const int prev = atomicCAS(&aset[h], -1, blk);
+        if (prev == -1 || prev == blk) break;
+        h = (h + 1) & (kAppendSetSize - 1);
+      }
+    }
+  }
+  auto appended = [&](int64_t blk) {
+    uint32_t h = block_hash(blk);
+    for (int probe = 0; probe < kAppendSetSize; ++probe) {
+      const int v = aset[h];
+      if (v == blk) return true;
+      if (v < 0) return false;
+      h = (h + 1) & (kAppendSetSize - 1);
+    }
+    return false;
+  };
+
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (warp == 0 && lane == 0) prefetch_tmap(&tmap_v);
-
-  griddep_wait();      // plan and rank-space queries are ready
-  griddep_launch();
-  const int64_t T = p.cum[p.nq];
-  // never more partitions than blocks, so every partition's range is non-empty
-  const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
-  const bool active = cta < G;   // uniform over the CTA
-  const int64_t g0 = active ? static_cast<int64_t>(cta) * T / G : 0;
-  const int64_t g1 = active ? static_cast<int64_t>(cta + 1) * T / G : 0;
+  griddep_launch();   // the combine + up-projection may start its prologue
 
   ReqWalker walk;
-  if (active) walk.init(p.cum, p.nq, g0);
+  if (active) walk.init(p.seq_lens, max_len, b_first, s_first);
 
   if (!active) {
     // no blocks for this CTA
@@ -468,14 +543,19 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
       const uint64_t pol = policy_evict_first();
       const uint8_t* kpages = static_cast<const uint8_t*>(p.k_pages);
       int64_t nk = 0, nv = 0;
+      bool waited = !step;
       for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
         walk.advance_to(g);
         const int64_t j = g - walk.bstart;
-        const int64_t raw = p.block_table[static_cast<int64_t>(p.qrow[walk.b]) * p.bt_stride + j];
+        const int64_t raw = p.block_table[static_cast<int64_t>(walk.b) * p.bt_stride + j];
         const bool bad = raw < 0 || raw >= p.num_blocks;
         if (bad) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
         const int64_t phys = bad ? 0 : raw;
-        const int64_t left = p.qlen[walk.b] - j * kBlockSize;
+        if (!waited && (wait_first || appended(phys))) {
+          griddep_wait();   // the step's append has written this block
+          waited = true;
+        }
+        const int64_t left = walk.len() - j * kBlockSize;
         const int nvalid = bad ? 0 : static_cast<int>(left < kBlockSize ? left : kBlockSize);
         const int ks = static_cast<int>(it % KST);
         if (it >= KST && !mbar_wait(&kempty[ks], ((it / KST) - 1) & 1, abort_flag, p.dev_err)) break;
@@ -566,6 +646,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
   } else if (SKIP && warp == 2 + NCW) {
     // ------------------------------------------ SKIP: value pages of the kept pages
     if (lane == 0) {
+      if (step) griddep_wait();   // pages an append ahead of this launch wrote
       const uint64_t pol = policy_evict_first();
       int64_t nv = 0;
       for (int64_t n = 0;; ++n) {
@@ -628,6 +709,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
     int64_t kk = 0;     // pages accumulated so far (SKIP: the kept ones), orders P / V use
     int64_t nd = 0;     // SKIP: decisions posted to the value-copy warp
     bool aborted = false;
+    griddep_wait();     // the rank-space queries of the launch ahead are written
 
     for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
       walk.advance_to(g);
@@ -637,12 +719,23 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
       bool ok = true;
       if (bi.seg_first) {
         // rank-space query of this request into the permuted layout
-        // qs[((h*2 + hi)*NCH + c)*4 + e] = q~[h][8c + 4hi + e]
-        const float* src = p.qt + static_cast<size_t>(walk.b) * S::H * S::RK;
-        for (int i = ctid; i < S::H * S::RK; i += CT) {
-          const int h = i / S::RK, k = i % S::RK;
-          const int c = k >> 3, hi = (k >> 2) & 1, e = k & 3;
-          qs[((h * 2 + hi) * NCH + c) * 4 + e] = src[i];
+        // qs[((h*2 + hi)*NCH + c)*4 + e] = q~[h][8c + 4hi + e]: four consecutive ranks
+        // stay together, so it moves as float4, every load issued before the first store
+        const float4* src = reinterpret_cast<const float4*>(p.qt) +
+                            static_cast<size_t>(walk.b) * (S::H * S::RK / 4);
+        constexpr int N4 = S::H * S::RK / 4, PER4 = (N4 + CT - 1) / CT;
+        float4 q4[PER4];
+#pragma unroll
+        for (int u = 0; u < PER4; ++u)
+          if (ctid + u * CT < N4) q4[u] = __ldcg(src + ctid + u * CT);
+#pragma unroll
+        for (int u = 0; u < PER4; ++u) {
+          const int i4 = ctid + u * CT;
+          if (i4 < N4) {
+            const int h = (i4 * 4) / S::RK, k = (i4 * 4) % S::RK;
+            const int c = k >> 3, hi = (k >> 2) & 1;
+            *reinterpret_cast<float4*>(qs + ((h * 2 + hi) * NCH + c) * 4) = q4[u];
+          }
         }
         named_bar_sync(1, CT);
       }
@@ -787,7 +880,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
       const bool kept = !SKIP || (f & 4);
       if constexpr (SKIP) {
         if (ctid == 0 && p.page_kept != nullptr)
-          p.page_kept[static_cast<int64_t>(p.qrow[walk.b]) * p.bt_stride + (g - walk.bstart)] =
+          p.page_kept[static_cast<int64_t>(walk.b) * p.bt_stride + (g - walk.bstart)] =
               kept ? 1 : 0;
         if (kept) {
           if (ctid == 0) {   // its value page: to the value-copy warp, as early as possible
@@ -902,12 +995,12 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
               float v[16];
               tmem_ld16(ta, v);
               tmem_wait_ld();
+              // head-major: the lanes of a warp (consecutive ranks) store 128 contiguous
+              // bytes per head
               if (rrow < S::R) {
-                float4* dst = reinterpret_cast<float4*>(rec + static_cast<size_t>(rrow) * HP + hh * 16);
-                dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-                dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-                dst[2] = make_float4(v[8], v[9], v[10], v[11]);
-                dst[3] = make_float4(v[12], v[13], v[14], v[15]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  rec[static_cast<size_t>(hh * 16 + e) * S::R + rrow] = v[e];
               }
             }
           }
@@ -952,135 +1045,6 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
   }
 }
 
-// ----------------------------------------------------------------------------- combine
-constexpr int kCombineThreads = 256;
-
-__device__ __forceinline__ int part_of(int64_t g, int64_t T, int G) {
-  // the CTA whose range [c*T/G, (c+1)*T/G) holds block g
-  return static_cast<int>(((g + 1) * G + T - 1) / T - 1);
-}
-
-// Merges a request's partial records (one per CTA range that touched it) into
-// z_h = sum_i 2^(m_i,h - M_h) z_i,h / sum_i 2^(m_i,h - M_h) l_i,h, M_h = max_i m_i,h.
-// One CTA per (request, slice of RB joint-rank rows); the slice of a record is RB * HP
-// contiguous floats.  Every pass is parallel over records: the (max, sum) pass spreads
-// the records over thread groups, the accumulation gives each float4 of the slice NG
-// threads that walk interleaved record subsets; partials are then added in a fixed order,
-// so the result does not depend on timing.  NG = 4 serves small batches, where a request
-// is split over many CTAs and there are few requests to spread the work.
-template <class S, int NG>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const AttnParams p) {
-  constexpr int HP = S::HP, H = S::H, R = S::R;
-  constexpr int F4 = kCombineThreads / NG;     // float4 per slice
-  constexpr int RB = F4 * 4 / HP;              // joint-rank rows per CTA
-  constexpr int MG = kCombineThreads / HP;     // record groups of the (max, sum) pass
-  constexpr size_t REC4 = S::REC / 4;
-  static_assert(R % RB == 0 && S::REC % 4 == 0, "combine tiling");
-  __shared__ float4 e_s4[kMaxParts * HP / 4];  // unnormalised weights e_i,h
-  __shared__ float red[MG][HP];
-  __shared__ float inv_l[HP];
-  __shared__ float4 part[NG > 1 ? NG - 1 : 1][F4];
-  __shared__ float zt[HP][RB + 1];
-  griddep_wait();
-  griddep_launch();
-  const int b = blockIdx.x;
-  const int r0 = blockIdx.y * RB;
-  const int tid = threadIdx.x;
-  const int64_t c0 = p.cum[b], c1 = p.cum[b + 1];
-  __half* zh = static_cast<__half*>(p.zhi) + static_cast<size_t>(b) * H * R;
-  __half* zl = static_cast<__half*>(p.zlo) + static_cast<size_t>(b) * H * R;
-  if (c1 == c0) {   // empty sequence: z = 0
-    for (int i = tid; i < H * RB; i += kCombineThreads) {
-      const size_t at = static_cast<size_t>(i / RB) * R + r0 + i % RB;
-      zh[at] = __float2half_rn(0.f);
-      zl[at] = __float2half_rn(0.f);
-    }
-    return;
-  }
-  const int64_t T = p.cum[p.nq];
-  const int G = static_cast<int>(T < p.parts ? T : p.parts);   // as in decode_main_kernel
-  const int pf = part_of(c0, T, G), pl = part_of(c1 - 1, T, G);
-  const int nrec = pl - pf + 1;
-  const float* rec0 = p.rec + static_cast<size_t>(b + pf) * S::REC;
-  float* e_s = reinterpret_cast<float*>(e_s4);
-  {
-    // ---- per-head maximum, then e_i,h = 2^(m_i,h - M_h) and the sum of e_i,h l_i,h
-    const int h = tid % HP, g = tid / HP;
-    const float* ml = rec0 + static_cast<size_t>(R) * HP + h;   // m at +0, l at +HP
-    float mx = -INFINITY;
-    for (int i = g; i < nrec; i += MG) {
-      const float m = __ldcg(ml + static_cast<size_t>(i) * S::REC);
-      e_s[i * HP + h] = m;
-      mx = fmaxf(mx, m);
-    }
-    red[g][h] = mx;
-    __syncthreads();
-    float M = -INFINITY;
-#pragma unroll
-    for (int gg = 0; gg < MG; ++gg) M = fmaxf(M, red[gg][h]);
-    float sum = 0.f;
-    for (int i = g; i < nrec; i += MG) {
-      const float m = e_s[i * HP + h];
-      const float e = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      e_s[i * HP + h] = e;
-      sum = fmaf(e, __ldcg(ml + static_cast<size_t>(i) * S::REC + HP), sum);
-    }
-    __syncthreads();   // every thread has read red[] for its maximum
-    red[g][h] = sum;
-    __syncthreads();
-    if (tid < HP) {
-      float L = 0.f;
-#pragma unroll
-      for (int gg = 0; gg < MG; ++gg) L += red[gg][tid];
-      inv_l[tid] = L > 0.f ? 1.f / L : 0.f;
-    }
-  }
-  // ---- accumulate this thread's float4 of the slice over its subset of the records
-  const int f = tid % F4, grp = tid / F4;
-  const int rr = (4 * f) / HP, h0 = (4 * f) % HP;
-  const float4* src = reinterpret_cast<const float4*>(rec0 + static_cast<size_t>(r0 + rr) * HP + h0);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int i = grp; i < nrec; i += NG) {
-    const float4 v = __ldcg(src + static_cast<size_t>(i) * REC4);
-    const float4 e = e_s4[(i * HP + h0) / 4];
-    acc.x = fmaf(e.x, v.x, acc.x);
-    acc.y = fmaf(e.y, v.y, acc.y);
-    acc.z = fmaf(e.z, v.z, acc.z);
-    acc.w = fmaf(e.w, v.w, acc.w);
-  }
-  if (NG > 1) {
-    if (grp > 0) part[grp - 1][f] = acc;
-    __syncthreads();
-    if (grp == 0) {
-#pragma unroll
-      for (int gg = 0; gg < NG - 1; ++gg) {
-        const float4 q = part[gg][f];
-        acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
-      }
-    }
-  } else {
-    __syncthreads();   // inv_l is ready
-  }
-  if (grp == 0) {
-    zt[h0 + 0][rr] = acc.x * inv_l[h0 + 0];
-    zt[h0 + 1][rr] = acc.y * inv_l[h0 + 1];
-    zt[h0 + 2][rr] = acc.z * inv_l[h0 + 2];
-    zt[h0 + 3][rr] = acc.w * inv_l[h0 + 3];
-  }
-  __syncthreads();
-  // z as an unevaluated fp16 pair (hi + lo) so the up-projection can run on fp16 tensor
-  // cores with fp32-level accuracy
-  for (int i = tid; i < H * RB; i += kCombineThreads) {
-    const int hh = i / RB, x = i % RB;
-    const float z = zt[hh][x];
-    const __half hi = __float2half_rn(z);
-    const size_t at = static_cast<size_t>(hh) * R + r0 + x;
-    zh[at] = hi;
-    zl[at] = __float2half_rn(z - __half2float(hi));
-  }
-}
-
 // ----------------------------------------------------------------------------- launches
 template <class S>
 cudaError_t prepare_attn(int device) {
@@ -1099,18 +1063,15 @@ cudaError_t prepare_attn(int device) {
   return e;
 }
 
-// All kernels are launched as programmatic dependents of the kernel before them (each
-// waits for its predecessor before touching its outputs or the caller's inputs), so
-// launch latency and prologues overlap the predecessor's tail.  With profiling events
-// the plain stream order is kept so the events bracket decode_main exactly.
+// Launched as a programmatic dependent of the kernel before it (the query projection, with
+// a decode step's append): its prologue and plan, and its page copies unless they read
+// what an append in that launch writes, overlap that kernel.  With profiling events the
+// plain stream order is kept so the events bracket decode_main exactly.
 template <class S>
 cudaError_t launch_attn(const CUtensorMap& tmap_v, const CUtensorMap& tmap_k, const AttnParams& p,
                         cudaStream_t stream, cudaEvent_t prof_start, cudaEvent_t prof_stop) {
   const bool pdl = prof_start == nullptr;
-  const int qtiles = (p.nq + kQprojTile - 1) / kQprojTile;
-  cudaError_t e = launch_pdl(plan_qproj_kernel<S>, dim3(1 + S::H * qtiles), dim3(kPlanThreads), 0,
-                             stream, pdl, p);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   if (prof_start && (e = cudaEventRecord(prof_start, stream)) != cudaSuccess) return e;
   if (p.fp8_pages)
     e = launch_pdl(decode_main_kernel<S, true, false>, dim3(p.parts),
@@ -1126,21 +1087,13 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const CUtensorMap& tmap_k, co
                    tmap_v, tmap_k, p);
   if (e != cudaSuccess) return e;
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
-  // small batches: four threads per slice element so that a request's many records are
-  // read with more parallelism
-  constexpr int RB1 = kCombineThreads * 4 / S::HP, RB4 = RB1 / 4;
-  if (static_cast<int64_t>(p.nq) * (S::R / RB1) >= 2 * static_cast<int64_t>(p.parts))
-    return launch_pdl(combine_kernel<S, 1>, dim3(p.nq, S::R / RB1), dim3(kCombineThreads), 0,
-                      stream, pdl, p);
-  return launch_pdl(combine_kernel<S, 4>, dim3(p.nq, S::R / RB4), dim3(kCombineThreads), 0,
-                    stream, pdl, p);
+  return cudaSuccess;
 }
 
-// The plan alone (CTA 0 of the planning kernel); the prefill path projects its queries
-// on tensor cores instead.
+// The chunked prefill's plan (one CTA).
 template <class S>
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream, bool pdl) {
-  return launch_pdl(plan_qproj_kernel<S>, dim3(1), dim3(kPlanThreads), 0, stream, pdl, p);
+  return launch_pdl(plan_kernel<S>, dim3(1), dim3(kPlanThreads), 0, stream, pdl, p);
 }
 
 template cudaError_t launch_plan<ShapeMain>(const AttnParams&, cudaStream_t, bool);

@@ -1,5 +1,6 @@
-// Tensor-core projections: the append's key / value projections and the decode's W_v
-// up-projection, as tcgen05 GEMMs D[128 x NT] = A[128 x K] * B[NT x K]^T.
+// Tensor-core projections: the append's key / value projections (with, in the same
+// launch, the decode's rank-space queries) and the chunked prefill's rank-space queries,
+// as tcgen05 GEMMs D[128 x NT] = A[128 x K] * B[NT x K]^T.
 //
 // Both operands come from global memory through 2-D tensor maps with 128-byte swizzle
 // (64 fp16 of K per row), four pipeline stages, one elected thread issuing
@@ -15,9 +16,9 @@
 //                       boxes past the end of U_k, which the copy fills with zeros),
 //                       B = k tokens of heads h and h+1 (adjacent columns),
 //                       D[64 i + k][t] -> K page [slot_t / 16][h + i][slot_t % 16][k]
-//   up-projection:      A = W_v[:, h*d:(h+1)*d]^T (MN-major), B = z_hi and z_lo (the
-//                       fp16 high / low parts of the merged weighted coefficient sums),
-//                       D[j][q] = o_{q,h,j}, written as fp16.
+//   decode query job:   a key job with the decode queries as B (same launch as the
+//                       append): D[64 i + k][q] = q~_{q,h+i,k}, stored fp32, scaled by
+//                       log2(e)/sqrt(d), for the split-K scoring.
 //   query projection:   as a key job with the chunk's queries as B: D[k][q] = q~_{q,h,k},
 //                       scaled by log2(e)/sqrt(d) and stored as an fp16 (hi, lo) pair
 //                       (zero past r_k, up to 64), the prefill score MMA's A operand.
@@ -38,14 +39,17 @@ namespace rcp {
 constexpr int kGemmThreads = 128;
 constexpr int kABytes = 128 * 64 * 2;   // one A stage: 128 rows x 64 K (or 64 K x 128 M)
 
-enum GemmMode : int { kModeAppend = 0, kModeUpproj = 1, kModeQproj = 2 };
+enum GemmMode : int { kModeAppend = 0, kModeQproj = 2 };
 
 template <int NT, int KS, int NB, int STG>
 struct GemmSmem {
   static constexpr int B_BYTES = NT * 128;                     // one B operand stage
   static constexpr int STAGE = kABytes + NB * B_BYTES;
-  static constexpr int RECV_OFF = STG * STAGE;                 // split-K receive buffer
-  static constexpr int RECV_BYTES = KS > 1 ? 128 * NT * 4 : 0;
+  // split-K receive buffer: KS partial slices of 128 / KS rows, rows RS floats apart (the
+  // padding spreads the rows of a column over the banks)
+  static constexpr int RS = NT + 4;
+  static constexpr int RECV_OFF = STG * STAGE;
+  static constexpr int RECV_BYTES = KS > 1 ? 128 * RS * 4 : 0;
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;        // full[S], empty[S], acc
   static constexpr int MISC_OFF = BAR_OFF + (2 * STG + 1) * 8;
   static constexpr int DST_OFF = MISC_OFF + 16;                // append: page offset per column
@@ -53,6 +57,7 @@ struct GemmSmem {
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
   static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(MISC_OFF % 8 == 0 && DST_OFF % 8 == 0 && (RS * 4) % 16 == 0, "alignment");
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -64,19 +69,19 @@ struct GemmParams {
   int32_t T;
   int32_t fp8;            // pages hold E4M3 codes (round to nearest even, saturate)
   int64_t num_blocks;
-  // up-projection
-  void* out;
-  int32_t nq;
+  int32_t nq;             // decode queries (decode query jobs), prefill rows
   uint32_t* dev_err;
-  // rank-space queries for chunked prefill: fp16 hi / lo [nq][H][64], scaled
+  // rank-space queries: chunked prefill fp16 hi / lo [nq][H][64]; decode fp32 [nq][H][r_k]
   void* qhi;
   void* qlo;
+  float* qt;
   float qscale;
 };
 
 // Where one CTA's job reads and writes.
 struct GemmJob {
-  int kind;        // 0 value (append), 1 key (append), 2 up-projection, -1 idle
+  int kind;        // 0 value (append), 1 key (append), 3 prefill query, 4 decode query,
+                   // -1 idle
   int a_x, a_y;    // tensor-map coordinates of A's first k-block (x innermost)
   int b_x, b_y;    // coordinates of B's first k-block
   int a_step_x, a_step_y, b_step_x;   // per-k-block coordinate steps
@@ -87,7 +92,7 @@ struct GemmJob {
 };
 
 template <class S, int MODE, int NT, int KS>
-__device__ __forceinline__ GemmJob gemm_job(uint32_t rank) {
+__device__ __forceinline__ GemmJob gemm_job(uint32_t rank, int T) {
   GemmJob j{};
   const int cluster = blockIdx.x / KS;
   if constexpr (MODE == kModeAppend) {
@@ -96,6 +101,22 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank) {
     constexpr int NKG = (NP + KS - 1) / KS;
     constexpr int KBV = S::H * S::D / 64;
     constexpr int KBK = S::D / 64;
+    // the append's clusters come first (value jobs, then key jobs, per token tile), then
+    // the decode query jobs (head pairs, per query tile)
+    const int app_clusters = (T + NT - 1) / NT * (NM + NKG);
+    if (cluster >= app_clusters) {
+      const int qc = cluster - app_clusters;
+      const int pr = (qc % NKG) * KS + static_cast<int>(rank);
+      j.kind = pr < NP ? 4 : -1;
+      j.m0 = 2 * pr;
+      j.n0 = (qc / NKG) * NT;
+      j.kb0 = 0;
+      j.kb1 = 2 * KBK;
+      j.a_x = 0; j.a_y = j.m0 * S::RK; j.a_step_x = 64; j.a_step_y = 0;
+      j.b_x = j.m0 * S::D; j.b_y = j.n0; j.b_step_x = 64;
+      j.reduce = false;
+      return j;
+    }
     const int tile = cluster / (NM + NKG);
     const int sub = cluster % (NM + NKG);
     j.n0 = tile * NT;
@@ -127,18 +148,6 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank) {
     j.a_x = 0; j.a_y = h * S::RK; j.a_step_x = 64; j.a_step_y = 0;
     j.b_x = h * S::D; j.b_y = j.n0; j.b_step_x = 64;
     j.reduce = false;
-  } else {
-    constexpr int KBR = S::R / 64;
-    const int h = cluster % S::H;
-    const int tile = cluster / S::H;
-    j.kind = 2;
-    j.m0 = h;
-    j.n0 = tile * NT;
-    j.kb0 = static_cast<int>(rank) * KBR / KS;
-    j.kb1 = (static_cast<int>(rank) + 1) * KBR / KS;
-    j.a_x = h * S::D; j.a_y = j.kb0 * 64; j.a_step_x = 0; j.a_step_y = 64;
-    j.b_x = h * S::R + j.kb0 * 64; j.b_y = j.n0; j.b_step_x = 64;
-    j.reduce = KS > 1;
   }
   return j;
 }
@@ -167,6 +176,13 @@ template <class S>
 __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j,
                                            const int64_t* dst, int row, int col, float v) {
   const int n = j.n0 + col;
+  if (j.kind == 4) {
+    // decode query: rows 0..63 are head m0's ranks, rows 64..127 head m0 + 1's
+    const int hh = row >> 6, rr = row & 63;
+    if (rr < S::RK && n < p.nq)
+      p.qt[(static_cast<size_t>(n) * S::H + j.m0 + hh) * S::RK + rr] = v * p.qscale;
+    return;
+  }
   if (j.kind == 3) {
     if (n >= p.nq || row >= 64) return;
     const size_t at = (static_cast<size_t>(n) * S::H + j.m0) * 64 + row;
@@ -174,12 +190,6 @@ __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j
     const __half hi = __float2half_rn(q);
     static_cast<__half*>(p.qhi)[at] = hi;
     static_cast<__half*>(p.qlo)[at] = __float2half_rn(q - __half2float(hi));
-    return;
-  }
-  if (j.kind == 2) {
-    if (row < S::D && n < p.nq)
-      static_cast<__half*>(p.out)[(static_cast<size_t>(n) * S::H + j.m0) * S::D + row] =
-          __float2half_rn(v);
     return;
   }
   const int64_t d = dst[col];
@@ -208,10 +218,9 @@ template <class S, int MODE, int NT, int KS, int STG>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a2,
                 const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_b2,
-                const GemmParams p) {
-  constexpr int NB = MODE == kModeUpproj ? 2 : 1;     // B operands per stage (z_hi, z_lo)
+                const __grid_constant__ CUtensorMap map_b3, const GemmParams p) {
   constexpr int kGemmStages = STG;
-  using L = GemmSmem<NT, KS, NB, STG>;
+  using L = GemmSmem<NT, KS, 1, STG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -224,11 +233,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = KS > 1 ? cluster_ctarank() : 0;
-  const GemmJob j = gemm_job<S, MODE, NT, KS>(rank);
-  // A key job uses the U_k map; every other job reads W_v through map_a.
-  // key and query jobs read U_k through map_a2 and their tokens through map_b2
-  const CUtensorMap* amap = (j.kind == 1 || j.kind == 3) ? &map_a2 : &map_a;
-  const CUtensorMap* bmap = (j.kind == 1 || j.kind == 3) ? &map_b2 : &map_b;
+  const GemmJob j = gemm_job<S, MODE, NT, KS>(rank, p.T);
+  // value jobs read W_v through map_a and their tokens through map_b;
+  // key and prefill query jobs read U_k through map_a2 and their tokens through map_b2;
+  // decode query jobs read U_k through map_a2 and the queries through map_b3
+  const bool uk = j.kind == 1 || j.kind == 3 || j.kind == 4;
+  const CUtensorMap* amap = uk ? &map_a2 : &map_a;
+  const CUtensorMap* bmap = j.kind == 4 ? &map_b3 : (uk ? &map_b2 : &map_b);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
@@ -252,11 +263,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nkb = j.kind >= 0 ? j.kb1 - j.kb0 : 0;
   auto load_a = [&](int kb, int s) {
     uint8_t* st = sm + s * L::STAGE;
-    if (MODE == kModeUpproj) {
-      // W_v^T slice: two 64(j) x 64(r) boxes (MN-major atoms), rows r = k
-      tma_load_2d(st, amap, j.a_x, j.a_y + kb * j.a_step_y, &full[s]);
-      tma_load_2d(st + kABytes / 2, amap, j.a_x + 64, j.a_y + kb * j.a_step_y, &full[s]);
-    } else if (MODE == kModeAppend && j.kind == 1) {
+    if (MODE == kModeAppend && (j.kind == 1 || j.kind == 4)) {
       // block-diagonal pair: k-blocks [0, d/64) meet head m0's rows (top), the rest head
       // m0 + 1's (bottom); the other half is a box past the last row of U_k (zeros)
       constexpr int KBK = S::D / 64, OOB = S::H * S::RK;
@@ -270,17 +277,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto load_b = [&](int kb, int s) {
     uint8_t* st = sm + s * L::STAGE;
     tma_load_2d(st + kABytes, bmap, j.b_x + kb * j.b_step_x, j.b_y, &full[s]);
-    if (NB == 2)
-      tma_load_2d(st + kABytes + L::B_BYTES, &map_b2, j.b_x + kb * j.b_step_x, j.b_y, &full[s]);
   };
   // A is always a factor (W_v or U_k), which no kernel writes: its first stages are
   // fetched before waiting on the previous kernel, whose outputs only B may read.
+  constexpr uint32_t kStageTx = kABytes + L::B_BYTES;
   const int pre = nkb < kGemmStages ? nkb : kGemmStages;
   if (warp == 0 && lane == 0 && nkb > 0) {
     prefetch_tmap(amap);
     prefetch_tmap(bmap);
     for (int kb = 0; kb < pre; ++kb) {
-      mbar_arrive_expect_tx(&full[kb], kABytes + NB * L::B_BYTES);
+      mbar_arrive_expect_tx(&full[kb], kStageTx);
       load_a(kb, kb);
     }
   }
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int s = kb % kGemmStages;
       if (kb >= pre) {
         if (!mbar_wait(&empty[s], ((kb / kGemmStages) - 1) & 1, abort_flag, p.dev_err)) break;
-        mbar_arrive_expect_tx(&full[s], kABytes + NB * L::B_BYTES);
+        mbar_arrive_expect_tx(&full[s], kStageTx);
         load_a(kb, s);
       }
       load_b(kb, s);
@@ -305,7 +311,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_wait_drain(&full[i % kGemmStages], (i / kGemmStages) & 1);
   } else if (warp == 1 && lane == 0 && nkb > 0) {
     // -------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = make_idesc_f16(128, NT, MODE == kModeUpproj, false);
+    constexpr uint32_t idesc = make_idesc_f16(128, NT, false, false);
     int kb = 0;
     for (; kb < nkb; ++kb) {
       const int s = kb % kGemmStages;
@@ -315,15 +321,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t b0 = a0 + kABytes;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {   // four K=16 steps per 64-wide k-block
-        const uint64_t ad = MODE == kModeUpproj
-                                ? make_sdesc(a0 + k * 2048, kABytes / 2, 1024, kSwizzle128B)
-                                : make_sdesc(a0 + k * 32, 16, 1024, kSwizzle128B);
+        const uint64_t ad = make_sdesc(a0 + k * 32, 16, 1024, kSwizzle128B);
         const uint64_t bd = make_sdesc(b0 + k * 32, 16, 1024, kSwizzle128B);
         umma_f16(tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-        if (NB == 2) {
-          const uint64_t bd2 = make_sdesc(b0 + L::B_BYTES + k * 32, 16, 1024, kSwizzle128B);
-          umma_f16(tmem, ad, bd2, idesc, 1u);
-        }
       }
       umma_commit(&empty[s]);
     }
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t recv_local = smem_u32(recv);
     const uint32_t dst_rank = static_cast<uint32_t>(row / RPC);
     const uint32_t dst = map_to_rank(recv_local, dst_rank) +
-                         ((rank * RPC + (row % RPC)) * NT) * 4;
+                         ((rank * RPC + (row % RPC)) * L::RS) * 4;
 #pragma unroll 1
     for (int c0 = 0; c0 < NT; c0 += 16) {
       float v[16];
@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int rr = i % RPC, col = i / RPC;
       float acc = 0.f;
 #pragma unroll
-      for (int s = 0; s < KS; ++s) acc += recv[(s * RPC + rr) * NT + col];
+      for (int s = 0; s < KS; ++s) acc += recv[(s * RPC + rr) * L::RS + col];
       gemm_store<S>(p, j, dst_s, static_cast<int>(rank) * RPC + rr, col, acc);
     }
   }
@@ -399,7 +399,7 @@ template <class K>
 static cudaError_t launch_cluster(K kernel, int grid, int cluster, int smem, cudaStream_t stream,
                                   bool pdl, const CUtensorMap& a, const CUtensorMap& a2,
                                   const CUtensorMap& b, const CUtensorMap& b2,
-                                  const GemmParams& p) {
+                                  const CUtensorMap& b3, const GemmParams& p) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kGemmThreads);
@@ -414,7 +414,7 @@ static cudaError_t launch_cluster(K kernel, int grid, int cluster, int smem, cud
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a, a2, b, b2, p);
+  return cudaLaunchKernelEx(&cfg, kernel, a, a2, b, b2, b3, p);
 }
 
 // Append: small token counts split K over an 8-CTA cluster (64-token tiles); large ones
@@ -422,6 +422,9 @@ static cudaError_t launch_cluster(K kernel, int grid, int cluster, int smem, cud
 template <class S>
 struct AppendCfg {
   static constexpr int KS_SMALL = (S::H * S::D / 64) < 8 ? (S::H * S::D / 64) : 8;
+  // pipeline stages by token tile: every k-block of a split-K value job (or of a key /
+  // query job) in flight at once where shared memory allows
+  static constexpr int STG16 = 8, STG64 = 6, STG256 = 4;
 };
 
 template <class S>
@@ -433,29 +436,33 @@ cudaError_t prepare_gemm() {
       r = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
     return r;
   };
-  constexpr int KSS = AppendCfg<S>::KS_SMALL;
-  if ((e = set(gemm_kernel<S, kModeAppend, 64, KSS, 4>, GemmSmem<64, KSS, 1, 4>::ALLOC)) !=
-      cudaSuccess)
+  using AC = AppendCfg<S>;
+  constexpr int KSS = AC::KS_SMALL;
+  if ((e = set(gemm_kernel<S, kModeAppend, 16, KSS, AC::STG16>,
+               GemmSmem<16, KSS, 1, AC::STG16>::ALLOC)) != cudaSuccess)
     return e;
-  if ((e = set(gemm_kernel<S, kModeAppend, 256, 1, 4>, GemmSmem<256, 1, 1, 4>::ALLOC)) !=
-      cudaSuccess)
+  if ((e = set(gemm_kernel<S, kModeAppend, 64, KSS, AC::STG64>,
+               GemmSmem<64, KSS, 1, AC::STG64>::ALLOC)) != cudaSuccess)
+    return e;
+  if ((e = set(gemm_kernel<S, kModeAppend, 256, 1, AC::STG256>,
+               GemmSmem<256, 1, 1, AC::STG256>::ALLOC)) != cudaSuccess)
     return e;
   if ((e = set(gemm_kernel<S, kModeQproj, 64, 1, 2>, GemmSmem<64, 1, 1, 2>::ALLOC)) != cudaSuccess)
     return e;
   if ((e = set(gemm_kernel<S, kModeQproj, 256, 1, 2>, GemmSmem<256, 1, 1, 2>::ALLOC)) != cudaSuccess)
     return e;
-  constexpr int KSU = UpprojCfg<S>::KS, STU = UpprojCfg<S>::STAGES;
-  if ((e = set(gemm_kernel<S, kModeUpproj, UpprojCfg<S>::NT, KSU, STU>,
-               GemmSmem<UpprojCfg<S>::NT, KSU, 2, STU>::ALLOC)) != cudaSuccess)
-    return e;
   return cudaSuccess;
 }
 
+// The append's projections and, when ap.nq > 0, the decode's rank-space queries, in one
+// launch (either part may be empty).  q_rows: tensor map over the queries [nq][H*d] with
+// the same box as the token maps (64 x 64 when max(T, nq) <= 256, else 64 x 256).
 template <class S>
 cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
                                const CUtensorMap& v_rows, const CUtensorMap& k_rows,
-                               const AppendParams& ap, cudaStream_t stream) {
-  if (ap.T == 0) return cudaSuccess;
+                               const CUtensorMap& q_rows, const AppendParams& ap,
+                               cudaStream_t stream) {
+  if (ap.T == 0 && ap.nq == 0) return cudaSuccess;
   GemmParams p{};
   p.slots = ap.slots;
   p.k_pages = ap.k_pages;
@@ -464,18 +471,31 @@ cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
   p.fp8 = ap.fp8_pages;
   p.num_blocks = ap.num_blocks;
   p.dev_err = ap.dev_err;
+  p.qt = ap.qt;
+  p.nq = ap.nq;
+  p.qscale = ap.qscale;
+  using AC = AppendCfg<S>;
   constexpr int NM = (S::R + 127) / 128;
-  if (ap.T <= 256) {
-    constexpr int KS = AppendCfg<S>::KS_SMALL;
-    constexpr int NKG = (S::H / 2 + KS - 1) / KS;
-    const int tiles = (ap.T + 63) / 64;
-    return launch_cluster(gemm_kernel<S, kModeAppend, 64, KS, 4>, tiles * (NM + NKG) * KS, KS,
-                          GemmSmem<64, KS, 1, 4>::ALLOC, stream, true, w_v, u_k, v_rows, k_rows, p);
+  constexpr int KS = AC::KS_SMALL;
+  constexpr int NKG = (S::H / 2 + KS - 1) / KS;
+  const int rows = ap.T > ap.nq ? ap.T : ap.nq;
+  if (rows <= 16) {   // a decode step of up to 16 requests: 16-row tiles
+    const int clusters = (ap.T + 15) / 16 * (NM + NKG) + (ap.nq + 15) / 16 * NKG;
+    return launch_cluster(gemm_kernel<S, kModeAppend, 16, KS, AC::STG16>, clusters * KS, KS,
+                          GemmSmem<16, KS, 1, AC::STG16>::ALLOC, stream, true, w_v, u_k, v_rows,
+                          k_rows, q_rows, p);
   }
-  // many tokens: 256-token tiles, no split
-  const int tiles = (ap.T + 255) / 256;
-  return launch_cluster(gemm_kernel<S, kModeAppend, 256, 1, 4>, tiles * (NM + S::H / 2), 1,
-                        GemmSmem<256, 1, 1, 4>::ALLOC, stream, true, w_v, u_k, v_rows, k_rows, p);
+  if (rows <= 256) {
+    const int clusters = (ap.T + 63) / 64 * (NM + NKG) + (ap.nq + 63) / 64 * NKG;
+    return launch_cluster(gemm_kernel<S, kModeAppend, 64, KS, AC::STG64>, clusters * KS, KS,
+                          GemmSmem<64, KS, 1, AC::STG64>::ALLOC, stream, true, w_v, u_k, v_rows,
+                          k_rows, q_rows, p);
+  }
+  // many tokens or queries: 256-row tiles, no split
+  const int clusters = (ap.T + 255) / 256 * (NM + S::H / 2) + (ap.nq + 255) / 256 * (S::H / 2);
+  return launch_cluster(gemm_kernel<S, kModeAppend, 256, 1, AC::STG256>, clusters, 1,
+                        GemmSmem<256, 1, 1, AC::STG256>::ALLOC, stream, true, w_v, u_k, v_rows,
+                        k_rows, q_rows, p);
 }
 
 template <class S>
@@ -491,46 +511,30 @@ cudaError_t launch_qproj_gemm(const CUtensorMap& u_k, const CUtensorMap& q_rows,
   if (nq <= 256) {
     const int tiles = (nq + 63) / 64;
     return launch_cluster(gemm_kernel<S, kModeQproj, 64, 1, 2>, tiles * S::H, 1,
-                          GemmSmem<64, 1, 1, 2>::ALLOC, stream, pdl, u_k, u_k, q_rows, q_rows, p);
+                          GemmSmem<64, 1, 1, 2>::ALLOC, stream, pdl, u_k, u_k, q_rows, q_rows,
+                          q_rows, p);
   }
   const int tiles = (nq + 255) / 256;
   return launch_cluster(gemm_kernel<S, kModeQproj, 256, 1, 2>, tiles * S::H, 1,
-                        GemmSmem<256, 1, 1, 2>::ALLOC, stream, pdl, u_k, u_k, q_rows, q_rows, p);
-}
-
-template <class S>
-cudaError_t launch_upproj_gemm(const CUtensorMap& w_v_mn, const CUtensorMap& z_hi,
-                               const CUtensorMap& z_lo, void* out, int nq, uint32_t* dev_err,
-                               cudaStream_t stream, bool pdl) {
-  GemmParams p{};
-  p.out = out;
-  p.nq = nq;
-  p.dev_err = dev_err;
-  constexpr int NT = UpprojCfg<S>::NT, KS = UpprojCfg<S>::KS, STG = UpprojCfg<S>::STAGES;
-  const int tiles = (nq + NT - 1) / NT;
-  return launch_cluster(gemm_kernel<S, kModeUpproj, NT, KS, STG>, tiles * S::H * KS, KS,
-                        GemmSmem<NT, KS, 2, STG>::ALLOC, stream, pdl, w_v_mn, w_v_mn, z_hi, z_lo, p);
+                        GemmSmem<256, 1, 1, 2>::ALLOC, stream, pdl, u_k, u_k, q_rows, q_rows,
+                        q_rows, p);
 }
 
 template cudaError_t prepare_gemm<ShapeMain>();
 template cudaError_t prepare_gemm<ShapeTiny>();
 template cudaError_t launch_append_gemm<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
                                                    const CUtensorMap&, const CUtensorMap&,
-                                                   const AppendParams&, cudaStream_t);
+                                                   const CUtensorMap&, const AppendParams&,
+                                                   cudaStream_t);
 template cudaError_t launch_append_gemm<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
                                                    const CUtensorMap&, const CUtensorMap&,
-                                                   const AppendParams&, cudaStream_t);
+                                                   const CUtensorMap&, const AppendParams&,
+                                                   cudaStream_t);
 template cudaError_t launch_qproj_gemm<ShapeMain>(const CUtensorMap&, const CUtensorMap&, void*,
                                                   void*, int, float, uint32_t*, cudaStream_t,
                                                   bool);
 template cudaError_t launch_qproj_gemm<ShapeTiny>(const CUtensorMap&, const CUtensorMap&, void*,
                                                   void*, int, float, uint32_t*, cudaStream_t,
                                                   bool);
-template cudaError_t launch_upproj_gemm<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
-                                                   const CUtensorMap&, void*, int, uint32_t*,
-                                                   cudaStream_t, bool);
-template cudaError_t launch_upproj_gemm<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
-                                                   const CUtensorMap&, void*, int, uint32_t*,
-                                                   cudaStream_t, bool);
 
 }  // namespace rcp

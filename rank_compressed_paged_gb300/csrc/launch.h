@@ -9,10 +9,12 @@ namespace rcp {
 
 template <class S>
 cudaError_t prepare_attn(int device);
+// The decode's split-K attention kernel (plans its own work from seq_lens; reads the
+// rank-space queries the launch before it wrote).
 template <class S>
 cudaError_t launch_attn(const CUtensorMap& tmap_v, const CUtensorMap& tmap_k, const AttnParams& p,
                         cudaStream_t stream, cudaEvent_t prof_start, cudaEvent_t prof_stop);
-// Plan + rank-space queries only (the prefill path's first kernel).
+// The prefill plan (the prefill path's first kernel).
 template <class S>
 cudaError_t launch_plan(const AttnParams& p, cudaStream_t stream, bool pdl);
 template <class S>
@@ -35,21 +37,28 @@ cudaError_t launch_widen(const AttnParams& p, void* k16, void* v16, int32_t* tab
                          int64_t max_pages, int num_sms, cudaStream_t stream, bool pdl);
 template <class S>
 cudaError_t prepare_gemm();
-// k_rows / v_rows: tensor maps over the new tokens' k and v ([T][H*d], box 64 x NT with
-// NT = 64 when T <= 256, else 256).
+// The append (k_rows / v_rows: tensor maps over the new tokens' k and v, [T][H*d]) and,
+// when p.nq > 0, the decode's rank-space queries (q_rows over [nq][H*d]) in one launch;
+// boxes 64 x NT with NT = 16 when max(T, nq) <= 16, 64 when it is <= 256, else 256.
 template <class S>
 cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
                                const CUtensorMap& v_rows, const CUtensorMap& k_rows,
-                               const AppendParams& p, cudaStream_t stream);
+                               const CUtensorMap& q_rows, const AppendParams& p,
+                               cudaStream_t stream);
 // Prefill rank-space queries on tensor cores (q_rows: [nq][H*d] fp16, boxes 64 x 64 when
 // nq <= 256, else 64 x 256).
 template <class S>
 cudaError_t launch_qproj_gemm(const CUtensorMap& u_k, const CUtensorMap& q_rows, void* qhi,
                               void* qlo, int nq, float qscale, uint32_t* dev_err,
                               cudaStream_t stream, bool pdl);
+// Split-K combine fused with the W_v up-projection (combine.cu).  rec_slices / rec_ml: fp32
+// tensor maps over the records [(nq + kMaxParts)][REC] with boxes of CombineCfg::CHUNK rows
+// by RANKS floats / of REC_ROWS rows by 4 floats.
 template <class S>
-cudaError_t launch_upproj_gemm(const CUtensorMap& w_v_mn, const CUtensorMap& z_hi,
-                               const CUtensorMap& z_lo, void* out, int nq, uint32_t* dev_err,
-                               cudaStream_t stream, bool pdl);
+cudaError_t prepare_combine();
+template <class S>
+cudaError_t launch_combine_upproj(const CUtensorMap& w_v_mn, const CUtensorMap& rec_slices,
+                                  const CUtensorMap& rec_ml, const CombineParams& p,
+                                  cudaStream_t stream, bool pdl);
 
 }  // namespace rcp

@@ -7,7 +7,8 @@
 namespace rcp {
 
 constexpr int kBlockSize = 16;   // tokens per page
-constexpr int kMaxParts = 256;   // upper bound on decode work partitions (CTAs)
+constexpr int kMaxParts = 152;   // decode work partitions (CTAs) at most: one per SM of a
+                                 // GB300; bounds the records the combine stages per tile
 
 constexpr int pow2_at_least(int x, int lo) {
   int p = lo;
@@ -28,21 +29,28 @@ struct Shape {
   static constexpr int KPAGE_BYTES = H * BS * RK * 2;   // one block of K coefficients
   static constexpr int VPAGE_BYTES = BS * R * 2;        // one block of V coefficients
   static constexpr int VSTAGE_BYTES = NCHUNK * 2 * 2048;  // smem A operand of NCHUNK MMAs
-  static constexpr int REC = R * HP + 2 * HP;           // floats in one partial record
+  // floats in one split-K partial record: the accumulator head-major [HP][R], then the
+  // running maximum m[HP] and sum l[HP]
+  static constexpr int REC = R * HP + 2 * HP;
   static_assert(NCHUNK * HP <= 512, "accumulator must fit in tensor memory");
 };
 
 using ShapeMain = Shape<32, 128, 64, 1024>;
 using ShapeTiny = Shape<4, 64, 16, 64>;
 
-// Up-projection GEMM: 64 query rows per tile; the value rank R is split over a cluster of
-// up to 8 CTAs (one 64-wide k-block at least per CTA).
+// Split-K combine + W_v up-projection (combine.cu): tiles of NT requests; the value rank R
+// is cut into KSPLIT slices of KB 64-wide k-blocks (RANKS ranks), one CTA per (tile, head,
+// slice).  The records a tile's requests own (at most REC_ROWS: NT requests over at most
+// kMaxParts partitions) stream through NBUF tensor copies of CHUNK records.
 template <class S>
-struct UpprojCfg {
+struct CombineCfg {
   static constexpr int NT = 64;
-  static constexpr int KS = (S::R / 64) < 8 ? (S::R / 64) : 8;
-  static constexpr int KB_PER_CTA = (S::R / 64) / KS;
-  static constexpr int STAGES = KB_PER_CTA < 4 ? KB_PER_CTA : 4;   // pipeline depth needed
+  static constexpr int KSPLIT = (S::R / 64) < 8 ? (S::R / 64) : 8;
+  static constexpr int KB = (S::R / 64) / KSPLIT;
+  static constexpr int RANKS = KB * 64;
+  static constexpr int REC_ROWS = NT + kMaxParts;
+  static constexpr int CHUNK = 32, NBUF = 2;
+  static_assert((S::R / 64) % KSPLIT == 0, "combine slices");
 };
 
 // Chunked prefill: 128 query rows x 128 keys per tile; the value rank is cut into slices
@@ -71,7 +79,7 @@ inline int64_t prefill_max_tiles(int64_t nq) { return (nq + 127) / 128 + nq; }
 
 // Workspace carve-up for nq query rows (all offsets 256-byte aligned).
 struct WsLayout {
-  size_t cum, qlen, qrow, qt, rec, zhi, zlo, tile_b, tile_qt, tcount, total;
+  size_t cum, qlen, qrow, qt, rec, upart, ucnt, tile_b, tile_qt, tcount, total;
 };
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 template <class S>
@@ -87,15 +95,20 @@ inline WsLayout ws_layout(int64_t nq) {
   w.tile_b = o;  o = align256(o + sizeof(int32_t) * prefill_max_tiles(nq));
   w.tile_qt = o; o = align256(o + sizeof(int32_t) * prefill_max_tiles(nq));
   w.tcount = o;  o = align256(o + sizeof(int32_t));
-  // decode only from here on
+  // decode only from here on: split-K partial records, one per (request, partition)
+  // segment, at index request + partition
   w.rec = o;  o = align256(o + sizeof(float) * (nq + kMaxParts) * static_cast<size_t>(S::REC));
-  w.zhi = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
-  w.zlo = o;  o = align256(o + 2 * nq * S::H * static_cast<size_t>(S::R));
+  // the combine's fp32 partial outputs [tile][head][slice][NT][128] and its counter per
+  // (tile, head)
+  const size_t tiles = static_cast<size_t>((nq + CombineCfg<S>::NT - 1) / CombineCfg<S>::NT);
+  w.upart = o;
+  o = align256(o + sizeof(float) * tiles * S::H * CombineCfg<S>::KSPLIT * CombineCfg<S>::NT * 128);
+  w.ucnt = o; o = align256(o + sizeof(int32_t) * tiles * S::H);
   w.total = o;
   return w;
 }
 
-// The reconstructing prefill never uses the decode-only regions at the end (rec, zhi, zlo):
+// The reconstructing prefill never uses the decode-only region at the end (rec):
 // its per-request block prefix sums and the reconstructed values V^ start where they
 // start, for at most batch x max_blocks_per_seq pages.
 struct ReconLayout {
@@ -134,13 +147,13 @@ struct AttnParams {
   void* out;                  // [nq][H][d] fp16
   uint32_t* dev_err;
   // workspace regions
-  int64_t* cum;               // [nq+1] prefix sums of blocks per query row
-  int32_t* qlen;              // [nq] keys attended by each query row
-  int32_t* qrow;              // [nq] block-table row of each query row
+  int64_t* cum;               // [nq+1] prefix sums of blocks per query row (decode: written
+                              // by partition 0 of the split-K kernel for the combine)
+  int32_t* qlen;              // [nq] keys attended by each query row (prefill plan)
+  int32_t* qrow;              // [nq] block-table row of each query row (prefill plan)
   float* qt;                  // [nq][H][r_k] rank-space queries, scaled by log2(e)/sqrt(d)
   float* rec;                 // [(nq + parts)][REC] split partials
-  void* zhi;                  // [nq][H][R] fp16 high part of the merged weighted sums z
-  void* zlo;                  // [nq][H][R] fp16 low part: z - fp16(z)
+  int32_t* ucnt;              // decode: [tiles][H] combine counters, zeroed by partition 0
   // prefill only (nullptr for decode)
   int32_t* tile_b;            // [max tiles] request of each 128-row query tile
   int32_t* tile_qt;           // [max tiles] tile index within its request
@@ -161,9 +174,24 @@ struct AttnParams {
   int32_t sparse;
   float skip_tau;
   uint8_t* page_kept;         // sparse, optional: [rows][bt_stride], 1 = page read, 0 = skipped
-  int32_t late_wait;          // planning kernel may run alongside its predecessor (an append
-                              // of the same step that it does not read) and waits at its end
+  // decode step: the slots the step's own append writes (the kernel before the split-K
+  // kernel); a partition waits for the append before it copies a page among them
+  const int64_t* slots;
+  int32_t n_slots;
   float qscale;               // log2(e) / sqrt(d)
+};
+
+// What the split-K combine + up-projection of a decode call sees (combine.cu).
+struct CombineParams {
+  const int64_t* cum;         // [nq+1] block prefix sums, written by the split-K kernel
+  const float* rec;           // [(nq + parts)][REC] partial records (head-major accumulator,
+                              // then m[HP], l[HP]), record id = request + partition
+  float* upart;               // [tiles][H][KSPLIT][NT][128] fp32 partial outputs
+  int32_t* ucnt;              // [tiles][H] arrivals, zero on entry
+  void* out;                  // [nq][H][d] fp16
+  uint32_t* dev_err;
+  int32_t nq;
+  int32_t parts;              // split-K partitions launched
 };
 
 struct AppendParams {
@@ -178,6 +206,10 @@ struct AppendParams {
   int64_t num_blocks;
   int32_t T;
   int32_t fp8_pages;          // store E4M3 codes instead of fp16
+  // decode: the rank-space queries are projected in the same launch (nq = 0: none)
+  float* qt;                  // [nq][H][r_k] fp32, q~ scaled by qscale
+  int32_t nq;
+  float qscale;
 };
 
 }  // namespace rcp

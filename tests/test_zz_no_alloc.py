@@ -57,17 +57,17 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
         assert_close(got, oref, what="noalloc vs oracle")
 
 
-def test_noalloc_limit_is_batch_123_at_the_main_shape():
-    """The header's limit for (H, d, r_k, R) = (32, 128, 64, 1024): batch 123 runs, batch
-    124 is refused without a launch."""
+def test_noalloc_limit_is_batch_157_at_the_main_shape():
+    """The header's limit for (H, d, r_k, R) = (32, 128, 64, 1024): batch 157 runs, batch
+    158 is refused without a launch."""
     import torch
     from rank_compressed_paged_gb300 import _lib
     inp = wl.make_decode_inputs(MAIN, [16], seed=5)
     c = inp.cache
     cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
-    assert cache.workspace_bytes(123) <= _lib.RCP_NOALLOC_SCRATCH_BYTES
-    assert cache.workspace_bytes(124) > _lib.RCP_NOALLOC_SCRATCH_BYTES
-    for big, want in ((123, _lib.RCP_OK), (124, _lib.RCP_ERR_WORKSPACE)):
+    assert cache.workspace_bytes(157) <= _lib.RCP_NOALLOC_SCRATCH_BYTES
+    assert cache.workspace_bytes(158) > _lib.RCP_NOALLOC_SCRATCH_BYTES
+    for big, want in ((157, _lib.RCP_OK), (158, _lib.RCP_ERR_WORKSPACE)):
         q = torch.zeros((big, 32, 128), dtype=torch.float16, device="cuda")
         lens = torch.zeros(big, dtype=torch.int32, device="cuda")        # empty sequences
         table = torch.zeros((big, 1), dtype=torch.int32, device="cuda")
