@@ -41,8 +41,9 @@ loop; the skippable set matches a hand-built score pattern; a sequential running
 pass drops a subset of it; the output change stays within the derived bound.  4-bit
 pages and rotation (tests/test_oracle_int4.py): grid values round-trip exactly, codes are
 the nearest grid points by enumeration, errors stay within half a step without saturation,
-a hand-packed byte fixes the nibble order, and a rotation folded into the factors leaves
-decode unchanged.
+a hand-packed byte fixes the nibble order, a hand-packed page (tests/golden/int4_page.json)
+fixes the page layout, every group an append writes is re-derived by enumeration, and a
+rotation folded into the factors leaves decode unchanged.
 """
 from __future__ import annotations
 
@@ -381,6 +382,82 @@ def int4_page_values(kc, ks, vc, vs, v_group: int = 64):
     kv = int4_decode(kc, ks[..., None], kc.shape[-1])
     vv = int4_decode(vc, vs, v_group)
     return kv, vv
+
+
+# The 4-bit page format (bytes per physical block; reading taken for the page layout, the
+# page gives none): a K page holds the codes of its [H][bs][r_k] coefficients packed two
+# per byte (pack_int4 along r_k), then the fp16 scales [H][bs] of its key rows; a V page
+# holds the codes of its [bs][R] coefficients packed along R, then the fp16 scales
+# [bs][R / 64] of its 64-coefficient groups.  Little-endian fp16.
+
+def int4_page_bytes(num_heads: int, rank_k: int, rank_v: int, block_size: int = 16):
+    """(bytes of a K page, bytes of a V page) in the 4-bit format."""
+    kb = num_heads * block_size * rank_k // 2 + num_heads * block_size * 2
+    vb = block_size * rank_v // 2 + block_size * (rank_v // 64) * 2
+    return kb, vb
+
+
+def int4_pack_pages(kc, ks, vc, vs):
+    """Byte pages [nb][K bytes], [nb][V bytes] from codes kc [nb][H][bs][r_k] (int8),
+    scales ks [nb][H][bs] (fp16), codes vc [nb][bs][R], scales vs [nb][bs][R / 64]."""
+    nb = np.asarray(kc).shape[0]
+    kb = np.concatenate([pack_int4(kc).reshape(nb, -1),
+                         np.ascontiguousarray(np.asarray(ks, np.float16)).reshape(nb, -1)
+                         .view(np.uint8)], axis=1)
+    vb = np.concatenate([pack_int4(vc).reshape(nb, -1),
+                         np.ascontiguousarray(np.asarray(vs, np.float16)).reshape(nb, -1)
+                         .view(np.uint8)], axis=1)
+    return kb, vb
+
+
+def int4_unpack_pages(k_bytes, v_bytes, num_heads: int, rank_k: int, rank_v: int,
+                      block_size: int = 16):
+    """Inverse of int4_pack_pages: (kc, ks, vc, vs)."""
+    kb = np.asarray(k_bytes, np.uint8)
+    vb = np.asarray(v_bytes, np.uint8)
+    nb = kb.shape[0]
+    nk = num_heads * block_size * rank_k // 2
+    nv = block_size * rank_v // 2
+    kc = unpack_int4(kb[:, :nk].reshape(nb, num_heads, block_size, rank_k // 2))
+    ks = np.ascontiguousarray(kb[:, nk:]).view(np.float16).reshape(nb, num_heads, block_size)
+    vc = unpack_int4(vb[:, :nv].reshape(nb, block_size, rank_v // 2))
+    vs = np.ascontiguousarray(vb[:, nv:]).view(np.float16).reshape(nb, block_size, rank_v // 64)
+    return kc, ks, vc, vs
+
+
+def int4_page_coefficients(k_bytes, v_bytes, num_heads: int, rank_k: int, rank_v: int,
+                           block_size: int = 16):
+    """The coefficient values (fp64) 4-bit byte pages hold, as K pages [nb][H][bs][r_k] and
+    V pages [nb][bs][R] for the decode and prefill definitions above."""
+    kc, ks, vc, vs = int4_unpack_pages(k_bytes, v_bytes, num_heads, rank_k, rank_v, block_size)
+    return int4_page_values(kc, ks, vc, vs, 64)
+
+
+def append_kv_int4(k_bytes, v_bytes, U_k, W_v, k, v, slot_mapping, block_size: int = 16):
+    """append_kv for 4-bit pages (returns copies): each new token's projections (fp64) are
+    quantized per group (int4_encode: a key row of r_k values, 64 value coefficients) and
+    written, codes and scales, at its slot; slot -1 writes nothing."""
+    U = _f64(U_k)
+    W = _f64(W_v)
+    k = _f64(k)
+    v = _f64(v)
+    T, H, d = k.shape
+    rk, R = U.shape[1], W.shape[0]
+    kc, ks, vc, vs = int4_unpack_pages(k_bytes, v_bytes, H, rk, R, block_size)
+    kc, ks, vc, vs = kc.copy(), ks.copy(), vc.copy(), vs.copy()
+    for i in range(T):
+        s = int(slot_mapping[i])
+        if s < 0:
+            continue
+        blk, off = s // block_size, s % block_size
+        for h in range(H):
+            c, sc = int4_encode(U[h] @ k[i, h], rk)
+            kc[blk, h, off] = c
+            ks[blk, h, off] = sc[0]
+        c, sc = int4_encode(W @ v[i].reshape(H * d), 64)
+        vc[blk, off] = c
+        vs[blk, off] = sc
+    return int4_pack_pages(kc, ks, vc, vs)
 
 
 def prefill_attn(q, cu_chunk_lens, k_pages, v_pages, U_k, W_v, block_table, seq_lens,
