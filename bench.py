@@ -407,6 +407,39 @@ def make_flush(dev):
     return lambda: buf.fill_(1)
 
 
+def int4_pages_torch(kp, vp):
+    """The seeded fp16 pages (device tensors [nb][H][16][r_k], [nb][16][R]) in the 4-bit
+    byte format: per group (a key row of one head, 64 value coefficients of a token) the
+    smallest fp16 scale with 7 * scale >= max |x| and codes x / scale rounded to nearest
+    (ties to even), two per byte (the even coefficient in the low nibble), then the
+    group scales.  Input preparation only, done once before timing."""
+    import torch
+
+    def enc(x, group):
+        n = x.shape[-1]
+        xf = x.float().reshape(*x.shape[:-1], n // group, group)
+        amax = xf.abs().amax(-1)
+        s = (amax / 7).half()
+        s = torch.where(s.float() * 7 < amax, (s.view(torch.int16) + 1).view(torch.float16), s)
+        sf = s.float().unsqueeze(-1)
+        c = torch.where(sf > 0, torch.round(xf / torch.where(sf > 0, sf, 1.0)),
+                        torch.zeros_like(xf)).clamp(-7, 7).to(torch.int16).reshape(x.shape)
+        packed = ((c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)).to(torch.uint8)
+        return packed, s
+
+    nb = kp.shape[0]
+    out = []
+    for x, group in ((kp, kp.shape[-1]), (vp, 64)):
+        parts = []
+        for b0 in range(0, nb, 4096):   # bounded temporaries
+            codes, scales = enc(x[b0:b0 + 4096], group)
+            parts.append(torch.cat([codes.reshape(codes.shape[0], -1),
+                                    scales.contiguous().view(torch.uint8)
+                                    .reshape(codes.shape[0], -1)], dim=1))
+        out.append(torch.cat(parts, dim=0))
+    return out[0], out[1]
+
+
 def build_decode(dev, w, pages="fp16"):
     """The library cache and device tensors of a decode workload from make_workload."""
     import torch
@@ -421,6 +454,10 @@ def build_decode(dev, w, pages="fp16"):
         # the same seeded coefficients stored as E4M3 codes (torch's float8 cast)
         kp_dev = kp_dev.to(torch.float8_e4m3fn).view(torch.uint8)
         vp_dev = vp_dev.to(torch.float8_e4m3fn).view(torch.uint8)
+        del w["kp"], w["vp"]
+        torch.cuda.empty_cache()
+    elif pages == "int4":
+        kp_dev, vp_dev = int4_pages_torch(kp_dev, vp_dev)
         del w["kp"], w["vp"]
         torch.cuda.empty_cache()
     cache = PagedCoeffCache(shape["num_heads"], shape["head_dim"], shape["rank_k"],
@@ -450,7 +487,7 @@ def measure_decode_config(dev, stream, steps, warmup, shape_name, batch, seq=Non
 
     for _ in range(max(warmup, 3)):
         step()
-    coeff = wl.algorithmic_bytes_decode(shape, w["seq_lens"], 1 if pages == "fp8_e4m3" else 2)
+    coeff = wl.algorithmic_bytes_decode(shape, w["seq_lens"], pages)
     step_bytes = coeff + wl.factor_bytes(shape)
     flush = make_flush(dev) if coeff < 2 * L2_BYTES else None
     step_ms, kern_ms = time_steps(step, steps, stream, flush=flush, cache=cache)
@@ -579,8 +616,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- block-sparse decode: which pages the timed configuration reads (deterministic)
     sparse = None
-    coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"],
-                                              1 if args.pages == "fp8_e4m3" else 2)
+    coeff_bytes = wl.algorithmic_bytes_decode(SHAPE, w["seq_lens"], args.pages)
     read_bytes = coeff_bytes
     kept_tok = None   # block-sparse decode: tokens of the pages it reads
     if args.sparse is not None:
@@ -655,7 +691,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 4),
         "us_per_step": round(step_ms * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16" if args.pages == "fp16" else "e4m3 pages, f16/f32 arithmetic",
+        "dtype": {"fp16": "f16", "fp8_e4m3": "e4m3 pages, f16/f32 arithmetic",
+                  "int4": "4-bit pages with f16 scales, f16/f32 arithmetic"}[args.pages],
         "data": "synthetic",
         "config": {"workload": workload_name(), "batch": BATCH,
                    "seq_len": SEQ if not RAGGED else f"uniform {RAGGED[0]}..{RAGGED[1]}",
@@ -703,7 +740,7 @@ LAUNCHES_PER_DECODE_STEP = 3
 
 def measure_configs(dev, stream, args):
     """Every other configuration of the workload list, each timed on its own (one GPU):
-    decode steps at the tiny shape, batch 16 x 1024, E4M3 pages at batch 64 x 8192,
+    decode steps at the tiny shape, batch 16 x 1024, E4M3 and 4-bit pages at batch 64 x 8192,
     batch 20 x 32768, 64 ragged sequences, and the chunked prefill in both variants."""
     steps = max(args.steps, 20)
     out = {}
@@ -713,6 +750,8 @@ def measure_configs(dev, stream, args):
                                                 seq=1024, seed=1001)
     out["C2_b64_l8192_append_e4m3"] = measure_decode_config(
         dev, stream, steps, args.warmup, "mha32", 64, seq=8192, seed=1002, pages="fp8_e4m3")
+    out["C2_b64_l8192_append_int4"] = measure_decode_config(
+        dev, stream, steps, args.warmup, "mha32", 64, seq=8192, seed=1002, pages="int4")
     out["C3_b20_l32768"] = measure_decode_config(dev, stream, steps, args.warmup, "mha32", 20,
                                                  seq=32768, seed=1003)
     out["C3_ragged64_l128_16384"] = measure_decode_config(
@@ -881,7 +920,7 @@ def main():
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode")
     ap.add_argument("--prefill-batch", type=int, default=16)
     ap.add_argument("--prefill-variant", choices=["auto", "rank", "reconstruct"], default="auto")
-    ap.add_argument("--pages", choices=["fp16", "fp8_e4m3"], default="fp16",
+    ap.add_argument("--pages", choices=["fp16", "fp8_e4m3", "int4"], default="fp16",
                     help="decode page format (fp16 is the measured configuration)")
     ap.add_argument("--prefill-prior", type=int, default=4096)
     ap.add_argument("--prefill-chunk", type=int, default=256)
@@ -894,6 +933,8 @@ def main():
     PEAKED = args.peaked
     if args.sparse is not None and args.pages != "fp16":
         ap.error("--sparse needs fp16 pages")
+    if args.workload == "prefill" and args.pages == "int4":
+        ap.error("the prefill reads fp16 or E4M3 pages")
     if args.ragged:
         RAGGED = tuple(int(x) for x in args.ragged.split(","))
     rank, world, local_rank = dist_env()

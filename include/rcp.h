@@ -11,8 +11,9 @@
  *
  * Memory layout (all device buffers are owned by the caller; the library never
  * allocates device memory; every pointer must be 16-byte aligned):
- *     K pages   [num_blocks][H][block_size][r_k]   fp16 (or E4M3 bytes, see page_format)
- *     V pages   [num_blocks][block_size][R]        fp16 (or E4M3 bytes)
+ *     K pages   [num_blocks][H][block_size][r_k]   fp16 (or E4M3 bytes; 4-bit pages: see
+ *                                                  RCP_PAGES_INT4)
+ *     V pages   [num_blocks][block_size][R]        fp16 (or E4M3 bytes; 4-bit pages)
  *     U_k       [H][r_k][d]                        fp16
  *     W_v       [R][H*d]   (column h*d + j = head h, element j)   fp16
  *     q, out    [rows][H][d]                       fp16
@@ -61,6 +62,25 @@ typedef enum rcp_status {
                                  +-448; half the bytes per token.  Append, decode and the
                                  reconstructing prefill; rcp_prefill_attn and the
                                  block-sparse decode return RCP_ERR_UNSUPPORTED. */
+#define RCP_PAGES_INT4 2      /* 4-bit codes with fp16 scales ("KV-cache LLM serving" page,
+                                 "What it measured", item 1: 4-bit KV pages for capacity;
+                                 a rotation before quantizing folds into U_k and W_v, so it
+                                 needs no call of its own).  One K page is
+                                 H*16*r_k/2 bytes of codes (key row (h, t) at byte
+                                 (h*16 + t)*r_k/2, two per byte, even index in the low
+                                 nibble, two's complement in [-7, 7]) then H*16 fp16 scales
+                                 (row (h, t) at index h*16 + t); one V page is 16*R/2 bytes
+                                 of codes (token t at byte t*R/2) then 16*(R/64) fp16 scales
+                                 (token t, group g of 64 coefficients at index t*(R/64)+g).
+                                 A coefficient is code * scale.  The append accumulates in
+                                 fp32 and per group (a key row; 64 value coefficients) takes
+                                 the smallest fp16 scale with 7*scale >= max|x| and
+                                 code = x/scale rounded to nearest, ties to even.  The
+                                 decode widens value coefficients to fp16(code * scale)
+                                 (one rounding) and scores keys as scale * (codes . q~) in
+                                 fp32.  1,632 bytes per token at (32, 128, 64, 1024).
+                                 Append and decode only; the prefill calls and the
+                                 block-sparse decode return RCP_ERR_UNSUPPORTED. */
 
 typedef struct rcp_cache_config {
   int32_t num_heads;   /* H */
@@ -69,7 +89,7 @@ typedef struct rcp_cache_config {
   int32_t rank_v;      /* R, joint value coefficients per token */
   int32_t block_size;  /* tokens per page; this build supports 16 */
   int64_t num_blocks;  /* physical blocks in the K and V page buffers */
-  int32_t page_format; /* RCP_PAGES_FP16 or RCP_PAGES_FP8_E4M3 */
+  int32_t page_format; /* RCP_PAGES_FP16, RCP_PAGES_FP8_E4M3 or RCP_PAGES_INT4 */
 } rcp_cache_config;
 
 typedef struct rcp_cache rcp_cache;   /* opaque handle: borrowed pointers + host free list */

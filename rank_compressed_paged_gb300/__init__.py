@@ -99,6 +99,14 @@ def _stream(stream=None) -> int:
     return s.cuda_stream
 
 
+def int4_page_bytes(num_heads: int, rank_k: int, rank_v: int):
+    """Bytes of one 4-bit K page and one V page: the codes (two per byte), then the fp16
+    scales (one per key row of a head, one per 64 value coefficients of a token)."""
+    k = num_heads * BLOCK_SIZE * rank_k // 2 + num_heads * BLOCK_SIZE * 2
+    v = BLOCK_SIZE * rank_v // 2 + BLOCK_SIZE * (rank_v // 64) * 2
+    return k, v
+
+
 class PagedCoeffCache:
     """Paged low-rank coefficient cache on one GPU.
 
@@ -106,7 +114,9 @@ class PagedCoeffCache:
     [num_blocks][16][R], the factors, a device error word and a reusable workspace; the
     library handle borrows their pointers.  page_format "fp16" stores fp16 coefficients,
     "fp8_e4m3" stores E4M3 codes (uint8 tensors; prefill on them takes the reconstructing
-    variant, which first widens the pages it reads to fp16 in the workspace).
+    variant, which first widens the pages it reads to fp16 in the workspace), "int4" stores
+    4-bit codes with fp16 scales as raw bytes (K pages [num_blocks][int4_page_bytes()[0]],
+    V pages [num_blocks][int4_page_bytes()[1]], uint8; append and decode only).
     """
 
     def __init__(self, num_heads: int, head_dim: int, rank_k: int, rank_v: int,
@@ -119,7 +129,8 @@ class PagedCoeffCache:
             raise ValueError(f"the cache lives on a CUDA device, got {dev}")
         if dev.index is None:
             dev = torch.device("cuda", torch.cuda.current_device())
-        formats = {"fp16": _lib.RCP_PAGES_FP16, "fp8_e4m3": _lib.RCP_PAGES_FP8_E4M3}
+        formats = {"fp16": _lib.RCP_PAGES_FP16, "fp8_e4m3": _lib.RCP_PAGES_FP8_E4M3,
+                   "int4": _lib.RCP_PAGES_INT4}
         if page_format not in formats:
             raise ValueError(f"unknown page_format {page_format!r}")
         fmt = formats[page_format]
@@ -132,14 +143,18 @@ class PagedCoeffCache:
         _need("W_v", W_v, torch.float16, (rank_v, num_heads * head_dim), dev)
         self.U_k = U_k
         self.W_v = W_v
+        if fmt == _lib.RCP_PAGES_INT4:
+            kb, vb = int4_page_bytes(num_heads, rank_k, rank_v)
+            k_shape, v_shape = (num_blocks, kb), (num_blocks, vb)
+        else:
+            k_shape = (num_blocks, num_heads, BLOCK_SIZE, rank_k)
+            v_shape = (num_blocks, BLOCK_SIZE, rank_v)
         if k_pages is None:
-            k_pages = torch.zeros((num_blocks, num_heads, BLOCK_SIZE, rank_k),
-                                  dtype=page_dtype, device=dev)
+            k_pages = torch.zeros(k_shape, dtype=page_dtype, device=dev)
         if v_pages is None:
-            v_pages = torch.zeros((num_blocks, BLOCK_SIZE, rank_v), dtype=page_dtype,
-                                  device=dev)
-        _need("k_pages", k_pages, page_dtype, (num_blocks, num_heads, BLOCK_SIZE, rank_k), dev)
-        _need("v_pages", v_pages, page_dtype, (num_blocks, BLOCK_SIZE, rank_v), dev)
+            v_pages = torch.zeros(v_shape, dtype=page_dtype, device=dev)
+        _need("k_pages", k_pages, page_dtype, k_shape, dev)
+        _need("v_pages", v_pages, page_dtype, v_shape, dev)
         self.k_pages = k_pages
         self.v_pages = v_pages
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=dev)

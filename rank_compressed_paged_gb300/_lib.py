@@ -62,6 +62,7 @@ _SIG = {
 RCP_NOALLOC_SCRATCH_BYTES = 64 << 20
 RCP_PAGES_FP16 = 0
 RCP_PAGES_FP8_E4M3 = 1
+RCP_PAGES_INT4 = 2
 
 _lib = None
 

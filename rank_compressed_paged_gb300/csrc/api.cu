@@ -258,7 +258,7 @@ rcp_status launch_front(rcp_cache* c, const AppendArgs* app, const void* q, int3
   p.dev_err = c->dev_err;
   p.num_blocks = c->cfg.num_blocks;
   p.T = T;
-  p.fp8_pages = c->cfg.page_format == RCP_PAGES_FP8_E4M3 ? 1 : 0;
+  p.page_format = c->cfg.page_format;
   p.qt = qt;
   p.nq = nq;
   p.qscale = qscale;
@@ -316,7 +316,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   p.W_v = c->W_v;
   p.k_pages = c->k_pages;
   p.v_pages = c->v_pages;
-  p.fp8_pages = c->cfg.page_format == RCP_PAGES_FP8_E4M3 ? 1 : 0;
+  p.page_format = c->cfg.page_format;
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   p.cu_chunk = cu_chunk;
@@ -345,7 +345,9 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   const bool pdl = c->prof_start == nullptr;
   // the prefill kernels read fp16 pages; E4M3 pages are widened first (reconstructing
   // variant only: its workspace is sized by the pages the batch can reach)
-  if (cu_chunk && p.fp8_pages && !recon) return RCP_ERR_UNSUPPORTED;
+  if (cu_chunk && p.page_format != RCP_PAGES_FP16 && !recon) return RCP_ERR_UNSUPPORTED;
+  // the reconstructing prefill widens E4M3 pages; 4-bit pages have no prefill
+  if (cu_chunk && p.page_format == RCP_PAGES_INT4) return RCP_ERR_UNSUPPORTED;
   if (cu_chunk) {
     // chunked prefill: plan + fp16 rank-space queries, then the tiled tensor-core kernel
     const uint64_t hq = static_cast<uint64_t>(c->cfg.num_heads) * 64;
@@ -362,7 +364,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
       return RCP_ERR_CUDA;
     // reconstructing variant: V^ rows for at most batch x max_blocks_per_seq pages
     const int64_t max_pages = static_cast<int64_t>(batch) * max_blocks_per_seq;
-    const bool widen = recon && p.fp8_pages;
+    const bool widen = recon && p.page_format == RCP_PAGES_FP8_E4M3;
     CUtensorMap vhat_map = c->tmap_v, kp16_map = c->tmap_kp, vp16_map = c->tmap_v;
     Widened wd{nullptr, nullptr, nullptr};
     rcp::AttnParams pw = p;   // the widening pass reads the cache's own pages and table
@@ -386,7 +388,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
         p.v_pages = wd.v16;
         p.block_table = wd.table16;
         p.num_blocks = max_pages;
-        p.fp8_pages = 0;
+        p.page_format = RCP_PAGES_FP16;
       }
     }
     const CUtensorMap& vals = recon ? vhat_map : c->tmap_v;
@@ -480,7 +482,8 @@ const char* rcp_status_string(rcp_status s) {
 
 rcp_status rcp_config_supported(const rcp_cache_config* cfg) {
   if (!cfg) return RCP_ERR_INVALID_ARG;
-  if (cfg->page_format != RCP_PAGES_FP16 && cfg->page_format != RCP_PAGES_FP8_E4M3)
+  if (cfg->page_format != RCP_PAGES_FP16 && cfg->page_format != RCP_PAGES_FP8_E4M3 &&
+      cfg->page_format != RCP_PAGES_INT4)
     return RCP_ERR_UNSUPPORTED;
   return shape_of(cfg) == kShapeNone ? RCP_ERR_UNSUPPORTED : RCP_OK;
 }

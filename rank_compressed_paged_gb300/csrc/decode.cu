@@ -180,23 +180,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const AttnParams p) 
 constexpr int kAppendSetBits = 9;
 constexpr int kAppendSetSize = 1 << kAppendSetBits;   // a step appending more tokens than
                                                       // half this waits before any copy
-// F8: pages hold E4M3 codes.  K pages are scored straight from their bytes; V pages land
-// in raw stages and the compute warps widen them to fp16 in the swizzled layout the
+// FMT: the page format (RCP_PAGES_*).  Quantized pages (F8: E4M3 codes, or 4-bit codes
+// with fp16 scales) arrive whole by bulk copies; K pages are scored straight from their
+// bytes, V pages land in raw stages and are widened to fp16 in the swizzled layout the
 // tensor-core MMA reads (the layout the fp16 path's tensor-map copies produce).
-template <class S, bool F8, bool SKIP = false>
+template <class S, int FMT, bool SKIP = false>
 struct DecodeSmem {
+  static constexpr bool F8 = FMT != RCP_PAGES_FP16;                 // raw quantized pages
   static constexpr int DS = 4;                                      // SKIP: decision ring
   static constexpr int KST = F8 ? 3 : 2;                            // key page stages
   static constexpr int VST = 2;                                     // fp16 V stages (MMA A)
   static constexpr int VRS = F8 ? 3 : VST;                          // stages V copies land in
-  static constexpr int KP = F8 ? S::KPAGE_BYTES / 2 : S::KPAGE_BYTES;   // bytes per K page
-  static constexpr int VP = F8 ? S::VPAGE_BYTES / 2 : S::VPAGE_BYTES;   // bytes per V page
+  static constexpr int KP = FMT == RCP_PAGES_FP8_E4M3 ? S::KPAGE_BYTES / 2   // bytes per K page
+                           : FMT == RCP_PAGES_INT4 ? static_cast<int>(Int4Page<S>::KBYTES)
+                                                   : S::KPAGE_BYTES;
+  static constexpr int VP = FMT == RCP_PAGES_FP8_E4M3 ? S::VPAGE_BYTES / 2   // bytes per V page
+                           : FMT == RCP_PAGES_INT4 ? static_cast<int>(Int4Page<S>::VBYTES)
+                                                   : S::VPAGE_BYTES;
+  static constexpr int KPS = (KP + 127) & ~127;                     // stage strides
+  static constexpr int VPS = (VP + 127) & ~127;
   static constexpr int NBAR = 2 * KST + 2 * VRS + 4 + (F8 ? 2 * VST : 0) + (SKIP ? 2 * DS : 0);
   static constexpr int P_BYTES = S::HP * 16 * 2;
   static constexpr int V_OFF = 0;                                   // 1024-aligned stages
   static constexpr int K_OFF = V_OFF + VST * S::VSTAGE_BYTES;
-  static constexpr int VR_OFF = K_OFF + KST * KP;                   // raw E4M3 V stages
-  static constexpr int P_OFF = VR_OFF + (F8 ? VRS * VP : 0);
+  static constexpr int VR_OFF = K_OFF + KST * KPS;                  // raw E4M3 V stages
+  static constexpr int P_OFF = VR_OFF + (F8 ? VRS * VPS : 0);
   static constexpr int Q_OFF = P_OFF + 2 * P_BYTES;
   static constexpr int A_OFF = Q_OFF + S::H * S::RK * 4;            // alpha[2][HP]
   static constexpr int F_OFF = A_OFF + 2 * S::HP * 4;               // flags[2][4]
@@ -215,7 +223,7 @@ struct DecodeSmem {
                     BAR_OFF % 8 == 0,
                 "region alignment");
   static constexpr int ALLOC = TOTAL + 1024;                        // base alignment slack
-  static_assert(KP % 128 == 0 && VP % 16 == 0 && S::VSTAGE_BYTES % 1024 == 0, "alignment");
+  static_assert(KP % 16 == 0 && VP % 16 == 0 && S::VSTAGE_BYTES % 1024 == 0, "alignment");
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -224,11 +232,12 @@ struct DecodeSmem {
 // which widen the E4M3 V pages while the compute warps score.
 // SKIP: warp 0 copies keys only and warp 6 copies the value pages the compute warps keep.
 // (Eight compute warps measured slower there: more registers spilled and barrier traffic.)
-template <class S, bool F8, bool SKIP = false>
-constexpr int decode_compute_warps() { return (F8 && S::H % 8 == 0) ? 8 : 4; }
-template <class S, bool F8, bool SKIP = false>
+template <class S, int FMT, bool SKIP = false>
+constexpr int decode_compute_warps() { return (FMT != RCP_PAGES_FP16 && S::H % 8 == 0) ? 8 : 4; }
+template <class S, int FMT, bool SKIP = false>
 constexpr int decode_threads() {
-  return 32 * (2 + decode_compute_warps<S, F8, SKIP>() + (F8 ? 2 : 0) + (SKIP ? 1 : 0));
+  return 32 * (2 + decode_compute_warps<S, FMT, SKIP>() + (FMT != RCP_PAGES_FP16 ? 2 : 0) +
+               (SKIP ? 1 : 0));
 }
 
 // Two E4M3 codes (low byte first) to an fp16 pair / fp32 pair; E4M3 values are exact in
@@ -244,12 +253,24 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
   return __half22float2(__half2(r));
 }
 
-// Widens boxes [b0, b1) (64 columns each) of an E4M3 V page ([16][R] codes at src) into the
-// fp16 stage vb in the layout of the value MMA: box g at g * 2048, token row t at t * 128,
-// 16-byte chunk c at chunk c ^ (t % 8).  Tokens at or past nvalid (the sequence end, or a
-// rejected block) get zero rows, so whatever those slots hold cannot reach the accumulator
-// through 0 * NaN.  NT threads, this one is tid.
-template <class S, int NT>
+// Two 4-bit codes (one byte: the even coefficient in the low nibble, two's complement) times
+// their group's scale, as an fp16 pair.  Each nibble n becomes the fp16 1024 + (n ^ 8)
+// (exponent bits 0x6400 with n ^ 8 as the low mantissa bits), minus 1032 the signed code,
+// exactly; the product with the scale rounds once.
+__device__ __forceinline__ uint32_t int4x2_to_half2_bits(uint32_t byte, __half2 scale) {
+  const uint32_t b = ((byte & 0xFu) | ((byte & 0xF0u) << 12)) ^ 0x64086408u;
+  const __half2 code = __hsub2(*reinterpret_cast<const __half2*>(&b), __float2half2_rn(1032.f));
+  const __half2 v = __hmul2(code, scale);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Widens boxes [b0, b1) (64 columns each) of a quantized V page (E4M3: [16][R] codes at src;
+// 4-bit: [16][R/2] code bytes then the fp16 scales [16][R/64]) into the fp16 stage vb in
+// the layout of the value MMA: box g at g * 2048, token row t at t * 128, 16-byte chunk c
+// at chunk c ^ (t % 8).  Tokens at or past nvalid (the sequence end, or a rejected block)
+// get zero rows, so whatever those slots hold cannot reach the accumulator through 0 * NaN.
+// NT threads, this one is tid.
+template <class S, int FMT, int NT>
 __device__ __forceinline__ void widen_v_boxes(const uint8_t* src, uint8_t* vb, int nvalid, int b0,
                                               int b1, int tid) {
   const int n = (b1 - b0) * kBlockSize * 8;
@@ -258,11 +279,22 @@ __device__ __forceinline__ void widen_v_boxes(const uint8_t* src, uint8_t* vb, i
     const int c = idx & 7, tt = (idx >> 3) % kBlockSize, gb = b0 + (idx >> 3) / kBlockSize;
     uint4 o = make_uint4(0, 0, 0, 0);
     if (tt < nvalid) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(src + tt * S::R + gb * 64 + c * 8);
-      o.x = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x & 0xFFFFu));
-      o.y = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x >> 16));
-      o.z = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y & 0xFFFFu));
-      o.w = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y >> 16));
+      if constexpr (FMT == RCP_PAGES_INT4) {
+        // box gb is exactly scale group gb: 8 codes (4 bytes) per 16-byte output chunk
+        const uint32_t raw = *reinterpret_cast<const uint32_t*>(src + tt * (S::R / 2) + gb * 32 + c * 4);
+        const __half2 sc = __half2half2(reinterpret_cast<const __half*>(
+            src + Int4Page<S>::VCODES)[tt * (S::R / 64) + gb]);
+        o.x = int4x2_to_half2_bits(raw & 0xFFu, sc);
+        o.y = int4x2_to_half2_bits((raw >> 8) & 0xFFu, sc);
+        o.z = int4x2_to_half2_bits((raw >> 16) & 0xFFu, sc);
+        o.w = int4x2_to_half2_bits(raw >> 24, sc);
+      } else {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src + tt * S::R + gb * 64 + c * 8);
+        o.x = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x & 0xFFFFu));
+        o.y = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x >> 16));
+        o.z = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y & 0xFFFFu));
+        o.w = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y >> 16));
+      }
     }
     *reinterpret_cast<uint4*>(vb + gb * 2048 + tt * 128 + ((c ^ (tt & 7)) << 4)) = o;
   }
@@ -314,16 +346,17 @@ struct BlockInfo {
 };
 
 
-template <class S, bool F8, bool SKIP>
-__global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
+template <class S, int FMT, bool SKIP>
+__global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     decode_main_kernel(const __grid_constant__ CUtensorMap tmap_v,
                        const __grid_constant__ CUtensorMap tmap_k, const AttnParams p) {
+  constexpr bool F8 = FMT != RCP_PAGES_FP16;   // quantized pages (E4M3 or 4-bit)
   static_assert(!(F8 && SKIP), "block-sparse decode reads fp16 pages");
   // fp16 key pages with 128-byte rows (r_k = 64) arrive 128-byte swizzled (two TMA boxes of
   // 256 rows): chunk c of row r sits at chunk c ^ (r % 8), so the 16 lanes scoring one
   // head read the same logical chunk, conflict-free on the keys and as a broadcast on q~
   constexpr bool KSWZ = !F8 && S::RK == 64;
-  using L = DecodeSmem<S, F8, SKIP>;
+  using L = DecodeSmem<S, FMT, SKIP>;
   constexpr int KST = L::KST, VST = L::VST, VRS = L::VRS, HP = S::HP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -346,8 +379,8 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
   uint64_t* vfree = vcvt + VST;           // F8 [VST] fp16 V stage read by its MMAs
   uint64_t* decfull = pfree + 2 + (F8 ? 2 * VST : 0);   // SKIP [DS] a decision was posted
   uint64_t* decempty = decfull + L::DS;                  // SKIP [DS] ... and taken
-  constexpr int NTHR = decode_threads<S, F8, SKIP>();
-  constexpr int NCW = decode_compute_warps<S, F8, SKIP>();   // compute warps 2 .. NCW+1
+  constexpr int NTHR = decode_threads<S, FMT, SKIP>();
+  constexpr int NCW = decode_compute_warps<S, FMT, SKIP>();   // compute warps 2 .. NCW+1
   // F8: V boxes widened by warps 10-11; the compute warps widen the remaining ones (a
   // split measured to balance the two groups' time per block)
   constexpr int WB = S::NBOX >= 16 ? 10 : S::NBOX;
@@ -566,10 +599,10 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
           constexpr int ROWS = S::H * kBlockSize;   // key rows of a page
 #pragma unroll
           for (int half = 0; half < ROWS / 256; ++half)
-            tma_load_2d_hint(kst + ks * L::KP + half * 256 * 128, &tmap_k, 0,
+            tma_load_2d_hint(kst + ks * L::KPS + half * 256 * 128, &tmap_k, 0,
                              static_cast<int32_t>(phys * ROWS + half * 256), &kfull[ks], pol);
         } else {
-          bulk_g2s_hint(kst + ks * L::KP, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
+          bulk_g2s_hint(kst + ks * L::KPS, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
         }
         ++nk;
         if constexpr (SKIP) continue;   // values wait until the page is known to be needed
@@ -579,7 +612,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
         mbar_arrive_expect_tx(&vfull[vs], L::VP);
         if constexpr (F8) {
           // the page's [16][R] codes, contiguous
-          bulk_g2s_hint(vraw + vs * L::VP, static_cast<const uint8_t*>(p.v_pages) + phys * L::VP,
+          bulk_g2s_hint(vraw + vs * L::VPS, static_cast<const uint8_t*>(p.v_pages) + phys * L::VP,
                         L::VP, &vfull[vs], pol);
         } else {
 #pragma unroll 1
@@ -677,7 +710,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
       bool ok = mbar_wait(&vfull[vr], (it / VRS) & 1, abort_flag, p.dev_err);
       if (it >= VST) ok = mbar_wait(&vfree[vs], ((it / VST) - 1) & 1, abort_flag, p.dev_err) && ok;
       if (!__all_sync(0xffffffffu, ok)) break;
-      widen_v_boxes<S, 64>(vraw + vr * L::VP, vst + vs * S::VSTAGE_BYTES, vinfo[vr], 0, WB, vt);
+      widen_v_boxes<S, FMT, 64>(vraw + vr * L::VPS, vst + vs * S::VSTAGE_BYTES, vinfo[vr], 0, WB, vt);
       fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
       __syncwarp();
       if (lane == 0) {
@@ -749,10 +782,42 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
         s[r] = -INFINITY;
         if (ok && head_ok(r)) {
           const int h = head_of(r);
-          const uint8_t* kstage = kst + ks * L::KP;   // this page's key stage
+          const uint8_t* kstage = kst + ks * L::KPS;   // this page's key stage
           // two packed fp32x2 accumulators = four independent chains
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-          if constexpr (F8) {
+          float kscale = 1.f;   // 4-bit pages: the key row's scale, applied to the dot product
+          if constexpr (FMT == RCP_PAGES_INT4) {
+            // r_k/2 bytes per key row: 8-byte chunks of 16 codes, rotated over the 16 lanes
+            // so their rows' chunks spread over the banks; each 32-bit word holds codes
+            // 8c .. 8c+7 (code 8c+i in nibble i).  A nibble n becomes the fp32 2^23 + (n ^ 8)
+            // (exponent bits 0x4B000000), minus 2^23 + 8 the signed code, exactly.
+            constexpr int RB = S::RK / 2, NU = RB / 8;
+            const uint8_t* krow = kstage + (h * kBlockSize + t) * RB;
+            kscale = __half2float(
+                reinterpret_cast<const __half*>(kstage + Int4Page<S>::KCODES)[h * kBlockSize + t]);
+            const float2 bias = make_float2(-8388616.f, -8388616.f);
+#pragma unroll
+            for (int v = 0; v < NU; ++v) {
+              const int u = (v + t) % NU;
+              const uint2 kv = *reinterpret_cast<const uint2*>(krow + u * 8);
+              const uint32_t w2[2] = {kv.x, kv.y};
+#pragma unroll
+              for (int hw = 0; hw < 2; ++hw) {
+                const int c = 2 * u + hw;
+                const float4 qa = qs4[(h * 2 + 0) * NCH + c];
+                const float4 qb = qs4[(h * 2 + 1) * NCH + c];
+                const uint32_t w = w2[hw];
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  f[i] = __uint_as_float(((w >> (4 * i)) & 0xFu) ^ 0x4B000008u);
+                acc0 = fma_f32x2(add_f32x2(make_float2(f[0], f[1]), bias), make_float2(qa.x, qa.y), acc0);
+                acc1 = fma_f32x2(add_f32x2(make_float2(f[2], f[3]), bias), make_float2(qa.z, qa.w), acc1);
+                acc0 = fma_f32x2(add_f32x2(make_float2(f[4], f[5]), bias), make_float2(qb.x, qb.y), acc0);
+                acc1 = fma_f32x2(add_f32x2(make_float2(f[6], f[7]), bias), make_float2(qb.z, qb.w), acc1);
+              }
+            }
+          } else if constexpr (F8) {
             // 16 E4M3 codes per 16-byte chunk; lanes 2u and 2u+1 start at chunk u so the
             // 16 tokens' 64-byte rows spread over all banks
             constexpr int NCH8 = S::RK / 16;
@@ -798,6 +863,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
             }
           }
           s[r] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+          if constexpr (FMT == RCP_PAGES_INT4) s[r] *= kscale;
         }
       }
       __syncwarp();
@@ -949,7 +1015,7 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
         // MMA that read it two blocks ago)
         const int vr = static_cast<int>(it % VRS);
         ok = mbar_wait(&vfull[vr], (it / VRS) & 1, abort_flag, p.dev_err) && ok;
-        widen_v_boxes<S, CT>(vraw + vr * L::VP, vst + static_cast<int>(it % VST) * S::VSTAGE_BYTES,
+        widen_v_boxes<S, FMT, CT>(vraw + vr * L::VPS, vst + static_cast<int>(it % VST) * S::VSTAGE_BYTES,
                              bi.nvalid, WB, S::NBOX, ctid);
         __syncwarp();
         if (lane == 0) mbar_arrive(&vempty[vr]);
@@ -1049,17 +1115,18 @@ __global__ void __launch_bounds__(decode_threads<S, F8, SKIP>(), 1)
 template <class S>
 cudaError_t prepare_attn(int device) {
   (void)device;
-  cudaError_t e = cudaFuncSetAttribute(decode_main_kernel<S, false, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DecodeSmem<S, false>::ALLOC);
+  auto set = [](auto kernel, int smem) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  };
+  cudaError_t e = set(decode_main_kernel<S, RCP_PAGES_FP16, false>, DecodeSmem<S, RCP_PAGES_FP16>::ALLOC);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_main_kernel<S, true, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecodeSmem<S, true>::ALLOC);
+    e = set(decode_main_kernel<S, RCP_PAGES_FP8_E4M3, false>,
+            DecodeSmem<S, RCP_PAGES_FP8_E4M3>::ALLOC);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_main_kernel<S, false, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecodeSmem<S, false, true>::ALLOC);
+    e = set(decode_main_kernel<S, RCP_PAGES_INT4, false>, DecodeSmem<S, RCP_PAGES_INT4>::ALLOC);
+  if (e == cudaSuccess)
+    e = set(decode_main_kernel<S, RCP_PAGES_FP16, true>,
+            DecodeSmem<S, RCP_PAGES_FP16, true>::ALLOC);
   return e;
 }
 
@@ -1073,17 +1140,22 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const CUtensorMap& tmap_k, co
   const bool pdl = prof_start == nullptr;
   cudaError_t e = cudaSuccess;
   if (prof_start && (e = cudaEventRecord(prof_start, stream)) != cudaSuccess) return e;
-  if (p.fp8_pages)
-    e = launch_pdl(decode_main_kernel<S, true, false>, dim3(p.parts),
-                   dim3(decode_threads<S, true>()), DecodeSmem<S, true>::ALLOC, stream, pdl,
+  constexpr int F16 = RCP_PAGES_FP16, E4M3 = RCP_PAGES_FP8_E4M3, I4 = RCP_PAGES_INT4;
+  if (p.page_format == E4M3)
+    e = launch_pdl(decode_main_kernel<S, E4M3, false>, dim3(p.parts),
+                   dim3(decode_threads<S, E4M3>()), DecodeSmem<S, E4M3>::ALLOC, stream, pdl,
                    tmap_v, tmap_k, p);
+  else if (p.page_format == I4)
+    e = launch_pdl(decode_main_kernel<S, I4, false>, dim3(p.parts),
+                   dim3(decode_threads<S, I4>()), DecodeSmem<S, I4>::ALLOC, stream, pdl, tmap_v,
+                   tmap_k, p);
   else if (p.sparse)
-    e = launch_pdl(decode_main_kernel<S, false, true>, dim3(p.parts),
-                   dim3(decode_threads<S, false, true>()), DecodeSmem<S, false, true>::ALLOC,
-                   stream, pdl, tmap_v, tmap_k, p);
+    e = launch_pdl(decode_main_kernel<S, F16, true>, dim3(p.parts),
+                   dim3(decode_threads<S, F16, true>()), DecodeSmem<S, F16, true>::ALLOC, stream,
+                   pdl, tmap_v, tmap_k, p);
   else
-    e = launch_pdl(decode_main_kernel<S, false, false>, dim3(p.parts),
-                   dim3(decode_threads<S, false>()), DecodeSmem<S, false>::ALLOC, stream, pdl,
+    e = launch_pdl(decode_main_kernel<S, F16, false>, dim3(p.parts),
+                   dim3(decode_threads<S, F16>()), DecodeSmem<S, F16>::ALLOC, stream, pdl,
                    tmap_v, tmap_k, p);
   if (e != cudaSuccess) return e;
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;

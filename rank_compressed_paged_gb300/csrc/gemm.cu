@@ -53,7 +53,8 @@ struct GemmSmem {
   static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;        // full[S], empty[S], acc
   static constexpr int MISC_OFF = BAR_OFF + (2 * STG + 1) * 8;
   static constexpr int DST_OFF = MISC_OFF + 16;                // append: page offset per column
-  static constexpr int TOTAL = DST_OFF + NT * 8;
+  static constexpr int RED_OFF = DST_OFF + NT * 8;             // 4-bit append: [4 warps][16]
+  static constexpr int TOTAL = RED_OFF + 4 * 16 * 4;
   static constexpr int ALLOC = TOTAL + 1024;
   static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
   static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment");
@@ -67,7 +68,8 @@ struct GemmParams {
   void* k_pages;
   void* v_pages;
   int32_t T;
-  int32_t fp8;            // pages hold E4M3 codes (round to nearest even, saturate)
+  int32_t fmt;            // RCP_PAGES_*: fp16, E4M3 (round to nearest even, saturate) or
+                          // 4-bit codes with per-group fp16 scales
   int64_t num_blocks;
   int32_t nq;             // decode queries (decode query jobs), prefill rows
   uint32_t* dev_err;
@@ -152,10 +154,10 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank, int T) {
   return j;
 }
 
-// Page offset (in fp16 elements) that column col of an append job writes from, or -1 when
-// the token is padding (slot < 0), past the token count, or has an out-of-range slot
-// (which also raises the device error bit).  Computed once per column before the
-// epilogue so that the store loop issues no dependent loads.
+// Page offset (in fp16 elements; 4-bit pages: the slot itself) that column col of an append
+// job writes from, or -1 when the token is padding (slot < 0), past the token count, or has
+// an out-of-range slot (which also raises the device error bit).  Computed once per column
+// before the epilogue so that the store loop issues no dependent loads.
 template <class S>
 __device__ __forceinline__ int64_t append_dst(const GemmParams& p, const GemmJob& j, int col) {
   const int n = j.n0 + col;
@@ -166,9 +168,82 @@ __device__ __forceinline__ int64_t append_dst(const GemmParams& p, const GemmJob
     atomicOr(p.dev_err, RCP_DEVERR_BAD_SLOT);
     return -1;
   }
+  if (p.fmt == RCP_PAGES_INT4) return s;
   const int64_t blk = s / kBlockSize, off = s % kBlockSize;
   return j.kind == 0 ? (blk * kBlockSize + off) * S::R
                      : ((blk * S::H + j.m0) * kBlockSize + off) * S::RK;
+}
+
+// Round x / s to the nearest integer, ties to even, exactly for the fp32 x and fp16 s an
+// append meets: the fp32 quotient's integer is corrected by the residual x - k s, which an
+// fma computes exactly here (k s has at most 14 significant bits and lies within s of x).
+__device__ __forceinline__ int rne_div(float x, float s) {
+  float k = rintf(__fdiv_rn(x, s));
+  const float r = fmaf(-k, s, x);
+  const float a2 = 2.f * fabsf(r);
+  if (a2 > s || (a2 == s && fmodf(k, 2.f) != 0.f)) k += r > 0.f ? 1.f : -1.f;
+  return static_cast<int>(k);
+}
+
+// 4-bit pages: quantize NC finished columns c0 .. c0+NC-1 of an append job, held by every
+// thread as v[] for its row (TMEM lane), and store codes and scales.  A group is 64 rows:
+// a key row of one head (rows 0..63, 64..127 of a key-pair job; rows at or past r_k of a
+// head are not coefficients) or 64 value coefficients (m0 + 0..63, m0 + 64..127).  Per
+// group: the smallest fp16 scale with 7 * scale >= max |x|, codes x / scale rounded to
+// nearest, ties to even, in [-7, 7]; two codes per byte, the even row in the low nibble.
+// All kGemmThreads threads take part (block barriers).
+template <class S, int NC>
+__device__ __forceinline__ void int4_store_columns(const GemmParams& p, const GemmJob& j,
+                                                   const int64_t* dst, float* red, int c0,
+                                                   const float* v) {
+  using P = Int4Page<S>;
+  const int row = threadIdx.x, warp = row >> 5, lane = row & 31;
+  const bool valid = j.kind == 1 ? (row & 63) < S::RK : j.m0 + row < S::R;
+  float a[NC];
+#pragma unroll
+  for (int e = 0; e < NC; ++e) {
+    a[e] = valid ? fabsf(v[e]) : 0.f;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) a[e] = fmaxf(a[e], __shfl_xor_sync(0xffffffffu, a[e], o));
+  }
+  if (lane == 0)
+#pragma unroll
+    for (int e = 0; e < NC; ++e) red[warp * 16 + e] = a[e];
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < NC; ++e) {
+    const float amax = fmaxf(red[warp * 16 + e], red[(warp ^ 1) * 16 + e]);
+    __half sh = __float2half_ru(__fdiv_rn(amax, 7.f));
+    if (__half2float(sh) * 7.f < amax)   // the quotient's fp32 rounding went down
+      sh = __ushort_as_half(static_cast<unsigned short>(__half_as_ushort(sh) + 1));
+    const float sf = __half2float(sh);
+    int code = 0;
+    if (valid && sf > 0.f) code = max(-7, min(7, rne_div(v[e], sf)));
+    const int hi = __shfl_down_sync(0xffffffffu, code, 1);   // the next row's code
+    const int64_t s = dst[c0 + e];
+    if (s < 0 || !valid) continue;
+    const int64_t blk = s / kBlockSize, off = s % kBlockSize;
+    uint8_t* page;
+    int64_t cbyte, sidx;
+    bool first;   // the group's first row stores its scale
+    if (j.kind == 1) {
+      const int hh = j.m0 + (row >> 6), rr = row & 63;
+      page = static_cast<uint8_t*>(p.k_pages) + blk * P::KBYTES;
+      cbyte = ((hh * kBlockSize + off) * S::RK + rr) / 2;
+      sidx = hh * kBlockSize + off;
+      first = rr == 0;
+      if (first) reinterpret_cast<__half*>(page + P::KCODES)[sidx] = sh;
+    } else {
+      const int r = j.m0 + row;
+      page = static_cast<uint8_t*>(p.v_pages) + blk * P::VBYTES;
+      cbyte = (off * S::R + r) / 2;
+      sidx = off * (S::R / 64) + r / 64;
+      first = (r & 63) == 0;
+      if (first) reinterpret_cast<__half*>(page + P::VCODES)[sidx] = sh;
+    }
+    if ((row & 1) == 0) page[cbyte] = static_cast<uint8_t>((code & 0xF) | ((hi & 0xF) << 4));
+  }
+  __syncthreads();   // red[] is reused by the next call
 }
 
 // Write one finished output element (row, column) of a job.
@@ -208,7 +283,7 @@ __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j
     at = d + hh * kBlockSize * S::RK + rr;
     pages = p.k_pages;
   }
-  if (p.fp8)
+  if (p.fmt == RCP_PAGES_FP8_E4M3)
     static_cast<__nv_fp8_storage_t*>(pages)[at] = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
   else
     static_cast<__half*>(pages)[at] = __float2half_rn(v);
@@ -344,7 +419,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const int row = warp * 32 + lane;                          // TMEM lane = output row
   const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  if (!j.reduce) {
+  // 4-bit pages: an append job quantizes whole 64-row groups (uniform over the CTA, and
+  // over the cluster for split-K value jobs)
+  const bool int4 = MODE == kModeAppend && p.fmt == RCP_PAGES_INT4 && (j.kind == 0 || j.kind == 1);
+  float* red = reinterpret_cast<float*>(sm + L::RED_OFF);
+  if (int4 && !j.reduce) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < NT; c0 += 16) {
+      float v[16];
+      if (have_acc) {
+        tmem_ld16(trow + c0, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+      }
+      int4_store_columns<S, 16>(p, j, dst_s, red, c0, v);
+    }
+  } else if (int4) {
+    if constexpr (KS > 1) {
+    // split-K: column c belongs to peer c / CPC, which receives every row of it (a group
+    // spans 64 rows) in slot [my rank][row][c % CPC]
+    constexpr int CPC = NT / KS;
+    static_assert(CPC >= 1 && CPC <= 16 && NT % KS == 0, "4-bit split-K columns");
+    const uint32_t recv_local = smem_u32(recv);
+#pragma unroll 1
+    for (int c0 = 0; c0 < NT; c0 += 16) {
+      float v[16];
+      if (have_acc) {
+        tmem_ld16(trow + c0, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int col = c0 + e;
+        st_cluster_f32(map_to_rank(recv_local, static_cast<uint32_t>(col / CPC)) +
+                           ((rank * 128 + row) * CPC + col % CPC) * 4,
+                       v[e]);
+      }
+    }
+    cluster_sync_all();
+    float v[CPC];
+#pragma unroll
+    for (int c = 0; c < CPC; ++c) {
+      float acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < KS; ++s) acc += recv[(s * 128 + row) * CPC + c];
+      v[c] = acc;
+    }
+    int4_store_columns<S, CPC>(p, j, dst_s, red, static_cast<int>(rank) * CPC, v);
+    }
+  } else if (!j.reduce) {
     if (have_acc) {
 #pragma unroll 1
       for (int c0 = 0; c0 < NT; c0 += 16) {
@@ -468,7 +596,7 @@ cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
   p.k_pages = ap.k_pages;
   p.v_pages = ap.v_pages;
   p.T = ap.T;
-  p.fp8 = ap.fp8_pages;
+  p.fmt = ap.page_format;
   p.num_blocks = ap.num_blocks;
   p.dev_err = ap.dev_err;
   p.qt = ap.qt;

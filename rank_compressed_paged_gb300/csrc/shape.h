@@ -35,6 +35,16 @@ struct Shape {
   static_assert(NCHUNK * HP <= 512, "accumulator must fit in tensor memory");
 };
 
+// 4-bit pages: bytes of one K page (codes [H][16][r_k/2], then fp16 scales [H][16]) and of
+// one V page (codes [16][R/2], then fp16 scales [16][R/64]).
+template <class S>
+struct Int4Page {
+  static constexpr int64_t KCODES = S::H * kBlockSize * S::RK / 2;
+  static constexpr int64_t KBYTES = KCODES + S::H * kBlockSize * 2;
+  static constexpr int64_t VCODES = kBlockSize * S::R / 2;
+  static constexpr int64_t VBYTES = VCODES + kBlockSize * (S::R / 64) * 2;
+};
+
 using ShapeMain = Shape<32, 128, 64, 1024>;
 using ShapeTiny = Shape<4, 64, 16, 64>;
 
@@ -168,7 +178,7 @@ struct AttnParams {
   int32_t batch;
   int32_t nq;
   int32_t parts;              // decode CTAs (work partitions)
-  int32_t fp8_pages;          // pages hold E4M3 codes (decode only)
+  int32_t page_format;        // RCP_PAGES_* of the pages the kernels read
   // block-sparse decode: a page whose every head's largest score is more than skip_tau
   // (log2 units) below that head's running maximum is left out, values unread
   int32_t sparse;
@@ -205,7 +215,7 @@ struct AppendParams {
   uint32_t* dev_err;
   int64_t num_blocks;
   int32_t T;
-  int32_t fp8_pages;          // store E4M3 codes instead of fp16
+  int32_t page_format;        // RCP_PAGES_*: fp16, E4M3 or 4-bit codes with scales
   // decode: the rank-space queries are projected in the same launch (nq = 0: none)
   float* qt;                  // [nq][H][r_k] fp32, q~ scaled by qscale
   int32_t nq;

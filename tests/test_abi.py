@@ -50,7 +50,9 @@ def test_config_support_and_status_strings(lib):
     assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, rk=48))) == _lib.RCP_ERR_UNSUPPORTED
     assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, fmt=_lib.RCP_PAGES_FP8_E4M3))) == \
         _lib.RCP_OK
-    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, fmt=2))) == _lib.RCP_ERR_UNSUPPORTED
+    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, fmt=_lib.RCP_PAGES_INT4))) == \
+        _lib.RCP_OK
+    assert lib.rcp_config_supported(ctypes.byref(_cfg(_lib, fmt=3))) == _lib.RCP_ERR_UNSUPPORTED
     assert lib.rcp_config_supported(None) == _lib.RCP_ERR_INVALID_ARG
     for code in range(6):
         assert lib.rcp_status_string(code)
@@ -186,6 +188,11 @@ def test_sparse_decode_host_checks(lib):
     assert lib.rcp_decode_attn_sparse(h8, 0x1000, 0x2000, 64, 0x3000, 16, 0.01, None, 0x4000, ws,
                                       b.value, None) == _lib.RCP_ERR_UNSUPPORTED
     lib.rcp_destroy_cache(h8)
+    st, h4 = _create(lib, _lib, _cfg(_lib, fmt=_lib.RCP_PAGES_INT4))
+    assert st == _lib.RCP_OK
+    assert lib.rcp_decode_attn_sparse(h4, 0x1000, 0x2000, 64, 0x3000, 16, 0.01, None, 0x4000, ws,
+                                      b.value, None) == _lib.RCP_ERR_UNSUPPORTED
+    lib.rcp_destroy_cache(h4)
 
 
 def test_reconstruct_workspace_grows_by_the_widened_pages_for_e4m3(lib):

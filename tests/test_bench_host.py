@@ -79,8 +79,10 @@ def test_byte_accounting():
     coeff = wl.algorithmic_bytes_decode(shape, np.full(64, 8192))
     assert coeff == 64 * 8192 * (32 * 64 + 1024) * 2 == 3221225472
     assert wl.factor_bytes(shape) == (32 * 64 * 128 + 1024 * 32 * 128) * 2 == 8912896
-    assert wl.algorithmic_bytes_decode(shape, [100], 1) * 2 == wl.algorithmic_bytes_decode(
-        shape, [100])
+    assert wl.algorithmic_bytes_decode(shape, [100], "fp8_e4m3") * 2 == \
+        wl.algorithmic_bytes_decode(shape, [100])
+    # 4-bit pages: 32 heads x 64 codes / 2 + 32 scales x 2 + 1024 / 2 + 16 scales x 2 bytes
+    assert wl.page_bytes_per_token(shape, "int4") == 1024 + 64 + 512 + 32 == 1632
     per_req = bench.bytes_per_request()
     assert abs(per_req * bench.BATCH - (coeff + wl.factor_bytes(shape))) < 1e-3
 
@@ -108,3 +110,20 @@ def test_decode_step_flop_count():
     assert f["upproj"] == 2 * 64 * 32 * 1024 * 128
     assert f["total"] == sum(v for k, v in f.items() if k != "total")
     assert bench.decode_step_flops([16, 16], kept_tokens=16)["pv"] == 2 * 16 * 32 * 1024
+
+
+def test_bench_int4_page_preparation_matches_the_oracle_encoding():
+    """The bench stores its seeded fp16 pages as 4-bit pages with torch ops; the bytes must
+    be the oracle's encoding of the same coefficients."""
+    import torch
+    from oracle import rcp_oracle as orc
+    rng = np.random.default_rng(5)
+    H, rk, R = 4, 16, 128
+    kp = wl.fp16(rng.standard_normal((3, H, 16, rk)))
+    vp = wl.fp16(rng.standard_normal((3, 16, R)) * 3)
+    kp[1, 2, 5] = 0.0                      # an all-zero group
+    kb, vb = bench.int4_pages_torch(torch.from_numpy(kp), torch.from_numpy(vp))
+    kc, ks, vc, vs = orc.int4_pages(kp, vp)
+    ko, vo = orc.int4_pack_pages(kc, ks, vc, vs)
+    assert np.array_equal(kb.numpy(), ko)
+    assert np.array_equal(vb.numpy(), vo)

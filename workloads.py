@@ -391,11 +391,23 @@ def make_paged_cache_device(seq_lens, shape: dict, seed: int, device="cuda",
     return kp, vp, table, seq_lens
 
 
-def algorithmic_bytes_decode(shape: dict, seq_lens, elem_bytes: int = 2) -> int:
-    """Coefficient bytes one decode step reads: (H*r_k + R) * elem_bytes per cached token
-    (2 for fp16 pages, 1 for E4M3 pages)."""
-    per_tok = (shape["num_heads"] * shape["rank_k"] + shape["rank_v"]) * elem_bytes
-    return int(np.sum(np.asarray(seq_lens, dtype=np.int64))) * per_tok
+def page_bytes_per_token(shape: dict, pages: str = "fp16") -> int:
+    """Bytes of K and V pages per cached token: (H*r_k + R) coefficients at 2 bytes (fp16)
+    or 1 (E4M3); 4-bit pages hold half a byte per coefficient plus an fp16 scale per key
+    row of a head and per 64 value coefficients."""
+    H, rk, R = shape["num_heads"], shape["rank_k"], shape["rank_v"]
+    if pages == "fp16":
+        return (H * rk + R) * 2
+    if pages == "fp8_e4m3":
+        return H * rk + R
+    if pages == "int4":
+        return H * rk // 2 + 2 * H + R // 2 + 2 * (R // 64)
+    raise ValueError(pages)
+
+
+def algorithmic_bytes_decode(shape: dict, seq_lens, pages: str = "fp16") -> int:
+    """Page bytes one decode step reads: page_bytes_per_token per cached token."""
+    return int(np.sum(np.asarray(seq_lens, dtype=np.int64))) * page_bytes_per_token(shape, pages)
 
 
 def factor_bytes(shape: dict) -> int:
