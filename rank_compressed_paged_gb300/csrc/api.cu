@@ -38,7 +38,8 @@ struct rcp_cache {
   CUtensorMap tmap_uk;      // U_k as [H*r_k][d], 64 x 128 boxes (query projection: A)
   CUtensorMap tmap_uk64;    // U_k as [H*r_k][d], 64 x 64 boxes (append key pairs: A)
   CUtensorMap tmap_kp;      // K pages as [num_blocks*H*16][r_k], 64 x 16 boxes (prefill B)
-  CUtensorMap tmap_kpage;   // the same rows, 64 x 256 boxes (decode: half a page per box)
+  CUtensorMap tmap_kpage;   // the same rows, 64 x 256 boxes (decode: half a page per box;
+                            // E4M3 pages: bytes, 64-byte swizzle)
   // optional events recorded around the split-K attention kernel
   cudaEvent_t prof_start;
   cudaEvent_t prof_stop;
@@ -89,6 +90,21 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A 2-D byte tensor map with 64-byte swizzle (E4M3 key pages with 64-byte rows: the
+// decode's tensor-core scoring reads them as the swizzled K-major operand).
+bool encode_2d_u8_sw64(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                       uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rows == 0) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(inner), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -158,6 +174,12 @@ rcp_status ensure_device(rcp_cache* c) {
                  static_cast<uint64_t>(g.num_blocks) * g.num_heads * 16,
                  static_cast<uint64_t>(g.rank_k) * 2, 64,
                  g.num_heads * 16 < 256 ? static_cast<uint32_t>(g.num_heads * 16) : 256))
+    return RCP_ERR_CUDA;
+  // E4M3 key pages with 64-byte rows: the decode copies them through a byte map
+  if (g.page_format == RCP_PAGES_FP8_E4M3 && g.rank_k == 64 &&
+      !encode_2d_u8_sw64(&c->tmap_kpage, c->k_pages, 64,
+                         static_cast<uint64_t>(g.num_blocks) * g.num_heads * 16,
+                         g.num_heads * 16 < 256 ? static_cast<uint32_t>(g.num_heads * 16) : 256))
     return RCP_ERR_CUDA;
   c->num_sms = sms;
   c->device = dev;

@@ -184,11 +184,26 @@ constexpr int kAppendSetSize = 1 << kAppendSetBits;   // a step appending more t
 // with fp16 scales) arrive whole by bulk copies; K pages are scored straight from their
 // bytes, V pages land in raw stages and are widened to fp16 in the swizzled layout the
 // tensor-core MMA reads (the layout the fp16 path's tensor-map copies produce).
+// TSC (E4M3 pages, r_k = 64, heads a multiple of 16): the keys are scored on the tensor
+// cores.  Per 8-head group one kind::f8f6f4 MMA (M = 128 key rows of a page, the group's
+// heads x 16 tokens; K = r_k) multiplies the E4M3 codes, as the page's TMA copy lands them
+// (64-byte swizzle), by the group's query split into four E4M3 terms: head h's q~, scaled
+// by a power of two 2^e_h that brings its largest entry into [128, 256), is t0 + t1 + t2
+// + t3 with t0 = e4m3(q), t1 = e4m3(q - t0), ... (each residual at most 2^-4 of the one
+// before: 2^-16 relative after four terms, down to E4M3's subnormal step).  The 32 columns
+// of a group's result are 8 per head pair: (term, head parity); a key row's score is the
+// sum of its head's four columns times 2^-e_h.
+template <class S, int FMT, bool SKIP>
+constexpr bool decode_tensor_scores() {
+  return FMT == RCP_PAGES_FP8_E4M3 && S::RK == 64 && S::H % 16 == 0 && !SKIP;
+}
+
 template <class S, int FMT, bool SKIP = false>
 struct DecodeSmem {
   static constexpr bool F8 = FMT != RCP_PAGES_FP16;                 // raw quantized pages
+  static constexpr bool TSC = decode_tensor_scores<S, FMT, SKIP>();
   static constexpr int DS = 4;                                      // SKIP: decision ring
-  static constexpr int KST = F8 ? 3 : 2;                            // key page stages
+  static constexpr int KST = F8 && !TSC ? 3 : 2;                    // key page stages
   static constexpr int VST = 2;                                     // fp16 V stages (MMA A)
   static constexpr int VRS = F8 ? 3 : VST;                          // stages V copies land in
   static constexpr int KP = FMT == RCP_PAGES_FP8_E4M3 ? S::KPAGE_BYTES / 2   // bytes per K page
@@ -199,32 +214,49 @@ struct DecodeSmem {
                                                    : S::VPAGE_BYTES;
   static constexpr int KPS = (KP + 127) & ~127;                     // stage strides
   static constexpr int VPS = (VP + 127) & ~127;
-  static constexpr int NBAR = 2 * KST + 2 * VRS + 4 + (F8 ? 2 * VST : 0) + (SKIP ? 2 * DS : 0);
+  static constexpr int NBAR = 2 * KST + 2 * VRS + 4 + (F8 ? 2 * VST : 0) + (SKIP ? 2 * DS : 0) +
+                              (TSC ? 8 : 0);
   static constexpr int P_BYTES = S::HP * 16 * 2;
   static constexpr int V_OFF = 0;                                   // 1024-aligned stages
   static constexpr int K_OFF = V_OFF + VST * S::VSTAGE_BYTES;
   static constexpr int VR_OFF = K_OFF + KST * KPS;                  // raw E4M3 V stages
   static constexpr int P_OFF = VR_OFF + (F8 ? VRS * VPS : 0);
   static constexpr int Q_OFF = P_OFF + 2 * P_BYTES;
-  static constexpr int A_OFF = Q_OFF + S::H * S::RK * 4;            // alpha[2][HP]
+  // TSC: the query operand ([H/8 groups][32 rows][r_k] E4M3, K-major without swizzle:
+  // 8-row x 16-byte core matrices, 128 bytes apart along K, 512 along the rows; one buffer,
+  // rewritten once the previous segment's scoring MMAs completed) and the score factors
+  // 2^-e_h per segment parity [2][H]; otherwise q~ in fp32
+  static constexpr int QOP_BYTES = (S::H / 8) * 32 * S::RK;
+  static constexpr int Q_BYTES = TSC ? QOP_BYTES + 2 * S::H * 4 : S::H * S::RK * 4;
+  static constexpr int A_OFF = Q_OFF + Q_BYTES;                     // alpha[2][HP]
   static constexpr int F_OFF = A_OFF + 2 * S::HP * 4;               // flags[2][4]
   static constexpr int BAR_OFF = F_OFF + 64;                        // NBAR mbarriers
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;               // tmem slot, abort flag
   static constexpr int INFO_OFF = MISC_OFF + 16;                    // valid tokens per stage:
   // K stages, then V; SKIP adds the physical block of each K stage, the decision ring and
-  // the info word of each P buffer
-  static constexpr int INFO_BYTES = (KST + VRS) * 4 + (SKIP ? (KST + DS + 2) * 4 : 0);
+  // the info word of each P buffer; TSC the valid tokens of each score buffer
+  static constexpr int INFO_BYTES = (2 * KST + VRS + DS + 4) * 4;
+  // TMEM: the value accumulator [NCHUNK x 128 lanes][HP], then (TSC) two score buffers of
+  // H/8 groups x 32 columns
+  static constexpr int SCOL = S::NCHUNK * S::HP;
+  static constexpr int TMEM_COLS = TSC ? pow2_at_least(SCOL + 2 * (S::H / 8) * 32, 32)
+                                       : S::TMEM_COLS;
   // the partition's plan: 32 warp partials of the scans, then the block total, the first
   // request and its first block; then the set of blocks a decode step's append writes
   static constexpr int PLAN_OFF = (INFO_OFF + INFO_BYTES + 7) & ~7;
   static constexpr int HASH_OFF = PLAN_OFF + (32 + 4) * 8;
-  static constexpr int TOTAL = HASH_OFF + kAppendSetSize * 4;
+  // the copy warp's page ring: physical block and valid tokens of two batches of 32 pages
+  static constexpr int PG_OFF = HASH_OFF + kAppendSetSize * 4;
+  static constexpr int TOTAL = PG_OFF + 2 * 2 * 32 * 4;
   static_assert(PLAN_OFF % 8 == 0 && HASH_OFF % 4 == 0 && A_OFF % 16 == 0 && Q_OFF % 16 == 0 &&
                     BAR_OFF % 8 == 0,
                 "region alignment");
   static constexpr int ALLOC = TOTAL + 1024;                        // base alignment slack
   static_assert(KP % 16 == 0 && VP % 16 == 0 && S::VSTAGE_BYTES % 1024 == 0, "alignment");
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+  static_assert(TMEM_COLS <= 512, "tensor memory");
+  static_assert(!TSC || (K_OFF % 512 == 0 && KPS % 512 == 0 && Q_OFF % 16 == 0),
+                "64-byte swizzled key stages, query operands");
 };
 
 // Warp 0 copies, warp 1 issues the MMAs, warps 2 .. compute.
@@ -232,11 +264,21 @@ struct DecodeSmem {
 // which widen the E4M3 V pages while the compute warps score.
 // SKIP: warp 0 copies keys only and warp 6 copies the value pages the compute warps keep.
 // (Eight compute warps measured slower there: more registers spilled and barrier traffic.)
+// TSC: four compute warps (one per TMEM lane quarter: scores, softmax, weights) and six
+// warps that widen the V pages (and build the query operands), so that the widening's
+// conversions overlap the softmax's shuffle latencies instead of following them.
 template <class S, int FMT, bool SKIP = false>
-constexpr int decode_compute_warps() { return (FMT != RCP_PAGES_FP16 && S::H % 8 == 0) ? 8 : 4; }
+constexpr int decode_compute_warps() {
+  return decode_tensor_scores<S, FMT, SKIP>() ? 4
+                                              : (FMT != RCP_PAGES_FP16 && S::H % 8 == 0) ? 8 : 4;
+}
+template <class S, int FMT, bool SKIP = false>
+constexpr int decode_widen_warps() {
+  return decode_tensor_scores<S, FMT, SKIP>() ? 6 : FMT != RCP_PAGES_FP16 ? 2 : 0;
+}
 template <class S, int FMT, bool SKIP = false>
 constexpr int decode_threads() {
-  return 32 * (2 + decode_compute_warps<S, FMT, SKIP>() + (FMT != RCP_PAGES_FP16 ? 2 : 0) +
+  return 32 * (2 + decode_compute_warps<S, FMT, SKIP>() + decode_widen_warps<S, FMT, SKIP>() +
                (SKIP ? 1 : 0));
 }
 
@@ -264,6 +306,36 @@ __device__ __forceinline__ uint32_t int4x2_to_half2_bits(uint32_t byte, __half2 
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// E4M3 pages, an even number of boxes: as widen_v_boxes below, in units of 16 codes (one
+// 16-byte load, two 16-byte stores).  A warp's 32 units are 4 tokens x 2 adjacent boxes x 4
+// units, so its loads cover four 128-byte row pieces and its stores eight 128-byte stage
+// rows: no shared-memory bank is hit twice beyond the minimum.
+template <class S, int NT>
+__device__ __forceinline__ void widen_v_e4m3_pairs(const uint8_t* src, uint8_t* vb, int nvalid,
+                                                   int b0, int b1, int tid) {
+  const int n = (b1 - b0) * kBlockSize * 4;
+#pragma unroll 2
+  for (int idx = tid; idx < n; idx += NT) {
+    const int c16 = idx & 3, gl = (idx >> 2) & 1, tl = (idx >> 3) & 3, th = (idx >> 5) & 3;
+    const int tt = th * 4 + tl, gb = b0 + (idx >> 7) * 2 + gl;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (tt < nvalid) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(src + tt * S::R + gb * 64 + c16 * 16);
+      lo.x = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x & 0xFFFFu));
+      lo.y = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.x >> 16));
+      lo.z = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y & 0xFFFFu));
+      lo.w = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.y >> 16));
+      hi.x = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.z & 0xFFFFu));
+      hi.y = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.z >> 16));
+      hi.z = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.w & 0xFFFFu));
+      hi.w = e4m3x2_to_half2_bits(static_cast<uint16_t>(raw.w >> 16));
+    }
+    uint8_t* row = vb + gb * 2048 + tt * 128;
+    *reinterpret_cast<uint4*>(row + (((2 * c16) ^ (tt & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ (tt & 7)) << 4)) = hi;
+  }
+}
+
 // Widens boxes [b0, b1) (64 columns each) of a quantized V page (E4M3: [16][R] codes at src;
 // 4-bit: [16][R/2] code bytes then the fp16 scales [16][R/64]) into the fp16 stage vb in
 // the layout of the value MMA: box g at g * 2048, token row t at t * 128, 16-byte chunk c
@@ -273,6 +345,10 @@ __device__ __forceinline__ uint32_t int4x2_to_half2_bits(uint32_t byte, __half2 
 template <class S, int FMT, int NT>
 __device__ __forceinline__ void widen_v_boxes(const uint8_t* src, uint8_t* vb, int nvalid, int b0,
                                               int b1, int tid) {
+  if constexpr (FMT == RCP_PAGES_FP8_E4M3 && S::NBOX % 2 == 0) {
+    widen_v_e4m3_pairs<S, NT>(src, vb, nvalid, b0, b1, tid);
+    return;
+  }
   const int n = (b1 - b0) * kBlockSize * 8;
 #pragma unroll 4
   for (int idx = tid; idx < n; idx += NT) {
@@ -297,6 +373,53 @@ __device__ __forceinline__ void widen_v_boxes(const uint8_t* src, uint8_t* vb, i
       }
     }
     *reinterpret_cast<uint4*>(vb + gb * 2048 + tt * 128 + ((c ^ (tt & 7)) << 4)) = o;
+  }
+}
+
+// TSC: the query operand of one request (q: its q~ [H][r_k] fp32) and its score factors
+// (qi[h] = 2^-e_h), by 64 threads (vt): two per head, 32 ranks each.  Row n = 8p + 2j + e
+// of group g holds term j of head 8g + 2p + e; byte (n, k) of a group sits at
+// (n / 8) * 512 + (k / 16) * 128 + (n % 8) * 16 + k % 16.
+template <class S>
+__device__ __forceinline__ void build_query_operand(const float* q, uint8_t* qo, float* qi,
+                                                    int vt) {
+  for (int i = vt; i < 2 * S::H; i += 64) {
+    const int h = i >> 1, half = i & 1;
+    const float4* src = reinterpret_cast<const float4*>(q + h * S::RK + half * 32);
+    float x[32];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float4 v = __ldcg(src + u);
+      x[4 * u] = v.x;
+      x[4 * u + 1] = v.y;
+      x[4 * u + 2] = v.z;
+      x[4 * u + 3] = v.w;
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fabsf(x[k]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));   // the partner holds the other half
+    int E = 0;
+    frexpf(mx, &E);                                         // mx = m 2^E, m in [0.5, 1)
+    const int sh = 8 - E;                                   // largest entry -> [128, 256)
+    if (half == 0) qi[h] = ldexpf(1.f, -sh);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) x[k] = ldexpf(x[k], sh);
+    uint8_t* base = qo + (h >> 3) * 32 * S::RK + ((h & 7) >> 1) * 512 + (h & 1) * 16 +
+                    half * 2 * 128;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w[8];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(x[k], __NV_SATFINITE, __NV_E4M3);
+        x[k] -= __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));   // exact
+        const uint32_t b = static_cast<uint32_t>(c) << (8 * (k & 3));
+        w[k >> 2] = (k & 3) ? (w[k >> 2] | b) : b;
+      }
+      *reinterpret_cast<uint4*>(base + j * 32) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(base + j * 32 + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
   }
 }
 
@@ -357,6 +480,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   // head read the same logical chunk, conflict-free on the keys and as a broadcast on q~
   constexpr bool KSWZ = !F8 && S::RK == 64;
   using L = DecodeSmem<S, FMT, SKIP>;
+  constexpr bool TSC = L::TSC;   // keys scored on the tensor cores (E4M3 pages)
   constexpr int KST = L::KST, VST = L::VST, VRS = L::VRS, HP = S::HP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -366,6 +490,8 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   uint8_t* vraw = sm + L::VR_OFF;
   uint8_t* pbuf = sm + L::P_OFF;
   float* qs = reinterpret_cast<float*>(sm + L::Q_OFF);
+  uint8_t* qop = sm + L::Q_OFF;                                              // TSC [2]
+  float* qinv = reinterpret_cast<float*>(sm + L::Q_OFF + L::QOP_BYTES);   // TSC [2][H]
   float* alpha_s = reinterpret_cast<float*>(sm + L::A_OFF);
   int* flags_s = reinterpret_cast<int*>(sm + L::F_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
@@ -379,11 +505,16 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   uint64_t* vfree = vcvt + VST;           // F8 [VST] fp16 V stage read by its MMAs
   uint64_t* decfull = pfree + 2 + (F8 ? 2 * VST : 0);   // SKIP [DS] a decision was posted
   uint64_t* decempty = decfull + L::DS;                  // SKIP [DS] ... and taken
+  uint64_t* sfull = decfull + (SKIP ? 2 * L::DS : 0);    // TSC [2] a page's scores are in TMEM
+  uint64_t* sfree = sfull + 2;                           // TSC [2] ... and were read
+  uint64_t* qfull = sfree + 2;                           // TSC [2] a segment's query operand
+  uint64_t* qfree = qfull + 2;                           // TSC [2] ... its MMAs completed
   constexpr int NTHR = decode_threads<S, FMT, SKIP>();
   constexpr int NCW = decode_compute_warps<S, FMT, SKIP>();   // compute warps 2 .. NCW+1
   // F8: V boxes widened by warps 10-11; the compute warps widen the remaining ones (a
   // split measured to balance the two groups' time per block)
-  constexpr int WB = S::NBOX >= 16 ? 10 : S::NBOX;
+  constexpr int NWW = decode_widen_warps<S, FMT, SKIP>();   // widening warps NCW+2 ..
+  constexpr int WB = TSC ? S::NBOX : S::NBOX >= 16 ? 6 : S::NBOX;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
   // tokens of the block in each stage that are attended, published by the copy thread
@@ -397,6 +528,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   int* kphys = vinfo + VRS;
   int* dec_s = kphys + KST;
   int* pinfo = dec_s + L::DS;
+  int* sinfo = pinfo + 2;   // TSC: valid tokens of the page in each score buffer
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -405,15 +537,24 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < KST; ++i) {
       mbar_init(&kfull[i], 1);
-      mbar_init(&kempty[i], NCW);
+      mbar_init(&kempty[i], TSC ? 1 : NCW);   // TSC: the scoring MMAs' commit
+    }
+    if constexpr (TSC) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&sfull[i], 2);    // the MMA thread's arrive (after sinfo) + the commit
+        mbar_init(&sfree[i], NCW);
+        mbar_init(&qfull[i], 2);    // the two widening warps
+        mbar_init(&qfree[i], 1 + NCW);   // the MMAs' commit + each compute warp's read of
+                                         // the score factors
+      }
     }
     for (int i = 0; i < VRS; ++i) {
       mbar_init(&vfull[i], 1);
-      mbar_init(&vempty[i], F8 ? 2 + (WB < S::NBOX ? NCW : 0) : 1);
+      mbar_init(&vempty[i], F8 ? NWW + (WB < S::NBOX ? NCW : 0) : 1);
     }
     if constexpr (F8) {
       for (int i = 0; i < VST; ++i) {
-        mbar_init(&vcvt[i], 2);
+        mbar_init(&vcvt[i], NWW);
         mbar_init(&vfree[i], 1);
       }
     }
@@ -431,7 +572,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, S::TMEM_COLS);
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
   }
   // Zero both P buffers (padded head rows stay zero) and any part of a V stage that no
@@ -572,62 +713,104 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     // no blocks for this CTA
   } else if (warp == 0) {
     // ------------------------------------------------------------------ copy producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      const uint8_t* kpages = static_cast<const uint8_t*>(p.k_pages);
-      int64_t nk = 0, nv = 0;
-      bool waited = !step;
-      for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
-        walk.advance_to(g);
-        const int64_t j = g - walk.bstart;
-        const int64_t raw = p.block_table[static_cast<int64_t>(walk.b) * p.bt_stride + j];
+    // The whole warp looks up the block ids and valid tokens of 32 pages at a time (lane l:
+    // page c0 + l), one batch ahead of the copies, so that lane 0 never waits on a table
+    // load; lane 0 issues the copies.
+    int* pg_phys = reinterpret_cast<int*>(sm + L::PG_OFF);   // [2][32]
+    int* pg_nval = pg_phys + 64;                              // [2][32]
+    ReqWalker lw = walk;
+    auto lookup = [&](int64_t gb, int& ph, int& nv) {
+      const int64_t g = gb + lane;
+      ph = 0;
+      nv = 0;
+      if (g < g1) {
+        lw.advance_to(g);
+        const int64_t j = g - lw.bstart;
+        const int64_t raw = p.block_table[static_cast<int64_t>(lw.b) * p.bt_stride + j];
         const bool bad = raw < 0 || raw >= p.num_blocks;
         if (bad) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
-        const int64_t phys = bad ? 0 : raw;
-        if (!waited && (wait_first || appended(phys))) {
-          griddep_wait();   // the step's append has written this block
-          waited = true;
-        }
-        const int64_t left = walk.len() - j * kBlockSize;
-        const int nvalid = bad ? 0 : static_cast<int>(left < kBlockSize ? left : kBlockSize);
-        const int ks = static_cast<int>(it % KST);
-        if (it >= KST && !mbar_wait(&kempty[ks], ((it / KST) - 1) & 1, abort_flag, p.dev_err)) break;
-        kinfo[ks] = nvalid;
-        if constexpr (SKIP) kphys[ks] = static_cast<int>(phys);
-        mbar_arrive_expect_tx(&kfull[ks], L::KP);
-        if constexpr (KSWZ) {
-          constexpr int ROWS = S::H * kBlockSize;   // key rows of a page
+        ph = bad ? 0 : static_cast<int>(raw);
+        const int64_t left = lw.len() - j * kBlockSize;
+        nv = bad ? 0 : static_cast<int>(left < kBlockSize ? left : kBlockSize);
+      }
+    };
+    {
+      int ph, nv;
+      lookup(g0, ph, nv);
+      pg_phys[lane] = ph;
+      pg_nval[lane] = nv;
+    }
+    __syncwarp();
+    const uint64_t pol = policy_evict_first();
+    const uint8_t* kpages = static_cast<const uint8_t*>(p.k_pages);
+    int64_t nk = 0, nv = 0;
+    bool waited = !step;
+    bool stop = false;
+    for (int64_t c0 = g0, batch = 0; c0 < g1 && !stop; c0 += 32, ++batch) {
+      int ph_n = 0, nv_n = 0;   // the next batch: loads in flight while lane 0 copies
+      if (c0 + 32 < g1) lookup(c0 + 32, ph_n, nv_n);
+      if (lane == 0) {
+        const int cnt = static_cast<int>(g1 - c0 < 32 ? g1 - c0 : 32);
+        for (int i = 0; i < cnt; ++i) {
+          const int64_t it = c0 - g0 + i;
+          const int64_t phys = pg_phys[(batch & 1) * 32 + i];
+          const int nvalid = pg_nval[(batch & 1) * 32 + i];
+          if (!waited && (wait_first || appended(phys))) {
+            griddep_wait();   // the step's append has written this block
+            waited = true;
+          }
+          const int ks = static_cast<int>(it % KST);
+          if (it >= KST && !mbar_wait(&kempty[ks], ((it / KST) - 1) & 1, abort_flag, p.dev_err)) {
+            stop = true;
+            break;
+          }
+          kinfo[ks] = nvalid;
+          if constexpr (SKIP) kphys[ks] = static_cast<int>(phys);
+          mbar_arrive_expect_tx(&kfull[ks], L::KP);
+          if constexpr (KSWZ || TSC) {
+            constexpr int ROWS = S::H * kBlockSize;   // key rows of a page
+            constexpr int RB = TSC ? S::RK : S::RK * 2;   // bytes per row
 #pragma unroll
-          for (int half = 0; half < ROWS / 256; ++half)
-            tma_load_2d_hint(kst + ks * L::KPS + half * 256 * 128, &tmap_k, 0,
-                             static_cast<int32_t>(phys * ROWS + half * 256), &kfull[ks], pol);
-        } else {
-          bulk_g2s_hint(kst + ks * L::KPS, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
-        }
-        ++nk;
-        if constexpr (SKIP) continue;   // values wait until the page is known to be needed
-        const int vs = static_cast<int>(it % VRS);
-        if (it >= VRS && !mbar_wait(&vempty[vs], ((it / VRS) - 1) & 1, abort_flag, p.dev_err)) break;
-        vinfo[vs] = nvalid;
-        mbar_arrive_expect_tx(&vfull[vs], L::VP);
-        if constexpr (F8) {
-          // the page's [16][R] codes, contiguous
-          bulk_g2s_hint(vraw + vs * L::VPS, static_cast<const uint8_t*>(p.v_pages) + phys * L::VP,
-                        L::VP, &vfull[vs], pol);
-        } else {
+            for (int half = 0; half < ROWS / 256; ++half)
+              tma_load_2d_hint(kst + ks * L::KPS + half * 256 * RB, &tmap_k, 0,
+                               static_cast<int32_t>(phys * ROWS + half * 256), &kfull[ks], pol);
+          } else {
+            bulk_g2s_hint(kst + ks * L::KPS, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
+          }
+          ++nk;
+          if constexpr (SKIP) continue;   // values wait until the page is known to be needed
+          const int vs = static_cast<int>(it % VRS);
+          if (it >= VRS && !mbar_wait(&vempty[vs], ((it / VRS) - 1) & 1, abort_flag, p.dev_err)) {
+            stop = true;
+            break;
+          }
+          vinfo[vs] = nvalid;
+          mbar_arrive_expect_tx(&vfull[vs], L::VP);
+          if constexpr (F8) {
+            // the page's [16][R] codes, contiguous
+            bulk_g2s_hint(vraw + vs * L::VPS,
+                          static_cast<const uint8_t*>(p.v_pages) + phys * L::VP, L::VP,
+                          &vfull[vs], pol);
+          } else {
 #pragma unroll 1
-          for (int bx = 0; bx < S::NBOX; ++bx)
-            tma_load_2d_hint(vst + vs * S::VSTAGE_BYTES + bx * 2048, &tmap_v, bx * 64,
-                             static_cast<int32_t>(phys * kBlockSize), &vfull[vs], pol);
+            for (int bx = 0; bx < S::NBOX; ++bx)
+              tma_load_2d_hint(vst + vs * S::VSTAGE_BYTES + bx * 2048, &tmap_v, bx * 64,
+                               static_cast<int32_t>(phys * kBlockSize), &vfull[vs], pol);
+          }
+          ++nv;
         }
-        ++nv;
       }
-      if (*abort_flag) {   // let copies already in flight land before the CTA exits
-        for (int64_t i = (nk > KST ? nk - KST : 0); i < nk; ++i)
-          mbar_wait_drain(&kfull[i % KST], (i / KST) & 1);
-        for (int64_t i = (nv > VRS ? nv - VRS : 0); i < nv; ++i)
-          mbar_wait_drain(&vfull[i % VRS], (i / VRS) & 1);
-      }
+      stop = __shfl_sync(0xffffffffu, stop, 0);
+      __syncwarp();   // lane 0 has read this batch's slot before it is rewritten
+      pg_phys[((batch + 1) & 1) * 32 + lane] = ph_n;
+      pg_nval[((batch + 1) & 1) * 32 + lane] = nv_n;
+      __syncwarp();
+    }
+    if (lane == 0 && *abort_flag) {   // let copies already in flight land before the CTA exits
+      for (int64_t i = (nk > KST ? nk - KST : 0); i < nk; ++i)
+        mbar_wait_drain(&kfull[i % KST], (i / KST) & 1);
+      for (int64_t i = (nv > VRS ? nv - VRS : 0); i < nv; ++i)
+        mbar_wait_drain(&vfull[i % VRS], (i / VRS) & 1);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------------- MMA issuer
@@ -656,7 +839,50 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
           ++issued;
         }
       }
-      for (int64_t g = g0, it = 0; !SKIP && g < g1; ++g, ++it) {
+      // TSC: the scores of page it + 1 go out before the values of page it, so that the
+      // compute warps find the next page's scores ready when they finish this one
+      ReqWalker wsc = walk;   // the scoring MMAs' own walk, one page ahead
+      int64_t nseg = 0;       // segments whose scoring has started
+      auto issue_scores = [&](int64_t g, int64_t it) -> bool {
+        wsc.advance_to(g);
+        const bool first = (g == g0) || (g == wsc.bstart);
+        const bool last = (g == g1 - 1) || (g + 1 == wsc.bend);
+        if (first) ++nseg;
+        const int qb = static_cast<int>((nseg - 1) & 1);
+        const int ks = static_cast<int>(it % KST), sb = static_cast<int>(it & 1);
+        if (first && !mbar_wait(&qfull[qb], ((nseg - 1) >> 1) & 1, abort_flag, p.dev_err))
+          return false;
+        if (!mbar_wait(&kfull[ks], (it / KST) & 1, abort_flag, p.dev_err)) return false;
+        if (it >= 2 && !mbar_wait(&sfree[sb], ((it >> 1) - 1) & 1, abort_flag, p.dev_err))
+          return false;
+        sinfo[sb] = kinfo[ks];
+        mbar_arrive(&sfull[sb]);
+        tc_fence_after();
+        constexpr uint32_t idesc_s = make_idesc_f16(128, 32, false, false);   // E4M3 = format 0
+        const uint32_t kaddr = smem_u32(kst + ks * L::KPS);
+        const uint32_t qaddr = smem_u32(qop);
+#pragma unroll
+        for (int gi = 0; gi < S::H / 8; ++gi) {
+#pragma unroll
+          for (int kk = 0; kk < S::RK / 32; ++kk) {
+            const uint64_t adesc =
+                make_sdesc(kaddr + gi * 128 * S::RK + kk * 32, 16, 512, kSwizzle64B);
+            const uint64_t bdesc =
+                make_sdesc(qaddr + gi * 32 * S::RK + kk * 256, 128, 512, kSwizzleNone);
+            umma_f8(tmem_base + L::SCOL + sb * (S::H / 8) * 32 + gi * 32, adesc, bdesc, idesc_s,
+                    kk > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&sfull[sb]);
+        umma_commit(&kempty[ks]);
+        if (last) umma_commit(&qfree[qb]);
+        return true;
+      };
+      bool run = true;
+      if constexpr (TSC) run = g0 < g1 && issue_scores(g0, 0);
+      for (int64_t g = g0, it = 0; !SKIP && run && g < g1; ++g, ++it) {
+        if constexpr (TSC)
+          if (g + 1 < g1 && !issue_scores(g + 1, it + 1)) break;
         walk.advance_to(g);
         const bool seg_first = (g == g0) || (g == walk.bstart);
         const int vs = static_cast<int>(it % VST), ps = static_cast<int>(it & 1);
@@ -704,13 +930,40 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   } else if (F8 && warp >= 2 + NCW) {
     // ------------------------------------------ F8: widen E4M3 V pages to fp16 stages
     // boxes [0, WB) here; the compute warps widen the rest after writing P
-    const int vt = threadIdx.x - 32 * (2 + NCW);   // 0..63
+    const int vt = threadIdx.x - 32 * (2 + NCW);   // 0 .. 32 NWW - 1
+    const bool q_builder = vt < 64;                  // TSC: warps NCW+2, NCW+3
+    ReqWalker wq = walk;   // TSC: these warps also write each segment's query operand
+    int64_t nseg = 0;
+    bool q_ready = false;
     for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
+      if constexpr (TSC) {
+        wq.advance_to(g);
+        if (q_builder && (g == g0 || g == wq.bstart)) {
+          ++nseg;
+          const int qb = static_cast<int>((nseg - 1) & 1);
+          // the previous segment's scoring MMAs have read the operand, and the compute
+          // warps hold its score factors (qfree of segment nseg - 2)
+          const int64_t prev = nseg - 2;
+          bool ok = prev < 0 ||
+                    mbar_wait(&qfree[prev & 1], (prev >> 1) & 1, abort_flag, p.dev_err);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          if (!q_ready) {
+            griddep_wait();   // the rank-space queries of the launch ahead are written
+            q_ready = true;
+          }
+          build_query_operand<S>(p.qt + static_cast<size_t>(wq.b) * S::H * S::RK, qop,
+                                 qinv + qb * S::H, vt);
+          fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qfull[qb]);
+        }
+      }
       const int vr = static_cast<int>(it % VRS), vs = static_cast<int>(it % VST);
       bool ok = mbar_wait(&vfull[vr], (it / VRS) & 1, abort_flag, p.dev_err);
       if (it >= VST) ok = mbar_wait(&vfree[vs], ((it / VST) - 1) & 1, abort_flag, p.dev_err) && ok;
       if (!__all_sync(0xffffffffu, ok)) break;
-      widen_v_boxes<S, FMT, 64>(vraw + vr * L::VPS, vst + vs * S::VSTAGE_BYTES, vinfo[vr], 0, WB, vt);
+      widen_v_boxes<S, FMT, 32 * NWW>(vraw + vr * L::VPS, vst + vs * S::VSTAGE_BYTES, vinfo[vr], 0,
+                                      WB, vt);
       fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
       __syncwarp();
       if (lane == 0) {
@@ -738,7 +991,14 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     const float4* qs4 = reinterpret_cast<const float4*>(qs);
     // warp cw takes heads cw*HPW .., two per round (one per half-warp)
     auto head_ok = [&](int r) { return 2 * r + hl < HPW; };
-    auto head_of = [&](int r) { return cw * HPW + 2 * r + hl; };
+    // TSC: a warp reads the score rows of its TMEM lane quarter: heads 8 gi + 2 quarter +
+    // (0, 1) of groups gi = (cw / 4) ROUNDS + r
+    auto head_of = [&](int r) {
+      return TSC ? 8 * ((cw / 4) * ROUNDS + r) + 2 * quarter + hl : cw * HPW + 2 * r + hl;
+    };
+    static_assert(!TSC || S::H == 8 * ROUNDS * (NCW / 4), "tensor scoring head split");
+    float qf[ROUNDS];   // TSC: the segment's score factors 2^-e_h of this lane's heads
+    int64_t nseg_c = 0;
     int64_t kk = 0;     // pages accumulated so far (SKIP: the kept ones), orders P / V use
     int64_t nd = 0;     // SKIP: decisions posted to the value-copy warp
     bool aborted = false;
@@ -750,7 +1010,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
       bi.seg_first = (g == g0) || (g == walk.bstart);
       bi.seg_last = (g == g1 - 1) || (g + 1 == walk.bend);
       bool ok = true;
-      if (bi.seg_first) {
+      if (!TSC && bi.seg_first) {
         // rank-space query of this request into the permuted layout
         // qs[((h*2 + hi)*NCH + c)*4 + e] = q~[h][8c + 4hi + e]: four consecutive ranks
         // stay together, so it moves as float4, every load issued before the first store
@@ -773,10 +1033,46 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
         named_bar_sync(1, CT);
       }
       const int ks = static_cast<int>(it % KST);
+      float s[ROUNDS];
+      int kph = 0;
+      if constexpr (TSC) {
+        // scores from the tensor cores: per round one 8-column load (this lane quarter's
+        // head pair: term-major, head parity minor)
+        const int sb = static_cast<int>(it & 1);
+        ok = mbar_wait(&sfull[sb], (it >> 1) & 1, abort_flag, p.dev_err);
+        ok = __all_sync(0xffffffffu, ok);   // TMEM loads are warp-collective
+        bi.nvalid = ok ? sinfo[sb] : 0;
+        if (bi.seg_first) {
+          ++nseg_c;
+          const int qb = static_cast<int>((nseg_c - 1) & 1);
+#pragma unroll
+          for (int r = 0; r < ROUNDS; ++r) qf[r] = qinv[qb * S::H + head_of(r)];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qfree[qb]);
+        }
+        tc_fence_after();
+        float v[ROUNDS][8];
+        if (ok) {
+#pragma unroll
+          for (int r = 0; r < ROUNDS; ++r)
+            tmem_ld8(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + L::SCOL +
+                         sb * (S::H / 8) * 32 + ((cw / 4) * ROUNDS + r) * 32 + quarter * 8,
+                     v[r]);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int r = 0; r < ROUNDS; ++r) {
+          const float a = hl ? v[r][1] : v[r][0], b = hl ? v[r][3] : v[r][2];
+          const float c = hl ? v[r][5] : v[r][4], d = hl ? v[r][7] : v[r][6];
+          s[r] = ok ? ((a + b) + (c + d)) * qf[r] : -INFINITY;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfree[sb]);
+      } else {
       ok = mbar_wait(&kfull[ks], (it / KST) & 1, abort_flag, p.dev_err);
       bi.nvalid = kinfo[ks];
-      const int kph = SKIP ? kphys[ks] : 0;
-      float s[ROUNDS];
+      if constexpr (SKIP) kph = kphys[ks];
 #pragma unroll
       for (int r = 0; r < ROUNDS; ++r) {
         s[r] = -INFINITY;
@@ -868,6 +1164,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&kempty[ks]);
+      }   // scores on the CUDA cores
 
       // online softmax (base 2), lazy rescale: the reference max only moves when a block
       // max exceeds it by more than kRescaleThreshold, so the accumulator is rarely touched
@@ -1107,7 +1404,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::TMEM_COLS);
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
 }
 
