@@ -40,6 +40,7 @@ RAGGED = None           # (lo, hi): per-sequence lengths uniform in [lo, hi] ins
 PEAKED = False          # peaked-attention pages and queries (workloads.PEAKED)
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_b64_l8192.md")
 SPARSE_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_sparse_b64_l8192_peaked.md")
+E4M3_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_e4m3_b64_l8192.md")
 KERNEL_SRC = os.path.join(ROOT, "rank_compressed_paged_gb300", "csrc", "decode.cu")
 
 
@@ -509,6 +510,9 @@ def measure_decode_config(dev, stream, steps, warmup, shape_name, batch, seq=Non
            "kernel_frac_of_8TBps": round(coeff / (kern_ms * 1e-3) / 8e12, 4),
            "pv_tflops_kernel": round(decode_step_flops(w["seq_lens"], shape=shape)["pv"] /
                                      (kern_ms * 1e-3) / 1e12, 2)}
+    if (shape_name, batch, seq, ragged, pages) == ("mha32", 64, 8192, None, "fp8_e4m3"):
+        # DRAM bytes per launch from the committed ncu summary of this kernel source
+        res["traffic"] = ncu_traffic_per_launch(E4M3_PROFILE_SUMMARY)
     del cache, t, w
     torch.cuda.empty_cache()
     return res
@@ -669,6 +673,9 @@ def run_ours(args, rank, world, local_rank):
             traffic = ncu_traffic_per_launch()
         elif args.sparse == 2.0 ** -8 and PEAKED:
             traffic = ncu_traffic_per_launch(SPARSE_PROFILE_SUMMARY)
+    elif (args.pages == "fp8_e4m3" and not RAGGED and BATCH == 64 and SEQ == 8192 and
+          not PEAKED):
+        traffic = ncu_traffic_per_launch(E4M3_PROFILE_SUMMARY)
     if configs is not None:
         configs["C2_b64_l8192_append"] = {
             "see": "headline keys (value, us_per_step, roofline)", "us_per_step":
@@ -723,8 +730,10 @@ def run_ours(args, rank, world, local_rank):
         "contraction": {"flops_per_step": flops,
                         "tflops_step": round(world * flops["total"] / (step_ms * 1e-3) / 1e12, 2),
                         "pv_tflops_kernel": round(flops["pv"] / (kern_ms * 1e-3) / 1e12, 2),
-                        "note": "P*C_v on tcgen05 (fp16 in, fp32 accumulation); scores on CUDA "
-                                "cores; query / output projections and the append on tcgen05"},
+                        "note": "P*C_v on tcgen05 (fp16 in, fp32 accumulation); scores on " +
+                                ("tcgen05 (E4M3 keys x a four-term E4M3 query split)"
+                                 if args.pages == "fp8_e4m3" else "CUDA cores") +
+                                "; query / output projections and the append on tcgen05"},
         "sparse": sparse,
         "gpu_launches": args.steps * LAUNCHES_PER_DECODE_STEP,
         "clocks": clk.summary(),
