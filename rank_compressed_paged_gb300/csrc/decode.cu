@@ -193,15 +193,20 @@ constexpr int kAppendSetSize = 1 << kAppendSetBits;   // a step appending more t
 // before: 2^-16 relative after four terms, down to E4M3's subnormal step).  The 32 columns
 // of a group's result are 8 per head pair: (term, head parity); a key row's score is the
 // sum of its head's four columns times 2^-e_h.
+// 4-bit pages take the same path: the widening warps first write each key page's codes as
+// E4M3 values (integers in [-7, 7] are exact in E4M3) in the same 64-byte swizzled layout,
+// and a key row's score is further multiplied by the row's scale.
 template <class S, int FMT, bool SKIP>
 constexpr bool decode_tensor_scores() {
-  return FMT == RCP_PAGES_FP8_E4M3 && S::RK == 64 && S::H % 16 == 0 && !SKIP;
+  return (FMT == RCP_PAGES_FP8_E4M3 || FMT == RCP_PAGES_INT4) && S::RK == 64 &&
+         S::H % 16 == 0 && !SKIP;
 }
 
 template <class S, int FMT, bool SKIP = false>
 struct DecodeSmem {
   static constexpr bool F8 = FMT != RCP_PAGES_FP16;                 // raw quantized pages
   static constexpr bool TSC = decode_tensor_scores<S, FMT, SKIP>();
+  static constexpr bool I4T = TSC && FMT == RCP_PAGES_INT4;         // 4-bit keys widened
   static constexpr int DS = 4;                                      // SKIP: decision ring
   static constexpr int KST = F8 && !TSC ? 3 : 2;                    // key page stages
   static constexpr int VST = 2;                                     // fp16 V stages (MMA A)
@@ -212,15 +217,20 @@ struct DecodeSmem {
   static constexpr int VP = FMT == RCP_PAGES_FP8_E4M3 ? S::VPAGE_BYTES / 2   // bytes per V page
                            : FMT == RCP_PAGES_INT4 ? static_cast<int>(Int4Page<S>::VBYTES)
                                                    : S::VPAGE_BYTES;
-  static constexpr int KPS = (KP + 127) & ~127;                     // stage strides
+  // stage strides; I4T: the key stages hold the widened E4M3 operand, the raw 4-bit pages
+  // land in KST raw stages of their own
+  static constexpr int OPB = S::H * kBlockSize * S::RK;             // E4M3 key operand
+  static constexpr int KRPS = (KP + 127) & ~127;
+  static constexpr int KPS = I4T ? OPB : KRPS;
   static constexpr int VPS = (VP + 127) & ~127;
   static constexpr int NBAR = 2 * KST + 2 * VRS + 4 + (F8 ? 2 * VST : 0) + (SKIP ? 2 * DS : 0) +
-                              (TSC ? 8 : 0);
+                              (TSC ? 8 : 0) + (I4T ? 2 * KST : 0);
   static constexpr int P_BYTES = S::HP * 16 * 2;
   static constexpr int V_OFF = 0;                                   // 1024-aligned stages
   static constexpr int K_OFF = V_OFF + VST * S::VSTAGE_BYTES;
-  static constexpr int VR_OFF = K_OFF + KST * KPS;                  // raw E4M3 V stages
-  static constexpr int P_OFF = VR_OFF + (F8 ? VRS * VPS : 0);
+  static constexpr int VR_OFF = K_OFF + KST * KPS;                  // raw quantized V stages
+  static constexpr int KR_OFF = VR_OFF + (F8 ? VRS * VPS : 0);      // I4T: raw key stages
+  static constexpr int P_OFF = KR_OFF + (I4T ? KST * KRPS : 0);
   static constexpr int Q_OFF = P_OFF + 2 * P_BYTES;
   // TSC: the query operand ([H/8 groups][32 rows][r_k] E4M3, K-major without swizzle:
   // 8-row x 16-byte core matrices, 128 bytes apart along K, 512 along the rows; one buffer,
@@ -228,14 +238,16 @@ struct DecodeSmem {
   // 2^-e_h per segment parity [2][H]; otherwise q~ in fp32
   static constexpr int QOP_BYTES = (S::H / 8) * 32 * S::RK;
   static constexpr int Q_BYTES = TSC ? QOP_BYTES + 2 * S::H * 4 : S::H * S::RK * 4;
-  static constexpr int A_OFF = Q_OFF + Q_BYTES;                     // alpha[2][HP]
+  // I4T: the key-row scales of the page in each score buffer [2][H][16] (fp32)
+  static constexpr int KSC_OFF = Q_OFF + Q_BYTES;
+  static constexpr int A_OFF = KSC_OFF + (I4T ? 2 * S::H * kBlockSize * 4 : 0);   // alpha[2][HP]
   static constexpr int F_OFF = A_OFF + 2 * S::HP * 4;               // flags[2][4]
   static constexpr int BAR_OFF = F_OFF + 64;                        // NBAR mbarriers
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;               // tmem slot, abort flag
   static constexpr int INFO_OFF = MISC_OFF + 16;                    // valid tokens per stage:
   // K stages, then V; SKIP adds the physical block of each K stage, the decision ring and
   // the info word of each P buffer; TSC the valid tokens of each score buffer
-  static constexpr int INFO_BYTES = (2 * KST + VRS + DS + 4) * 4;
+  static constexpr int INFO_BYTES = (2 * KST + VRS + DS + 4 + KST) * 4;   // + I4T operand stages
   // TMEM: the value accumulator [NCHUNK x 128 lanes][HP], then (TSC) two score buffers of
   // H/8 groups x 32 columns
   static constexpr int SCOL = S::NCHUNK * S::HP;
@@ -257,6 +269,7 @@ struct DecodeSmem {
   static_assert(TMEM_COLS <= 512, "tensor memory");
   static_assert(!TSC || (K_OFF % 512 == 0 && KPS % 512 == 0 && Q_OFF % 16 == 0),
                 "64-byte swizzled key stages, query operands");
+  static_assert(!I4T || (KR_OFF % 16 == 0 && KSC_OFF % 16 == 0), "raw key stages, scales");
 };
 
 // Warp 0 copies, warp 1 issues the MMAs, warps 2 .. compute.
@@ -336,6 +349,37 @@ __device__ __forceinline__ void widen_v_e4m3_pairs(const uint8_t* src, uint8_t* 
   }
 }
 
+// 4-bit pages, an even number of boxes: as widen_v_boxes below, in units of 16 codes (8 code
+// bytes, one scale), mapped to lanes like widen_v_e4m3_pairs.
+template <class S, int NT>
+__device__ __forceinline__ void widen_v_int4_pairs(const uint8_t* src, uint8_t* vb, int nvalid,
+                                                   int b0, int b1, int tid) {
+  const int n = (b1 - b0) * kBlockSize * 4;
+  const __half* scales = reinterpret_cast<const __half*>(src + Int4Page<S>::VCODES);
+#pragma unroll 8   // measured: 2 -> 652 us, 4 -> 885 us, 8 -> 588 us at batch 64 x 8192
+  for (int idx = tid; idx < n; idx += NT) {
+    const int c16 = idx & 3, gl = (idx >> 2) & 1, tl = (idx >> 3) & 3, th = (idx >> 5) & 3;
+    const int tt = th * 4 + tl, gb = b0 + (idx >> 7) * 2 + gl;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (tt < nvalid) {
+      const uint2 raw =
+          *reinterpret_cast<const uint2*>(src + tt * (S::R / 2) + gb * 32 + c16 * 8);
+      const __half2 sc = __half2half2(scales[tt * (S::R / 64) + gb]);
+      lo.x = int4x2_to_half2_bits(raw.x & 0xFFu, sc);
+      lo.y = int4x2_to_half2_bits((raw.x >> 8) & 0xFFu, sc);
+      lo.z = int4x2_to_half2_bits((raw.x >> 16) & 0xFFu, sc);
+      lo.w = int4x2_to_half2_bits(raw.x >> 24, sc);
+      hi.x = int4x2_to_half2_bits(raw.y & 0xFFu, sc);
+      hi.y = int4x2_to_half2_bits((raw.y >> 8) & 0xFFu, sc);
+      hi.z = int4x2_to_half2_bits((raw.y >> 16) & 0xFFu, sc);
+      hi.w = int4x2_to_half2_bits(raw.y >> 24, sc);
+    }
+    uint8_t* row = vb + gb * 2048 + tt * 128;
+    *reinterpret_cast<uint4*>(row + (((2 * c16) ^ (tt & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ (tt & 7)) << 4)) = hi;
+  }
+}
+
 // Widens boxes [b0, b1) (64 columns each) of a quantized V page (E4M3: [16][R] codes at src;
 // 4-bit: [16][R/2] code bytes then the fp16 scales [16][R/64]) into the fp16 stage vb in
 // the layout of the value MMA: box g at g * 2048, token row t at t * 128, 16-byte chunk c
@@ -347,6 +391,10 @@ __device__ __forceinline__ void widen_v_boxes(const uint8_t* src, uint8_t* vb, i
                                               int b1, int tid) {
   if constexpr (FMT == RCP_PAGES_FP8_E4M3 && S::NBOX % 2 == 0) {
     widen_v_e4m3_pairs<S, NT>(src, vb, nvalid, b0, b1, tid);
+    return;
+  }
+  if constexpr (FMT == RCP_PAGES_INT4 && S::NBOX % 2 == 0) {
+    widen_v_int4_pairs<S, NT>(src, vb, nvalid, b0, b1, tid);
     return;
   }
   const int n = (b1 - b0) * kBlockSize * 8;
@@ -374,6 +422,50 @@ __device__ __forceinline__ void widen_v_boxes(const uint8_t* src, uint8_t* vb, i
     }
     *reinterpret_cast<uint4*>(vb + gb * 2048 + tt * 128 + ((c ^ (tt & 7)) << 4)) = o;
   }
+}
+
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// Four 4-bit codes (two's complement; code i in nibble i of x's low 16 bits) as four E4M3
+// bytes.  A byte permutation looks up the code's low three bits in the table of E4M3 values
+// 0..7 and in that of -8..-1; a third, in its sign-replicating mode (selector bit 3 = the
+// code's sign bit), marks the negative codes, and the mark picks the second table's byte.
+__device__ __forceinline__ uint32_t int4x4_to_e4m3x4(uint32_t x) {
+  const uint32_t sel = x & 0x7777u;
+  const uint32_t pos = prmt_b32(0x44403800u, 0x4E4C4A48u, sel);   // 0, 1, 2, .. 7
+  const uint32_t neg = prmt_b32(0xCACCCED0u, 0xB8C0C4C8u, sel);   // -8, -7, .. -1
+  const uint32_t m7 = prmt_b32(0x80808080u, 0x80808080u, x) & 0x7F7F7F7Fu;   // 0x7F: negative
+  const uint32_t m = m7 | (m7 << 1);                               // 0xFF: negative
+  return (pos & ~m) | (neg & m);
+}
+
+// I4T: one 4-bit key page (raw: codes [H][16][r_k / 2] then fp16 scales [H][16]) widened to
+// the E4M3 scoring operand op (row r = h * 16 + t, 64 bytes, 16-byte chunk c at c ^ ((r / 2)
+// % 4): the layout a 64-byte swizzled tensor copy writes) and its scales to ksc [H][16] fp32.
+// NT threads; a unit is 16 code bytes (half a row).
+template <class S, int NT>
+__device__ __forceinline__ void widen_k_int4(const uint8_t* raw, uint8_t* op, float* ksc,
+                                             int tid) {
+  static_assert(S::RK == 64, "rows of 32 code bytes");
+  constexpr int UNITS = S::H * kBlockSize * 2;
+#pragma unroll 8
+  for (int u = tid; u < UNITS; u += NT) {
+    const int r = u >> 1, half = u & 1;
+    const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 32 + half * 16);
+    const uint4 lo = make_uint4(int4x4_to_e4m3x4(w.x), int4x4_to_e4m3x4(w.x >> 16),
+                                int4x4_to_e4m3x4(w.y), int4x4_to_e4m3x4(w.y >> 16));
+    const uint4 hi = make_uint4(int4x4_to_e4m3x4(w.z), int4x4_to_e4m3x4(w.z >> 16),
+                                int4x4_to_e4m3x4(w.w), int4x4_to_e4m3x4(w.w >> 16));
+    uint8_t* row = op + r * 64;
+    const int sw = (r >> 1) & 3;
+    *reinterpret_cast<uint4*>(row + (((2 * half) ^ sw) << 4)) = lo;
+    *reinterpret_cast<uint4*>(row + (((2 * half + 1) ^ sw) << 4)) = hi;
+  }
+  const __half* sc = reinterpret_cast<const __half*>(raw + Int4Page<S>::KCODES);
+  for (int i = tid; i < S::H * kBlockSize; i += NT) ksc[i] = __half2float(sc[i]);
 }
 
 // TSC: the query operand of one request (q: its q~ [H][r_k] fp32) and its score factors
@@ -480,7 +572,8 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   // head read the same logical chunk, conflict-free on the keys and as a broadcast on q~
   constexpr bool KSWZ = !F8 && S::RK == 64;
   using L = DecodeSmem<S, FMT, SKIP>;
-  constexpr bool TSC = L::TSC;   // keys scored on the tensor cores (E4M3 pages)
+  constexpr bool TSC = L::TSC;   // keys scored on the tensor cores (E4M3 or 4-bit pages)
+  constexpr bool I4T = L::I4T;   // 4-bit keys widened to E4M3 first
   constexpr int KST = L::KST, VST = L::VST, VRS = L::VRS, HP = S::HP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -488,6 +581,8 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   uint8_t* vst = sm + L::V_OFF;
   uint8_t* kst = sm + L::K_OFF;
   uint8_t* vraw = sm + L::VR_OFF;
+  uint8_t* kraw = sm + L::KR_OFF;                                     // I4T raw key stages
+  float* ksc = reinterpret_cast<float*>(sm + L::KSC_OFF);             // I4T [2][H][16]
   uint8_t* pbuf = sm + L::P_OFF;
   float* qs = reinterpret_cast<float*>(sm + L::Q_OFF);
   uint8_t* qop = sm + L::Q_OFF;                                              // TSC [2]
@@ -509,6 +604,8 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   uint64_t* sfree = sfull + 2;                           // TSC [2] ... and were read
   uint64_t* qfull = sfree + 2;                           // TSC [2] a segment's query operand
   uint64_t* qfree = qfull + 2;                           // TSC [2] ... its MMAs completed
+  uint64_t* kopfull = qfree + 2;                         // I4T [KST] widened key operand
+  uint64_t* kopempty = kopfull + KST;                    // I4T [KST] ... its MMAs completed
   constexpr int NTHR = decode_threads<S, FMT, SKIP>();
   constexpr int NCW = decode_compute_warps<S, FMT, SKIP>();   // compute warps 2 .. NCW+1
   // F8: V boxes widened by warps 10-11; the compute warps widen the remaining ones (a
@@ -529,6 +626,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   int* dec_s = kphys + KST;
   int* pinfo = dec_s + L::DS;
   int* sinfo = pinfo + 2;   // TSC: valid tokens of the page in each score buffer
+  int* oinfo = sinfo + 2;   // I4T: valid tokens of the page in each operand stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -537,7 +635,12 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < KST; ++i) {
       mbar_init(&kfull[i], 1);
-      mbar_init(&kempty[i], TSC ? 1 : NCW);   // TSC: the scoring MMAs' commit
+      // TSC: the scoring MMAs' commit; I4T: the widening warps (raw stage)
+      mbar_init(&kempty[i], I4T ? NWW : TSC ? 1 : NCW);
+      if constexpr (I4T) {
+        mbar_init(&kopfull[i], NWW);
+        mbar_init(&kopempty[i], 1);
+      }
     }
     if constexpr (TSC) {
       for (int i = 0; i < 2; ++i) {
@@ -767,7 +870,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
           kinfo[ks] = nvalid;
           if constexpr (SKIP) kphys[ks] = static_cast<int>(phys);
           mbar_arrive_expect_tx(&kfull[ks], L::KP);
-          if constexpr (KSWZ || TSC) {
+          if constexpr (KSWZ || (TSC && !I4T)) {
             constexpr int ROWS = S::H * kBlockSize;   // key rows of a page
             constexpr int RB = TSC ? S::RK : S::RK * 2;   // bytes per row
 #pragma unroll
@@ -775,7 +878,8 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
               tma_load_2d_hint(kst + ks * L::KPS + half * 256 * RB, &tmap_k, 0,
                                static_cast<int32_t>(phys * ROWS + half * 256), &kfull[ks], pol);
           } else {
-            bulk_g2s_hint(kst + ks * L::KPS, kpages + phys * L::KP, L::KP, &kfull[ks], pol);
+            bulk_g2s_hint(I4T ? kraw + ks * L::KRPS : kst + ks * L::KPS, kpages + phys * L::KP,
+                          L::KP, &kfull[ks], pol);
           }
           ++nk;
           if constexpr (SKIP) continue;   // values wait until the page is known to be needed
@@ -852,10 +956,11 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
         const int ks = static_cast<int>(it % KST), sb = static_cast<int>(it & 1);
         if (first && !mbar_wait(&qfull[qb], ((nseg - 1) >> 1) & 1, abort_flag, p.dev_err))
           return false;
-        if (!mbar_wait(&kfull[ks], (it / KST) & 1, abort_flag, p.dev_err)) return false;
+        if (!mbar_wait(I4T ? &kopfull[ks] : &kfull[ks], (it / KST) & 1, abort_flag, p.dev_err))
+          return false;
         if (it >= 2 && !mbar_wait(&sfree[sb], ((it >> 1) - 1) & 1, abort_flag, p.dev_err))
           return false;
-        sinfo[sb] = kinfo[ks];
+        sinfo[sb] = I4T ? oinfo[ks] : kinfo[ks];
         mbar_arrive(&sfull[sb]);
         tc_fence_after();
         constexpr uint32_t idesc_s = make_idesc_f16(128, 32, false, false);   // E4M3 = format 0
@@ -874,7 +979,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
           }
         }
         umma_commit(&sfull[sb]);
-        umma_commit(&kempty[ks]);
+        umma_commit(I4T ? &kopempty[ks] : &kempty[ks]);
         if (last) umma_commit(&qfree[qb]);
         return true;
       };
@@ -956,6 +1061,25 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
           fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
           __syncwarp();
           if (lane == 0) mbar_arrive(&qfull[qb]);
+        }
+      }
+      if constexpr (I4T) {
+        // this page's key codes as the E4M3 scoring operand, once the raw page landed, the
+        // operand stage's MMAs completed and the compute warps read the scales two pages ago
+        const int ks = static_cast<int>(it % KST), sb = static_cast<int>(it & 1);
+        bool kok = mbar_wait(&kfull[ks], (it / KST) & 1, abort_flag, p.dev_err);
+        if (it >= KST)
+          kok = mbar_wait(&kopempty[ks], ((it / KST) - 1) & 1, abort_flag, p.dev_err) && kok;
+        if (it >= 2) kok = mbar_wait(&sfree[sb], ((it >> 1) - 1) & 1, abort_flag, p.dev_err) && kok;
+        if (!__all_sync(0xffffffffu, kok)) break;
+        widen_k_int4<S, 32 * NWW>(kraw + ks * L::KRPS, kst + ks * L::KPS,
+                                  ksc + sb * S::H * kBlockSize, vt);
+        if (vt == 0) oinfo[ks] = kinfo[ks];
+        fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&kempty[ks]);    // the raw page may be overwritten
+          mbar_arrive(&kopfull[ks]);   // the operand is ready
         }
       }
       const int vr = static_cast<int>(it % VRS), vs = static_cast<int>(it % VST);
@@ -1065,6 +1189,8 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
           const float a = hl ? v[r][1] : v[r][0], b = hl ? v[r][3] : v[r][2];
           const float c = hl ? v[r][5] : v[r][4], d = hl ? v[r][7] : v[r][6];
           s[r] = ok ? ((a + b) + (c + d)) * qf[r] : -INFINITY;
+          if constexpr (I4T)   // the key row's scale
+            s[r] *= ksc[sb * S::H * kBlockSize + head_of(r) * kBlockSize + t];
         }
         tc_fence_before();
         __syncwarp();
