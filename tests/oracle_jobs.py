@@ -26,6 +26,19 @@ def decode_request(job):
     return orc.decode_attn(q, kp, vp, U, W, tab, np.array([L], np.int32), 16)
 
 
+def decode_request_quantized(job):
+    """job: (q [1][H][d], K page bytes, V page bytes, U, W, L, page format): the oracle
+    decodes the bytes (E4M3 codes, or 4-bit codes with their scales) and attends them."""
+    q, kb, vb, U, W, L, fmt = job
+    if fmt == "fp8_e4m3":
+        kp, vp = orc.e4m3_decode(kb), orc.e4m3_decode(vb)
+    else:
+        H, rk, R = U.shape[0], U.shape[1], W.shape[0]
+        kp, vp = orc.int4_page_coefficients(kb, vb, H, rk, R)
+    tab = np.arange(kp.shape[0], dtype=np.int32)[None]
+    return orc.decode_attn(q, kp, vp, U, W, tab, np.array([L], np.int32), 16)
+
+
 def prefill_request(job):
     """job: (q, k, v rows of the chunk, kp, vp, U, W, prior, chunk): the chunk is appended
     at positions prior .. prior + chunk - 1, then the chunk's rows attend causally."""

@@ -11,7 +11,7 @@ import pytest
 
 import workloads as wl
 from tests.gpu_util import assert_close, t
-from tests.oracle_jobs import decode_request, prefill_request, run_pool
+from tests.oracle_jobs import decode_request, decode_request_quantized, prefill_request, run_pool
 
 pytestmark = pytest.mark.gpu
 
@@ -76,6 +76,46 @@ def test_decode_b20_l32768_every_request():
 def test_decode_ragged64_every_request():
     lens = wl.ragged_lengths(np.random.default_rng(1003), 64, 128, 16384)
     _decode_every_request(lens, 1013, append=False)
+
+
+@pytest.mark.parametrize("pages", ["fp8_e4m3", "int4"])
+def test_quantized_decode_b64_l8192_every_request(pages):
+    """E4M3 and 4-bit pages at the batch-64 x 8192 size: the seeded fp16 pages are encoded
+    by torch casts (E4M3) or the benchmark's torch encoder (4-bit), the GPU decodes them in
+    the benchmark's launch configuration, and the oracle decodes every request from host
+    copies of the same bytes."""
+    import torch
+    import bench
+    from rank_compressed_paged_gb300 import PagedCoeffCache
+    lens = np.full(64, 8192, np.int32)
+    kp, vp, table, lens = wl.make_paged_cache_device(lens, MAIN, 1102, device="cuda",
+                                                     spare_blocks=16)
+    if pages == "fp8_e4m3":
+        kq = kp.to(torch.float8_e4m3fn).view(torch.uint8)
+        vq = vp.to(torch.float8_e4m3fn).view(torch.uint8)
+    else:
+        kq, vq = bench.int4_pages_torch(kp, vp)
+    del kp, vp
+    torch.cuda.empty_cache()
+    rng = np.random.default_rng(1102)
+    U, W = wl.make_factors(rng, 32, 128, 64, 1024)
+    cache = PagedCoeffCache(32, 128, 64, 1024, kq.shape[0], t(U), t(W), k_pages=kq,
+                            v_pages=vq, page_format=pages)
+    B = len(lens)
+    q = wl.fp16(rng.standard_normal((B, 32, 128)))
+    out = cache.decode_attn(t(q), t(table), t(lens)).cpu().numpy()
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    jobs = []
+    for b in range(B):
+        ids = torch.from_numpy(table[b, :wl.blocks_needed(lens[b])].astype(np.int64)).cuda()
+        jobs.append((q[b:b + 1], cache.k_pages.index_select(0, ids).cpu().numpy(),
+                     cache.v_pages.index_select(0, ids).cpu().numpy(), U, W, int(lens[b]), pages))
+    del cache, kq, vq
+    torch.cuda.empty_cache()
+    refs = run_pool(decode_request_quantized, jobs)
+    for b, ref in enumerate(refs):
+        assert_close(out[b:b + 1], ref, what=f"{pages} request {b}")
 
 
 def test_prefill_b16_p4096_c256_every_request_both_variants():
