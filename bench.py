@@ -14,6 +14,7 @@ sequences (weak scaling, no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import contextlib
 import datetime
 import hashlib
 import json
@@ -116,7 +117,9 @@ def ncu_traffic_per_launch(summary=None):
 
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples (every 10 ms, each with its timestamp);
-    the summary keeps the samples taken while the timed region ran."""
+    the summary keeps the samples taken while the timed region ran.  Timed regions can be
+    marked (``with clk.region(): ...``); the summary then describes the first one and adds
+    the samples of all marked regions of the run."""
 
     def __init__(self, index: int):
         self.index = index
@@ -124,6 +127,15 @@ class ClockSampler:
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
         os.close(fd)
         self.t0 = self.t1 = None
+        self.regions = []
+
+    @contextlib.contextmanager
+    def region(self):
+        t0 = time.time()
+        try:
+            yield
+        finally:
+            self.regions.append((t0, time.time()))
 
     def __enter__(self):
         try:
@@ -171,18 +183,33 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = self._rows()
         os.unlink(self.path)
-        inside = [r for r in rows if self.t0 <= r[0] <= self.t1]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        regions = self.regions or [(self.t0, self.t1)]
+        t0, t1 = regions[0]
+
+        def stats(rs):
+            reasons = {n for r in rs for n, v in zip(names, r[3]) if v.lower() == "active"}
+            sm = [r[1] for r in rs]
+            return sm, reasons
+
+        inside = [r for r in rows if t0 <= r[0] <= t1]
         window = "timed region"
         if not inside:   # a region shorter than the sampling interval: nearest samples
-            inside = [r for r in rows if self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+            inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
             window = "timed region +- 50 ms"
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = {n for r in inside for n, v in zip(names, r[3]) if v.lower() == "active"}
-        sm = [r[1] for r in inside]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": inside[-1][2] if inside else None,
-                "reasons": sorted(reasons), "samples": len(sm), "window": window,
-                "region_s": round(self.t1 - self.t0, 3)}
+        sm, reasons = stats(inside)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": inside[-1][2] if inside else None,
+               "reasons": sorted(reasons), "samples": len(sm), "window": window,
+               "region_s": round(t1 - t0, 3)}
+        if len(regions) > 1:   # every timed region of the run (device, kernel, end to end)
+            allr = [r for r in rows if any(a <= r[0] <= b for a, b in regions)]
+            sm2, reasons2 = stats(allr)
+            out["all_timed_regions"] = {
+                "regions": len(regions), "seconds": round(sum(b - a for a, b in regions), 3),
+                "samples": len(sm2), "sm_mhz": statistics.median(sm2) if sm2 else None,
+                "sm_min_mhz": min(sm2) if sm2 else None, "reasons": sorted(reasons2)}
+        return out
 
 
 def workload_name():
@@ -554,7 +581,8 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
+    clk = ClockSampler(local_rank).__enter__()
+    with clk.region():
         s_start.record(stream)
         for _ in range(args.steps):
             step()
@@ -567,10 +595,11 @@ def run_ours(args, rank, world, local_rank):
     # (the library then launches it in plain stream order so the events bracket it)
     k_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     k_stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        cache.set_profile_events(k_starts[i], k_stops[i])
-        step()
-    torch.cuda.synchronize()
+    with clk.region():
+        for i in range(args.steps):
+            cache.set_profile_events(k_starts[i], k_stops[i])
+            step()
+        torch.cuda.synchronize()
     cache.set_profile_events(None, None)
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k_starts, k_stops))
     assert cache.read_device_error() == 0, cache.read_device_error()
@@ -611,11 +640,13 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with clk.region():
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    clk.__exit__(None, None, None)
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
     # ---- block-sparse decode: which pages the timed configuration reads (deterministic)

@@ -17,11 +17,13 @@
 //                   accumulator and the running (max, sum) go to a partial record.  The
 //                   copies start while launch A still runs: only the compute warps wait
 //                   for it (for q~), and the copy thread only before a page that a decode
-//                   step's own append writes.  Variants: E4M3 pages (codes widened to fp16
-//                   in shared memory) and block-sparse (a page's V is loaded only when some
-//                   head's weight in it reaches the threshold; "KV-cache LLM serving" page,
-//                   "What it measured", item 3).
-//   C. (gemm.cu)    the split-K combine, merging each request's records in a fixed order
+//                   step's own append writes.  Variants: E4M3 pages (keys scored on the
+//                   tensor cores, values widened to fp16 in shared memory by their own
+//                   warps), 4-bit pages (key nibbles widened to E4M3 codes first, then the
+//                   same), and block-sparse (a page's V is loaded only when some head's
+//                   weight in it reaches the threshold; "KV-cache LLM serving" page, "What
+//                   it measured", item 3).
+//   C. (combine.cu) the split-K combine, merging each request's records in a fixed order
 //                   (deterministic), fused with o_h = W_v[:, h*d:(h+1)*d]^T z_h on tensor
 //                   cores.
 //
