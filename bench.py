@@ -42,6 +42,7 @@ PEAKED = False          # peaked-attention pages and queries (workloads.PEAKED)
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_b64_l8192.md")
 SPARSE_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_sparse_b64_l8192_peaked.md")
 E4M3_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_e4m3_b64_l8192.md")
+INT4_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_main_int4_b64_l8192.md")
 KERNEL_SRC = os.path.join(ROOT, "rank_compressed_paged_gb300", "csrc", "decode.cu")
 
 
@@ -537,9 +538,10 @@ def measure_decode_config(dev, stream, steps, warmup, shape_name, batch, seq=Non
            "kernel_frac_of_8TBps": round(coeff / (kern_ms * 1e-3) / 8e12, 4),
            "pv_tflops_kernel": round(decode_step_flops(w["seq_lens"], shape=shape)["pv"] /
                                      (kern_ms * 1e-3) / 1e12, 2)}
-    if (shape_name, batch, seq, ragged, pages) == ("mha32", 64, 8192, None, "fp8_e4m3"):
+    if (shape_name, batch, seq, ragged) == ("mha32", 64, 8192, None) and pages != "fp16":
         # DRAM bytes per launch from the committed ncu summary of this kernel source
-        res["traffic"] = ncu_traffic_per_launch(E4M3_PROFILE_SUMMARY)
+        res["traffic"] = ncu_traffic_per_launch(
+            E4M3_PROFILE_SUMMARY if pages == "fp8_e4m3" else INT4_PROFILE_SUMMARY)
     del cache, t, w
     torch.cuda.empty_cache()
     return res
@@ -704,9 +706,9 @@ def run_ours(args, rank, world, local_rank):
             traffic = ncu_traffic_per_launch()
         elif args.sparse == 2.0 ** -8 and PEAKED:
             traffic = ncu_traffic_per_launch(SPARSE_PROFILE_SUMMARY)
-    elif (args.pages == "fp8_e4m3" and not RAGGED and BATCH == 64 and SEQ == 8192 and
-          not PEAKED):
-        traffic = ncu_traffic_per_launch(E4M3_PROFILE_SUMMARY)
+    elif args.pages != "fp16" and not RAGGED and BATCH == 64 and SEQ == 8192 and not PEAKED:
+        traffic = ncu_traffic_per_launch(
+            E4M3_PROFILE_SUMMARY if args.pages == "fp8_e4m3" else INT4_PROFILE_SUMMARY)
     if configs is not None:
         configs["C2_b64_l8192_append"] = {
             "see": "headline keys (value, us_per_step, roofline)", "us_per_step":
