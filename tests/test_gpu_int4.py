@@ -199,3 +199,41 @@ def test_int4_cache_rejects_prefill_and_sparse_decode():
     q = t(inp.q[:1])
     with pytest.raises(RcpError):
         cache.decode_attn_sparse(q, t(c.block_table), t(inp.seq_lens_after), 1e-3)
+
+
+@pytest.mark.parametrize("shape_name", ["tiny", "mha32"])
+def test_int4_append_bad_slot_sets_error_and_writes_nothing(shape_name):
+    """A slot past the pool's capacity flags RCP_DEVERR_BAD_SLOT and leaves every byte of
+    the pages as it was (the other token of the call is written)."""
+    import torch
+    from rank_compressed_paged_gb300 import _lib
+    shape = wl.SHAPES[shape_name]
+    H, d, rk, R = _dims(shape)
+    rng = np.random.default_rng(195)
+    U, W = wl.make_factors(rng, H, d, rk, R)
+    k = wl.fp16(rng.standard_normal((2, H, d)))
+    v = wl.fp16(rng.standard_normal((2, H, d)))
+    slots = np.array([2 * 16 + 3, 5], np.int64)        # 2 blocks: slot 35 is past the end
+    kbytes, vbytes = orc.int4_page_bytes(H, rk, R)
+    kb = rng.integers(0, 256, size=(2, kbytes), dtype=np.uint8)
+    vb = rng.integers(0, 256, size=(2, vbytes), dtype=np.uint8)
+    cache = _int4_cache(shape, U, W, kb, vb)
+    cache.append_kv(t(k), t(v), t(slots))
+    torch.cuda.synchronize()
+    assert cache.read_device_error() & _lib.RCP_DEVERR_BAD_SLOT
+    kg, vg = cache.k_pages.cpu().numpy(), cache.v_pages.cpu().numpy()
+    # only slot 5 (block 0, offset 5) may differ from the input pages: its codes and scales
+    got = orc.int4_unpack_pages(kg, vg, H, rk, R)
+    was = orc.int4_unpack_pages(kb, vb, H, rk, R)
+    keep = np.arange(16) != 5
+    kc_g, ks_g, vc_g, vs_g = got
+    kc_i, ks_i, vc_i, vs_i = was
+    assert np.array_equal(kc_g[1], kc_i[1]) and np.array_equal(vc_g[1], vc_i[1])
+    assert np.array_equal(ks_g[1].view(np.uint16), ks_i[1].view(np.uint16))
+    assert np.array_equal(vs_g[1].view(np.uint16), vs_i[1].view(np.uint16))
+    assert np.array_equal(kc_g[0][:, keep], kc_i[0][:, keep])
+    assert np.array_equal(ks_g[0][:, keep].view(np.uint16), ks_i[0][:, keep].view(np.uint16))
+    assert np.array_equal(vc_g[0][keep], vc_i[0][keep])
+    assert np.array_equal(vs_g[0][keep].view(np.uint16), vs_i[0][keep].view(np.uint16))
+    assert not np.array_equal(vc_g[0][5], vc_i[0][5]) or not np.array_equal(
+        vs_g[0][5].view(np.uint16), vs_i[0][5].view(np.uint16))   # slot 5 was written
