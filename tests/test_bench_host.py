@@ -50,6 +50,25 @@ def test_clock_summary_widens_the_window_for_a_short_region():
     assert s["samples"] == 1 and s["window"] == "timed region +- 50 ms"
 
 
+def test_clock_summary_describes_the_first_region_and_counts_all_marked_ones():
+    c = bench.ClockSampler(0)
+    now = time.time()
+    c.t0, c.t1 = now, now + 1.0
+    c.regions = [(now, now + 0.1), (now + 0.3, now + 0.4), (now + 0.6, now + 0.7)]
+    c.proc = object()
+    with open(c.path, "w") as f:
+        f.write(_sample_line(now + 0.05, 2070))                   # first region
+        f.write(_sample_line(now + 0.2, 1000, ("Active",) * 4))   # between regions: ignored
+        f.write(_sample_line(now + 0.35, 1980))                   # second region
+        f.write(_sample_line(now + 0.65, 2070, ("Not Active", "Not Active", "Not Active",
+                                                "Active")))       # third region
+    s = c.summary()
+    assert s["samples"] == 1 and s["sm_mhz"] == 2070.0 and s["reasons"] == []
+    a = s["all_timed_regions"]
+    assert a["regions"] == 3 and a["samples"] == 3 and a["sm_min_mhz"] == 1980.0
+    assert a["sm_mhz"] == 2070.0 and a["reasons"] == ["sw_power_cap"]
+
+
 def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     src = tmp_path / "k.cu"
     src.write_text("int a = 1;  // one\n\n// a comment line\nint b = 2;\n")
