@@ -79,8 +79,10 @@ typedef enum rcp_status {
                                  decode widens value coefficients to fp16(code * scale)
                                  (one rounding) and scores keys as scale * (codes . q~) in
                                  fp32.  1,632 bytes per token at (32, 128, 64, 1024).
-                                 Append and decode only; the prefill calls and the
-                                 block-sparse decode return RCP_ERR_UNSUPPORTED. */
+                                 Append, decode and the reconstructing prefill (which
+                                 widens both K and V to fp16(code * scale));
+                                 rcp_prefill_attn and the block-sparse decode return
+                                 RCP_ERR_UNSUPPORTED. */
 
 typedef struct rcp_cache_config {
   int32_t num_heads;   /* H */
@@ -200,7 +202,7 @@ rcp_status rcp_decode_step(rcp_cache* cache, const void* k, const void* v,
  * the one before it, RCP_DEVERR_BAD_LEN is set and no row of out is written (so that no
  * two requests can claim the same rows).  out [num_query_rows][H][d] fp16.  workspace must hold
  * rcp_workspace_size(cache, num_query_rows) bytes.  fp16 pages only (RCP_ERR_UNSUPPORTED
- * for E4M3 pages: use rcp_prefill_attn_reconstruct). */
+ * for E4M3 and 4-bit pages: use rcp_prefill_attn_reconstruct). */
 rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_chunk_lens,
                             int32_t num_query_rows, const int32_t* block_table,
                             int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
@@ -216,10 +218,10 @@ rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_c
  * the rank-space variant once a request's chunk has more than rcp_prefill_crossover_rows
  * rows.  workspace must hold rcp_prefill_reconstruct_workspace_size(cache, num_query_rows,
  * batch, max_blocks_per_seq) bytes (256-byte aligned; it grows with the pages the batch
- * can reach, 2 * H * d * 16 bytes per page).  E4M3 pages: every page the batch reads is
- * first widened to fp16 (exact) in the workspace, which then also holds
- * 2 * 16 * (H * r_k + R) + 4 bytes per page the batch can reach; the result is that of the
- * same call on fp16 pages holding the decoded codes. */
+ * can reach, 2 * H * d * 16 bytes per page).  E4M3 and 4-bit pages: every page the batch
+ * reads is first widened to fp16 in the workspace (E4M3 exactly, 4-bit as fp16(code *
+ * scale)), which then also holds 2 * 16 * (H * r_k + R) + 4 bytes per page the batch can
+ * reach; the result is that of the same call on fp16 pages holding the widened values. */
 rcp_status rcp_prefill_attn_reconstruct(rcp_cache* cache, const void* q,
                                         const int32_t* cu_chunk_lens, int32_t num_query_rows,
                                         const int32_t* block_table, int32_t max_blocks_per_seq,

@@ -116,7 +116,8 @@ class PagedCoeffCache:
     "fp8_e4m3" stores E4M3 codes (uint8 tensors; prefill on them takes the reconstructing
     variant, which first widens the pages it reads to fp16 in the workspace), "int4" stores
     4-bit codes with fp16 scales as raw bytes (K pages [num_blocks][int4_page_bytes()[0]],
-    V pages [num_blocks][int4_page_bytes()[1]], uint8; append and decode only).
+    V pages [num_blocks][int4_page_bytes()[1]], uint8; prefill on them takes the
+    reconstructing variant, as for E4M3; no block-sparse decode).
     """
 
     def __init__(self, num_heads: int, head_dim: int, rank_k: int, rank_v: int,
@@ -311,7 +312,7 @@ class PagedCoeffCache:
                                     out)
         mb = int(block_table.shape[1])
         if variant == "auto":
-            variant = "reconstruct" if (self.page_format == "fp8_e4m3" or
+            variant = "reconstruct" if (self.page_format != "fp16" or
                                         (B > 0 and rows >= B * RECONSTRUCT_MIN_CHUNK)) else "rank"
         if variant not in ("rank", "reconstruct"):
             raise ValueError(f"unknown prefill variant {variant!r}")

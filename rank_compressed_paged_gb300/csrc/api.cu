@@ -235,7 +235,7 @@ Widened fill_recon(rcp::AttnParams& p, void* ws, int64_t nq, int64_t batch, int6
 }
 
 size_t recon_ws_bytes(const rcp_cache* c, int64_t nq, int64_t batch, int64_t max_blocks) {
-  const bool widen = c->cfg.page_format == RCP_PAGES_FP8_E4M3;
+  const bool widen = c->cfg.page_format != RCP_PAGES_FP16;
   return c->shape == kShapeMain ? rcp::recon_layout<ShapeMain>(nq, batch, max_blocks, widen).total
                                 : rcp::recon_layout<ShapeTiny>(nq, batch, max_blocks, widen).total;
 }
@@ -365,11 +365,9 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   if (c->shape == kShapeMain) fill_ws<ShapeMain>(p, ws, nq);
   else fill_ws<ShapeTiny>(p, ws, nq);
   const bool pdl = c->prof_start == nullptr;
-  // the prefill kernels read fp16 pages; E4M3 pages are widened first (reconstructing
-  // variant only: its workspace is sized by the pages the batch can reach)
+  // the prefill kernels read fp16 pages; E4M3 and 4-bit pages are widened first
+  // (reconstructing variant only: its workspace is sized by the pages the batch can reach)
   if (cu_chunk && p.page_format != RCP_PAGES_FP16 && !recon) return RCP_ERR_UNSUPPORTED;
-  // the reconstructing prefill widens E4M3 pages; 4-bit pages have no prefill
-  if (cu_chunk && p.page_format == RCP_PAGES_INT4) return RCP_ERR_UNSUPPORTED;
   if (cu_chunk) {
     // chunked prefill: plan + fp16 rank-space queries, then the tiled tensor-core kernel
     const uint64_t hq = static_cast<uint64_t>(c->cfg.num_heads) * 64;
@@ -386,7 +384,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
       return RCP_ERR_CUDA;
     // reconstructing variant: V^ rows for at most batch x max_blocks_per_seq pages
     const int64_t max_pages = static_cast<int64_t>(batch) * max_blocks_per_seq;
-    const bool widen = recon && p.page_format == RCP_PAGES_FP8_E4M3;
+    const bool widen = recon && p.page_format != RCP_PAGES_FP16;
     CUtensorMap vhat_map = c->tmap_v, kp16_map = c->tmap_kp, vp16_map = c->tmap_v;
     Widened wd{nullptr, nullptr, nullptr};
     rcp::AttnParams pw = p;   // the widening pass reads the cache's own pages and table

@@ -41,6 +41,7 @@
 
 #include "launch.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 #include "shape.h"
 
 namespace rcp {
@@ -310,16 +311,6 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
   return __half22float2(__half2(r));
 }
 
-// Two 4-bit codes (one byte: the even coefficient in the low nibble, two's complement) times
-// their group's scale, as an fp16 pair.  Each nibble n becomes the fp16 1024 + (n ^ 8)
-// (exponent bits 0x6400 with n ^ 8 as the low mantissa bits), minus 1032 the signed code,
-// exactly; the product with the scale rounds once.
-__device__ __forceinline__ uint32_t int4x2_to_half2_bits(uint32_t byte, __half2 scale) {
-  const uint32_t b = ((byte & 0xFu) | ((byte & 0xF0u) << 12)) ^ 0x64086408u;
-  const __half2 code = __hsub2(*reinterpret_cast<const __half2*>(&b), __float2half2_rn(1032.f));
-  const __half2 v = __hmul2(code, scale);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 // E4M3 pages, an even number of boxes: as widen_v_boxes below, in units of 16 codes (one
 // 16-byte load, two 16-byte stores).  A warp's 32 units are 4 tokens x 2 adjacent boxes x 4

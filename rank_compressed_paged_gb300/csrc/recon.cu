@@ -26,6 +26,7 @@
 
 #include "launch.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 #include "rcp.h"
 #include "shape.h"
 
@@ -203,12 +204,14 @@ __global__ void __launch_bounds__(kRcThreads, 2)
   }
 }
 
-// ------------------------------------------------------------- E4M3 pages for prefill
-// The prefill kernels read fp16 pages through tensor maps.  For a cache of E4M3 pages the
-// reconstructing prefill first widens every page the batch reads (the plan's page order,
-// as for V^) into fp16 copies in the workspace and re-addresses the block table to them;
-// E4M3 values are exact in fp16, so the kernels that follow compute the same result as
-// on the codes themselves.  A streaming pass: 48 KiB read and 96 KiB written per page.
+// ------------------------------------------------ quantized pages for prefill
+// The prefill kernels read fp16 pages through tensor maps.  For a cache of E4M3 or 4-bit
+// pages the reconstructing prefill first widens every page the batch reads (the plan's page
+// order, as for V^) into fp16 copies in the workspace and re-addresses the block table to
+// them.  E4M3 values are exact in fp16, so the kernels that follow compute the same result
+// as on the codes themselves; a 4-bit value becomes fp16(code x scale), one rounding (as in
+// the decode's value widening).  A streaming pass: 48 KiB (E4M3) or 25.5 KiB (4-bit) read
+// and 96 KiB written per page.
 constexpr int kWidenThreads = 256;
 
 __device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t codes) {   // low byte -> low half
@@ -217,13 +220,18 @@ __device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t codes) {   // low byte
   return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
 }
 
-template <class S>
+template <class S, int FMT>
 __global__ void __launch_bounds__(kWidenThreads)
     widen_pages_kernel(const AttnParams p, __half* k16, __half* v16, int32_t* table16) {
-  constexpr int KB8 = S::H * kBlockSize * S::RK;   // bytes of an E4M3 key page
-  constexpr int VB8 = kBlockSize * S::R;           // bytes of an E4M3 value page
-  constexpr int KC = KB8 / 16, VC = VB8 / 16;      // 16-byte chunks of codes
-  static_assert(KB8 % 16 == 0 && VB8 % 16 == 0, "page size");
+  constexpr bool I4 = FMT == RCP_PAGES_INT4;
+  constexpr int KN = S::H * kBlockSize * S::RK;    // coefficients of a key page
+  constexpr int VN = kBlockSize * S::R;            // coefficients of a value page
+  // bytes of a page; E4M3: the codes; 4-bit: codes then fp16 scales
+  constexpr int KB8 = I4 ? static_cast<int>(Int4Page<S>::KBYTES) : KN;
+  constexpr int VB8 = I4 ? static_cast<int>(Int4Page<S>::VBYTES) : VN;
+  // work items: 16 code bytes (E4M3) or 4 code bytes (4-bit), each 8 or 16 B of output
+  constexpr int KC = I4 ? KN / 8 : KN / 16, VC = I4 ? VN / 8 : VN / 16;
+  static_assert(KN % 16 == 0 && VN % 16 == 0 && S::RK % 8 == 0, "page size");
   __shared__ int64_t s_phys;
   griddep_wait();   // page prefix sums (plan) and the appended chunk are visible
   griddep_launch();
@@ -252,16 +260,38 @@ __global__ void __launch_bounds__(kWidenThreads)
     if (phys >= 0) {
       const uint4* ks = reinterpret_cast<const uint4*>(k8 + phys * KB8);
       const uint4* vs = reinterpret_cast<const uint4*>(v8 + phys * VB8);
-      uint4* kd = reinterpret_cast<uint4*>(k16 + g * KB8);
-      uint4* vd = reinterpret_cast<uint4*>(v16 + g * VB8);
-      for (int c = threadIdx.x; c < KC + VC; c += kWidenThreads) {
-        const bool key = c < KC;
-        const uint4 raw = key ? ks[c] : vs[c - KC];
-        uint4* dst = key ? kd + 2 * c : vd + 2 * (c - KC);
-        dst[0] = make_uint4(widen_e4m3x2(raw.x), widen_e4m3x2(raw.x >> 16), widen_e4m3x2(raw.y),
-                            widen_e4m3x2(raw.y >> 16));
-        dst[1] = make_uint4(widen_e4m3x2(raw.z), widen_e4m3x2(raw.z >> 16), widen_e4m3x2(raw.w),
-                            widen_e4m3x2(raw.w >> 16));
+      uint4* kd = reinterpret_cast<uint4*>(k16 + g * KN);   // fp16 copies: KN, VN halves
+      uint4* vd = reinterpret_cast<uint4*>(v16 + g * VN);
+      if constexpr (I4) {
+        // 8 coefficients (4 code bytes) of one scale group per item: key groups are the r_k
+        // values of a (head, token) row, value groups 64 joint coefficients of a token
+        const uint8_t* kb = k8 + phys * KB8;
+        const uint8_t* vb = v8 + phys * VB8;
+        const __half* ksc = reinterpret_cast<const __half*>(kb + Int4Page<S>::KCODES);
+        const __half* vsc = reinterpret_cast<const __half*>(vb + Int4Page<S>::VCODES);
+        for (int c = threadIdx.x; c < KC + VC; c += kWidenThreads) {
+          const bool key = c < KC;
+          const int e0 = (key ? c : c - KC) * 8;           // first coefficient of the item
+          const uint32_t raw = *reinterpret_cast<const uint32_t*>((key ? kb : vb) + e0 / 2);
+          const __half2 sc = __half2half2(key ? ksc[e0 / S::RK]
+                                              : vsc[(e0 / S::R) * (S::R / 64) + (e0 % S::R) / 64]);
+          uint4* dst = reinterpret_cast<uint4*>((key ? reinterpret_cast<__half*>(kd)
+                                                     : reinterpret_cast<__half*>(vd)) + e0);
+          *dst = make_uint4(int4x2_to_half2_bits(raw & 0xFFu, sc),
+                            int4x2_to_half2_bits((raw >> 8) & 0xFFu, sc),
+                            int4x2_to_half2_bits((raw >> 16) & 0xFFu, sc),
+                            int4x2_to_half2_bits(raw >> 24, sc));
+        }
+      } else {
+        for (int c = threadIdx.x; c < KC + VC; c += kWidenThreads) {
+          const bool key = c < KC;
+          const uint4 raw = key ? ks[c] : vs[c - KC];
+          uint4* dst = key ? kd + 2 * c : vd + 2 * (c - KC);
+          dst[0] = make_uint4(widen_e4m3x2(raw.x), widen_e4m3x2(raw.x >> 16), widen_e4m3x2(raw.y),
+                              widen_e4m3x2(raw.y >> 16));
+          dst[1] = make_uint4(widen_e4m3x2(raw.z), widen_e4m3x2(raw.z >> 16), widen_e4m3x2(raw.w),
+                              widen_e4m3x2(raw.w >> 16));
+        }
       }
     }
     __syncthreads();   // s_phys is rewritten for the next page
@@ -275,8 +305,12 @@ cudaError_t launch_widen(const AttnParams& p, void* k16, void* v16, int32_t* tab
   if (max_pages <= 0) return cudaSuccess;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;   // grid-stride over the pages
   const unsigned grid = static_cast<unsigned>(max_pages < cap ? max_pages : cap);
-  return launch_pdl(widen_pages_kernel<S>, dim3(grid), dim3(kWidenThreads), 0, stream, pdl, p,
-                    static_cast<__half*>(k16), static_cast<__half*>(v16), table16);
+  if (p.page_format == RCP_PAGES_INT4)
+    return launch_pdl(widen_pages_kernel<S, RCP_PAGES_INT4>, dim3(grid), dim3(kWidenThreads), 0,
+                      stream, pdl, p, static_cast<__half*>(k16), static_cast<__half*>(v16),
+                      table16);
+  return launch_pdl(widen_pages_kernel<S, RCP_PAGES_FP8_E4M3>, dim3(grid), dim3(kWidenThreads), 0,
+                    stream, pdl, p, static_cast<__half*>(k16), static_cast<__half*>(v16), table16);
 }
 
 template <class S>

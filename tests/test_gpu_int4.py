@@ -186,19 +186,71 @@ def test_int4_decode_step_equals_append_then_decode():
     assert_close(ob.cpu().numpy(), ref, what="int4 step")
 
 
-def test_int4_cache_rejects_prefill_and_sparse_decode():
+def test_int4_cache_rejects_rank_space_prefill_and_sparse_decode():
     from rank_compressed_paged_gb300 import RcpError
     inp = wl.make_prefill_inputs(MAIN, [40], [20], seed=187)
     c = inp.cache
     kb, vb = _bytes(MAIN, c.k_pages, c.v_pages)
     cache = _int4_cache(MAIN, inp.U_k, inp.W_v, kb, vb)
-    for variant in ("rank", "reconstruct"):
-        with pytest.raises(RcpError):
-            cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
-                               t(inp.seq_lens_after), variant=variant)
+    with pytest.raises(RcpError):
+        cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
+                           t(inp.seq_lens_after), variant="rank")
     q = t(inp.q[:1])
     with pytest.raises(RcpError):
         cache.decode_attn_sparse(q, t(c.block_table), t(inp.seq_lens_after), 1e-3)
+
+
+@pytest.mark.parametrize("shape,prior,chunk,seed", [
+    (TINY, [37, 0, 100, 5], [21, 16, 40, 0], 188),
+    (MAIN, [300, 0, 1024, 17], [64, 130, 3, 1], 189),
+])
+def test_int4_prefill_on_oracle_pages(shape, prior, chunk, seed):
+    """Every page, the chunk's included, holds the oracle's 4-bit encoding (its own append of
+    the chunk); the GPU runs the prefill alone (widening pass, reconstruction, attention)
+    and the oracle attends the values code x scale."""
+    import torch
+    inp = wl.make_prefill_inputs(shape, prior, chunk, seed=seed, fill=np.nan)
+    c = inp.cache
+    kb, vb = _bytes(shape, c.k_pages, c.v_pages)
+    ko, vo = orc.append_kv_int4(kb, vb, inp.U_k, inp.W_v, inp.k, inp.v, inp.slot_mapping, 16)
+    cache = _int4_cache(shape, inp.U_k, inp.W_v, ko, vo)
+    out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
+                             t(inp.seq_lens_after))
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    kv, vv = _values(shape, ko, vo)
+    ref = orc.prefill_attn(inp.q, inp.cu_chunk_lens, kv, vv, inp.U_k, inp.W_v, c.block_table,
+                           inp.seq_lens_after, 16)
+    assert_close(out.cpu().numpy(), ref, what="int4 prefill")
+    # the pages themselves are untouched by the widening pass
+    assert np.array_equal(cache.k_pages.cpu().numpy(), ko)
+    assert np.array_equal(cache.v_pages.cpu().numpy(), vo)
+
+
+def test_int4_prefill_after_its_own_append():
+    """Chunk appended by the GPU with pair-sum factors on narrow inputs (bytes exact on both
+    sides), then the prefill."""
+    import torch
+    inp = wl.make_prefill_inputs(MAIN, [500, 64, 0], [100, 33, 16], seed=190, fill=np.nan)
+    c = inp.cache
+    rng = np.random.default_rng(290)
+    U, W = wl.pair_sum_factors(rng, 32, 128, 64, 1024)
+    k = wl.fp16_narrow(rng, inp.k.shape, emin=-6, emax=-1)
+    v = wl.fp16_narrow(rng, inp.v.shape, emin=-6, emax=-1)
+    kb, vb = _bytes(MAIN, c.k_pages, c.v_pages)
+    cache = _int4_cache(MAIN, U, W, kb, vb)
+    cache.append_kv(t(k), t(v), t(inp.slot_mapping))
+    out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
+                             t(inp.seq_lens_after))
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    ko, vo = orc.append_kv_int4(kb, vb, U, W, k, v, inp.slot_mapping, 16)
+    assert np.array_equal(cache.k_pages.cpu().numpy(), ko)
+    assert np.array_equal(cache.v_pages.cpu().numpy(), vo)
+    kv, vv = _values(MAIN, ko, vo)
+    ref = orc.prefill_attn(inp.q, inp.cu_chunk_lens, kv, vv, U, W, c.block_table,
+                           inp.seq_lens_after, 16)
+    assert_close(out.cpu().numpy(), ref, what="int4 prefill after append")
 
 
 @pytest.mark.parametrize("shape_name", ["tiny", "mha32"])
