@@ -59,9 +59,9 @@ typedef enum rcp_status {
 #define RCP_PAGES_FP16 0      /* IEEE fp16 coefficients */
 #define RCP_PAGES_FP8_E4M3 1  /* E4M3 codes (OCP 8-bit float: bias 7, 3 mantissa bits, max
                                  448): the append rounds to nearest even and saturates to
-                                 +-448; half the bytes per token.  Append, decode and the
-                                 reconstructing prefill; rcp_prefill_attn and the
-                                 block-sparse decode return RCP_ERR_UNSUPPORTED. */
+                                 +-448; half the bytes per token.  Append, decode and both
+                                 prefill variants (pages widened to fp16 first); the
+                                 block-sparse decode returns RCP_ERR_UNSUPPORTED. */
 #define RCP_PAGES_INT4 2      /* 4-bit codes with fp16 scales ("KV-cache LLM serving" page,
                                  "What it measured", item 1: 4-bit KV pages for capacity;
                                  a rotation before quantizing folds into U_k and W_v, so it
@@ -79,10 +79,9 @@ typedef enum rcp_status {
                                  decode widens value coefficients to fp16(code * scale)
                                  (one rounding) and scores keys as scale * (codes . q~) in
                                  fp32.  1,632 bytes per token at (32, 128, 64, 1024).
-                                 Append, decode and the reconstructing prefill (which
-                                 widens both K and V to fp16(code * scale));
-                                 rcp_prefill_attn and the block-sparse decode return
-                                 RCP_ERR_UNSUPPORTED. */
+                                 Append, decode and both prefill variants (which widen K
+                                 and V to fp16(code * scale) first); the block-sparse
+                                 decode returns RCP_ERR_UNSUPPORTED. */
 
 typedef struct rcp_cache_config {
   int32_t num_heads;   /* H */
@@ -175,7 +174,8 @@ rcp_status rcp_decode_attn(rcp_cache* cache, const void* q, const int32_t* block
  *   page_kept: NULL, or device uint8 [batch][max_blocks_per_seq]: entry (b, j) is set to 1
  *     if page j of request b was read and 0 if it was left out; entries at or past
  *     ceil(seq_lens[b] / 16) are not written.
- * fp16 pages only (RCP_ERR_UNSUPPORTED for E4M3 pages).  Workspace as rcp_decode_attn. */
+ * fp16 pages only (RCP_ERR_UNSUPPORTED for E4M3 and 4-bit pages).  Workspace as
+ * rcp_decode_attn. */
 rcp_status rcp_decode_attn_sparse(rcp_cache* cache, const void* q, const int32_t* block_table,
                                   int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                   int32_t batch, float skip_threshold, uint8_t* page_kept,
@@ -201,8 +201,10 @@ rcp_status rcp_decode_step(rcp_cache* cache, const void* k, const void* v,
  * 0 .. that position (causal).  cu_chunk_lens must not decrease: if any entry is below
  * the one before it, RCP_DEVERR_BAD_LEN is set and no row of out is written (so that no
  * two requests can claim the same rows).  out [num_query_rows][H][d] fp16.  workspace must hold
- * rcp_workspace_size(cache, num_query_rows) bytes.  fp16 pages only (RCP_ERR_UNSUPPORTED
- * for E4M3 and 4-bit pages: use rcp_prefill_attn_reconstruct). */
+ * rcp_workspace_size(cache, num_query_rows) bytes; on E4M3 and 4-bit pages, which are first
+ * widened to fp16 in the workspace as for rcp_prefill_attn_reconstruct, it must hold
+ * rcp_prefill_reconstruct_workspace_size(cache, num_query_rows, batch,
+ * max_blocks_per_seq) bytes. */
 rcp_status rcp_prefill_attn(rcp_cache* cache, const void* q, const int32_t* cu_chunk_lens,
                             int32_t num_query_rows, const int32_t* block_table,
                             int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,

@@ -113,11 +113,11 @@ class PagedCoeffCache:
     Owns (as torch tensors) the K pages [num_blocks][H][16][r_k], V pages
     [num_blocks][16][R], the factors, a device error word and a reusable workspace; the
     library handle borrows their pointers.  page_format "fp16" stores fp16 coefficients,
-    "fp8_e4m3" stores E4M3 codes (uint8 tensors; prefill on them takes the reconstructing
-    variant, which first widens the pages it reads to fp16 in the workspace), "int4" stores
-    4-bit codes with fp16 scales as raw bytes (K pages [num_blocks][int4_page_bytes()[0]],
-    V pages [num_blocks][int4_page_bytes()[1]], uint8; prefill on them takes the
-    reconstructing variant, as for E4M3; no block-sparse decode).
+    "fp8_e4m3" stores E4M3 codes (uint8 tensors), "int4" stores 4-bit codes with fp16
+    scales as raw bytes (K pages [num_blocks][int4_page_bytes()[0]], V pages
+    [num_blocks][int4_page_bytes()[1]], uint8).  A prefill on quantized pages first widens
+    the pages it reads to fp16 in the workspace (the "auto" variant reconstructs); they have
+    no block-sparse decode.
     """
 
     def __init__(self, num_heads: int, head_dim: int, rank_k: int, rank_v: int,
@@ -317,7 +317,10 @@ class PagedCoeffCache:
         if variant not in ("rank", "reconstruct"):
             raise ValueError(f"unknown prefill variant {variant!r}")
         if variant == "rank":
-            ws = self.workspace(rows) if workspace is None else workspace
+            # quantized pages are widened into the workspace first (both variants)
+            need = (self.workspace_bytes(rows) if self.page_format == "fp16"
+                    else self.reconstruct_workspace_bytes(rows, B, mb))
+            ws = self.workspace(rows, need) if workspace is None else workspace
             fn, name = self._lib.rcp_prefill_attn, "rcp_prefill_attn"
         else:
             ws = self.workspace(rows, self.reconstruct_workspace_bytes(rows, B, mb)) \

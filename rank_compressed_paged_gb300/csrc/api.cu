@@ -326,7 +326,9 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
       (cu_chunk && (reinterpret_cast<uintptr_t>(cu_chunk) & 3u)))
     return RCP_ERR_INVALID_ARG;
-  if (ws_size < (recon ? recon_ws_bytes(c, nq, batch, max_blocks_per_seq) : ws_bytes(c, nq)))
+  // a prefill on quantized pages widens the pages it reads into the workspace (both variants)
+  const bool paged_ws = recon || (cu_chunk && c->cfg.page_format != RCP_PAGES_FP16);
+  if (ws_size < (paged_ws ? recon_ws_bytes(c, nq, batch, max_blocks_per_seq) : ws_bytes(c, nq)))
     return RCP_ERR_WORKSPACE;
   // block-sparse decode reads fp16 pages
   if (sparse && (cu_chunk || c->cfg.page_format != RCP_PAGES_FP16)) return RCP_ERR_UNSUPPORTED;
@@ -365,9 +367,8 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   if (c->shape == kShapeMain) fill_ws<ShapeMain>(p, ws, nq);
   else fill_ws<ShapeTiny>(p, ws, nq);
   const bool pdl = c->prof_start == nullptr;
-  // the prefill kernels read fp16 pages; E4M3 and 4-bit pages are widened first
-  // (reconstructing variant only: its workspace is sized by the pages the batch can reach)
-  if (cu_chunk && p.page_format != RCP_PAGES_FP16 && !recon) return RCP_ERR_UNSUPPORTED;
+  // the prefill kernels read fp16 pages; E4M3 and 4-bit pages are widened first into the
+  // workspace, which is then sized by the pages the batch can reach
   if (cu_chunk) {
     // chunked prefill: plan + fp16 rank-space queries, then the tiled tensor-core kernel
     const uint64_t hq = static_cast<uint64_t>(c->cfg.num_heads) * 64;
@@ -384,17 +385,18 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
       return RCP_ERR_CUDA;
     // reconstructing variant: V^ rows for at most batch x max_blocks_per_seq pages
     const int64_t max_pages = static_cast<int64_t>(batch) * max_blocks_per_seq;
-    const bool widen = recon && p.page_format != RCP_PAGES_FP16;
+    const bool widen = p.page_format != RCP_PAGES_FP16;
     CUtensorMap vhat_map = c->tmap_v, kp16_map = c->tmap_kp, vp16_map = c->tmap_v;
     Widened wd{nullptr, nullptr, nullptr};
     rcp::AttnParams pw = p;   // the widening pass reads the cache's own pages and table
-    if (recon) {
+    if (recon || widen) {
       if (max_pages * 16 >= (int64_t{1} << 31)) return RCP_ERR_UNSUPPORTED;
       if (widen && max_pages * c->cfg.num_heads * 16 >= (int64_t{1} << 31)) return RCP_ERR_UNSUPPORTED;
       wd = c->shape == kShapeMain
                ? fill_recon<ShapeMain>(p, ws, nq, batch, max_blocks_per_seq, widen)
                : fill_recon<ShapeTiny>(p, ws, nq, batch, max_blocks_per_seq, widen);
-      if (!encode_2d(&vhat_map, p.vhat, hdq, static_cast<uint64_t>(max_pages) * 16, hdq * 2, 64, 128))
+      if (recon && !encode_2d(&vhat_map, p.vhat, hdq, static_cast<uint64_t>(max_pages) * 16,
+                              hdq * 2, 64, 128))
         return RCP_ERR_CUDA;
       if (widen) {
         pw = p;   // with the plan's page prefix sums
@@ -411,7 +413,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
         p.page_format = RCP_PAGES_FP16;
       }
     }
-    const CUtensorMap& vals = recon ? vhat_map : c->tmap_v;
+    const CUtensorMap& vals = recon ? vhat_map : widen ? vp16_map : c->tmap_v;
     const CUtensorMap& kmap = widen ? kp16_map : c->tmap_kp;
     const CUtensorMap& vsrc = widen ? vp16_map : c->tmap_v;
     if (c->shape == kShapeMain) {

@@ -208,8 +208,19 @@ def test_reconstruct_workspace_grows_by_the_widened_pages_for_e4m3(lib):
     pages = 16 * 272
     extra = pages * 2 * 16 * (32 * 64 + 1024) + pages * 4
     assert extra <= b.value - a.value <= extra + 3 * 256
+    # the rank-space prefill on quantized pages widens them too: the query-row workspace
+    # alone is refused before any launch (E4M3 and 4-bit alike)
+    st4, h4 = _create(lib, _lib, _cfg(_lib, fmt=_lib.RCP_PAGES_INT4))
+    assert st4 == _lib.RCP_OK
+    small = ctypes.c_size_t()
+    for h in (h8, h4):
+        assert lib.rcp_workspace_size(h, 64, ctypes.byref(small)) == 0
+        assert small.value < b.value
+        assert lib.rcp_prefill_attn(h, 0x1000, 0x5000, 64, 0x2000, 272, 0x3000, 16, 0x4000,
+                                    0x100000, small.value, None) == _lib.RCP_ERR_WORKSPACE
     lib.rcp_destroy_cache(h16)
     lib.rcp_destroy_cache(h8)
+    lib.rcp_destroy_cache(h4)
 
 
 def _declared_param_counts():

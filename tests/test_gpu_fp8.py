@@ -158,14 +158,22 @@ def test_fp8_decode_step_equals_append_then_decode():
     assert_close(ob.cpu().numpy(), ref, what="fp8 step")
 
 
-def test_fp8_cache_rejects_rank_space_prefill():
-    from rank_compressed_paged_gb300 import RcpError
-    inp = wl.make_prefill_inputs(MAIN, [40], [20], seed=87)
+def test_fp8_rank_space_prefill_on_oracle_pages():
+    """The rank-space variant on E4M3 pages: the pages it reads are widened into the
+    workspace first; the result is the oracle's on the decoded codes."""
+    import torch
+    inp = wl.make_prefill_inputs(MAIN, [300, 0, 1024, 17], [64, 130, 3, 1], seed=87, fill=np.nan)
     c = inp.cache
-    cache = _fp8_cache(MAIN, inp.U_k, inp.W_v, _codes(c.k_pages), _codes(c.v_pages))
-    with pytest.raises(RcpError):
-        cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
-                           t(inp.seq_lens_after), variant="rank")
+    ko, vo = orc.append_kv_fp8(_codes(c.k_pages), _codes(c.v_pages), inp.U_k, inp.W_v, inp.k,
+                               inp.v, inp.slot_mapping, 16)
+    cache = _fp8_cache(MAIN, inp.U_k, inp.W_v, ko, vo)
+    out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
+                             t(inp.seq_lens_after), variant="rank")
+    torch.cuda.synchronize()
+    assert cache.read_device_error() == 0
+    ref = orc.prefill_attn(inp.q, inp.cu_chunk_lens, orc.e4m3_decode(ko), orc.e4m3_decode(vo),
+                           inp.U_k, inp.W_v, c.block_table, inp.seq_lens_after, 16)
+    assert_close(out.cpu().numpy(), ref, what="fp8 rank-space prefill")
 
 
 @pytest.mark.parametrize("shape,prior,chunk,seed", [

@@ -186,28 +186,26 @@ def test_int4_decode_step_equals_append_then_decode():
     assert_close(ob.cpu().numpy(), ref, what="int4 step")
 
 
-def test_int4_cache_rejects_rank_space_prefill_and_sparse_decode():
+def test_int4_cache_rejects_sparse_decode():
     from rank_compressed_paged_gb300 import RcpError
-    inp = wl.make_prefill_inputs(MAIN, [40], [20], seed=187)
+    inp = wl.make_decode_inputs(MAIN, [40, 7], seed=187)
     c = inp.cache
     kb, vb = _bytes(MAIN, c.k_pages, c.v_pages)
     cache = _int4_cache(MAIN, inp.U_k, inp.W_v, kb, vb)
     with pytest.raises(RcpError):
-        cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
-                           t(inp.seq_lens_after), variant="rank")
-    q = t(inp.q[:1])
-    with pytest.raises(RcpError):
-        cache.decode_attn_sparse(q, t(c.block_table), t(inp.seq_lens_after), 1e-3)
+        cache.decode_attn_sparse(t(inp.q), t(c.block_table), t(c.seq_lens), 1e-3)
 
 
+@pytest.mark.parametrize("variant", ["reconstruct", "rank"])
 @pytest.mark.parametrize("shape,prior,chunk,seed", [
     (TINY, [37, 0, 100, 5], [21, 16, 40, 0], 188),
     (MAIN, [300, 0, 1024, 17], [64, 130, 3, 1], 189),
 ])
-def test_int4_prefill_on_oracle_pages(shape, prior, chunk, seed):
+def test_int4_prefill_on_oracle_pages(shape, prior, chunk, seed, variant):
     """Every page, the chunk's included, holds the oracle's 4-bit encoding (its own append of
-    the chunk); the GPU runs the prefill alone (widening pass, reconstruction, attention)
-    and the oracle attends the values code x scale."""
+    the chunk); the GPU runs the prefill alone (widening pass, then the reconstruction and
+    attention, or the rank-space attention) and the oracle attends the values code x
+    scale."""
     import torch
     inp = wl.make_prefill_inputs(shape, prior, chunk, seed=seed, fill=np.nan)
     c = inp.cache
@@ -215,7 +213,7 @@ def test_int4_prefill_on_oracle_pages(shape, prior, chunk, seed):
     ko, vo = orc.append_kv_int4(kb, vb, inp.U_k, inp.W_v, inp.k, inp.v, inp.slot_mapping, 16)
     cache = _int4_cache(shape, inp.U_k, inp.W_v, ko, vo)
     out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(c.block_table),
-                             t(inp.seq_lens_after))
+                             t(inp.seq_lens_after), variant=variant)
     torch.cuda.synchronize()
     assert cache.read_device_error() == 0
     kv, vv = _values(shape, ko, vo)
