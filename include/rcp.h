@@ -59,9 +59,9 @@ typedef enum rcp_status {
 #define RCP_PAGES_FP16 0      /* IEEE fp16 coefficients */
 #define RCP_PAGES_FP8_E4M3 1  /* E4M3 codes (OCP 8-bit float: bias 7, 3 mantissa bits, max
                                  448): the append rounds to nearest even and saturates to
-                                 +-448; half the bytes per token.  Append, decode and both
-                                 prefill variants (pages widened to fp16 first); the
-                                 block-sparse decode returns RCP_ERR_UNSUPPORTED. */
+                                 +-448; half the bytes per token.  Append, decode (dense
+                                 and block-sparse) and both prefill variants (pages
+                                 widened to fp16 first). */
 #define RCP_PAGES_INT4 2      /* 4-bit codes with fp16 scales ("KV-cache LLM serving" page,
                                  "What it measured", item 1: 4-bit KV pages for capacity;
                                  a rotation before quantizing folds into U_k and W_v, so it
@@ -79,9 +79,9 @@ typedef enum rcp_status {
                                  decode widens value coefficients to fp16(code * scale)
                                  (one rounding) and scores keys as scale * (codes . q~) in
                                  fp32.  1,632 bytes per token at (32, 128, 64, 1024).
-                                 Append, decode and both prefill variants (which widen K
-                                 and V to fp16(code * scale) first); the block-sparse
-                                 decode returns RCP_ERR_UNSUPPORTED. */
+                                 Append, decode (dense and block-sparse) and both prefill
+                                 variants (which widen K and V to fp16(code * scale)
+                                 first). */
 
 typedef struct rcp_cache_config {
   int32_t num_heads;   /* H */
@@ -169,13 +169,16 @@ rcp_status rcp_decode_attn(rcp_cache* cache, const void* q, const int32_t* block
  * with its first page kept), so which pages are left out depends on how the batch is
  * partitioned; every page left out satisfies the rule against the running maximum, which
  * never exceeds the maximum over the whole sequence.
- *   skip_threshold: in [0, 1); 0 leaves no page out (same result as rcp_decode_attn, bit
- *     for bit); otherwise RCP_ERR_INVALID_ARG.
+ *   skip_threshold: in [0, 1); 0 leaves no page out; otherwise RCP_ERR_INVALID_ARG.
+ *     With 0 the result is that of rcp_decode_attn bit for bit on fp16 pages, and on
+ *     quantized pages where the dense decode also scores keys on the CUDA cores (r_k != 64
+ *     or H % 16 != 0); elsewhere the dense decode scores E4M3 and 4-bit keys on the tensor
+ *     cores and the two agree to rounding.
  *   page_kept: NULL, or device uint8 [batch][max_blocks_per_seq]: entry (b, j) is set to 1
  *     if page j of request b was read and 0 if it was left out; entries at or past
  *     ceil(seq_lens[b] / 16) are not written.
- * fp16 pages only (RCP_ERR_UNSUPPORTED for E4M3 and 4-bit pages).  Workspace as
- * rcp_decode_attn. */
+ * Every page format: E4M3 and 4-bit keys are scored on the CUDA cores here (a page's
+ * value codes are widened only once the page is kept).  Workspace as rcp_decode_attn. */
 rcp_status rcp_decode_attn_sparse(rcp_cache* cache, const void* q, const int32_t* block_table,
                                   int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                   int32_t batch, float skip_threshold, uint8_t* page_kept,

@@ -330,8 +330,8 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
   const bool paged_ws = recon || (cu_chunk && c->cfg.page_format != RCP_PAGES_FP16);
   if (ws_size < (paged_ws ? recon_ws_bytes(c, nq, batch, max_blocks_per_seq) : ws_bytes(c, nq)))
     return RCP_ERR_WORKSPACE;
-  // block-sparse decode reads fp16 pages
-  if (sparse && (cu_chunk || c->cfg.page_format != RCP_PAGES_FP16)) return RCP_ERR_UNSUPPORTED;
+  // block-sparse skipping is a decode option
+  if (sparse && cu_chunk) return RCP_ERR_UNSUPPORTED;
   rcp_status st = ensure_device(c);
   if (st != RCP_OK) return st;
   rcp::AttnParams p{};

@@ -249,8 +249,9 @@ struct DecodeSmem {
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;               // tmem slot, abort flag
   static constexpr int INFO_OFF = MISC_OFF + 16;                    // valid tokens per stage:
   // K stages, then V; SKIP adds the physical block of each K stage, the decision ring and
-  // the info word of each P buffer; TSC the valid tokens of each score buffer
-  static constexpr int INFO_BYTES = (2 * KST + VRS + DS + 4 + KST) * 4;   // + I4T operand stages
+  // the info word of each P buffer; TSC the valid tokens of each score buffer; I4T those of
+  // each operand stage; SKIP the valid tokens of each decision
+  static constexpr int INFO_BYTES = (2 * KST + VRS + DS + 4 + KST + DS) * 4;
   // TMEM: the value accumulator [NCHUNK x 128 lanes][HP], then (TSC) two score buffers of
   // H/8 groups x 32 columns
   static constexpr int SCOL = S::NCHUNK * S::HP;
@@ -278,8 +279,12 @@ struct DecodeSmem {
 // Warp 0 copies, warp 1 issues the MMAs, warps 2 .. compute.
 // F8: eight compute warps (2-9; scoring E4M3 keys costs more per byte) and warps 10-11,
 // which widen the E4M3 V pages while the compute warps score.
-// SKIP: warp 0 copies keys only and warp 6 copies the value pages the compute warps keep.
-// (Eight compute warps measured slower there: more registers spilled and barrier traffic.)
+// SKIP: warp 0 copies keys only and the last warp copies the value pages the compute warps
+// keep.  fp16 pages: four compute warps (eight measured slower there: more registers
+// spilled and barrier traffic).  Quantized pages: the keys are scored on the CUDA cores by
+// eight compute warps (the tensor-core scoring issues a page's scores before it is known
+// which value pages are needed), and four widening warps widen every kept V page.
+// SKIP + F8: warps 2-9 compute, 10-13 widen, 14 copies the kept value pages.
 // TSC: four compute warps (one per TMEM lane quarter: scores, softmax, weights) and six
 // warps that widen the V pages (and build the query operands), so that the widening's
 // conversions overlap the softmax's shuffle latencies instead of following them.
@@ -290,7 +295,10 @@ constexpr int decode_compute_warps() {
 }
 template <class S, int FMT, bool SKIP = false>
 constexpr int decode_widen_warps() {
-  return decode_tensor_scores<S, FMT, SKIP>() ? 6 : FMT != RCP_PAGES_FP16 ? 2 : 0;
+  return decode_tensor_scores<S, FMT, SKIP>()  ? 6
+         : FMT == RCP_PAGES_FP16               ? 0
+         : (SKIP && S::H % 8 == 0)             ? 4
+                                               : 2;
 }
 template <class S, int FMT, bool SKIP = false>
 constexpr int decode_threads() {
@@ -559,7 +567,6 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     decode_main_kernel(const __grid_constant__ CUtensorMap tmap_v,
                        const __grid_constant__ CUtensorMap tmap_k, const AttnParams p) {
   constexpr bool F8 = FMT != RCP_PAGES_FP16;   // quantized pages (E4M3 or 4-bit)
-  static_assert(!(F8 && SKIP), "block-sparse decode reads fp16 pages");
   // fp16 key pages with 128-byte rows (r_k = 64) arrive 128-byte swizzled (two TMA boxes of
   // 256 rows): chunk c of row r sits at chunk c ^ (r % 8), so the 16 lanes scoring one
   // head read the same logical chunk, conflict-free on the keys and as a broadcast on q~
@@ -606,7 +613,9 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   constexpr int NWW = decode_widen_warps<S, FMT, SKIP>();   // widening warps NCW+2 ..
   // (4-bit pages: the widening warps also widen the key codes, so the compute warps take
   // 10 of the 16 value boxes: measured 521 us at batch 64 x 8192 against 588 us for none)
-  constexpr int WB = (TSC && FMT == RCP_PAGES_FP8_E4M3) ? S::NBOX : S::NBOX >= 16 ? 6 : S::NBOX;
+  // (SKIP: all of them, in the order of the kept pages)
+  constexpr int WB =
+      (SKIP || (TSC && FMT == RCP_PAGES_FP8_E4M3)) ? S::NBOX : S::NBOX >= 16 ? 6 : S::NBOX;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
   // tokens of the block in each stage that are attended, published by the copy thread
@@ -622,6 +631,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   int* pinfo = dec_s + L::DS;
   int* sinfo = pinfo + 2;   // TSC: valid tokens of the page in each score buffer
   int* oinfo = sinfo + 2;   // I4T: valid tokens of the page in each operand stage
+  int* dec_n = oinfo + KST; // SKIP: valid tokens of each kept page of the decision ring
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -924,7 +934,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
           if (!mbar_wait(&pfull[ps], (kk >> 1) & 1, abort_flag, p.dev_err)) break;
           const int info = pinfo[ps];
           if (info < 0) break;
-          if (!mbar_wait(&vfull[vs], (kk / VST) & 1, abort_flag, p.dev_err)) break;
+          if (!mbar_wait(F8 ? &vcvt[vs] : &vfull[vs], (kk / VST) & 1, abort_flag, p.dev_err)) break;
           tc_fence_after();
           const uint32_t vaddr = smem_u32(vst + vs * S::VSTAGE_BYTES);
           const uint64_t bdesc = make_sdesc(smem_u32(pbuf + ps * L::P_BYTES), 128, 256, kSwizzleNone);
@@ -933,7 +943,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
             const uint64_t adesc = make_sdesc(vaddr + i * 4096, 2048, 1024, kSwizzle128B);
             umma_f16(tmem_base + i * HP, adesc, bdesc, idesc, info ? 0u : 1u);
           }
-          umma_commit(&vempty[vs]);
+          umma_commit(F8 ? &vfree[vs] : &vempty[vs]);
           umma_commit(&pfree[ps]);
           ++issued;
         }
@@ -1002,30 +1012,45 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
       }
       if (issued > 0) mbar_wait_drain(&pfree[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
     }
-  } else if (SKIP && warp == 2 + NCW) {
+  } else if (SKIP && warp == 2 + NCW + NWW) {
     // ------------------------------------------ SKIP: value pages of the kept pages
+    // (F8: the raw pages, into the stages the widening warps read; after the last one a
+    // stage whose info word is -1 tells them that no page follows)
     if (lane == 0) {
       if (step) griddep_wait();   // pages an append ahead of this launch wrote
       const uint64_t pol = policy_evict_first();
+      constexpr int NS = F8 ? VRS : VST;   // stages the copies land in
       int64_t nv = 0;
       for (int64_t n = 0;; ++n) {
         const int ds = static_cast<int>(n % L::DS);
         if (!mbar_wait(&decfull[ds], (n / L::DS) & 1, abort_flag, p.dev_err)) break;
-        const int phys = dec_s[ds];
+        const int phys = dec_s[ds], nval = dec_n[ds];
         mbar_arrive(&decempty[ds]);
-        if (phys < 0) break;
-        const int vs = static_cast<int>(nv % VST);
-        if (nv >= VST && !mbar_wait(&vempty[vs], ((nv / VST) - 1) & 1, abort_flag, p.dev_err)) break;
-        mbar_arrive_expect_tx(&vfull[vs], L::VP);
+        const int vs = static_cast<int>(nv % NS);
+        if (phys < 0 && !F8) break;
+        if (nv >= NS && !mbar_wait(&vempty[vs], ((nv / NS) - 1) & 1, abort_flag, p.dev_err)) break;
+        if constexpr (F8) {
+          vinfo[vs] = phys < 0 ? -1 : nval;
+          if (phys < 0) {
+            mbar_arrive(&vfull[vs]);
+            break;
+          }
+          mbar_arrive_expect_tx(&vfull[vs], L::VP);
+          bulk_g2s_hint(vraw + vs * L::VPS,
+                        static_cast<const uint8_t*>(p.v_pages) + static_cast<int64_t>(phys) * L::VP,
+                        L::VP, &vfull[vs], pol);
+        } else {
+          mbar_arrive_expect_tx(&vfull[vs], L::VP);
 #pragma unroll 1
-        for (int bx = 0; bx < S::NBOX; ++bx)
-          tma_load_2d_hint(vst + vs * S::VSTAGE_BYTES + bx * 2048, &tmap_v, bx * 64,
-                           phys * kBlockSize, &vfull[vs], pol);
+          for (int bx = 0; bx < S::NBOX; ++bx)
+            tma_load_2d_hint(vst + vs * S::VSTAGE_BYTES + bx * 2048, &tmap_v, bx * 64,
+                             phys * kBlockSize, &vfull[vs], pol);
+        }
         ++nv;
       }
       if (*abort_flag)   // let copies already in flight land before the CTA exits
-        for (int64_t i = (nv > VST ? nv - VST : 0); i < nv; ++i)
-          mbar_wait_drain(&vfull[i % VST], (i / VST) & 1);
+        for (int64_t i = (nv > NS ? nv - NS : 0); i < nv; ++i)
+          mbar_wait_drain(&vfull[i % NS], (i / NS) & 1);
     }
   } else if (F8 && warp >= 2 + NCW) {
     // ------------------------------------------ F8: widen E4M3 V pages to fp16 stages
@@ -1035,7 +1060,23 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     ReqWalker wq = walk;   // TSC: these warps also write each segment's query operand
     int64_t nseg = 0;
     bool q_ready = false;
-    for (int64_t g = g0, it = 0; g < g1; ++g, ++it) {
+    // SKIP: the kept pages, in order, until a stage whose info word is -1
+    for (int64_t n = 0; SKIP; ++n) {
+      const int vr = static_cast<int>(n % VRS), vs = static_cast<int>(n % VST);
+      bool ok = mbar_wait(&vfull[vr], (n / VRS) & 1, abort_flag, p.dev_err);
+      if (n >= VST) ok = mbar_wait(&vfree[vs], ((n / VST) - 1) & 1, abort_flag, p.dev_err) && ok;
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int nval = vinfo[vr];
+      if (nval < 0) break;
+      widen_v_boxes<S, FMT, 32 * NWW>(vraw + vr * L::VPS, vst + vs * S::VSTAGE_BYTES, nval, 0, WB, vt);
+      fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&vempty[vr]);   // this warp is done with the raw page
+        mbar_arrive(&vcvt[vs]);     // its part of the fp16 stage is ready
+      }
+    }
+    for (int64_t g = g0, it = 0; !SKIP && g < g1; ++g, ++it) {
       if constexpr (TSC) {
         wq.advance_to(g);
         if (q_builder && (g == g0 || g == wq.bstart)) {
@@ -1372,6 +1413,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
             if (nd < L::DS ||
                 mbar_wait(&decempty[ds], ((nd / L::DS) - 1) & 1, abort_flag, p.dev_err)) {
               dec_s[ds] = kph;
+              dec_n[ds] = bi.nvalid;
               mbar_arrive(&decfull[ds]);
             }
           }
@@ -1545,6 +1587,11 @@ cudaError_t prepare_attn(int device) {
   if (e == cudaSuccess)
     e = set(decode_main_kernel<S, RCP_PAGES_FP16, true>,
             DecodeSmem<S, RCP_PAGES_FP16, true>::ALLOC);
+  if (e == cudaSuccess)
+    e = set(decode_main_kernel<S, RCP_PAGES_FP8_E4M3, true>,
+            DecodeSmem<S, RCP_PAGES_FP8_E4M3, true>::ALLOC);
+  if (e == cudaSuccess)
+    e = set(decode_main_kernel<S, RCP_PAGES_INT4, true>, DecodeSmem<S, RCP_PAGES_INT4, true>::ALLOC);
   return e;
 }
 
@@ -1559,22 +1606,24 @@ cudaError_t launch_attn(const CUtensorMap& tmap_v, const CUtensorMap& tmap_k, co
   cudaError_t e = cudaSuccess;
   if (prof_start && (e = cudaEventRecord(prof_start, stream)) != cudaSuccess) return e;
   constexpr int F16 = RCP_PAGES_FP16, E4M3 = RCP_PAGES_FP8_E4M3, I4 = RCP_PAGES_INT4;
+  auto go = [&](auto kernel, int threads, int smem) {
+    return launch_pdl(kernel, dim3(p.parts), dim3(threads), smem, stream, pdl, tmap_v, tmap_k, p);
+  };
   if (p.page_format == E4M3)
-    e = launch_pdl(decode_main_kernel<S, E4M3, false>, dim3(p.parts),
-                   dim3(decode_threads<S, E4M3>()), DecodeSmem<S, E4M3>::ALLOC, stream, pdl,
-                   tmap_v, tmap_k, p);
+    e = p.sparse ? go(decode_main_kernel<S, E4M3, true>, decode_threads<S, E4M3, true>(),
+                      DecodeSmem<S, E4M3, true>::ALLOC)
+                 : go(decode_main_kernel<S, E4M3, false>, decode_threads<S, E4M3>(),
+                      DecodeSmem<S, E4M3>::ALLOC);
   else if (p.page_format == I4)
-    e = launch_pdl(decode_main_kernel<S, I4, false>, dim3(p.parts),
-                   dim3(decode_threads<S, I4>()), DecodeSmem<S, I4>::ALLOC, stream, pdl, tmap_v,
-                   tmap_k, p);
-  else if (p.sparse)
-    e = launch_pdl(decode_main_kernel<S, F16, true>, dim3(p.parts),
-                   dim3(decode_threads<S, F16, true>()), DecodeSmem<S, F16, true>::ALLOC, stream,
-                   pdl, tmap_v, tmap_k, p);
+    e = p.sparse ? go(decode_main_kernel<S, I4, true>, decode_threads<S, I4, true>(),
+                      DecodeSmem<S, I4, true>::ALLOC)
+                 : go(decode_main_kernel<S, I4, false>, decode_threads<S, I4>(),
+                      DecodeSmem<S, I4>::ALLOC);
   else
-    e = launch_pdl(decode_main_kernel<S, F16, false>, dim3(p.parts),
-                   dim3(decode_threads<S, F16>()), DecodeSmem<S, F16>::ALLOC, stream, pdl,
-                   tmap_v, tmap_k, p);
+    e = p.sparse ? go(decode_main_kernel<S, F16, true>, decode_threads<S, F16, true>(),
+                      DecodeSmem<S, F16, true>::ALLOC)
+                 : go(decode_main_kernel<S, F16, false>, decode_threads<S, F16>(),
+                      DecodeSmem<S, F16>::ALLOC);
   if (e != cudaSuccess) return e;
   if (prof_stop && (e = cudaEventRecord(prof_stop, stream)) != cudaSuccess) return e;
   return cudaSuccess;

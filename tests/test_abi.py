@@ -168,7 +168,8 @@ def test_prefill_crossover_and_reconstruct_workspace(lib):
 
 
 def test_sparse_decode_host_checks(lib):
-    """Threshold range, page format and workspace are checked before any CUDA call."""
+    """Threshold range and workspace are checked before any CUDA call, for every page
+    format."""
     from rank_compressed_paged_gb300 import _lib
     st, h = _create(lib, _lib, _cfg(_lib))
     b = ctypes.c_size_t()
@@ -183,16 +184,17 @@ def test_sparse_decode_host_checks(lib):
     assert lib.rcp_decode_attn_sparse(h, 0x1000, 0x2000, 64, 0x3000, 0, 0.01, None, 0x4000, ws,
                                       b.value, None) == _lib.RCP_OK   # empty batch
     lib.rcp_destroy_cache(h)
-    st, h8 = _create(lib, _lib, _cfg(_lib, fmt=_lib.RCP_PAGES_FP8_E4M3))
-    assert st == _lib.RCP_OK
-    assert lib.rcp_decode_attn_sparse(h8, 0x1000, 0x2000, 64, 0x3000, 16, 0.01, None, 0x4000, ws,
-                                      b.value, None) == _lib.RCP_ERR_UNSUPPORTED
-    lib.rcp_destroy_cache(h8)
-    st, h4 = _create(lib, _lib, _cfg(_lib, fmt=_lib.RCP_PAGES_INT4))
-    assert st == _lib.RCP_OK
-    assert lib.rcp_decode_attn_sparse(h4, 0x1000, 0x2000, 64, 0x3000, 16, 0.01, None, 0x4000, ws,
-                                      b.value, None) == _lib.RCP_ERR_UNSUPPORTED
-    lib.rcp_destroy_cache(h4)
+    for fmt in (_lib.RCP_PAGES_FP8_E4M3, _lib.RCP_PAGES_INT4):
+        # every page format is accepted: the same host checks, no CUDA call for an empty batch
+        st, hq = _create(lib, _lib, _cfg(_lib, fmt=fmt))
+        assert st == _lib.RCP_OK
+        assert lib.rcp_decode_attn_sparse(hq, 0x1000, 0x2000, 64, 0x3000, 16, 2.0, None, 0x4000,
+                                          ws, b.value, None) == _lib.RCP_ERR_INVALID_ARG
+        assert lib.rcp_decode_attn_sparse(hq, 0x1000, 0x2000, 64, 0x3000, 16, 0.01, None, 0x4000,
+                                          ws, 1024, None) == _lib.RCP_ERR_WORKSPACE
+        assert lib.rcp_decode_attn_sparse(hq, 0x1000, 0x2000, 64, 0x3000, 0, 0.01, None, 0x4000,
+                                          ws, b.value, None) == _lib.RCP_OK
+        lib.rcp_destroy_cache(hq)
 
 
 def test_reconstruct_workspace_grows_by_the_widened_pages_for_e4m3(lib):

@@ -186,16 +186,6 @@ def test_int4_decode_step_equals_append_then_decode():
     assert_close(ob.cpu().numpy(), ref, what="int4 step")
 
 
-def test_int4_cache_rejects_sparse_decode():
-    from rank_compressed_paged_gb300 import RcpError
-    inp = wl.make_decode_inputs(MAIN, [40, 7], seed=187)
-    c = inp.cache
-    kb, vb = _bytes(MAIN, c.k_pages, c.v_pages)
-    cache = _int4_cache(MAIN, inp.U_k, inp.W_v, kb, vb)
-    with pytest.raises(RcpError):
-        cache.decode_attn_sparse(t(inp.q), t(c.block_table), t(c.seq_lens), 1e-3)
-
-
 @pytest.mark.parametrize("variant", ["reconstruct", "rank"])
 @pytest.mark.parametrize("shape,prior,chunk,seed", [
     (TINY, [37, 0, 100, 5], [21, 16, 40, 0], 188),
