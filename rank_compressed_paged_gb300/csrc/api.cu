@@ -427,7 +427,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
         e = rcp::launch_widen<ShapeMain>(pw, wd.k16, wd.v16, wd.table16, max_pages, c->num_sms, s,
                                          pdl);
       if (e == cudaSuccess && recon)
-        e = rcp::launch_recon<ShapeMain>(vsrc, c->tmap_wv_mn, p, max_pages, s, pdl);
+        e = rcp::launch_recon<ShapeMain>(vsrc, c->tmap_wv_mn, p, max_pages, c->num_sms, s, pdl);
       if (e == cudaSuccess)
         e = rcp::launch_prefill<ShapeMain>(qhi_map, qlo_map, kmap, vals, c->tmap_wv_mn, p,
                                            max_tiles, s, pdl, recon);
@@ -442,7 +442,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
         e = rcp::launch_widen<ShapeTiny>(pw, wd.k16, wd.v16, wd.table16, max_pages, c->num_sms, s,
                                          pdl);
       if (e == cudaSuccess && recon)
-        e = rcp::launch_recon<ShapeTiny>(vsrc, c->tmap_wv_mn, p, max_pages, s, pdl);
+        e = rcp::launch_recon<ShapeTiny>(vsrc, c->tmap_wv_mn, p, max_pages, c->num_sms, s, pdl);
       if (e == cudaSuccess)
         e = rcp::launch_prefill<ShapeTiny>(qhi_map, qlo_map, kmap, vals, c->tmap_wv_mn, p,
                                            max_tiles, s, pdl, recon);

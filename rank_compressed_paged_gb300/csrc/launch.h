@@ -25,12 +25,13 @@ template <class S>
 cudaError_t launch_prefill(const CUtensorMap& qhi, const CUtensorMap& qlo, const CUtensorMap& kp,
                            const CUtensorMap& vp, const CUtensorMap& w, const AttnParams& p,
                            int max_tiles, cudaStream_t stream, bool pdl, bool recon);
-// V^ = C_v W_v for the pages of every request with chunk rows (max_pages bounds them).
+// V^ = C_v W_v for the pages of every request with chunk rows (max_pages bounds them), by
+// persistent CTA pairs (at most num_sms / 2).
 template <class S>
 cudaError_t prepare_recon();
 template <class S>
 cudaError_t launch_recon(const CUtensorMap& vp, const CUtensorMap& w_v_mn, const AttnParams& p,
-                         int64_t max_pages, cudaStream_t stream, bool pdl);
+                         int64_t max_pages, int num_sms, cudaStream_t stream, bool pdl);
 // E4M3 pages: fp16 copies of the batch's pages (plan order) and the re-addressed table.
 template <class S>
 cudaError_t launch_widen(const AttnParams& p, void* k16, void* v16, int32_t* table16,

@@ -9,14 +9,19 @@
 // R*d/(R-d) ~ 146 rows per request.
 //
 // The keys of all such requests, page after page in request order (prefix sums in
-// vcum), are the rows of one GEMM D[keys x H*d] = C_v[keys x R] * W_v[R x H*d]:
-//   * one CTA per (128 keys = 8 pages, 256 columns): A = the 8 pages' C_v rows, one
-//     16 x 64 tensor-map box per page per 64-wide k-block (K-major, 128-byte swizzle);
-//     B = W_v[k-block rows, 256 columns], four 64 x 64 boxes (MN-major);
-//   * tcgen05.mma M=128, N=256, K=16 steps into a 256-column TMEM accumulator, two
-//     pipeline stages; two CTAs share an SM so one's epilogue overlaps the other's loop;
-//   * the epilogue writes V^ rows as fp16, zero for the slots of a page past the end of
-//     its sequence (so that the attention can never meet 0 * NaN there).
+// vcum), are the rows of one GEMM D[keys x H*d] = C_v[keys x R] * W_v[R x H*d], cut into
+// tiles of 256 keys (16 pages) x 256 columns:
+//   * persistent CTA pairs (2-CTA clusters, one CTA per SM) take the tiles in turn; each
+//     CTA stages its 128 keys' C_v rows (A: one 16 x 64 tensor-map box per page per 64-wide
+//     k-block, K-major, 128-byte swizzle) and half of the W_v tile (B: 128 columns, two
+//     64 x 64 boxes, MN-major), so a k-block costs each SM 32 KB of operands instead of
+//     the 48 KB of a one-CTA 128 x 256 tile;
+//   * the even CTA issues tcgen05.mma.cta_group::2, M=256, N=256, K=16 steps; both CTAs'
+//     copies complete on the even CTA's stage barrier and each commit frees the stage in
+//     both CTAs; a CTA's tensor memory holds two 256-column accumulators of its 128 rows,
+//     so the epilogue of one tile overlaps the MMAs of the next;
+//   * four epilogue warps write V^ rows as fp16, zero for the slots of a page past the end
+//     of its sequence (so that the attention can never meet 0 * NaN there).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -32,26 +37,37 @@
 
 namespace rcp {
 
-constexpr int kRcThreads = 128;   // warp 0 copies, warp 1 MMAs, all four the epilogue
+// warp 0 copies, warp 1 issues the MMAs (even CTA), warps 2-5 the epilogue, warp 6 looks
+// up the pages of the tiles ahead
+constexpr int kRcThreads = 224;
+constexpr int kRcRing = 4;   // tiles whose page rows are looked up ahead
 
 template <class S>
 struct ReconSmem {
   using C = ReconCfg<S>;
   static constexpr int A_BYTES = C::MT * 128;          // 128 keys x 64 ranks
-  static constexpr int B_BYTES = C::NT * 128;          // 64 ranks x 256 columns
+  static constexpr int B_BYTES = C::NTC * 128;         // 64 ranks x 128 columns
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int BAR_OFF = C::STG * STAGE;       // full[STG], empty[STG], acc
-  static constexpr int INFO_OFF = BAR_OFF + (2 * C::STG + 1) * 8;   // [8] valid tokens / page
-  static constexpr int MISC_OFF = INFO_OFF + 8 * 4;    // tmem slot, abort flag
+  // the epilogue warps' staging buffers: 32 rows x 64 columns of fp16 each (16-byte chunk c
+  // of row r at chunk c ^ (r % 8)), so that V^ leaves in whole 128-byte row pieces
+  static constexpr int EPI_OFF = C::STG * STAGE;
+  static constexpr int EPI_BYTES = 32 * 128;
+  // the page rows of the next tiles: [kRcRing][8] TMA row coordinates
+  static constexpr int ROW_OFF = EPI_OFF + 4 * EPI_BYTES;
+  // full[STG] (even CTA), empty[STG], tfull[2], tempty[2] (even CTA), rfull / rempty[kRcRing]
+  static constexpr int BAR_OFF = ROW_OFF + kRcRing * 8 * 4;
+  static constexpr int MISC_OFF = BAR_OFF + (2 * C::STG + 4 + 2 * kRcRing) * 8;   // tmem slot, abort
   static constexpr int TOTAL = MISC_OFF + 16;
   static constexpr int ALLOC = TOTAL + 1024;
-  static constexpr int TMEM_COLS = C::NT;
+  static constexpr int TMEM_COLS = 2 * C::NT;          // two accumulators
   static_assert(STAGE % 1024 == 0, "stages keep 1024-byte alignment");
-  static_assert(2 * ALLOC <= 228 * 1024, "two CTAs per SM");
+  // more than half an SM's shared memory: one CTA per SM, so the two CTAs of a pair always
+  // sit on two SMs and each has the SM's whole tensor memory
+  static_assert(2 * ALLOC > 228 * 1024 && ALLOC <= 227 * 1024, "one CTA per SM");
 };
 
 template <class S>
-__global__ void __launch_bounds__(kRcThreads, 2)
+__global__ void __launch_bounds__(kRcThreads, 1)
     recon_kernel(const __grid_constant__ CUtensorMap vp_map, const __grid_constant__ CUtensorMap w_map,
                  const AttnParams p) {
   using C = ReconCfg<S>;
@@ -62,34 +78,47 @@ __global__ void __launch_bounds__(kRcThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
   uint64_t* empty = full + C::STG;
-  uint64_t* accb = empty + C::STG;
-  int* valid_s = reinterpret_cast<int*>(sm + L::INFO_OFF);
+  uint64_t* tfull = empty + C::STG;    // [2] accumulator b holds a finished tile
+  uint64_t* tempty = tfull + 2;        // [2] ... and both CTAs' epilogues have read it
+  uint64_t* rfull = tempty + 2;        // [kRcRing] a tile's page rows are written
+  uint64_t* rempty = rfull + kRcRing;  // [kRcRing] ... and were read
+  int32_t* rows_s = reinterpret_cast<int32_t*>(sm + L::ROW_OFF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x / NTN, nt = blockIdx.x % NTN;   // CTAs of one key tile adjacent
+  const uint32_t rank = cluster_ctarank();                    // 0: issues the MMAs
+  const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;   // pair, pairs
 
   griddep_wait();   // page prefix sums (plan) and the appended chunk are visible
   griddep_launch();
   const int64_t total = p.vcum[p.batch];
-  const int64_t g0 = static_cast<int64_t>(tile) * BPT;       // first page of the tile
-  if (g0 >= total) return;                                   // uniform over the CTA
+  const int64_t ntiles = (total + 2 * BPT - 1) / (2 * BPT) * NTN;
+  if (cid >= ntiles) return;   // uniform over the pair, before any cluster operation
+  // tile t: keys of pages [16 (t / NTN), +16), columns [256 (t % NTN), +256); this CTA's
+  // pages start at 16 (t / NTN) + 8 rank
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STG; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accb, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * 4);   // the four epilogue warps of each CTA
+    }
+    for (int r = 0; r < kRcRing; ++r) {
+      mbar_init(&rfull[r], 1);
+      mbar_init(&rempty[r], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, L::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist before any copy or arrival reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -97,110 +126,172 @@ __global__ void __launch_bounds__(kRcThreads, 2)
     // ------------------------------------------------------------------ copies
     prefetch_tmap(&vp_map);
     prefetch_tmap(&w_map);
-    int32_t phys[BPT];
-    int nload = 0;
+    int64_t n = 0;   // k-blocks issued (stage n % STG)
+    bool ok = true;
+    for (int64_t t = cid, i = 0; ok && t < ntiles; t += ncl, ++i) {
+      const int r = static_cast<int>(i % kRcRing);
+      if (!mbar_wait(&rfull[r], (i / kRcRing) & 1, abort_flag, p.dev_err)) break;
+      int32_t yrow[BPT];
 #pragma unroll
-    for (int jb = 0; jb < BPT; ++jb) {
-      const int64_t g = g0 + jb;
-      int32_t id = -1, nvalid = 0;
+      for (int jb = 0; jb < BPT; ++jb) yrow[jb] = rows_s[r * 8 + jb];
+      mbar_arrive(&rempty[r]);
+      const int x0 = static_cast<int>(t % NTN) * C::NT + static_cast<int>(rank) * C::NTC;
+      for (int kb = 0; kb < C::KB; ++kb, ++n) {
+        const int s = static_cast<int>(n % C::STG);
+        if (n >= C::STG &&
+            !mbar_wait(&empty[s], ((n / C::STG) - 1) & 1, abort_flag, p.dev_err)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = sm + s * L::STAGE;
+        const uint32_t fb = map_to_rank(smem_u32(&full[s]), 0);
+        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * L::STAGE);
+#pragma unroll
+        for (int jb = 0; jb < BPT; ++jb)
+          tma_load_2d_pair(st + jb * 2048, &vp_map, kb * 64, yrow[jb], fb);
+#pragma unroll
+        for (int q = 0; q < C::NTC / 64; ++q)
+          tma_load_2d_pair(st + L::A_BYTES + q * 8192, &w_map, x0 + q * 64, kb * 64, fb);
+      }
+    }
+    // the commits of the last stages (arrivals on this CTA's barriers) land before it exits
+    for (int64_t i = (n > C::STG ? n - C::STG : 0); i < n; ++i)
+      mbar_wait_drain(&empty[i % C::STG], (i / C::STG) & 1);
+  } else if (warp == 6) {
+    // ------------------------------------------------------------------- page lookups
+    // lane j resolves page j of this CTA's half of each tile: its TMA row, or row -16 (all
+    // out of bounds: the copy fills zeros and still counts its full bytes, so every stage
+    // completes on a fixed byte count) past the batch's pages or for a rejected id
+    for (int64_t t = cid, i = 0; t < ntiles; t += ncl, ++i) {
+      const int r = static_cast<int>(i % kRcRing);
+      const bool ok = i < kRcRing ||
+                      mbar_wait(&rempty[r], ((i / kRcRing) - 1) & 1, abort_flag, p.dev_err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (lane < BPT) {
+        int32_t y = -kBlockSize;
+        const int64_t g = (t / NTN) * 2 * BPT + rank * BPT + lane;
+        if (g < total) {
+          int lo = 0, hi = p.batch;                 // request b with vcum[b] <= g < vcum[b+1]
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.vcum[mid] <= g) lo = mid; else hi = mid;
+          }
+          const int32_t id = p.block_table[static_cast<int64_t>(lo) * p.bt_stride + (g - p.vcum[lo])];
+          if (id >= 0 && id < p.num_blocks) y = id * kBlockSize;
+          else if (t % NTN == 0) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
+        }
+        rows_s[r * 8 + lane] = y;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull[r]);
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ------------------------------------------------------------------- MMAs
+    constexpr uint32_t idesc = make_idesc_f16(2 * C::MT, C::NT, false, true);
+    int64_t n = 0;
+    bool ok = true;
+    for (int64_t t = cid, i = 0; ok && t < ntiles; t += ncl, ++i) {
+      const int b = static_cast<int>(i & 1);
+      // both CTAs' epilogues have read this accumulator's previous tile
+      if (i >= 2 && !mbar_wait(&tempty[b], ((i >> 1) - 1) & 1, abort_flag, p.dev_err)) break;
+      tc_fence_after();
+      const uint32_t dt = tmem + b * C::NT;
+      for (int kb = 0; kb < C::KB; ++kb, ++n) {
+        const int s = static_cast<int>(n % C::STG);
+        if (!mbar_wait(&full[s], (n / C::STG) & 1, abort_flag, p.dev_err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sm + s * L::STAGE);
+        const uint32_t b0 = a0 + L::A_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {   // four K=16 steps per 64-wide k-block
+          const uint64_t ad = make_sdesc(a0 + k * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = make_sdesc(b0 + k * 2048, 8192, 1024, kSwizzle128B);
+          umma_f16_pair(dt, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit_pair(&empty[s], 0x3);
+      }
+      if (ok) umma_commit_pair(&tfull[b], 0x3);
+    }
+    // the last commits land before this CTA (and its peer, through the final cluster
+    // barrier) goes on
+    if (n > 0) mbar_wait_drain(&empty[(n - 1) % C::STG], ((n - 1) / C::STG) & 1);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------------- epilogue
+    // warp w reads TMEM lane quarter w % 4: rows 32 (w % 4) .. of this CTA's 128 keys.  A
+    // 64-column chunk goes TMEM -> registers -> the warp's staging buffer (row per lane), then
+    // leaves as 8 stores of 4 rows x 128 bytes each.
+    const int q = warp & 3, row = q * 32 + lane;
+    const uint32_t tarr = map_to_rank(smem_u32(&tempty[0]), 0);
+    uint8_t* ebuf = sm + L::EPI_OFF + (warp - 2) * L::EPI_BYTES;
+    for (int64_t t = cid, i = 0; t < ntiles; t += ncl, ++i) {
+      const int b = static_cast<int>(i & 1);
+      // this row's page and whether it holds a token of its sequence in a valid block,
+      // resolved before the accumulator is waited for
+      const int64_t g = (t / NTN) * 2 * BPT + rank * BPT + row / kBlockSize;
+      const int tok = row % kBlockSize;
+      bool keep = false;
       if (g < total) {
-        int lo = 0, hi = p.batch;                 // request b with vcum[b] <= g < vcum[b+1]
+        int lo = 0, hi = p.batch;
         while (hi - lo > 1) {
           const int mid = (lo + hi) >> 1;
           if (p.vcum[mid] <= g) lo = mid; else hi = mid;
         }
         const int64_t blk = g - p.vcum[lo];
-        id = p.block_table[static_cast<int64_t>(lo) * p.bt_stride + blk];
-        if (id < 0 || id >= p.num_blocks) {
-          atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
-          id = -1;
-        } else {
-          const int64_t left = p.seq_lens[lo] - blk * kBlockSize;
-          nvalid = static_cast<int32_t>(left < kBlockSize ? left : kBlockSize);
-        }
+        const int32_t id = p.block_table[static_cast<int64_t>(lo) * p.bt_stride + blk];
+        keep = id >= 0 && id < p.num_blocks && blk * kBlockSize + tok < p.seq_lens[lo];
       }
-      phys[jb] = id;
-      valid_s[jb] = nvalid;
-      nload += id >= 0;
-    }
-    int issued = 0;
-    for (int kb = 0; kb < C::KB; ++kb) {
-      const int s = kb % C::STG;
-      if (kb >= C::STG &&
-          !mbar_wait(&empty[s], ((kb / C::STG) - 1) & 1, abort_flag, p.dev_err))
+      // the row this lane stores in the copy-out: 4 rows per instruction, 8 lanes per row
+      const int orow = lane >> 3, ochunk = lane & 7;
+      const int64_t g_first = (t / NTN) * 2 * BPT + rank * BPT + (q * 32) / kBlockSize;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], (i >> 1) & 1, abort_flag, p.dev_err)))
         break;
-      uint8_t* st = sm + s * L::STAGE;
-      mbar_arrive_expect_tx(&full[s], nload * 2048 + L::B_BYTES);
-#pragma unroll
-      for (int jb = 0; jb < BPT; ++jb)
-        if (phys[jb] >= 0)
-          tma_load_2d(st + jb * 2048, &vp_map, kb * 64, phys[jb] * kBlockSize, &full[s]);
-#pragma unroll
-      for (int q = 0; q < C::NT / 64; ++q)
-        tma_load_2d(st + L::A_BYTES + q * 8192, &w_map, nt * C::NT + q * 64, kb * 64, &full[s]);
-      ++issued;
-    }
-    if (*abort_flag)
-      for (int i = (issued > C::STG ? issued - C::STG : 0); i < issued; ++i)
-        mbar_wait_drain(&full[i % C::STG], (i / C::STG) & 1);
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------------- MMAs
-    constexpr uint32_t idesc = make_idesc_f16(128, C::NT, false, true);
-    int kb = 0;
-    for (; kb < C::KB; ++kb) {
-      const int s = kb % C::STG;
-      if (!mbar_wait(&full[s], (kb / C::STG) & 1, abort_flag, p.dev_err)) break;
       tc_fence_after();
-      const uint32_t a0 = smem_u32(sm + s * L::STAGE);
-      const uint32_t b0 = a0 + L::A_BYTES;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {   // four K=16 steps per 64-wide k-block
-        const uint64_t ad = make_sdesc(a0 + k * 32, 16, 1024, kSwizzle128B);
-        const uint64_t bd = make_sdesc(b0 + k * 2048, 8192, 1024, kSwizzle128B);
-        umma_f16(tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-      }
-      umma_commit(&empty[s]);
-    }
-    umma_commit(accb);
-    if (kb < C::KB) mbar_wait_drain(accb, 0);
-  }
-  __syncwarp();
-  __syncthreads();   // valid_s is written
-
-  // ------------------------------------------------------------------- epilogue
-  // TMEM lane = key row of the tile; warp-uniform guards around the collective loads
-  const bool have = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort_flag, p.dev_err));
-  tc_fence_after();
-  const int row = warp * 32 + lane;
-  const int64_t g = g0 + row / kBlockSize;
-  const bool in_range = g < total;
-  const bool keep = row % kBlockSize < valid_s[row / kBlockSize];
-  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  __half* dst = static_cast<__half*>(p.vhat) + (g * kBlockSize + row % kBlockSize) * HD + nt * C::NT;
+      const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * C::NT;
 #pragma unroll 1
-  for (int c0 = 0; c0 < C::NT; c0 += 16) {
-    float v[16];
-    if (have) {
-      tmem_ld16(trow + c0, v);
-      tmem_wait_ld();
-    }
-    uint32_t w8[8];
+      for (int c64 = 0; c64 < C::NT; c64 += 64) {
 #pragma unroll
-    for (int e = 0; e < 16; e += 2) {
-      const __half2 hv = (have && keep) ? __floats2half2_rn(v[e], v[e + 1])
-                                        : __floats2half2_rn(0.f, 0.f);
-      w8[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
-    }
-    if (in_range) {
-      *reinterpret_cast<uint4*>(dst + c0) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-      *reinterpret_cast<uint4*>(dst + c0 + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+        for (int c16 = 0; c16 < 64; c16 += 16) {
+          float v[16];
+          tmem_ld16(trow + c64 + c16, v);
+          tmem_wait_ld();
+          uint32_t w8[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const __half2 hv = keep ? __floats2half2_rn(v[e], v[e + 1]) : __floats2half2_rn(0.f, 0.f);
+            w8[e / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          const int c0 = c16 / 8;   // first 16-byte chunk of these 16 columns
+          *reinterpret_cast<uint4*>(ebuf + lane * 128 + (((c0) ^ (lane & 7)) << 4)) =
+              make_uint4(w8[0], w8[1], w8[2], w8[3]);
+          *reinterpret_cast<uint4*>(ebuf + lane * 128 + (((c0 + 1) ^ (lane & 7)) << 4)) =
+              make_uint4(w8[4], w8[5], w8[6], w8[7]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r0 = 0; r0 < 32; r0 += 4) {
+          const int r = r0 + orow;   // row of the warp's 32
+          const uint4 val = *reinterpret_cast<const uint4*>(ebuf + r * 128 + ((ochunk ^ (r & 7)) << 4));
+          const int64_t gr = g_first + r / kBlockSize;
+          if (gr < total)
+            *reinterpret_cast<uint4*>(static_cast<__half*>(p.vhat) +
+                                      (gr * kBlockSize + r % kBlockSize) * HD +
+                                      static_cast<int>(t % NTN) * C::NT + c64 + ochunk * 8) = val;
+        }
+        __syncwarp();   // the buffer is rewritten by the next chunk
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tarr + b * 8);   // this warp is done with buffer b
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // neither CTA leaves (or frees its columns) while the pair is busy
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, L::TMEM_COLS);
+    tmem_dealloc_pair(tmem, L::TMEM_COLS);
   }
 }
 
@@ -323,22 +414,36 @@ cudaError_t prepare_recon() {
 // actual count exit at once.
 template <class S>
 cudaError_t launch_recon(const CUtensorMap& vp, const CUtensorMap& w_v_mn, const AttnParams& p,
-                         int64_t max_pages, cudaStream_t stream, bool pdl) {
+                         int64_t max_pages, int num_sms, cudaStream_t stream, bool pdl) {
   using C = ReconCfg<S>;
-  const int64_t tiles = (max_pages + C::MT / kBlockSize - 1) / (C::MT / kBlockSize);
-  const int64_t grid = tiles * (S::H * S::D / C::NT);
+  constexpr int64_t PAGES = 2 * C::MT / kBlockSize;   // pages per tile
+  const int64_t tiles = (max_pages + PAGES - 1) / PAGES * (S::H * S::D / C::NT);
+  const int64_t pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;   // persistent
+  const int64_t grid = 2 * pairs;
   if (grid <= 0) return cudaSuccess;
-  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  return launch_pdl(recon_kernel<S>, dim3(static_cast<unsigned>(grid)), dim3(kRcThreads),
-                    ReconSmem<S>::ALLOC, stream, pdl, vp, w_v_mn, p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kRcThreads);
+  cfg.dynamicSmemBytes = ReconSmem<S>::ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, recon_kernel<S>, vp, w_v_mn, p);
 }
 
 template cudaError_t prepare_recon<ShapeMain>();
 template cudaError_t prepare_recon<ShapeTiny>();
 template cudaError_t launch_recon<ShapeMain>(const CUtensorMap&, const CUtensorMap&,
-                                             const AttnParams&, int64_t, cudaStream_t, bool);
+                                             const AttnParams&, int64_t, int, cudaStream_t, bool);
 template cudaError_t launch_recon<ShapeTiny>(const CUtensorMap&, const CUtensorMap&,
-                                             const AttnParams&, int64_t, cudaStream_t, bool);
+                                             const AttnParams&, int64_t, int, cudaStream_t, bool);
 template cudaError_t launch_widen<ShapeMain>(const AttnParams&, void*, void*, int32_t*, int64_t, int,
                                              cudaStream_t, bool);
 template cudaError_t launch_widen<ShapeTiny>(const AttnParams&, void*, void*, int32_t*, int64_t, int,

@@ -74,12 +74,12 @@ struct PrefillCfg {
   static_assert(S::R % RQ == 0 && RQ % 64 == 0 && S::RK <= 64 && S::D % 64 == 0, "prefill shape");
 };
 
-// Reconstructing prefill: V^ = C_v W_v for every cached key of the batch, 128 keys (8
-// pages) x 256 columns of H*d per CTA, K = R in 64-wide k-blocks, two pipeline stages
-// (two CTAs share an SM, so one's epilogue overlaps the other's main loop).
+// Reconstructing prefill: V^ = C_v W_v for every cached key of the batch, 256 keys (16
+// pages) x 256 columns of H*d per CTA pair (a 2-CTA cluster: 128 keys and 128 of the W_v
+// columns staged in each CTA), K = R in 64-wide k-blocks, STG pipeline stages.
 template <class S>
 struct ReconCfg {
-  static constexpr int MT = 128, NT = 256, KB = S::R / 64, STG = 2;
+  static constexpr int MT = 128, NT = 256, NTC = NT / 2, KB = S::R / 64, STG = 6;
   static_assert((S::H * S::D) % NT == 0 && S::R % 64 == 0, "reconstruct tiling");
 };
 
