@@ -667,8 +667,8 @@ def run_ours(args, rank, world, local_rank):
         n_pages = sum(wl.blocks_needed(int(x)) for x in L)
         n_kept = sum(int(kept[b, :wl.blocks_needed(int(L[b]))].sum()) for b in range(BATCH))
         # keys of every token + values of the kept pages' tokens
-        read_bytes = int(L.sum()) * SHAPE["num_heads"] * SHAPE["rank_k"] * 2 + \
-            kept_tok * SHAPE["rank_v"] * 2
+        read_bytes = int(L.sum()) * wl.key_bytes_per_token(SHAPE, args.pages) + \
+            kept_tok * wl.value_bytes_per_token(SHAPE, args.pages)
         sparse = {"threshold": args.sparse, "pages": n_pages,
                   "pages_skipped_frac": round(1 - n_kept / n_pages, 4),
                   "bytes_read": read_bytes,
@@ -764,8 +764,11 @@ def run_ours(args, rank, world, local_rank):
                         "tflops_step": round(world * flops["total"] / (step_ms * 1e-3) / 1e12, 2),
                         "pv_tflops_kernel": round(flops["pv"] / (kern_ms * 1e-3) / 1e12, 2),
                         "note": "P*C_v on tcgen05 (fp16 in, fp32 accumulation); scores on " +
-                                ("tcgen05 (E4M3 keys x a four-term E4M3 query split)"
-                                 if args.pages == "fp8_e4m3" else "CUDA cores") +
+                                ("CUDA cores" if args.pages == "fp16" or args.sparse is not None
+                                 else "tcgen05 (E4M3 keys x a four-term E4M3 query split)"
+                                 if args.pages == "fp8_e4m3"
+                                 else "tcgen05 (4-bit codes widened to E4M3 x a four-term E4M3 "
+                                      "query split, times the row scale)") +
                                 "; query / output projections and the append on tcgen05"},
         "sparse": sparse,
         "gpu_launches": args.steps * LAUNCHES_PER_DECODE_STEP,
@@ -973,8 +976,6 @@ def main():
     args = ap.parse_args()
     BATCH, SEQ = args.batch, args.seq_len
     PEAKED = args.peaked
-    if args.sparse is not None and args.pages != "fp16":
-        ap.error("--sparse needs fp16 pages")
     if args.workload == "prefill" and args.pages == "int4":
         ap.error("the prefill reads fp16 or E4M3 pages")
     if args.ragged:

@@ -146,3 +146,15 @@ def test_bench_int4_page_preparation_matches_the_oracle_encoding():
     ko, vo = orc.int4_pack_pages(kc, ks, vc, vs)
     assert np.array_equal(kb.numpy(), ko)
     assert np.array_equal(vb.numpy(), vo)
+
+
+def test_key_and_value_bytes_per_token_split_the_page_bytes():
+    """Per cached token at (32, 128, 64, 1024): fp16 4096 + 2048, E4M3 2048 + 1024, 4-bit
+    (32*64/2 code bytes + 32 fp16 row scales) + (512 code bytes + 16 fp16 group scales)."""
+    import workloads as wl
+    s = wl.SHAPES["mha32"]
+    want = {"fp16": (4096, 2048), "fp8_e4m3": (2048, 1024), "int4": (1088, 544)}
+    for pages, (k, v) in want.items():
+        assert wl.key_bytes_per_token(s, pages) == k
+        assert wl.value_bytes_per_token(s, pages) == v
+        assert wl.page_bytes_per_token(s, pages) == k + v

@@ -391,18 +391,35 @@ def make_paged_cache_device(seq_lens, shape: dict, seed: int, device="cuda",
     return kp, vp, table, seq_lens
 
 
-def page_bytes_per_token(shape: dict, pages: str = "fp16") -> int:
-    """Bytes of K and V pages per cached token: (H*r_k + R) coefficients at 2 bytes (fp16)
-    or 1 (E4M3); 4-bit pages hold half a byte per coefficient plus an fp16 scale per key
-    row of a head and per 64 value coefficients."""
-    H, rk, R = shape["num_heads"], shape["rank_k"], shape["rank_v"]
+def key_bytes_per_token(shape: dict, pages: str = "fp16") -> int:
+    """Bytes of K pages per cached token: H*r_k coefficients at 2 bytes (fp16) or 1 (E4M3);
+    4-bit pages hold half a byte per coefficient plus an fp16 scale per key row of a head."""
+    H, rk = shape["num_heads"], shape["rank_k"]
     if pages == "fp16":
-        return (H * rk + R) * 2
+        return H * rk * 2
     if pages == "fp8_e4m3":
-        return H * rk + R
+        return H * rk
     if pages == "int4":
-        return H * rk // 2 + 2 * H + R // 2 + 2 * (R // 64)
+        return H * rk // 2 + 2 * H
     raise ValueError(pages)
+
+
+def value_bytes_per_token(shape: dict, pages: str = "fp16") -> int:
+    """Bytes of V pages per cached token: R coefficients at 2 bytes (fp16) or 1 (E4M3);
+    4-bit pages hold half a byte per coefficient plus an fp16 scale per 64 of them."""
+    R = shape["rank_v"]
+    if pages == "fp16":
+        return R * 2
+    if pages == "fp8_e4m3":
+        return R
+    if pages == "int4":
+        return R // 2 + 2 * (R // 64)
+    raise ValueError(pages)
+
+
+def page_bytes_per_token(shape: dict, pages: str = "fp16") -> int:
+    """Bytes of K and V pages per cached token."""
+    return key_bytes_per_token(shape, pages) + value_bytes_per_token(shape, pages)
 
 
 def algorithmic_bytes_decode(shape: dict, seq_lens, pages: str = "fp16") -> int:
