@@ -201,8 +201,8 @@ constexpr int kAppendSetSize = 1 << kAppendSetBits;   // a step appending more t
 // and a key row's score is further multiplied by the row's scale.
 template <class S, int FMT, bool SKIP>
 constexpr bool decode_tensor_scores() {
-  return (FMT == RCP_PAGES_FP8_E4M3 || FMT == RCP_PAGES_INT4) && S::RK == 64 &&
-         S::H % 16 == 0 && !SKIP;
+  return (FMT == RCP_PAGES_FP8_E4M3 || (FMT == RCP_PAGES_INT4 && !SKIP)) && S::RK == 64 &&
+         S::H % 16 == 0;
 }
 
 template <class S, int FMT, bool SKIP = false>
@@ -214,6 +214,10 @@ struct DecodeSmem {
   static constexpr int KST = F8 && !TSC ? 3 : 2;                    // key page stages
   static constexpr int VST = 2;                                     // fp16 V stages (MMA A)
   static constexpr int VRS = F8 ? 3 : VST;                          // stages V copies land in
+  // P buffers: SKIP keeps four, so the compute warps can run four kept pages ahead of the
+  // value MMAs while those pages' values are fetched (a kept page's value copy starts only
+  // once the page is decided)
+  static constexpr int NPB = SKIP ? 4 : 2;
   static constexpr int KP = FMT == RCP_PAGES_FP8_E4M3 ? S::KPAGE_BYTES / 2   // bytes per K page
                            : FMT == RCP_PAGES_INT4 ? static_cast<int>(Int4Page<S>::KBYTES)
                                                    : S::KPAGE_BYTES;
@@ -226,7 +230,7 @@ struct DecodeSmem {
   static constexpr int KRPS = (KP + 127) & ~127;
   static constexpr int KPS = I4T ? OPB : KRPS;
   static constexpr int VPS = (VP + 127) & ~127;
-  static constexpr int NBAR = 2 * KST + 2 * VRS + 4 + (F8 ? 2 * VST : 0) + (SKIP ? 2 * DS : 0) +
+  static constexpr int NBAR = 2 * KST + 2 * VRS + 2 * NPB + (F8 ? 2 * VST : 0) + (SKIP ? 2 * DS : 0) +
                               (TSC ? 8 : 0) + (I4T ? 2 * KST : 0);
   static constexpr int P_BYTES = S::HP * 16 * 2;
   static constexpr int V_OFF = 0;                                   // 1024-aligned stages
@@ -234,7 +238,7 @@ struct DecodeSmem {
   static constexpr int VR_OFF = K_OFF + KST * KPS;                  // raw quantized V stages
   static constexpr int KR_OFF = VR_OFF + (F8 ? VRS * VPS : 0);      // I4T: raw key stages
   static constexpr int P_OFF = KR_OFF + (I4T ? KST * KRPS : 0);
-  static constexpr int Q_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int Q_OFF = P_OFF + NPB * P_BYTES;
   // TSC: the query operand ([H/8 groups][32 rows][r_k] E4M3, K-major without swizzle:
   // 8-row x 16-byte core matrices, 128 bytes apart along K, 512 along the rows; one buffer,
   // rewritten once the previous segment's scoring MMAs completed) and the score factors
@@ -250,8 +254,9 @@ struct DecodeSmem {
   static constexpr int INFO_OFF = MISC_OFF + 16;                    // valid tokens per stage:
   // K stages, then V; SKIP adds the physical block of each K stage, the decision ring and
   // the info word of each P buffer; TSC the valid tokens of each score buffer; I4T those of
-  // each operand stage; SKIP the valid tokens of each decision
-  static constexpr int INFO_BYTES = (2 * KST + VRS + DS + 4 + KST + DS) * 4;
+  // each operand stage; SKIP the valid tokens of each decision and (TSC) the physical
+  // block of each score buffer
+  static constexpr int INFO_BYTES = (2 * KST + VRS + DS + NPB + 2 + KST + DS + 2) * 4;
   // TMEM: the value accumulator [NCHUNK x 128 lanes][HP], then (TSC) two score buffers of
   // H/8 groups x 32 columns
   static constexpr int SCOL = S::NCHUNK * S::HP;
@@ -594,11 +599,12 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   uint64_t* kempty = kfull + KST;         // [KST] the compute warps scored the page
   uint64_t* vfull = kempty + KST;         // [VRS] a V page landed
   uint64_t* vempty = vfull + VRS;         // [VRS] its stage is free (MMA, or F8: widened)
-  uint64_t* pfull = vempty + VRS;         // [2]
-  uint64_t* pfree = pfull + 2;            // [2]
-  uint64_t* vcvt = pfree + 2;             // F8 [VST] fp16 V stage written by warps 6-7
+  constexpr int NPB = L::NPB;
+  uint64_t* pfull = vempty + VRS;         // [NPB]
+  uint64_t* pfree = pfull + NPB;          // [NPB]
+  uint64_t* vcvt = pfree + NPB;           // F8 [VST] fp16 V stage written by the widening warps
   uint64_t* vfree = vcvt + VST;           // F8 [VST] fp16 V stage read by its MMAs
-  uint64_t* decfull = pfree + 2 + (F8 ? 2 * VST : 0);   // SKIP [DS] a decision was posted
+  uint64_t* decfull = pfree + NPB + (F8 ? 2 * VST : 0);   // SKIP [DS] a decision was posted
   uint64_t* decempty = decfull + L::DS;                  // SKIP [DS] ... and taken
   uint64_t* sfull = decfull + (SKIP ? 2 * L::DS : 0);    // TSC [2] a page's scores are in TMEM
   uint64_t* sfree = sfull + 2;                           // TSC [2] ... and were read
@@ -611,6 +617,10 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   // F8: V boxes widened by warps 10-11; the compute warps widen the remaining ones (a
   // split measured to balance the two groups' time per block)
   constexpr int NWW = decode_widen_warps<S, FMT, SKIP>();   // widening warps NCW+2 ..
+  // warps that widen V pages: all widening warps, but with tensor-core scoring and
+  // skipping the first two build the query operands only (they follow every page, the
+  // others the kept pages)
+  constexpr int NVW = (TSC && SKIP) ? NWW - 2 : NWW;
   // (4-bit pages: the widening warps also widen the key codes, so the compute warps take
   // 10 of the 16 value boxes: measured 521 us at batch 64 x 8192 against 588 us for none)
   // (SKIP: all of them, in the order of the kept pages)
@@ -629,9 +639,10 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   int* kphys = vinfo + VRS;
   int* dec_s = kphys + KST;
   int* pinfo = dec_s + L::DS;
-  int* sinfo = pinfo + 2;   // TSC: valid tokens of the page in each score buffer
+  int* sinfo = pinfo + NPB; // TSC: valid tokens of the page in each score buffer
   int* oinfo = sinfo + 2;   // I4T: valid tokens of the page in each operand stage
   int* dec_n = oinfo + KST; // SKIP: valid tokens of each kept page of the decision ring
+  int* sphys = dec_n + L::DS;   // SKIP + TSC: physical block of the page in each score buffer
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -658,15 +669,15 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     }
     for (int i = 0; i < VRS; ++i) {
       mbar_init(&vfull[i], 1);
-      mbar_init(&vempty[i], F8 ? NWW + (WB < S::NBOX ? NCW : 0) : 1);
+      mbar_init(&vempty[i], F8 ? NVW + (WB < S::NBOX ? NCW : 0) : 1);
     }
     if constexpr (F8) {
       for (int i = 0; i < VST; ++i) {
-        mbar_init(&vcvt[i], NWW);
+        mbar_init(&vcvt[i], NVW);
         mbar_init(&vfree[i], 1);
       }
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NPB; ++i) {
       mbar_init(&pfull[i], NCW);
       mbar_init(&pfree[i], 1);
     }
@@ -685,7 +696,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   }
   // Zero both P buffers (padded head rows stay zero) and any part of a V stage that no
   // copy fills (value rank below a multiple of 128: those MMA rows are never stored).
-  for (int i = threadIdx.x; i < 2 * L::P_BYTES / 16; i += NTHR)
+  for (int i = threadIdx.x; i < NPB * L::P_BYTES / 16; i += NTHR)
     reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0, 0, 0, 0);
   if constexpr (S::NBOX < 2 * S::NCHUNK) {
     constexpr int ZB = (2 * S::NCHUNK - S::NBOX) * 2048 / 16;
@@ -926,12 +937,12 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc_f16(128, HP, /*a_mn_major=*/true, /*b_mn_major=*/false);
       int64_t issued = 0;
-      if constexpr (SKIP) {
+      if constexpr (SKIP && !TSC) {
         // kept pages only, in order; the info word of each P buffer says whether the page
         // opens a segment (accumulator overwritten) or that no page follows
         for (int64_t kk = 0;; ++kk) {
-          const int vs = static_cast<int>(kk % VST), ps = static_cast<int>(kk & 1);
-          if (!mbar_wait(&pfull[ps], (kk >> 1) & 1, abort_flag, p.dev_err)) break;
+          const int vs = static_cast<int>(kk % VST), ps = static_cast<int>(kk % NPB);
+          if (!mbar_wait(&pfull[ps], (kk / NPB) & 1, abort_flag, p.dev_err)) break;
           const int info = pinfo[ps];
           if (info < 0) break;
           if (!mbar_wait(F8 ? &vcvt[vs] : &vfull[vs], (kk / VST) & 1, abort_flag, p.dev_err)) break;
@@ -988,8 +999,67 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
         if (last) umma_commit(&qfree[qb]);
         return true;
       };
+      if constexpr (SKIP && TSC) {
+        // the scores of every page and the values of the kept pages, each issued as soon as
+        // it is ready (non-blocking probes): a page's scores never wait for an earlier
+        // page's decision, so the compute warps always find the next scores in flight
+        int64_t it_s = 0, kk = 0;   // pages scored, kept pages accumulated
+        uint64_t t_idle = 0;
+        while (true) {
+          bool progress = false;
+          if (g0 + it_s < g1) {
+            const int64_t g = g0 + it_s;
+            wsc.advance_to(g);
+            const bool first = (g == g0) || (g == wsc.bstart);
+            const int ks = static_cast<int>(it_s % KST), sb = static_cast<int>(it_s & 1);
+            const bool ready =
+                (!first || mbar_test_wait(&qfull[nseg & 1], (nseg >> 1) & 1)) &&
+                mbar_test_wait(&kfull[ks], (it_s / KST) & 1) &&
+                (it_s < 2 || mbar_test_wait(&sfree[sb], ((it_s >> 1) - 1) & 1));
+            if (ready) {
+              sphys[sb] = kphys[ks];
+              issue_scores(g, it_s);   // its waits are satisfied: they return at once
+              ++it_s;
+              progress = true;
+            }
+          }
+          const int ps = static_cast<int>(kk % NPB), vs = static_cast<int>(kk % VST);
+          if (mbar_test_wait(&pfull[ps], (kk / NPB) & 1)) {
+            const int info = pinfo[ps];
+            if (info < 0) break;   // every page is decided and every kept page accumulated
+            if (mbar_test_wait(&vcvt[vs], (kk / VST) & 1)) {
+              tc_fence_after();
+              const uint32_t vaddr = smem_u32(vst + vs * S::VSTAGE_BYTES);
+              const uint64_t bdesc =
+                  make_sdesc(smem_u32(pbuf + ps * L::P_BYTES), 128, 256, kSwizzleNone);
+#pragma unroll
+              for (int i = 0; i < S::NCHUNK; ++i) {
+                const uint64_t adesc = make_sdesc(vaddr + i * 4096, 2048, 1024, kSwizzle128B);
+                umma_f16(tmem_base + i * HP, adesc, bdesc, idesc, info ? 0u : 1u);
+              }
+              umma_commit(&vfree[vs]);
+              umma_commit(&pfree[ps]);
+              ++kk;
+              ++issued;
+              progress = true;
+            }
+          }
+          if (progress) {
+            t_idle = 0;
+            continue;
+          }
+          if (*abort_flag) break;
+          if (t_idle == 0) {
+            t_idle = globaltimer_ns();
+          } else if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(p.dev_err, RCP_DEVERR_TIMEOUT);
+            break;
+          }
+        }
+      }
       bool run = true;
-      if constexpr (TSC) run = g0 < g1 && issue_scores(g0, 0);
+      if constexpr (TSC && !SKIP) run = g0 < g1 && issue_scores(g0, 0);
       for (int64_t g = g0, it = 0; !SKIP && run && g < g1; ++g, ++it) {
         if constexpr (TSC)
           if (g + 1 < g1 && !issue_scores(g + 1, it + 1)) break;
@@ -1010,7 +1080,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
         umma_commit(&pfree[ps]);
         ++issued;
       }
-      if (issued > 0) mbar_wait_drain(&pfree[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
+      if (issued > 0) mbar_wait_drain(&pfree[(issued - 1) % NPB], ((issued - 1) / NPB) & 1);
     }
   } else if (SKIP && warp == 2 + NCW + NWW) {
     // ------------------------------------------ SKIP: value pages of the kept pages
@@ -1061,14 +1131,17 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
     int64_t nseg = 0;
     bool q_ready = false;
     // SKIP: the kept pages, in order, until a stage whose info word is -1
-    for (int64_t n = 0; SKIP; ++n) {
+    // (TSC: the query builders take no part; the other widening warps do the values)
+    const bool v_widener = !(TSC && SKIP) || !q_builder;
+    const int vw = (TSC && SKIP) ? vt - 64 : vt;   // 0 .. 32 NVW - 1 over the value wideners
+    for (int64_t n = 0; SKIP && v_widener; ++n) {
       const int vr = static_cast<int>(n % VRS), vs = static_cast<int>(n % VST);
       bool ok = mbar_wait(&vfull[vr], (n / VRS) & 1, abort_flag, p.dev_err);
       if (n >= VST) ok = mbar_wait(&vfree[vs], ((n / VST) - 1) & 1, abort_flag, p.dev_err) && ok;
       if (!__all_sync(0xffffffffu, ok)) break;
       const int nval = vinfo[vr];
       if (nval < 0) break;
-      widen_v_boxes<S, FMT, 32 * NWW>(vraw + vr * L::VPS, vst + vs * S::VSTAGE_BYTES, nval, 0, WB, vt);
+      widen_v_boxes<S, FMT, 32 * NVW>(vraw + vr * L::VPS, vst + vs * S::VSTAGE_BYTES, nval, 0, WB, vw);
       fence_proxy_async_smem();   // generic stores -> the MMA's async-proxy reads
       __syncwarp();
       if (lane == 0) {
@@ -1076,7 +1149,9 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
         mbar_arrive(&vcvt[vs]);     // its part of the fp16 stage is ready
       }
     }
-    for (int64_t g = g0, it = 0; !SKIP && g < g1; ++g, ++it) {
+    // every page in order: the query operands at segment starts (TSC), the 4-bit key codes
+    // (I4T) and, without skipping, the V pages
+    for (int64_t g = g0, it = 0; (!SKIP || (TSC && q_builder)) && g < g1; ++g, ++it) {
       if constexpr (TSC) {
         wq.advance_to(g);
         if (q_builder && (g == g0 || g == wq.bstart)) {
@@ -1099,6 +1174,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
           if (lane == 0) mbar_arrive(&qfull[qb]);
         }
       }
+      if constexpr (SKIP) continue;   // the values of kept pages are the other warps' part
       if constexpr (I4T) {
         // this page's key codes as the E4M3 scoring operand, once the raw page landed, the
         // operand stage's MMAs completed and the compute warps read the scales two pages ago
@@ -1202,6 +1278,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
         ok = mbar_wait(&sfull[sb], (it >> 1) & 1, abort_flag, p.dev_err);
         ok = __all_sync(0xffffffffu, ok);   // TMEM loads are warp-collective
         bi.nvalid = ok ? sinfo[sb] : 0;
+        if constexpr (SKIP) kph = sphys[sb];
         if (bi.seg_first) {
           ++nseg_c;
           const int qb = static_cast<int>((nseg_c - 1) & 1);
@@ -1429,12 +1506,12 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
 
       // P buffer / V stage order of this page among the accumulated ones
       const int64_t pi = SKIP ? kk : it;
-      const int ps = static_cast<int>(pi & 1);
+      const int ps = static_cast<int>(pi % NPB);
       if (kept) {
-      if (pi >= 2) ok = mbar_wait(&pfree[ps], ((pi >> 1) - 1) & 1, abort_flag, p.dev_err) && ok;
+      if (pi >= NPB) ok = mbar_wait(&pfree[ps], ((pi / NPB) - 1) & 1, abort_flag, p.dev_err) && ok;
       if (f & 1) {
         // rescale the accumulator columns after the previous block's MMAs have landed
-        ok = mbar_wait(&pfree[(pi - 1) & 1], ((pi - 1) >> 1) & 1, abort_flag, p.dev_err) && ok;
+        ok = mbar_wait(&pfree[(pi - 1) % NPB], ((pi - 1) / NPB) & 1, abort_flag, p.dev_err) && ok;
         ok = __all_sync(0xffffffffu, ok);   // TMEM loads / stores are warp-collective
         tc_fence_after();
         if (ok) {
@@ -1506,7 +1583,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
       if (bi.seg_last) {
         // the segment's last accumulated page (a segment's first page is always kept)
         const int64_t last = SKIP ? kk - 1 : it;
-        ok = mbar_wait(&pfree[last & 1], (last >> 1) & 1, abort_flag, p.dev_err) && ok;
+        ok = mbar_wait(&pfree[last % NPB], (last / NPB) & 1, abort_flag, p.dev_err) && ok;
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         if (ok) {
@@ -1547,7 +1624,7 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
         // no page follows: tell the MMA thread (the next P buffer's info word; its
         // previous use was read before the MMAs the last record waited for) and the
         // value-copy warp
-        const int ps = static_cast<int>(kk & 1);
+        const int ps = static_cast<int>(kk % NPB);
         if (ctid == 0) {
           pinfo[ps] = -1;
           const int ds = static_cast<int>(nd % L::DS);
