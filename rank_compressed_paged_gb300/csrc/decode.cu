@@ -285,18 +285,20 @@ struct DecodeSmem {
 // F8: eight compute warps (2-9; scoring E4M3 keys costs more per byte) and warps 10-11,
 // which widen the E4M3 V pages while the compute warps score.
 // SKIP: warp 0 copies keys only and the last warp copies the value pages the compute warps
-// keep.  fp16 pages: four compute warps (eight measured slower there: more registers
-// spilled and barrier traffic).  Quantized pages: the keys are scored on the CUDA cores by
-// eight compute warps (the tensor-core scoring issues a page's scores before it is known
-// which value pages are needed), and four widening warps widen every kept V page.
-// SKIP + F8: warps 2-9 compute, 10-13 widen, 14 copies the kept value pages.
+// keep.  fp16 pages: eight compute warps (warps 2-9; 10 copies the kept value pages): a
+// per-page clock trace showed the four of the dense kernel busy scoring about 3,200 cycles
+// of every skipped page while the keys were already resident, so the scoring, not the key
+// stream, set the pace (eight: 415 against 443 us at batch 64 x 8192, peaked).  E4M3 pages:
+// the tensor-core scoring, with two of the six widening warps building the query operands
+// and four widening the kept pages' values.  4-bit pages: the keys are scored on the CUDA
+// cores by eight compute warps, and four widening warps widen every kept V page.
 // TSC: four compute warps (one per TMEM lane quarter: scores, softmax, weights) and six
 // warps that widen the V pages (and build the query operands), so that the widening's
 // conversions overlap the softmax's shuffle latencies instead of following them.
 template <class S, int FMT, bool SKIP = false>
 constexpr int decode_compute_warps() {
   return decode_tensor_scores<S, FMT, SKIP>() ? 4
-                                              : (FMT != RCP_PAGES_FP16 && S::H % 8 == 0) ? 8 : 4;
+                                              : ((FMT != RCP_PAGES_FP16 || SKIP) && S::H % 8 == 0) ? 8 : 4;
 }
 template <class S, int FMT, bool SKIP = false>
 constexpr int decode_widen_warps() {
