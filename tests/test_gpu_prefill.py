@@ -90,3 +90,29 @@ def test_prefill_rejects_decreasing_chunk_offsets(variant):
     torch.cuda.synchronize()
     assert cache.read_device_error() & _lib.RCP_DEVERR_BAD_LEN
     assert torch.isnan(out).all()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prefill_rejects_bad_block_ids_on_device(variant):
+    """A prior page of request 1 names a block past the pool: the device error word gets
+    the bad-block bit, and request 0 (which reads none of request 1's pages) still matches
+    the oracle.  (The reconstructing variant copies such a page from row -16, all out of
+    bounds, so every stage still completes on its fixed byte count.)"""
+    import torch
+    from rank_compressed_paged_gb300 import _lib
+    inp = wl.make_prefill_inputs(MAIN, [300, 200], [64, 40], seed=47)
+    c = inp.cache
+    cache = make_cache(inp.shape, inp.U_k, inp.W_v, c.k_pages, c.v_pages)
+    cache.append_kv(t(inp.k), t(inp.v), t(inp.slot_mapping))
+    table = c.block_table.copy()
+    table[1, 2] = c.k_pages.shape[0] + 7              # out of range physical id
+    out = cache.prefill_attn(t(inp.q), t(inp.cu_chunk_lens), t(table), t(inp.seq_lens_after),
+                             variant=variant)
+    torch.cuda.synchronize()
+    assert cache.read_device_error() & _lib.RCP_DEVERR_BAD_BLOCK
+    kp, vp = orc.append_kv(c.k_pages, c.v_pages, inp.U_k, inp.W_v, inp.k, inp.v,
+                           inp.slot_mapping, 16)
+    n0 = int(inp.cu_chunk_lens[1])
+    ref0 = orc.prefill_attn(inp.q[:n0], inp.cu_chunk_lens[:2], kp, vp, inp.U_k, inp.W_v,
+                            c.block_table[:1], inp.seq_lens_after[:1], 16)
+    assert_close(out.cpu().numpy()[:n0], ref0, what=f"unaffected request ({variant})")
