@@ -103,8 +103,8 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank, int T) {
     constexpr int NKG = (NP + KS - 1) / KS;
     constexpr int KBV = S::H * S::D / 64;
     constexpr int KBK = S::D / 64;
-    // the append's clusters come first (value jobs, then key jobs, per token tile), then
-    // the decode query jobs (head pairs, per query tile)
+    // the append's clusters come first (the value jobs of every token tile, then their key
+    // jobs), then the decode query jobs (head pairs, per query tile)
     const int app_clusters = (T + NT - 1) / NT * (NM + NKG);
     if (cluster >= app_clusters) {
       const int qc = cluster - app_clusters;
@@ -119,8 +119,12 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank, int T) {
       j.reduce = false;
       return j;
     }
-    const int tile = cluster / (NM + NKG);
-    const int sub = cluster % (NM + NKG);
+    // value jobs of every token tile first (K = H d: the long ones, so they all start in
+    // the first wave), then the key jobs
+    const int ntile = (T + NT - 1) / NT;
+    const bool value_job = cluster < ntile * NM;
+    const int tile = value_job ? cluster / NM : (cluster - ntile * NM) / NKG;
+    const int sub = value_job ? cluster % NM : NM + (cluster - ntile * NM) % NKG;
     j.n0 = tile * NT;
     if (sub < NM) {
       j.kind = 0;
