@@ -35,8 +35,7 @@ struct rcp_cache {
   CUtensorMap tmap_v;       // V pages as [num_blocks*16][R], 64 x 16 boxes (decode A operand)
   CUtensorMap tmap_wv_k;    // W_v as [R][H*d], 64 x 128 boxes (append: K-major A)
   CUtensorMap tmap_wv_mn;   // W_v as [R][H*d], 64 x 64 boxes (up-projection: MN-major A)
-  CUtensorMap tmap_uk;      // U_k as [H*r_k][d], 64 x 128 boxes (query projection: A)
-  CUtensorMap tmap_uk64;    // U_k as [H*r_k][d], 64 x 64 boxes (append key pairs: A)
+  CUtensorMap tmap_uk64;    // U_k as [H*r_k][d], 64 x 64 boxes (key and query pairs: A)
   CUtensorMap tmap_kp;      // K pages as [num_blocks*H*16][r_k], 64 x 16 boxes (prefill B)
   CUtensorMap tmap_kpage;   // the same rows, 64 x 256 boxes (decode: half a page per box;
                             // E4M3 pages: bytes, 64-byte swizzle)
@@ -161,9 +160,6 @@ rcp_status ensure_device(rcp_cache* c) {
                  static_cast<uint64_t>(g.rank_v) * 2, 64, 16) ||
       !encode_2d(&c->tmap_wv_k, c->W_v, hd, g.rank_v, hd * 2, 64, 128) ||
       !encode_2d(&c->tmap_wv_mn, c->W_v, hd, g.rank_v, hd * 2, 64, 64) ||
-      !encode_2d(&c->tmap_uk, c->U_k, g.head_dim,
-                 static_cast<uint64_t>(g.num_heads) * g.rank_k, static_cast<uint64_t>(g.head_dim) * 2,
-                 64, 128) ||
       !encode_2d(&c->tmap_uk64, c->U_k, g.head_dim,
                  static_cast<uint64_t>(g.num_heads) * g.rank_k, static_cast<uint64_t>(g.head_dim) * 2,
                  64, 64) ||
@@ -419,7 +415,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
     if (c->shape == kShapeMain) {
       e = rcp::launch_plan<ShapeMain>(p, s, pdl);
       if (e == cudaSuccess)
-        e = rcp::launch_qproj_gemm<ShapeMain>(c->tmap_uk, q_map, p.qhi, p.qlo, nq, p.qscale,
+        e = rcp::launch_qproj_gemm<ShapeMain>(c->tmap_uk64, q_map, p.qhi, p.qlo, nq, p.qscale,
                                               c->dev_err, s, pdl);
       // profiling events bracket the attention proper: reconstruction + prefill kernel
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
@@ -434,7 +430,7 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
     } else {
       e = rcp::launch_plan<ShapeTiny>(p, s, pdl);
       if (e == cudaSuccess)
-        e = rcp::launch_qproj_gemm<ShapeTiny>(c->tmap_uk, q_map, p.qhi, p.qlo, nq, p.qscale,
+        e = rcp::launch_qproj_gemm<ShapeTiny>(c->tmap_uk64, q_map, p.qhi, p.qlo, nq, p.qscale,
                                               c->dev_err, s, pdl);
       // profiling events bracket the attention proper: reconstruction + prefill kernel
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);

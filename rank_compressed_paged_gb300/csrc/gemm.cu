@@ -145,14 +145,15 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank, int T) {
       j.reduce = false;
     }
   } else if constexpr (MODE == kModeQproj) {
-    const int h = blockIdx.x % S::H;
+    // two heads h, h+1 at once, block-diagonal over K = 2d as the append's key jobs
+    const int pr = blockIdx.x % (S::H / 2);
     j.kind = 3;
-    j.m0 = h;
-    j.n0 = (blockIdx.x / S::H) * NT;
+    j.m0 = 2 * pr;
+    j.n0 = (blockIdx.x / (S::H / 2)) * NT;
     j.kb0 = 0;
-    j.kb1 = S::D / 64;
-    j.a_x = 0; j.a_y = h * S::RK; j.a_step_x = 64; j.a_step_y = 0;
-    j.b_x = h * S::D; j.b_y = j.n0; j.b_step_x = 64;
+    j.kb1 = 2 * (S::D / 64);
+    j.a_x = 0; j.a_y = j.m0 * S::RK; j.a_step_x = 64; j.a_step_y = 0;
+    j.b_x = j.m0 * S::D; j.b_y = j.n0; j.b_step_x = 64;
     j.reduce = false;
   }
   return j;
@@ -263,9 +264,12 @@ __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j
     return;
   }
   if (j.kind == 3) {
-    if (n >= p.nq || row >= 64) return;
-    const size_t at = (static_cast<size_t>(n) * S::H + j.m0) * 64 + row;
-    float q = row < S::RK ? v * p.qscale : 0.f;   // rows past r_k belong to the next head
+    // rows 0..63 are head m0's ranks, rows 64..127 head m0 + 1's; rows past r_k hold the
+    // next heads' products and are written as the zero padding up to 64
+    const int hh = row >> 6, rr = row & 63;
+    if (n >= p.nq) return;
+    const size_t at = (static_cast<size_t>(n) * S::H + j.m0 + hh) * 64 + rr;
+    float q = rr < S::RK ? v * p.qscale : 0.f;
     const __half hi = __float2half_rn(q);
     static_cast<__half*>(p.qhi)[at] = hi;
     static_cast<__half*>(p.qlo)[at] = __float2half_rn(q - __half2float(hi));
@@ -342,7 +346,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nkb = j.kind >= 0 ? j.kb1 - j.kb0 : 0;
   auto load_a = [&](int kb, int s) {
     uint8_t* st = sm + s * L::STAGE;
-    if (MODE == kModeAppend && (j.kind == 1 || j.kind == 4)) {
+    if ((MODE == kModeAppend && (j.kind == 1 || j.kind == 4)) || MODE == kModeQproj) {
       // block-diagonal pair: k-blocks [0, d/64) meet head m0's rows (top), the rest head
       // m0 + 1's (bottom); the other half is a box past the last row of U_k (zeros)
       constexpr int KBK = S::D / 64, OOB = S::H * S::RK;
@@ -642,12 +646,12 @@ cudaError_t launch_qproj_gemm(const CUtensorMap& u_k, const CUtensorMap& q_rows,
   p.dev_err = dev_err;
   if (nq <= 256) {
     const int tiles = (nq + 63) / 64;
-    return launch_cluster(gemm_kernel<S, kModeQproj, 64, 1, 2>, tiles * S::H, 1,
+    return launch_cluster(gemm_kernel<S, kModeQproj, 64, 1, 2>, tiles * (S::H / 2), 1,
                           GemmSmem<64, 1, 1, 2>::ALLOC, stream, pdl, u_k, u_k, q_rows, q_rows,
                           q_rows, p);
   }
   const int tiles = (nq + 255) / 256;
-  return launch_cluster(gemm_kernel<S, kModeQproj, 256, 1, 2>, tiles * S::H, 1,
+  return launch_cluster(gemm_kernel<S, kModeQproj, 256, 1, 2>, tiles * (S::H / 2), 1,
                         GemmSmem<256, 1, 1, 2>::ALLOC, stream, pdl, u_k, u_k, q_rows, q_rows,
                         q_rows, p);
 }
