@@ -132,7 +132,9 @@ __global__ void __launch_bounds__(kCombThreads)
   {
     const int64_t T = p.cum[p.nq];
     const int64_t cn0 = p.cum[n0];
-    const int G = static_cast<int>(T < p.parts ? T : p.parts);   // partitions with blocks
+    // partitions with blocks (the split-K kernel's rule)
+    const int64_t Gm = (T + decode_min_pages<S>(p.nq) - 1) / decode_min_pages<S>(p.nq);
+    const int G = static_cast<int>(Gm < p.parts ? Gm : p.parts);
     // the partition whose range [c*T/G, (c+1)*T/G) holds block g
     auto part_of = [&](int64_t g) { return static_cast<int>(((g + 1) * G + T - 1) / T - 1); };
     // record ids of request n are n + first .. n + last partition it touched; over the

@@ -733,8 +733,11 @@ __global__ void __launch_bounds__(decode_threads<S, FMT, SKIP>(), 1)
   int64_t T = 0;
 #pragma unroll
   for (int i = 0; i < NWARP; ++i) T += red[i];
-  // never more partitions than blocks, so every partition's range is non-empty
-  const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
+  // never more partitions than blocks, so every partition's range is non-empty, and at
+  // least decode_min_pages(nq) blocks per partition, so that small batches do not spread
+  // over more partitions than pays for their split-K records (128 KiB each)
+  const int64_t Gm = (T + decode_min_pages<S>(p.nq) - 1) / decode_min_pages<S>(p.nq);
+  const int G = static_cast<int>(Gm < gridDim.x ? Gm : gridDim.x);
   const bool active = cta < G;   // uniform over the CTA
   const int64_t g0 = active ? static_cast<int64_t>(cta) * T / G : 0;
   const int64_t g1 = active ? static_cast<int64_t>(cta + 1) * T / G : 0;

@@ -10,6 +10,16 @@ constexpr int kBlockSize = 16;   // tokens per page
 constexpr int kMaxParts = 152;   // decode work partitions (CTAs) at most: one per SM of a
                                  // GB300; bounds the records the combine stages per tile
 
+// Fewest blocks a decode work partition takes for a batch of nq requests (the split-K kernel
+// and the merge derive the partition count from it alike).  With large pages (96 KiB of
+// coefficients at (32, 128, 64, 1024)) a partition's 128 KiB split-K record must pay for
+// itself: measured at batch 1 x 8192 tokens 45.2 / 43.8 / 48.0 us per step for 1 / 4 / 8
+// blocks, at 16 x 1024 58.7 / 58.7 / 55.0 us.  Small pages spread over every partition.
+template <class S>
+__host__ __device__ constexpr int decode_min_pages(int nq) {
+  return S::R >= 512 ? (nq >= 8 ? 8 : 4) : 1;
+}
+
 constexpr int pow2_at_least(int x, int lo) {
   int p = lo;
   while (p < x) p *= 2;
