@@ -158,18 +158,46 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tmem = *tmem_slot;
   if constexpr (NQ > 1) cluster_sync_all();   // peers are running before any remote store
 
-  if (warp == 0 || warp == 6) {
-    // -------------------------------------------------------------------- copies
+  if (warp == 0) {
+    // ------------------------------------------------------------------ key copies
+    // The whole warp: lane jb < 8 resolves page jb of each tile one tile ahead and issues
+    // that page's copy (the eight small copies of a tile set the kernel's pace when one
+    // thread issues them in turn); lane 0 waits for the stage and arms its byte count.
+    constexpr int BPT = KT / kBlockSize;                  // pages per key tile
     if (lane == 0) {
-      const bool keys = warp == 0;
-      if (keys) {
-        prefetch_tmap(&kp_map);
-        mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
-        tma_load_2d(sm, &qhi_map, h * 64, row0, q_full);
-        tma_load_2d(sm + L::Q_BYTES, &qlo_map, h * 64, row0, q_full);
-      } else {
-        prefetch_tmap(&vp_map);
+      prefetch_tmap(&kp_map);
+      mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
+      tma_load_2d(sm, &qhi_map, h * 64, row0, q_full);
+      tma_load_2d(sm + L::Q_BYTES, &qlo_map, h * 64, row0, q_full);
+    }
+    const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+    int32_t nxt = (lane < BPT && lane < nblk) ? table[lane] : -1;
+    for (int j = 0; j < nkt; ++j) {
+      const int s = j % NS;
+      const bool mine = lane < BPT && j * BPT + lane < nblk;
+      int32_t phys = mine ? nxt : -1;
+      if (mine && (phys < 0 || phys >= p.num_blocks)) {
+        atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
+        phys = -1;
       }
+      const int nb = (j + 1) * BPT + lane;                 // the next tile's page, in flight
+      nxt = (lane < BPT && nb < nblk) ? table[nb] : -1;
+      const int nload = __popc(__ballot_sync(0xffffffffu, phys >= 0));
+      bool ok = true;
+      if (lane == 0) {
+        ok = j < NS || mbar_wait(&k_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err);
+        if (ok) mbar_arrive_expect_tx(&k_full[s], nload * 2048);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;   // the byte count is armed first
+      if (phys >= 0)
+        tma_load_2d(sm + L::ST_OFF + s * L::STAGE + lane * 2048, &kp_map, 0,
+                    (phys * H + h) * kBlockSize, &k_full[s]);
+    }
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- value copies
+    if (lane == 0) {
+      constexpr bool keys = false;
+      prefetch_tmap(&vp_map);
       const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
       constexpr int BPT = KT / kBlockSize;                // pages per key tile
       // block ids of the next tile are fetched one tile ahead, off the critical path
@@ -198,14 +226,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         uint8_t* kst = sm + L::ST_OFF + s * L::STAGE;
         uint8_t* vst = kst + L::K_BYTES;
-        if (keys) {
-          if (j >= NS && !mbar_wait(&k_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err)) break;
-          mbar_arrive_expect_tx(&k_full[s], nload * 2048);
-#pragma unroll 1
-          for (int jb = 0; jb < BPT; ++jb)
-            if (phys[jb] >= 0)
-              tma_load_2d(kst + jb * 2048, &kp_map, 0, (phys[jb] * H + h) * kBlockSize, &k_full[s]);
-        } else if constexpr (RECON) {
+        if constexpr (RECON) {
           // V^ rows of the request are contiguous: one 64-column box of 128 keys per group
           if (j >= NS && !mbar_wait(&v_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err)) break;
           mbar_arrive_expect_tx(&v_full[s], NG * KT * 128);
