@@ -195,39 +195,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   } else if (warp == 6) {
     // ---------------------------------------------------------------- value copies
-    if (lane == 0) {
-      constexpr bool keys = false;
-      prefetch_tmap(&vp_map);
-      const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-      constexpr int BPT = KT / kBlockSize;                // pages per key tile
-      // block ids of the next tile are fetched one tile ahead, off the critical path
-      int32_t nxt[BPT];
-#pragma unroll
-      for (int jb = 0; jb < BPT; ++jb) nxt[jb] = jb < nblk ? table[jb] : -1;
-      for (int j = 0; j < nkt; ++j) {
-        const int s = j % NS;
-        int32_t phys[BPT];
-        int nload = 0;
-#pragma unroll
-        for (int jb = 0; jb < BPT; ++jb) {
-          const int blk = j * BPT + jb;
-          int32_t id = nxt[jb];
-          if (blk < nblk && (id < 0 || id >= p.num_blocks)) {
-            if (keys) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
-            id = -1;
-          }
-          phys[jb] = blk < nblk ? id : -1;
-          nload += phys[jb] >= 0;
-        }
-#pragma unroll
-        for (int jb = 0; jb < BPT; ++jb) {
-          const int blk = (j + 1) * BPT + jb;
-          nxt[jb] = blk < nblk ? table[blk] : -1;
-        }
-        uint8_t* kst = sm + L::ST_OFF + s * L::STAGE;
-        uint8_t* vst = kst + L::K_BYTES;
-        if constexpr (RECON) {
-          // V^ rows of the request are contiguous: one 64-column box of 128 keys per group
+    if constexpr (RECON) {
+      // V^ rows of the request are contiguous: one 64-column box of 128 keys per group
+      if (lane == 0) {
+        prefetch_tmap(&vp_map);
+        for (int j = 0; j < nkt; ++j) {
+          const int s = j % NS;
+          uint8_t* vst = sm + L::ST_OFF + s * L::STAGE + L::K_BYTES;
           if (j >= NS && !mbar_wait(&v_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err)) break;
           mbar_arrive_expect_tx(&v_full[s], NG * KT * 128);
           const int64_t vrow = p.vcum[b] * kBlockSize + static_cast<int64_t>(j) * KT;
@@ -235,21 +209,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int g = 0; g < NG; ++g)
             tma_load_2d(vst + g * KT * 128, &vp_map, h * D + g * 64, static_cast<int32_t>(vrow),
                         &v_full[s]);
-        } else {
-          if (j >= NS && !mbar_wait(&v_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err)) break;
-          mbar_arrive_expect_tx(&v_full[s], nload * NG * 2048);
-#pragma unroll 1
-          for (int jb = 0; jb < BPT; ++jb) {
-            if (phys[jb] < 0) continue;
+        }
+      }
+    } else {
+      // the value rank slice of each page: lane jb < 8 resolves page jb of each tile one
+      // tile ahead and issues its NG boxes, as the key copies
+      constexpr int BPT = KT / kBlockSize;
+      if (lane == 0) prefetch_tmap(&vp_map);
+      const int32_t* table = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+      int32_t nxt = (lane < BPT && lane < nblk) ? table[lane] : -1;
+      for (int j = 0; j < nkt; ++j) {
+        const int s = j % NS;
+        const bool mine = lane < BPT && j * BPT + lane < nblk;
+        const int32_t id = mine ? nxt : -1;
+        const int32_t phys = (id >= 0 && id < p.num_blocks) ? id : -1;   // keys report bad ids
+        const int nb = (j + 1) * BPT + lane;
+        nxt = (lane < BPT && nb < nblk) ? table[nb] : -1;
+        const int nload = __popc(__ballot_sync(0xffffffffu, phys >= 0));
+        bool go = true;
+        if (lane == 0) {
+          go = j < NS || mbar_wait(&v_empty[s], ((j / NS) - 1) & 1, abort_flag, p.dev_err);
+          if (go) mbar_arrive_expect_tx(&v_full[s], nload * NG * 2048);
+        }
+        if (!__shfl_sync(0xffffffffu, go, 0)) break;
+        uint8_t* vst = sm + L::ST_OFF + s * L::STAGE + L::K_BYTES;
+        if (phys >= 0) {
 #pragma unroll
-            for (int g = 0; g < NG; ++g)
-              tma_load_2d(vst + (g * BPT + jb) * 2048, &vp_map, slice * RQ + g * 64,
-                          phys[jb] * kBlockSize, &v_full[s]);
-          }
+          for (int g = 0; g < NG; ++g)
+            tma_load_2d(vst + (g * BPT + lane) * 2048, &vp_map, slice * RQ + g * 64,
+                        phys * kBlockSize, &v_full[s]);
         }
       }
       // the W_v rows of this slice, into stage memory once every value MMA is done
-      if (!RECON && !keys && mbar_wait(acc_done, 0, abort_flag, p.dev_err)) {
+      if (lane == 0 && mbar_wait(acc_done, 0, abort_flag, p.dev_err)) {
         mbar_arrive_expect_tx(w_full, L::W_BYTES);
         uint8_t* wst = sm + L::W_OFF;
         for (int g = 0; g < D / 64; ++g)
