@@ -297,6 +297,87 @@ __device__ __forceinline__ void gemm_store(const GemmParams& p, const GemmJob& j
     static_cast<__half*>(pages)[at] = __float2half_rn(v);
 }
 
+// One warp's epilogue staging area: 16 columns x 32 rows of at most 4 bytes (fp32 decode
+// queries; the prefill queries' fp16 hi and lo parts take two 1 KB planes).
+constexpr int kEpiWarpBytes = 16 * 32 * 4;
+
+// Write columns c0 .. c0+15 of a job's tile for rows 32 warp .. 32 warp + 31 (v[] holds this
+// lane's row).  In every destination a column's rows are contiguous (a page row's value
+// coefficients, a head's ranks), so the warp transposes the block through its staging area
+// and writes each column's run of rows as 16-byte pieces rather than an element per lane.
+// ES: bytes per element (4 decode queries, 2 fp16 pages and prefill queries, 1 E4M3 pages);
+// PL: planes (2 for the prefill queries' hi and lo parts).  Both fixed at compile time, so
+// that the piece loop unrolls with shifts and masks for its indexes.
+template <class S, int ES, int PL>
+__device__ __forceinline__ void gemm_store_block(const GemmParams& p, const GemmJob& j,
+                                                 const int64_t* dst, uint8_t* stage, int warp,
+                                                 int lane, int c0, const float (&v)[16]) {
+  static_assert(S::R % 32 == 0 && S::RK % 16 == 0, "runs of whole 16-byte pieces");
+  constexpr int NCH = 32 * ES / 16;    // 16-byte pieces of a column's 32 rows, per plane
+  constexpr int PER = 16 * NCH;        // pieces of the block, per plane
+  static_assert((PL * PER) % 32 == 0 && PL * 16 * 32 * ES <= kEpiWarpBytes, "staging");
+  const int hh = warp >> 1;            // key / query jobs: head m0 + hh
+  const int rr0 = (warp & 1) * 32;     // ... ranks rr0 .. rr0 + 31
+  int nvalid;
+  if constexpr (ES == 4) {             // decode queries, fp32
+    nvalid = min(32, max(0, S::RK - rr0));
+    float* s = reinterpret_cast<float*>(stage);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) s[e * 32 + lane] = v[e] * p.qscale;
+  } else if constexpr (PL == 2) {      // prefill queries, fp16 hi and lo
+    // ranks past r_k hold the next heads' products and are written as zero padding
+    nvalid = 32;
+    __half* s = reinterpret_cast<__half*>(stage);
+    const bool rank = rr0 + lane < S::RK;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float q = rank ? v[e] * p.qscale : 0.f;
+      const __half hi = __float2half_rn(q);
+      s[e * 32 + lane] = hi;
+      s[512 + e * 32 + lane] = __float2half_rn(q - __half2float(hi));
+    }
+  } else {                             // append: value or key page coefficients
+    nvalid = j.kind == 0 ? min(32, max(0, S::R - (j.m0 + warp * 32)))
+                         : min(32, max(0, S::RK - rr0));
+    if constexpr (ES == 1) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        stage[e * 32 + lane] = __nv_cvt_float_to_fp8(v[e], __NV_SATFINITE, __NV_E4M3);
+    } else {
+      __half* s = reinterpret_cast<__half*>(stage);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s[e * 32 + lane] = __float2half_rn(v[e]);
+    }
+  }
+  __syncwarp();
+  const int nvc = nvalid * ES / 16;    // pieces of a column that hold valid rows
+#pragma unroll
+  for (int it = 0; it < PL * PER / 32; ++it) {
+    const int i = lane + 32 * it;
+    const int plane = i / PER, c = (i % PER) / NCH, k = i % NCH;
+    if (k >= nvc) continue;
+    uint8_t* out;
+    if constexpr (ES == 4 || PL == 2) {
+      const int n = j.n0 + c0 + c;
+      if (n >= p.nq) continue;
+      const size_t hrow = static_cast<size_t>(n) * S::H + j.m0 + hh;
+      if constexpr (ES == 4)
+        out = reinterpret_cast<uint8_t*>(p.qt) + (hrow * S::RK + rr0) * 4;
+      else
+        out = static_cast<uint8_t*>(plane ? p.qlo : p.qhi) + (hrow * 64 + rr0) * 2;
+    } else {
+      const int64_t d = dst[c0 + c];
+      if (d < 0) continue;
+      out = j.kind == 0
+                ? static_cast<uint8_t*>(p.v_pages) + (d + j.m0 + warp * 32) * ES
+                : static_cast<uint8_t*>(p.k_pages) + (d + hh * kBlockSize * S::RK + rr0) * ES;
+    }
+    *reinterpret_cast<uint4*>(out + k * 16) =
+        *reinterpret_cast<const uint4*>(stage + plane * 1024 + c * 32 * ES + k * 16);
+  }
+  __syncwarp();   // the staging area is rewritten by the next block
+}
+
 template <class S, int MODE, int NT, int KS, int STG>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a2,
@@ -482,14 +563,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (!j.reduce) {
     if (have_acc) {
+      // the pipeline stages are idle once the accumulator is complete: each warp stages its
+      // blocks in the first stage
+      static_assert(4 * kEpiWarpBytes <= L::STAGE, "epilogue staging fits in one stage");
+      uint8_t* stage = sm + warp * kEpiWarpBytes;
+      auto blocks = [&](auto store) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < NT; c0 += 16) {
-        float v[16];
-        tmem_ld16(trow + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) gemm_store<S>(p, j, dst_s, row, c0 + e, v[e]);
-      }
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+          float v[16];
+          tmem_ld16(trow + c0, v);
+          tmem_wait_ld();
+          store(c0, v);
+        }
+      };
+      if (j.kind == 4)
+        blocks([&](int c0, const float(&v)[16]) { gemm_store_block<S, 4, 1>(p, j, dst_s, stage, warp, lane, c0, v); });
+      else if (j.kind == 3)
+        blocks([&](int c0, const float(&v)[16]) { gemm_store_block<S, 2, 2>(p, j, dst_s, stage, warp, lane, c0, v); });
+      else if (p.fmt == RCP_PAGES_FP8_E4M3)
+        blocks([&](int c0, const float(&v)[16]) { gemm_store_block<S, 1, 1>(p, j, dst_s, stage, warp, lane, c0, v); });
+      else
+        blocks([&](int c0, const float(&v)[16]) { gemm_store_block<S, 2, 1>(p, j, dst_s, stage, warp, lane, c0, v); });
     }
   } else {
     // split-K: row r belongs to peer r / RPC; send it to slot [my rank] of that peer
