@@ -48,6 +48,7 @@ namespace rcp {
 
 // ----------------------------------------------------------------------------- prefill plan
 constexpr int kPlanThreads = 256;
+constexpr int kPlanRegRows = 16;
 
 // One CTA: keys attended (qlen) and block-table row (qrow) of every chunk row, the prefix
 // sums of their blocks, the list of 128-row query tiles and (reconstructing variant) the
@@ -77,32 +78,42 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const AttnParams p) 
     __syncthreads();
     const bool cu_ok = cu_bad == 0;
     if (!cu_ok && tid == 0) atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
-    for (int b = tid; b < p.batch; b += kPlanThreads) {
-      const int32_t L = p.seq_lens[b];
-      const bool len_ok = L >= 0 && L <= max_len;
-      if (p.cu_chunk == nullptr) {
+    if (p.cu_chunk == nullptr) {
+      for (int b = tid; b < p.batch; b += kPlanThreads) {
+        const int32_t L = p.seq_lens[b];
+        const bool len_ok = L >= 0 && L <= max_len;
         if (!len_ok) atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
         p.qlen[b] = len_ok ? L : 0;
         p.qrow[b] = b;
-      } else {
-        const int32_t c0 = p.cu_chunk[b], c1 = p.cu_chunk[b + 1];
+      }
+    } else {
+      // a warp per request; its lanes write the request's rows
+      for (int b = tid >> 5; b < p.batch; b += kPlanThreads / 32) {
+        const int32_t L = p.seq_lens[b], c0 = p.cu_chunk[b], c1 = p.cu_chunk[b + 1];
         const int32_t n = c1 - c0;
-        if (!cu_ok || !len_ok || c0 < 0 || n < 0 || c1 > p.nq || n > L) {
-          atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
+        if (!cu_ok || L < 0 || L > max_len || c0 < 0 || n < 0 || c1 > p.nq || n > L) {
+          if ((tid & 31) == 0) atomicOr(p.dev_err, RCP_DEVERR_BAD_LEN);
           continue;
         }
-        for (int32_t i = 0; i < n; ++i) {
+        for (int32_t i = tid & 31; i < n; i += 32) {
           p.qlen[c0 + i] = L - n + i + 1;   // causal: row i sees keys 0 .. P + i
           p.qrow[c0 + i] = b;
         }
       }
     }
     __syncthreads();
-    // block-wide exclusive scan of per-thread sums (contiguous row ranges per thread)
+    // block-wide exclusive scan of per-thread sums (contiguous row ranges per thread); a
+    // thread's lengths are loaded kPlanRegRows at a time, all loads in flight together
     const int per = (p.nq + kPlanThreads - 1) / kPlanThreads;
     const int r0 = min(p.nq, tid * per), r1 = min(p.nq, r0 + per);
     int64_t s = 0;
-    for (int r = r0; r < r1; ++r) s += (p.qlen[r] + kBlockSize - 1) / kBlockSize;
+    for (int rb = r0; rb < r1; rb += kPlanRegRows) {
+      int32_t q[kPlanRegRows];
+#pragma unroll
+      for (int k = 0; k < kPlanRegRows; ++k) q[k] = rb + k < r1 ? p.qlen[rb + k] : 0;
+#pragma unroll
+      for (int k = 0; k < kPlanRegRows; ++k) s += (q[k] + kBlockSize - 1) / kBlockSize;
+    }
     const int lane = tid & 31, w = tid >> 5;
     int64_t incl = s;
 #pragma unroll
@@ -115,9 +126,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const AttnParams p) 
     int64_t acc = incl - s;
     for (int i = 0; i < w; ++i) acc += warp_sum[i];
     if (tid == 0) p.cum[0] = 0;
-    for (int r = r0; r < r1; ++r) {
-      acc += (p.qlen[r] + kBlockSize - 1) / kBlockSize;
-      p.cum[r + 1] = acc;
+    for (int rb = r0; rb < r1; rb += kPlanRegRows) {
+      int32_t q[kPlanRegRows];
+#pragma unroll
+      for (int k = 0; k < kPlanRegRows; ++k) q[k] = rb + k < r1 ? p.qlen[rb + k] : 0;
+#pragma unroll
+      for (int k = 0; k < kPlanRegRows; ++k) {
+        acc += (q[k] + kBlockSize - 1) / kBlockSize;
+        if (rb + k < r1) p.cum[rb + k + 1] = acc;
+      }
     }
     if (p.tile_b != nullptr) {
       // prefill: list the 128-row query tiles of every valid request, in request order
