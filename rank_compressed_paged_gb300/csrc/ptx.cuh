@@ -127,6 +127,18 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Pair copy multicast: the same box into every CTA of cta_mask (same shared-memory offset
+// in each); the bytes landing in a CTA are reported to the mbarrier at bar's offset in the
+// even CTA of that CTA's pair (bar_cluster: the issuing pair's even-CTA barrier).
+__device__ __forceinline__ void tma_load_2d_mc_pair(void* smem_dst, const CUtensorMap* map,
+                                                    int32_t x, int32_t y, uint32_t bar_cluster,
+                                                    uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask)
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -11,15 +11,22 @@
 // The keys of all such requests, page after page in request order (prefix sums in
 // vcum), are the rows of one GEMM D[keys x H*d] = C_v[keys x R] * W_v[R x H*d], cut into
 // tiles of 256 keys (16 pages) x 256 columns:
-//   * persistent CTA pairs (2-CTA clusters, one CTA per SM) take the tiles in turn; each
-//     CTA stages its 128 keys' C_v rows (A: one 16 x 64 tensor-map box per page per 64-wide
-//     k-block, K-major, 128-byte swizzle) and half of the W_v tile (B: 128 columns, two
-//     64 x 64 boxes, MN-major), so a k-block costs each SM 32 KB of operands instead of
-//     the 48 KB of a one-CTA 128 x 256 tile;
-//   * the even CTA issues tcgen05.mma.cta_group::2, M=256, N=256, K=16 steps; both CTAs'
-//     copies complete on the even CTA's stage barrier and each commit frees the stage in
-//     both CTAs; a CTA's tensor memory holds two 256-column accumulators of its 128 rows,
-//     so the epilogue of one tile overlaps the MMAs of the next;
+//   * persistent CTA pairs (one CTA per SM) take the tiles in turn; each CTA stages its 128
+//     keys' C_v rows (A: one 16 x 64 tensor-map box per page per 64-wide k-block, K-major,
+//     128-byte swizzle) and half of the W_v tile (B: 128 columns, two 64 x 64 boxes,
+//     MN-major), so a k-block costs each SM 32 KB of operands instead of the 48 KB of a
+//     one-CTA 128 x 256 tile;
+//   * a page holds only 16 keys, and the copy engine's cost per box set the kernel's pace
+//     with eight C_v boxes per CTA per k-block; so (when the columns split into an even
+//     number of tiles) two pairs form a 4-CTA cluster on one row of keys and adjacent
+//     column tiles, and each CTA copies half of its eight C_v boxes, multicast to itself
+//     and to the CTA holding the same keys in the other pair: six boxes per k-block;
+//   * both CTAs' copies of a pair (multicast ones included) complete on the pair's even-CTA
+//     stage barrier; the even CTA issues tcgen05.mma.cta_group::2, M=256, N=256, K=16
+//     steps; each commit frees the stage in every CTA of the cluster (a stage is refilled
+//     only when both pairs have read it); a CTA's tensor memory holds two 256-column
+//     accumulators of its 128 rows, so the epilogue of one tile overlaps the MMAs of the
+//     next;
 //   * four epilogue warps write V^ rows as fp16, zero for the slots of a page past the end
 //     of its sequence (so that the attention can never meet 0 * NaN there).
 #include <cuda.h>
@@ -66,6 +73,12 @@ struct ReconSmem {
   static_assert(2 * ALLOC > 228 * 1024 && ALLOC <= 227 * 1024, "one CTA per SM");
 };
 
+// CTA pairs per cluster: two when the column tiles pair up, else one
+template <class S>
+constexpr int recon_pairs() {
+  return (S::H * S::D / ReconCfg<S>::NT) % 2 == 0 ? 2 : 1;
+}
+
 template <class S>
 __global__ void __launch_bounds__(kRcThreads, 1)
     recon_kernel(const __grid_constant__ CUtensorMap vp_map, const __grid_constant__ CUtensorMap w_map,
@@ -73,6 +86,10 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   using C = ReconCfg<S>;
   using L = ReconSmem<S>;
   constexpr int HD = S::H * S::D, NTN = HD / C::NT, BPT = C::MT / kBlockSize;
+  constexpr int P = recon_pairs<S>(), CL = 2 * P;   // pairs, CTAs per cluster
+  constexpr int NU = NTN / P;                       // column units of a row tile
+  constexpr int BPC = BPT / P;                      // C_v boxes a CTA issues per k-block
+  static_assert(NTN % P == 0 && BPT % P == 0, "cluster split");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -86,21 +103,25 @@ __global__ void __launch_bounds__(kRcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();                    // 0: issues the MMAs
-  const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;   // pair, pairs
+  const uint32_t rank = cluster_ctarank();
+  const int h = static_cast<int>(rank & 1);          // half of the pair (0 issues the MMAs)
+  const int pr = static_cast<int>(rank >> 1);        // pair of the cluster
+  const uint32_t lead = rank & ~1u;                  // the pair's even CTA
+  const int64_t cid = blockIdx.x / CL, ncl = gridDim.x / CL;   // cluster, clusters
 
   griddep_wait();   // page prefix sums (plan) and the appended chunk are visible
   griddep_launch();
   const int64_t total = p.vcum[p.batch];
-  const int64_t ntiles = (total + 2 * BPT - 1) / (2 * BPT) * NTN;
-  if (cid >= ntiles) return;   // uniform over the pair, before any cluster operation
-  // tile t: keys of pages [16 (t / NTN), +16), columns [256 (t % NTN), +256); this CTA's
-  // pages start at 16 (t / NTN) + 8 rank
+  const int64_t ntiles = (total + 2 * BPT - 1) / (2 * BPT) * NU;   // cluster work units
+  if (cid >= ntiles) return;   // uniform over the cluster, before any cluster operation
+  // unit t: keys of pages [16 (t / NU), +16), pair pr's columns [256 ct, +256) with
+  // ct = (t % NU) P + pr; this CTA's keys are pages 16 (t / NU) + 8 h .. + 8, of which it
+  // copies the BPC starting at 8 h + BPC pr
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STG; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], P);   // a commit of every pair of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -118,24 +139,26 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     tmem_relinquish_pair();
   }
   tc_fence_before();
-  cluster_sync_all();   // both CTAs' barriers exist before any copy or arrival reaches them
+  cluster_sync_all();   // every CTA's barriers exist before any copy or arrival reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  auto col_tile = [&](int64_t t) { return static_cast<int>(t % NU) * P + pr; };
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------------ copies
     prefetch_tmap(&vp_map);
     prefetch_tmap(&w_map);
+    constexpr uint16_t kMcast = P == 2 ? 0x5 : 0x1;   // same half of both pairs
     int64_t n = 0;   // k-blocks issued (stage n % STG)
     bool ok = true;
     for (int64_t t = cid, i = 0; ok && t < ntiles; t += ncl, ++i) {
       const int r = static_cast<int>(i % kRcRing);
       if (!mbar_wait(&rfull[r], (i / kRcRing) & 1, abort_flag, p.dev_err)) break;
-      int32_t yrow[BPT];
+      int32_t yrow[BPC];
 #pragma unroll
-      for (int jb = 0; jb < BPT; ++jb) yrow[jb] = rows_s[r * 8 + jb];
+      for (int jb = 0; jb < BPC; ++jb) yrow[jb] = rows_s[r * 8 + jb];
       mbar_arrive(&rempty[r]);
-      const int x0 = static_cast<int>(t % NTN) * C::NT + static_cast<int>(rank) * C::NTC;
+      const int x0 = col_tile(t) * C::NT + h * C::NTC;
       for (int kb = 0; kb < C::KB; ++kb, ++n) {
         const int s = static_cast<int>(n % C::STG);
         if (n >= C::STG &&
@@ -144,11 +167,17 @@ __global__ void __launch_bounds__(kRcThreads, 1)
           break;
         }
         uint8_t* st = sm + s * L::STAGE;
-        const uint32_t fb = map_to_rank(smem_u32(&full[s]), 0);
-        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * L::STAGE);
+        const uint32_t fb = map_to_rank(smem_u32(&full[s]), lead);
+        // the pair's A (from every issuer) and B, in both CTAs
+        if (h == 0) mbar_arrive_expect_tx(&full[s], 2 * L::STAGE);
 #pragma unroll
-        for (int jb = 0; jb < BPT; ++jb)
-          tma_load_2d_pair(st + jb * 2048, &vp_map, kb * 64, yrow[jb], fb);
+        for (int jb = 0; jb < BPC; ++jb) {
+          uint8_t* dst = st + (pr * BPC + jb) * 2048;
+          if constexpr (P == 2)
+            tma_load_2d_mc_pair(dst, &vp_map, kb * 64, yrow[jb], fb, kMcast << h);
+          else
+            tma_load_2d_pair(dst, &vp_map, kb * 64, yrow[jb], fb);
+        }
 #pragma unroll
         for (int q = 0; q < C::NTC / 64; ++q)
           tma_load_2d_pair(st + L::A_BYTES + q * 8192, &w_map, x0 + q * 64, kb * 64, fb);
@@ -167,9 +196,9 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       const bool ok = i < kRcRing ||
                       mbar_wait(&rempty[r], ((i / kRcRing) - 1) & 1, abort_flag, p.dev_err);
       if (!__all_sync(0xffffffffu, ok)) break;
-      if (lane < BPT) {
+      if (lane < BPC) {
         int32_t y = -kBlockSize;
-        const int64_t g = (t / NTN) * 2 * BPT + rank * BPT + lane;
+        const int64_t g = (t / NU) * 2 * BPT + h * BPT + pr * BPC + lane;
         if (g < total) {
           int lo = 0, hi = p.batch;                 // request b with vcum[b] <= g < vcum[b+1]
           while (hi - lo > 1) {
@@ -178,14 +207,14 @@ __global__ void __launch_bounds__(kRcThreads, 1)
           }
           const int32_t id = p.block_table[static_cast<int64_t>(lo) * p.bt_stride + (g - p.vcum[lo])];
           if (id >= 0 && id < p.num_blocks) y = id * kBlockSize;
-          else if (t % NTN == 0) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
+          else if (t % NU == 0) atomicOr(p.dev_err, RCP_DEVERR_BAD_BLOCK);
         }
         rows_s[r * 8 + lane] = y;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rfull[r]);
     }
-  } else if (warp == 1 && lane == 0 && rank == 0) {
+  } else if (warp == 1 && lane == 0 && h == 0) {
     // ------------------------------------------------------------------- MMAs
     constexpr uint32_t idesc = make_idesc_f16(2 * C::MT, C::NT, false, true);
     int64_t n = 0;
@@ -211,26 +240,26 @@ __global__ void __launch_bounds__(kRcThreads, 1)
           const uint64_t bd = make_sdesc(b0 + k * 2048, 8192, 1024, kSwizzle128B);
           umma_f16_pair(dt, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
         }
-        umma_commit_pair(&empty[s], 0x3);
+        umma_commit_pair(&empty[s], static_cast<uint16_t>((1u << CL) - 1));   // every CTA
       }
-      if (ok) umma_commit_pair(&tfull[b], 0x3);
+      if (ok) umma_commit_pair(&tfull[b], static_cast<uint16_t>(0x3u << lead));
     }
     // the last commits land before this CTA (and its peer, through the final cluster
     // barrier) goes on
     if (n > 0) mbar_wait_drain(&empty[(n - 1) % C::STG], ((n - 1) / C::STG) & 1);
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------- epilogue
     // warp w reads TMEM lane quarter w % 4: rows 32 (w % 4) .. of this CTA's 128 keys.  A
     // 64-column chunk goes TMEM -> registers -> the warp's staging buffer (row per lane), then
     // leaves as 8 stores of 4 rows x 128 bytes each.
     const int q = warp & 3, row = q * 32 + lane;
-    const uint32_t tarr = map_to_rank(smem_u32(&tempty[0]), 0);
+    const uint32_t tarr = map_to_rank(smem_u32(&tempty[0]), lead);
     uint8_t* ebuf = sm + L::EPI_OFF + (warp - 2) * L::EPI_BYTES;
     for (int64_t t = cid, i = 0; t < ntiles; t += ncl, ++i) {
       const int b = static_cast<int>(i & 1);
       // this row's page and whether it holds a token of its sequence in a valid block,
       // resolved before the accumulator is waited for
-      const int64_t g = (t / NTN) * 2 * BPT + rank * BPT + row / kBlockSize;
+      const int64_t g = (t / NU) * 2 * BPT + h * BPT + row / kBlockSize;
       const int tok = row % kBlockSize;
       bool keep = false;
       if (g < total) {
@@ -245,7 +274,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       }
       // the row this lane stores in the copy-out: 4 rows per instruction, 8 lanes per row
       const int orow = lane >> 3, ochunk = lane & 7;
-      const int64_t g_first = (t / NTN) * 2 * BPT + rank * BPT + (q * 32) / kBlockSize;
+      const int64_t g_first = (t / NU) * 2 * BPT + h * BPT + (q * 32) / kBlockSize;
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], (i >> 1) & 1, abort_flag, p.dev_err)))
         break;
       tc_fence_after();
@@ -278,7 +307,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
           if (gr < total)
             *reinterpret_cast<uint4*>(static_cast<__half*>(p.vhat) +
                                       (gr * kBlockSize + r % kBlockSize) * HD +
-                                      static_cast<int>(t % NTN) * C::NT + c64 + ochunk * 8) = val;
+                                      col_tile(t) * C::NT + c64 + ochunk * 8) = val;
         }
         __syncwarp();   // the buffer is rewritten by the next chunk
       }
@@ -288,7 +317,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     }
   }
   tc_fence_before();
-  cluster_sync_all();   // neither CTA leaves (or frees its columns) while the pair is busy
+  cluster_sync_all();   // no CTA leaves (or frees its columns) while the cluster is busy
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, L::TMEM_COLS);
@@ -416,21 +445,36 @@ template <class S>
 cudaError_t launch_recon(const CUtensorMap& vp, const CUtensorMap& w_v_mn, const AttnParams& p,
                          int64_t max_pages, int num_sms, cudaStream_t stream, bool pdl) {
   using C = ReconCfg<S>;
+  constexpr int CL = 2 * recon_pairs<S>();
   constexpr int64_t PAGES = 2 * C::MT / kBlockSize;   // pages per tile
-  const int64_t tiles = (max_pages + PAGES - 1) / PAGES * (S::H * S::D / C::NT);
-  const int64_t pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;   // persistent
-  const int64_t grid = 2 * pairs;
-  if (grid <= 0) return cudaSuccess;
+  const int64_t units = (max_pages + PAGES - 1) / PAGES * (S::H * S::D / C::NT) / (CL / 2);
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kRcThreads);
   cfg.dynamicSmemBytes = ReconSmem<S>::ALLOC;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // persistent: as many clusters as can be resident at once (the SMs of a GPU partition
+  // do not always divide into 4-CTA clusters), queried once
+  static int fit = 0;
+  if (fit == 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>(CL * (num_sms / CL)));
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, recon_kernel<S>, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();   // a failed query leaves no error behind
+      n = num_sms / CL;
+    }
+    fit = n;
+  }
+  const int64_t clusters = units < fit ? units : fit;
+  const int64_t grid = CL * clusters;
+  if (grid <= 0) return cudaSuccess;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
