@@ -884,8 +884,8 @@ def measure_prefill(dev, stream, B, prior, chunk, variant, pages, steps, warmup)
           if variant == "reconstruct" else cache.workspace(T))
 
     def step():
-        cache.append_kv(k, v, slots)
-        cache.prefill_attn(q, cu, tab, ln, out=out, workspace=ws, variant=variant)
+        # one call: the chunk's append and its attention (rcp_prefill_step)
+        cache.prefill_step(k, v, slots, q, cu, tab, ln, out=out, workspace=ws, variant=variant)
 
     for _ in range(max(warmup, 3)):
         step()
@@ -895,7 +895,7 @@ def measure_prefill(dev, stream, B, prior, chunk, variant, pages, steps, warmup)
     kern_f = attn_f if variant == "rank" else prefill_recon_flops(prior, chunk, B)
     peak_tf, kind = measured_tensor_peak()
     res = {"variant": variant, "batch": B, "prior": prior, "chunk": chunk, "pages": pages,
-           "step": "append the chunk (T = B*chunk tokens) + chunk attention",
+           "step": "append the chunk (T = B*chunk tokens) + chunk attention, one rcp_prefill_step call",
            "ms_per_step": round(step_ms, 4),
            "algorithmic_flops": attn_f + app_f,
            "algorithmic_tflops_step": round((attn_f + app_f) / (step_ms * 1e-3) / 1e12, 2),

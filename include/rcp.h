@@ -234,6 +234,23 @@ rcp_status rcp_prefill_attn_reconstruct(rcp_cache* cache, const void* q,
                                         void* workspace, size_t workspace_bytes,
                                         rcp_stream stream);
 
+/* A chunked prefill step: rcp_append_kv(k, v, slot_mapping, num_tokens) (the chunk's own
+ * keys and values) followed by rcp_prefill_attn (reconstruct = 0) or
+ * rcp_prefill_attn_reconstruct (reconstruct = 1) with the remaining arguments, on one
+ * stream, with the same results.  Proxima page, "Per-prefill-chunk attention": each chunk
+ * row attends its causal prefix, which includes the chunk's own tokens, so a serving step
+ * appends them first.  Queued as one step: the chunk's query projection runs in the
+ * append's launch, and the plan beside it.  Arguments, layouts, workspace size and errors
+ * as the two calls; reconstruct other than 0 or 1 is RCP_ERR_INVALID_ARG; with
+ * num_query_rows = 0 only the append runs. */
+rcp_status rcp_prefill_step(rcp_cache* cache, const void* k, const void* v,
+                            const int64_t* slot_mapping, int32_t num_tokens, const void* q,
+                            const int32_t* cu_chunk_lens, int32_t num_query_rows,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, int32_t batch, int32_t reconstruct,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            rcp_stream stream);
+
 /* Workspace bytes of rcp_prefill_attn_reconstruct. */
 rcp_status rcp_prefill_reconstruct_workspace_size(const rcp_cache* cache, int32_t max_query_rows,
                                                   int32_t batch, int32_t max_blocks_per_seq,

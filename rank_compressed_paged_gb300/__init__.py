@@ -294,6 +294,20 @@ class PagedCoeffCache:
             ws.numel() * ws.element_size(), _stream(stream)))
         return out
 
+    def _prefill_variant(self, variant: str, rows: int, B: int) -> str:
+        if variant == "auto":
+            variant = "reconstruct" if (self.page_format != "fp16" or
+                                        (B > 0 and rows >= B * RECONSTRUCT_MIN_CHUNK)) else "rank"
+        if variant not in ("rank", "reconstruct"):
+            raise ValueError(f"unknown prefill variant {variant!r}")
+        return variant
+
+    def _prefill_workspace(self, variant: str, rows: int, B: int, mb: int):
+        # quantized pages are widened into the workspace first (both variants)
+        if variant == "rank" and self.page_format == "fp16":
+            return self.workspace(rows, self.workspace_bytes(rows))
+        return self.workspace(rows, self.reconstruct_workspace_bytes(rows, B, mb))
+
     def prefill_attn(self, q, cu_chunk_lens, block_table, seq_lens, out=None, workspace=None,
                      stream=None, variant: str = "auto"):
         """q: [sum chunk][H][d] fp16; cu_chunk_lens: [B+1] int32; seq_lens include the chunk.
@@ -311,23 +325,36 @@ class PagedCoeffCache:
         rows, B = _validate_prefill(self.device, H, d, q, cu_chunk_lens, block_table, seq_lens,
                                     out)
         mb = int(block_table.shape[1])
-        if variant == "auto":
-            variant = "reconstruct" if (self.page_format != "fp16" or
-                                        (B > 0 and rows >= B * RECONSTRUCT_MIN_CHUNK)) else "rank"
-        if variant not in ("rank", "reconstruct"):
-            raise ValueError(f"unknown prefill variant {variant!r}")
+        variant = self._prefill_variant(variant, rows, B)
+        ws = self._prefill_workspace(variant, rows, B, mb) if workspace is None else workspace
         if variant == "rank":
-            # quantized pages are widened into the workspace first (both variants)
-            need = (self.workspace_bytes(rows) if self.page_format == "fp16"
-                    else self.reconstruct_workspace_bytes(rows, B, mb))
-            ws = self.workspace(rows, need) if workspace is None else workspace
             fn, name = self._lib.rcp_prefill_attn, "rcp_prefill_attn"
         else:
-            ws = self.workspace(rows, self.reconstruct_workspace_bytes(rows, B, mb)) \
-                if workspace is None else workspace
             fn, name = self._lib.rcp_prefill_attn_reconstruct, "rcp_prefill_attn_reconstruct"
         _validate_workspace(self.device, ws)
         _lib.check(name, fn(
             self._h, _ptr(q), _ptr(cu_chunk_lens), rows, _ptr(block_table), mb, _ptr(seq_lens), B,
+            _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        return out
+
+    def prefill_step(self, k, v, slot_mapping, q, cu_chunk_lens, block_table, seq_lens,
+                     out=None, workspace=None, stream=None, variant: str = "auto"):
+        """append_kv(k, v, slot_mapping) then prefill_attn(q, cu_chunk_lens, ...), queued as
+        one step (the chunk's query projection shares the append's launch).  Arguments and
+        variant choice as the two calls."""
+        import torch
+        if out is None:
+            out = torch.empty_like(q)
+        H, d = self.shape["num_heads"], self.shape["head_dim"]
+        T = _validate_append(self.device, H, d, k, v, slot_mapping)
+        rows, B = _validate_prefill(self.device, H, d, q, cu_chunk_lens, block_table, seq_lens,
+                                    out)
+        mb = int(block_table.shape[1])
+        variant = self._prefill_variant(variant, rows, B)
+        ws = self._prefill_workspace(variant, rows, B, mb) if workspace is None else workspace
+        _validate_workspace(self.device, ws)
+        _lib.check("rcp_prefill_step", self._lib.rcp_prefill_step(
+            self._h, _ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(q), _ptr(cu_chunk_lens), rows,
+            _ptr(block_table), mb, _ptr(seq_lens), B, 1 if variant == "reconstruct" else 0,
             _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
         return out

@@ -52,6 +52,8 @@ _SIG = {
                                         ctypes.c_size_t, _P]),
     "rcp_prefill_attn_reconstruct": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _P, _I32, _P,
                                                     _P, ctypes.c_size_t, _P]),
+    "rcp_prefill_step": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _I32, _P, _I32, _P, _I32,
+                                        _I32, _P, _P, ctypes.c_size_t, _P]),
     "rcp_prefill_reconstruct_workspace_size": (ctypes.c_int, [_P, _I32, _I32, _I32,
                                                               ctypes.POINTER(ctypes.c_size_t)]),
     "rcp_prefill_crossover_rows": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),

@@ -260,9 +260,12 @@ rcp_status check_append(const AppendArgs& a) {
 }
 
 // The projection launch: a step's append (app->T tokens; none when app is null) and, when
-// nq > 0, the decode's rank-space queries q~ (fp32 into qt), as tcgen05 jobs of one grid.
+// nq > 0, the rank-space queries q~: a decode's (fp32 into qt) or, when qhi is set, a
+// chunked prefill's (fp16 hi / lo pairs), as tcgen05 jobs of one grid.  wait_at_exit: the
+// launch before this one writes nothing this one touches, and is waited for only at exit.
 rcp_status launch_front(rcp_cache* c, const AppendArgs* app, const void* q, int32_t nq,
-                        float* qt, float qscale, cudaStream_t s) {
+                        float* qt, float qscale, cudaStream_t s, void* qhi = nullptr,
+                        void* qlo = nullptr, bool wait_at_exit = false) {
   const int32_t T = app ? app->T : 0;
   if (T == 0 && nq == 0) return RCP_OK;
   rcp::AppendParams p{};
@@ -278,8 +281,11 @@ rcp_status launch_front(rcp_cache* c, const AppendArgs* app, const void* q, int3
   p.T = T;
   p.page_format = c->cfg.page_format;
   p.qt = qt;
+  p.qhi = qhi;
+  p.qlo = qlo;
   p.nq = nq;
   p.qscale = qscale;
+  p.wait_at_exit = wait_at_exit ? 1 : 0;
   // the new tokens' k and v and the queries as [rows][H*d] B operands (16-row tiles up to
   // 16 rows, 64-row tiles up to 256, else 256-row tiles); an absent operand takes another's
   // map (never read)
@@ -412,11 +418,20 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
     const CUtensorMap& vals = recon ? vhat_map : widen ? vp16_map : c->tmap_v;
     const CUtensorMap& kmap = widen ? kp16_map : c->tmap_kp;
     const CUtensorMap& vsrc = widen ? vp16_map : c->tmap_v;
+    // a step with the chunk's append: the plan first, then one projection launch for the
+    // append and the chunk's queries, which runs beside the plan (it waits for the plan
+    // only at exit: the plan writes the workspace's plan arrays, the projections the pages
+    // and the query pairs)
+    const bool fused = app && app->T > 0;
     if (c->shape == kShapeMain) {
       e = rcp::launch_plan<ShapeMain>(p, s, pdl);
-      if (e == cudaSuccess)
+      if (e == cudaSuccess && fused) {
+        if (launch_front(c, app, q, nq, nullptr, p.qscale, s, p.qhi, p.qlo, pdl) != RCP_OK)
+          return RCP_ERR_CUDA;
+      } else if (e == cudaSuccess) {
         e = rcp::launch_qproj_gemm<ShapeMain>(c->tmap_uk64, q_map, p.qhi, p.qlo, nq, p.qscale,
                                               c->dev_err, s, pdl);
+      }
       // profiling events bracket the attention proper: reconstruction + prefill kernel
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
       if (e == cudaSuccess && widen)
@@ -429,9 +444,13 @@ rcp_status run_attention(rcp_cache* c, const void* q, const int32_t* cu_chunk, i
                                            max_tiles, s, pdl, recon);
     } else {
       e = rcp::launch_plan<ShapeTiny>(p, s, pdl);
-      if (e == cudaSuccess)
+      if (e == cudaSuccess && fused) {
+        if (launch_front(c, app, q, nq, nullptr, p.qscale, s, p.qhi, p.qlo, pdl) != RCP_OK)
+          return RCP_ERR_CUDA;
+      } else if (e == cudaSuccess) {
         e = rcp::launch_qproj_gemm<ShapeTiny>(c->tmap_uk64, q_map, p.qhi, p.qlo, nq, p.qscale,
                                               c->dev_err, s, pdl);
+      }
       // profiling events bracket the attention proper: reconstruction + prefill kernel
       if (e == cudaSuccess && c->prof_start) e = cudaEventRecord(c->prof_start, s);
       if (e == cudaSuccess && widen)
@@ -660,6 +679,21 @@ rcp_status rcp_prefill_attn_reconstruct(rcp_cache* c, const void* q, const int32
   if (!cu_chunk_lens) return RCP_ERR_INVALID_ARG;
   return run_attention(c, q, cu_chunk_lens, num_query_rows, block_table, max_blocks_per_seq,
                        seq_lens, batch, out, workspace, workspace_bytes, stream, nullptr, true);
+}
+
+rcp_status rcp_prefill_step(rcp_cache* c, const void* k, const void* v,
+                            const int64_t* slot_mapping, int32_t num_tokens, const void* q,
+                            const int32_t* cu_chunk_lens, int32_t num_query_rows,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, int32_t batch, int32_t reconstruct,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            rcp_stream stream) {
+  if (!cu_chunk_lens || num_tokens < 0 || (reconstruct != 0 && reconstruct != 1))
+    return RCP_ERR_INVALID_ARG;
+  const AppendArgs app{k, v, slot_mapping, num_tokens};
+  return run_attention(c, q, cu_chunk_lens, num_query_rows, block_table, max_blocks_per_seq,
+                       seq_lens, batch, out, workspace, workspace_bytes, stream, &app,
+                       reconstruct != 0);
 }
 
 rcp_status rcp_prefill_reconstruct_workspace_size(const rcp_cache* c, int32_t max_query_rows,

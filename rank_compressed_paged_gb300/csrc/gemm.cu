@@ -18,7 +18,9 @@
 //                       D[64 i + k][t] -> K page [slot_t / 16][h + i][slot_t % 16][k]
 //   decode query job:   a key job with the decode queries as B (same launch as the
 //                       append): D[64 i + k][q] = q~_{q,h+i,k}, stored fp32, scaled by
-//                       log2(e)/sqrt(d), for the split-K scoring.
+//                       log2(e)/sqrt(d), for the split-K scoring; a chunked prefill step
+//                       puts its query projections (below) in the append's launch the
+//                       same way.
 //   query projection:   as a key job with the chunk's queries as B: D[k][q] = q~_{q,h,k},
 //                       scaled by log2(e)/sqrt(d) and stored as an fp16 (hi, lo) pair
 //                       (zero past r_k, up to 64), the prefill score MMA's A operand.
@@ -78,6 +80,7 @@ struct GemmParams {
   void* qlo;
   float* qt;
   float qscale;
+  int32_t wait_at_exit;   // wait for the previous launch at exit instead of before the copies
 };
 
 // Where one CTA's job reads and writes.
@@ -94,7 +97,7 @@ struct GemmJob {
 };
 
 template <class S, int MODE, int NT, int KS>
-__device__ __forceinline__ GemmJob gemm_job(uint32_t rank, int T) {
+__device__ __forceinline__ GemmJob gemm_job(uint32_t rank, int T, bool prefill_q) {
   GemmJob j{};
   const int cluster = blockIdx.x / KS;
   if constexpr (MODE == kModeAppend) {
@@ -104,12 +107,12 @@ __device__ __forceinline__ GemmJob gemm_job(uint32_t rank, int T) {
     constexpr int KBV = S::H * S::D / 64;
     constexpr int KBK = S::D / 64;
     // the append's clusters come first (the value jobs of every token tile, then their key
-    // jobs), then the decode query jobs (head pairs, per query tile)
+    // jobs), then the query jobs (head pairs, per query tile): decode or prefill queries
     const int app_clusters = (T + NT - 1) / NT * (NM + NKG);
     if (cluster >= app_clusters) {
       const int qc = cluster - app_clusters;
       const int pr = (qc % NKG) * KS + static_cast<int>(rank);
-      j.kind = pr < NP ? 4 : -1;
+      j.kind = pr < NP ? (prefill_q ? 3 : 4) : -1;
       j.m0 = 2 * pr;
       j.n0 = (qc / NKG) * NT;
       j.kb0 = 0;
@@ -397,13 +400,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = KS > 1 ? cluster_ctarank() : 0;
-  const GemmJob j = gemm_job<S, MODE, NT, KS>(rank, p.T);
+  const GemmJob j = gemm_job<S, MODE, NT, KS>(rank, p.T, p.qhi != nullptr);
   // value jobs read W_v through map_a and their tokens through map_b;
-  // key and prefill query jobs read U_k through map_a2 and their tokens through map_b2;
-  // decode query jobs read U_k through map_a2 and the queries through map_b3
+  // key jobs (and the query jobs of the query-projection launch) read U_k through map_a2
+  // and their rows through map_b2; query jobs of an append launch read U_k through map_a2
+  // and the queries through map_b3
   const bool uk = j.kind == 1 || j.kind == 3 || j.kind == 4;
+  const bool qjob = j.kind == 4 || (MODE == kModeAppend && j.kind == 3);
   const CUtensorMap* amap = uk ? &map_a2 : &map_a;
-  const CUtensorMap* bmap = j.kind == 4 ? &map_b3 : (uk ? &map_b2 : &map_b);
+  const CUtensorMap* bmap = qjob ? &map_b3 : (uk ? &map_b2 : &map_b);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
@@ -427,7 +432,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int nkb = j.kind >= 0 ? j.kb1 - j.kb0 : 0;
   auto load_a = [&](int kb, int s) {
     uint8_t* st = sm + s * L::STAGE;
-    if ((MODE == kModeAppend && (j.kind == 1 || j.kind == 4)) || MODE == kModeQproj) {
+    if ((MODE == kModeAppend && (j.kind == 1 || j.kind == 3 || j.kind == 4)) ||
+        MODE == kModeQproj) {
       // block-diagonal pair: k-blocks [0, d/64) meet head m0's rows (top), the rest head
       // m0 + 1's (bottom); the other half is a box past the last row of U_k (zeros)
       constexpr int KBK = S::D / 64, OOB = S::H * S::RK;
@@ -454,7 +460,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       load_a(kb, kb);
     }
   }
-  griddep_wait();                     // operands written by the previous kernel are visible
+  // operands written by the previous kernel are visible (unless that kernel writes nothing
+  // this one touches: then it is waited for at exit, so that kernels after this one still
+  // see its results)
+  if (!p.wait_at_exit) griddep_wait();
   griddep_launch();
 
   if (warp == 0 && lane == 0 && nkb > 0) {
@@ -622,6 +631,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, L::TMEM_COLS);
   }
+  if (p.wait_at_exit) griddep_wait();
 }
 
 // --------------------------------------------------------------------------- launchers
@@ -684,8 +694,8 @@ cudaError_t prepare_gemm() {
   return cudaSuccess;
 }
 
-// The append's projections and, when ap.nq > 0, the decode's rank-space queries, in one
-// launch (either part may be empty).  q_rows: tensor map over the queries [nq][H*d] with
+// The append's projections and, when ap.nq > 0, the rank-space queries (a decode's, or a
+// chunked prefill step's when ap.qhi is set), in one launch (either part may be empty).  q_rows: tensor map over the queries [nq][H*d] with
 // the same box as the token maps (64 x 64 when max(T, nq) <= 256, else 64 x 256).
 template <class S>
 cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
@@ -702,8 +712,11 @@ cudaError_t launch_append_gemm(const CUtensorMap& w_v, const CUtensorMap& u_k,
   p.num_blocks = ap.num_blocks;
   p.dev_err = ap.dev_err;
   p.qt = ap.qt;
+  p.qhi = ap.qhi;
+  p.qlo = ap.qlo;
   p.nq = ap.nq;
   p.qscale = ap.qscale;
+  p.wait_at_exit = ap.wait_at_exit;
   using AC = AppendCfg<S>;
   constexpr int NM = (S::R + 127) / 128;
   constexpr int KS = AC::KS_SMALL;

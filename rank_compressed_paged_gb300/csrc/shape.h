@@ -226,10 +226,16 @@ struct AppendParams {
   int64_t num_blocks;
   int32_t T;
   int32_t page_format;        // RCP_PAGES_*: fp16, E4M3 or 4-bit codes with scales
-  // decode: the rank-space queries are projected in the same launch (nq = 0: none)
+  // the rank-space queries are projected in the same launch (nq = 0: none): decode as fp32
+  // into qt, or (qhi != nullptr) a prefill chunk's as fp16 (hi, lo) pairs into qhi / qlo
   float* qt;                  // [nq][H][r_k] fp32, q~ scaled by qscale
+  void* qhi;                  // [nq][H][64] fp16 each, zero past r_k
+  void* qlo;
   int32_t nq;
   float qscale;
+  // wait for the launch before this one only at exit (that launch writes nothing this
+  // one reads or writes), so that both run at once
+  int32_t wait_at_exit;
 };
 
 }  // namespace rcp
