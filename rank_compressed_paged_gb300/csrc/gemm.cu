@@ -183,14 +183,18 @@ __device__ __forceinline__ int64_t append_dst(const GemmParams& p, const GemmJob
 }
 
 // Round x / s to the nearest integer, ties to even, exactly for the fp32 x and fp16 s an
-// append meets: the fp32 quotient's integer is corrected by the residual x - k s, which an
-// fma computes exactly here (k s has at most 14 significant bits and lies within s of x).
-__device__ __forceinline__ int rne_div(float x, float s) {
-  float k = rintf(__fdiv_rn(x, s));
+// append meets: k = rint(x * inv), inv a reciprocal of s within a few 2^-22 (relative), is
+// within one of that integer (|x / s| <= 7), and the residual x - k s, which an fma computes
+// exactly here (k s has at most 15 significant bits and lies within s of x), decides: beyond
+// s / 2 the neighbour on its side, at s / 2 the even one.  No division, so no branch: the
+// columns of an epilogue block interleave.
+__device__ __forceinline__ int rne_div(float x, float s, float inv) {
+  const float k = rintf(x * inv);
   const float r = fmaf(-k, s, x);
   const float a2 = 2.f * fabsf(r);
-  if (a2 > s || (a2 == s && fmodf(k, 2.f) != 0.f)) k += r > 0.f ? 1.f : -1.f;
-  return static_cast<int>(k);
+  const int ki = static_cast<int>(k);
+  if (a2 > s || (a2 == s && (ki & 1) != 0)) return ki + (r > 0.f ? 1 : -1);
+  return ki;
 }
 
 // 4-bit pages: quantize NC finished columns c0 .. c0+NC-1 of an append job, held by every
@@ -218,15 +222,28 @@ __device__ __forceinline__ void int4_store_columns(const GemmParams& p, const Ge
 #pragma unroll
     for (int e = 0; e < NC; ++e) red[warp * 16 + e] = a[e];
   __syncthreads();
+  // every column's scale and code first (independent chains), then the stores
+  __half shs[NC];
+  int codes[NC];
 #pragma unroll
   for (int e = 0; e < NC; ++e) {
     const float amax = fmaxf(red[warp * 16 + e], red[(warp ^ 1) * 16 + e]);
-    __half sh = __float2half_ru(__fdiv_rn(amax, 7.f));
-    if (__half2float(sh) * 7.f < amax)   // the quotient's fp32 rounding went down
-      sh = __ushort_as_half(static_cast<unsigned short>(__half_as_ushort(sh) + 1));
+    // the smallest fp16 h with 7 h >= amax: amax * (1/7) is within 2^-23 (relative) of
+    // amax / 7, so h is that product rounded down or one of the next two fp16 values (7 h is
+    // exact in fp32, so each test is exact)
+    __half sh = __float2half_rd(amax * (1.f / 7.f));
+#pragma unroll
+    for (int up = 0; up < 2; ++up)
+      if (__half2float(sh) * 7.f < amax)
+        sh = __ushort_as_half(static_cast<unsigned short>(__half_as_ushort(sh) + 1));
+    shs[e] = sh;
     const float sf = __half2float(sh);
-    int code = 0;
-    if (valid && sf > 0.f) code = max(-7, min(7, rne_div(v[e], sf)));
+    codes[e] = (valid && sf > 0.f) ? max(-7, min(7, rne_div(v[e], sf, __fdividef(1.f, sf)))) : 0;
+  }
+#pragma unroll
+  for (int e = 0; e < NC; ++e) {
+    const __half sh = shs[e];
+    const int code = codes[e];
     const int hi = __shfl_down_sync(0xffffffffu, code, 1);   // the next row's code
     const int64_t s = dst[c0 + e];
     if (s < 0 || !valid) continue;
@@ -551,12 +568,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = 0.f;
       }
+      if constexpr (CPC % 4 == 0) {   // four columns of one peer per 16-byte store
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int col = c0 + e;
-        st_cluster_f32(map_to_rank(recv_local, static_cast<uint32_t>(col / CPC)) +
-                           ((rank * 128 + row) * CPC + col % CPC) * 4,
-                       v[e]);
+        for (int e = 0; e < 16; e += 4) {
+          const int col = c0 + e;
+          st_cluster_v4(map_to_rank(recv_local, static_cast<uint32_t>(col / CPC)) +
+                            ((rank * 128 + row) * CPC + col % CPC) * 4,
+                        v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = c0 + e;
+          st_cluster_f32(map_to_rank(recv_local, static_cast<uint32_t>(col / CPC)) +
+                             ((rank * 128 + row) * CPC + col % CPC) * 4,
+                         v[e]);
+        }
       }
     }
     cluster_sync_all();
