@@ -131,6 +131,30 @@ def test_workspace_size_and_host_checks(lib):
     lib.rcp_destroy_cache(h)
 
 
+def test_prefill_step_host_checks(lib):
+    """rcp_prefill_step refuses bad arguments before any CUDA call, as the append and the
+    prefill calls it stands for do; with no tokens and no query rows it has nothing to do."""
+    from rank_compressed_paged_gb300 import _lib
+    st, h = _create(lib, _lib, _cfg(_lib))
+    b = ctypes.c_size_t()
+    assert lib.rcp_prefill_reconstruct_workspace_size(h, 8, 2, 64, ctypes.byref(b)) == _lib.RCP_OK
+    ws = 0x100000
+
+    def step(k=0x1000, T=8, cu=0x5000, nq=8, recon=1, ws_bytes=None):
+        return lib.rcp_prefill_step(h, k, 0x2000, 0x3000, T, 0x4000, cu, nq, 0x6000, 64, 0x7000,
+                                    2, recon, 0x8000, ws, b.value if ws_bytes is None else ws_bytes,
+                                    None)
+
+    assert step(recon=2) == _lib.RCP_ERR_INVALID_ARG          # neither variant
+    assert step(recon=-1) == _lib.RCP_ERR_INVALID_ARG
+    assert step(cu=None) == _lib.RCP_ERR_INVALID_ARG          # a prefill needs chunk offsets
+    assert step(T=-1) == _lib.RCP_ERR_INVALID_ARG
+    assert step(k=0x1008) == _lib.RCP_ERR_INVALID_ARG         # misaligned keys of the append
+    assert step(ws_bytes=1024) == _lib.RCP_ERR_WORKSPACE      # workspace of the prefill call
+    assert step(T=0, nq=0) == _lib.RCP_OK                     # nothing to append or attend
+    lib.rcp_destroy_cache(h)
+
+
 def test_python_layer_fails_loudly_without_library(tmp_path):
     from rank_compressed_paged_gb300 import _lib
     saved = _lib._lib
