@@ -188,9 +188,10 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       mbar_wait_drain(&empty[i % C::STG], (i / C::STG) & 1);
   } else if (warp == 6) {
     // ------------------------------------------------------------------- page lookups
-    // lane j resolves page j of this CTA's half of each tile: its TMA row, or row -16 (all
-    // out of bounds: the copy fills zeros and still counts its full bytes, so every stage
-    // completes on a fixed byte count) past the batch's pages or for a rejected id
+    // lane j < BPC resolves the j-th page this CTA copies of each unit (page BPC pr + j of
+    // its half): its TMA row, or row -16 (all out of bounds: the copy fills zeros and still
+    // counts its full bytes, so every stage completes on a fixed byte count) past the
+    // batch's pages or for a rejected id
     for (int64_t t = cid, i = 0; t < ntiles; t += ncl, ++i) {
       const int r = static_cast<int>(i % kRcRing);
       const bool ok = i < kRcRing ||
