@@ -80,7 +80,7 @@ struct GemmParams {
   void* qlo;
   float* qt;
   float qscale;
-  int32_t wait_at_exit;   // wait for the previous launch at exit instead of before the copies
+  int32_t wait_at_exit;   // wait for the previous launch at exit (one CTA) instead of first
 };
 
 // Where one CTA's job reads and writes.
@@ -658,7 +658,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, L::TMEM_COLS);
   }
-  if (p.wait_at_exit) griddep_wait();
+  // the launch before is waited for by one CTA: this grid cannot complete until that CTA
+  // leaves, so kernels after it still find the earlier launch complete, while the short
+  // jobs' CTAs leave their SMs at once (CTA 0 runs a value job, the longest)
+  if (p.wait_at_exit && blockIdx.x == 0) griddep_wait();
 }
 
 // --------------------------------------------------------------------------- launchers
